@@ -1,0 +1,431 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+The oracle is checked against things other than itself:
+  * torch fp64 dense attention with a mask built from the OFFSET condition
+    (j - i = k*(dilation+1), k in [-w, w_upper]) -- a different formulation
+    from the oracle's slot loop -- and torch autograd for the gradients;
+  * closed forms: the valid slot range, full-window = dense softmax attention,
+    one-sided window = causal attention (torch.tril mask);
+  * invariants: softmax rows sum to 1, dilation = interleave of undilated
+    bands on x[r::s], adjoint identities of the three banded products;
+  * central finite differences of the forward;
+  * a hand-worked tiny example (tests/golden/band_qk_tiny.txt);
+  * planted mistakes: textual mutants of band_oracle.c must fail these pins.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+RNG_SEED = 4242
+
+
+def rng(seed=RNG_SEED):
+    return np.random.default_rng(seed)
+
+
+def dense_mask(n, w, wu, dil, gidx=()):
+    """Allowed (query, key) pairs from the offset condition, built with torch."""
+    s = dil + 1
+    i = torch.arange(n).view(-1, 1)
+    j = torch.arange(n).view(1, -1)
+    off = j - i
+    m = (off >= -w * s) & (off <= wu * s) & (torch.remainder(off, s) == 0)
+    if len(gidx):
+        g = torch.zeros(n, dtype=torch.bool)
+        g[list(gidx)] = True
+        m = (m & ~g.view(1, -1)) | g.view(1, -1) | g.view(-1, 1)
+    return m
+
+
+def torch_attention(Q, K, V, mask, scale):
+    """Dense masked softmax attention in fp64 (library routines only)."""
+    s = scale * Q @ K.transpose(-1, -2)
+    s = s.masked_fill(~mask, float("-inf"))
+    return torch.softmax(s, -1) @ V, torch.logsumexp(s, -1)
+
+
+def closed_form_range(i, n, w, wu, s):
+    """First/last valid slot of row i: t_lo = max(0, w - floor(i/s)),
+    t_hi = min(D-1, w + floor((n-1-i)/s))."""
+    D = w + wu + 1
+    return max(0, w - i // s), min(D - 1, w + (n - 1 - i) // s)
+
+
+def randn(*shape, seed=0):
+    return rng(seed).standard_normal(shape)
+
+
+# --------------------------------------------------------------------------
+# hand-worked example
+# --------------------------------------------------------------------------
+def load_golden():
+    cases, cur = [], None
+    with open(os.path.join(HERE, "golden", "band_qk_tiny.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("case"):
+                _, w, wu, d = line.split()
+                cur = (int(w), int(wu), int(d), [])
+                cases.append(cur)
+            else:
+                cur[3].append([float(x) for x in line.split()])
+    return cases
+
+
+GOLD_Q = np.array([[1, 0], [0, 1], [1, 1], [2, 0], [0, 2]], dtype=np.float64)[None]
+GOLD_K = np.array([[1, 2], [3, 4], [5, 6], [7, 8], [9, 10]], dtype=np.float64)[None]
+
+
+def pin_golden():
+    for w, wu, d, rows in load_golden():
+        S = oracle.band_qk(GOLD_Q, GOLD_K, w, wu, d, alpha=1.0, padding=-7.0)
+        np.testing.assert_array_equal(S[0], np.array(rows))
+
+
+def test_golden_tiny():
+    pin_golden()
+
+
+# --------------------------------------------------------------------------
+# band scores against the dense product
+# --------------------------------------------------------------------------
+SCORE_CASES = [  # n, w, w_upper, dilation
+    (37, 5, 3, 0), (37, 4, 4, 2), (50, 3, 0, 1), (8, 20, 20, 0), (1, 2, 2, 0),
+    (29, 0, 0, 0), (33, 0, 6, 3), (64, 16, 16, 0),
+]
+
+
+def pin_scores(n, w, wu, d, alpha=0.37, padding=-3.5):
+    A, B = randn(2, n, 5, seed=1), randn(2, n, 5, seed=2)
+    S = oracle.band_qk(A, B, w, wu, d, alpha=alpha, padding=padding)
+    dense = alpha * torch.from_numpy(A) @ torch.from_numpy(B).transpose(-1, -2)
+    mask = dense_mask(n, w, wu, d)
+    s = d + 1
+    for i in range(n):
+        keys = torch.nonzero(mask[i]).flatten()
+        lo, hi = closed_form_range(i, n, w, wu, s)
+        assert len(keys) == hi - lo + 1
+        np.testing.assert_allclose(S[:, i, lo:hi + 1], dense[:, i, keys].numpy(), rtol=1e-12,
+                                   atol=1e-12)
+        assert np.all(S[:, i, :lo] == padding) and np.all(S[:, i, hi + 1:] == padding)
+
+
+@pytest.mark.parametrize("n,w,wu,d", SCORE_CASES)
+def test_band_scores_vs_dense(n, w, wu, d):
+    pin_scores(n, w, wu, d)
+
+
+# --------------------------------------------------------------------------
+# attention forward: definition and the per-kernel chain against torch
+# --------------------------------------------------------------------------
+ATTN_CASES = [  # n, hd, w, w_upper, dilation, global idx
+    (24, 8, 30, 30, 0, ()),         # full window: dense attention
+    (24, 8, 27, 0, 0, ()),          # one-sided window >= n: causal attention
+    (41, 6, 4, 2, 0, ()),
+    (41, 6, 3, 3, 1, ()),
+    (45, 4, 2, 5, 3, ()),
+    (40, 6, 3, 3, 0, (0, 1, 7, 39)),
+    (43, 5, 2, 4, 2, (3, 20)),
+    (12, 4, 2, 2, 0, tuple(range(12))),  # every token global: dense attention
+]
+
+
+def chain_fwd(Q, K, V, w, wu, d, scale, gidx):
+    if gidx:
+        S, Sg, Sr = oracle.band_qk(Q, K, w, wu, d, alpha=scale, padding=11.0, global_idx=gidx)
+        P, lse, Pg, Pr = oracle.band_softmax(S, w, wu, d, gidx, Sg, Sr)
+        O = oracle.band_pv(P, V, w, wu, d, 1.0, gidx, Pg, Pr)
+    else:
+        S = oracle.band_qk(Q, K, w, wu, d, alpha=scale, padding=11.0)
+        P, lse = oracle.band_softmax(S, w, wu, d)
+        O = oracle.band_pv(P, V, w, wu, d, 1.0)
+    return O, lse
+
+
+def pin_attention(n, hd, w, wu, d, gidx):
+    Q, K, V = (randn(3, n, hd, seed=s) for s in (3, 4, 5))
+    scale = 1.0 / np.sqrt(hd)
+    mask = dense_mask(n, w, wu, d, gidx)
+    O_t, lse_t = torch_attention(*(torch.from_numpy(x) for x in (Q, K, V)), mask, scale)
+    O, lse = oracle.attention_fwd(Q, K, V, w, wu, d, scale, gidx)
+    np.testing.assert_allclose(O, O_t.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_t.numpy(), rtol=1e-12, atol=1e-12)
+    O2, lse2 = chain_fwd(Q, K, V, w, wu, d, scale, gidx)
+    np.testing.assert_allclose(O2, O_t.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse_t.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("n,hd,w,wu,d,gidx", ATTN_CASES)
+def test_attention_vs_torch(n, hd, w, wu, d, gidx):
+    pin_attention(n, hd, w, wu, d, gidx)
+
+
+def test_causal_is_tril():
+    """One-sided window covering the sequence = causal attention (torch.tril)."""
+    n, hd = 19, 4
+    Q, K, V = (randn(1, n, hd, seed=s) for s in (6, 7, 8))
+    mask = torch.tril(torch.ones(n, n, dtype=torch.bool))
+    O_t, _ = torch_attention(*(torch.from_numpy(x) for x in (Q, K, V)), mask, 0.5)
+    O, _ = oracle.attention_fwd(Q, K, V, n + 3, 0, 0, 0.5)
+    np.testing.assert_allclose(O, O_t.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_full_window_is_sdpa():
+    """Full window = torch's scaled_dot_product_attention (no mask)."""
+    n, hd = 21, 8
+    Q, K, V = (randn(2, n, hd, seed=s) for s in (9, 10, 11))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        *(torch.from_numpy(x) for x in (Q, K, V)))
+    O, _ = oracle.attention_fwd(Q, K, V, n, n, 0)
+    np.testing.assert_allclose(O, ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# softmax invariants
+# --------------------------------------------------------------------------
+def pin_softmax_rows(n=45, w=4, wu=6, d=1, gidx=(2, 9)):
+    S = randn(2, n, w + wu + 1, seed=12) * 3
+    Sg = randn(2, n, len(gidx), seed=13)
+    Sr = randn(2, len(gidx), n, seed=14)
+    P, lse, Pg, Pr = oracle.band_softmax(S, w, wu, d, gidx, Sg, Sr)
+    s = d + 1
+    g = set(gidx)
+    for i in range(n):
+        lo, hi = closed_form_range(i, n, w, wu, s)
+        if i in g:
+            assert np.all(P[:, i] == 0) and np.all(Pg[:, i] == 0)
+            continue
+        tot = P[:, i].sum(-1) + Pg[:, i].sum(-1)
+        np.testing.assert_allclose(tot, 1.0, rtol=0, atol=1e-12)
+        assert np.all(P[:, i, :lo] == 0) and np.all(P[:, i, hi + 1:] == 0)
+        for t in range(lo, hi + 1):
+            if i + (t - w) * s in g:
+                assert np.all(P[:, i, t] == 0)
+    np.testing.assert_allclose(Pr.sum(-1), 1.0, rtol=0, atol=1e-12)
+    # no globals: rows sum to one over the closed-form range alone
+    P0, _ = oracle.band_softmax(S, w, wu, d)
+    np.testing.assert_allclose(P0.sum(-1), 1.0, rtol=0, atol=1e-12)
+
+
+def test_softmax_rows_sum_to_one():
+    pin_softmax_rows()
+
+
+# --------------------------------------------------------------------------
+# dilation = interleave of undilated bands on x[r::s]
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [1, 3])
+def test_dilation_interleave(d):
+    n, hd, w, wu = 41, 5, 3, 2
+    s = d + 1
+    Q, K, V = (randn(2, n, hd, seed=s_) for s_ in (15, 16, 17))
+    O, lse = oracle.attention_fwd(Q, K, V, w, wu, d, 0.4)
+    S = oracle.band_qk(Q, K, w, wu, d, alpha=0.4, padding=-1.0)
+    for r in range(s):
+        sub = slice(r, None, s)
+        O_r, lse_r = oracle.attention_fwd(Q[:, sub], K[:, sub], V[:, sub], w, wu, 0, 0.4)
+        np.testing.assert_allclose(O[:, sub], O_r, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(lse[:, sub], lse_r, rtol=1e-13, atol=1e-13)
+        S_r = oracle.band_qk(Q[:, sub], K[:, sub], w, wu, 0, alpha=0.4, padding=-1.0)
+        np.testing.assert_array_equal(S[:, sub], S_r)
+
+
+# --------------------------------------------------------------------------
+# adjoint identities of the three banded products
+# --------------------------------------------------------------------------
+def pin_adjoint(n=38, hd=6, w=5, wu=2, d=1, gidx=()):
+    A, B = randn(2, n, hd, seed=18), randn(2, n, hd, seed=19)
+    D = w + wu + 1
+    X = randn(2, n, D, seed=20)
+    # slots a consumer ignores carry no weight in <S, X>
+    s = d + 1
+    g = set(gidx)
+    for i in range(n):
+        for t in range(D):
+            j = i + (t - w) * s
+            if j < 0 or j >= n or j in g or i in g:
+                X[:, i, t] = 0.0
+    if gidx:
+        G = len(gidx)
+        Xg, Xr = randn(2, n, G, seed=21), randn(2, G, n, seed=22)
+        Xg[:, list(gidx)] = 0.0
+        S, Sg, Sr = oracle.band_qk(A, B, w, wu, d, 1.0, 0.0, gidx)
+        lhs = (S * X).sum() + (Sg * Xg).sum() + (Sr * Xr).sum()
+        mid = (A * oracle.band_pv(X, B, w, wu, d, 1.0, gidx, Xg, Xr)).sum()
+        rhs = (B * oracle.band_t(X, A, w, wu, d, 1.0, gidx, Xg, Xr)).sum()
+    else:
+        S = oracle.band_qk(A, B, w, wu, d, 1.0, 0.0)
+        lhs = (S * X).sum()
+        mid = (A * oracle.band_pv(X, B, w, wu, d, 1.0)).sum()
+        rhs = (B * oracle.band_t(X, A, w, wu, d, 1.0)).sum()
+    assert abs(lhs - mid) <= 1e-12 * abs(lhs) + 1e-12
+    assert abs(lhs - rhs) <= 1e-12 * abs(lhs) + 1e-12
+
+
+@pytest.mark.parametrize("gidx", [(), (0, 5, 17)])
+def test_adjoint_identities(gidx):
+    pin_adjoint(gidx=gidx)
+
+
+# --------------------------------------------------------------------------
+# gradients
+# --------------------------------------------------------------------------
+GRAD_CASES = [  # n, hd, w, w_upper, dilation, gidx
+    (33, 6, 4, 4, 0, ()),
+    (37, 5, 3, 1, 2, ()),
+    (30, 4, 3, 3, 0, (0, 4, 29)),
+    (16, 4, 20, 0, 0, ()),
+]
+
+
+def torch_grads(Q, K, V, dO, mask, scale):
+    t = [torch.from_numpy(x).clone().requires_grad_(True) for x in (Q, K, V)]
+    O, _ = torch_attention(*t, mask, scale)
+    O.backward(torch.from_numpy(dO))
+    return [x.grad.numpy() for x in t]
+
+
+def chain_bwd(Q, K, V, dO, w, wu, d, scale, gidx):
+    """The backward as the five banded calls a GPU user makes."""
+    if gidx:
+        S, Sg, Sr = oracle.band_qk(Q, K, w, wu, d, scale, 0.0, gidx)
+        P, _, Pg, Pr = oracle.band_softmax(S, w, wu, d, gidx, Sg, Sr)
+        dP, dPg, dPr = oracle.band_qk(dO, V, w, wu, d, 1.0, 0.0, gidx)
+        dS, dSg, dSr = oracle.band_softmax_bwd(P, dP, w, wu, d, gidx, Pg, dPg, Pr, dPr)
+        dQ = oracle.band_pv(dS, K, w, wu, d, scale, gidx, dSg, dSr)
+        dK = oracle.band_t(dS, Q, w, wu, d, scale, gidx, dSg, dSr)
+        dV = oracle.band_t(P, dO, w, wu, d, 1.0, gidx, Pg, Pr)
+    else:
+        S = oracle.band_qk(Q, K, w, wu, d, scale, 0.0)
+        P, _ = oracle.band_softmax(S, w, wu, d)
+        dP = oracle.band_qk(dO, V, w, wu, d, 1.0, 0.0)
+        dS = oracle.band_softmax_bwd(P, dP, w, wu, d)
+        dQ = oracle.band_pv(dS, K, w, wu, d, scale)
+        dK = oracle.band_t(dS, Q, w, wu, d, scale)
+        dV = oracle.band_t(P, dO, w, wu, d, 1.0)
+    return dQ, dK, dV
+
+
+def pin_grads(n, hd, w, wu, d, gidx):
+    Q, K, V, dO = (randn(2, n, hd, seed=s) for s in (23, 24, 25, 26))
+    scale = 0.45
+    ref = torch_grads(Q, K, V, dO, dense_mask(n, w, wu, d, gidx), scale)
+    for got in (oracle.attention_bwd(Q, K, V, dO, w, wu, d, scale, gidx),
+                chain_bwd(Q, K, V, dO, w, wu, d, scale, gidx)):
+        for g, r in zip(got, ref):
+            np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("n,hd,w,wu,d,gidx", GRAD_CASES)
+def test_grads_vs_autograd(n, hd, w, wu, d, gidx):
+    pin_grads(n, hd, w, wu, d, gidx)
+
+
+def test_grads_finite_difference():
+    n, hd, w, wu, d, gidx = 12, 3, 2, 1, 1, (5,)
+    Q, K, V, dO = (randn(1, n, hd, seed=s) for s in (27, 28, 29, 30))
+    scale, h = 0.7, 1e-6
+    grads = oracle.attention_bwd(Q, K, V, dO, w, wu, d, scale, gidx)
+
+    def loss(Q_, K_, V_):
+        return float((oracle.attention_fwd(Q_, K_, V_, w, wu, d, scale, gidx)[0] * dO).sum())
+
+    for which, g in enumerate(grads):
+        for idx in [(0, 0, 0), (0, 5, 1), (0, 7, 2), (0, 11, 0), (0, 3, 1)]:
+            args = [Q.copy(), K.copy(), V.copy()]
+            args[which][idx] += h
+            up = loss(*args)
+            args[which][idx] -= 2 * h
+            dn = loss(*args)
+            fd = (up - dn) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(fd)), (which, idx, fd, g[idx])
+
+
+def test_bad_global_index_rejected():
+    A = randn(1, 10, 2)
+    for bad in ((3, 3), (5, 2), (10,), (-1,)):
+        with pytest.raises(ValueError):
+            oracle.band_qk(A, A, 1, 1, 0, global_idx=bad)
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: every mutant of the oracle must fail at least one pin
+# --------------------------------------------------------------------------
+MUTANTS = {
+    "key_offset": ("(long long)(t - w) * s;", "(long long)(t - w + 1) * s;"),
+    "stride": ("const int D = w + wu + 1, s = dil + 1;",
+               "const int D = w + wu + 1, s = dil + 1 + (dil > 0);"),
+    "softmax_no_divide": ("? exp(srow[t] - m) / z : 0.0;", "? exp(srow[t] - m) : 0.0;"),
+    "pv_alpha_dropped": ("for (int c = 0; c < hd; ++c) o[c] *= alpha;", ""),
+    "t_operand": ("x[(size_t)j * hd + c] += alpha * b[t] * yi;",
+                  "x[(size_t)j * hd + c] += alpha * b[t] * y[(size_t)j * hd + c];"),
+    "softmax_bwd_sign": ("? P[r * D + t] * (dP[r * D + t] - delta)",
+                         "? P[r * D + t] * (dP[r * D + t] + delta)"),
+    "bwd_dk_scale": ("+= scale * sbuf[(size_t)bh * nnz + u] * qi;",
+                     "+= sbuf[(size_t)bh * nnz + u] * qi;"),
+    "global_cols_dropped_from_sum": (
+        "for (int q = 0; q < G; ++q) z += exp(Sg[((size_t)bh * n + i) * G + q] - m);", ""),
+    "global_key_not_excluded": ("if (gmask && gmask[j]) return 0;", ""),
+    "qk_transposed": ("srow[t] = alpha * dot(a, B + ((size_t)bh * n + j) * hd, hd);",
+                      "srow[t] = alpha * dot(B + ((size_t)bh * n + i) * hd,"
+                      " A + ((size_t)bh * n + j) * hd, hd);"),
+}
+
+
+def run_all_pins():
+    pin_golden()
+    for c in SCORE_CASES:
+        pin_scores(*c)
+    for c in ATTN_CASES:
+        pin_attention(*c)
+    pin_softmax_rows()
+    pin_adjoint()
+    pin_adjoint(gidx=(0, 5, 17))
+    for c in GRAD_CASES:
+        pin_grads(*c)
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_fails_pins(name):
+    old, new = MUTANTS[name]
+    with open(os.path.join(os.path.dirname(oracle.__file__), "band_oracle.c")) as f:
+        src = f.read()
+    assert old in src, f"mutation anchor for {name} not found"
+    with tempfile.TemporaryDirectory() as tmp:
+        c = os.path.join(tmp, "mutant.c")
+        so = os.path.join(tmp, "mutant.so")
+        with open(c, "w") as f:
+            f.write(src.replace(old, new))
+        subprocess.check_call(["gcc", "-O1", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-o",
+                               so, c, "-lm"])
+        saved = oracle._load()  # the real library, typed; the mutant borrows its signatures
+        try:
+            mut = ctypes.CDLL(so)
+            for fname in ("orc_num_threads", "orc_band_qk", "orc_band_softmax", "orc_band_pv",
+                          "orc_band_t", "orc_band_softmax_bwd", "orc_attention_fwd",
+                          "orc_attention_bwd"):
+                src_f, dst_f = getattr(oracle._lib, fname), getattr(mut, fname)
+                dst_f.argtypes, dst_f.restype = src_f.argtypes, src_f.restype
+            oracle._lib = mut
+            with pytest.raises(AssertionError):
+                run_all_pins()
+        finally:
+            oracle._lib = saved
+
+
+def test_real_oracle_passes_all_pins():
+    run_all_pins()
