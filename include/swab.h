@@ -1,0 +1,174 @@
+/*
+ * swab.h -- C ABI of the sliding-window (banded) attention library for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (pages: "Developing a faster schedule for Longformer's
+ * kernel", TVM forum, posts 1, 3, 5 and 6):
+ *   Longformer attention is built from a banded ("diagonal") matrix product:
+ *   of Q.K^T only the diagonals k in [-w, w_upper] are computed, with
+ *   dilation d (key stride s = d + 1), so query row i meets key
+ *       j = i + k*s,   k = t - w,   slot t in [0, D),   D = w + w_upper + 1.
+ *   A slot whose key falls outside [0, n) holds the constant `padding`.
+ *   Post 6 names three modes of one kernel: the forward product (dense x
+ *   dense^T -> band, t3d3 = 2w+1) and two backward products (band x dense,
+ *   transpose_t1 = 0, and band^T x dense, transpose_t1 = 1).  The author
+ *   merged them into one function only because he could not put several
+ *   kernels into one .so; here they are separate entry points.
+ *
+ * Global tokens ("[WIP] Improve LongformerAttention performance", ONNX
+ * Runtime issue, item (1): one global index of length S shared by the batch):
+ *   G sorted, unique positions shared by every (b, h).  A row i not in G
+ *   attends to its band keys that are not in G plus all of G; a row in G
+ *   attends to every key.  The extra dense pieces live in caller-owned
+ *   companion tensors (swab_glob): `cols` [b,h,n,G] holds every row's value
+ *   at the G global keys, `rows` [b,h,G,n] holds the dense rows of the G
+ *   global queries.  Band slots whose key is in G, and the band rows and
+ *   `cols` rows of global queries, are not used by attention.
+ *
+ * Conventions for every entry point:
+ *   - Layouts are row-major and contiguous: dense tensors (Q, K, V, O, dO,
+ *     dQ, dK, dV) [b,h,n,head_dim]; band tensors (S, P, dP, dS) [b,h,n,D];
+ *     lse [b,h,n] fp32.  Element type = desc->dtype for all but lse.
+ *   - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *     aligned.  Band tensors must be readable up to the next 16-byte
+ *     boundary past their last element (any cudaMalloc / PyTorch allocation
+ *     is).  The library allocates, frees and synchronises nothing.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on it; results are ready when the stream reaches them.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed validation returns an error and launches nothing.
+ *   - Invalid slots (key outside [0, n)) of an INPUT band tensor are ignored,
+ *     whatever they hold; `padding` is written only by band_qk.
+ *   - No entry point aborts or prints.  A launch failure returns
+ *     SWAB_ERR_CUDA.  Device-side waits are bounded: a wait that gives up
+ *     records SWAB_ERR_TIMEOUT in the library's device status word, read with
+ *     swab_device_status().
+ *   - Tensor-core paths: dtype f16/bf16 with head_dim 64.  dtype f32 runs an
+ *     exact-fp32 FFMA path (head_dim 1..128).
+ */
+#ifndef SWAB_H
+#define SWAB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define SWAB_API __declspec(dllexport)
+#else
+#define SWAB_API __attribute__((visibility("default")))
+#endif
+
+#define SWAB_MAX_GLOBAL 256  /* most global tokens per call */
+#define SWAB_MAX_DILATION 15 /* key stride at most 16 */
+
+typedef enum swab_status {
+    SWAB_OK = 0,
+    SWAB_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad global index */
+    SWAB_ERR_UNSUPPORTED = 2, /* head_dim / dtype / size outside what is built */
+    SWAB_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned */
+    SWAB_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed */
+    SWAB_ERR_TIMEOUT = 5      /* a device wait gave up (see swab_device_status) */
+} swab_status;
+
+typedef enum swab_dtype { SWAB_F32 = 0, SWAB_F16 = 1, SWAB_BF16 = 2 } swab_dtype;
+
+/* Problem description: the kernel parameters of the TVM forum thread, posts
+ * 5-6 (b, n, h, w, w_upper, padding; the head dimension replaces m = 768
+ * divided over h = 12 heads) plus the dilation of post 3 and the global
+ * index of the ONNX Runtime issue. */
+typedef struct swab_desc {
+    int32_t b;                 /* batch */
+    int32_t h;                 /* heads (merged with the batch: slices b*h) */
+    int32_t n;                 /* sequence length, >= 1 */
+    int32_t head_dim;          /* 64 for f16/bf16; 1..128 for f32 */
+    int32_t w;                 /* keys on the left, >= 0 */
+    int32_t w_upper;           /* keys on the right, >= 0 (0 = autoregressive) */
+    int32_t dilation;          /* 0..SWAB_MAX_DILATION; key stride dilation+1 */
+    float padding;             /* value band_qk writes where the key is outside [0,n) */
+    int32_t dtype;             /* swab_dtype of every tensor except lse */
+    int32_t n_global;          /* G, 0..SWAB_MAX_GLOBAL; 0 = no global tokens */
+    const int32_t *global_idx; /* HOST array of G sorted unique positions in [0,n) */
+} swab_desc;
+
+/* Companion of a band tensor when n_global > 0 (device pointers, dtype of the
+ * band tensor).  Pass NULL when n_global == 0. */
+typedef struct swab_glob {
+    void *cols; /* [b,h,n,G]: value of row i at key global_idx[g] */
+    void *rows; /* [b,h,G,n]: dense row of query global_idx[g] over all keys */
+} swab_glob;
+
+/* Forward product (TVM thread, post 6: dense x dense^T -> t3d3 = D diagonals):
+ *   S[i,t] = alpha * sum_c A[i,c] * B[j,c]  with j = i + (t-w)*s in [0,n),
+ *   S[i,t] = padding otherwise; accumulation in fp32, one round-to-nearest
+ *   into the output dtype.
+ * Forward scores: A = Q, B = K, alpha = 1/sqrt(head_dim).  Backward:
+ * A = dO, B = V, alpha = 1 gives dP.  With globals, also writes
+ * Sg->cols[i,g] = alpha*A[i].B[G[g]] and Sg->rows[g,j] = alpha*A[G[g]].B[j]. */
+SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, const void *B,
+                             void *S, const swab_glob *Sg, void *stream);
+
+/* Masked row softmax over the band (nvFuser issue "HuggingFace
+ * BertForMaskedLM - Log Softmax Fusion...", fusion 1: max, exp(x - max), sum,
+ * divide, in fp32):
+ *   P[i,t] = exp(S[i,t] - m_i) / Z_i on used slots, 0 on the others;
+ *   lse[i] = m_i + log Z_i (lse may be NULL).
+ * With globals the row also covers Sg->cols (written to Pg->cols); a global
+ * query's row is the dense Sg->rows row (written to Pg->rows) and its band
+ * row and cols row are written as zeros. */
+SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const swab_glob *Sg,
+                                  void *P, const swab_glob *Pg, float *lse, void *stream);
+
+/* Band x dense product (TVM thread, post 6: transpose_t1 = 0, t1d3 = 2w+1):
+ *   O[i,c] = alpha * sum over used slots t of P[i,t] * V[j(i,t), c]
+ *            (+ alpha * sum_g Pg->cols[i,g] * V[G[g],c]);
+ *   a global query's row is alpha * sum_j Pg->rows[g,j] * V[j,c].
+ * Forward: O = P.V (alpha = 1).  Backward: dQ = band_pv(alpha, dS, K). */
+SWAB_API swab_status band_pv(const swab_desc *desc, float alpha, const void *P,
+                             const swab_glob *Pg, const void *V, void *O, void *stream);
+
+/* Transposed band x dense product (TVM thread, post 6: transpose_t1 = 1):
+ *   X[j,c] = alpha * sum over (i,t) with j(i,t) = j, t used, of Bd[i,t]*Y[i,c]
+ *            (+ global terms of Bg->cols and Bg->rows).
+ * band_qk_bwd_t gives dK = alpha * dS^T.Q; band_pv_bwd_t gives
+ * dV = P^T.dO (alpha = 1).  The two names run the same kernel.
+ * Deterministic: every output row has one writer, no atomics. */
+SWAB_API swab_status band_qk_bwd_t(const swab_desc *desc, float alpha, const void *dS,
+                                   const swab_glob *dSg, const void *Q, void *dK, void *stream);
+SWAB_API swab_status band_pv_bwd_t(const swab_desc *desc, float alpha, const void *P,
+                                   const swab_glob *Pg, const void *dO, void *dV, void *stream);
+
+/* Softmax backward on the band (derivative of band_softmax):
+ *   dS[i,t] = P[i,t] * (dP[i,t] - delta_i) on used slots, 0 elsewhere,
+ *   delta_i = sum over used slots of P*dP (+ sum_g Pg*dPg);
+ * global pieces likewise (dSg->cols, dSg->rows). */
+SWAB_API swab_status band_softmax_bwd(const swab_desc *desc, const void *P, const swab_glob *Pg,
+                                      const void *dP, const swab_glob *dPg, void *dS,
+                                      const swab_glob *dSg, void *stream);
+
+/* Fused forward: the same O (and lse, may be NULL) as band_qk(scale) ->
+ * band_softmax -> band_pv, with the scores kept on chip (never written to
+ * memory).  Global tokens are not supported here (n_global must be 0). */
+SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const void *Q,
+                                    const void *K, const void *V, void *O, float *lse,
+                                    void *stream);
+
+/* Human-readable name of a status code (static string). */
+SWAB_API const char *swab_status_string(swab_status status);
+
+/* Reads (and, if reset != 0, clears) the library's device status word on the
+ * current device: bit k set means SWAB status k was raised by a kernel.
+ * Synchronises the device.  Returns SWAB_ERR_CUDA if the read fails. */
+SWAB_API swab_status swab_device_status(int32_t *flags, int32_t reset);
+
+/* Library version, e.g. "0.1.0". */
+SWAB_API const char *swab_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWAB_H */

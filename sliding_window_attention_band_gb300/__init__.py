@@ -1,0 +1,16 @@
+"""Sliding-window (banded, "diagonal") attention for one NVIDIA GB300 (sm_103a).
+
+The compute runs in hand-written CUDA kernels behind a C ABI (include/swab.h,
+built into ``_lib/libswab.so`` by ``build.build()``); this package is the thin
+ctypes binding over it plus the seeded input generators.  Nothing here
+computes attention on the host.
+"""
+from ._binding import (API_FUNCTIONS, Desc, SwabError, band_attention, band_pv,  # noqa: F401
+                       band_pv_bwd_t, band_qk, band_qk_bwd_t, band_softmax, band_softmax_bwd,
+                       device_status, library_path, load, status_string, version)
+from .inputs import WORKLOADS, Workload, seeded_qkvo, workload_inputs  # noqa: F401
+
+__all__ = ["Desc", "SwabError", "band_qk", "band_softmax", "band_pv", "band_qk_bwd_t",
+           "band_pv_bwd_t", "band_softmax_bwd", "band_attention", "device_status", "load",
+           "library_path", "version", "status_string", "WORKLOADS", "Workload",
+           "seeded_qkvo", "workload_inputs"]

@@ -1,0 +1,266 @@
+"""ctypes binding of libswab.so (include/swab.h).
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  If the
+library has not been built, every call raises ``SwabError`` -- there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+SWAB_OK = 0
+STATUS_NAMES = ["SWAB_OK", "SWAB_ERR_INVALID_ARG", "SWAB_ERR_UNSUPPORTED",
+                "SWAB_ERR_MISALIGNED", "SWAB_ERR_CUDA", "SWAB_ERR_TIMEOUT"]
+MAX_GLOBAL = 256
+MAX_DILATION = 15
+
+_DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+# every symbol the header declares
+API_FUNCTIONS = ("band_qk", "band_softmax", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
+                 "band_softmax_bwd", "band_attention", "swab_status_string",
+                 "swab_device_status", "swab_version")
+
+
+class SwabError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{fn} failed: {name}")
+        self.status = status
+        self.status_name = name
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int32), ("h", ctypes.c_int32), ("n", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("w", ctypes.c_int32),
+                ("w_upper", ctypes.c_int32), ("dilation", ctypes.c_int32),
+                ("padding", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("n_global", ctypes.c_int32), ("global_idx", ctypes.POINTER(ctypes.c_int32))]
+
+
+class _Glob(ctypes.Structure):
+    _fields_ = [("cols", ctypes.c_void_p), ("rows", ctypes.c_void_p)]
+
+
+class Desc:
+    """Problem description (swab_desc).  Keeps the host global index alive."""
+
+    def __init__(self, b, h, n, head_dim, w, w_upper, dilation=0, padding=0.0,
+                 dtype=torch.float16, global_idx=None):
+        if dtype not in _DTYPES:
+            raise ValueError(f"unsupported dtype {dtype}")
+        self.b, self.h, self.n, self.head_dim = int(b), int(h), int(n), int(head_dim)
+        self.w, self.w_upper, self.dilation = int(w), int(w_upper), int(dilation)
+        self.padding = float(padding)
+        self.dtype = dtype
+        gi = list(global_idx) if global_idx is not None else []
+        self.global_idx = tuple(int(x) for x in gi)
+        self._gi = (ctypes.c_int32 * max(1, len(gi)))(*gi) if gi else None
+        self.c = _Desc(self.b, self.h, self.n, self.head_dim, self.w, self.w_upper,
+                       self.dilation, self.padding, _DTYPES[dtype], len(gi),
+                       ctypes.cast(self._gi, ctypes.POINTER(ctypes.c_int32)) if gi else None)
+
+    @property
+    def BH(self):
+        return self.b * self.h
+
+    @property
+    def D(self):
+        return self.w + self.w_upper + 1
+
+    @property
+    def G(self):
+        return len(self.global_idx)
+
+    @classmethod
+    def from_workload(cls, wl):
+        return cls(wl.b, wl.h, wl.n, wl.head_dim, wl.w, wl.w_upper, wl.dilation, wl.padding,
+                   wl.dtype, wl.global_idx)
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libswab.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise SwabError("load (libswab.so not built; run "
+                                "sliding_window_attention_band_gb300.build.build())", 4)
+            lib = ctypes.CDLL(path)
+            P = ctypes.c_void_p
+            D = ctypes.POINTER(_Desc)
+            Gp = ctypes.POINTER(_Glob)
+            f, i32 = ctypes.c_float, ctypes.c_int32
+            sigs = {
+                "band_qk": [D, f, P, P, P, Gp, P],
+                "band_softmax": [D, P, Gp, P, Gp, P, P],
+                "band_pv": [D, f, P, Gp, P, P, P],
+                "band_qk_bwd_t": [D, f, P, Gp, P, P, P],
+                "band_pv_bwd_t": [D, f, P, Gp, P, P, P],
+                "band_softmax_bwd": [D, P, Gp, P, Gp, P, Gp, P],
+                "band_attention": [D, f, P, P, P, P, P, P],
+                "swab_device_status": [ctypes.POINTER(i32), i32],
+            }
+            for name, args in sigs.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            lib.swab_status_string.restype = ctypes.c_char_p
+            lib.swab_status_string.argtypes = [ctypes.c_int]
+            lib.swab_version.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def version() -> str:
+    return load().swab_version().decode()
+
+
+def status_string(code: int) -> str:
+    return load().swab_status_string(code).decode()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, like):
+    if stream is None:
+        if like is not None and like.is_cuda:
+            return ctypes.c_void_p(torch.cuda.current_stream(like.device).cuda_stream)
+        return None
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _glob(g):
+    if g is None:
+        return None
+    cols, rows = g
+    return ctypes.byref(_Glob(cols.data_ptr() if cols is not None else None,
+                              rows.data_ptr() if rows is not None else None))
+
+
+def _check_shape(name, t, shape, dtype):
+    if t is None:
+        return
+    if t.numel() != _numel(shape):
+        raise ValueError(f"{name}: expected {shape} elements, got shape {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected dtype {dtype}, got {t.dtype}")
+
+
+def _numel(shape):
+    k = 1
+    for s in shape:
+        k *= s
+    return k
+
+
+def _call(name, *args):
+    rc = getattr(load(), name)(*args)
+    if rc != SWAB_OK:
+        raise SwabError(name, rc)
+
+
+def _dense(d):
+    return (d.BH, d.n, d.head_dim)
+
+
+def _band(d):
+    return (d.BH, d.n, d.D)
+
+
+# ---------------------------------------------------------------------------
+# the entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+def band_qk(desc: Desc, alpha, A, B, S, Sg=None, stream=None):
+    """S = alpha * A.B^T on the band (padding outside the sequence)."""
+    for n_, t, sh in (("A", A, _dense(desc)), ("B", B, _dense(desc)), ("S", S, _band(desc))):
+        _check_shape(n_, t, sh, desc.dtype)
+    _call("band_qk", ctypes.byref(desc.c), float(alpha), _ptr(A), _ptr(B), _ptr(S), _glob(Sg),
+          _stream(stream, S))
+
+
+def band_softmax(desc: Desc, S, P, lse=None, Sg=None, Pg=None, stream=None):
+    """P = masked row softmax of S; lse (fp32, optional) = log-sum-exp per row."""
+    _check_shape("S", S, _band(desc), desc.dtype)
+    _check_shape("P", P, _band(desc), desc.dtype)
+    _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
+    _call("band_softmax", ctypes.byref(desc.c), _ptr(S), _glob(Sg), _ptr(P), _glob(Pg),
+          _ptr(lse), _stream(stream, P))
+
+
+def band_pv(desc: Desc, alpha, P, V, O, Pg=None, stream=None):
+    """O = alpha * band(P).V."""
+    _check_shape("P", P, _band(desc), desc.dtype)
+    _check_shape("V", V, _dense(desc), desc.dtype)
+    _check_shape("O", O, _dense(desc), desc.dtype)
+    _call("band_pv", ctypes.byref(desc.c), float(alpha), _ptr(P), _glob(Pg), _ptr(V), _ptr(O),
+          _stream(stream, O))
+
+
+def band_qk_bwd_t(desc: Desc, alpha, dS, Q, dK, dSg=None, stream=None):
+    """dK = alpha * band(dS)^T.Q."""
+    _check_shape("dS", dS, _band(desc), desc.dtype)
+    _check_shape("Q", Q, _dense(desc), desc.dtype)
+    _check_shape("dK", dK, _dense(desc), desc.dtype)
+    _call("band_qk_bwd_t", ctypes.byref(desc.c), float(alpha), _ptr(dS), _glob(dSg), _ptr(Q),
+          _ptr(dK), _stream(stream, dK))
+
+
+def band_pv_bwd_t(desc: Desc, alpha, P, dO, dV, Pg=None, stream=None):
+    """dV = alpha * band(P)^T.dO."""
+    _check_shape("P", P, _band(desc), desc.dtype)
+    _check_shape("dO", dO, _dense(desc), desc.dtype)
+    _check_shape("dV", dV, _dense(desc), desc.dtype)
+    _call("band_pv_bwd_t", ctypes.byref(desc.c), float(alpha), _ptr(P), _glob(Pg), _ptr(dO),
+          _ptr(dV), _stream(stream, dV))
+
+
+def band_softmax_bwd(desc: Desc, P, dP, dS, Pg=None, dPg=None, dSg=None, stream=None):
+    """dS = P * (dP - rowsum(P * dP)) on the used slots."""
+    for n_, t in (("P", P), ("dP", dP), ("dS", dS)):
+        _check_shape(n_, t, _band(desc), desc.dtype)
+    _call("band_softmax_bwd", ctypes.byref(desc.c), _ptr(P), _glob(Pg), _ptr(dP), _glob(dPg),
+          _ptr(dS), _glob(dSg), _stream(stream, dS))
+
+
+def band_attention(desc: Desc, scale, Q, K, V, O, lse=None, stream=None):
+    """Fused forward: O (and lse) of band_qk -> band_softmax -> band_pv, scores on chip."""
+    for n_, t in (("Q", Q), ("K", K), ("V", V), ("O", O)):
+        _check_shape(n_, t, _dense(desc), desc.dtype)
+    _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
+    _call("band_attention", ctypes.byref(desc.c), float(scale), _ptr(Q), _ptr(K), _ptr(V),
+          _ptr(O), _ptr(lse), _stream(stream, O))
+
+
+def device_status(reset: bool = True) -> int:
+    """The library's device status word (bit k = status k raised by a kernel)."""
+    flags = ctypes.c_int32(0)
+    _call("swab_device_status", ctypes.byref(flags), 1 if reset else 0)
+    return int(flags.value)

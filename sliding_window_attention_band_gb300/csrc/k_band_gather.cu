@@ -1,0 +1,363 @@
+// k_band_gather.cu -- the two backward-mode banded products of "Developing a
+// faster schedule for Longformer's kernel" (TVM forum, post 6):
+//   transpose_t1 = 0 (band x dense -> dense):
+//       O[i,c] = alpha * sum_t P[i,t] * V[i + (t-w)*s, c]
+//   transpose_t1 = 1 (band^T x dense -> dense):
+//       X[j,c] = alpha * sum over (i,t) with i + (t-w)*s = j of Bd[i,t]*Y[i,c]
+// Forward P.V and dQ = dS.K use the first; dK = dS^T.Q and dV = P^T.dO the
+// second.
+//
+// Both are run as dense tcgen05 products over a window, with the banded
+// operand expanded on the fly into a dense tile in shared memory (zeros off
+// the band).  The key observation: in both products one "line" of the dense
+// A tile is a contiguous piece of ONE band row, shifted:
+//   band_pv : A[q][k]  (M = query q, K = key k)    = P[q][k - q + const]
+//   band_t  : A[m][q]  (M = key m,   K = query q)  = Bd[q][m - q + const]
+// so for both the line of query q is band row q read from some slot on, and
+// only the tile layout differs (K-major for band_pv, MN-major for band_t).
+//
+// A line starts at an arbitrary 2-byte boundary.  Lines whose query indices
+// agree mod 8 start at the same offset mod 16 bytes (the row pitch in
+// elements is D and the slot start moves by -1 per query), so each warp task
+// takes lines of one such class: its 16-byte loads are coalesced, and the
+// realignment shift is the same for all 32 lanes.  The realigned 16-byte
+// pieces are written into the 128-byte-swizzled layout the tensor core reads.
+//
+// CTA = 128 output rows (queries for band_pv, keys for band_t) of one residue
+// of the key stride; the K dimension (keys / queries) is walked 64 at a time.
+// Warp 0 loads the dense operand (V or Y) with TMA, warp 1 owns tensor memory
+// and issues MMAs, warps 2..9 build the A stages and finally drain the fp32
+// accumulator (TMEM lane = output row).
+#include <type_traits>
+
+#include "swab_internal.h"
+
+namespace swab {
+namespace {
+
+constexpr int kBM = 128;    // output rows per tile (MMA M)
+constexpr int kKC = 64;     // K per stage
+constexpr int kStages = 4;
+constexpr int kGW = 8;      // gather warps
+constexpr int kThreads = 32 * (2 + kGW);
+constexpr int kATile = kBM * kKC * 2;    // 16 KB
+constexpr int kBTile = kKC * 64 * 2;     // 8 KB (64 rows x 64 halves)
+constexpr int kSmemBytes = kStages * (kATile + kBTile) + 1024 + 1024;
+constexpr uint32_t kTmemCols = 64;
+
+// bytes [2e, 2e + 16) of the 32-byte value (lo, hi), e in [0, 8)
+template <int E>
+__device__ __forceinline__ uint4 shift_extract(const uint4 &lo, const uint4 &hi) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    constexpr int ws = E / 2;
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if constexpr (E % 2 == 0) {
+            o[k] = w[k + ws];
+        } else {
+            o[k] = __funnelshift_r(w[k + ws], w[k + ws + 1], 16);
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint4 extract_elems(const uint4 &lo, const uint4 &hi, int e) {
+    switch (e) {  // e is uniform across the warp
+        case 0: return lo;
+        case 1: return shift_extract<1>(lo, hi);
+        case 2: return shift_extract<2>(lo, hi);
+        case 3: return shift_extract<3>(lo, hi);
+        case 4: return shift_extract<4>(lo, hi);
+        case 5: return shift_extract<5>(lo, hi);
+        case 6: return shift_extract<6>(lo, hi);
+        default: return shift_extract<7>(lo, hi);
+    }
+}
+
+// Zero the 16-bit elements outside [lo, hi) of an 8-element piece.
+__device__ __forceinline__ uint4 mask_elems(uint4 v, int lo, int hi) {
+    uint32_t m[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int e0 = 2 * k, e1 = 2 * k + 1;
+        m[k] = ((e0 >= lo && e0 < hi) ? 0x0000ffffu : 0u) | ((e1 >= lo && e1 < hi) ? 0xffff0000u : 0u);
+    }
+    return make_uint4(v.x & m[0], v.y & m[1], v.z & m[2], v.w & m[3]);
+}
+
+// Load 8 consecutive band elements starting at element offset `e_start` of the
+// band tensor (any 2-byte boundary), keeping only positions [vlo, vhi) of the
+// 8 (the rest read as zero and are not fetched when no valid byte lies in a
+// 16-byte piece).  `shift` = e_start mod 8, uniform across the warp.
+__device__ __forceinline__ uint4 load_line_piece(const uint16_t *band, long long e_start,
+                                                 int shift, int vlo, int vhi) {
+    vlo = max(vlo, 0);
+    vhi = min(vhi, 8);
+    if (vlo >= vhi) return make_uint4(0, 0, 0, 0);
+    const long long e_al = e_start - shift;  // multiple of 8
+    const uint16_t *p = band + e_al;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (shift + vlo < 8) lo = ldg16(p);
+    if (shift + vhi > 8) hi = ldg16(p + 8);
+    uint4 v = extract_elems(lo, hi, shift);
+    if (vlo > 0 || vhi < 8) v = mask_elems(v, vlo, vhi);
+    return v;
+}
+
+template <typename T, bool kTrans>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_band_gather_tc(const __grid_constant__ TmapSet mapB, const GatherArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *atile = base;                               // kStages x 16 KB
+    uint8_t *btile = base + kStages * kATile;            // kStages x 8 KB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(btile + kStages * kBTile);
+    uint64_t *afull = bars;                  // [kStages], count kGW
+    uint64_t *bfull = bars + kStages;        // [kStages], TMA
+    uint64_t *empty = bars + 2 * kStages;    // [kStages], MMA commit
+    uint64_t *accfull = bars + 3 * kStages;  // [1]
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(accfull + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const Geom &g = p.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.y, bh = blockIdx.z;
+    const int nr = residue_len(g.n, g.s, r);
+    const int a0 = blockIdx.x * kBM;
+    if (a0 >= nr) return;
+    // K range: keys for band_pv, queries for band_t
+    const int k_lo = kTrans ? max(a0 - g.wu, 0) : max(a0 - g.w, 0);
+    const int k_hi = kTrans ? min(a0 + kBM - 1 + g.w, nr - 1) : min(a0 + kBM - 1 + g.wu, nr - 1);
+    const int nck = (k_hi - k_lo + kKC) / kKC;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&afull[i], kGW);
+            mbar_init(&bfull[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(accfull, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const CUtensorMap *mb = &mapB.m[r];
+            tma_prefetch_desc(mb);
+            for (int c = 0; c < nck; ++c) {
+                const int st = c % kStages;
+                const uint32_t ph = (c / kStages) & 1;
+                if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err)) break;
+                mbar_arrive_expect_tx(&bfull[st], kBTile);
+                tma_load_3d(btile + st * kBTile, mb, &bfull[st], 0, k_lo + c * kKC, bh);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr bool kBf16 = !std::is_same<T, __half>::value;
+            const uint32_t idesc = idesc_f16(kBM, 64, kBf16, kTrans, true);
+            bool ok = true;
+            for (int c = 0; c < nck && ok; ++c) {
+                const int st = c % kStages;
+                const uint32_t ph = (c / kStages) & 1;
+                ok = mbar_wait(&bfull[st], ph, abort_flag, p.err) &&
+                     mbar_wait(&afull[st], ph, abort_flag, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(atile + st * kATile);
+                const uint32_t b_addr = smem_u32(btile + st * kBTile);
+#pragma unroll
+                for (int k = 0; k < kKC / 16; ++k) {
+                    // A: K-major (band_pv) advances 32 B per K=16 step inside the
+                    // 128-B swizzle row; MN-major (band_t) advances 16 lines of
+                    // 128 B.  B (dense rows, MN-major) advances 16 lines.
+                    const uint64_t ad = kTrans ? sdesc_sw128(a_addr + 2048 * k, kKC * 128, 1024)
+                                               : sdesc_sw128(a_addr + 32 * k, 16, 1024);
+                    // N = 64 is one 128-B block: the MN-block stride is unused, so it is
+                    // given the same value as the 8-line K-group stride.
+                    const uint64_t bd = sdesc_sw128(b_addr + 2048 * k, 1024, 1024);
+                    mma_f16_ss(tmem, ad, bd, idesc, (c > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(&empty[st]);
+            }
+            if (ok) mma_commit(accfull);
+        }
+    } else {
+        // ---------------- gather warps ----------------
+        const int gw = warp - 2;
+        const uint16_t *band = reinterpret_cast<const uint16_t *>(p.band);
+        const long long slice_row0 = (long long)bh * g.n + r;  // band row of sub-index 0
+        bool ok = true;
+        for (int c = 0; c < nck; ++c) {
+            const int st = c % kStages;
+            const uint32_t ph = (c / kStages) & 1;
+            ok = mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            const uint32_t a_addr = smem_u32(atile + st * kATile);
+            const int kc0 = k_lo + c * kKC;  // first K index of this stage
+#pragma unroll 1
+            for (int task = gw; task < 32; task += kGW) {
+                const int cls = task & 7, sub = task >> 3;
+                int line, j;  // line within the stage tile, 16-byte piece of the line
+                int qq;       // query sub-index of the line
+                long long e_line;  // element offset of the line's first element
+                int vlo, vhi;      // valid element range of the line
+                uint32_t dst;
+                if (!kTrans) {
+                    // 128 lines (queries) x 64 keys: 4 lines per task, 8 pieces each
+                    line = cls + 8 * (4 * sub + (lane >> 3));
+                    j = lane & 7;
+                    qq = a0 + line;
+                    // element k of the line is key kc0 + k, slot kc0 + k - qq + w
+                    e_line = (slice_row0 + (long long)g.s * qq) * g.D + (kc0 - qq + g.w);
+                    vlo = qq - g.w - kc0;
+                    vhi = min(vlo + g.D, k_hi - kc0 + 1);
+                    if (qq >= nr) vhi = vlo;  // padded query rows read as zero
+                    dst = a_addr + line * 128 + ((j ^ (line & 7)) << 4);
+                } else {
+                    // 64 lines (queries) x 128 keys: 2 lines per task, 16 pieces each
+                    line = cls + 8 * (2 * sub + (lane >> 4));
+                    j = lane & 15;
+                    qq = kc0 + line;
+                    // element m of the line is key a0 + m, slot a0 + m - qq + w
+                    e_line = (slice_row0 + (long long)g.s * qq) * g.D + (a0 - qq + g.w);
+                    vlo = qq - g.w - a0;
+                    vhi = min(vlo + g.D, nr - a0);
+                    if (qq >= nr) vhi = vlo;
+                    dst = a_addr + (j >> 3) * (kKC * 128) + line * 128 + (((j & 7) ^ (line & 7)) << 4);
+                }
+                const long long e_start = e_line + 8 * j;
+                const int shift = (int)(e_line & 7);  // same for every line of the task
+                const uint4 v = load_line_piece(band, e_start, shift, vlo - 8 * j, vhi - 8 * j);
+                sts16(dst, v);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[st]);
+        }
+        // ---------------- epilogue ----------------
+        const bool acc_ok = ok && mbar_wait(accfull, 0, abort_flag, p.err);
+        if (__all_sync(0xffffffffu, acc_ok)) {
+            tc_fence_after();
+            const int quarter = warp & 3;
+            const int half = gw >> 2;  // columns [32*half, 32*half + 32)
+            const int m = quarter * 32 + lane;
+            uint32_t v[32];
+            tmem_ld32(tmem_addr(tmem, quarter * 32, half * 32), v);
+            tmem_ld_wait();
+            const int row = a0 + m;
+            if (row < nr) {
+                T *out = reinterpret_cast<T *>(p.out) +
+                         ((long long)bh * g.n + r + (long long)g.s * row) * 64 + half * 32;
+                uint4 *o4 = reinterpret_cast<uint4 *>(out);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w;
+                    w.x = pack2<T>(p.alpha * __uint_as_float(v[8 * q + 0]), p.alpha * __uint_as_float(v[8 * q + 1]));
+                    w.y = pack2<T>(p.alpha * __uint_as_float(v[8 * q + 2]), p.alpha * __uint_as_float(v[8 * q + 3]));
+                    w.z = pack2<T>(p.alpha * __uint_as_float(v[8 * q + 4]), p.alpha * __uint_as_float(v[8 * q + 5]));
+                    w.w = pack2<T>(p.alpha * __uint_as_float(v[8 * q + 6]), p.alpha * __uint_as_float(v[8 * q + 7]));
+                    o4[q] = w;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// exact fp32 paths
+// ---------------------------------------------------------------------------
+// band_pv: one CTA per output row, one thread per channel.
+__global__ void __launch_bounds__(128) k_band_pv_f32(const DenseArgs p) {
+    const Geom &g = p.g;
+    const long long R = blockIdx.x;
+    const int i = (int)(R % g.n);
+    const long long bh = R / g.n;
+    const int c = threadIdx.x;
+    if (c >= g.hd) return;
+    const float *P = reinterpret_cast<const float *>(p.A) + R * g.D;
+    const float *V = reinterpret_cast<const float *>(p.B) + bh * g.n * g.hd;
+    const int t_lo = max(0, g.w - i / g.s);
+    const int t_hi = min(g.D - 1, g.w + (g.n - 1 - i) / g.s);
+    float acc = 0.f;
+    for (int t = t_lo; t <= t_hi; ++t) {
+        const long long j = (long long)i + (long long)(t - g.w) * g.s;
+        acc = fmaf(P[t], V[j * g.hd + c], acc);
+    }
+    reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
+}
+
+// band_t: one CTA per output row j (a key), one thread per channel; the
+// queries meeting key j are i = j - (t-w)*s for the slots t that keep i in range.
+__global__ void __launch_bounds__(128) k_band_t_f32(const DenseArgs p) {
+    const Geom &g = p.g;
+    const long long R = blockIdx.x;
+    const int j = (int)(R % g.n);
+    const long long bh = R / g.n;
+    const int c = threadIdx.x;
+    if (c >= g.hd) return;
+    const float *Bd = reinterpret_cast<const float *>(p.A) + bh * g.n * g.D;
+    const float *Y = reinterpret_cast<const float *>(p.B) + bh * g.n * g.hd;
+    float acc = 0.f;
+    for (int t = 0; t < g.D; ++t) {
+        const long long i = (long long)j - (long long)(t - g.w) * g.s;
+        if (i < 0 || i >= g.n) continue;
+        acc = fmaf(Bd[i * g.D + t], Y[i * g.hd + c], acc);
+    }
+    reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
+}
+
+template <typename T, bool kTrans>
+cudaError_t launch_gather(const TmapSet &mapB, const GatherArgs &a, cudaStream_t st) {
+    const int tiles = (a.g.nsub + kBM - 1) / kBM;
+    dim3 grid(tiles, a.g.s, a.g.BH);
+    cudaError_t e = cudaFuncSetAttribute(k_band_gather_tc<T, kTrans>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k_band_gather_tc<T, kTrans><<<grid, kThreads, kSmemBytes, st>>>(mapB, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_band_gather_tc(DType dt, bool transposed, const TmapSet &mapB,
+                                  const GatherArgs &a, cudaStream_t st) {
+    if (dt == kF16) {
+        return transposed ? launch_gather<__half, true>(mapB, a, st)
+                          : launch_gather<__half, false>(mapB, a, st);
+    }
+    return transposed ? launch_gather<__nv_bfloat16, true>(mapB, a, st)
+                      : launch_gather<__nv_bfloat16, false>(mapB, a, st);
+}
+
+cudaError_t launch_band_pv_f32(const DenseArgs &a, cudaStream_t st) {
+    const long long rows = (long long)a.g.BH * a.g.n;
+    k_band_pv_f32<<<(unsigned)rows, 128, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_band_t_f32(const DenseArgs &a, cudaStream_t st) {
+    const long long rows = (long long)a.g.BH * a.g.n;
+    k_band_t_f32<<<(unsigned)rows, 128, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace swab

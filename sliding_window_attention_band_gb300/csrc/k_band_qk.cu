@@ -1,0 +1,238 @@
+// k_band_qk.cu -- the forward banded product ("Developing a faster schedule
+// for Longformer's kernel", TVM forum, post 6: dense x dense^T restricted to
+// t3d3 = w + w_upper + 1 diagonals):
+//     S[i,t] = alpha * A[i] . B[i + (t-w)*s]   (padding where the key is
+//     outside the sequence).
+//
+// Tensor-core kernel (f16 / bf16, head_dim 64).  One CTA owns 128 query rows
+// of one residue r (rows r + s*a, a in [a0, a0+128)) and walks the keys its
+// band touches, 128 at a time.  Each step is one dense 128x128x64 product
+// computed with tcgen05.mma into tensor memory, oriented so that the KEY
+// chunk is the M operand: TMEM lane = key, column = query.  An epilogue
+// thread then holds one key against 128 queries, and for a fixed query the
+// 32 lanes of a warp hold 32 consecutive keys = 32 consecutive band slots of
+// that query's row, so every store instruction writes 64 contiguous bytes.
+// Out-of-band entries of the dense tile are simply not stored.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads (query tile once, key
+// chunks into a 4-stage ring), warp 1 owns tensor memory and issues the MMAs
+// (two 128-column accumulators, ping-pong), warps 2-5 drain the accumulators.
+#include <type_traits>
+
+#include "swab_internal.h"
+
+namespace swab {
+namespace {
+
+constexpr int kBM = 128;          // keys per chunk (MMA M)
+constexpr int kBN = 128;          // queries per tile (MMA N)
+constexpr int kStages = 4;        // key-chunk ring depth
+constexpr int kThreads = 192;
+constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 halves
+constexpr int kSmemBytes = kStages * kTileBytes + kTileBytes + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr uint32_t kTmemCols = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_band_qk_tc(const __grid_constant__ TmapSet mapA, const __grid_constant__ TmapSet mapB,
+                 const QKArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *ktile = base;                                 // kStages x 16 KB (A: keys)
+    uint8_t *qtile = base + kStages * kTileBytes;          // 16 KB (B: queries)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(qtile + kTileBytes);
+    uint64_t *kfull = bars;                 // [kStages]
+    uint64_t *kempty = bars + kStages;      // [kStages]
+    uint64_t *qfull = bars + 2 * kStages;   // [1]
+    uint64_t *tfull = qfull + 1;            // [2]
+    uint64_t *tempty = tfull + 2;           // [2]
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const Geom &g = p.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.y, bh = blockIdx.z;
+    const int nr = residue_len(g.n, g.s, r);
+    const int a0 = blockIdx.x * kBN;
+    if (a0 >= nr) return;  // whole CTA leaves before any barrier or allocation
+    const int kb_lo = max(a0 - g.w, 0);
+    const int kb_hi = min(a0 + kBN - 1 + g.wu, nr - 1);
+    const int nck = (kb_hi - kb_lo + kBM) / kBM;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&kempty[i], 1);
+        }
+        mbar_init(qfull, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 128);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const CUtensorMap *ma = &mapA.m[r];
+            const CUtensorMap *mb = &mapB.m[r];
+            tma_prefetch_desc(ma);
+            tma_prefetch_desc(mb);
+            mbar_arrive_expect_tx(qfull, kTileBytes);
+            tma_load_3d(qtile, ma, qfull, 0, a0, bh);
+            for (int c = 0; c < nck; ++c) {
+                const int st = c % kStages;
+                const uint32_t ph = (c / kStages) & 1;
+                if (!mbar_wait(&kempty[st], ph ^ 1, abort_flag, p.err)) break;
+                mbar_arrive_expect_tx(&kfull[st], kTileBytes);
+                tma_load_3d(ktile + st * kTileBytes, mb, &kfull[st], 0, kb_lo + c * kBM, bh);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+            const uint32_t idesc = idesc_f16(kBM, kBN, kBf16, false, false);
+            const uint32_t q_addr = smem_u32(qtile);
+            if (mbar_wait(qfull, 0, abort_flag, p.err)) {
+                for (int c = 0; c < nck; ++c) {
+                    const int st = c % kStages;
+                    const uint32_t ph = (c / kStages) & 1;
+                    const int b = c & 1;
+                    const uint32_t bph = (c >> 1) & 1;
+                    if (!mbar_wait(&kfull[st], ph, abort_flag, p.err)) break;
+                    if (!mbar_wait(&tempty[b], bph ^ 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+                    const uint32_t k_addr = smem_u32(ktile + st * kTileBytes);
+                    const uint32_t d = tmem + b * kBN;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        mma_f16_ss(d, sdesc_sw128(k_addr + 32 * k, 16, 1024),
+                                   sdesc_sw128(q_addr + 32 * k, 16, 1024), idesc, k > 0);
+                    }
+                    mma_commit(&kempty[st]);
+                    mma_commit(&tfull[b]);
+                }
+            }
+        }
+    } else {
+        // epilogue: warps 2..5, TMEM lane quarter = warp % 4
+        const int quarter = warp & 3;
+        const int m = quarter * 32 + lane;  // key within the chunk
+        T *S = reinterpret_cast<T *>(p.S);
+        const long long row0 = (long long)bh * g.n + r + (long long)g.s * a0;
+        const long long stepq = (long long)g.s * g.D - 1;  // offset change per query
+        const float alpha = p.alpha;
+        for (int c = 0; c < nck; ++c) {
+            const int b = c & 1;
+            const uint32_t bph = (c >> 1) & 1;
+            const bool ok = mbar_wait(&tfull[b], bph, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, ok)) break;  // keep the warp converged for tcgen05.ld
+            tc_fence_after();
+            const int kk = kb_lo + c * kBM + m;  // key sub-index of this lane
+            const bool key_ok = kk <= kb_hi;
+            // element offset of (query a0, this key); query q adds q*stepq
+            const long long off0 = row0 * g.D + (kk - a0 + g.w);
+            const int tq0 = kk - a0 + g.w;  // slot of query a0; query q has tq0 - q
+#pragma unroll 1
+            for (int grp = 0; grp < 4; ++grp) {
+                uint32_t v[32];
+                tmem_ld32(tmem_addr(tmem, quarter * 32, b * kBN + grp * 32), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int q = grp * 32 + j;
+                    const int t = tq0 - q;
+                    if (key_ok && (unsigned)t < (unsigned)g.D && a0 + q < nr) {
+                        S[off0 + (long long)q * stepq] = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[b]);
+        }
+        // padding: slots whose key lies outside [0, nr)
+        const T pad = Elt<T>::from_f(g.padding);
+        for (int q = warp - 2; q < kBN; q += 4) {
+            const int qq = a0 + q;
+            if (qq >= nr) break;
+            const int t_lo = max(0, g.w - qq);
+            const int t_hi = min(g.D - 1, g.w + nr - 1 - qq);
+            T *row = S + ((long long)bh * g.n + r + (long long)g.s * qq) * g.D;
+            for (int t = lane; t < t_lo; t += 32) row[t] = pad;
+            for (int t = t_hi + 1 + lane; t < g.D; t += 32) row[t] = pad;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// exact fp32 path: one CTA per query row, threads over slots, FFMA dot products
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) k_band_qk_f32(const DenseArgs p) {
+    const Geom &g = p.g;
+    const long long R = blockIdx.x;  // row in [0, BH*n)
+    const int i = (int)(R % g.n);
+    const long long bh = R / g.n;
+    __shared__ float arow[128];
+    const float *A = reinterpret_cast<const float *>(p.A) + R * g.hd;
+    const float *B = reinterpret_cast<const float *>(p.B) + bh * g.n * g.hd;
+    for (int c = threadIdx.x; c < g.hd; c += blockDim.x) arow[c] = A[c];
+    __syncthreads();
+    float *S = reinterpret_cast<float *>(p.out) + R * g.D;
+    for (int t = threadIdx.x; t < g.D; t += blockDim.x) {
+        const long long j = (long long)i + (long long)(t - g.w) * g.s;
+        if (j < 0 || j >= g.n) {
+            S[t] = g.padding;
+        } else {
+            const float *b = B + j * g.hd;
+            float acc = 0.f;
+            for (int c = 0; c < g.hd; ++c) acc = fmaf(arow[c], b[c], acc);
+            S[t] = p.alpha * acc;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_band_qk_tc(DType dt, const TmapSet &mapA, const TmapSet &mapB,
+                              const QKArgs &a, cudaStream_t st) {
+    const int tiles = (a.g.nsub + kBN - 1) / kBN;
+    dim3 grid(tiles, a.g.s, a.g.BH);
+    cudaError_t e;
+    if (dt == kF16) {
+        e = cudaFuncSetAttribute(k_band_qk_tc<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        k_band_qk_tc<__half><<<grid, kThreads, kSmemBytes, st>>>(mapA, mapB, a);
+    } else {
+        e = cudaFuncSetAttribute(k_band_qk_tc<__nv_bfloat16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        k_band_qk_tc<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(mapA, mapB, a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_band_qk_f32(const DenseArgs &a, cudaStream_t st) {
+    const long long rows = (long long)a.g.BH * a.g.n;
+    k_band_qk_f32<<<(unsigned)rows, 128, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace swab

@@ -1,0 +1,298 @@
+// swab_api.cu -- the C ABI of include/swab.h: argument validation, tensor-map
+// encoding, and kernel launches.  Validation runs on the host before any
+// CUDA call, so a bad argument never reaches the GPU.  The library links the
+// CUDA runtime statically and reaches the driver only through
+// cudaGetDriverEntryPointByVersion, so it loads on a machine without a GPU.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "swab_internal.h"
+
+namespace swab {
+
+// The device status word: bit k set = a kernel raised swab_status k.
+__device__ unsigned g_status_word;
+
+namespace {
+
+const char *const kStatusNames[] = {
+    "SWAB_OK", "SWAB_ERR_INVALID_ARG", "SWAB_ERR_UNSUPPORTED",
+    "SWAB_ERR_MISALIGNED", "SWAB_ERR_CUDA", "SWAB_ERR_TIMEOUT",
+};
+
+size_t elt_size(DType dt) { return dt == kF32 ? 4 : 2; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side checks of the descriptor; fills the kernel geometry.
+swab_status check_desc(const swab_desc *d, Geom *g, DType *dt) {
+    if (!d) return SWAB_ERR_INVALID_ARG;
+    if (d->b < 1 || d->h < 1 || d->n < 1 || d->head_dim < 1) return SWAB_ERR_INVALID_ARG;
+    if (d->w < 0 || d->w_upper < 0 || d->dilation < 0) return SWAB_ERR_INVALID_ARG;
+    if (d->dtype != SWAB_F32 && d->dtype != SWAB_F16 && d->dtype != SWAB_BF16)
+        return SWAB_ERR_INVALID_ARG;
+    if (d->n_global < 0 || d->n_global > SWAB_MAX_GLOBAL) return SWAB_ERR_INVALID_ARG;
+    if (d->n_global > 0) {
+        if (!d->global_idx) return SWAB_ERR_INVALID_ARG;
+        for (int k = 0; k < d->n_global; ++k) {
+            const int32_t j = d->global_idx[k];
+            if (j < 0 || j >= d->n) return SWAB_ERR_INVALID_ARG;
+            if (k > 0 && d->global_idx[k - 1] >= j) return SWAB_ERR_INVALID_ARG;
+        }
+    }
+    if (d->dilation > SWAB_MAX_DILATION) return SWAB_ERR_UNSUPPORTED;
+    const long long BH = (long long)d->b * d->h;
+    const long long D = (long long)d->w + d->w_upper + 1;
+    if (BH > 65535) return SWAB_ERR_UNSUPPORTED;          // grid z
+    if (D > (1ll << 24)) return SWAB_ERR_UNSUPPORTED;
+    if (BH * d->n > 0x7fffffffll) return SWAB_ERR_UNSUPPORTED;  // row index fits int32 grid
+    if (d->dtype == SWAB_F32) {
+        if (d->head_dim > 128) return SWAB_ERR_UNSUPPORTED;
+    } else if (d->head_dim != 64) {
+        return SWAB_ERR_UNSUPPORTED;
+    }
+    g->BH = (int)BH;
+    g->n = d->n;
+    g->hd = d->head_dim;
+    g->w = d->w;
+    g->wu = d->w_upper;
+    g->s = d->dilation + 1;
+    g->D = (int)D;
+    g->nsub = (d->n + g->s - 1) / g->s;
+    g->padding = d->padding;
+    *dt = static_cast<DType>(d->dtype);
+    return SWAB_OK;
+}
+
+swab_status check_ptrs(std::initializer_list<const void *> ptrs) {
+    for (const void *p : ptrs) {
+        if (!p) return SWAB_ERR_INVALID_ARG;
+        if (!aligned16(p)) return SWAB_ERR_MISALIGNED;
+    }
+    return SWAB_OK;
+}
+
+// ---------------------------------------------------------------------------
+// driver entry point for tensor-map encoding
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// One map per residue r: rows r, r+s, ... of every slice of a [BH, n, 64]
+// tensor; box = 64 elements x box_rows rows, 128-byte swizzle, zero fill
+// outside the residue's rows.
+bool build_rows_maps(TmapSet *set, const void *base, const Geom &g, DType dt, int box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const size_t es = elt_size(dt);
+    const CUtensorMapDataType ty =
+        dt == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    std::memset(set, 0, sizeof(*set));
+    for (int r = 0; r < g.s; ++r) {
+        int nr = residue_len(g.n, g.s, r);
+        const int rr = nr > 0 ? r : 0;  // empty residue: never loaded, encode a valid map
+        if (nr == 0) nr = 1;
+        cuuint64_t dims[3] = {64, (cuuint64_t)nr, (cuuint64_t)g.BH};
+        cuuint64_t strides[2] = {(cuuint64_t)g.s * 64 * es, (cuuint64_t)g.n * 64 * es};
+        cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        void *ptr = const_cast<char *>(static_cast<const char *>(base)) + (size_t)rr * 64 * es;
+        CUresult res = enc(&set->m[r], ty, 3, ptr, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (res != CUDA_SUCCESS) return false;
+    }
+    return true;
+}
+
+// Address of the status word on the current device (cached per device).
+unsigned *status_word() {
+    static std::mutex mu;
+    static unsigned *cache[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned *>(p);
+    }
+    return cache[dev];
+}
+
+swab_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SWAB_OK : SWAB_ERR_CUDA; }
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// globals are accepted by the descriptor check but not yet by these paths
+swab_status check_no_globals(const swab_desc *d) {
+    return d->n_global > 0 ? SWAB_ERR_UNSUPPORTED : SWAB_OK;
+}
+
+// The two transposed-product names share this body.
+swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, const void *Y,
+                          void *X, void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    if ((s = check_ptrs({Bd, Y, X})) != SWAB_OK) return s;
+    if (dt == kF32) {
+        DenseArgs a{g, alpha, Bd, Y, X};
+        return from_cuda(launch_band_t_f32(a, as_stream(stream)));
+    }
+    TmapSet mapY;
+    if (!build_rows_maps(&mapY, Y, g, dt, kGatherBoxRows)) return SWAB_ERR_CUDA;
+    unsigned *err = status_word();
+    if (!err) return SWAB_ERR_CUDA;
+    GatherArgs a{g, alpha, Bd, X, err};
+    return from_cuda(launch_band_gather_tc(dt, true, mapY, a, as_stream(stream)));
+}
+
+}  // namespace
+}  // namespace swab
+
+using namespace swab;
+
+extern "C" {
+
+SWAB_API const char *swab_version(void) { return "0.1.0"; }
+
+SWAB_API const char *swab_status_string(swab_status status) {
+    const int k = static_cast<int>(status);
+    if (k < 0 || k >= (int)(sizeof(kStatusNames) / sizeof(kStatusNames[0])))
+        return "SWAB_UNKNOWN_STATUS";
+    return kStatusNames[k];
+}
+
+SWAB_API swab_status swab_device_status(int32_t *flags, int32_t reset) {
+    if (!flags) return SWAB_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SWAB_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return SWAB_ERR_CUDA;
+    *flags = static_cast<int32_t>(v);
+    if (reset) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess)
+            return SWAB_ERR_CUDA;
+    }
+    return SWAB_OK;
+}
+
+SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, const void *B,
+                             void *S, const swab_glob *Sg, void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    (void)Sg;
+    if ((s = check_ptrs({A, B, S})) != SWAB_OK) return s;
+    if (dt == kF32) {
+        DenseArgs a{g, alpha, A, B, S};
+        return from_cuda(launch_band_qk_f32(a, as_stream(stream)));
+    }
+    TmapSet mapA, mapB;
+    if (!build_rows_maps(&mapA, A, g, dt, kQKBoxRows) ||
+        !build_rows_maps(&mapB, B, g, dt, kQKBoxRows))
+        return SWAB_ERR_CUDA;
+    unsigned *err = status_word();
+    if (!err) return SWAB_ERR_CUDA;
+    QKArgs a{g, alpha, S, err};
+    return from_cuda(launch_band_qk_tc(dt, mapA, mapB, a, as_stream(stream)));
+}
+
+SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const swab_glob *Sg,
+                                  void *P, const swab_glob *Pg, float *lse, void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    (void)Sg;
+    (void)Pg;
+    if ((s = check_ptrs({S, P})) != SWAB_OK) return s;
+    if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
+    SoftmaxArgs a{g, S, nullptr, P, lse, nullptr};
+    return from_cuda(launch_band_softmax(dt, a, as_stream(stream)));
+}
+
+SWAB_API swab_status band_pv(const swab_desc *desc, float alpha, const void *P,
+                             const swab_glob *Pg, const void *V, void *O, void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    (void)Pg;
+    if ((s = check_ptrs({P, V, O})) != SWAB_OK) return s;
+    if (dt == kF32) {
+        DenseArgs a{g, alpha, P, V, O};
+        return from_cuda(launch_band_pv_f32(a, as_stream(stream)));
+    }
+    TmapSet mapV;
+    if (!build_rows_maps(&mapV, V, g, dt, kGatherBoxRows)) return SWAB_ERR_CUDA;
+    unsigned *err = status_word();
+    if (!err) return SWAB_ERR_CUDA;
+    GatherArgs a{g, alpha, P, O, err};
+    return from_cuda(launch_band_gather_tc(dt, false, mapV, a, as_stream(stream)));
+}
+
+SWAB_API swab_status band_qk_bwd_t(const swab_desc *desc, float alpha, const void *dS,
+                                   const swab_glob *dSg, const void *Q, void *dK, void *stream) {
+    (void)dSg;
+    return band_t_common(desc, alpha, dS, Q, dK, stream);
+}
+
+SWAB_API swab_status band_pv_bwd_t(const swab_desc *desc, float alpha, const void *P,
+                                   const swab_glob *Pg, const void *dO, void *dV, void *stream) {
+    (void)Pg;
+    return band_t_common(desc, alpha, P, dO, dV, stream);
+}
+
+SWAB_API swab_status band_softmax_bwd(const swab_desc *desc, const void *P, const swab_glob *Pg,
+                                      const void *dP, const swab_glob *dPg, void *dS,
+                                      const swab_glob *dSg, void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    (void)Pg;
+    (void)dPg;
+    (void)dSg;
+    if ((s = check_ptrs({P, dP, dS})) != SWAB_OK) return s;
+    SoftmaxArgs a{g, P, dP, dS, nullptr, nullptr};
+    return from_cuda(launch_band_softmax_bwd(dt, a, as_stream(stream)));
+}
+
+SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const void *Q,
+                                    const void *K, const void *V, void *O, float *lse,
+                                    void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    if ((s = check_ptrs({Q, K, V, O})) != SWAB_OK) return s;
+    if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
+    (void)scale;
+    (void)stream;
+    return SWAB_ERR_UNSUPPORTED;  // fused kernel not built yet
+}
+
+}  // extern "C"

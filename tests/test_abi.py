@@ -1,0 +1,175 @@
+"""C-ABI boundary tests that need no GPU.
+
+* the library builds, loads on a machine without a driver, and exports every
+  function include/swab.h declares;
+* invalid arguments come back as the documented status before any CUDA call
+  (the pointers below are fake, never dereferenced: validation rejects the
+  call first).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from sliding_window_attention_band_gb300 import _binding as B
+from sliding_window_attention_band_gb300 import build as swab_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swab.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA = 0, 1, 2, 3, 4
+FAKE = 0x10000  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    swab_build.build()
+    return B.load()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    return re.findall(r"SWAB_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_lists_every_binding():
+    names = declared_functions()
+    assert sorted(names) == sorted(B.API_FUNCTIONS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert B.version() == "0.1.0"
+    for code, name in enumerate(B.STATUS_NAMES):
+        assert B.status_string(code) == name
+    assert B.status_string(99) == "SWAB_UNKNOWN_STATUS"
+
+
+def desc(**kw):
+    base = dict(b=1, h=2, n=256, head_dim=64, w=16, w_upper=16, dilation=0, padding=0.0,
+                dtype=torch.float16, global_idx=None)
+    base.update(kw)
+    return B.Desc(**base)
+
+
+def call(lib, name, d, *ptrs, alpha=0.125):
+    P = ctypes.c_void_p
+    if name == "band_qk":
+        return lib.band_qk(ctypes.byref(d.c), alpha, P(ptrs[0]), P(ptrs[1]), P(ptrs[2]), None,
+                           None)
+    if name == "band_softmax":
+        return lib.band_softmax(ctypes.byref(d.c), P(ptrs[0]), None, P(ptrs[1]), None,
+                                P(ptrs[2]) if len(ptrs) > 2 else None, None)
+    if name in ("band_pv", "band_qk_bwd_t", "band_pv_bwd_t"):
+        return getattr(lib, name)(ctypes.byref(d.c), alpha, P(ptrs[0]), None, P(ptrs[1]),
+                                  P(ptrs[2]), None)
+    if name == "band_softmax_bwd":
+        return lib.band_softmax_bwd(ctypes.byref(d.c), P(ptrs[0]), None, P(ptrs[1]), None,
+                                    P(ptrs[2]), None, None)
+    if name == "band_attention":
+        return lib.band_attention(ctypes.byref(d.c), alpha, P(ptrs[0]), P(ptrs[1]),
+                                  P(ptrs[2]), P(ptrs[3]), None, None)
+    raise KeyError(name)
+
+
+ALL3 = ["band_qk", "band_softmax", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
+        "band_softmax_bwd"]
+
+
+@pytest.mark.parametrize("name", ALL3 + ["band_attention"])
+def test_null_descriptor(lib, name):
+    P = ctypes.c_void_p
+    fn = getattr(lib, name)
+    if name == "band_attention":
+        rc = fn(None, 1.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, None)
+    elif name == "band_qk":
+        rc = fn(None, 1.0, P(FAKE), P(FAKE), P(FAKE), None, None)
+    elif name == "band_softmax":
+        rc = fn(None, P(FAKE), None, P(FAKE), None, None, None)
+    elif name == "band_softmax_bwd":
+        rc = fn(None, P(FAKE), None, P(FAKE), None, P(FAKE), None, None)
+    else:
+        rc = fn(None, 1.0, P(FAKE), None, P(FAKE), P(FAKE), None)
+    assert rc == INVALID
+
+
+@pytest.mark.parametrize("name", ALL3)
+@pytest.mark.parametrize("bad,expected", [
+    (dict(n=0), INVALID), (dict(b=0), INVALID), (dict(w=-1), INVALID),
+    (dict(w_upper=-2), INVALID), (dict(dilation=-1), INVALID), (dict(dilation=16), UNSUPPORTED),
+    (dict(head_dim=128), UNSUPPORTED), (dict(head_dim=0), INVALID),
+    (dict(global_idx=[3, 3]), INVALID), (dict(global_idx=[5, 2]), INVALID),
+    (dict(global_idx=[256]), INVALID), (dict(global_idx=[-1]), INVALID),
+    (dict(b=300, h=300), UNSUPPORTED),
+])
+def test_bad_descriptor(lib, name, bad, expected):
+    assert call(lib, name, desc(**bad), FAKE, FAKE, FAKE) == expected
+
+
+def test_bad_dtype(lib):
+    d = desc()
+    d.c.dtype = 7
+    assert call(lib, "band_qk", d, FAKE, FAKE, FAKE) == INVALID
+
+
+def test_too_many_globals(lib):
+    d = desc(n=1000, global_idx=list(range(257)))
+    assert call(lib, "band_qk", d, FAKE, FAKE, FAKE) == INVALID
+
+
+def test_f32_head_dim_limit(lib):
+    assert call(lib, "band_qk", desc(dtype=torch.float32, head_dim=129), FAKE, FAKE, FAKE) == \
+        UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ALL3)
+def test_null_and_misaligned_pointers(lib, name):
+    d = desc()
+    assert call(lib, name, d, 0, FAKE, FAKE) == INVALID
+    assert call(lib, name, d, FAKE, 0, FAKE) == INVALID
+    assert call(lib, name, d, FAKE + 2, FAKE, FAKE) == MISALIGNED
+    assert call(lib, name, d, FAKE, FAKE + 8, FAKE) == MISALIGNED
+    assert call(lib, name, d, FAKE, FAKE, FAKE + 4) == MISALIGNED
+    if name != "band_softmax":  # its third pointer (lse) is optional
+        assert call(lib, name, d, FAKE, FAKE, 0) == INVALID
+
+
+def test_lse_misaligned(lib):
+    assert call(lib, "band_softmax", desc(), FAKE, FAKE, FAKE + 4) == MISALIGNED
+
+
+def test_device_status_null(lib):
+    assert lib.swab_device_status(None, 0) == INVALID
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32])
+def test_valid_call_without_gpu_reports_cuda_error(lib, dtype):
+    """Valid arguments on a machine with no GPU: the launch fails cleanly."""
+    assert call(lib, "band_qk", desc(dtype=dtype), FAKE, FAKE, FAKE) == CUDA
+    assert call(lib, "band_softmax", desc(dtype=dtype), FAKE, FAKE) == CUDA
+
+
+def test_binding_shape_checks():
+    d = desc()
+    with pytest.raises(ValueError):
+        B.band_qk(d, 1.0, torch.zeros(3), torch.zeros(3), torch.zeros(3))
+    with pytest.raises(ValueError):
+        B.Desc(1, 1, 8, 64, 1, 1, dtype=torch.int32)
+
+
+def test_binding_raises_swab_error(lib):
+    d = desc(n=0)
+    with pytest.raises(B.SwabError) as ei:
+        B._call("band_qk", ctypes.byref(d.c), 1.0, ctypes.c_void_p(FAKE),
+                ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), None, None)
+    assert ei.value.status_name == "SWAB_ERR_INVALID_ARG"

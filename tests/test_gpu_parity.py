@@ -1,0 +1,308 @@
+"""GPU parity: every kernel of the library against the fp64 CPU oracle.
+
+Both sides get the same dtype-rounded inputs (upcast to fp64 for the oracle,
+exactly).  Tolerances:
+  * fp16/bf16 banded scores: normwise  max|gpu - ref| / max|ref|  <= 2e-3 over
+    valid slots (one RNE rounding of an fp32 accumulator is at most 2^-9
+    relative for bf16, 2^-12 for fp16); padding slots bit-exact;
+  * dense outputs of the unit kernels fed random (non-probability) bands:
+    the same normwise 2e-3;
+  * attention chains (O, P, dQ, dK, dV): max abs 1e-2;
+  * fp32 inputs: normwise relative 1e-5 (FFMA path, no TF32);
+  * band indexing probes: bit-exact.
+Invalid slots of every band INPUT are filled with NaN: the kernels must
+ignore them.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sliding_window_attention_band_gb300 as swab
+from sliding_window_attention_band_gb300 import build as swab_build
+from sliding_window_attention_band_gb300.inputs import (WORKLOADS, seeded_band, seeded_qkvo,
+                                                        workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+SCORE_TOL = 2e-3
+ABS_TOL = 1e-2
+F32_TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    swab_build.build()
+    swab.load()
+    swab.device_status(reset=True)
+    yield
+    assert swab.device_status(reset=True) == 0, "a kernel raised the device status word"
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def valid_mask(n, w, wu, dil):
+    """[n, D] bool: slot t of row i holds a key inside the sequence."""
+    s = dil + 1
+    i = np.arange(n)[:, None]
+    t = np.arange(w + wu + 1)[None, :]
+    j = i + (t - w) * s
+    return (j >= 0) & (j < n)
+
+
+def poison_invalid(band, n, w, wu, dil):
+    m = torch.from_numpy(~valid_mask(n, w, wu, dil))
+    out = band.clone()
+    out[:, m] = float("nan")
+    return out
+
+
+def normwise(got, ref, mask=None):
+    if mask is not None:
+        got, ref = got[..., mask], ref[..., mask]
+    den = np.max(np.abs(ref))
+    return float(np.max(np.abs(got - ref)) / (den if den > 0 else 1.0))
+
+
+def dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def empty_band(d, dtype=None):
+    return torch.empty((d.BH, d.n, d.D), dtype=dtype or d.dtype, device="cuda")
+
+
+def empty_dense(d):
+    return torch.empty((d.BH, d.n, d.head_dim), dtype=d.dtype, device="cuda")
+
+
+# ---------------------------------------------------------------------------
+# unit parity, small ragged cases spanning several tiles
+# ---------------------------------------------------------------------------
+UNIT_CASES = [  # BH, n, w, w_upper, dilation, dtype
+    (2, 1000, 64, 64, 0, torch.float16),
+    (3, 777, 100, 37, 2, torch.bfloat16),
+    (1, 300, 256, 256, 0, torch.float16),
+    (2, 640, 0, 127, 1, torch.float16),
+    (1, 1100, 300, 0, 0, torch.bfloat16),
+    (2, 515, 3, 3, 3, torch.float16),
+    (1, 129, 1, 2, 0, torch.bfloat16),
+    (2, 200, 20, 20, 0, torch.float32),
+    (1, 333, 7, 30, 2, torch.float32),
+]
+
+
+def unit_ids(c):
+    return f"BH{c[0]}-n{c[1]}-w{c[2]}-wu{c[3]}-d{c[4]}-{str(c[5]).split('.')[-1]}"
+
+
+def mkdesc(BH, n, w, wu, d, dtype, padding=0.0, hd=64):
+    return swab.Desc(1, BH, n, hd, w, wu, d, padding, dtype)
+
+
+def score_tol(dtype):
+    return F32_TOL if dtype == torch.float32 else SCORE_TOL
+
+
+@pytest.mark.parametrize("case", UNIT_CASES, ids=unit_ids)
+def test_band_qk_unit(case):
+    BH, n, w, wu, dil, dtype = case
+    d = mkdesc(BH, n, w, wu, dil, dtype, padding=-3.25)
+    A, B = seeded_qkvo(BH, n, 64, dtype, seed=11, count=2)
+    S = empty_band(d)
+    swab.band_qk(d, 0.125, *dev(A, B), S)
+    ref = oracle.band_qk(f64(A), f64(B), w, wu, dil, alpha=0.125, padding=-3.25)
+    got = f64(S)
+    m = valid_mask(n, w, wu, dil)
+    assert np.all(got[:, ~m] == -3.25), "padding slots must hold the padding value exactly"
+    assert normwise(got, ref, m) <= score_tol(dtype)
+
+
+@pytest.mark.parametrize("case", UNIT_CASES, ids=unit_ids)
+def test_band_softmax_unit(case):
+    BH, n, w, wu, dil, dtype = case
+    d = mkdesc(BH, n, w, wu, dil, dtype)
+    S = (seeded_band(BH, n, d.D, torch.float32, seed=12) * 3).to(dtype)
+    P = empty_band(d)
+    lse = torch.empty((BH, n), dtype=torch.float32, device="cuda")
+    swab.band_softmax(d, poison_invalid(S, n, w, wu, dil).cuda(), P, lse)
+    refP, reflse = oracle.band_softmax(f64(S), w, wu, dil)
+    got = f64(P)
+    tol = 1e-6 if dtype == torch.float32 else ABS_TOL
+    assert np.max(np.abs(got - refP)) <= tol
+    assert np.max(np.abs(f64(lse) - reflse)) <= 1e-4 * max(1.0, np.max(np.abs(reflse)))
+    assert np.all(got[:, ~valid_mask(n, w, wu, dil)] == 0.0)
+
+
+@pytest.mark.parametrize("case", UNIT_CASES, ids=unit_ids)
+def test_band_pv_unit(case):
+    BH, n, w, wu, dil, dtype = case
+    d = mkdesc(BH, n, w, wu, dil, dtype)
+    P = seeded_band(BH, n, d.D, dtype, seed=13)
+    (V,) = seeded_qkvo(BH, n, 64, dtype, seed=14, count=1)
+    O = empty_dense(d)
+    swab.band_pv(d, 0.75, poison_invalid(P, n, w, wu, dil).cuda(), V.cuda(), O)
+    ref = oracle.band_pv(f64(P), f64(V), w, wu, dil, alpha=0.75)
+    assert normwise(f64(O), ref) <= score_tol(dtype)
+
+
+@pytest.mark.parametrize("case", UNIT_CASES, ids=unit_ids)
+@pytest.mark.parametrize("name", ["band_qk_bwd_t", "band_pv_bwd_t"])
+def test_band_t_unit(case, name):
+    BH, n, w, wu, dil, dtype = case
+    d = mkdesc(BH, n, w, wu, dil, dtype)
+    Bd = seeded_band(BH, n, d.D, dtype, seed=15)
+    (Y,) = seeded_qkvo(BH, n, 64, dtype, seed=16, count=1)
+    X = empty_dense(d)
+    getattr(swab, name)(d, 0.5, poison_invalid(Bd, n, w, wu, dil).cuda(), Y.cuda(), X)
+    ref = oracle.band_t(f64(Bd), f64(Y), w, wu, dil, alpha=0.5)
+    assert normwise(f64(X), ref) <= score_tol(dtype)
+
+
+@pytest.mark.parametrize("case", UNIT_CASES, ids=unit_ids)
+def test_band_softmax_bwd_unit(case):
+    BH, n, w, wu, dil, dtype = case
+    d = mkdesc(BH, n, w, wu, dil, dtype)
+    P = seeded_band(BH, n, d.D, dtype, seed=17)
+    dP = seeded_band(BH, n, d.D, dtype, seed=18)
+    dS = empty_band(d)
+    swab.band_softmax_bwd(d, poison_invalid(P, n, w, wu, dil).cuda(),
+                          poison_invalid(dP, n, w, wu, dil).cuda(), dS)
+    ref = oracle.band_softmax_bwd(f64(P), f64(dP), w, wu, dil)
+    got = f64(dS)
+    m = valid_mask(n, w, wu, dil)
+    assert np.all(got[:, ~m] == 0.0)
+    assert normwise(got, ref, m) <= score_tol(dtype)
+
+
+# ---------------------------------------------------------------------------
+# bit-exact band indexing probes
+# ---------------------------------------------------------------------------
+PROBE_CASES = [  # BH, n, w, w_upper, dilation, dtype
+    (2, 1000, 64, 64, 0, torch.float16),
+    (1, 4100, 256, 256, 3, torch.bfloat16),
+    (1, 2049, 500, 0, 1, torch.float16),
+]
+
+
+def digit(j, k):
+    return (j >> (5 * k)) & 31  # base-32 digits: exact in fp16 and bf16
+
+
+@pytest.mark.parametrize("case", PROBE_CASES, ids=unit_ids)
+def test_index_probe_band_qk(case):
+    BH, n, w, wu, dil, dtype = case
+    d = mkdesc(BH, n, w, wu, dil, dtype, padding=-1.0)
+    j = torch.arange(n)
+    for k in range(3):
+        Q = torch.zeros(BH, n, 64)
+        Q[:, :, k] = 1.0
+        K = torch.zeros(BH, n, 64)
+        K[:, :, k] = digit(j, k).float()
+        Q, K = Q.to(dtype), K.to(dtype)
+        S = empty_band(d)
+        swab.band_qk(d, 1.0, *dev(Q, K), S)
+        ref = oracle.band_qk(f64(Q), f64(K), w, wu, dil, alpha=1.0, padding=-1.0)
+        np.testing.assert_array_equal(f64(S), ref)
+
+
+def one_hot_band(BH, n, w, wu, dil, dtype, seed):
+    """One valid slot per row set to 1, other valid slots 0, invalid slots NaN."""
+    D = w + wu + 1
+    m = valid_mask(n, w, wu, dil)
+    rng = np.random.default_rng(seed)
+    band = np.zeros((BH, n, D), dtype=np.float32)
+    for i in range(n):
+        ts = np.nonzero(m[i])[0]
+        for b in range(BH):
+            band[b, i, rng.choice(ts)] = 1.0
+    band[:, ~m] = np.nan
+    return torch.from_numpy(band).to(dtype)
+
+
+@pytest.mark.parametrize("case", PROBE_CASES, ids=unit_ids)
+def test_index_probe_band_pv_and_t(case):
+    BH, n, w, wu, dil, dtype = case
+    d = mkdesc(BH, n, w, wu, dil, dtype)
+    band = one_hot_band(BH, n, w, wu, dil, dtype, seed=19)
+    Y = torch.zeros(BH, n, 64)
+    for k in range(3):
+        Y[:, :, k] = digit(torch.arange(n), k).float()
+    Y = Y.to(dtype)
+    clean = torch.nan_to_num(band.float(), nan=0.0)
+    O = empty_dense(d)
+    swab.band_pv(d, 1.0, band.cuda(), Y.cuda(), O)
+    np.testing.assert_array_equal(f64(O), oracle.band_pv(f64(clean), f64(Y), w, wu, dil))
+    if dtype == torch.float16:  # column sums of digits stay exact in fp16
+        X = empty_dense(d)
+        swab.band_pv_bwd_t(d, 1.0, band.cuda(), Y.cuda(), X)
+        np.testing.assert_array_equal(f64(X), oracle.band_t(f64(clean), f64(Y), w, wu, dil))
+
+
+# ---------------------------------------------------------------------------
+# the full chain (forward + backward) on the named workloads
+# ---------------------------------------------------------------------------
+def gpu_chain(d, Q, K, V, dO, scale):
+    S, P, dP, dS = (empty_band(d) for _ in range(4))
+    lse = torch.empty((d.BH, d.n), dtype=torch.float32, device="cuda")
+    O, dQ, dK, dV = (empty_dense(d) for _ in range(4))
+    swab.band_qk(d, scale, Q, K, S)
+    swab.band_softmax(d, S, P, lse)
+    swab.band_pv(d, 1.0, P, V, O)
+    swab.band_qk(d, 1.0, dO, V, dP)
+    swab.band_softmax_bwd(d, P, dP, dS)
+    swab.band_pv(d, scale, dS, K, dQ)
+    swab.band_qk_bwd_t(d, scale, dS, Q, dK)
+    swab.band_pv_bwd_t(d, 1.0, P, dO, dV)
+    torch.cuda.synchronize()
+    return dict(S=S, P=P, lse=lse, O=O, dQ=dQ, dK=dK, dV=dV)
+
+
+def check_chain(wl, slices, backward=True):
+    Q, K, V, dO = workload_inputs(wl)
+    d = swab.Desc.from_workload(wl)
+    out = gpu_chain(d, *dev(Q, K, V, dO), wl.scale)
+    w, wu, dil = wl.w, wl.w_upper, wl.dilation
+    m = valid_mask(wl.n, w, wu, dil)
+    f32 = wl.dtype == torch.float32
+    for b in slices:
+        sl = slice(b, b + 1)
+        q, k, v, go = (f64(x[sl]) for x in (Q, K, V, dO))
+        refS = oracle.band_qk(q, k, w, wu, dil, alpha=wl.scale, padding=wl.padding)
+        gotS = f64(out["S"][sl])
+        assert np.all(gotS[:, ~m] == wl.padding)
+        assert normwise(gotS, refS, m) <= (F32_TOL if f32 else SCORE_TOL)
+        refO, reflse = oracle.attention_fwd(q, k, v, w, wu, dil, wl.scale)
+        refP, _ = oracle.band_softmax(refS, w, wu, dil)
+        if f32:
+            assert normwise(f64(out["P"][sl]), refP) <= F32_TOL
+            assert normwise(f64(out["O"][sl]), refO) <= F32_TOL
+        else:
+            assert np.max(np.abs(f64(out["P"][sl]) - refP)) <= ABS_TOL
+            assert np.max(np.abs(f64(out["O"][sl]) - refO)) <= ABS_TOL
+        assert np.max(np.abs(f64(out["lse"][sl]) - reflse)) <= (1e-5 if f32 else 2e-2)
+        if backward:
+            rq, rk, rv = oracle.attention_bwd(q, k, v, go, w, wu, dil, wl.scale)
+            for name, ref in (("dQ", rq), ("dK", rk), ("dV", rv)):
+                got = f64(out[name][sl])
+                if f32:
+                    assert normwise(got, ref) <= F32_TOL, name
+                else:
+                    assert np.max(np.abs(got - ref)) <= ABS_TOL, name
+
+
+def test_chain_config1_fp32_full():
+    check_chain(WORKLOADS[1], slices=range(WORKLOADS[1].BH))
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_chain_config_fp16_sampled(cfg):
+    check_chain(WORKLOADS[cfg], slices=(0, 7))
+
+
+def test_chain_config5_materialised_sampled():
+    check_chain(WORKLOADS[5], slices=(5,), backward=False)
