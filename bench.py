@@ -1,0 +1,478 @@
+#!/usr/bin/env python3
+"""Benchmark: banded attention forward + backward on one GB300 (sm_103a).
+
+One step = one forward + backward pass of sliding-window attention over the
+Longformer-base workload (b=1, h=12, n=4096, head_dim=64, w=w_upper=256,
+fp16, dilation 0), every kernel launched through the C ABI:
+
+  band_qk(Q,K)->S, band_softmax(S)->P,lse, band_pv(P,V)->O,
+  band_qk(dO,V)->dP, band_softmax_bwd(P,dP)->dS, band_pv(dS,K)->dQ,
+  band_qk_bwd_t(dS,Q)->dK, band_pv_bwd_t(P,dO)->dV.
+
+`value` is TFLOP/s on algorithmic flops (6 banded contractions x 2*head_dim
+per valid (query, key) pair) over device time with inputs resident in HBM.
+L2 is flushed (a 256 MB write) before every step, outside the timed events.
+`e2e` is the same metric with pinned-host inputs copied in and the outputs
+(O, dQ, dK, dV) copied back inside the timed region.
+
+--impl reference times the fp64 CPU oracle (the only reference this subject
+has) on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+(b,h) slices are independent; there is no exchange), scaling "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sliding_window_attention_band_gb300.inputs import WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "banded attention fwd+bwd ms & TFLOP/s at n=4096,w=256,d=0/3; % of roofline"
+MAIN_CFG = 2
+ALSO_CFG = 3
+N_CONTRACTIONS = 6
+FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# accounting (algorithmic work of one step)
+# ---------------------------------------------------------------------------
+def valid_pairs(wl) -> int:
+    s = wl.dilation + 1
+    i = np.arange(wl.n, dtype=np.int64)
+    t_lo = np.maximum(0, wl.w - i // s)
+    t_hi = np.minimum(wl.D - 1, wl.w + (wl.n - 1 - i) // s)
+    return int((t_hi - t_lo + 1).sum()) * wl.BH
+
+
+def step_flops(wl) -> float:
+    return float(N_CONTRACTIONS * 2 * wl.head_dim * valid_pairs(wl))
+
+
+def kernel_bytes(wl) -> dict:
+    e = torch.finfo(wl.dtype).bits // 8
+    dense = wl.BH * wl.n * wl.head_dim * e
+    band = wl.BH * wl.n * wl.D * e
+    lse = wl.BH * wl.n * 4
+    return {
+        "band_qk": 2 * dense + band,
+        "band_softmax": 2 * band + lse,
+        "band_pv": band + 2 * dense,
+        "band_softmax_bwd": 3 * band,
+        "band_t": band + 2 * dense,
+    }
+
+
+def kernel_flops(wl) -> dict:
+    c = 2.0 * wl.head_dim * valid_pairs(wl)
+    return {"band_qk": c, "band_softmax": 0.0, "band_pv": c, "band_softmax_bwd": 0.0,
+            "band_t": c}
+
+
+# ---------------------------------------------------------------------------
+# the step
+# ---------------------------------------------------------------------------
+class Step:
+    """Buffers and launches of one forward + backward step."""
+
+    NAMES = ["band_qk", "band_softmax", "band_pv", "band_qk", "band_softmax_bwd", "band_pv",
+             "band_t", "band_t"]
+
+    def __init__(self, wl, device):
+        import sliding_window_attention_band_gb300 as swab
+
+        self.swab = swab
+        self.wl = wl
+        self.d = swab.Desc.from_workload(wl)
+        Q, K, V, dO = workload_inputs(wl)
+        self.host = [x.pin_memory() for x in (Q, K, V, dO)]
+        self.Q, self.K, self.V, self.dO = (x.to(device) for x in (Q, K, V, dO))
+        band = (wl.BH, wl.n, wl.D)
+        dense = (wl.BH, wl.n, wl.head_dim)
+        mk = lambda shape: torch.empty(shape, dtype=wl.dtype, device=device)  # noqa: E731
+        self.S, self.P, self.dP, self.dS = (mk(band) for _ in range(4))
+        self.O, self.dQ, self.dK, self.dV = (mk(dense) for _ in range(4))
+        self.lse = torch.empty((wl.BH, wl.n), dtype=torch.float32, device=device)
+        self.out_host = [torch.empty(dense, dtype=wl.dtype).pin_memory() for _ in range(4)]
+
+    def launches(self):
+        s, d, sc = self.swab, self.d, self.wl.scale
+        return [
+            lambda: s.band_qk(d, sc, self.Q, self.K, self.S),
+            lambda: s.band_softmax(d, self.S, self.P, self.lse),
+            lambda: s.band_pv(d, 1.0, self.P, self.V, self.O),
+            lambda: s.band_qk(d, 1.0, self.dO, self.V, self.dP),
+            lambda: s.band_softmax_bwd(d, self.P, self.dP, self.dS),
+            lambda: s.band_pv(d, sc, self.dS, self.K, self.dQ),
+            lambda: s.band_qk_bwd_t(d, sc, self.dS, self.Q, self.dK),
+            lambda: s.band_pv_bwd_t(d, 1.0, self.P, self.dO, self.dV),
+        ]
+
+    def run(self, events=None):
+        for k, fn in enumerate(self.launches()):
+            if events is not None:
+                events[k].record()
+            fn()
+        if events is not None:
+            events[-1].record()
+
+    def h2d(self):
+        for dst, src in zip((self.Q, self.K, self.V, self.dO), self.host):
+            dst.copy_(src, non_blocking=True)
+
+    def d2h(self):
+        for dst, src in zip(self.out_host, (self.O, self.dQ, self.dK, self.dV)):
+            dst.copy_(src, non_blocking=True)
+
+    @property
+    def h2d_bytes(self):
+        return sum(x.numel() * x.element_size() for x in self.host)
+
+    @property
+    def d2h_bytes(self):
+        return sum(x.numel() * x.element_size() for x in self.out_host)
+
+
+def time_steps(step, steps, warmup, flush):
+    """Per-step device times (ms) and per-kernel times (ms) over `steps` steps."""
+    for _ in range(warmup):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    nk = len(step.NAMES)
+    per_step, per_kernel = [], [[] for _ in range(nk)]
+    for _ in range(steps):
+        flush.zero_()  # L2 flush outside the timed events
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+        step.run(ev)
+        torch.cuda.synchronize()
+        per_step.append(ev[0].elapsed_time(ev[-1]))
+        for k in range(nk):
+            per_kernel[k].append(ev[k].elapsed_time(ev[k + 1]))
+    return per_step, per_kernel
+
+
+def time_e2e(step, steps, warmup, flush):
+    for _ in range(warmup):
+        step.h2d()
+        step.run()
+        step.d2h()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step.h2d()
+        step.run()
+        step.d2h()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return times
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# roofline
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash(kernel):
+    files = {"band_qk": "k_band_qk.cu", "band_pv": "k_band_gather.cu", "band_t": "k_band_gather.cu",
+             "band_softmax": "k_softmax.cu", "band_softmax_bwd": "k_softmax.cu"}
+    path = os.path.join(ROOT, "sliding_window_attention_band_gb300", "csrc", files[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source
+    still matches the one profiled; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    ent = table.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_sha256_16") != kernel_source_hash(kernel):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def roofline(wl, names, per_kernel_ms, peaks):
+    """The kernel with the largest total time in the step."""
+    tot = {}
+    cnt = {}
+    for name, ts in zip(names, per_kernel_ms):
+        tot[name] = tot.get(name, 0.0) + sum(ts)
+        cnt[name] = cnt.get(name, 0) + len(ts)
+    top = max(tot, key=tot.get)
+    avg_ms = tot[top] / cnt[top]
+    nbytes = kernel_bytes(wl)[top]
+    flops = kernel_flops(wl)[top]
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_tc > t_hbm:
+        ach, peak, unit, bound = flops / (avg_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor"
+    else:
+        ach, peak, unit, bound = nbytes / (avg_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
+    return {"kernel": top, "bound": bound, "achieved": round(ach, 1), "peak": peak,
+            "unit": unit, "frac": round(ach / peak, 4), "traffic": ncu_traffic(top, wl.name),
+            "algorithmic_bytes": nbytes, "avg_launch_us": round(avg_ms * 1e3, 2),
+            "peak_source": peaks["source"]}
+
+
+def step_roofline_frac(wl, names, per_kernel_ms, peaks):
+    """sum over kernels of max(bytes/BW, flops/TC) / measured step time."""
+    kb, kf = kernel_bytes(wl), kernel_flops(wl)
+    ideal = sum(max(kb[nm] / (peaks["hbm_gbs"] * 1e9), kf[nm] / (peaks["bf16_tflops"] * 1e12))
+                for nm in names)
+    meas = sum(statistics.mean(ts) for ts in per_kernel_ms) * 1e-3
+    return ideal / meas
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+def oracle_step(wl, slices):
+    """The same fwd+bwd chain on the fp64 oracle for `slices` (b,h) slices."""
+    import oracle
+
+    Q, K, V, dO = workload_inputs(wl)
+    q, k, v, go = (x[:slices].double().numpy() for x in (Q, K, V, dO))
+    w, wu, dil, sc = wl.w, wl.w_upper, wl.dilation, wl.scale
+    t0 = time.perf_counter()
+    S = oracle.band_qk(q, k, w, wu, dil, sc, wl.padding)
+    P, _ = oracle.band_softmax(S, w, wu, dil)
+    oracle.band_pv(P, v, w, wu, dil, 1.0)
+    dP = oracle.band_qk(go, v, w, wu, dil, 1.0, wl.padding)
+    dS = oracle.band_softmax_bwd(P, dP, w, wu, dil)
+    oracle.band_pv(dS, k, w, wu, dil, sc)
+    oracle.band_t(dS, q, w, wu, dil, sc)
+    oracle.band_t(P, go, w, wu, dil, 1.0)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    import oracle
+
+    t1 = oracle_step(wl, 1)
+    slices = int(max(1, min(wl.BH, budget_s // max(t1, 1e-3))))
+    t = oracle_step(wl, slices) if slices > 1 else t1
+    flops = step_flops(wl) * slices / wl.BH
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{slices} of {wl.BH} (b,h) slices of {wl.name}, full fwd+bwd chain in fp64, "
+                      f"{t:.2f} s"}
+
+
+def run_reference(args):
+    import oracle
+
+    wl = WORKLOADS[MAIN_CFG]
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_step(wl, 1)
+    ts = [oracle_step(wl, 1) for _ in range(args.steps)]
+    flops = step_flops(wl) / wl.BH
+    val = flops / statistics.mean(ts) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(statistics.mean(ts) * 1e3 * wl.BH, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {**wl.describe(), "parallelism": "none (host oracle)"},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s",
+                             "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"each step: 1 of {wl.BH} (b,h) slices, fwd+bwd chain, fp64; "
+                                       "ms_per_step scaled to all slices"},
+            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="swab", choices=["swab", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+
+    from sliding_window_attention_band_gb300 import build as swab_build
+
+    if rank == 0 or world == 1:
+        swab_build.build()
+    if dist:
+        dist.barrier()
+    import sliding_window_attention_band_gb300 as swab
+
+    swab.load()
+    device = torch.device("cuda", local)
+    wl = WORKLOADS[MAIN_CFG]
+    step = Step(wl, device)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    per_step, per_kernel = time_steps(step, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+
+    dev_ms = sum(per_step)
+    if dist:
+        t = torch.tensor([dev_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_ms = float(t.item())
+    ms_per_step = dev_ms / args.steps
+    flops = step_flops(wl)
+    value = world * flops * args.steps / (dev_ms * 1e-3) / 1e12
+
+    # dilation-3 companion (same step, config 3)
+    also = {}
+    wl3 = WORKLOADS[ALSO_CFG]
+    step3 = Step(wl3, device)
+    ps3, pk3 = time_steps(step3, max(3, args.steps // 2), 3, flush)
+    also[wl3.name] = {"ms_per_step": round(statistics.mean(ps3), 4),
+                      "tflops": round(step_flops(wl3) / (statistics.mean(ps3) * 1e-3) / 1e12, 3),
+                      "per_kernel_us": {f"{i}:{nm}": round(statistics.mean(t) * 1e3, 2)
+                                        for i, (nm, t) in enumerate(zip(step3.NAMES, pk3))}}
+    del step3
+
+    e2e_ms = time_e2e(step, max(3, args.steps // 2), 3, flush)
+    e2e_val = world * flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+    if swab.device_status(reset=True) != 0:
+        raise SystemExit("a kernel raised the device status word during the benchmark")
+
+    peaks = measured_peaks()
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {**wl.describe(), "parallelism": f"replicas x{world}" if world > 1 else "none",
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "step": "fwd+bwd: band_qk, band_softmax, band_pv, band_qk(dO,V), "
+                           "band_softmax_bwd, band_pv(dS,K), band_qk_bwd_t, band_pv_bwd_t",
+                   "flops_per_step": flops},
+        "per_kernel_us": {f"{i}:{nm}": round(statistics.mean(t) * 1e3, 2)
+                          for i, (nm, t) in enumerate(zip(step.NAMES, per_kernel))},
+        "roofline": roofline(wl, step.NAMES, per_kernel, peaks),
+        "step_roofline_frac": round(step_roofline_frac(wl, step.NAMES, per_kernel, peaks), 4),
+        "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": step.h2d_bytes, "d2h_bytes_per_step": step.d2h_bytes,
+                "ms_per_step": round(statistics.mean(e2e_ms), 4)},
+        "gpu_launches": len(step.NAMES) * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 3),
+        "also": also,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -2,11 +2,14 @@
 
 Both sides get the same dtype-rounded inputs (upcast to fp64 for the oracle,
 exactly).  Tolerances:
-  * fp16/bf16 banded scores: normwise  max|gpu - ref| / max|ref|  <= 2e-3 over
-    valid slots (one RNE rounding of an fp32 accumulator is at most 2^-9
-    relative for bf16, 2^-12 for fp16); padding slots bit-exact;
+  * fp16 banded scores: normwise  max|gpu - ref| / max|ref|  <= 2e-3 over
+    valid slots (one RNE rounding of the fp32 accumulator costs at most
+    2^-11 = 4.9e-4 relative); padding slots bit-exact;
+  * bf16 banded scores: 2e-3 is below the format's own resolution -- one
+    correctly rounded bf16 store is off by up to 2^-8 = 3.9e-3 relative -- so
+    the bound is that unit roundoff plus 1e-4 of fp32-accumulation slack;
   * dense outputs of the unit kernels fed random (non-probability) bands:
-    the same normwise 2e-3;
+    the same per-dtype bounds;
   * attention chains (O, P, dQ, dK, dV): max abs 1e-2;
   * fp32 inputs: normwise relative 1e-5 (FFMA path, no TF32);
   * band indexing probes: bit-exact.
@@ -104,8 +107,11 @@ def mkdesc(BH, n, w, wu, d, dtype, padding=0.0, hd=64):
     return swab.Desc(1, BH, n, hd, w, wu, d, padding, dtype)
 
 
+BF16_SCORE_TOL = 2.0 ** -8 + 1e-4
+
+
 def score_tol(dtype):
-    return F32_TOL if dtype == torch.float32 else SCORE_TOL
+    return {torch.float32: F32_TOL, torch.float16: SCORE_TOL, torch.bfloat16: BF16_SCORE_TOL}[dtype]
 
 
 @pytest.mark.parametrize("case", UNIT_CASES, ids=unit_ids)
@@ -275,7 +281,7 @@ def check_chain(wl, slices, backward=True):
         refS = oracle.band_qk(q, k, w, wu, dil, alpha=wl.scale, padding=wl.padding)
         gotS = f64(out["S"][sl])
         assert np.all(gotS[:, ~m] == wl.padding)
-        assert normwise(gotS, refS, m) <= (F32_TOL if f32 else SCORE_TOL)
+        assert normwise(gotS, refS, m) <= score_tol(wl.dtype)
         refO, reflse = oracle.attention_fwd(q, k, v, w, wu, dil, wl.scale)
         refP, _ = oracle.band_softmax(refS, w, wu, dil)
         if f32:
@@ -306,3 +312,40 @@ def test_chain_config_fp16_sampled(cfg):
 
 def test_chain_config5_materialised_sampled():
     check_chain(WORKLOADS[5], slices=(5,), backward=False)
+
+
+# ---------------------------------------------------------------------------
+# fused forward: scores kept on chip
+# ---------------------------------------------------------------------------
+def check_fused(d, Q, K, V, scale, slices, f32):
+    O = empty_dense(d)
+    lse = torch.empty((d.BH, d.n), dtype=torch.float32, device="cuda")
+    swab.band_attention(d, scale, *dev(Q, K, V), O, lse)
+    torch.cuda.synchronize()
+    for b in slices:
+        sl = slice(b, b + 1)
+        refO, reflse = oracle.attention_fwd(f64(Q[sl]), f64(K[sl]), f64(V[sl]), d.w, d.w_upper,
+                                            d.dilation, scale)
+        gotO, gotl = f64(O[sl]), f64(lse[sl])
+        if f32:
+            assert normwise(gotO, refO) <= F32_TOL
+            assert np.max(np.abs(gotl - reflse)) <= 1e-5
+        else:
+            assert np.max(np.abs(gotO - refO)) <= ABS_TOL
+            assert np.max(np.abs(gotl - reflse)) <= 2e-2
+
+
+@pytest.mark.parametrize("case", UNIT_CASES, ids=unit_ids)
+def test_band_attention_unit(case):
+    BH, n, w, wu, dil, dtype = case
+    d = mkdesc(BH, n, w, wu, dil, dtype)
+    Q, K, V = seeded_qkvo(BH, n, 64, dtype, seed=21, count=3)
+    check_fused(d, Q, K, V, 0.125, range(BH), dtype == torch.float32)
+
+
+@pytest.mark.parametrize("cfg,slices", [(1, (0, 1)), (2, (0, 11)), (3, (4,)), (5, (2,))])
+def test_band_attention_config(cfg, slices):
+    wl = WORKLOADS[cfg]
+    Q, K, V, _ = workload_inputs(wl)
+    check_fused(swab.Desc.from_workload(wl), Q, K, V, wl.scale, slices,
+                wl.dtype == torch.float32)
