@@ -290,9 +290,19 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
     if ((s = check_no_globals(desc)) != SWAB_OK) return s;
     if ((s = check_ptrs({Q, K, V, O})) != SWAB_OK) return s;
     if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
-    (void)scale;
-    (void)stream;
-    return SWAB_ERR_UNSUPPORTED;  // fused kernel not built yet
+    if (dt == kF32) {
+        AttnArgsF32 a{g, scale, static_cast<const float *>(Q), static_cast<const float *>(K),
+                      static_cast<const float *>(V), static_cast<float *>(O), lse};
+        return from_cuda(launch_band_attention_f32(a, as_stream(stream)));
+    }
+    TmapSet mq, mk, mv;
+    if (!build_rows_maps(&mq, Q, g, dt, kQKBoxRows) || !build_rows_maps(&mk, K, g, dt, kQKBoxRows) ||
+        !build_rows_maps(&mv, V, g, dt, kQKBoxRows))
+        return SWAB_ERR_CUDA;
+    unsigned *err = status_word();
+    if (!err) return SWAB_ERR_CUDA;
+    AttnArgs a{g, scale, O, lse, err};
+    return from_cuda(launch_band_attention_tc(dt, mq, mk, mv, a, as_stream(stream)));
 }
 
 }  // extern "C"

@@ -51,6 +51,22 @@ struct SoftmaxArgs {
     unsigned *err;
 };
 
+struct AttnArgs {     // fused forward, tensor-core path
+    Geom g;
+    float scale;
+    void *O;          // [BH, n, 64]
+    float *lse;       // [BH, n] or null
+    unsigned *err;
+};
+
+struct AttnArgsF32 {  // fused forward, fp32 path
+    Geom g;
+    float scale;
+    const float *Q, *K, *V;
+    float *O;
+    float *lse;
+};
+
 struct DenseArgs {    // fp32 FFMA path
     Geom g;
     float alpha;
@@ -64,6 +80,9 @@ cudaError_t launch_band_qk_tc(DType dt, const TmapSet &mapA, const TmapSet &mapB
                               const QKArgs &a, cudaStream_t st);
 cudaError_t launch_band_gather_tc(DType dt, bool transposed, const TmapSet &mapB,
                                   const GatherArgs &a, cudaStream_t st);
+cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
+                                     const TmapSet &mapV, const AttnArgs &a, cudaStream_t st);
+cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st);
 // fp32 FFMA paths
 cudaError_t launch_band_qk_f32(const DenseArgs &a, cudaStream_t st);
 cudaError_t launch_band_pv_f32(const DenseArgs &a, cudaStream_t st);
