@@ -86,25 +86,6 @@ __device__ __forceinline__ uint4 mask_elems(uint4 v, int lo, int hi) {
     return make_uint4(v.x & m[0], v.y & m[1], v.z & m[2], v.w & m[3]);
 }
 
-// Load 8 consecutive band elements starting at element offset `e_start` of the
-// band tensor (any 2-byte boundary), keeping only positions [vlo, vhi) of the
-// 8 (the rest read as zero and are not fetched when no valid byte lies in a
-// 16-byte piece).  `shift` = e_start mod 8, uniform across the warp.
-__device__ __forceinline__ uint4 load_line_piece(const uint16_t *band, long long e_start,
-                                                 int shift, int vlo, int vhi) {
-    vlo = max(vlo, 0);
-    vhi = min(vhi, 8);
-    if (vlo >= vhi) return make_uint4(0, 0, 0, 0);
-    const long long e_al = e_start - shift;  // multiple of 8
-    const uint16_t *p = band + e_al;
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-    if (shift + vlo < 8) lo = ldg16(p);
-    if (shift + vhi > 8) hi = ldg16(p + 8);
-    uint4 v = extract_elems(lo, hi, shift);
-    if (vlo > 0 || vhi < 8) v = mask_elems(v, vlo, vhi);
-    return v;
-}
-
 template <typename T, bool kTrans>
 __global__ void __launch_bounds__(kThreads, 2)
     k_band_gather_tc(const __grid_constant__ TmapSet mapB, const GatherArgs p) {
@@ -195,52 +176,91 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ---------------- gather warps ----------------
+        // Each warp owns 4 of the 32 tasks of a stage (task = lines of one
+        // class mod 8).  Per task the line geometry is fixed up to a per-stage
+        // increment, so it is set up once; per stage the warp first issues all
+        // of its band loads (up to 8 per lane, before it even waits for the
+        // stage to be free), then realigns and stores them.
         const int gw = warp - 2;
         const uint16_t *band = reinterpret_cast<const uint16_t *>(p.band);
         const long long slice_row0 = (long long)bh * g.n + r;  // band row of sub-index 0
+        constexpr int kTasks = 32 / kGW;
+        long long e_line[kTasks];  // element offset of this lane's 8 elements, stage 0
+        int vlo[kTasks];           // first valid element of the lane's piece, stage 0
+        int vcap[kTasks];          // valid elements end at min(vlo + D, vcap - stage*64) (pv) / vcap (t)
+        int shift[kTasks];
+        int qline[kTasks];         // band_t: query sub-index of the lane's line at stage 0
+        uint32_t dst[kTasks];      // byte offset inside the A stage
+        long long e_step;          // e_line increment per stage
+#pragma unroll
+        for (int u = 0; u < kTasks; ++u) {
+            const int task = gw + kGW * u;
+            const int cls = task & 7, sub = task >> 3;
+            if (!kTrans) {
+                // 128 lines (queries) x 64 keys: 4 lines per task, 8 pieces each
+                const int line = cls + 8 * (4 * sub + (lane >> 3));
+                const int j = lane & 7;
+                const int qq = a0 + line;
+                const long long el = (slice_row0 + (long long)g.s * qq) * g.D + (k_lo - qq + g.w);
+                shift[u] = (int)(el & 7);
+                e_line[u] = el + 8 * j;
+                vlo[u] = qq - g.w - k_lo - 8 * j;
+                vcap[u] = qq < nr ? (k_hi - k_lo + 1 - 8 * j) : -(1 << 30);
+                qline[u] = 0;
+                dst[u] = line * 128 + ((j ^ (line & 7)) << 4);
+            } else {
+                // 64 lines (queries) x 128 keys: 2 lines per task, 16 pieces each
+                const int line = cls + 8 * (2 * sub + (lane >> 4));
+                const int j = lane & 15;
+                const int qq = k_lo + line;
+                const long long el = (slice_row0 + (long long)g.s * qq) * g.D + (a0 - qq + g.w);
+                shift[u] = (int)(el & 7);
+                e_line[u] = el + 8 * j;
+                vlo[u] = qq - g.w - a0 - 8 * j;
+                vcap[u] = nr - a0 - 8 * j;
+                qline[u] = qq;
+                dst[u] = (j >> 3) * (kKC * 128) + line * 128 + (((j & 7) ^ (line & 7)) << 4);
+            }
+        }
+        e_step = kTrans ? (long long)kKC * ((long long)g.s * g.D - 1) : kKC;
         bool ok = true;
         for (int c = 0; c < nck; ++c) {
             const int st = c % kStages;
             const uint32_t ph = (c / kStages) & 1;
+            uint4 lo[kTasks], hi[kTasks];
+            int plo[kTasks], phi[kTasks];
+#pragma unroll
+            for (int u = 0; u < kTasks; ++u) {
+                // valid elements of this lane's piece: [plo, phi) within [0, 8)
+                int l0, h0;
+                if (!kTrans) {
+                    l0 = vlo[u] - kKC * c;
+                    h0 = min(l0 + g.D, vcap[u] - kKC * c);
+                } else {
+                    l0 = vlo[u] + kKC * c;
+                    h0 = (qline[u] + kKC * c < nr) ? min(l0 + g.D, vcap[u]) : l0;
+                }
+                plo[u] = max(l0, 0);
+                phi[u] = min(h0, 8);
+                lo[u] = make_uint4(0, 0, 0, 0);
+                hi[u] = make_uint4(0, 0, 0, 0);
+                if (plo[u] < phi[u]) {
+                    const uint16_t *ptr = band + (e_line[u] + e_step * c - shift[u]);
+                    if (shift[u] + plo[u] < 8) lo[u] = ldg16(ptr);
+                    if (shift[u] + phi[u] > 8) hi[u] = ldg16(ptr + 8);
+                }
+            }
             ok = mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             const uint32_t a_addr = smem_u32(atile + st * kATile);
-            const int kc0 = k_lo + c * kKC;  // first K index of this stage
-#pragma unroll 1
-            for (int task = gw; task < 32; task += kGW) {
-                const int cls = task & 7, sub = task >> 3;
-                int line, j;  // line within the stage tile, 16-byte piece of the line
-                int qq;       // query sub-index of the line
-                long long e_line;  // element offset of the line's first element
-                int vlo, vhi;      // valid element range of the line
-                uint32_t dst;
-                if (!kTrans) {
-                    // 128 lines (queries) x 64 keys: 4 lines per task, 8 pieces each
-                    line = cls + 8 * (4 * sub + (lane >> 3));
-                    j = lane & 7;
-                    qq = a0 + line;
-                    // element k of the line is key kc0 + k, slot kc0 + k - qq + w
-                    e_line = (slice_row0 + (long long)g.s * qq) * g.D + (kc0 - qq + g.w);
-                    vlo = qq - g.w - kc0;
-                    vhi = min(vlo + g.D, k_hi - kc0 + 1);
-                    if (qq >= nr) vhi = vlo;  // padded query rows read as zero
-                    dst = a_addr + line * 128 + ((j ^ (line & 7)) << 4);
-                } else {
-                    // 64 lines (queries) x 128 keys: 2 lines per task, 16 pieces each
-                    line = cls + 8 * (2 * sub + (lane >> 4));
-                    j = lane & 15;
-                    qq = kc0 + line;
-                    // element m of the line is key a0 + m, slot a0 + m - qq + w
-                    e_line = (slice_row0 + (long long)g.s * qq) * g.D + (a0 - qq + g.w);
-                    vlo = qq - g.w - a0;
-                    vhi = min(vlo + g.D, nr - a0);
-                    if (qq >= nr) vhi = vlo;
-                    dst = a_addr + (j >> 3) * (kKC * 128) + line * 128 + (((j & 7) ^ (line & 7)) << 4);
+#pragma unroll
+            for (int u = 0; u < kTasks; ++u) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (plo[u] < phi[u]) {
+                    v = extract_elems(lo[u], hi[u], shift[u]);
+                    if (plo[u] > 0 || phi[u] < 8) v = mask_elems(v, plo[u], phi[u]);
                 }
-                const long long e_start = e_line + 8 * j;
-                const int shift = (int)(e_line & 7);  // same for every line of the task
-                const uint4 v = load_line_piece(band, e_start, shift, vlo - 8 * j, vhi - 8 * j);
-                sts16(dst, v);
+                sts16(a_addr + dst[u], v);
             }
             fence_proxy_async_smem();
             __syncwarp();

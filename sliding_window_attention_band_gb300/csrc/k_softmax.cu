@@ -9,19 +9,31 @@
 // t_hi = min(D-1, w + floor((n-1-i)/s)).
 // Backward:  dS = P * (dP - delta_i), delta_i = sum over valid slots P*dP.
 //
-// One warp per band row.  A band row of D elements starts at an arbitrary
-// element boundary, so the warp walks the row's aligned 16-byte pieces
-// (128-bit loads, 32 consecutive pieces per warp instruction).  Pieces that
+// One warp per band row.  A row of D elements starts at an arbitrary element
+// boundary, so the warp walks the row's aligned 16-byte pieces (128-bit
+// loads, 32 consecutive pieces per warp instruction).  All index math is
+// 32-bit and relative to the row's first aligned piece; a piece whose
+// elements are all valid takes a path with no per-element tests.  Pieces that
 // straddle a row boundary are shared with the neighbouring row's warp: they
-// are read whole but written element by element, only the elements of this
-// row; every other piece is written with one 128-bit store.  Two passes: the
-// reduction, then the write; the second pass re-reads the row from L1/L2.
+// are read whole but written element by element (only this row's elements);
+// every other piece is written with one 128-bit store.
+// Rows of at most 17 pieces per lane are read once into registers; longer
+// rows stream twice (the second read hits L1/L2).
+// exp is computed as 2^(x*log2(e) - m*log2(e)) with the ex2.approx
+// instruction (relative error about 2^-22).
 #include "swab_internal.h"
 
 namespace swab {
 namespace {
 
-constexpr int kRowsPerBlock = 8;  // warps per CTA
+constexpr int kRowsPerBlock = 4;  // warps per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 template <typename T> struct Vec {
     static constexpr int N = 16 / sizeof(T);  // elements per 16-byte piece
@@ -55,155 +67,83 @@ __device__ __forceinline__ uint4 pack(const float (&x)[Vec<T>::N]) {
     }
 }
 
-struct RowSpan {
-    long long e0;       // first element of the row
-    long long c0, c1;   // first / last aligned piece touching the row
-    int t_lo, t_hi;     // valid slots
+// A band row in "piece coordinates": element x of the row's first aligned
+// piece is slot x - lead.  Valid slots map to x in [xlo, xhi]; the row's own
+// elements are x in [lead, lead + D).
+struct Row {
+    long long piece0;  // index (in 16-byte pieces) of the first piece touching the row
+    int lead, npieces, xlo, xhi, xend;
 };
 
-__device__ __forceinline__ RowSpan row_span(const Geom &g, long long R, int epc) {
-    RowSpan rs;
-    const int i = (int)(R % g.n);
-    rs.e0 = R * g.D;
-    rs.c0 = rs.e0 / epc;
-    rs.c1 = (rs.e0 + g.D - 1) / epc;
-    rs.t_lo = max(0, g.w - i / g.s);
-    rs.t_hi = min(g.D - 1, g.w + (g.n - 1 - i) / g.s);
-    return rs;
+template <typename T>
+__device__ __forceinline__ Row make_row(const Geom &g, int R) {
+    constexpr int N = Vec<T>::N;
+    Row rw;
+    const int i = R % g.n;
+    const int t_lo = max(0, g.w - i / g.s);
+    const int t_hi = min(g.D - 1, g.w + (g.n - 1 - i) / g.s);
+    const long long e0 = (long long)R * g.D;
+    rw.lead = (int)(e0 & (N - 1));
+    rw.piece0 = e0 / N;
+    rw.npieces = (rw.lead + g.D + N - 1) / N;
+    rw.xlo = t_lo + rw.lead;
+    rw.xhi = t_hi + rw.lead;
+    rw.xend = rw.lead + g.D;
+    return rw;
 }
 
 template <typename T>
-__device__ __forceinline__ void store_piece(T *base, long long piece, const RowSpan &rs,
-                                            int D, const float (&y)[Vec<T>::N]) {
+__device__ __forceinline__ void store_piece(uint4 *out, int pc, const Row &rw,
+                                            const float (&y)[Vec<T>::N]) {
     constexpr int N = Vec<T>::N;
-    const long long pe = piece * N;
-    if (pe >= rs.e0 && pe + N <= rs.e0 + D) {
-        *reinterpret_cast<uint4 *>(base + pe) = pack<T>(y);
+    const int x0 = pc * N;
+    if (x0 >= rw.lead && x0 + N <= rw.xend) {
+        out[pc] = pack<T>(y);
     } else {
+        T *e = reinterpret_cast<T *>(out + pc);
 #pragma unroll
-        for (int u = 0; u < N; ++u) {
-            const long long e = pe + u;
-            if (e >= rs.e0 && e < rs.e0 + D) base[e] = Elt<T>::from_f(y[u]);
-        }
+        for (int u = 0; u < N; ++u)
+            if (x0 + u >= rw.lead && x0 + u < rw.xend) e[u] = Elt<T>::from_f(y[u]);
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kRowsPerBlock * 32) k_band_softmax_stream(const SoftmaxArgs p) {
-    constexpr int N = Vec<T>::N;
-    const Geom &g = p.g;
-    const int lane = threadIdx.x & 31;
-    const long long R = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (R >= (long long)g.BH * g.n) return;
-    const RowSpan rs = row_span(g, R, N);
-    const T *S = reinterpret_cast<const T *>(p.S);
-    // pass 1: running max / sum of this lane's valid elements
-    float m = -INFINITY, z = 0.f;
-    for (long long c = rs.c0 + lane; c <= rs.c1; c += 32) {
-        float x[N];
-        unpack<T>(ldg16(S + c * N), x);
-#pragma unroll
-        for (int u = 0; u < N; ++u) {
-            const long long t = c * N + u - rs.e0;
-            if (t >= rs.t_lo && t <= rs.t_hi) {
-                if (x[u] > m) {
-                    z = z * expf(m - x[u]) + 1.f;
-                    m = x[u];
-                } else {
-                    z += expf(x[u] - m);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-        const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
-        const float mn = fmaxf(m, m2);
-        z = (m == -INFINITY ? 0.f : z * expf(m - mn)) + (m2 == -INFINITY ? 0.f : z2 * expf(m2 - mn));
-        m = mn;
-    }
-    const float inv = 1.f / z;
-    // pass 2: probabilities
-    T *P = reinterpret_cast<T *>(p.P);
-    for (long long c = rs.c0 + lane; c <= rs.c1; c += 32) {
-        float x[N];
-        unpack<T>(ldg16(S + c * N), x);
-#pragma unroll
-        for (int u = 0; u < N; ++u) {
-            const long long t = c * N + u - rs.e0;
-            x[u] = (t >= rs.t_lo && t <= rs.t_hi) ? expf(x[u] - m) * inv : 0.f;
-        }
-        store_piece<T>(P, c, rs, g.D, x);
-    }
-    if (p.lse && lane == 0) p.lse[R] = m + logf(z);
+__device__ __forceinline__ bool all_valid(int x0, int n, const Row &rw) {
+    return x0 >= rw.xlo && x0 + n - 1 <= rw.xhi;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kRowsPerBlock * 32) k_band_softmax_bwd_stream(const SoftmaxArgs p) {
-    constexpr int N = Vec<T>::N;
-    const Geom &g = p.g;
-    const int lane = threadIdx.x & 31;
-    const long long R = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (R >= (long long)g.BH * g.n) return;
-    const RowSpan rs = row_span(g, R, N);
-    const T *P = reinterpret_cast<const T *>(p.S);
-    const T *dP = reinterpret_cast<const T *>(p.S2);
-    float delta = 0.f;
-    for (long long c = rs.c0 + lane; c <= rs.c1; c += 32) {
-        float x[N], y[N];
-        unpack<T>(ldg16(P + c * N), x);
-        unpack<T>(ldg16(dP + c * N), y);
-#pragma unroll
-        for (int u = 0; u < N; ++u) {
-            const long long t = c * N + u - rs.e0;
-            if (t >= rs.t_lo && t <= rs.t_hi) delta = fmaf(x[u], y[u], delta);
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
-    T *dS = reinterpret_cast<T *>(p.P);
-    for (long long c = rs.c0 + lane; c <= rs.c1; c += 32) {
-        float x[N], y[N];
-        unpack<T>(ldg16(P + c * N), x);
-        unpack<T>(ldg16(dP + c * N), y);
-#pragma unroll
-        for (int u = 0; u < N; ++u) {
-            const long long t = c * N + u - rs.e0;
-            x[u] = (t >= rs.t_lo && t <= rs.t_hi) ? x[u] * (y[u] - delta) : 0.f;
-        }
-        store_piece<T>(dS, c, rs, g.D, x);
-    }
-}
-
-// Register-resident variants: the row's pieces (at most NCH per lane) are
-// read once and kept in registers.
+// ---------------------------------------------------------------------------
+// register-resident rows
+// ---------------------------------------------------------------------------
 template <typename T, int NCH>
-__global__ void __launch_bounds__(kRowsPerBlock * 32) k_band_softmax_reg(const SoftmaxArgs p) {
+__global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const SoftmaxArgs p) {
     constexpr int N = Vec<T>::N;
-    constexpr bool kKeep = NCH * N <= 32;  // keep exp() values, else recompute
-    constexpr float kLog2e = 1.4426950408889634f;
+    constexpr bool kKeep = NCH * N <= 32;  // keep exp() values in registers
     const Geom &g = p.g;
     const int lane = threadIdx.x & 31;
-    const long long R = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (R >= (long long)g.BH * g.n) return;
-    const RowSpan rs = row_span(g, R, N);
-    const T *S = reinterpret_cast<const T *>(p.S);
+    const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (R >= g.BH * g.n) return;
+    const Row rw = make_row<T>(g, R);
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
     uint4 raw[NCH];
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
-        const long long c = rs.c0 + lane + 32 * k;
-        raw[k] = c <= rs.c1 ? ldg16(S + c * N) : make_uint4(0, 0, 0, 0);
+        const int pc = lane + 32 * k;
+        raw[k] = pc < rw.npieces ? ldg16(src + pc) : make_uint4(0, 0, 0, 0);
     }
     float m = -INFINITY;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
+        const int x0 = (lane + 32 * k) * N;
         float x[N];
         unpack<T>(raw[k], x);
-        const long long t0 = (rs.c0 + lane + 32 * k) * N - rs.e0;
+        if (all_valid(x0, N, rw)) {
 #pragma unroll
-        for (int u = 0; u < N; ++u)
-            if (t0 + u >= rs.t_lo && t0 + u <= rs.t_hi) m = fmaxf(m, x[u]);
+            for (int u = 0; u < N; ++u) m = fmaxf(m, x[u]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < N; ++u)
+                if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) m = fmaxf(m, x[u]);
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -212,13 +152,14 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_band_softmax_reg(const S
     float e[kKeep ? NCH * N : 1];
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
+        const int x0 = (lane + 32 * k) * N;
         float x[N];
         unpack<T>(raw[k], x);
-        const long long t0 = (rs.c0 + lane + 32 * k) * N - rs.e0;
+        const bool full = all_valid(x0, N, rw);
 #pragma unroll
         for (int u = 0; u < N; ++u) {
-            const bool v = t0 + u >= rs.t_lo && t0 + u <= rs.t_hi;
-            const float ev = v ? exp2f(fmaf(x[u], kLog2e, -mb)) : 0.f;
+            const bool v = full || (x0 + u >= rw.xlo && x0 + u <= rw.xhi);
+            const float ev = v ? ex2(fmaf(x[u], kLog2e, -mb)) : 0.f;
             z += ev;
             if constexpr (kKeep) e[k * N + u] = ev;
         }
@@ -226,11 +167,12 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_band_softmax_reg(const S
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     const float inv = 1.f / z;
-    T *P = reinterpret_cast<T *>(p.P);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
-        const long long c = rs.c0 + lane + 32 * k;
-        if (c > rs.c1) break;
+        const int pc = lane + 32 * k;
+        if (pc >= rw.npieces) break;
+        const int x0 = pc * N;
         float y[N];
         if constexpr (kKeep) {
 #pragma unroll
@@ -238,63 +180,163 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_band_softmax_reg(const S
         } else {
             float x[N];
             unpack<T>(raw[k], x);
-            const long long t0 = c * N - rs.e0;
+            const bool full = all_valid(x0, N, rw);
 #pragma unroll
             for (int u = 0; u < N; ++u) {
-                const bool v = t0 + u >= rs.t_lo && t0 + u <= rs.t_hi;
-                y[u] = v ? exp2f(fmaf(x[u], kLog2e, -mb)) * inv : 0.f;
+                const bool v = full || (x0 + u >= rw.xlo && x0 + u <= rw.xhi);
+                y[u] = v ? ex2(fmaf(x[u], kLog2e, -mb)) * inv : 0.f;
             }
         }
-        store_piece<T>(P, c, rs, g.D, y);
+        store_piece<T>(dst, pc, rw, y);
     }
     if (p.lse && lane == 0) p.lse[R] = m + logf(z);
 }
 
 template <typename T, int NCH>
-__global__ void __launch_bounds__(kRowsPerBlock * 32) k_band_softmax_bwd_reg(const SoftmaxArgs p) {
+__global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const SoftmaxArgs p) {
     constexpr int N = Vec<T>::N;
     const Geom &g = p.g;
     const int lane = threadIdx.x & 31;
-    const long long R = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (R >= (long long)g.BH * g.n) return;
-    const RowSpan rs = row_span(g, R, N);
-    const T *P = reinterpret_cast<const T *>(p.S);
-    const T *dP = reinterpret_cast<const T *>(p.S2);
+    const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (R >= g.BH * g.n) return;
+    const Row rw = make_row<T>(g, R);
+    const uint4 *sp = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
+    const uint4 *sd = reinterpret_cast<const uint4 *>(p.S2) + rw.piece0;
     uint4 rp[NCH], rd[NCH];
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
-        const long long c = rs.c0 + lane + 32 * k;
-        rp[k] = c <= rs.c1 ? ldg16(P + c * N) : make_uint4(0, 0, 0, 0);
-        rd[k] = c <= rs.c1 ? ldg16(dP + c * N) : make_uint4(0, 0, 0, 0);
+        const int pc = lane + 32 * k;
+        const bool in = pc < rw.npieces;
+        rp[k] = in ? ldg16(sp + pc) : make_uint4(0, 0, 0, 0);
+        rd[k] = in ? ldg16(sd + pc) : make_uint4(0, 0, 0, 0);
     }
     float delta = 0.f;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
+        const int x0 = (lane + 32 * k) * N;
         float x[N], y[N];
         unpack<T>(rp[k], x);
         unpack<T>(rd[k], y);
-        const long long t0 = (rs.c0 + lane + 32 * k) * N - rs.e0;
+        if (all_valid(x0, N, rw)) {
 #pragma unroll
-        for (int u = 0; u < N; ++u)
-            if (t0 + u >= rs.t_lo && t0 + u <= rs.t_hi) delta = fmaf(x[u], y[u], delta);
+            for (int u = 0; u < N; ++u) delta = fmaf(x[u], y[u], delta);
+        } else {
+#pragma unroll
+            for (int u = 0; u < N; ++u)
+                if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) delta = fmaf(x[u], y[u], delta);
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
-    T *dS = reinterpret_cast<T *>(p.P);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
-        const long long c = rs.c0 + lane + 32 * k;
-        if (c > rs.c1) break;
+        const int pc = lane + 32 * k;
+        if (pc >= rw.npieces) break;
+        const int x0 = pc * N;
         float x[N], y[N];
         unpack<T>(rp[k], x);
         unpack<T>(rd[k], y);
-        const long long t0 = c * N - rs.e0;
+        const bool full = all_valid(x0, N, rw);
 #pragma unroll
         for (int u = 0; u < N; ++u) {
-            const bool v = t0 + u >= rs.t_lo && t0 + u <= rs.t_hi;
+            const bool v = full || (x0 + u >= rw.xlo && x0 + u <= rw.xhi);
             x[u] = v ? x[u] * (y[u] - delta) : 0.f;
         }
-        store_piece<T>(dS, c, rs, g.D, x);
+        store_piece<T>(dst, pc, rw, x);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// streaming rows (longer than the register path holds): two reads
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const SoftmaxArgs p) {
+    constexpr int N = Vec<T>::N;
+    const Geom &g = p.g;
+    const int lane = threadIdx.x & 31;
+    const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (R >= g.BH * g.n) return;
+    const Row rw = make_row<T>(g, R);
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
+    // pass 1: per-lane running max (log2 units) and sum, one rescale per piece
+    float m = -INFINITY, z = 0.f;
+    for (int pc = lane; pc < rw.npieces; pc += 32) {
+        float x[N];
+        unpack<T>(ldg16(src + pc), x);
+        const int x0 = pc * N;
+        float pm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            x[u] *= kLog2e;
+            if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) pm = fmaxf(pm, x[u]);
+        }
+        if (pm == -INFINITY) continue;
+        const float mn = fmaxf(m, pm);
+        z = (m == -INFINITY) ? 0.f : z * ex2(m - mn);
+#pragma unroll
+        for (int u = 0; u < N; ++u)
+            if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) z += ex2(x[u] - mn);
+        m = mn;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
+        const float mn = fmaxf(m, m2);
+        z = (m == -INFINITY ? 0.f : z * ex2(m - mn)) + (m2 == -INFINITY ? 0.f : z2 * ex2(m2 - mn));
+        m = mn;
+    }
+    const float inv = 1.f / z;
+    uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
+    for (int pc = lane; pc < rw.npieces; pc += 32) {
+        float x[N];
+        unpack<T>(ldg16(src + pc), x);
+        const int x0 = pc * N;
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            const bool v = x0 + u >= rw.xlo && x0 + u <= rw.xhi;
+            x[u] = v ? ex2(fmaf(x[u], kLog2e, -m)) * inv : 0.f;
+        }
+        store_piece<T>(dst, pc, rw, x);
+    }
+    if (p.lse && lane == 0) p.lse[R] = m / kLog2e + logf(z);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const SoftmaxArgs p) {
+    constexpr int N = Vec<T>::N;
+    const Geom &g = p.g;
+    const int lane = threadIdx.x & 31;
+    const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (R >= g.BH * g.n) return;
+    const Row rw = make_row<T>(g, R);
+    const uint4 *sp = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
+    const uint4 *sd = reinterpret_cast<const uint4 *>(p.S2) + rw.piece0;
+    float delta = 0.f;
+    for (int pc = lane; pc < rw.npieces; pc += 32) {
+        float x[N], y[N];
+        unpack<T>(ldg16(sp + pc), x);
+        unpack<T>(ldg16(sd + pc), y);
+        const int x0 = pc * N;
+#pragma unroll
+        for (int u = 0; u < N; ++u)
+            if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) delta = fmaf(x[u], y[u], delta);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
+    for (int pc = lane; pc < rw.npieces; pc += 32) {
+        float x[N], y[N];
+        unpack<T>(ldg16(sp + pc), x);
+        unpack<T>(ldg16(sd + pc), y);
+        const int x0 = pc * N;
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            const bool v = x0 + u >= rw.xlo && x0 + u <= rw.xhi;
+            x[u] = v ? x[u] * (y[u] - delta) : 0.f;
+        }
+        store_piece<T>(dst, pc, rw, x);
     }
 }
 
@@ -304,24 +346,23 @@ cudaError_t launch_sm(const SoftmaxArgs &a, bool bwd, cudaStream_t st) {
     const long long rows = (long long)a.g.BH * a.g.n;
     const unsigned blocks = (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock);
     const dim3 blk(kRowsPerBlock * 32);
-    // most aligned pieces a row can touch, spread over 32 lanes
-    const long long pieces = (a.g.D + N - 1) / N + 1;
+    const long long pieces = (a.g.D + N - 1) / N + 1;  // most pieces a row touches
     const long long per_lane = (pieces + 31) / 32;
     if (bwd) {
-        if (per_lane <= 1) k_band_softmax_bwd_reg<T, 1><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 2) k_band_softmax_bwd_reg<T, 2><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 3) k_band_softmax_bwd_reg<T, 3><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 4) k_band_softmax_bwd_reg<T, 4><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 8) k_band_softmax_bwd_reg<T, 8><<<blocks, blk, 0, st>>>(a);
-        else k_band_softmax_bwd_stream<T><<<blocks, blk, 0, st>>>(a);
+        if (per_lane <= 1) k_softmax_bwd_reg<T, 1><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 2) k_softmax_bwd_reg<T, 2><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 3) k_softmax_bwd_reg<T, 3><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 4) k_softmax_bwd_reg<T, 4><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 8) k_softmax_bwd_reg<T, 8><<<blocks, blk, 0, st>>>(a);
+        else k_softmax_bwd_stream<T><<<blocks, blk, 0, st>>>(a);
     } else {
-        if (per_lane <= 1) k_band_softmax_reg<T, 1><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 2) k_band_softmax_reg<T, 2><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 3) k_band_softmax_reg<T, 3><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 4) k_band_softmax_reg<T, 4><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 8) k_band_softmax_reg<T, 8><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 17) k_band_softmax_reg<T, 17><<<blocks, blk, 0, st>>>(a);
-        else k_band_softmax_stream<T><<<blocks, blk, 0, st>>>(a);
+        if (per_lane <= 1) k_softmax_reg<T, 1><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 2) k_softmax_reg<T, 2><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 3) k_softmax_reg<T, 3><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 4) k_softmax_reg<T, 4><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 8) k_softmax_reg<T, 8><<<blocks, blk, 0, st>>>(a);
+        else if (per_lane <= 17) k_softmax_reg<T, 17><<<blocks, blk, 0, st>>>(a);
+        else k_softmax_stream<T><<<blocks, blk, 0, st>>>(a);
     }
     return cudaGetLastError();
 }
