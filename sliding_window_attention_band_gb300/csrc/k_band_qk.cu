@@ -7,12 +7,23 @@
 // Tensor-core kernel (f16 / bf16, head_dim 64).  One CTA owns 128 query rows
 // of one residue r (rows r + s*a, a in [a0, a0+128)) and walks the keys its
 // band touches, 128 at a time.  Each step is one dense 128x128x64 product
-// computed with tcgen05.mma into tensor memory, oriented so that the KEY
-// chunk is the M operand: TMEM lane = key, column = query.  An epilogue
-// thread then holds one key against 128 queries, and for a fixed query the
-// 32 lanes of a warp hold 32 consecutive keys = 32 consecutive band slots of
-// that query's row, so every store instruction writes 64 contiguous bytes.
-// Out-of-band entries of the dense tile are simply not stored.
+// computed with tcgen05.mma into tensor memory.  Out-of-band entries of the
+// dense tile are simply not stored.  Two epilogues:
+//
+//  * ROWS (used when s*D - 1 is a multiple of 16, e.g. every undilated band
+//    with D = 2^k + 1): the QUERY tile is the M operand, so TMEM lane = query
+//    row and each thread streams its own band row.  Consecutive chunks hand a
+//    row consecutive slots, and because the row pitch minus one is a
+//    multiple of 16 elements, every row of the CTA has the same offset modulo
+//    32 bytes.  The epilogue is compiled once per offset (16 cases, picked
+//    once per CTA): each 32-value TMEM group becomes two aligned 32-byte
+//    pieces (one st.global.v8 each, a full sector), carrying the leftover
+//    values in registers to the next group or chunk.  Only the two pieces at
+//    the ends of a row's valid range are stored element by element.
+//  * KEYS (any geometry): the KEY chunk is the M operand, TMEM lane = key,
+//    column = query; for a fixed query the 32 lanes of a warp hold 32
+//    consecutive band slots of that query's row, so each store instruction
+//    writes 64 contiguous bytes.
 //
 // Warp roles (192 threads): warp 0 issues TMA loads (query tile once, key
 // chunks into a 4-stage ring), warp 1 owns tensor memory and issues the MMAs
@@ -32,7 +43,115 @@ constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 halves
 constexpr int kSmemBytes = kStages * kTileBytes + kTileBytes + 1024 /*barriers*/ + 1024 /*align*/;
 constexpr uint32_t kTmemCols = 256;
 
+__device__ __forceinline__ void stg_v8(void *ptr, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// Store 16 consecutive values (elements 16*P .. 16*P+15 of `base`, a 32-byte
+// aligned pointer); elements outside [lo, hi] are left untouched.
 template <typename T>
+__device__ __forceinline__ void store_piece16(T *base, long long P, const float (&y)[16],
+                                              long long lo, long long hi) {
+    const long long e0 = P * 16;
+    if (e0 >= lo && e0 + 15 <= hi) {
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = pack2<T>(y[2 * k], y[2 * k + 1]);
+        stg_v8(base + e0, w);
+    } else if (e0 + 15 >= lo && e0 <= hi) {
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (e0 + u >= lo && e0 + u <= hi) base[e0 + u] = Elt<T>::from_f(y[u]);
+    }
+}
+
+struct RowsCtx {
+    uint64_t *tfull, *tempty;
+    volatile int *abort_flag;
+    unsigned *err;
+    uint32_t lane_base;  // TMEM address of this warp's lane quarter, column 0
+    int nck;
+    long long piece0;    // piece of value 0 of chunk 0 (its first DL positions precede it)
+    long long ev_lo, ev_hi;  // valid elements of this thread's row
+    float alpha;
+};
+
+// ROWS epilogue for one thread = one query row; DL = offset of the row's
+// chunk-0 value 0 inside its 16-element piece.
+template <typename T, int DL>
+__device__ __noinline__ void qk_rows_epilogue(const RowsCtx &x, T *base) {
+    float carry[DL > 0 ? DL : 1];
+#pragma unroll
+    for (int i = 0; i < (DL > 0 ? DL : 1); ++i) carry[i] = 0.f;
+    for (int c = 0; c < x.nck; ++c) {
+        const int b = c & 1;
+        const uint32_t bph = (c >> 1) & 1;
+        const bool ok = mbar_wait(&x.tfull[b], bph, x.abort_flag, x.err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+#pragma unroll 1
+        for (int grp = 0; grp < 4; ++grp) {
+            uint32_t v[32];
+            tmem_ld32(x.lane_base + b * kBN + grp * 32, v);
+            tmem_ld_wait();
+            float y[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = x.alpha * __uint_as_float(v[i]);
+            float pa[16], pb[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                if constexpr (DL > 0) pa[q] = q < DL ? carry[q < DL ? q : 0] : y[q - DL];
+                else pa[q] = y[q];
+                pb[q] = y[16 - DL + q];
+            }
+            const long long P = x.piece0 + 8 * c + 2 * grp;
+            store_piece16<T>(base, P, pa, x.ev_lo, x.ev_hi);
+            store_piece16<T>(base, P + 1, pb, x.ev_lo, x.ev_hi);
+            if constexpr (DL > 0) {
+#pragma unroll
+                for (int q = 0; q < DL; ++q) carry[q] = y[32 - DL + q];
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&x.tempty[b]);
+    }
+    if constexpr (DL > 0) {  // the open piece after the last chunk
+        float pa[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) pa[q] = q < DL ? carry[q < DL ? q : 0] : 0.f;
+        const long long P = x.piece0 + 8 * x.nck;
+        const long long e0 = P * 16;
+#pragma unroll
+        for (int u = 0; u < DL; ++u)
+            if (e0 + u >= x.ev_lo && e0 + u <= x.ev_hi) base[e0 + u] = Elt<T>::from_f(pa[u]);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void qk_rows_dispatch(int dl, const RowsCtx &x, T *base) {
+    switch (dl) {
+        case 0: qk_rows_epilogue<T, 0>(x, base); break;
+        case 1: qk_rows_epilogue<T, 1>(x, base); break;
+        case 2: qk_rows_epilogue<T, 2>(x, base); break;
+        case 3: qk_rows_epilogue<T, 3>(x, base); break;
+        case 4: qk_rows_epilogue<T, 4>(x, base); break;
+        case 5: qk_rows_epilogue<T, 5>(x, base); break;
+        case 6: qk_rows_epilogue<T, 6>(x, base); break;
+        case 7: qk_rows_epilogue<T, 7>(x, base); break;
+        case 8: qk_rows_epilogue<T, 8>(x, base); break;
+        case 9: qk_rows_epilogue<T, 9>(x, base); break;
+        case 10: qk_rows_epilogue<T, 10>(x, base); break;
+        case 11: qk_rows_epilogue<T, 11>(x, base); break;
+        case 12: qk_rows_epilogue<T, 12>(x, base); break;
+        case 13: qk_rows_epilogue<T, 13>(x, base); break;
+        case 14: qk_rows_epilogue<T, 14>(x, base); break;
+        default: qk_rows_epilogue<T, 15>(x, base); break;
+    }
+}
+
+template <typename T, bool kRows>
 __global__ void __launch_bounds__(kThreads, 2)
     k_band_qk_tc(const __grid_constant__ TmapSet mapA, const __grid_constant__ TmapSet mapB,
                  const QKArgs p) {
@@ -116,8 +235,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const uint32_t d = tmem + b * kBN;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        mma_f16_ss(d, sdesc_sw128(k_addr + 32 * k, 16, 1024),
-                                   sdesc_sw128(q_addr + 32 * k, 16, 1024), idesc, k > 0);
+                        const uint64_t kd = sdesc_sw128(k_addr + 32 * k, 16, 1024);
+                        const uint64_t qd = sdesc_sw128(q_addr + 32 * k, 16, 1024);
+                        if constexpr (kRows) mma_f16_ss(d, qd, kd, idesc, k > 0);
+                        else mma_f16_ss(d, kd, qd, idesc, k > 0);
                     }
                     mma_commit(&kempty[st]);
                     mma_commit(&tfull[b]);
@@ -127,8 +248,36 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else {
         // epilogue: warps 2..5, TMEM lane quarter = warp % 4
         const int quarter = warp & 3;
-        const int m = quarter * 32 + lane;  // key within the chunk
         T *S = reinterpret_cast<T *>(p.S);
+        if constexpr (kRows) {
+            const int q = quarter * 32 + lane;  // query row of this thread
+            const int qq = a0 + q;
+            // element coordinates relative to a 32-byte aligned base
+            const uintptr_t sa = reinterpret_cast<uintptr_t>(p.S);
+            T *base = reinterpret_cast<T *>(sa & ~static_cast<uintptr_t>(31));
+            const long long eoff = (long long)((sa & 31) / sizeof(T));
+            const long long erow = ((long long)bh * g.n + r + (long long)g.s * qq) * g.D + eoff;
+            const long long e0 = erow + (kb_lo - qq + g.w);  // value 0 of chunk 0
+            RowsCtx x;
+            x.tfull = tfull;
+            x.tempty = tempty;
+            x.abort_flag = abort_flag;
+            x.err = p.err;
+            x.lane_base = tmem_addr(tmem, quarter * 32, 0);
+            x.nck = nck;
+            x.alpha = p.alpha;
+            const int dl = (int)(e0 & 15);  // the same for every row of the CTA
+            x.piece0 = (e0 - dl) / 16;
+            if (qq < nr) {
+                x.ev_lo = erow + max(0, g.w - qq);
+                x.ev_hi = erow + min(g.D - 1, g.w + nr - 1 - qq);
+            } else {
+                x.ev_lo = 1;
+                x.ev_hi = 0;
+            }
+            qk_rows_dispatch<T>(__shfl_sync(0xffffffffu, dl, 0), x, base);
+        } else {
+        const int m = quarter * 32 + lane;  // key within the chunk
         const long long row0 = (long long)bh * g.n + r + (long long)g.s * a0;
         const long long stepq = (long long)g.s * g.D - 1;  // offset change per query
         const float alpha = p.alpha;
@@ -159,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             tc_fence_before();
             mbar_arrive(&tempty[b]);
+        }
         }
         // padding: slots whose key lies outside [0, nr)
         const T pad = Elt<T>::from_f(g.padding);
@@ -208,25 +358,29 @@ __global__ void __launch_bounds__(128) k_band_qk_f32(const DenseArgs p) {
     }
 }
 
+template <typename T, bool kRows>
+cudaError_t launch_qk(const TmapSet &mapA, const TmapSet &mapB, const QKArgs &a, cudaStream_t st) {
+    const int tiles = (a.g.nsub + kBN - 1) / kBN;
+    dim3 grid(tiles, a.g.s, a.g.BH);
+    cudaError_t e = cudaFuncSetAttribute(k_band_qk_tc<T, kRows>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k_band_qk_tc<T, kRows><<<grid, kThreads, kSmemBytes, st>>>(mapA, mapB, a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_band_qk_tc(DType dt, const TmapSet &mapA, const TmapSet &mapB,
                               const QKArgs &a, cudaStream_t st) {
-    const int tiles = (a.g.nsub + kBN - 1) / kBN;
-    dim3 grid(tiles, a.g.s, a.g.BH);
-    cudaError_t e;
-    if (dt == kF16) {
-        e = cudaFuncSetAttribute(k_band_qk_tc<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
-        if (e != cudaSuccess) return e;
-        k_band_qk_tc<__half><<<grid, kThreads, kSmemBytes, st>>>(mapA, mapB, a);
-    } else {
-        e = cudaFuncSetAttribute(k_band_qk_tc<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        k_band_qk_tc<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(mapA, mapB, a);
-    }
-    return cudaGetLastError();
+    // the row-streaming epilogue needs every row of a CTA at the same offset
+    // modulo 16 elements: (s*D - 1) % 16 == 0
+    const bool rows = ((long long)a.g.s * a.g.D - 1) % 16 == 0;
+    if (dt == kF16)
+        return rows ? launch_qk<__half, true>(mapA, mapB, a, st)
+                    : launch_qk<__half, false>(mapA, mapB, a, st);
+    return rows ? launch_qk<__nv_bfloat16, true>(mapA, mapB, a, st)
+                : launch_qk<__nv_bfloat16, false>(mapA, mapB, a, st);
 }
 
 cudaError_t launch_band_qk_f32(const DenseArgs &a, cudaStream_t st) {
