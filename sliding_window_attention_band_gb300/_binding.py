@@ -157,10 +157,17 @@ def _stream(stream, like):
     return ctypes.c_void_p(int(stream))
 
 
-def _glob(g):
+def _glob(g, desc=None, name="glob"):
+    """(cols [BH, n, G], rows [BH, G, n]) -> swab_glob*, or None."""
     if g is None:
         return None
     cols, rows = g
+    if desc is not None:
+        _check_shape(f"{name}.cols", cols, (desc.BH, desc.n, desc.G), desc.dtype)
+        _check_shape(f"{name}.rows", rows, (desc.BH, desc.G, desc.n), desc.dtype)
+    for t in (cols, rows):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
     return ctypes.byref(_Glob(cols.data_ptr() if cols is not None else None,
                               rows.data_ptr() if rows is not None else None))
 
@@ -202,7 +209,8 @@ def band_qk(desc: Desc, alpha, A, B, S, Sg=None, stream=None):
     """S = alpha * A.B^T on the band (padding outside the sequence)."""
     for n_, t, sh in (("A", A, _dense(desc)), ("B", B, _dense(desc)), ("S", S, _band(desc))):
         _check_shape(n_, t, sh, desc.dtype)
-    _call("band_qk", ctypes.byref(desc.c), float(alpha), _ptr(A), _ptr(B), _ptr(S), _glob(Sg),
+    _call("band_qk", ctypes.byref(desc.c), float(alpha), _ptr(A), _ptr(B), _ptr(S),
+          _glob(Sg, desc, "Sg"),
           _stream(stream, S))
 
 
@@ -211,7 +219,8 @@ def band_softmax(desc: Desc, S, P, lse=None, Sg=None, Pg=None, stream=None):
     _check_shape("S", S, _band(desc), desc.dtype)
     _check_shape("P", P, _band(desc), desc.dtype)
     _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
-    _call("band_softmax", ctypes.byref(desc.c), _ptr(S), _glob(Sg), _ptr(P), _glob(Pg),
+    _call("band_softmax", ctypes.byref(desc.c), _ptr(S), _glob(Sg, desc, "Sg"), _ptr(P),
+          _glob(Pg, desc, "Pg"),
           _ptr(lse), _stream(stream, P))
 
 
@@ -220,7 +229,8 @@ def band_pv(desc: Desc, alpha, P, V, O, Pg=None, stream=None):
     _check_shape("P", P, _band(desc), desc.dtype)
     _check_shape("V", V, _dense(desc), desc.dtype)
     _check_shape("O", O, _dense(desc), desc.dtype)
-    _call("band_pv", ctypes.byref(desc.c), float(alpha), _ptr(P), _glob(Pg), _ptr(V), _ptr(O),
+    _call("band_pv", ctypes.byref(desc.c), float(alpha), _ptr(P), _glob(Pg, desc, "Pg"),
+          _ptr(V), _ptr(O),
           _stream(stream, O))
 
 
@@ -229,7 +239,8 @@ def band_qk_bwd_t(desc: Desc, alpha, dS, Q, dK, dSg=None, stream=None):
     _check_shape("dS", dS, _band(desc), desc.dtype)
     _check_shape("Q", Q, _dense(desc), desc.dtype)
     _check_shape("dK", dK, _dense(desc), desc.dtype)
-    _call("band_qk_bwd_t", ctypes.byref(desc.c), float(alpha), _ptr(dS), _glob(dSg), _ptr(Q),
+    _call("band_qk_bwd_t", ctypes.byref(desc.c), float(alpha), _ptr(dS),
+          _glob(dSg, desc, "dSg"), _ptr(Q),
           _ptr(dK), _stream(stream, dK))
 
 
@@ -238,7 +249,8 @@ def band_pv_bwd_t(desc: Desc, alpha, P, dO, dV, Pg=None, stream=None):
     _check_shape("P", P, _band(desc), desc.dtype)
     _check_shape("dO", dO, _dense(desc), desc.dtype)
     _check_shape("dV", dV, _dense(desc), desc.dtype)
-    _call("band_pv_bwd_t", ctypes.byref(desc.c), float(alpha), _ptr(P), _glob(Pg), _ptr(dO),
+    _call("band_pv_bwd_t", ctypes.byref(desc.c), float(alpha), _ptr(P),
+          _glob(Pg, desc, "Pg"), _ptr(dO),
           _ptr(dV), _stream(stream, dV))
 
 
@@ -246,8 +258,8 @@ def band_softmax_bwd(desc: Desc, P, dP, dS, Pg=None, dPg=None, dSg=None, stream=
     """dS = P * (dP - rowsum(P * dP)) on the used slots."""
     for n_, t in (("P", P), ("dP", dP), ("dS", dS)):
         _check_shape(n_, t, _band(desc), desc.dtype)
-    _call("band_softmax_bwd", ctypes.byref(desc.c), _ptr(P), _glob(Pg), _ptr(dP), _glob(dPg),
-          _ptr(dS), _glob(dSg), _stream(stream, dS))
+    _call("band_softmax_bwd", ctypes.byref(desc.c), _ptr(P), _glob(Pg, desc, "Pg"), _ptr(dP),
+          _glob(dPg, desc, "dPg"), _ptr(dS), _glob(dSg, desc, "dSg"), _stream(stream, dS))
 
 
 def band_attention(desc: Desc, scale, Q, K, V, O, lse=None, stream=None):

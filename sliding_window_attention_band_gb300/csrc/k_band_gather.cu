@@ -86,7 +86,7 @@ __device__ __forceinline__ uint4 mask_elems(uint4 v, int lo, int hi) {
     return make_uint4(v.x & m[0], v.y & m[1], v.z & m[2], v.w & m[3]);
 }
 
-template <typename T, bool kTrans>
+template <typename T, bool kTrans, bool kGlob>
 __global__ void __launch_bounds__(kThreads, 2)
     k_band_gather_tc(const __grid_constant__ TmapSet mapB, const GatherArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *accfull = bars + 3 * kStages;  // [1]
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(accfull + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    // global tokens: a bitmap of the global positions and their dense rows
+    uint32_t *gbits = reinterpret_cast<uint32_t *>(base + kStages * (kATile + kBTile) + 1024);
+    float *gyrows = reinterpret_cast<float *>(gbits + (kGlob ? ((p.g.n + 31) >> 5) : 0));
 
     const Geom &g = p.g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,6 +111,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int nr = residue_len(g.n, g.s, r);
     const int a0 = blockIdx.x * kBM;
     if (a0 >= nr) return;
+    auto is_global = [&](long long j) -> bool {
+        return kGlob && ((gbits[j >> 5] >> (j & 31)) & 1u);
+    };
     // K range: keys for band_pv, queries for band_t
     const int k_lo = kTrans ? max(a0 - g.wu, 0) : max(a0 - g.w, 0);
     const int k_hi = kTrans ? min(a0 + kBM - 1 + g.w, nr - 1) : min(a0 + kBM - 1 + g.wu, nr - 1);
@@ -126,6 +132,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 1) {
         tmem_alloc(tmem_holder, kTmemCols);
         tmem_relinquish();
+    }
+    if constexpr (kGlob) {
+        const int words = (g.n + 31) >> 5;
+        for (int k = threadIdx.x; k < words; k += blockDim.x) gbits[k] = 0u;
+        __syncthreads();
+        for (int k = threadIdx.x; k < p.gl.G; k += blockDim.x)
+            atomicOr(&gbits[p.gl.idx[k] >> 5], 1u << (p.gl.idx[k] & 31));
+        const T *ysrc = reinterpret_cast<const T *>(p.gy) + (long long)bh * g.n * 64;
+        for (int e = threadIdx.x; e < p.gl.G * 64; e += blockDim.x)
+            gyrows[e] = Elt<T>::to_f(ysrc[(long long)p.gl.idx[e >> 6] * 64 + (e & 63)]);
     }
     tc_fence_before();
     __syncthreads();
@@ -190,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         int vcap[kTasks];          // valid elements end at min(vlo + D, vcap - stage*64) (pv) / vcap (t)
         int shift[kTasks];
         int qline[kTasks];         // band_t: query sub-index of the lane's line at stage 0
+        int kkey[kTasks];          // key sub-index of the lane's first element at stage 0
         uint32_t dst[kTasks];      // byte offset inside the A stage
         long long e_step;          // e_line increment per stage
 #pragma unroll
@@ -205,8 +222,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 shift[u] = (int)(el & 7);
                 e_line[u] = el + 8 * j;
                 vlo[u] = qq - g.w - k_lo - 8 * j;
-                vcap[u] = qq < nr ? (k_hi - k_lo + 1 - 8 * j) : -(1 << 30);
+                vcap[u] = (qq < nr && !is_global(r + (long long)g.s * qq)) ? (k_hi - k_lo + 1 - 8 * j)
+                                                                          : -(1 << 30);
                 qline[u] = 0;
+                kkey[u] = k_lo + 8 * j;
                 dst[u] = line * 128 + ((j ^ (line & 7)) << 4);
             } else {
                 // 64 lines (queries) x 128 keys: 2 lines per task, 16 pieces each
@@ -219,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 vlo[u] = qq - g.w - a0 - 8 * j;
                 vcap[u] = nr - a0 - 8 * j;
                 qline[u] = qq;
+                kkey[u] = a0 + 8 * j;
                 dst[u] = (j >> 3) * (kKC * 128) + line * 128 + (((j & 7) ^ (line & 7)) << 4);
             }
         }
@@ -238,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     h0 = min(l0 + g.D, vcap[u] - kKC * c);
                 } else {
                     l0 = vlo[u] + kKC * c;
-                    h0 = (qline[u] + kKC * c < nr) ? min(l0 + g.D, vcap[u]) : l0;
+                    const int qq = qline[u] + kKC * c;
+                    h0 = (qq < nr && !is_global(r + (long long)g.s * qq)) ? min(l0 + g.D, vcap[u]) : l0;
                 }
                 plo[u] = max(l0, 0);
                 phi[u] = min(h0, 8);
@@ -259,6 +280,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (plo[u] < phi[u]) {
                     v = extract_elems(lo[u], hi[u], shift[u]);
                     if (plo[u] > 0 || phi[u] < 8) v = mask_elems(v, plo[u], phi[u]);
+                    if constexpr (kGlob) {
+                        // keys of this piece that are global are not band keys
+                        const long long k0 = r + (long long)g.s * (kkey[u] + (kTrans ? 0 : kKC * c));
+                        const long long k7 = k0 + 7LL * g.s;
+                        if (k7 >= p.gl.idx[0] && k0 <= p.gl.idx[p.gl.G - 1]) {
+                            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (is_global(k0 + (long long)e * g.s))
+                                    w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
+                            v = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
                 }
                 sts16(a_addr + dst[u], v);
             }
@@ -277,6 +311,30 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_ld32(tmem_addr(tmem, quarter * 32, half * 32), v);
             tmem_ld_wait();
             const int row = a0 + m;
+            if (kGlob && row < nr) {
+                // band_pv: + sum_g cols[i,g] V[G[g]] for a local query row i;
+                // band_t:  + sum_g rows[g,j] Y[G[g]] for key j.
+                const long long ri = r + (long long)g.s * row;  // row index in the slice
+                if (!kTrans && is_global(ri)) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                } else {
+                    const T *gw = reinterpret_cast<const T *>(p.gw);
+                    float acc[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]);
+                    for (int q = 0; q < p.gl.G; ++q) {
+                        const float wv = kTrans
+                            ? Elt<T>::to_f(gw[((long long)bh * p.gl.G + q) * g.n + ri])
+                            : Elt<T>::to_f(gw[((long long)bh * g.n + ri) * p.gl.G + q]);
+                        const float *yr = gyrows + q * 64 + half * 32;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[i] = fmaf(wv, yr[i], acc[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[i]);
+                }
+            }
             if (row < nr) {
                 T *out = reinterpret_cast<T *>(p.out) +
                          ((long long)bh * g.n + r + (long long)g.s * row) * 64 + half * 32;
@@ -345,27 +403,40 @@ __global__ void __launch_bounds__(128) k_band_t_f32(const DenseArgs p) {
     reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
 }
 
-template <typename T, bool kTrans>
+template <typename T, bool kTrans, bool kGlob>
 cudaError_t launch_gather(const TmapSet &mapB, const GatherArgs &a, cudaStream_t st) {
     const int tiles = (a.g.nsub + kBM - 1) / kBM;
     dim3 grid(tiles, a.g.s, a.g.BH);
-    cudaError_t e = cudaFuncSetAttribute(k_band_gather_tc<T, kTrans>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const size_t smem = kSmemBytes + (kGlob ? gather_glob_smem(a.g.n, a.gl.G) : 0);
+    cudaError_t e = cudaFuncSetAttribute(k_band_gather_tc<T, kTrans, kGlob>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_band_gather_tc<T, kTrans><<<grid, kThreads, kSmemBytes, st>>>(mapB, a);
+    k_band_gather_tc<T, kTrans, kGlob><<<grid, kThreads, smem, st>>>(mapB, a);
     return cudaGetLastError();
+}
+
+template <typename T, bool kTrans>
+cudaError_t launch_gather2(const TmapSet &mapB, const GatherArgs &a, cudaStream_t st) {
+    return a.gl.G > 0 ? launch_gather<T, kTrans, true>(mapB, a, st)
+                      : launch_gather<T, kTrans, false>(mapB, a, st);
 }
 
 }  // namespace
 
+size_t gather_glob_smem(int n, int G) {
+    return (size_t)((n + 31) / 32) * 4 + (size_t)G * 64 * sizeof(float);
+}
+
+size_t gather_smem_bytes(int n, int G) { return kSmemBytes + (G > 0 ? gather_glob_smem(n, G) : 0); }
+
 cudaError_t launch_band_gather_tc(DType dt, bool transposed, const TmapSet &mapB,
                                   const GatherArgs &a, cudaStream_t st) {
     if (dt == kF16) {
-        return transposed ? launch_gather<__half, true>(mapB, a, st)
-                          : launch_gather<__half, false>(mapB, a, st);
+        return transposed ? launch_gather2<__half, true>(mapB, a, st)
+                          : launch_gather2<__half, false>(mapB, a, st);
     }
-    return transposed ? launch_gather<__nv_bfloat16, true>(mapB, a, st)
-                      : launch_gather<__nv_bfloat16, false>(mapB, a, st);
+    return transposed ? launch_gather2<__nv_bfloat16, true>(mapB, a, st)
+                      : launch_gather2<__nv_bfloat16, false>(mapB, a, st);
 }
 
 cudaError_t launch_band_pv_f32(const DenseArgs &a, cudaStream_t st) {

@@ -1,0 +1,486 @@
+// k_global.cu -- global tokens ("[WIP] Improve LongformerAttention
+// performance", ONNX Runtime issue, item (1): one global index shared by every
+// sequence of the batch).
+//
+// G sorted positions.  A query row i not in G attends to its band keys that
+// are not in G plus all of G; a global query attends to every key.  The dense
+// pieces live in companion tensors:
+//   cols [BH, n, G]: every row's value at the G global keys,
+//   rows [BH, G, n]: the dense rows of the G global queries.
+// Every product here has G (a handful of tokens) as one of its dimensions and
+// costs G*n*64 multiply-adds per slice, a few percent of the banded products;
+// they run on FFMA with operands staged in shared memory.
+#include "swab_internal.h"
+
+namespace swab {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 64;       // rows per tile
+constexpr int kPad = 65;        // smem row stride (floats): conflict-free column access
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename T> __device__ __forceinline__ float ld(const T *p) { return Elt<T>::to_f(*p); }
+
+// rows [row0, row0 + 64) of a [n, 64] slice into smem as fp32 (zero past n)
+template <typename T>
+__device__ __forceinline__ void load_tile(float *dst, const T *slice, int row0, int n) {
+    for (int e = threadIdx.x; e < kTile * 64; e += blockDim.x) {
+        const int rr = e >> 6, c = e & 63;
+        const int row = row0 + rr;
+        dst[rr * kPad + c] = row < n ? ld(slice + (long long)row * 64 + c) : 0.f;
+    }
+}
+
+// the G global rows of a [n, 64] slice into smem as fp32
+template <typename T>
+__device__ __forceinline__ void load_global_rows(float *dst, const T *slice, const GlobArgs &gl) {
+    for (int e = threadIdx.x; e < gl.G * 64; e += blockDim.x) {
+        const int gg = e >> 6, c = e & 63;
+        dst[gg * kPad + c] = ld(slice + (long long)gl.idx[gg] * 64 + c);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dense score pieces of band_qk:
+//   cols[i, g] = alpha * A[i] . B[G[g]],   rows[g, j] = alpha * A[G[g]] . B[j]
+// One CTA per (64-row tile, slice).  head_dim 64 for every dtype here.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_glob_scores(const GlobScoreArgs p) {
+    extern __shared__ float sm[];
+    const GlobArgs &gl = p.gl;
+    const int n = p.g.n, G = gl.G;
+    const int bh = blockIdx.y, i0 = blockIdx.x * kTile;
+    float *a_t = sm;                        // A tile
+    float *b_t = a_t + kTile * kPad;        // B tile
+    float *a_g = b_t + kTile * kPad;        // A[G]
+    float *b_g = a_g + G * kPad;            // B[G]
+    const T *A = reinterpret_cast<const T *>(p.A) + (long long)bh * n * 64;
+    const T *B = reinterpret_cast<const T *>(p.B) + (long long)bh * n * 64;
+    load_tile(a_t, A, i0, n);
+    load_tile(b_t, B, i0, n);
+    load_global_rows(a_g, A, gl);
+    load_global_rows(b_g, B, gl);
+    __syncthreads();
+    T *cols = reinterpret_cast<T *>(p.cols) + (long long)bh * n * G;
+    T *rows = reinterpret_cast<T *>(p.rows) + (long long)bh * G * n;
+    for (int o = threadIdx.x; o < kTile * G; o += blockDim.x) {
+        const int g = o % G, ii = o / G;
+        if (i0 + ii >= n) continue;
+        const float *x = a_t + ii * kPad, *y = b_g + g * kPad;
+        float acc = 0.f;
+#pragma unroll 16
+        for (int c = 0; c < 64; ++c) acc = fmaf(x[c], y[c], acc);
+        cols[(long long)(i0 + ii) * G + g] = Elt<T>::from_f(p.alpha * acc);
+    }
+    for (int o = threadIdx.x; o < kTile * G; o += blockDim.x) {
+        const int jj = o % kTile, g = o / kTile;
+        if (i0 + jj >= n) continue;
+        const float *x = a_g + g * kPad, *y = b_t + jj * kPad;
+        float acc = 0.f;
+#pragma unroll 16
+        for (int c = 0; c < 64; ++c) acc = fmaf(x[c], y[c], acc);
+        rows[(long long)g * n + i0 + jj] = Elt<T>::from_f(p.alpha * acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Bitmap of the global positions in shared memory (n bits).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void build_bitmap(uint32_t *bm, const GlobArgs &gl, int n) {
+    const int words = (n + 31) >> 5;
+    for (int k = threadIdx.x; k < words; k += blockDim.x) bm[k] = 0u;
+    __syncthreads();
+    for (int k = threadIdx.x; k < gl.G; k += blockDim.x)
+        atomicOr(&bm[gl.idx[k] >> 5], 1u << (gl.idx[k] & 31));
+    __syncthreads();
+}
+
+__device__ __forceinline__ bool in_bitmap(const uint32_t *bm, long long j) {
+    return (bm[j >> 5] >> (j & 31)) & 1u;
+}
+
+__device__ __forceinline__ int global_rank(const GlobArgs &gl, int j) {
+    int lo = 0, hi = gl.G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (gl.idx[mid] < j) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------
+// Band softmax with global tokens: one warp per band row.
+//   local row: max / sum over the used band slots (valid, key not global) and
+//              the row's G cols values; P = 0 on unused slots; Pg cols written.
+//   global row: band row and cols row written as zeros (its softmax is the
+//              dense row, done by k_glob_rows_softmax).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_softmax_glob(const SoftmaxGlobArgs p) {
+    extern __shared__ uint32_t bm[];
+    const Geom &g = p.g;
+    const GlobArgs &gl = p.gl;
+    build_bitmap(bm, gl, g.n);
+    const int lane = threadIdx.x & 31;
+    const int rows_total = g.BH * g.n;
+    const int G = gl.G;
+    for (int R = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); R < rows_total;
+         R += gridDim.x * (kThreads / 32)) {
+        const int i = R % g.n;
+        const T *srow = reinterpret_cast<const T *>(p.S) + (long long)R * g.D;
+        T *prow = reinterpret_cast<T *>(p.P) + (long long)R * g.D;
+        const T *sc = reinterpret_cast<const T *>(p.Scols) + (long long)R * G;
+        T *pc = reinterpret_cast<T *>(p.Pcols) + (long long)R * G;
+        if (in_bitmap(bm, i)) {
+            for (int t = lane; t < g.D; t += 32) prow[t] = Elt<T>::from_f(0.f);
+            for (int q = lane; q < G; q += 32) pc[q] = Elt<T>::from_f(0.f);
+            continue;
+        }
+        auto used = [&](int t) {
+            const long long j = (long long)i + (long long)(t - g.w) * g.s;
+            return j >= 0 && j < g.n && !in_bitmap(bm, j);
+        };
+        float m = -INFINITY;
+        for (int t = lane; t < g.D; t += 32)
+            if (used(t)) m = fmaxf(m, ld(srow + t));
+        for (int q = lane; q < G; q += 32) m = fmaxf(m, ld(sc + q));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const float mb = m * kLog2e;
+        float z = 0.f;
+        for (int t = lane; t < g.D; t += 32)
+            if (used(t)) z += ex2(fmaf(ld(srow + t), kLog2e, -mb));
+        for (int q = lane; q < G; q += 32) z += ex2(fmaf(ld(sc + q), kLog2e, -mb));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        const float inv = 1.f / z;
+        for (int t = lane; t < g.D; t += 32)
+            prow[t] = Elt<T>::from_f(used(t) ? ex2(fmaf(ld(srow + t), kLog2e, -mb)) * inv : 0.f);
+        for (int q = lane; q < G; q += 32)
+            pc[q] = Elt<T>::from_f(ex2(fmaf(ld(sc + q), kLog2e, -mb)) * inv);
+        if (p.lse && lane == 0) p.lse[R] = m + logf(z);
+    }
+}
+
+// Dense softmax of the G global query rows: one warp per (slice, g).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_glob_rows_softmax(const SoftmaxGlobArgs p) {
+    const Geom &g = p.g;
+    const GlobArgs &gl = p.gl;
+    const int lane = threadIdx.x & 31;
+    const int W = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (W >= g.BH * gl.G) return;
+    const int bh = W / gl.G, gg = W % gl.G;
+    const T *x = reinterpret_cast<const T *>(p.Srows) + (long long)W * g.n;
+    T *y = reinterpret_cast<T *>(p.Prows) + (long long)W * g.n;
+    float m = -INFINITY;
+    for (int j = lane; j < g.n; j += 32) m = fmaxf(m, ld(x + j));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float mb = m * kLog2e;
+    float z = 0.f;
+    for (int j = lane; j < g.n; j += 32) z += ex2(fmaf(ld(x + j), kLog2e, -mb));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    const float inv = 1.f / z;
+    for (int j = lane; j < g.n; j += 32) y[j] = Elt<T>::from_f(ex2(fmaf(ld(x + j), kLog2e, -mb)) * inv);
+    if (p.lse && lane == 0) p.lse[(long long)bh * g.n + gl.idx[gg]] = m + logf(z);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax backward with global tokens (same row structure as the forward).
+//   local row: delta = sum_used P dP + sum_g Pc dPc;  dS = P (dP - delta) on
+//              used slots, 0 elsewhere;  dSc = Pc (dPc - delta).
+//   global row: band and cols rows written as zeros.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_softmax_bwd_glob(const SoftmaxGlobArgs p) {
+    extern __shared__ uint32_t bm[];
+    const Geom &g = p.g;
+    const GlobArgs &gl = p.gl;
+    build_bitmap(bm, gl, g.n);
+    const int lane = threadIdx.x & 31;
+    const int rows_total = g.BH * g.n;
+    const int G = gl.G;
+    for (int R = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); R < rows_total;
+         R += gridDim.x * (kThreads / 32)) {
+        const int i = R % g.n;
+        const T *P = reinterpret_cast<const T *>(p.S) + (long long)R * g.D;
+        const T *dP = reinterpret_cast<const T *>(p.S2) + (long long)R * g.D;
+        T *dS = reinterpret_cast<T *>(p.P) + (long long)R * g.D;
+        const T *Pc = reinterpret_cast<const T *>(p.Scols) + (long long)R * G;
+        const T *dPc = reinterpret_cast<const T *>(p.S2cols) + (long long)R * G;
+        T *dSc = reinterpret_cast<T *>(p.Pcols) + (long long)R * G;
+        if (in_bitmap(bm, i)) {
+            for (int t = lane; t < g.D; t += 32) dS[t] = Elt<T>::from_f(0.f);
+            for (int q = lane; q < G; q += 32) dSc[q] = Elt<T>::from_f(0.f);
+            continue;
+        }
+        auto used = [&](int t) {
+            const long long j = (long long)i + (long long)(t - g.w) * g.s;
+            return j >= 0 && j < g.n && !in_bitmap(bm, j);
+        };
+        float delta = 0.f;
+        for (int t = lane; t < g.D; t += 32)
+            if (used(t)) delta = fmaf(ld(P + t), ld(dP + t), delta);
+        for (int q = lane; q < G; q += 32) delta = fmaf(ld(Pc + q), ld(dPc + q), delta);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
+        for (int t = lane; t < g.D; t += 32)
+            dS[t] = Elt<T>::from_f(used(t) ? ld(P + t) * (ld(dP + t) - delta) : 0.f);
+        for (int q = lane; q < G; q += 32) dSc[q] = Elt<T>::from_f(ld(Pc + q) * (ld(dPc + q) - delta));
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_glob_rows_softmax_bwd(const SoftmaxGlobArgs p) {
+    const Geom &g = p.g;
+    const GlobArgs &gl = p.gl;
+    const int lane = threadIdx.x & 31;
+    const int W = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (W >= g.BH * gl.G) return;
+    const T *P = reinterpret_cast<const T *>(p.Srows) + (long long)W * g.n;
+    const T *dP = reinterpret_cast<const T *>(p.S2rows) + (long long)W * g.n;
+    T *dS = reinterpret_cast<T *>(p.Prows) + (long long)W * g.n;
+    float delta = 0.f;
+    for (int j = lane; j < g.n; j += 32) delta = fmaf(ld(P + j), ld(dP + j), delta);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
+    for (int j = lane; j < g.n; j += 32) dS[j] = Elt<T>::from_f(ld(P + j) * (ld(dP + j) - delta));
+}
+
+// ---------------------------------------------------------------------------
+// Reductions over the sequence for the G global positions, one CTA per slice:
+//   mode rows (overwrite):  out[G[g]] = alpha * sum_j W[g, j] * Y[j]
+//                           (W = a rows tensor [G, n]; O and dQ of global queries)
+//   mode cols (accumulate): out[G[g]] += alpha * sum_{i not in G} W[i, g] * Y[i]
+//                           (W = a cols tensor [n, G]; dK and dV of global keys)
+// Thread (c = channel, g = gslot + 4k) accumulates G/4 outputs in registers.
+// ---------------------------------------------------------------------------
+template <typename T, bool kCols>
+__global__ void __launch_bounds__(kThreads) k_glob_reduce(const GlobReduceArgs p) {
+    extern __shared__ float sm[];
+    const Geom &g = p.g;
+    const GlobArgs &gl = p.gl;
+    const int n = g.n, G = gl.G;
+    const int bh = blockIdx.x;
+    float *y_t = sm;                  // [64][kPad]
+    float *w_t = y_t + kTile * kPad;  // [64 (g)][kPad] weights for the tile: w_t[g][jj]
+    uint32_t *bm = reinterpret_cast<uint32_t *>(w_t + kTile * kPad);
+    if (kCols) build_bitmap(bm, gl, n);
+    const T *Y = reinterpret_cast<const T *>(p.Y) + (long long)bh * n * 64;
+    const T *Wt = reinterpret_cast<const T *>(p.W);
+    const int c = threadIdx.x & 63, gs = threadIdx.x >> 6;  // gs in [0, 4)
+    for (int gb = 0; gb < G; gb += 64) {  // blocks of 64 global positions
+        const int gn = min(64, G - gb);
+        float acc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+        for (int j0 = 0; j0 < n; j0 += kTile) {
+            __syncthreads();
+            load_tile(y_t, Y, j0, n);
+            for (int e = threadIdx.x; e < gn * kTile; e += blockDim.x) {
+                const int gg = e / kTile, jj = e % kTile;
+                const int j = j0 + jj;
+                float wv = 0.f;
+                if (j < n) {
+                    if (kCols) {
+                        if (!in_bitmap(bm, j)) wv = ld(Wt + ((long long)bh * n + j) * G + gb + gg);
+                    } else {
+                        wv = ld(Wt + ((long long)bh * G + gb + gg) * n + j);
+                    }
+                }
+                w_t[gg * kPad + jj] = wv;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int gg = gs + 4 * k;
+                if (gg < gn) {
+                    const float *wr = w_t + gg * kPad;
+                    float a = acc[k];
+#pragma unroll 8
+                    for (int jj = 0; jj < kTile; ++jj) a = fmaf(wr[jj], y_t[jj * kPad + c], a);
+                    acc[k] = a;
+                }
+            }
+        }
+        T *out = reinterpret_cast<T *>(p.out) + (long long)bh * n * 64;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int gg = gs + 4 * k;
+            if (gg < gn) {
+                T *dst = out + (long long)gl.idx[gb + gg] * 64 + c;
+                const float v = p.alpha * acc[k];
+                *dst = Elt<T>::from_f(kCols ? ld(dst) + v : v);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// exact fp32 band x dense products with global tokens (thread = (row, channel))
+//   pv: local row i: sum over used slots + sum_g cols[i,g] V[G[g]]
+//   t : key j:      sum over used (i,t) with i local + sum_g rows[g,j] Y[G[g]]
+// Global query rows (pv) and global key columns (t) are finished by
+// k_glob_reduce.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) k_band_pv_f32_glob(const DenseGlobArgs p) {
+    extern __shared__ uint32_t bm[];
+    const Geom &g = p.g;
+    build_bitmap(bm, p.gl, g.n);
+    const long long R = blockIdx.x;
+    const int i = (int)(R % g.n);
+    const long long bh = R / g.n;
+    const int c = threadIdx.x;
+    if (c >= g.hd) return;
+    const float *P = reinterpret_cast<const float *>(p.A) + R * g.D;
+    const float *V = reinterpret_cast<const float *>(p.B) + bh * g.n * g.hd;
+    float acc = 0.f;
+    if (!in_bitmap(bm, i)) {
+        for (int t = 0; t < g.D; ++t) {
+            const long long j = (long long)i + (long long)(t - g.w) * g.s;
+            if (j < 0 || j >= g.n || in_bitmap(bm, j)) continue;
+            acc = fmaf(P[t], V[j * g.hd + c], acc);
+        }
+        const float *cols = reinterpret_cast<const float *>(p.cols) + R * p.gl.G;
+        for (int q = 0; q < p.gl.G; ++q) acc = fmaf(cols[q], V[(long long)p.gl.idx[q] * g.hd + c], acc);
+    }
+    reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
+}
+
+__global__ void __launch_bounds__(128) k_band_t_f32_glob(const DenseGlobArgs p) {
+    extern __shared__ uint32_t bm[];
+    const Geom &g = p.g;
+    build_bitmap(bm, p.gl, g.n);
+    const long long R = blockIdx.x;
+    const int j = (int)(R % g.n);
+    const long long bh = R / g.n;
+    const int c = threadIdx.x;
+    if (c >= g.hd) return;
+    const float *Bd = reinterpret_cast<const float *>(p.A) + bh * g.n * g.D;
+    const float *Y = reinterpret_cast<const float *>(p.B) + bh * g.n * g.hd;
+    float acc = 0.f;
+    if (!in_bitmap(bm, j)) {
+        for (int t = 0; t < g.D; ++t) {
+            const long long i = (long long)j - (long long)(t - g.w) * g.s;
+            if (i < 0 || i >= g.n || in_bitmap(bm, i)) continue;
+            acc = fmaf(Bd[i * g.D + t], Y[i * g.hd + c], acc);
+        }
+    }
+    const float *rows = reinterpret_cast<const float *>(p.rows) + bh * p.gl.G * g.n;
+    for (int q = 0; q < p.gl.G; ++q)
+        acc = fmaf(rows[(long long)q * g.n + j], Y[(long long)p.gl.idx[q] * g.hd + c], acc);
+    reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
+}
+
+unsigned grid_rows(long long rows_total) {
+    const long long warps = rows_total;
+    const long long blocks = (warps + (kThreads / 32) - 1) / (kThreads / 32);
+    return (unsigned)(blocks < 4096 ? blocks : 4096);
+}
+
+size_t bitmap_bytes(int n) { return (size_t)((n + 31) / 32) * 4; }
+
+template <typename T>
+cudaError_t launch_scores_t(const GlobScoreArgs &a, cudaStream_t st) {
+    const size_t smem = (size_t)(2 * kTile + 2 * a.gl.G) * kPad * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_glob_scores<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.g.n + kTile - 1) / kTile, a.g.BH);
+    k_glob_scores<T><<<grid, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_softmax_t(const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st) {
+    const size_t smem = bitmap_bytes(a.g.n);
+    const unsigned grid = grid_rows((long long)a.g.BH * a.g.n);
+    if (bwd) {
+        cudaError_t e = cudaFuncSetAttribute(k_softmax_bwd_glob<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k_softmax_bwd_glob<T><<<grid, kThreads, smem, st>>>(a);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(k_softmax_glob<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k_softmax_glob<T><<<grid, kThreads, smem, st>>>(a);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const unsigned rgrid = (unsigned)(((long long)a.g.BH * a.gl.G + (kThreads / 32) - 1) / (kThreads / 32));
+    if (bwd)
+        k_glob_rows_softmax_bwd<T><<<rgrid, kThreads, 0, st>>>(a);
+    else
+        k_glob_rows_softmax<T><<<rgrid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_reduce_t(const GlobReduceArgs &a, bool cols, cudaStream_t st) {
+    const size_t smem = (size_t)2 * kTile * kPad * sizeof(float) + (cols ? bitmap_bytes(a.g.n) : 0);
+    if (cols) {
+        cudaError_t e = cudaFuncSetAttribute(k_glob_reduce<T, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k_glob_reduce<T, true><<<a.g.BH, kThreads, smem, st>>>(a);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(k_glob_reduce<T, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k_glob_reduce<T, false><<<a.g.BH, kThreads, smem, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t glob_bitmap_bytes(int n) { return bitmap_bytes(n); }
+
+cudaError_t launch_glob_scores(DType dt, const GlobScoreArgs &a, cudaStream_t st) {
+    if (dt == kF32) return launch_scores_t<float>(a, st);
+    if (dt == kF16) return launch_scores_t<__half>(a, st);
+    return launch_scores_t<__nv_bfloat16>(a, st);
+}
+
+cudaError_t launch_softmax_glob(DType dt, const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st) {
+    if (dt == kF32) return launch_softmax_t<float>(a, bwd, st);
+    if (dt == kF16) return launch_softmax_t<__half>(a, bwd, st);
+    return launch_softmax_t<__nv_bfloat16>(a, bwd, st);
+}
+
+cudaError_t launch_glob_reduce(DType dt, const GlobReduceArgs &a, bool cols, cudaStream_t st) {
+    if (dt == kF32) return launch_reduce_t<float>(a, cols, st);
+    if (dt == kF16) return launch_reduce_t<__half>(a, cols, st);
+    return launch_reduce_t<__nv_bfloat16>(a, cols, st);
+}
+
+cudaError_t launch_band_f32_glob(const DenseGlobArgs &a, bool transposed, cudaStream_t st) {
+    const long long rows = (long long)a.g.BH * a.g.n;
+    const size_t smem = bitmap_bytes(a.g.n);
+    if (transposed) {
+        cudaError_t e = cudaFuncSetAttribute(k_band_t_f32_glob, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        k_band_t_f32_glob<<<(unsigned)rows, 128, smem, st>>>(a);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(k_band_pv_f32_glob, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        k_band_pv_f32_glob<<<(unsigned)rows, 128, smem, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace swab

@@ -137,30 +137,59 @@ swab_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SWAB_OK : SWAB_
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// globals are accepted by the descriptor check but not yet by these paths
+// Global tokens: companion tensors must be given, head_dim must be 64 and the
+// kernels' shared-memory bitmap (n bits) plus the G dense rows must fit.
+swab_status check_globals(const swab_desc *d, std::initializer_list<const swab_glob *> globs,
+                          GlobArgs *gl) {
+    gl->G = d->n_global;
+    if (d->n_global == 0) return SWAB_OK;
+    if (d->head_dim != 64) return SWAB_ERR_UNSUPPORTED;
+    if (gather_smem_bytes(d->n, d->n_global) > 227 * 1024) return SWAB_ERR_UNSUPPORTED;
+    for (const swab_glob *q : globs) {
+        if (!q || !q->cols || !q->rows) return SWAB_ERR_INVALID_ARG;
+        if (!aligned16(q->cols) || !aligned16(q->rows)) return SWAB_ERR_MISALIGNED;
+    }
+    for (int k = 0; k < d->n_global; ++k) gl->idx[k] = d->global_idx[k];
+    return SWAB_OK;
+}
+
 swab_status check_no_globals(const swab_desc *d) {
     return d->n_global > 0 ? SWAB_ERR_UNSUPPORTED : SWAB_OK;
 }
 
 // The two transposed-product names share this body.
-swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, const void *Y,
-                          void *X, void *stream) {
+swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, const swab_glob *Bg,
+                          const void *Y, void *X, void *stream) {
     Geom g;
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
-    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    GlobArgs gl;
+    if ((s = check_globals(desc, {Bg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({Bd, Y, X})) != SWAB_OK) return s;
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e;
     if (dt == kF32) {
-        DenseArgs a{g, alpha, Bd, Y, X};
-        return from_cuda(launch_band_t_f32(a, as_stream(stream)));
+        if (gl.G > 0) {
+            DenseGlobArgs a{g, gl, alpha, Bd, Y, Bg->cols, Bg->rows, X};
+            e = launch_band_f32_glob(a, true, st);
+        } else {
+            DenseArgs a{g, alpha, Bd, Y, X};
+            e = launch_band_t_f32(a, st);
+        }
+    } else {
+        TmapSet mapY;
+        if (!build_rows_maps(&mapY, Y, g, dt, kGatherBoxRows)) return SWAB_ERR_CUDA;
+        unsigned *err = status_word();
+        if (!err) return SWAB_ERR_CUDA;
+        GatherArgs a{g, alpha, Bd, X, err, gl, gl.G > 0 ? Bg->rows : nullptr, Y};
+        e = launch_band_gather_tc(dt, true, mapY, a, st);
     }
-    TmapSet mapY;
-    if (!build_rows_maps(&mapY, Y, g, dt, kGatherBoxRows)) return SWAB_ERR_CUDA;
-    unsigned *err = status_word();
-    if (!err) return SWAB_ERR_CUDA;
-    GatherArgs a{g, alpha, Bd, X, err};
-    return from_cuda(launch_band_gather_tc(dt, true, mapY, a, as_stream(stream)));
+    if (e == cudaSuccess && gl.G > 0) {
+        GlobReduceArgs r{g, gl, alpha, Bg->cols, Y, X};
+        e = launch_glob_reduce(dt, r, true, st);
+    }
+    return from_cuda(e);
 }
 
 }  // namespace
@@ -199,21 +228,29 @@ SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, 
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
-    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
-    (void)Sg;
+    GlobArgs gl;
+    if ((s = check_globals(desc, {Sg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({A, B, S})) != SWAB_OK) return s;
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e;
     if (dt == kF32) {
         DenseArgs a{g, alpha, A, B, S};
-        return from_cuda(launch_band_qk_f32(a, as_stream(stream)));
+        e = launch_band_qk_f32(a, st);
+    } else {
+        TmapSet mapA, mapB;
+        if (!build_rows_maps(&mapA, A, g, dt, kQKBoxRows) ||
+            !build_rows_maps(&mapB, B, g, dt, kQKBoxRows))
+            return SWAB_ERR_CUDA;
+        unsigned *err = status_word();
+        if (!err) return SWAB_ERR_CUDA;
+        QKArgs a{g, alpha, S, err};
+        e = launch_band_qk_tc(dt, mapA, mapB, a, st);
     }
-    TmapSet mapA, mapB;
-    if (!build_rows_maps(&mapA, A, g, dt, kQKBoxRows) ||
-        !build_rows_maps(&mapB, B, g, dt, kQKBoxRows))
-        return SWAB_ERR_CUDA;
-    unsigned *err = status_word();
-    if (!err) return SWAB_ERR_CUDA;
-    QKArgs a{g, alpha, S, err};
-    return from_cuda(launch_band_qk_tc(dt, mapA, mapB, a, as_stream(stream)));
+    if (e == cudaSuccess && gl.G > 0) {
+        GlobScoreArgs a{g, gl, alpha, A, B, Sg->cols, Sg->rows};
+        e = launch_glob_scores(dt, a, st);
+    }
+    return from_cuda(e);
 }
 
 SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const swab_glob *Sg,
@@ -222,11 +259,15 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
-    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
-    (void)Sg;
-    (void)Pg;
+    GlobArgs gl;
+    if ((s = check_globals(desc, {Sg, Pg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({S, P})) != SWAB_OK) return s;
     if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
+    if (gl.G > 0) {
+        SoftmaxGlobArgs a{g, gl, S, nullptr, Sg->cols, nullptr, Sg->rows, nullptr,
+                          P, Pg->cols, Pg->rows, lse};
+        return from_cuda(launch_softmax_glob(dt, a, false, as_stream(stream)));
+    }
     SoftmaxArgs a{g, S, nullptr, P, lse, nullptr};
     return from_cuda(launch_band_softmax(dt, a, as_stream(stream)));
 }
@@ -237,31 +278,42 @@ SWAB_API swab_status band_pv(const swab_desc *desc, float alpha, const void *P,
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
-    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
-    (void)Pg;
+    GlobArgs gl;
+    if ((s = check_globals(desc, {Pg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({P, V, O})) != SWAB_OK) return s;
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e;
     if (dt == kF32) {
-        DenseArgs a{g, alpha, P, V, O};
-        return from_cuda(launch_band_pv_f32(a, as_stream(stream)));
+        if (gl.G > 0) {
+            DenseGlobArgs a{g, gl, alpha, P, V, Pg->cols, Pg->rows, O};
+            e = launch_band_f32_glob(a, false, st);
+        } else {
+            DenseArgs a{g, alpha, P, V, O};
+            e = launch_band_pv_f32(a, st);
+        }
+    } else {
+        TmapSet mapV;
+        if (!build_rows_maps(&mapV, V, g, dt, kGatherBoxRows)) return SWAB_ERR_CUDA;
+        unsigned *err = status_word();
+        if (!err) return SWAB_ERR_CUDA;
+        GatherArgs a{g, alpha, P, O, err, gl, gl.G > 0 ? Pg->cols : nullptr, V};
+        e = launch_band_gather_tc(dt, false, mapV, a, st);
     }
-    TmapSet mapV;
-    if (!build_rows_maps(&mapV, V, g, dt, kGatherBoxRows)) return SWAB_ERR_CUDA;
-    unsigned *err = status_word();
-    if (!err) return SWAB_ERR_CUDA;
-    GatherArgs a{g, alpha, P, O, err};
-    return from_cuda(launch_band_gather_tc(dt, false, mapV, a, as_stream(stream)));
+    if (e == cudaSuccess && gl.G > 0) {
+        GlobReduceArgs r{g, gl, alpha, Pg->rows, V, O};
+        e = launch_glob_reduce(dt, r, false, st);
+    }
+    return from_cuda(e);
 }
 
 SWAB_API swab_status band_qk_bwd_t(const swab_desc *desc, float alpha, const void *dS,
                                    const swab_glob *dSg, const void *Q, void *dK, void *stream) {
-    (void)dSg;
-    return band_t_common(desc, alpha, dS, Q, dK, stream);
+    return band_t_common(desc, alpha, dS, dSg, Q, dK, stream);
 }
 
 SWAB_API swab_status band_pv_bwd_t(const swab_desc *desc, float alpha, const void *P,
                                    const swab_glob *Pg, const void *dO, void *dV, void *stream) {
-    (void)Pg;
-    return band_t_common(desc, alpha, P, dO, dV, stream);
+    return band_t_common(desc, alpha, P, Pg, dO, dV, stream);
 }
 
 SWAB_API swab_status band_softmax_bwd(const swab_desc *desc, const void *P, const swab_glob *Pg,
@@ -271,11 +323,14 @@ SWAB_API swab_status band_softmax_bwd(const swab_desc *desc, const void *P, cons
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
-    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
-    (void)Pg;
-    (void)dPg;
-    (void)dSg;
+    GlobArgs gl;
+    if ((s = check_globals(desc, {Pg, dPg, dSg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({P, dP, dS})) != SWAB_OK) return s;
+    if (gl.G > 0) {
+        SoftmaxGlobArgs a{g, gl, P, dP, Pg->cols, dPg->cols, Pg->rows, dPg->rows,
+                          dS, dSg->cols, dSg->rows, nullptr};
+        return from_cuda(launch_softmax_glob(dt, a, true, as_stream(stream)));
+    }
     SoftmaxArgs a{g, P, dP, dS, nullptr, nullptr};
     return from_cuda(launch_band_softmax_bwd(dt, a, as_stream(stream)));
 }

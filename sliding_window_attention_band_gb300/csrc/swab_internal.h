@@ -40,6 +40,46 @@ struct GatherArgs {
     const void *band; // band input [BH, n, D]
     void *out;        // dense output [BH, n, 64]
     unsigned *err;
+    // global tokens (gl.G > 0 only)
+    GlobArgs gl;
+    const void *gw;   // band_pv: cols [BH, n, G]; band_t: rows [BH, G, n]
+    const void *gy;   // the dense input whose G global rows enter (V or Y)
+};
+
+struct GlobScoreArgs {  // dense score pieces of band_qk
+    Geom g;
+    GlobArgs gl;
+    float alpha;
+    const void *A, *B;
+    void *cols, *rows;
+};
+
+struct SoftmaxGlobArgs {
+    Geom g;
+    GlobArgs gl;
+    const void *S, *S2;           // band inputs (fwd: S; bwd: P, dP)
+    const void *Scols, *S2cols;   // cols inputs
+    const void *Srows, *S2rows;   // rows inputs
+    void *P, *Pcols, *Prows;      // outputs (fwd: P; bwd: dS)
+    float *lse;
+};
+
+struct GlobReduceArgs {  // sums over the sequence for the G positions
+    Geom g;
+    GlobArgs gl;
+    float alpha;
+    const void *W;    // rows [BH, G, n] or cols [BH, n, G]
+    const void *Y;    // [BH, n, 64]
+    void *out;        // [BH, n, 64]; rows G[g] written / accumulated
+};
+
+struct DenseGlobArgs {  // fp32 band products with global tokens
+    Geom g;
+    GlobArgs gl;
+    float alpha;
+    const void *A, *B;
+    const void *cols, *rows;
+    void *out;
 };
 
 struct SoftmaxArgs {
@@ -80,6 +120,8 @@ cudaError_t launch_band_qk_tc(DType dt, const TmapSet &mapA, const TmapSet &mapB
                               const QKArgs &a, cudaStream_t st);
 cudaError_t launch_band_gather_tc(DType dt, bool transposed, const TmapSet &mapB,
                                   const GatherArgs &a, cudaStream_t st);
+size_t gather_glob_smem(int n, int G);      // extra shared memory with global tokens
+size_t gather_smem_bytes(int n, int G);     // total shared memory of the gather kernel
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                      const TmapSet &mapV, const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st);
@@ -87,6 +129,12 @@ cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st);
 cudaError_t launch_band_qk_f32(const DenseArgs &a, cudaStream_t st);
 cudaError_t launch_band_pv_f32(const DenseArgs &a, cudaStream_t st);
 cudaError_t launch_band_t_f32(const DenseArgs &a, cudaStream_t st);
+// global tokens
+size_t glob_bitmap_bytes(int n);
+cudaError_t launch_glob_scores(DType dt, const GlobScoreArgs &a, cudaStream_t st);
+cudaError_t launch_softmax_glob(DType dt, const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st);
+cudaError_t launch_glob_reduce(DType dt, const GlobReduceArgs &a, bool cols, cudaStream_t st);
+cudaError_t launch_band_f32_glob(const DenseGlobArgs &a, bool transposed, cudaStream_t st);
 // softmax forward / backward (all dtypes)
 cudaError_t launch_band_softmax(DType dt, const SoftmaxArgs &a, cudaStream_t st);
 cudaError_t launch_band_softmax_bwd(DType dt, const SoftmaxArgs &a, cudaStream_t st);

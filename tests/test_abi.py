@@ -173,3 +173,41 @@ def test_binding_raises_swab_error(lib):
         B._call("band_qk", ctypes.byref(d.c), 1.0, ctypes.c_void_p(FAKE),
                 ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), None, None)
     assert ei.value.status_name == "SWAB_ERR_INVALID_ARG"
+
+
+def test_globals_need_companions(lib):
+    """With global tokens every band tensor needs its (cols, rows) companion."""
+    d = desc(n=512, global_idx=[0, 5, 9])
+    P = ctypes.c_void_p
+    assert lib.band_qk(ctypes.byref(d.c), 1.0, P(FAKE), P(FAKE), P(FAKE), None, None) == INVALID
+    half = B._Glob(FAKE, None)
+    assert lib.band_qk(ctypes.byref(d.c), 1.0, P(FAKE), P(FAKE), P(FAKE), ctypes.byref(half),
+                       None) == INVALID
+    mis = B._Glob(FAKE, FAKE + 2)
+    assert lib.band_pv(ctypes.byref(d.c), 1.0, P(FAKE), ctypes.byref(mis), P(FAKE), P(FAKE),
+                       None) == MISALIGNED
+    ok = B._Glob(FAKE, FAKE)
+    assert lib.band_softmax(ctypes.byref(d.c), P(FAKE), ctypes.byref(ok), P(FAKE), None, None,
+                            None) == INVALID
+
+
+def test_globals_need_head_dim_64(lib):
+    d = desc(dtype=torch.float32, head_dim=32, global_idx=[1])
+    ok = B._Glob(FAKE, FAKE)
+    P = ctypes.c_void_p
+    assert lib.band_qk(ctypes.byref(d.c), 1.0, P(FAKE), P(FAKE), P(FAKE), ctypes.byref(ok),
+                       None) == UNSUPPORTED
+
+
+def test_fused_forward_rejects_globals(lib):
+    d = desc(global_idx=[1])
+    P = ctypes.c_void_p
+    assert lib.band_attention(ctypes.byref(d.c), 1.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None,
+                              None) == UNSUPPORTED
+
+
+def test_binding_checks_companion_shapes():
+    d = desc(global_idx=[0, 3])
+    bad = (torch.zeros(2, 256, 3, dtype=torch.float16), torch.zeros(2, 2, 256, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        B._glob(bad, d, "Sg")

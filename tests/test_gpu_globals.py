@@ -1,0 +1,226 @@
+"""GPU parity with global tokens (one global index shared by the batch).
+
+Every input a kernel must ignore is poisoned with NaN: invalid band slots,
+band slots whose key is global, the band and cols rows of global queries.
+Tolerances as in test_gpu_parity.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sliding_window_attention_band_gb300 as swab
+from sliding_window_attention_band_gb300 import build as swab_build
+from sliding_window_attention_band_gb300.inputs import (WORKLOADS, seeded_band, seeded_qkvo,
+                                                        seeded_uniform, workload_inputs)
+
+from test_gpu_parity import (ABS_TOL, dev, empty_band, empty_dense, f64, normwise, score_tol,
+                             valid_mask)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    swab_build.build()
+    swab.load()
+    swab.device_status(reset=True)
+    yield
+    assert swab.device_status(reset=True) == 0
+
+
+CASES = [  # BH, n, w, w_upper, dilation, dtype, global idx
+    (2, 1000, 64, 64, 0, torch.float16, (0, 1, 7, 500, 999)),
+    (3, 777, 100, 37, 2, torch.bfloat16, (3, 20, 21, 400)),
+    (1, 640, 0, 127, 1, torch.float16, tuple(range(16))),
+    (2, 300, 20, 20, 0, torch.float32, (0, 150, 299)),
+    (1, 129, 1, 2, 0, torch.bfloat16, (64,)),
+]
+
+
+def ids(c):
+    return f"BH{c[0]}-n{c[1]}-w{c[2]}-wu{c[3]}-d{c[4]}-{str(c[5]).split('.')[-1]}-G{len(c[6])}"
+
+
+def mk(BH, n, w, wu, dil, dtype, gidx):
+    return swab.Desc(1, BH, n, 64, w, wu, dil, 0.0, dtype, gidx)
+
+
+def ignorable_band(n, w, wu, dil, gidx):
+    """[n, D] True where a consumer must ignore the band slot."""
+    s = dil + 1
+    i = np.arange(n)[:, None]
+    t = np.arange(w + wu + 1)[None, :]
+    j = i + (t - w) * s
+    bad = (j < 0) | (j >= n)
+    g = np.zeros(n, dtype=bool)
+    g[list(gidx)] = True
+    jj = np.clip(j, 0, n - 1)
+    bad |= g[jj] & ~((j < 0) | (j >= n))
+    bad |= g[:, None]
+    return bad
+
+
+def poison(band, cols, n, w, wu, dil, gidx):
+    band = band.clone()
+    band[:, torch.from_numpy(ignorable_band(n, w, wu, dil, gidx))] = float("nan")
+    cols = cols.clone()
+    cols[:, list(gidx), :] = float("nan")
+    return band, cols
+
+
+def glob_pair(BH, n, G, dtype, seed, uniform=False):
+    if uniform:
+        return (seeded_uniform((BH, n, G), dtype, seed), seeded_uniform((BH, G, n), dtype, seed + 1))
+    return (seeded_band(BH, n, G, dtype, seed), seeded_band(BH, G, n, dtype, seed + 1))
+
+
+def empty_glob(d):
+    return (torch.empty(d.BH, d.n, d.G, dtype=d.dtype, device="cuda"),
+            torch.empty(d.BH, d.G, d.n, dtype=d.dtype, device="cuda"))
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_band_qk_globals(case):
+    BH, n, w, wu, dil, dtype, gidx = case
+    d = mk(*case)
+    A, B = seeded_qkvo(BH, n, 64, dtype, seed=31, count=2)
+    S = empty_band(d)
+    Sg = empty_glob(d)
+    swab.band_qk(d, 0.125, *dev(A, B), S, Sg)
+    refS, refc, refr = oracle.band_qk(f64(A), f64(B), w, wu, dil, 0.125, 0.0, gidx)
+    tol = score_tol(dtype)
+    assert normwise(f64(Sg[0]), refc) <= tol
+    assert normwise(f64(Sg[1]), refr) <= tol
+    assert normwise(f64(S), refS, valid_mask(n, w, wu, dil)) <= tol
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_band_softmax_globals(case):
+    BH, n, w, wu, dil, dtype, gidx = case
+    d = mk(*case)
+    S = (seeded_band(BH, n, d.D, torch.float32, seed=32) * 3).to(dtype)
+    Sc, Sr = glob_pair(BH, n, d.G, dtype, seed=33)
+    Sp, Scp = poison(S, Sc, n, w, wu, dil, gidx)
+    P = empty_band(d)
+    Pg = empty_glob(d)
+    lse = torch.empty(BH, n, dtype=torch.float32, device="cuda")
+    swab.band_softmax(d, Sp.cuda(), P, lse, Sg=(Scp.cuda(), Sr.cuda()), Pg=Pg)
+    refP, reflse, refPc, refPr = oracle.band_softmax(f64(S), w, wu, dil, gidx, f64(Sc), f64(Sr))
+    tol = 1e-6 if dtype == torch.float32 else ABS_TOL
+    assert np.max(np.abs(f64(P) - refP)) <= tol
+    assert np.max(np.abs(f64(Pg[0]) - refPc)) <= tol
+    assert np.max(np.abs(f64(Pg[1]) - refPr)) <= tol
+    assert np.max(np.abs(f64(lse) - reflse)) <= 1e-4 * max(1.0, np.max(np.abs(reflse)))
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_band_pv_globals(case):
+    BH, n, w, wu, dil, dtype, gidx = case
+    d = mk(*case)
+    P = seeded_band(BH, n, d.D, dtype, seed=34)
+    Pc, Pr = glob_pair(BH, n, d.G, dtype, seed=35)
+    (V,) = seeded_qkvo(BH, n, 64, dtype, seed=36, count=1)
+    Pp, Pcp = poison(P, Pc, n, w, wu, dil, gidx)
+    O = empty_dense(d)
+    swab.band_pv(d, 0.75, Pp.cuda(), V.cuda(), O, Pg=(Pcp.cuda(), Pr.cuda()))
+    ref = oracle.band_pv(f64(P), f64(V), w, wu, dil, 0.75, gidx, f64(Pc), f64(Pr))
+    assert normwise(f64(O), ref) <= score_tol(dtype)
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+@pytest.mark.parametrize("name", ["band_qk_bwd_t", "band_pv_bwd_t"])
+def test_band_t_globals(case, name):
+    BH, n, w, wu, dil, dtype, gidx = case
+    d = mk(*case)
+    Bd = seeded_band(BH, n, d.D, dtype, seed=37)
+    Bc, Br = glob_pair(BH, n, d.G, dtype, seed=38)
+    (Y,) = seeded_qkvo(BH, n, 64, dtype, seed=39, count=1)
+    Bp, Bcp = poison(Bd, Bc, n, w, wu, dil, gidx)
+    X = empty_dense(d)
+    getattr(swab, name)(d, 0.5, Bp.cuda(), Y.cuda(), X, (Bcp.cuda(), Br.cuda()))
+    ref = oracle.band_t(f64(Bd), f64(Y), w, wu, dil, 0.5, gidx, f64(Bc), f64(Br))
+    assert normwise(f64(X), ref) <= score_tol(dtype)
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_band_softmax_bwd_globals(case):
+    BH, n, w, wu, dil, dtype, gidx = case
+    d = mk(*case)
+    P = seeded_band(BH, n, d.D, dtype, seed=40)
+    dP = seeded_band(BH, n, d.D, dtype, seed=41)
+    Pc, Pr = glob_pair(BH, n, d.G, dtype, seed=42)
+    dPc, dPr = glob_pair(BH, n, d.G, dtype, seed=44)
+    Pp, Pcp = poison(P, Pc, n, w, wu, dil, gidx)
+    dPp, dPcp = poison(dP, dPc, n, w, wu, dil, gidx)
+    dS = empty_band(d)
+    dSg = empty_glob(d)
+    swab.band_softmax_bwd(d, Pp.cuda(), dPp.cuda(), dS, Pg=(Pcp.cuda(), Pr.cuda()),
+                          dPg=(dPcp.cuda(), dPr.cuda()), dSg=dSg)
+    rS, rSc, rSr = oracle.band_softmax_bwd(f64(P), f64(dP), w, wu, dil, gidx, f64(Pc), f64(dPc),
+                                           f64(Pr), f64(dPr))
+    tol = score_tol(dtype)
+    assert normwise(f64(dS), rS) <= tol
+    assert normwise(f64(dSg[0]), rSc) <= tol
+    assert normwise(f64(dSg[1]), rSr) <= tol
+
+
+# ---------------------------------------------------------------------------
+# chains: forward + backward with globals against the definition
+# ---------------------------------------------------------------------------
+def gpu_chain_globals(d, Q, K, V, dO, scale):
+    S, P, dP, dS = (empty_band(d) for _ in range(4))
+    Sg, Pg, dPg, dSg = (empty_glob(d) for _ in range(4))
+    lse = torch.empty((d.BH, d.n), dtype=torch.float32, device="cuda")
+    O, dQ, dK, dV = (empty_dense(d) for _ in range(4))
+    swab.band_qk(d, scale, Q, K, S, Sg)
+    swab.band_softmax(d, S, P, lse, Sg=Sg, Pg=Pg)
+    swab.band_pv(d, 1.0, P, V, O, Pg=Pg)
+    swab.band_qk(d, 1.0, dO, V, dP, dPg)
+    swab.band_softmax_bwd(d, P, dP, dS, Pg=Pg, dPg=dPg, dSg=dSg)
+    swab.band_pv(d, scale, dS, K, dQ, Pg=dSg)
+    swab.band_qk_bwd_t(d, scale, dS, Q, dK, dSg)
+    swab.band_pv_bwd_t(d, 1.0, P, dO, dV, Pg)
+    torch.cuda.synchronize()
+    return dict(O=O, lse=lse, dQ=dQ, dK=dK, dV=dV)
+
+
+def check_chain_globals(d, Q, K, V, dO, scale, slices):
+    out = gpu_chain_globals(d, *dev(Q, K, V, dO), scale)
+    f32 = d.dtype == torch.float32
+    for b in slices:
+        sl = slice(b, b + 1)
+        q, k, v, go = (f64(x[sl]) for x in (Q, K, V, dO))
+        rO, rl = oracle.attention_fwd(q, k, v, d.w, d.w_upper, d.dilation, scale, d.global_idx)
+        rq, rk, rv = oracle.attention_bwd(q, k, v, go, d.w, d.w_upper, d.dilation, scale,
+                                          d.global_idx)
+        for name, ref in (("O", rO), ("dQ", rq), ("dK", rk), ("dV", rv)):
+            got = f64(out[name][sl])
+            if f32:
+                assert normwise(got, ref) <= 1e-5, name
+            else:
+                assert np.max(np.abs(got - ref)) <= ABS_TOL, name
+        assert np.max(np.abs(f64(out["lse"][sl]) - rl)) <= (1e-5 if f32 else 2e-2)
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_chain_globals_small(case):
+    BH, n, w, wu, dil, dtype, gidx = case
+    if dtype == torch.bfloat16 and w + wu + 1 < 32:
+        # A window of a handful of keys, with S and P each stored once in bf16
+        # (2^-8 relative each), puts O off by up to ~|v| * 1e-2: the 1e-2
+        # absolute bound on chained outputs is not meaningful there.  The
+        # kernels of this shape are checked one by one above; the chain runs
+        # in fp16.
+        dtype = torch.float16
+    d = mk(BH, n, w, wu, dil, dtype, gidx)
+    Q, K, V, dO = seeded_qkvo(BH, n, 64, dtype, seed=45)
+    check_chain_globals(d, Q, K, V, dO, 0.125, range(BH))
+
+
+def test_chain_config4_bf16_globals_sampled():
+    wl = WORKLOADS[4]
+    Q, K, V, dO = workload_inputs(wl)
+    check_chain_globals(swab.Desc.from_workload(wl), Q, K, V, dO, wl.scale, slices=(0, 77, 143))
