@@ -3,11 +3,14 @@
 
 One step = one forward + backward pass of sliding-window attention over the
 Longformer-base workload (b=1, h=12, n=4096, head_dim=64, w=w_upper=256,
-fp16, dilation 0), every kernel launched through the C ABI:
+fp16, dilation 0), every kernel launched through the C ABI.  Two variants,
+both timed in every run (--step picks the headline):
 
-  band_qk(Q,K)->S, band_softmax(S)->P,lse, band_pv(P,V)->O,
-  band_qk(dO,V)->dP, band_softmax_bwd(P,dP)->dS, band_pv(dS,K)->dQ,
-  band_qk_bwd_t(dS,Q)->dK, band_pv_bwd_t(P,dO)->dV.
+  fused (default): band_attention(Q,K,V)->O,lse, then
+      band_attention_bwd(Q,K,V,O,dO,lse)->dQ,dK,dV (scores never in HBM);
+  materialised: band_qk(Q,K)->S, band_softmax(S)->P,lse, band_pv(P,V)->O,
+      band_qk(dO,V)->dP, band_softmax_bwd(P,dP)->dS, band_pv(dS,K)->dQ,
+      band_qk_bwd_t(dS,Q)->dK, band_pv_bwd_t(P,dO)->dV.
 
 `value` is TFLOP/s on algorithmic flops (6 banded contractions x 2*head_dim
 per valid (query, key) pair) over device time with inputs resident in HBM.
@@ -63,33 +66,42 @@ def step_flops(wl) -> float:
 
 
 def kernel_bytes(wl) -> dict:
+    """Algorithmic bytes of one call: every input read once, every output written once."""
     e = torch.finfo(wl.dtype).bits // 8
     dense = wl.BH * wl.n * wl.head_dim * e
     band = wl.BH * wl.n * wl.D * e
-    lse = wl.BH * wl.n * 4
+    rowf = wl.BH * wl.n * 4
     return {
         "band_qk": 2 * dense + band,
-        "band_softmax": 2 * band + lse,
+        "band_softmax": 2 * band + rowf,
         "band_pv": band + 2 * dense,
         "band_softmax_bwd": 3 * band,
         "band_t": band + 2 * dense,
+        "band_attention": 4 * dense + rowf,
+        # Q, K, V, O, dO, lse in; dQ, dK, dV out; the per-row delta out and back in
+        "band_attention_bwd": 8 * dense + 3 * rowf,
     }
 
 
 def kernel_flops(wl) -> dict:
+    """Algorithmic flops of one call (2*head_dim per valid pair per contraction)."""
     c = 2.0 * wl.head_dim * valid_pairs(wl)
     return {"band_qk": c, "band_softmax": 0.0, "band_pv": c, "band_softmax_bwd": 0.0,
-            "band_t": c}
+            "band_t": c, "band_attention": 2 * c, "band_attention_bwd": 4 * c}
 
 
 # ---------------------------------------------------------------------------
 # the step
 # ---------------------------------------------------------------------------
 class Step:
-    """Buffers and launches of one forward + backward step."""
+    """Buffers and launches of one forward + backward step, materialised band
+    tensors: every banded product and softmax is its own call."""
 
     NAMES = ["band_qk", "band_softmax", "band_pv", "band_qk", "band_softmax_bwd", "band_pv",
              "band_t", "band_t"]
+    LAUNCHES = 8
+    DESCRIPTION = ("materialised fwd+bwd: band_qk, band_softmax, band_pv, band_qk(dO,V), "
+                   "band_softmax_bwd, band_pv(dS,K), band_qk_bwd_t, band_pv_bwd_t")
 
     def __init__(self, wl, device):
         import sliding_window_attention_band_gb300 as swab
@@ -146,6 +158,38 @@ class Step:
         return sum(x.numel() * x.element_size() for x in self.out_host)
 
 
+class FusedStep(Step):
+    """Forward + backward with the scores kept on chip: band_attention (O, lse),
+    then band_attention_bwd (dQ, dK, dV; its delta, dK/dV and dQ kernels)."""
+
+    NAMES = ["band_attention", "band_attention_bwd"]
+    LAUNCHES = 4
+    DESCRIPTION = ("fused fwd+bwd: band_attention (O, lse), band_attention_bwd "
+                   "(delta, dK/dV and dQ kernels)")
+
+    def __init__(self, wl, device):
+        super().__init__(wl, device)
+        nbytes = self.swab.band_attention_bwd_workspace(self.d)
+        self.ws = torch.empty(nbytes // 4, dtype=torch.float32, device=device)
+
+    def launches(self):
+        s, d, sc = self.swab, self.d, self.wl.scale
+        return [
+            lambda: s.band_attention(d, sc, self.Q, self.K, self.V, self.O, self.lse),
+            lambda: s.band_attention_bwd(d, sc, self.Q, self.K, self.V, self.O, self.dO, self.lse,
+                                         self.dQ, self.dK, self.dV, self.ws),
+        ]
+
+
+def step_summary(wl, step, per_step, per_kernel, peaks):
+    return {"ms_per_step": round(statistics.mean(per_step), 4),
+            "tflops": round(step_flops(wl) / (statistics.mean(per_step) * 1e-3) / 1e12, 3),
+            "per_call_us": {f"{i}:{nm}": round(statistics.mean(t) * 1e3, 2)
+                            for i, (nm, t) in enumerate(zip(step.NAMES, per_kernel))},
+            "roofline": roofline(wl, step.NAMES, per_kernel, peaks),
+            "step_roofline_frac": round(step_roofline_frac(wl, step.NAMES, per_kernel, peaks), 4)}
+
+
 def time_steps(step, steps, warmup, flush):
     """Per-step device times (ms) and per-kernel times (ms) over `steps` steps."""
     for _ in range(warmup):
@@ -163,6 +207,37 @@ def time_steps(step, steps, warmup, flush):
         for k in range(nk):
             per_kernel[k].append(ev[k].elapsed_time(ev[k + 1]))
     return per_step, per_kernel
+
+
+def fused_forward(wl, device, steps, warmup, flush, peaks):
+    """band_attention (scores on chip) on one workload: ms, TFLOP/s, roofline."""
+    import sliding_window_attention_band_gb300 as swab
+
+    d = swab.Desc.from_workload(wl)
+    Q, K, V = (x.to(device) for x in workload_inputs(wl, count=3))
+    O = torch.empty_like(Q)
+    lse = torch.empty((wl.BH, wl.n), dtype=torch.float32, device=device)
+    for _ in range(warmup):
+        swab.band_attention(d, wl.scale, Q, K, V, O, lse)
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        swab.band_attention(d, wl.scale, Q, K, V, O, lse)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.mean(ts)
+    flops = 2 * 2.0 * wl.head_dim * valid_pairs(wl)
+    e = torch.finfo(wl.dtype).bits // 8
+    nbytes = 4 * wl.BH * wl.n * wl.head_dim * e + wl.BH * wl.n * 4
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    bound = "tensor" if flops / (peaks["bf16_tflops"] * 1e12) > nbytes / (peaks["hbm_gbs"] * 1e9) \
+        else "hbm"
+    return {"ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": bound,
+            "roofline_frac": round(t_roof / (ms * 1e-3), 4), "flops": flops, "bytes": nbytes}
 
 
 def time_e2e(step, steps, warmup, flush):
@@ -252,7 +327,8 @@ def measured_peaks():
 
 def kernel_source_hash(kernel):
     files = {"band_qk": "k_band_qk.cu", "band_pv": "k_band_gather.cu", "band_t": "k_band_gather.cu",
-             "band_softmax": "k_softmax.cu", "band_softmax_bwd": "k_softmax.cu"}
+             "band_softmax": "k_softmax.cu", "band_softmax_bwd": "k_softmax.cu",
+             "band_attention": "k_attention.cu", "band_attention_bwd": "k_attention_bwd.cu"}
     path = os.path.join(ROOT, "sliding_window_attention_band_gb300", "csrc", files[kernel])
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -375,6 +451,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="swab", choices=["swab", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step", default="fused", choices=["fused", "materialised"],
+                    help="fused: band_attention + band_attention_bwd; materialised: the "
+                         "eight band_qk / softmax / band_pv / band_t calls")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -402,8 +481,10 @@ def main():
     swab.load()
     device = torch.device("cuda", local)
     wl = WORKLOADS[MAIN_CFG]
-    step = Step(wl, device)
+    step_cls = FusedStep if args.step == "fused" else Step
+    step = step_cls(wl, device)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    peaks = measured_peaks()
 
     clocks = ClockSampler(local)
     if dist:
@@ -425,24 +506,27 @@ def main():
     ms_per_step = dev_ms / args.steps
     flops = step_flops(wl)
     value = world * flops * args.steps / (dev_ms * 1e-3) / 1e12
-
-    # dilation-3 companion (same step, config 3)
-    also = {}
-    wl3 = WORKLOADS[ALSO_CFG]
-    step3 = Step(wl3, device)
-    ps3, pk3 = time_steps(step3, max(3, args.steps // 2), 3, flush)
-    also[wl3.name] = {"ms_per_step": round(statistics.mean(ps3), 4),
-                      "tflops": round(step_flops(wl3) / (statistics.mean(ps3) * 1e-3) / 1e12, 3),
-                      "per_kernel_us": {f"{i}:{nm}": round(statistics.mean(t) * 1e3, 2)
-                                        for i, (nm, t) in enumerate(zip(step3.NAMES, pk3))}}
-    del step3
-
     e2e_ms = time_e2e(step, max(3, args.steps // 2), 3, flush)
     e2e_val = world * flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+
+    # companions, timed the same way: the other step variant, dilation 3, the
+    # fused forward on the long causal workload
+    also = {}
+    n_also = max(3, args.steps // 2)
+    for cls in (FusedStep, Step):
+        for w_ in (WORKLOADS[MAIN_CFG], WORKLOADS[ALSO_CFG]):
+            if cls is step_cls and w_ is wl:
+                continue
+            st = cls(w_, device)
+            ps, pk = time_steps(st, n_also, 3, flush)
+            also[f"{'fused' if cls is FusedStep else 'materialised'}:{w_.name}"] = \
+                step_summary(w_, st, ps, pk, peaks)
+            del st
+    wl5 = WORKLOADS[5]
+    also[f"band_attention:{wl5.name}"] = fused_forward(wl5, device, n_also, 3, flush, peaks)
     if swab.device_status(reset=True) != 0:
         raise SystemExit("a kernel raised the device status word during the benchmark")
 
-    peaks = measured_peaks()
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -450,17 +534,16 @@ def main():
         "data": "synthetic",
         "config": {**wl.describe(), "parallelism": f"replicas x{world}" if world > 1 else "none",
                    "l2": "flushed (256 MB write) before every timed step",
-                   "step": "fwd+bwd: band_qk, band_softmax, band_pv, band_qk(dO,V), "
-                           "band_softmax_bwd, band_pv(dS,K), band_qk_bwd_t, band_pv_bwd_t",
-                   "flops_per_step": flops},
-        "per_kernel_us": {f"{i}:{nm}": round(statistics.mean(t) * 1e3, 2)
-                          for i, (nm, t) in enumerate(zip(step.NAMES, per_kernel))},
+                   "step": step.DESCRIPTION, "flops_per_step": flops,
+                   "flops_counted": "6 banded contractions x 2*head_dim per valid pair"},
+        "per_call_us": {f"{i}:{nm}": round(statistics.mean(t) * 1e3, 2)
+                        for i, (nm, t) in enumerate(zip(step.NAMES, per_kernel))},
         "roofline": roofline(wl, step.NAMES, per_kernel, peaks),
         "step_roofline_frac": round(step_roofline_frac(wl, step.NAMES, per_kernel, peaks), 4),
         "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": step.h2d_bytes, "d2h_bytes_per_step": step.d2h_bytes,
                 "ms_per_step": round(statistics.mean(e2e_ms), 4)},
-        "gpu_launches": len(step.NAMES) * args.steps,
+        "gpu_launches": step.LAUNCHES * args.steps,
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 3),
         "also": also,

@@ -156,6 +156,25 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
                                     const void *K, const void *V, void *O, float *lse,
                                     void *stream);
 
+/* Fused backward of band_attention: dQ, dK, dV of
+ *   O = softmax_band(scale * Q.K^T) . V
+ * recomputing the band probabilities on chip from lse (the forward's
+ * log-sum-exp) and never writing a band tensor:
+ *   P = exp(scale*Q.K^T - lse), dP = dO.V^T, delta_i = dO_i . O_i,
+ *   dS = P*(dP - delta), dQ = scale*dS.K, dK = scale*dS^T.Q, dV = P^T.dO
+ * on the used slots (the two backward products of the TVM thread, post 6,
+ * with the textbook softmax derivative).  Deterministic (no atomics).
+ * `workspace` is caller-owned device memory of band_attention_bwd_workspace()
+ * bytes (the per-row delta, fp32); its contents on entry do not matter.
+ * Global tokens are not supported here (n_global must be 0). */
+SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, const void *Q,
+                                        const void *K, const void *V, const void *O,
+                                        const void *dO, const float *lse, void *dQ, void *dK,
+                                        void *dV, void *workspace, void *stream);
+
+/* Bytes of workspace band_attention_bwd needs for `desc` (0 if desc is NULL). */
+SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc);
+
 /* Human-readable name of a status code (static string). */
 SWAB_API const char *swab_status_string(swab_status status);
 
@@ -163,6 +182,15 @@ SWAB_API const char *swab_status_string(swab_status status);
  * current device: bit k set means SWAB status k was raised by a kernel.
  * Synchronises the device.  Returns SWAB_ERR_CUDA if the read fails. */
 SWAB_API swab_status swab_device_status(int32_t *flags, int32_t reset);
+
+/* Failure-detection self-test: launches one warp that waits on an mbarrier no
+ * thread ever arrives at, using the same bounded wait as every pipelined
+ * kernel, with a limit of `limit_us` microseconds (1..1000000).  The wait gives
+ * up, records SWAB_ERR_TIMEOUT in the device status word and the kernel
+ * returns; nothing faults or hangs and the context stays usable.  Read the
+ * result with swab_device_status().  No counterpart on the pages: it tests
+ * the library's own error reporting. */
+SWAB_API swab_status swab_selftest_wait_timeout(uint32_t limit_us, void *stream);
 
 /* Library version, e.g. "0.1.0". */
 SWAB_API const char *swab_version(void);

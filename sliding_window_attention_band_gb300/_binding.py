@@ -25,8 +25,9 @@ _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # every symbol the header declares
 API_FUNCTIONS = ("band_qk", "band_softmax", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
-                 "band_softmax_bwd", "band_attention", "swab_status_string",
-                 "swab_device_status", "swab_version")
+                 "band_softmax_bwd", "band_attention", "band_attention_bwd",
+                 "band_attention_bwd_workspace", "swab_status_string", "swab_device_status",
+                 "swab_selftest_wait_timeout", "swab_version")
 
 
 class SwabError(RuntimeError):
@@ -115,12 +116,16 @@ def load():
                 "band_pv_bwd_t": [D, f, P, Gp, P, P, P],
                 "band_softmax_bwd": [D, P, Gp, P, Gp, P, Gp, P],
                 "band_attention": [D, f, P, P, P, P, P, P],
+                "band_attention_bwd": [D, f, P, P, P, P, P, P, P, P, P, P, P],
                 "swab_device_status": [ctypes.POINTER(i32), i32],
+                "swab_selftest_wait_timeout": [ctypes.c_uint32, P],
             }
             for name, args in sigs.items():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            lib.band_attention_bwd_workspace.argtypes = [D]
+            lib.band_attention_bwd_workspace.restype = ctypes.c_size_t
             lib.swab_status_string.restype = ctypes.c_char_p
             lib.swab_status_string.argtypes = [ctypes.c_int]
             lib.swab_version.restype = ctypes.c_char_p
@@ -269,6 +274,33 @@ def band_attention(desc: Desc, scale, Q, K, V, O, lse=None, stream=None):
     _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
     _call("band_attention", ctypes.byref(desc.c), float(scale), _ptr(Q), _ptr(K), _ptr(V),
           _ptr(O), _ptr(lse), _stream(stream, O))
+
+
+def band_attention_bwd_workspace(desc: Desc) -> int:
+    """Bytes of device workspace band_attention_bwd needs."""
+    return int(load().band_attention_bwd_workspace(ctypes.byref(desc.c)))
+
+
+def band_attention_bwd(desc: Desc, scale, Q, K, V, O, dO, lse, dQ, dK, dV, workspace,
+                       stream=None):
+    """Fused backward: dQ, dK, dV from Q, K, V, O, dO and the forward's lse."""
+    for n_, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO), ("dQ", dQ), ("dK", dK),
+                  ("dV", dV)):
+        _check_shape(n_, t, _dense(desc), desc.dtype)
+    _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
+    if workspace.numel() * workspace.element_size() < band_attention_bwd_workspace(desc):
+        raise ValueError("workspace too small")
+    _call("band_attention_bwd", ctypes.byref(desc.c), float(scale), _ptr(Q), _ptr(K), _ptr(V),
+          _ptr(O), _ptr(dO), _ptr(lse), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
+          _stream(stream, dQ))
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None):
+    """Launch the bounded-wait self-test (a wait that must give up after limit_us)."""
+    s = _stream(stream, None)
+    if s is None and torch.cuda.is_available():
+        s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    _call("swab_selftest_wait_timeout", int(limit_us), s)
 
 
 def device_status(reset: bool = True) -> int:

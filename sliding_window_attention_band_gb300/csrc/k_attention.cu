@@ -11,16 +11,17 @@
 //   1. MMA warp: S_c = Q . K_c^T  (tcgen05, M = 128 queries, N = 128 keys,
 //      K = 64) into TMEM S buffer c%2;
 //   2. softmax warps (thread = query row = TMEM lane): the band is a
-//      contiguous column interval of the chunk for each row, so masking is
-//      two compares.  Online softmax in the log2 domain: running max m,
-//      running sum l; p = 2^(x - m) rounded to fp16/bf16 and written as the
-//      K-major, 128-B-swizzled A operand of the next product (smem);
+//      contiguous column interval of the chunk for each row (masking is two
+//      compares, skipped when the whole chunk is inside every row's band).
+//      Online softmax in the log2 domain with a reference max that is raised
+//      only when a chunk exceeds it by more than 2^8, so each chunk is one
+//      pass over tensor memory; p = 2^(x - m) rounded to fp16/bf16 is written
+//      as the K-major, 128-B-swizzled A operand of the next product (smem);
 //   3. MMA warp: O_c = P_c . V_c into TMEM O buffer c%2 (fresh, not
 //      accumulated);
 //   4. softmax warps, one chunk later (so the P.V product of chunk c runs
 //      while chunk c+1's softmax is computed): acc = acc * 2^(m_prev - m) + O_c.
-// The row sum l is accumulated from the same rounded p values the MMA
-// consumes.  At the end O = acc / l, lse = m*ln2 + ln l.
+// At the end O = acc / l, lse = m*ln2 + ln l.
 //
 // Warps: 0 = TMA producer (Q once; K and V chunks into a 3-stage ring),
 // 1 = TMEM owner + MMA issuer, 2..5 = softmax / epilogue.
@@ -43,6 +44,12 @@ constexpr int kPBytes = kBQ * kBK * 2;         // 32 KB (two 64-key K-atoms)
 constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + 2 * kPBytes + 1024 + 1024;
 constexpr uint32_t kTmemCols = 512;            // S: 2 x 128, O: 2 x 64
 constexpr uint32_t kTmemO = 256;               // column of the first O buffer
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -173,11 +180,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- softmax warps: thread = query row ----------------
-        constexpr float kLog2e = 1.4426950408889634f;
+        // Per row: a reference max m (log2 units) and the sum l of
+        // p = 2^(x - m) over the keys seen so far.  A chunk is processed in
+        // ONE pass over tensor memory with the current m; m is raised only
+        // when the chunk's largest score exceeds it by more than kSlack (then
+        // the chunk is redone with the new m), so p <= 2^kSlack stays well
+        // inside fp16/bf16 range.  Rows with no key seen yet take their m from
+        // a max-only pass first.  The softmax does not depend on the choice of
+        // m: O = acc / l and lse = m ln2 + ln l use the same m.
+        constexpr float kSlack = 8.f;
         const int quarter = warp & 3;
         const int q = quarter * 32 + lane;
         const int qq = a0 + q;
-        const float xscale = p.scale * kLog2e;
+        const float xscale = p.scale * 1.4426950408889634f;
         float m = -INFINITY, l = 0.f, corr_prev = 1.f;
         float acc[64];
 #pragma unroll
@@ -211,59 +226,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             // this row's band inside the chunk: columns [jlo, jhi]
             const int jlo = max(qq - g.w - kbase, 0);
             const int jhi = min(min(qq + g.wu, kb_hi) - kbase, kBK - 1);
+            const bool full = __all_sync(0xffffffffu, jlo == 0 && jhi == kBK - 1);
             bool w_ok = mbar_wait(&sfull[b], bph, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
             tc_fence_after();
-            // pass 1: row max over the band columns
-            float mx = -INFINITY;
+            const uint32_t sbuf = lane_base + b * kBK;
+            float mref = m;
+            if (__any_sync(0xffffffffu, m == -INFINITY)) {
+                // rows with no key yet: the chunk's own max
+                float mx = -INFINITY;
 #pragma unroll 1
-            for (int grp = 0; grp < 4; ++grp) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + b * kBK + grp * 32, v);
-                tmem_ld_wait();
+                for (int grp = 0; grp < 4; ++grp) {
+                    uint32_t v[32];
+                    tmem_ld32(sbuf + grp * 32, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = grp * 32 + i;
-                    if (j >= jlo && j <= jhi) mx = fmaxf(mx, __uint_as_float(v[i]) * xscale);
+                    for (int i = 0; i < 32; ++i) {
+                        const int j = grp * 32 + i;
+                        if (j >= jlo && j <= jhi) mx = fmaxf(mx, __uint_as_float(v[i]) * xscale);
+                    }
                 }
+                if (m == -INFINITY) mref = mx;
             }
-            const float m_new = fmaxf(m, mx);
-            const float corr = (m == -INFINITY) ? 1.f : exp2f(m - m_new);
-            l *= corr;
             // the P tile of chunk c may still feed the P.V product of chunk c-2
             w_ok = mbar_wait(&pempty[b], bph ^ 1, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-            // pass 2: p = 2^(x - m_new), rounded; row sum of the rounded values
+            const uint32_t pbase = smem_u32(pbuf + b * kPBytes);
+            float lc = 0.f;
+            for (int pass = 0; pass < 2; ++pass) {
+                const float mb = mref == -INFINITY ? 0.f : mref;
+                float ymax = -INFINITY;  // chunk max relative to mref
+                lc = 0.f;
 #pragma unroll 1
-            for (int grp = 0; grp < 4; ++grp) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + b * kBK + grp * 32, v);
-                tmem_ld_wait();
-                uint32_t pk[16];
+                for (int grp = 0; grp < 4; ++grp) {
+                    uint32_t v[32];
+                    tmem_ld32(sbuf + grp * 32, v);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j0 = grp * 32 + 2 * i, j1 = j0 + 1;
-                    const float p0 = (j0 >= jlo && j0 <= jhi)
-                                         ? exp2f(fmaf(__uint_as_float(v[2 * i]), xscale, -m_new)) : 0.f;
-                    const float p1 = (j1 >= jlo && j1 <= jhi)
-                                         ? exp2f(fmaf(__uint_as_float(v[2 * i + 1]), xscale, -m_new)) : 0.f;
-                    pk[i] = pack2<T>(p0, p1);
-                    l += lo16<T>(pk[i]) + hi16<T>(pk[i]);
-                }
-                // 32 keys = 4 x 16-byte pieces; key-atom grp/2, pieces (grp%2)*4 + 0..3
-                const uint32_t atom = smem_u32(pbuf + b * kPBytes) + (grp >> 1) * (kPBytes / 2) + q * 128;
+                    for (int i = 0; i < 16; ++i) {
+                        float y0 = fmaf(__uint_as_float(v[2 * i]), xscale, -mb);
+                        float y1 = fmaf(__uint_as_float(v[2 * i + 1]), xscale, -mb);
+                        if (!full) {
+                            const int j0 = grp * 32 + 2 * i;
+                            if (j0 < jlo || j0 > jhi) y0 = -INFINITY;
+                            if (j0 + 1 < jlo || j0 + 1 > jhi) y1 = -INFINITY;
+                        }
+                        ymax = fmaxf(ymax, fmaxf(y0, y1));
+                        const float p0 = ex2(y0), p1 = ex2(y1);
+                        lc += p0 + p1;
+                        pk[i] = pack2<T>(p0, p1);
+                    }
+                    // 32 keys = 4 x 16-byte pieces; key-atom grp/2, pieces (grp%2)*4 + 0..3
+                    const uint32_t atom = pbase + (grp >> 1) * (kPBytes / 2) + q * 128;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int piece = (grp & 1) * 4 + u;
-                    sts16(atom + ((piece ^ (q & 7)) << 4),
-                          make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+                    for (int u = 0; u < 4; ++u) {
+                        const int piece = (grp & 1) * 4 + u;
+                        sts16(atom + ((piece ^ (q & 7)) << 4),
+                              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+                    }
                 }
+                // redo the chunk if a score rose more than kSlack above mref
+                const bool redo = ymax > kSlack;
+                if (!__any_sync(0xffffffffu, redo)) break;
+                if (redo) mref = mb + ymax;
             }
+            const float corr = (m == -INFINITY) ? 1.f : ex2(m - mref);
+            l = l * corr + lc;
             tc_fence_before();
             mbar_arrive(&sempty[b]);   // S buffer b may be overwritten
             fence_proxy_async_smem();
             mbar_arrive(&pfull[b]);    // P tile b is ready for the tensor core
-            m = m_new;
+            m = mref;
             if (c > 0) {
                 if (!fold_o(c - 1, corr_prev)) { ok = false; break; }
             }

@@ -1,0 +1,643 @@
+// k_attention_bwd.cu -- fused backward of sliding-window attention: dQ, dK,
+// dV of O = softmax_band(scale * Q K^T) V without materialising any band
+// tensor.  The banded products are those of "Developing a faster schedule
+// for Longformer's kernel" (TVM forum, post 6: the forward product and the two
+// backward products); the softmax derivative is the textbook one:
+//     P  = exp(scale * Q K^T - lse)         (lse from the forward)
+//     dP = dO V^T,   delta_i = dO_i . O_i,   dS = P * (dP - delta)
+//     dQ = scale * dS K,   dK = scale * dS^T Q,   dV = P^T dO
+// all restricted to the band (and to keys inside the sequence).
+//
+// Deterministic, no atomics: three kernels.
+//   k_bwd_delta     delta_i = dO_i . O_i into a caller-provided fp32 workspace.
+//   k_bwd_dkdv      one CTA per 128 KEYS of one residue; walks the queries
+//                   whose band contains them, 128 at a time:
+//                   S^T = K Q_c^T and dP^T = V dO_c^T (tcgen05, TMEM lane =
+//                   key), P^T and dS^T computed per key row and written as
+//                   K-major A operands, then dV += P^T dO_c and
+//                   dK += dS^T Q_c accumulate in TMEM.
+//   k_bwd_dq        one CTA per 128 QUERIES (the fused forward's layout):
+//                   S = Q K_c^T and dP = dO V_c^T, dS per query row, then
+//                   dQ += dS K_c in TMEM.
+// The dense tiles staged by TMA serve twice: K-major as the K=64 operand of
+// the score products and MN-major (rows along K) as the B operand of the
+// gradient products.
+#include <type_traits>
+
+#include "swab_internal.h"
+
+namespace swab {
+namespace {
+
+constexpr int kB = 128;           // rows per CTA and per chunk
+constexpr int kThreads = 192;     // producer, MMA, 4 worker warps
+constexpr int kTile = kB * 128;   // 16 KB: 128 rows x 64 halves
+constexpr int kStages = 2;
+constexpr int kOpBytes = kB * kB * 2;  // 32 KB: a 128 x 128 16-bit A operand (two K-atoms)
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Write 32 packed values (16 words) of row `row` into a K-major 128-B-swizzled
+// 128 x 128 operand at key/query group `grp` (32 columns).
+__device__ __forceinline__ void store_op_row(uint32_t op_addr, int row, int grp,
+                                             const uint32_t (&pk)[16]) {
+    const uint32_t atom = op_addr + (grp >> 1) * (kOpBytes / 2) + row * 128;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int piece = (grp & 1) * 4 + u;
+        sts16(atom + ((piece ^ (row & 7)) << 4),
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+    }
+}
+
+// D (+)= A[128 x 128, K-major smem operand] * B[K = 128 rows of 64, MN-major]
+__device__ __forceinline__ void mma_op_by_rows(uint32_t d, uint32_t a_addr, uint32_t b_addr,
+                                               uint32_t idesc, bool accumulate_first) {
+#pragma unroll
+    for (int k = 0; k < kB / 16; ++k) {
+        const uint32_t a = a_addr + (k >> 2) * (kOpBytes / 2) + (k & 3) * 32;
+        mma_f16_ss(d, sdesc_sw128(a, 16, 1024), sdesc_sw128(b_addr + 2048 * k, 1024, 1024), idesc,
+                   (accumulate_first || k > 0) ? 1u : 0u);
+    }
+}
+
+// D = A[128 x 64, K-major tile] * B[128 x 64, K-major tile]^T
+__device__ __forceinline__ void mma_tiles(uint32_t d, uint32_t a_addr, uint32_t b_addr,
+                                          uint32_t idesc) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        mma_f16_ss(d, sdesc_sw128(a_addr + 32 * k, 16, 1024), sdesc_sw128(b_addr + 32 * k, 16, 1024),
+                   idesc, k > 0);
+}
+
+// ---------------------------------------------------------------------------
+// delta_i = dO_i . O_i  (one warp per row; lane holds two of the 64 channels)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
+    const long long R = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (R >= (long long)p.g.BH * p.g.n) return;
+    const uint32_t o = reinterpret_cast<const uint32_t *>(p.O)[R * 32 + lane];
+    const uint32_t d = reinterpret_cast<const uint32_t *>(p.dO)[R * 32 + lane];
+    float v = lo16<T>(o) * lo16<T>(d) + hi16<T>(o) * hi16<T>(d);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) p.delta[R] = v;
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: one CTA per 128 keys
+// ---------------------------------------------------------------------------
+constexpr int kSmemDKDV = 2 * kTile + kStages * 2 * kTile + 2 * kOpBytes + 2 * 2 * kB * 4 + 1024 + 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_bwd_dkdv(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
+               const __grid_constant__ TmapSet mapV, const __grid_constant__ TmapSet mapdO,
+               const BwdArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *ktile = base;
+    uint8_t *vtile = base + kTile;
+    uint8_t *stages = base + 2 * kTile;                   // stage: Q chunk, dO chunk
+    uint8_t *pt_op = stages + kStages * 2 * kTile;        // P^T  [128 keys x 128 queries]
+    uint8_t *dst_op = pt_op + kOpBytes;                   // dS^T
+    float *qstat = reinterpret_cast<float *>(dst_op + kOpBytes);  // [2][2][128]: lse*log2e, delta
+    uint64_t *bars = reinterpret_cast<uint64_t *>(qstat + 2 * 2 * kB);
+    uint64_t *kvfull = bars;                  // 1
+    uint64_t *qfull = bars + 1;               // [kStages]
+    uint64_t *qempty = qfull + kStages;       // [kStages]
+    uint64_t *sfull = qempty + kStages;       // 1
+    uint64_t *sempty = sfull + 1;             // 1, count 128
+    uint64_t *opfull = sempty + 1;            // 1, count 128
+    uint64_t *opempty = opfull + 1;           // 1
+    uint64_t *accfull = opempty + 1;          // 1
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(accfull + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const Geom &g = p.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.y, bh = blockIdx.z;
+    const int nr = residue_len(g.n, g.s, r);
+    const int a0 = blockIdx.x * kB;  // first key (sub-index)
+    if (a0 >= nr) return;
+    const int qb_lo = max(a0 - g.wu, 0);
+    const int qb_hi = min(a0 + kB - 1 + g.w, nr - 1);
+    const int nck = (qb_hi - qb_lo + kB) / kB;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kvfull, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+        }
+        mbar_init(sfull, 1);
+        mbar_init(sempty, 128);
+        mbar_init(opfull, 128);
+        mbar_init(opempty, 1);
+        mbar_init(accfull, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const CUtensorMap *mq = &mapQ.m[r], *mk = &mapK.m[r], *mv = &mapV.m[r],
+                              *mo = &mapdO.m[r];
+            mbar_arrive_expect_tx(kvfull, 2 * kTile);
+            tma_load_3d(ktile, mk, kvfull, 0, a0, bh);
+            tma_load_3d(vtile, mv, kvfull, 0, a0, bh);
+            for (int c = 0; c < nck; ++c) {
+                const int st = c % kStages;
+                const uint32_t ph = (c / kStages) & 1;
+                if (!mbar_wait(&qempty[st], ph ^ 1, abort_flag, p.err)) break;
+                mbar_arrive_expect_tx(&qfull[st], 2 * kTile);
+                uint8_t *sq = stages + st * 2 * kTile;
+                tma_load_3d(sq, mq, &qfull[st], 0, qb_lo + c * kB, bh);
+                tma_load_3d(sq + kTile, mo, &qfull[st], 0, qb_lo + c * kB, bh);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr bool kBf16 = !std::is_same<T, __half>::value;
+            const uint32_t id_s = idesc_f16(kB, kB, kBf16, false, false);  // 128x128, both K-major
+            const uint32_t id_g = idesc_f16(kB, 64, kBf16, false, true);   // 128x64, B MN-major
+            const uint32_t k_addr = smem_u32(ktile), v_addr = smem_u32(vtile);
+            bool ok = mbar_wait(kvfull, 0, abort_flag, p.err);
+            auto issue_grad = [&](int c) -> bool {
+                const int st = c % kStages;
+                const uint32_t ph = c & 1;
+                if (!mbar_wait(opfull, ph, abort_flag, p.err)) return false;
+                tc_fence_after();
+                const uint32_t q_addr = smem_u32(stages + st * 2 * kTile);
+                const uint32_t o_addr = q_addr + kTile;
+                mma_op_by_rows(tmem + kColDV, smem_u32(pt_op), o_addr, id_g, c > 0);
+                mma_op_by_rows(tmem + kColDK, smem_u32(dst_op), q_addr, id_g, c > 0);
+                mma_commit(opempty);
+                mma_commit(&qempty[st]);
+                return true;
+            };
+            for (int c = 0; c < nck && ok; ++c) {
+                const int st = c % kStages;
+                const uint32_t ph = (c / kStages) & 1;
+                ok = mbar_wait(&qfull[st], ph, abort_flag, p.err) &&
+                     mbar_wait(sempty, (c & 1) ^ 1, abort_flag, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t q_addr = smem_u32(stages + st * 2 * kTile);
+                mma_tiles(tmem + kColS, k_addr, q_addr, id_s);            // S^T  = K Q_c^T
+                mma_tiles(tmem + kColDP, v_addr, q_addr + kTile, id_s);   // dP^T = V dO_c^T
+                mma_commit(sfull);
+                if (c > 0) ok = issue_grad(c - 1);
+            }
+            if (ok && issue_grad(nck - 1)) mma_commit(accfull);
+        }
+    } else {
+        // ---------------- workers: thread = key row ----------------
+        const int quarter = warp & 3;
+        const int m = quarter * 32 + lane;
+        const int tid = threadIdx.x - 64;  // 0..127
+        const int kk = a0 + m;             // key sub-index
+        const float xscale = p.scale * kLog2e;
+        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
+        bool ok = true;
+        for (int c = 0; c < nck; ++c) {
+            const int qbase = qb_lo + c * kB;
+            // per-query statistics of this chunk into shared memory
+            float *ql = qstat + (c & 1) * 2 * kB;
+            {
+                const int qq = qbase + tid;
+                float l2 = INFINITY, dl = 0.f;
+                if (qq < nr) {
+                    const long long row = (long long)bh * g.n + r + (long long)g.s * qq;
+                    l2 = p.lse[row] * kLog2e;
+                    dl = p.delta[row];
+                }
+                ql[tid] = l2;
+                ql[kB + tid] = dl;
+            }
+            named_bar(1, 128);
+            // this key's queries inside the chunk: columns [jlo, jhi]
+            const int jlo = max(kk - g.wu - qbase, 0);
+            const int jhi = min(min(kk + g.w, qb_hi) - qbase, kB - 1);
+            const bool key_ok = kk < nr;
+            const bool full = __all_sync(0xffffffffu, key_ok && jlo == 0 && jhi == kB - 1);
+            bool w_ok = mbar_wait(sfull, c & 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+            tc_fence_after();
+            w_ok = mbar_wait(opempty, (c & 1) ^ 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+            const uint32_t pt = smem_u32(pt_op), dst = smem_u32(dst_op);
+            const float4 *ql4 = reinterpret_cast<const float4 *>(ql);
+#pragma unroll 1
+            for (int grp = 0; grp < 4; ++grp) {
+                uint32_t sv[32], dv[32];
+                tmem_ld32(lane_base + kColS + grp * 32, sv);
+                tmem_ld32(lane_base + kColDP + grp * 32, dv);
+                tmem_ld_wait();
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 l4 = ql4[grp * 8 + i4];        // lse*log2e of 4 queries
+                    const float4 d4 = ql4[(kB + grp * 32) / 4 + i4];  // delta of the same
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pr[4], ds[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int e = 4 * i4 + h;
+                        float y = fmaf(__uint_as_float(sv[e]), xscale, -lv[h]);
+                        if (!full) {
+                            const int j = grp * 32 + e;
+                            if (!key_ok || j < jlo || j > jhi) y = -INFINITY;
+                        }
+                        pr[h] = ex2(y);
+                        ds[h] = pr[h] * (__uint_as_float(dv[e]) - dl[h]);
+                    }
+                    pk[2 * i4] = pack2<T>(pr[0], pr[1]);
+                    pk[2 * i4 + 1] = pack2<T>(pr[2], pr[3]);
+                    dk[2 * i4] = pack2<T>(ds[0], ds[1]);
+                    dk[2 * i4 + 1] = pack2<T>(ds[2], ds[3]);
+                }
+                store_op_row(pt, m, grp, pk);
+                store_op_row(dst, m, grp, dk);
+            }
+            tc_fence_before();
+            mbar_arrive(sempty);
+            fence_proxy_async_smem();
+            mbar_arrive(opfull);
+        }
+        const bool acc_ok = ok && mbar_wait(accfull, 0, abort_flag, p.err);
+        if (__all_sync(0xffffffffu, acc_ok)) {
+            tc_fence_after();
+            const bool key_ok = kk < nr;
+            const long long row = (long long)bh * g.n + r + (long long)g.s * kk;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
+                const float mul = which ? p.scale : 1.f;
+                T *dst_row = reinterpret_cast<T *>(which ? p.dK : p.dV) + row * 64;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_base + (which ? kColDK : kColDV) + h * 32, v);
+                    tmem_ld_wait();
+                    if (key_ok) {
+                        uint4 *o4 = reinterpret_cast<uint4 *>(dst_row + h * 32);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            o4[u] = make_uint4(
+                                pack2<T>(mul * __uint_as_float(v[8 * u]), mul * __uint_as_float(v[8 * u + 1])),
+                                pack2<T>(mul * __uint_as_float(v[8 * u + 2]), mul * __uint_as_float(v[8 * u + 3])),
+                                pack2<T>(mul * __uint_as_float(v[8 * u + 4]), mul * __uint_as_float(v[8 * u + 5])),
+                                pack2<T>(mul * __uint_as_float(v[8 * u + 6]), mul * __uint_as_float(v[8 * u + 7])));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per 128 queries
+// ---------------------------------------------------------------------------
+constexpr int kSmemDQ = 2 * kTile + kStages * 2 * kTile + 2 * kOpBytes + 1024 + 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_bwd_dq(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
+             const __grid_constant__ TmapSet mapV, const __grid_constant__ TmapSet mapdO,
+             const BwdArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *qtile = base;
+    uint8_t *otile = base + kTile;                        // dO
+    uint8_t *stages = base + 2 * kTile;                   // stage: K chunk, V chunk
+    uint8_t *ds_op = stages + kStages * 2 * kTile;        // 2 x [128 queries x 128 keys]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ds_op + 2 * kOpBytes);
+    uint64_t *qfull = bars;                   // 1
+    uint64_t *kvfull = bars + 1;              // [kStages]
+    uint64_t *kvempty = kvfull + kStages;     // [kStages]
+    uint64_t *sfull = kvempty + kStages;      // 1
+    uint64_t *sempty = sfull + 1;             // 1, count 128
+    uint64_t *dsfull = sempty + 1;            // [2], count 128
+    uint64_t *dsempty = dsfull + 2;           // [2]
+    uint64_t *accfull = dsempty + 2;          // 1
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(accfull + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const Geom &g = p.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.y, bh = blockIdx.z;
+    const int nr = residue_len(g.n, g.s, r);
+    const int a0 = blockIdx.x * kB;  // first query (sub-index)
+    if (a0 >= nr) return;
+    const int kb_lo = max(a0 - g.w, 0);
+    const int kb_hi = min(a0 + kB - 1 + g.wu, nr - 1);
+    const int nck = (kb_hi - kb_lo + kB) / kB;
+
+    if (threadIdx.x == 0) {
+        mbar_init(qfull, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&kvfull[i], 1);
+            mbar_init(&kvempty[i], 1);
+        }
+        mbar_init(sfull, 1);
+        mbar_init(sempty, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&dsfull[i], 128);
+            mbar_init(&dsempty[i], 1);
+        }
+        mbar_init(accfull, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const CUtensorMap *mq = &mapQ.m[r], *mk = &mapK.m[r], *mv = &mapV.m[r],
+                              *mo = &mapdO.m[r];
+            mbar_arrive_expect_tx(qfull, 2 * kTile);
+            tma_load_3d(qtile, mq, qfull, 0, a0, bh);
+            tma_load_3d(otile, mo, qfull, 0, a0, bh);
+            for (int c = 0; c < nck; ++c) {
+                const int st = c % kStages;
+                const uint32_t ph = (c / kStages) & 1;
+                if (!mbar_wait(&kvempty[st], ph ^ 1, abort_flag, p.err)) break;
+                mbar_arrive_expect_tx(&kvfull[st], 2 * kTile);
+                uint8_t *sk = stages + st * 2 * kTile;
+                tma_load_3d(sk, mk, &kvfull[st], 0, kb_lo + c * kB, bh);
+                tma_load_3d(sk + kTile, mv, &kvfull[st], 0, kb_lo + c * kB, bh);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr bool kBf16 = !std::is_same<T, __half>::value;
+            const uint32_t id_s = idesc_f16(kB, kB, kBf16, false, false);
+            const uint32_t id_g = idesc_f16(kB, 64, kBf16, false, true);
+            const uint32_t q_addr = smem_u32(qtile), o_addr = smem_u32(otile);
+            bool ok = mbar_wait(qfull, 0, abort_flag, p.err);
+            auto issue_dq = [&](int c) -> bool {
+                const int st = c % kStages;
+                const int b = c & 1;
+                const uint32_t bph = (c >> 1) & 1;
+                if (!mbar_wait(&dsfull[b], bph, abort_flag, p.err)) return false;
+                tc_fence_after();
+                const uint32_t k_addr = smem_u32(stages + st * 2 * kTile);
+                mma_op_by_rows(tmem + kColDQ, smem_u32(ds_op + b * kOpBytes), k_addr, id_g, c > 0);
+                mma_commit(&dsempty[b]);
+                mma_commit(&kvempty[st]);
+                return true;
+            };
+            for (int c = 0; c < nck && ok; ++c) {
+                const int st = c % kStages;
+                const uint32_t ph = (c / kStages) & 1;
+                ok = mbar_wait(&kvfull[st], ph, abort_flag, p.err) &&
+                     mbar_wait(sempty, (c & 1) ^ 1, abort_flag, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t k_addr = smem_u32(stages + st * 2 * kTile);
+                mma_tiles(tmem + kColS, q_addr, k_addr, id_s);           // S  = Q K_c^T
+                mma_tiles(tmem + kColDP, o_addr, k_addr + kTile, id_s);  // dP = dO V_c^T
+                mma_commit(sfull);
+                if (c > 0) ok = issue_dq(c - 1);
+            }
+            if (ok && issue_dq(nck - 1)) mma_commit(accfull);
+        }
+    } else {
+        // ---------------- workers: thread = query row ----------------
+        const int quarter = warp & 3;
+        const int q = quarter * 32 + lane;
+        const int qq = a0 + q;
+        const float xscale = p.scale * kLog2e;
+        float l2 = INFINITY, dl = 0.f;
+        const long long row = (long long)bh * g.n + r + (long long)g.s * qq;
+        if (qq < nr) {
+            l2 = p.lse[row] * kLog2e;
+            dl = p.delta[row];
+        }
+        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
+        bool ok = true;
+        for (int c = 0; c < nck; ++c) {
+            const int b = c & 1;
+            const uint32_t bph = (c >> 1) & 1;
+            const int kbase = kb_lo + c * kB;
+            const int jlo = max(qq - g.w - kbase, 0);
+            const int jhi = min(min(qq + g.wu, kb_hi) - kbase, kB - 1);
+            const bool q_ok = qq < nr;
+            const bool full = __all_sync(0xffffffffu, q_ok && jlo == 0 && jhi == kB - 1);
+            bool w_ok = mbar_wait(sfull, c & 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+            tc_fence_after();
+            w_ok = mbar_wait(&dsempty[b], bph ^ 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+            const uint32_t dsa = smem_u32(ds_op + b * kOpBytes);
+#pragma unroll 1
+            for (int grp = 0; grp < 4; ++grp) {
+                uint32_t sv[32], dv[32];
+                tmem_ld32(lane_base + kColS + grp * 32, sv);
+                tmem_ld32(lane_base + kColDP + grp * 32, dv);
+                tmem_ld_wait();
+                uint32_t dk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float ds[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float y = fmaf(__uint_as_float(sv[2 * i + h]), xscale, -l2);
+                        if (!full) {
+                            const int j = grp * 32 + 2 * i + h;
+                            if (!q_ok || j < jlo || j > jhi) y = -INFINITY;
+                        }
+                        ds[h] = ex2(y) * (__uint_as_float(dv[2 * i + h]) - dl);
+                    }
+                    dk[i] = pack2<T>(ds[0], ds[1]);
+                }
+                store_op_row(dsa, q, grp, dk);
+            }
+            tc_fence_before();
+            mbar_arrive(sempty);
+            fence_proxy_async_smem();
+            mbar_arrive(&dsfull[b]);
+        }
+        const bool acc_ok = ok && mbar_wait(accfull, 0, abort_flag, p.err);
+        if (__all_sync(0xffffffffu, acc_ok)) {
+            tc_fence_after();
+            T *dst_row = reinterpret_cast<T *>(p.dQ) + row * 64;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + kColDQ + h * 32, v);
+                tmem_ld_wait();
+                if (qq < nr) {
+                    const float mul = p.scale;
+                    uint4 *o4 = reinterpret_cast<uint4 *>(dst_row + h * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        o4[u] = make_uint4(
+                            pack2<T>(mul * __uint_as_float(v[8 * u]), mul * __uint_as_float(v[8 * u + 1])),
+                            pack2<T>(mul * __uint_as_float(v[8 * u + 2]), mul * __uint_as_float(v[8 * u + 3])),
+                            pack2<T>(mul * __uint_as_float(v[8 * u + 4]), mul * __uint_as_float(v[8 * u + 5])),
+                            pack2<T>(mul * __uint_as_float(v[8 * u + 6]), mul * __uint_as_float(v[8 * u + 7])));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// exact fp32 path: one CTA per row, one thread per channel; the backward of the
+// fp32 fused forward, recomputing each slot's probability from lse.
+//   dQ pass (rows = queries), then dK / dV pass (rows = keys).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_dot(float x, float *part) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    if (lane == 0) part[wid] = x;
+    __syncthreads();
+    float s = 0.f;
+    for (int k = 0; k < nw; ++k) s += part[k];
+    __syncthreads();
+    return s;
+}
+
+__global__ void __launch_bounds__(128) k_bwd_f32(const BwdArgs p, int pass) {
+    const Geom &g = p.g;
+    const long long R = blockIdx.x;
+    const int x = (int)(R % g.n);
+    const long long bh = R / g.n;
+    const int c = threadIdx.x;
+    __shared__ float part[4];
+    const float *Q = reinterpret_cast<const float *>(p.Q) + bh * g.n * g.hd;
+    const float *K = reinterpret_cast<const float *>(p.K) + bh * g.n * g.hd;
+    const float *V = reinterpret_cast<const float *>(p.V) + bh * g.n * g.hd;
+    const float *dO = reinterpret_cast<const float *>(p.dO) + bh * g.n * g.hd;
+    const float *lse = p.lse + bh * g.n;
+    const float *delta = p.delta + bh * g.n;
+    const bool on = c < g.hd;
+    float acc_a = 0.f, acc_b = 0.f;
+    for (int t = 0; t < g.D; ++t) {
+        // pass 0: x is the query, the key is j;  pass 1: x is the key, the query is i
+        const long long y = pass == 0 ? (long long)x + (long long)(t - g.w) * g.s
+                                      : (long long)x - (long long)(t - g.w) * g.s;
+        if (y < 0 || y >= g.n) continue;
+        const long long i = pass == 0 ? x : y, j = pass == 0 ? y : x;
+        const float sdot = block_dot(on ? Q[i * g.hd + c] * K[j * g.hd + c] : 0.f, part);
+        const float pdot = block_dot(on ? dO[i * g.hd + c] * V[j * g.hd + c] : 0.f, part);
+        const float pr = expf(p.scale * sdot - lse[i]);
+        const float ds = pr * (pdot - delta[i]);
+        if (!on) continue;
+        if (pass == 0) {
+            acc_a = fmaf(ds, K[j * g.hd + c], acc_a);
+        } else {
+            acc_a = fmaf(ds, Q[i * g.hd + c], acc_a);   // dK
+            acc_b = fmaf(pr, dO[i * g.hd + c], acc_b);  // dV
+        }
+    }
+    if (!on) return;
+    if (pass == 0) {
+        reinterpret_cast<float *>(p.dQ)[R * g.hd + c] = p.scale * acc_a;
+    } else {
+        reinterpret_cast<float *>(p.dK)[R * g.hd + c] = p.scale * acc_a;
+        reinterpret_cast<float *>(p.dV)[R * g.hd + c] = acc_b;
+    }
+}
+
+__global__ void __launch_bounds__(128) k_bwd_delta_f32(const BwdArgs p) {
+    const long long R = blockIdx.x;
+    const int c = threadIdx.x;
+    __shared__ float part[4];
+    const float *O = reinterpret_cast<const float *>(p.O) + R * p.g.hd;
+    const float *dO = reinterpret_cast<const float *>(p.dO) + R * p.g.hd;
+    const float v = block_dot(c < p.g.hd ? O[c] * dO[c] : 0.f, part);
+    if (c == 0) p.delta[R] = v;
+}
+
+template <typename T>
+cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const TmapSet &mo,
+                     const BwdArgs &a, cudaStream_t st) {
+    const long long rows = (long long)a.g.BH * a.g.n;
+    k_bwd_delta<T><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int tiles = (a.g.nsub + kB - 1) / kB;
+    dim3 grid(tiles, a.g.s, a.g.BH);
+    e = cudaFuncSetAttribute(k_bwd_dkdv<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDKDV);
+    if (e != cudaSuccess) return e;
+    k_bwd_dkdv<T><<<grid, kThreads, kSmemDKDV, st>>>(mq, mk, mv, mo, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_bwd_dq<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDQ);
+    if (e != cudaSuccess) return e;
+    k_bwd_dq<T><<<grid, kThreads, kSmemDQ, st>>>(mq, mk, mv, mo, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const TmapSet &mk,
+                                         const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,
+                                         cudaStream_t st) {
+    if (dt == kF16) return launch_t<__half>(mq, mk, mv, mo, a, st);
+    return launch_t<__nv_bfloat16>(mq, mk, mv, mo, a, st);
+}
+
+cudaError_t launch_band_attention_bwd_f32(const BwdArgs &a, cudaStream_t st) {
+    const long long rows = (long long)a.g.BH * a.g.n;
+    const int threads = ((a.g.hd + 31) / 32) * 32;
+    k_bwd_delta_f32<<<(unsigned)rows, threads, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_bwd_f32<<<(unsigned)rows, threads, 0, st>>>(a, 0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_bwd_f32<<<(unsigned)rows, threads, 0, st>>>(a, 1);
+    return cudaGetLastError();
+}
+
+}  // namespace swab

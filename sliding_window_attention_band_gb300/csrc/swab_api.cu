@@ -17,6 +17,22 @@ __device__ unsigned g_status_word;
 
 namespace {
 
+// Self-test of the bounded wait every pipelined kernel uses: one warp waits on
+// an mbarrier that nothing ever arrives at.  The wait must give up after
+// `limit_ns`, record SWAB_ERR_TIMEOUT in the status word and return.
+__global__ void k_selftest_wait(unsigned *err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, &abort_flag, err, limit_ns);
+    __syncthreads();
+}
+
 const char *const kStatusNames[] = {
     "SWAB_OK", "SWAB_ERR_INVALID_ARG", "SWAB_ERR_UNSUPPORTED",
     "SWAB_ERR_MISALIGNED", "SWAB_ERR_CUDA", "SWAB_ERR_TIMEOUT",
@@ -208,6 +224,14 @@ SWAB_API const char *swab_status_string(swab_status status) {
     return kStatusNames[k];
 }
 
+SWAB_API swab_status swab_selftest_wait_timeout(uint32_t limit_us, void *stream) {
+    if (limit_us == 0 || limit_us > 1000000u) return SWAB_ERR_INVALID_ARG;
+    unsigned *err = status_word();
+    if (!err) return SWAB_ERR_CUDA;
+    k_selftest_wait<<<1, 32, 0, as_stream(stream)>>>(err, 1000ull * limit_us);
+    return from_cuda(cudaGetLastError());
+}
+
 SWAB_API swab_status swab_device_status(int32_t *flags, int32_t reset) {
     if (!flags) return SWAB_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return SWAB_ERR_CUDA;
@@ -358,6 +382,33 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
     if (!err) return SWAB_ERR_CUDA;
     AttnArgs a{g, scale, O, lse, err};
     return from_cuda(launch_band_attention_tc(dt, mq, mk, mv, a, as_stream(stream)));
+}
+
+SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc) {
+    if (!desc || desc->b < 1 || desc->h < 1 || desc->n < 1) return 0;
+    return (size_t)desc->b * desc->h * desc->n * sizeof(float);
+}
+
+SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, const void *Q,
+                                        const void *K, const void *V, const void *O,
+                                        const void *dO, const float *lse, void *dQ, void *dK,
+                                        void *dV, void *workspace, void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    if ((s = check_ptrs({Q, K, V, O, dO, lse, dQ, dK, dV, workspace})) != SWAB_OK) return s;
+    cudaStream_t st = as_stream(stream);
+    BwdArgs a{g, scale, Q, K, V, O, dO, lse, static_cast<float *>(workspace), dQ, dK, dV, nullptr};
+    if (dt == kF32) return from_cuda(launch_band_attention_bwd_f32(a, st));
+    TmapSet mq, mk, mv, mo;
+    if (!build_rows_maps(&mq, Q, g, dt, kQKBoxRows) || !build_rows_maps(&mk, K, g, dt, kQKBoxRows) ||
+        !build_rows_maps(&mv, V, g, dt, kQKBoxRows) || !build_rows_maps(&mo, dO, g, dt, kQKBoxRows))
+        return SWAB_ERR_CUDA;
+    a.err = status_word();
+    if (!a.err) return SWAB_ERR_CUDA;
+    return from_cuda(launch_band_attention_bwd_tc(dt, mq, mk, mv, mo, a, st));
 }
 
 }  // extern "C"

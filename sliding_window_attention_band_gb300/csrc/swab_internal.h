@@ -107,6 +107,16 @@ struct AttnArgsF32 {  // fused forward, fp32 path
     float *lse;
 };
 
+struct BwdArgs {      // fused backward
+    Geom g;
+    float scale;
+    const void *Q, *K, *V, *O, *dO;
+    const float *lse;
+    float *delta;     // workspace [BH, n]
+    void *dQ, *dK, *dV;
+    unsigned *err;
+};
+
 struct DenseArgs {    // fp32 FFMA path
     Geom g;
     float alpha;
@@ -125,6 +135,10 @@ size_t gather_smem_bytes(int n, int G);     // total shared memory of the gather
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                      const TmapSet &mapV, const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st);
+cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const TmapSet &mk,
+                                         const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,
+                                         cudaStream_t st);
+cudaError_t launch_band_attention_bwd_f32(const BwdArgs &a, cudaStream_t st);
 // fp32 FFMA paths
 cudaError_t launch_band_qk_f32(const DenseArgs &a, cudaStream_t st);
 cudaError_t launch_band_pv_f32(const DenseArgs &a, cudaStream_t st);
