@@ -64,6 +64,7 @@ extern "C" {
 
 #define SWAB_MAX_GLOBAL 256  /* most global tokens per call */
 #define SWAB_MAX_DILATION 15 /* key stride at most 16 */
+#define SWAB_NOALLOC_MAX_ROWS (1u << 22) /* b*h*n limit of band_attention_bwd_noalloc */
 
 typedef enum swab_status {
     SWAB_OK = 0,
@@ -174,6 +175,31 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
 
 /* Bytes of workspace band_attention_bwd needs for `desc` (0 if desc is NULL). */
 SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc);
+
+/* band_attention_bwd for callers that cannot allocate device memory: the same
+ * computation, arguments and results, minus the workspace.  Some callers have
+ * no way to obtain a device buffer of their own -- code running under an
+ * allocator or memory pool they do not control, plugins handed only input and
+ * output pointers, or contexts where a cudaMalloc would synchronise or is
+ * forbidden -- so this variant keeps its per-row scratch in a module-scope
+ * device array of SWAB_NOALLOC_MAX_ROWS floats (16 MiB), which every GPU that
+ * loads the library holds until the process exits.  Nothing is allocated or
+ * freed by the call (no cudaMalloc, cudaFree or allocating library routine).
+ *   - b*h*n must not exceed SWAB_NOALLOC_MAX_ROWS; larger problems return
+ *     SWAB_ERR_UNSUPPORTED (use band_attention_bwd with a workspace).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (every call overwrites what it reads before reading it).  Calls whose
+ *     executions overlap on the GPU -- on different streams, or from different
+ *     threads without ordering -- race on it; serialise them.
+ * The pages have no counterpart for this entry point: it only changes where
+ * the library's own scratch lives. */
+SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float scale, const void *Q,
+                                                const void *K, const void *V, const void *O,
+                                                const void *dO, const float *lse, void *dQ,
+                                                void *dK, void *dV, void *stream);
 
 /* Human-readable name of a status code (static string). */
 SWAB_API const char *swab_status_string(swab_status status);

@@ -6,7 +6,8 @@ ctypes binding over it plus the seeded input generators.  Nothing here
 computes attention on the host.
 """
 from ._binding import (API_FUNCTIONS, Desc, SwabError, band_attention,  # noqa: F401
-                       band_attention_bwd, band_attention_bwd_workspace, band_pv,
+                       band_attention_bwd, band_attention_bwd_noalloc,
+                       band_attention_bwd_workspace, band_pv,
                        band_pv_bwd_t, band_qk, band_qk_bwd_t, band_softmax, band_softmax_bwd,
                        device_status, library_path, load, selftest_wait_timeout,
                        status_string, version)
@@ -14,6 +15,7 @@ from .inputs import WORKLOADS, Workload, seeded_qkvo, workload_inputs  # noqa: F
 
 __all__ = ["Desc", "SwabError", "band_qk", "band_softmax", "band_pv", "band_qk_bwd_t",
            "band_pv_bwd_t", "band_softmax_bwd", "band_attention", "band_attention_bwd",
+           "band_attention_bwd_noalloc",
            "band_attention_bwd_workspace", "device_status", "selftest_wait_timeout", "load",
            "library_path", "version", "status_string", "WORKLOADS", "Workload",
            "seeded_qkvo", "workload_inputs"]

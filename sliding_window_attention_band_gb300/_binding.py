@@ -26,7 +26,8 @@ _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 # every symbol the header declares
 API_FUNCTIONS = ("band_qk", "band_softmax", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
                  "band_softmax_bwd", "band_attention", "band_attention_bwd",
-                 "band_attention_bwd_workspace", "swab_status_string", "swab_device_status",
+                 "band_attention_bwd_workspace", "band_attention_bwd_noalloc",
+                 "swab_status_string", "swab_device_status",
                  "swab_selftest_wait_timeout", "swab_version")
 
 
@@ -117,6 +118,7 @@ def load():
                 "band_softmax_bwd": [D, P, Gp, P, Gp, P, Gp, P],
                 "band_attention": [D, f, P, P, P, P, P, P],
                 "band_attention_bwd": [D, f, P, P, P, P, P, P, P, P, P, P, P],
+                "band_attention_bwd_noalloc": [D, f, P, P, P, P, P, P, P, P, P, P],
                 "swab_device_status": [ctypes.POINTER(i32), i32],
                 "swab_selftest_wait_timeout": [ctypes.c_uint32, P],
             }
@@ -301,6 +303,24 @@ def selftest_wait_timeout(limit_us: int = 20000, stream=None):
     if s is None and torch.cuda.is_available():
         s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     _call("swab_selftest_wait_timeout", int(limit_us), s)
+
+
+NOALLOC_MAX_ROWS = 1 << 22
+
+
+def band_attention_bwd_noalloc(desc: Desc, scale, Q, K, V, O, dO, lse, dQ, dK, dV, stream=None):
+    """band_attention_bwd without a workspace argument, for callers that cannot
+    allocate device memory: the library keeps the per-row scratch in a
+    module-scope device array (b*h*n <= NOALLOC_MAX_ROWS).  Calls that overlap
+    on the GPU share that array and race; the first call on a device resolves
+    the array's address and should come before any stream capture."""
+    for n_, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO), ("dQ", dQ), ("dK", dK),
+                  ("dV", dV)):
+        _check_shape(n_, t, _dense(desc), desc.dtype)
+    _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
+    _call("band_attention_bwd_noalloc", ctypes.byref(desc.c), float(scale), _ptr(Q), _ptr(K),
+          _ptr(V), _ptr(O), _ptr(dO), _ptr(lse), _ptr(dQ), _ptr(dK), _ptr(dV),
+          _stream(stream, dQ))
 
 
 def device_status(reset: bool = True) -> int:

@@ -22,11 +22,42 @@
 // The dense tiles staged by TMA serve twice: K-major as the K=64 operand of
 // the score products and MN-major (rows along K) as the B operand of the
 // gradient products.
+#include <mutex>
 #include <type_traits>
 
 #include "swab_internal.h"
 
 namespace swab {
+
+// Device scratch for band_attention_bwd_noalloc: the per-row delta that the
+// regular entry point keeps in a caller-provided workspace.  It is a
+// module-scope array, so every GPU that loads the library holds it (16 MiB)
+// until the process exits, and every call of that entry point on a device
+// shares it.
+static __device__ __align__(256) float g_noalloc_delta[SWAB_NOALLOC_MAX_ROWS];
+
+// Device address of g_noalloc_delta on the current device.  In host code the
+// array's name only stands in for the symbol, so the address is looked up
+// with cudaGetSymbolAddress, once per device (the first call on a device does
+// it) and cached.
+cudaError_t noalloc_delta_scratch(float **out) {
+    static std::mutex mu;
+    static float *cache[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_delta);
+        if (e != cudaSuccess) return e;
+        cache[dev] = static_cast<float *>(ptr);
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
 namespace {
 
 constexpr int kB = 128;           // rows per CTA and per chunk

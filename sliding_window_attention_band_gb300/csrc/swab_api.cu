@@ -411,4 +411,29 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
     return from_cuda(launch_band_attention_bwd_tc(dt, mq, mk, mv, mo, a, st));
 }
 
+SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float scale, const void *Q,
+                                                const void *K, const void *V, const void *O,
+                                                const void *dO, const float *lse, void *dQ,
+                                                void *dK, void *dV, void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
+    if ((long long)g.BH * g.n > (long long)SWAB_NOALLOC_MAX_ROWS) return SWAB_ERR_UNSUPPORTED;
+    if ((s = check_ptrs({Q, K, V, O, dO, lse, dQ, dK, dV})) != SWAB_OK) return s;
+    float *scratch = nullptr;
+    if (noalloc_delta_scratch(&scratch) != cudaSuccess) return SWAB_ERR_CUDA;
+    cudaStream_t st = as_stream(stream);
+    BwdArgs a{g, scale, Q, K, V, O, dO, lse, scratch, dQ, dK, dV, nullptr};
+    if (dt == kF32) return from_cuda(launch_band_attention_bwd_f32(a, st));
+    TmapSet mq, mk, mv, mo;
+    if (!build_rows_maps(&mq, Q, g, dt, kQKBoxRows) || !build_rows_maps(&mk, K, g, dt, kQKBoxRows) ||
+        !build_rows_maps(&mv, V, g, dt, kQKBoxRows) || !build_rows_maps(&mo, dO, g, dt, kQKBoxRows))
+        return SWAB_ERR_CUDA;
+    a.err = status_word();
+    if (!a.err) return SWAB_ERR_CUDA;
+    return from_cuda(launch_band_attention_bwd_tc(dt, mq, mk, mv, mo, a, st));
+}
+
 }  // extern "C"
