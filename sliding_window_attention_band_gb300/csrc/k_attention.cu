@@ -18,13 +18,16 @@
 //      pass over tensor memory; p = 2^(x - m) rounded to fp16/bf16 is written
 //      as the K-major, 128-B-swizzled A operand of the next product (smem);
 //   3. MMA warp: O_c = P_c . V_c into TMEM O buffer c%2 (fresh, not
-//      accumulated);
+//      accumulated), split along the keys into two halves with their own
+//      buffers, one per softmax warp half;
 //   4. softmax warps, one chunk later (so the P.V product of chunk c runs
 //      while chunk c+1's softmax is computed): acc = acc * 2^(m_prev - m) + O_c.
 // At the end O = acc / l, lse = m*ln2 + ln l.
 //
 // Warps: 0 = TMA producer (Q once; K and V chunks into a 3-stage ring),
-// 1 = TMEM owner + MMA issuer, 2..5 = softmax / epilogue.
+// 1 = TMEM owner + MMA issuer, 2..9 = softmax / epilogue (two per TMEM lane
+// quarter, each owning one key half of every chunk; the halves merge their
+// running max, sum and accumulator once, at the end).
 #include <type_traits>
 
 #include "swab_internal.h"
@@ -35,20 +38,25 @@ namespace {
 constexpr int kBQ = 128;      // queries per CTA (M)
 constexpr int kBK = 128;      // keys per chunk (N of S, K of P.V)
 constexpr int kStages = 3;    // K/V ring
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // producer, MMA, 8 softmax warps (2 per TMEM lane quarter)
+constexpr int kWorkers = 256;
 constexpr int kQBytes = kBQ * 128;             // 16 KB
 constexpr int kKBytes = kBK * 128;             // 16 KB
 constexpr int kVBytes = kBK * 128;             // 16 KB
 constexpr int kStageBytes = kKBytes + kVBytes; // 32 KB
 constexpr int kPBytes = kBQ * kBK * 2;         // 32 KB (two 64-key K-atoms)
 constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + 2 * kPBytes + 1024 + 1024;
-constexpr uint32_t kTmemCols = 512;            // S: 2 x 128, O: 2 x 64
-constexpr uint32_t kTmemO = 256;               // column of the first O buffer
+constexpr uint32_t kTmemCols = 512;            // S: 2 x 128, O: 2 chunks x 2 key halves x 64
+constexpr uint32_t kTmemO = 256;               // O of chunk parity b, key half h at 256 + 128b + 64h
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 template <typename T>
@@ -92,11 +100,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&sempty[i], 128);
-            mbar_init(&pfull[i], 128);
+            mbar_init(&sempty[i], kWorkers);
+            mbar_init(&pfull[i], kWorkers);
             mbar_init(&pempty[i], 1);
             mbar_init(&ofull[i], 1);
-            mbar_init(&oempty[i], 128);
+            mbar_init(&oempty[i], kWorkers);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -145,13 +153,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t p_addr = smem_u32(pbuf + b * kPBytes);
                 const uint32_t v_addr = smem_u32(kv + st * kStageBytes + kKBytes);
-                const uint32_t d = tmem + kTmemO + b * 64;
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k) {
-                    // A (P): two 64-key K-atoms of 16 KB; 32 B per K=16 step inside one.
-                    const uint32_t a = p_addr + (k >> 2) * (kPBytes / 2) + (k & 3) * 32;
-                    mma_f16_ss(d, sdesc_sw128(a, 16, 1024),
-                               sdesc_sw128(v_addr + 2048 * k, 1024, 1024), idesc_o, k > 0);
+                for (int h = 0; h < 2; ++h) {
+                    // keys [64h, 64h + 64): K-atom h of P, rows 64h.. of V
+                    const uint32_t d = tmem + kTmemO + b * 128 + h * 64;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t a = p_addr + h * (kPBytes / 2) + k * 32;
+                        mma_f16_ss(d, sdesc_sw128(a, 16, 1024),
+                                   sdesc_sw128(v_addr + h * 8192 + 2048 * k, 1024, 1024), idesc_o, k > 0);
+                    }
                 }
                 mma_commit(&ofull[b]);
                 mma_commit(&pempty[b]);
@@ -180,16 +191,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- softmax warps: thread = query row ----------------
-        // Per row: a reference max m (log2 units) and the sum l of
-        // p = 2^(x - m) over the keys seen so far.  A chunk is processed in
-        // ONE pass over tensor memory with the current m; m is raised only
-        // when the chunk's largest score exceeds it by more than kSlack (then
-        // the chunk is redone with the new m), so p <= 2^kSlack stays well
-        // inside fp16/bf16 range.  Rows with no key seen yet take their m from
-        // a max-only pass first.  The softmax does not depend on the choice of
-        // m: O = acc / l and lse = m ln2 + ln l use the same m.
+        // Two warps per TMEM lane quarter: warp half h owns key columns
+        // [64h, 64h + 64) of every chunk and keeps its own reference max m,
+        // sum l and accumulator (its P.V half goes to its own TMEM buffer), so
+        // the halves never wait on each other until the final merge.
+        // Per half: a chunk is processed in ONE pass over tensor memory with
+        // the current m; m is raised only when the chunk's largest score
+        // exceeds it by more than kSlack (the chunk is then redone with the
+        // new m), so p <= 2^kSlack stays well inside fp16/bf16 range.  A half
+        // with no key seen yet takes its m from a max-only pass first.  The
+        // softmax does not depend on the choice of m.
         constexpr float kSlack = 8.f;
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int q = quarter * 32 + lane;
         const int qq = a0 + q;
         const float xscale = p.scale * 1.4426950408889634f;
@@ -209,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t v[32];
-                tmem_ld32(lane_base + kTmemO + b * 64 + h * 32, v);
+                tmem_ld32(lane_base + kTmemO + b * 128 + half * 64 + h * 32, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) acc[h * 32 + i] = fmaf(acc[h * 32 + i], corr, __uint_as_float(v[i]));
@@ -226,17 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // this row's band inside the chunk: columns [jlo, jhi]
             const int jlo = max(qq - g.w - kbase, 0);
             const int jhi = min(min(qq + g.wu, kb_hi) - kbase, kBK - 1);
-            const bool full = __all_sync(0xffffffffu, jlo == 0 && jhi == kBK - 1);
+            const bool full = __all_sync(0xffffffffu, jlo <= 64 * half && jhi >= 64 * half + 63);
             bool w_ok = mbar_wait(&sfull[b], bph, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sbuf = lane_base + b * kBK;
             float mref = m;
             if (__any_sync(0xffffffffu, m == -INFINITY)) {
-                // rows with no key yet: the chunk's own max
                 float mx = -INFINITY;
 #pragma unroll 1
-                for (int grp = 0; grp < 4; ++grp) {
+                for (int grp = 2 * half; grp < 2 * half + 2; ++grp) {
                     uint32_t v[32];
                     tmem_ld32(sbuf + grp * 32, v);
                     tmem_ld_wait();
@@ -258,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float ymax = -INFINITY;  // chunk max relative to mref
                 lc = 0.f;
 #pragma unroll 1
-                for (int grp = 0; grp < 4; ++grp) {
+                for (int grp = 2 * half; grp < 2 * half + 2; ++grp) {
                     uint32_t v[32];
                     tmem_ld32(sbuf + grp * 32, v);
                     tmem_ld_wait();
@@ -304,18 +317,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             corr_prev = corr;
         }
         if (ok) ok = fold_o(nck - 1, corr_prev);
-        if (ok && qq < nr) {
-            const float inv = 1.f / l;
-            T *out = reinterpret_cast<T *>(p.O) + ((long long)bh * g.n + r + (long long)g.s * qq) * 64;
+        // merge the two key halves: every P.V product is complete, so the P
+        // tiles are free to carry each half's (m, l) and the accumulator
+        // channels the other half writes out
+        float *xs = reinterpret_cast<float *>(pbuf);  // [2 halves][128 rows][34]
+        const bool all_ok = __all_sync(0xffffffffu, ok);
+        // static register indices only: split acc by half with branches
+        float keep[32], give[32];
+        if (half == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                keep[i] = acc[i];
+                give[i] = acc[32 + i];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                keep[i] = acc[32 + i];
+                give[i] = acc[i];
+            }
+        }
+        if (all_ok) {
+            float *mine = xs + (half * kBQ + q) * 34;
+            mine[0] = m;
+            mine[1] = l;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mine[2 + i] = give[i];
+        }
+        named_bar_sync(1, kWorkers);
+        if (all_ok && qq < nr) {
+            const float *other = xs + ((1 - half) * kBQ + q) * 34;
+            const float pm = other[0], pl = other[1];
+            const float M = fmaxf(m, pm);
+            const float f = m == -INFINITY ? 0.f : ex2(m - M);
+            const float pf = pm == -INFINITY ? 0.f : ex2(pm - M);
+            const float inv = 1.f / (l * f + pl * pf);
+            T *out = reinterpret_cast<T *>(p.O) + ((long long)bh * g.n + r + (long long)g.s * qq) * 64 +
+                     half * 32;
             uint4 *o4 = reinterpret_cast<uint4 *>(out);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                o4[u] = make_uint4(pack2<T>(acc[8 * u] * inv, acc[8 * u + 1] * inv),
-                                   pack2<T>(acc[8 * u + 2] * inv, acc[8 * u + 3] * inv),
-                                   pack2<T>(acc[8 * u + 4] * inv, acc[8 * u + 5] * inv),
-                                   pack2<T>(acc[8 * u + 6] * inv, acc[8 * u + 7] * inv));
+            for (int u = 0; u < 4; ++u) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    y[e] = (keep[8 * u + e] * f + other[2 + 8 * u + e] * pf) * inv;
+                o4[u] = make_uint4(pack2<T>(y[0], y[1]), pack2<T>(y[2], y[3]), pack2<T>(y[4], y[5]),
+                                   pack2<T>(y[6], y[7]));
             }
-            if (p.lse) p.lse[(long long)bh * g.n + r + (long long)g.s * qq] = m * 0.6931471805599453f + logf(l);
+            if (p.lse && half == 0)
+                p.lse[(long long)bh * g.n + r + (long long)g.s * qq] =
+                    M * 0.6931471805599453f + logf(l * f + pl * pf);
         }
     }
     tc_fence_before();

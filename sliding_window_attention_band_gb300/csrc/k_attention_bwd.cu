@@ -61,7 +61,8 @@ cudaError_t noalloc_delta_scratch(float **out) {
 namespace {
 
 constexpr int kB = 128;           // rows per CTA and per chunk
-constexpr int kThreads = 192;     // producer, MMA, 4 worker warps
+constexpr int kThreads = 320;     // producer, MMA, 8 worker warps (2 per TMEM lane quarter)
+constexpr int kWorkers = 256;
 constexpr int kTile = kB * 128;   // 16 KB: 128 rows x 64 halves
 constexpr int kStages = 2;
 constexpr int kOpBytes = kB * kB * 2;  // 32 KB: a 128 x 128 16-bit A operand (two K-atoms)
@@ -112,19 +113,42 @@ __device__ __forceinline__ void mma_tiles(uint32_t d, uint32_t a_addr, uint32_t 
 }
 
 // ---------------------------------------------------------------------------
-// delta_i = dO_i . O_i  (one warp per row; lane holds two of the 64 channels)
+// delta_i = dO_i . O_i: 8 lanes per row, 16-byte loads, each warp keeps 4
+// groups of 4 rows (16 rows, 8 loads per lane) in flight before reducing.
 // ---------------------------------------------------------------------------
+constexpr int kDeltaRowsPerWarp = 16;
+
 template <typename T>
 __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
-    const long long R = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const long long rows = (long long)p.g.BH * p.g.n;
     const int lane = threadIdx.x & 31;
-    if (R >= (long long)p.g.BH * p.g.n) return;
-    const uint32_t o = reinterpret_cast<const uint32_t *>(p.O)[R * 32 + lane];
-    const uint32_t d = reinterpret_cast<const uint32_t *>(p.dO)[R * 32 + lane];
-    float v = lo16<T>(o) * lo16<T>(d) + hi16<T>(o) * hi16<T>(d);
+    const long long warp_row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kDeltaRowsPerWarp;
+    const uint4 *O = reinterpret_cast<const uint4 *>(p.O);
+    const uint4 *dO = reinterpret_cast<const uint4 *>(p.dO);
+    uint4 o[kDeltaRowsPerWarp / 4], d[kDeltaRowsPerWarp / 4];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0) p.delta[R] = v;
+    for (int k = 0; k < kDeltaRowsPerWarp / 4; ++k) {
+        const long long R = warp_row0 + 4 * k + (lane >> 3);
+        if (R < rows) {
+            o[k] = ldg16(O + R * 8 + (lane & 7));
+            d[k] = ldg16(dO + R * 8 + (lane & 7));
+        } else {
+            o[k] = d[k] = make_uint4(0, 0, 0, 0);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kDeltaRowsPerWarp / 4; ++k) {
+        const uint32_t ow[4] = {o[k].x, o[k].y, o[k].z, o[k].w};
+        const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+        float v = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            v = fmaf(lo16<T>(ow[u]), lo16<T>(dw[u]), fmaf(hi16<T>(ow[u]), hi16<T>(dw[u]), v));
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        const long long R = warp_row0 + 4 * k + (lane >> 3);
+        if ((lane & 7) == 0 && R < rows) p.delta[R] = v;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -175,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&qempty[i], 1);
         }
         mbar_init(sfull, 1);
-        mbar_init(sempty, 128);
-        mbar_init(opfull, 128);
+        mbar_init(sempty, kWorkers);
+        mbar_init(opfull, kWorkers);
         mbar_init(opempty, 1);
         mbar_init(accfull, 1);
         *abort_flag = 0;
@@ -246,9 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- workers: thread = key row ----------------
+        // two warps per TMEM lane quarter; warp half h owns query columns
+        // [64h, 64h + 64) of every chunk
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int m = quarter * 32 + lane;
-        const int tid = threadIdx.x - 64;  // 0..127
+        const int tid = threadIdx.x - 64;  // 0..255
         const int kk = a0 + m;             // key sub-index
         const float xscale = p.scale * kLog2e;
         const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
@@ -258,22 +285,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // per-query statistics of this chunk into shared memory
             float *ql = qstat + (c & 1) * 2 * kB;
             {
-                const int qq = qbase + tid;
-                float l2 = INFINITY, dl = 0.f;
-                if (qq < nr) {
-                    const long long row = (long long)bh * g.n + r + (long long)g.s * qq;
-                    l2 = p.lse[row] * kLog2e;
-                    dl = p.delta[row];
-                }
-                ql[tid] = l2;
-                ql[kB + tid] = dl;
+                const int qi = tid & (kB - 1);
+                const int qq = qbase + qi;
+                const long long row = (long long)bh * g.n + r + (long long)g.s * qq;
+                if (tid < kB) ql[qi] = qq < nr ? p.lse[row] * kLog2e : INFINITY;
+                else ql[kB + qi] = qq < nr ? p.delta[row] : 0.f;
             }
-            named_bar(1, 128);
+            named_bar(1, kWorkers);
             // this key's queries inside the chunk: columns [jlo, jhi]
             const int jlo = max(kk - g.wu - qbase, 0);
             const int jhi = min(min(kk + g.w, qb_hi) - qbase, kB - 1);
             const bool key_ok = kk < nr;
-            const bool full = __all_sync(0xffffffffu, key_ok && jlo == 0 && jhi == kB - 1);
+            const bool full = __all_sync(0xffffffffu, key_ok && jlo <= 64 * half && jhi >= 64 * half + 63);
             bool w_ok = mbar_wait(sfull, c & 1, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
             tc_fence_after();
@@ -282,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t pt = smem_u32(pt_op), dst = smem_u32(dst_op);
             const float4 *ql4 = reinterpret_cast<const float4 *>(ql);
 #pragma unroll 1
-            for (int grp = 0; grp < 4; ++grp) {
+            for (int grp = 2 * half; grp < 2 * half + 2; ++grp) {
                 uint32_t sv[32], dv[32];
                 tmem_ld32(lane_base + kColS + grp * 32, sv);
                 tmem_ld32(lane_base + kColDP + grp * 32, dv);
@@ -324,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool key_ok = kk < nr;
             const long long row = (long long)bh * g.n + r + (long long)g.s * kk;
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
+            {
+                const int which = half;  // half 0 writes dV, half 1 writes dK
                 const float mul = which ? p.scale : 1.f;
                 T *dst_row = reinterpret_cast<T *>(which ? p.dK : p.dV) + row * 64;
 #pragma unroll 1
@@ -402,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&kvempty[i], 1);
         }
         mbar_init(sfull, 1);
-        mbar_init(sempty, 128);
+        mbar_init(sempty, kWorkers);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&dsfull[i], 128);
+            mbar_init(&dsfull[i], kWorkers);
             mbar_init(&dsempty[i], 1);
         }
         mbar_init(accfull, 1);
@@ -474,7 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- workers: thread = query row ----------------
+        // two warps per TMEM lane quarter; warp half h owns key columns
+        // [64h, 64h + 64) of every chunk
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int q = quarter * 32 + lane;
         const int qq = a0 + q;
         const float xscale = p.scale * kLog2e;
@@ -493,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int jlo = max(qq - g.w - kbase, 0);
             const int jhi = min(min(qq + g.wu, kb_hi) - kbase, kB - 1);
             const bool q_ok = qq < nr;
-            const bool full = __all_sync(0xffffffffu, q_ok && jlo == 0 && jhi == kB - 1);
+            const bool full = __all_sync(0xffffffffu, q_ok && jlo <= 64 * half && jhi >= 64 * half + 63);
             bool w_ok = mbar_wait(sfull, c & 1, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
             tc_fence_after();
@@ -501,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
             const uint32_t dsa = smem_u32(ds_op + b * kOpBytes);
 #pragma unroll 1
-            for (int grp = 0; grp < 4; ++grp) {
+            for (int grp = 2 * half; grp < 2 * half + 2; ++grp) {
                 uint32_t sv[32], dv[32];
                 tmem_ld32(lane_base + kColS + grp * 32, sv);
                 tmem_ld32(lane_base + kColDP + grp * 32, dv);
@@ -532,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__all_sync(0xffffffffu, acc_ok)) {
             tc_fence_after();
             T *dst_row = reinterpret_cast<T *>(p.dQ) + row * 64;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
+            {
+                const int h = half;  // channels [32h, 32h + 32)
                 uint32_t v[32];
                 tmem_ld32(lane_base + kColDQ + h * 32, v);
                 tmem_ld_wait();
@@ -633,7 +659,8 @@ template <typename T>
 cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const TmapSet &mo,
                      const BwdArgs &a, cudaStream_t st) {
     const long long rows = (long long)a.g.BH * a.g.n;
-    k_bwd_delta<T><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a);
+    const long long per_block = 8LL * kDeltaRowsPerWarp;
+    k_bwd_delta<T><<<(unsigned)((rows + per_block - 1) / per_block), 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int tiles = (a.g.nsub + kB - 1) / kB;
