@@ -5,29 +5,34 @@
 // exp of the difference, sum, divide, fp32) from nvFuser issue "HuggingFace
 // BertForMaskedLM - Log Softmax Fusion with Autocast has bad perf", fusion 1.
 //
-// One CTA = 128 query rows of one residue r of the key stride (rows
-// r + s*a, a in [a0, a0+128)).  The keys its band touches are walked 128 at
-// a time; for chunk c:
-//   1. MMA warp: S_c = Q . K_c^T  (tcgen05, M = 128 queries, N = 128 keys,
-//      K = 64) into TMEM S buffer c%2;
-//   2. softmax warps (thread = query row = TMEM lane): the band is a
-//      contiguous column interval of the chunk for each row (masking is two
-//      compares, skipped when the whole chunk is inside every row's band).
-//      Online softmax in the log2 domain with a reference max that is raised
-//      only when a chunk exceeds it by more than 2^8, so each chunk is one
-//      pass over tensor memory; p = 2^(x - m) rounded to fp16/bf16 is written
-//      as the K-major, 128-B-swizzled A operand of the next product (smem);
-//   3. MMA warp: O_c = P_c . V_c into TMEM O buffer c%2 (fresh, not
-//      accumulated), split along the keys into two halves with their own
-//      buffers, one per softmax warp half;
-//   4. softmax warps, one chunk later (so the P.V product of chunk c runs
-//      while chunk c+1's softmax is computed): acc = acc * 2^(m_prev - m) + O_c.
-// At the end O = acc / l, lse = m*ln2 + ln l.
+// Work unit ("tile") = 128 query rows of one residue r of the key stride
+// (rows r + s*a, a in [a0, a0+128)).  The kernel is persistent: one CTA per
+// SM walks the tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...; a per-CTA
+// chunk counter runs across tiles, so the K/V ring, the score and P buffers
+// and their barriers carry straight on from one tile into the next (the
+// next tile's Q and K/V loads and its first Q.K^T product overlap the
+// current tile's epilogue).  For chunk c (128 keys) of a tile:
+//   1. MMA warp: S_c = Q . K_c^T (tcgen05, M = 128 queries, N = 128 keys,
+//      K = 64) into TMEM score buffer c%2;
+//   2. softmax warps: four per TMEM lane quarter, warp part j owning chunk
+//      columns [32j, 32j+32) of its 32 rows (thread = query row).  Each keeps
+//      its own reference max m (log2 domain) and sum l; m is raised only when
+//      the chunk's largest score exceeds it by more than 2^8, so p = 2^(x-m)
+//      <= 2^8 stays well inside fp16/bf16.  p is written as the K-major,
+//      128-B-swizzled A operand of the next product;
+//   3. MMA warp: O_j += P_c[:, part j] . V_c[part j] into part j's own fp32
+//      accumulator in TMEM (4 x 64 columns), so no accumulator lives in
+//      registers; when a part raises m it rescales its own accumulator rows
+//      in place (tcgen05.ld / st) before the product that uses the new m.
+// Tile epilogue: the four parts of a row exchange (m_j, l_j) through shared
+// memory; part j then reads channels [16j, 16j+16) of all four accumulators,
+// combines them (O = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j) and
+// writes them out; lse = M ln 2 + ln L.
 //
-// Warps: 0 = TMA producer (Q once; K and V chunks into a 3-stage ring),
-// 1 = TMEM owner + MMA issuer, 2..9 = softmax / epilogue (two per TMEM lane
-// quarter, each owning one key half of every chunk; the halves merge their
-// running max, sum and accumulator once, at the end).
+// Warps: 0 = TMA producer (Q double-buffered, K and V chunks into a 3-stage
+// ring), 1 = TMEM owner + MMA issuer, 2..17 = softmax / epilogue.  Every
+// wait is a bounded mbarrier wait (no bar.sync inside the loops), so a
+// timeout anywhere lets every warp leave.
 #include <type_traits>
 
 #include "swab_internal.h"
@@ -35,19 +40,22 @@
 namespace swab {
 namespace {
 
-constexpr int kBQ = 128;      // queries per CTA (M)
-constexpr int kBK = 128;      // keys per chunk (N of S, K of P.V)
-constexpr int kStages = 3;    // K/V ring
-constexpr int kThreads = 320;   // producer, MMA, 8 softmax warps (2 per TMEM lane quarter)
-constexpr int kWorkers = 256;
-constexpr int kQBytes = kBQ * 128;             // 16 KB
-constexpr int kKBytes = kBK * 128;             // 16 KB
-constexpr int kVBytes = kBK * 128;             // 16 KB
-constexpr int kStageBytes = kKBytes + kVBytes; // 32 KB
-constexpr int kPBytes = kBQ * kBK * 2;         // 32 KB (two 64-key K-atoms)
-constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + 2 * kPBytes + 1024 + 1024;
-constexpr uint32_t kTmemCols = 512;            // S: 2 x 128, O: 2 chunks x 2 key halves x 64
-constexpr uint32_t kTmemO = 256;               // O of chunk parity b, key half h at 256 + 128b + 64h
+constexpr int kBQ = 128;        // queries per tile (M)
+constexpr int kBK = 128;        // keys per chunk (N of S, K of P.V)
+constexpr int kStages = 3;      // K/V ring
+constexpr int kParts = 4;       // key parts of a chunk: 32 keys each
+constexpr int kWorkerWarps = 4 * kParts;
+constexpr int kWorkers = 32 * kWorkerWarps;     // 512
+constexpr int kThreads = 64 + kWorkers;         // producer, MMA, softmax warps
+constexpr int kQBytes = kBQ * 128;              // 16 KB
+constexpr int kKBytes = kBK * 128;              // 16 KB
+constexpr int kStageBytes = 2 * kKBytes;        // K and V: 32 KB
+constexpr int kPBytes = kBQ * kBK * 2;          // 32 KB (two 64-key K-atoms)
+constexpr int kMlBytes = 2 * kParts * kBQ * 8;  // (m, l) exchange, two tile parities
+constexpr int kSmemBytes = 2 * kQBytes + kStages * kStageBytes + 2 * kPBytes + kMlBytes + 1024 + 1024;
+constexpr uint32_t kTmemCols = 512;             // S: 2 x 128, O: 4 parts x 64
+constexpr uint32_t kTmemO = 256;                // O of part j at 256 + 64 j
+constexpr float kSlack = 8.f;                   // log2 headroom of the reference max
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -55,8 +63,68 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+// packed fp32 pairs (sm_100 family): one instruction for two lanes of work
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Largest (kMin: smallest) of 32 values: four independent 8-value chains.
+template <bool kMin>
+__device__ __forceinline__ float reduce32(const float (&x)[32]) {
+    float c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float *y = x + 8 * k;
+        float a = kMin ? min3(y[0], y[1], y[2]) : max3(y[0], y[1], y[2]);
+        a = kMin ? min3(a, y[3], y[4]) : max3(a, y[3], y[4]);
+        a = kMin ? min3(a, y[5], y[6]) : max3(a, y[5], y[6]);
+        c[k] = kMin ? fminf(a, y[7]) : fmaxf(a, y[7]);
+    }
+    return kMin ? fminf(min3(c[0], c[1], c[2]), c[3]) : fmaxf(max3(c[0], c[1], c[2]), c[3]);
+}
+
+struct Tile {
+    int a0, r, bh, nr, kb_lo, kb_hi, nck;
+};
+
+// Tile t -> (query block, residue, slice); false when the block lies past the
+// end of its residue (every role skips such tiles the same way).
+__device__ __forceinline__ bool decode_tile(const Geom &g, int t, int xt, Tile &tl) {
+    tl.a0 = (t % xt) * kBQ;
+    const int rest = t / xt;
+    tl.r = rest % g.s;
+    tl.bh = rest / g.s;
+    tl.nr = residue_len(g.n, g.s, tl.r);
+    if (tl.a0 >= tl.nr) return false;
+    tl.kb_lo = max(tl.a0 - g.w, 0);
+    tl.kb_hi = min(tl.a0 + kBQ - 1 + g.wu, tl.nr - 1);
+    tl.nck = (tl.kb_hi - tl.kb_lo + kBK) / kBK;
+    return true;
 }
 
 template <typename T>
@@ -66,46 +134,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *qtile = base;
-    uint8_t *kv = base + kQBytes;                        // stage st: K at +0, V at +kKBytes
+    uint8_t *qtile = base;                               // 2 x 16 KB
+    uint8_t *kv = base + 2 * kQBytes;                    // stage st: K at +0, V at +kKBytes
     uint8_t *pbuf = kv + kStages * kStageBytes;          // 2 x 32 KB
-    uint64_t *bars = reinterpret_cast<uint64_t *>(pbuf + 2 * kPBytes);
-    uint64_t *qfull = bars;                  // 1
-    uint64_t *kvfull = bars + 1;             // [kStages]
+    float2 *mlx = reinterpret_cast<float2 *>(pbuf + 2 * kPBytes);  // [2][kParts][kBQ]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(pbuf + 2 * kPBytes + kMlBytes);
+    uint64_t *qfull = bars;                  // [2]
+    uint64_t *qempty = qfull + 2;            // [2]
+    uint64_t *kvfull = qempty + 2;           // [kStages]
     uint64_t *kvempty = kvfull + kStages;    // [kStages]
     uint64_t *sfull = kvempty + kStages;     // [2]
-    uint64_t *sempty = sfull + 2;            // [2] count 128
-    uint64_t *pfull = sempty + 2;            // [2] count 128
-    uint64_t *pempty = pfull + 2;            // [2]
-    uint64_t *ofull = pempty + 2;            // [2]
-    uint64_t *oempty = ofull + 2;            // [2] count 128
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(oempty + 2);
+    uint64_t *sempty = sfull + 2;            // [2] count kWorkers
+    uint64_t *pfull = sempty + 2;            // [2] count kWorkers
+    uint64_t *ofull = pfull + 2;             // 1: P.V product of a chunk done
+    uint64_t *mlbar = ofull + 1;             // [4] per lane quarter, count 128
+    uint64_t *mmadone = mlbar + 4;           // 1: drain of the MMA pipe at exit
+    uint64_t *drain = mmadone + 1;           // 1 int: never set (drain waits ignore aborts)
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *no_abort = reinterpret_cast<volatile int *>(drain);
 
     const Geom &g = p.g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.y, bh = blockIdx.z;
-    const int nr = residue_len(g.n, g.s, r);
-    const int a0 = blockIdx.x * kBQ;
-    if (a0 >= nr) return;
-    const int kb_lo = max(a0 - g.w, 0);
-    const int kb_hi = min(a0 + kBQ - 1 + g.wu, nr - 1);
-    const int nck = (kb_hi - kb_lo + kBK) / kBK;
+    const int xt = (g.nsub + kBQ - 1) / kBQ;
+    const int ntiles = xt * g.s * g.BH;
 
     if (threadIdx.x == 0) {
-        mbar_init(qfull, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sempty[i], kWorkers);
+            mbar_init(&pfull[i], kWorkers);
+        }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&kvfull[i], 1);
             mbar_init(&kvempty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sfull[i], 1);
-            mbar_init(&sempty[i], kWorkers);
-            mbar_init(&pfull[i], kWorkers);
-            mbar_init(&pempty[i], 1);
-            mbar_init(&ofull[i], 1);
-            mbar_init(&oempty[i], kWorkers);
-        }
+        mbar_init(ofull, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&mlbar[i], 128);
+        mbar_init(mmadone, 1);
+        *no_abort = 0;
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -118,255 +187,307 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
+    // The producer and MMA warps run their loops warp-uniformly (every lane
+    // walks the tiles and waits on the barriers) and only lane 0 issues the
+    // copies, products and commits.
     if (warp == 0) {
-        if (lane == 0) {
-            const CUtensorMap *mq = &mapQ.m[r], *mk = &mapK.m[r], *mv = &mapV.m[r];
-            tma_prefetch_desc(mq);
-            tma_prefetch_desc(mk);
-            tma_prefetch_desc(mv);
-            mbar_arrive_expect_tx(qfull, kQBytes);
-            tma_load_3d(qtile, mq, qfull, 0, a0, bh);
-            for (int c = 0; c < nck; ++c) {
-                const int st = c % kStages;
-                const uint32_t ph = (c / kStages) & 1;
-                if (!mbar_wait(&kvempty[st], ph ^ 1, abort_flag, p.err)) break;
-                mbar_arrive_expect_tx(&kvfull[st], kStageBytes);
-                uint8_t *stage = kv + st * kStageBytes;
-                tma_load_3d(stage, mk, &kvfull[st], 0, kb_lo + c * kBK, bh);
-                tma_load_3d(stage + kKBytes, mv, &kvfull[st], 0, kb_lo + c * kBK, bh);
+        uint32_t gc = 0, it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            Tile tl;
+            if (!decode_tile(g, t, xt, tl)) continue;
+            const CUtensorMap *mq = &mapQ.m[tl.r], *mk = &mapK.m[tl.r], *mv = &mapV.m[tl.r];
+            const int qb = it & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&qempty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.err)))
+                break;
+            if (lane == 0) {
+                tma_prefetch_desc(mq);
+                tma_prefetch_desc(mk);
+                tma_prefetch_desc(mv);
+                mbar_arrive_expect_tx(&qfull[qb], kQBytes);
+                tma_load_3d(qtile + qb * kQBytes, mq, &qfull[qb], 0, tl.a0, tl.bh);
+            }
+            __syncwarp();
+            ++it;
+            for (int c = 0; c < tl.nck; ++c) {
+                const int st = gc % kStages;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&kvempty[st], ((gc / kStages) & 1) ^ 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&kvfull[st], kStageBytes);
+                    uint8_t *stage = kv + st * kStageBytes;
+                    tma_load_3d(stage, mk, &kvfull[st], 0, tl.kb_lo + c * kBK, tl.bh);
+                    tma_load_3d(stage + kKBytes, mv, &kvfull[st], 0, tl.kb_lo + c * kBK, tl.bh);
+                }
+                __syncwarp();
+                ++gc;
             }
         }
+        // every copy issued lands before the CTA may exit (the last use of
+        // each stage and Q buffer; earlier ones completed before reuse)
+        for (uint32_t k = gc > (uint32_t)kStages ? gc - kStages : 0; k < gc; ++k)
+            mbar_wait(&kvfull[k % kStages], (k / kStages) & 1, no_abort, nullptr, 100000000ull);
+        for (uint32_t k = it > 2u ? it - 2 : 0; k < it; ++k)
+            mbar_wait(&qfull[k & 1], (k >> 1) & 1, no_abort, nullptr, 100000000ull);
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr bool kBf16 = !std::is_same<T, __half>::value;
-            const uint32_t idesc_s = idesc_f16(kBQ, kBK, kBf16, false, false);
-            const uint32_t idesc_o = idesc_f16(kBQ, 64, kBf16, false, true);
-            const uint32_t q_addr = smem_u32(qtile);
-            bool ok = mbar_wait(qfull, 0, abort_flag, p.err);
-            // P.V of chunk c (issued after S of chunk c+1 so that the two overlap)
-            auto issue_pv = [&](int c) -> bool {
-                const int st = c % kStages;
-                const int b = c & 1;
-                const uint32_t bph = (c >> 1) & 1;
-                if (!mbar_wait(&pfull[b], bph, abort_flag, p.err)) return false;
-                if (!mbar_wait(&oempty[b], bph ^ 1, abort_flag, p.err)) return false;
-                tc_fence_after();
-                const uint32_t p_addr = smem_u32(pbuf + b * kPBytes);
-                const uint32_t v_addr = smem_u32(kv + st * kStageBytes + kKBytes);
+        constexpr bool kBf16 = !std::is_same<T, __half>::value;
+        constexpr uint32_t idesc_s = idesc_f16(kBQ, kBK, kBf16, false, false);
+        constexpr uint32_t idesc_o = idesc_f16(kBQ, 64, kBf16, false, true);
+        // Shared-memory descriptors are built once; a buffer, stage or K step
+        // only moves the start address field (address >> 4, which stays below
+        // 2^14 for any shared-memory address), so each one is a 64-bit add of
+        // a compile-time offset.
+        const uint64_t qdesc = sdesc_sw128(smem_u32(qtile), 16, 1024);
+        const uint64_t kdesc = sdesc_sw128(smem_u32(kv), 16, 1024);
+        const uint64_t vdesc = sdesc_sw128(smem_u32(kv + kKBytes), 1024, 1024);
+        const uint64_t pdesc = sdesc_sw128(smem_u32(pbuf), 16, 1024);
+        // O_j (+)= P[:, part j] . V[part j]: the P.V product of chunk gg
+        auto issue_pv = [&](uint32_t gg, bool first) -> bool {
+            const int st = gg % kStages;
+            const int b = gg & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&pfull[b], (gg >> 1) & 1, abort_flag, p.err)))
+                return false;
+            tc_fence_after();
+            const uint64_t pa = pdesc + (uint64_t)((b * kPBytes) >> 4);
+            const uint64_t va = vdesc + (uint64_t)((st * kStageBytes) >> 4);
+            if (lane == 0) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // keys [64h, 64h + 64): K-atom h of P, rows 64h.. of V
-                    const uint32_t d = tmem + kTmemO + b * 128 + h * 64;
+                for (int j = 0; j < kParts; ++j) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t a = p_addr + h * (kPBytes / 2) + k * 32;
-                        mma_f16_ss(d, sdesc_sw128(a, 16, 1024),
-                                   sdesc_sw128(v_addr + h * 8192 + 2048 * k, 1024, 1024), idesc_o, k > 0);
+                    for (int kk = 0; kk < 2; ++kk) {
+                        // keys 32j + 16kk ..: atom j/2 of P, rows 32j + 16kk.. of V
+                        mma_f16_ss(tmem + kTmemO + 64 * j,
+                                   pa + (((j >> 1) * (kPBytes / 2) + (j & 1) * 64 + kk * 32) >> 4),
+                                   va + (((2 * j + kk) * 2048) >> 4), idesc_o,
+                                   (first && kk == 0) ? 0u : 1u);
                     }
                 }
-                mma_commit(&ofull[b]);
-                mma_commit(&pempty[b]);
+                mma_commit(ofull);
                 mma_commit(&kvempty[st]);
-                return true;
-            };
-            for (int c = 0; c < nck && ok; ++c) {
-                const int st = c % kStages;
-                const uint32_t ph = (c / kStages) & 1;
-                const int b = c & 1;
-                const uint32_t bph = (c >> 1) & 1;
-                ok = mbar_wait(&kvfull[st], ph, abort_flag, p.err) &&
-                     mbar_wait(&sempty[b], bph ^ 1, abort_flag, p.err);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t k_addr = smem_u32(kv + st * kStageBytes);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    mma_f16_ss(tmem + b * kBK, sdesc_sw128(q_addr + 32 * k, 16, 1024),
-                               sdesc_sw128(k_addr + 32 * k, 16, 1024), idesc_s, k > 0);
-                }
-                mma_commit(&sfull[b]);
-                if (c > 0) ok = issue_pv(c - 1);
             }
-            if (ok) issue_pv(nck - 1);
-        }
-    } else {
-        // ---------------- softmax warps: thread = query row ----------------
-        // Two warps per TMEM lane quarter: warp half h owns key columns
-        // [64h, 64h + 64) of every chunk and keeps its own reference max m,
-        // sum l and accumulator (its P.V half goes to its own TMEM buffer), so
-        // the halves never wait on each other until the final merge.
-        // Per half: a chunk is processed in ONE pass over tensor memory with
-        // the current m; m is raised only when the chunk's largest score
-        // exceeds it by more than kSlack (the chunk is then redone with the
-        // new m), so p <= 2^kSlack stays well inside fp16/bf16 range.  A half
-        // with no key seen yet takes its m from a max-only pass first.  The
-        // softmax does not depend on the choice of m.
-        constexpr float kSlack = 8.f;
-        const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;
-        const int q = quarter * 32 + lane;
-        const int qq = a0 + q;
-        const float xscale = p.scale * 1.4426950408889634f;
-        float m = -INFINITY, l = 0.f, corr_prev = 1.f;
-        float acc[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
-        bool ok = true;
-
-        auto fold_o = [&](int c, float corr) -> bool {
-            const int b = c & 1;
-            const uint32_t bph = (c >> 1) & 1;
-            const bool w_ok = mbar_wait(&ofull[b], bph, abort_flag, p.err);
-            if (!__all_sync(0xffffffffu, w_ok)) return false;
-            tc_fence_after();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + kTmemO + b * 128 + half * 64 + h * 32, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) acc[h * 32 + i] = fmaf(acc[h * 32 + i], corr, __uint_as_float(v[i]));
-            }
-            tc_fence_before();
-            mbar_arrive(&oempty[b]);
+            __syncwarp();
             return true;
         };
-
-        for (int c = 0; c < nck; ++c) {
-            const int b = c & 1;
-            const uint32_t bph = (c >> 1) & 1;
-            const int kbase = kb_lo + c * kBK;
-            // this row's band inside the chunk: columns [jlo, jhi]
-            const int jlo = max(qq - g.w - kbase, 0);
-            const int jhi = min(min(qq + g.wu, kb_hi) - kbase, kBK - 1);
-            const bool full = __all_sync(0xffffffffu, jlo <= 64 * half && jhi >= 64 * half + 63);
-            bool w_ok = mbar_wait(&sfull[b], bph, abort_flag, p.err);
-            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sbuf = lane_base + b * kBK;
-            float mref = m;
-            if (__any_sync(0xffffffffu, m == -INFINITY)) {
-                float mx = -INFINITY;
-#pragma unroll 1
-                for (int grp = 2 * half; grp < 2 * half + 2; ++grp) {
-                    uint32_t v[32];
-                    tmem_ld32(sbuf + grp * 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int j = grp * 32 + i;
-                        if (j >= jlo && j <= jhi) mx = fmaxf(mx, __uint_as_float(v[i]) * xscale);
-                    }
+        uint32_t gc = 0, it = 0, prev = 0;
+        bool ok = true, have_prev = false, prev_first = false;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            Tile tl;
+            if (!decode_tile(g, t, xt, tl)) continue;
+            // the last product of the previous tile goes first: its epilogue
+            // need not wait for this tile's loads
+            if (have_prev) {
+                have_prev = false;
+                if (!issue_pv(prev, prev_first)) {
+                    ok = false;
+                    break;
                 }
-                if (m == -INFINITY) mref = mx;
             }
-            // the P tile of chunk c may still feed the P.V product of chunk c-2
-            w_ok = mbar_wait(&pempty[b], bph ^ 1, abort_flag, p.err);
-            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-            const uint32_t pbase = smem_u32(pbuf + b * kPBytes);
-            float lc = 0.f;
-            for (int pass = 0; pass < 2; ++pass) {
-                const float mb = mref == -INFINITY ? 0.f : mref;
-                float ymax = -INFINITY;  // chunk max relative to mref
-                lc = 0.f;
-#pragma unroll 1
-                for (int grp = 2 * half; grp < 2 * half + 2; ++grp) {
-                    uint32_t v[32];
-                    tmem_ld32(sbuf + grp * 32, v);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
+            const int qb = it & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&qfull[qb], (it >> 1) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            const uint64_t qa = qdesc + (uint64_t)((qb * kQBytes) >> 4);
+            for (int c = 0; c < tl.nck; ++c, ++gc) {
+                const int st = gc % kStages;
+                const int b = gc & 1;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&kvfull[st], (gc / kStages) & 1, abort_flag, p.err) &&
+                                    mbar_wait(&sempty[b], ((gc >> 1) & 1) ^ 1, abort_flag, p.err));
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t ka = kdesc + (uint64_t)((st * kStageBytes) >> 4);
+                if (lane == 0) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float y0 = fmaf(__uint_as_float(v[2 * i]), xscale, -mb);
-                        float y1 = fmaf(__uint_as_float(v[2 * i + 1]), xscale, -mb);
-                        if (!full) {
-                            const int j0 = grp * 32 + 2 * i;
-                            if (j0 < jlo || j0 > jhi) y0 = -INFINITY;
-                            if (j0 + 1 < jlo || j0 + 1 > jhi) y1 = -INFINITY;
-                        }
-                        ymax = fmaxf(ymax, fmaxf(y0, y1));
-                        const float p0 = ex2(y0), p1 = ex2(y1);
-                        lc += p0 + p1;
-                        pk[i] = pack2<T>(p0, p1);
-                    }
-                    // 32 keys = 4 x 16-byte pieces; key-atom grp/2, pieces (grp%2)*4 + 0..3
-                    const uint32_t atom = pbase + (grp >> 1) * (kPBytes / 2) + q * 128;
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16_ss(tmem + b * kBK, qa + 2 * k, ka + 2 * k, idesc_s, k > 0);
+                    if (c == tl.nck - 1) mma_commit(&qempty[qb]);
+                    mma_commit(&sfull[b]);
+                }
+                __syncwarp();
+                if (have_prev && !issue_pv(prev, prev_first)) {
+                    ok = false;
+                    break;
+                }
+                have_prev = true;
+                prev = gc;
+                prev_first = c == 0;
+            }
+            ++it;
+        }
+        if (ok && have_prev) issue_pv(prev, prev_first);
+        // every product issued is complete before the accumulators are freed
+        if (lane == 0) mma_commit(mmadone);
+        __syncwarp();
+        mbar_wait(mmadone, 0, no_abort, nullptr, 100000000ull);
+    } else {
+        // ---------------- softmax warps: thread = query row ----------------
+        const int quarter = warp & 3;
+        const int part = (warp - 2) >> 2;
+        const int q = quarter * 32 + lane;
+        const float xscale = p.scale * 1.4426950408889634f;
+        const bool neg_scale = xscale < 0.f;
+        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
+        const uint32_t o_mine = lane_base + kTmemO + 64 * part;
+        uint32_t gc = 0, it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            Tile tl;
+            if (!decode_tile(g, t, xt, tl)) continue;
+            const int qq = tl.a0 + q;
+            float m = -INFINITY, l = 0.f;
+            for (int c = 0; c < tl.nck; ++c, ++gc) {
+                const int b = gc & 1;
+                const int kbase = tl.kb_lo + c * kBK + 32 * part;
+                // this row's band inside the part: columns [max(jlo,0), min(jhi,31)]
+                const int jlo = max(qq - g.w - kbase, 0);
+                const int jhi = min(min(qq + g.wu, tl.kb_hi) - kbase, 31);
+                const uint32_t vmask = jlo > jhi ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
+                const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
+                const bool empty = __all_sync(0xffffffffu, vmask == 0u);
+                bool w_ok = mbar_wait(&sfull[b], (gc >> 1) & 1, abort_flag, p.err);
+                if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+                tc_fence_after();
+                float x[32];
+                {
+                    uint32_t v[32];
+                    tmem_ld32(lane_base + b * kBK + 32 * part, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
+                }
+                tc_fence_before();
+                mbar_arrive(&sempty[b]);   // the scores are in registers
+                // P tile b last fed the product of chunk gc-2, which is done
+                const uint32_t prow = smem_u32(pbuf + b * kPBytes) + (part >> 1) * (kPBytes / 2) + q * 128;
+                float cmax = -INFINITY, lc = 0.f;
+                if (empty) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int piece = (grp & 1) * 4 + u;
-                        sts16(atom + ((piece ^ (q & 7)) << 4),
-                              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+                        const int piece = (part & 1) * 4 + u;
+                        sts16(prow + ((piece ^ (q & 7)) << 4), make_uint4(0u, 0u, 0u, 0u));
                     }
+                } else {
+                    // chunk max of the scaled scores from the raw ones: the
+                    // largest raw score for a positive scale, the smallest
+                    // for a negative one; columns outside the band are
+                    // replaced by the value that never wins
+                    if (!full) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (!((vmask >> i) & 1u)) x[i] = neg_scale ? INFINITY : -INFINITY;
+                    }
+                    const float vm = neg_scale ? reduce32<true>(x) : reduce32<false>(x);
+                    cmax = vmask == 0u ? -INFINITY : vm * xscale;
                 }
-                // redo the chunk if a score rose more than kSlack above mref
-                const bool redo = ymax > kSlack;
-                if (!__any_sync(0xffffffffu, redo)) break;
-                if (redo) mref = mb + ymax;
+                const bool raise = m == -INFINITY || cmax > m + kSlack;
+                const float mref = raise ? cmax : m;
+                if (!empty) {
+                    const float mb = mref == -INFINITY ? 0.f : mref;
+                    const uint64_t xs2 = f2(xscale, xscale), nb2 = f2(-mb, -mb);
+                    uint64_t lc2 = f2(0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 8 * u + 2 * e;
+                            float y0, y1;
+                            f2split(fma2(f2(x[i], x[i + 1]), xs2, nb2), y0, y1);
+                            float p0 = ex2(y0), p1 = ex2(y1);
+                            if (!full) {
+                                if (!((vmask >> i) & 1u)) p0 = 0.f;
+                                if (!((vmask >> (i + 1)) & 1u)) p1 = 0.f;
+                            }
+                            lc2 = add2(lc2, f2(p0, p1));
+                            pk[e] = pack2<T>(p0, p1);
+                        }
+                        const int piece = (part & 1) * 4 + u;
+                        sts16(prow + ((piece ^ (q & 7)) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                    }
+                    float l0, l1;
+                    f2split(lc2, l0, l1);
+                    lc = l0 + l1;
+                }
+                const bool rescale = raise && m != -INFINITY;
+                const float corr = rescale ? ex2(m - mref) : 1.f;
+                l = l * corr + lc;
+                if (c > 0) {
+                    // the product of chunk gc-1 has landed in O: it may be rescaled
+                    w_ok = mbar_wait(ofull, (gc - 1) & 1, abort_flag, p.err);
+                    if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t o[32];
+                        tmem_ld32(o_mine + 32 * h, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                        tmem_st32(o_mine + 32 * h, o);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                mbar_arrive(&pfull[b]);    // P tile b (and the rescaled O) are ready
+                m = mref;
             }
-            const float corr = (m == -INFINITY) ? 1.f : ex2(m - mref);
-            l = l * corr + lc;
-            tc_fence_before();
-            mbar_arrive(&sempty[b]);   // S buffer b may be overwritten
-            fence_proxy_async_smem();
-            mbar_arrive(&pfull[b]);    // P tile b is ready for the tensor core
-            m = mref;
-            if (c > 0) {
-                if (!fold_o(c - 1, corr_prev)) { ok = false; break; }
+            if (!ok) break;
+            // ---------------- tile epilogue ----------------
+            bool w_ok = mbar_wait(ofull, (gc - 1) & 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+            tc_fence_after();
+            float2 *ml = mlx + (it & 1) * kParts * kBQ;
+            ml[part * kBQ + q] = make_float2(m, l);
+            mbar_arrive(&mlbar[quarter]);
+            w_ok = mbar_wait(&mlbar[quarter], it & 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+            float M = -INFINITY;
+            float2 e[kParts];
+#pragma unroll
+            for (int j = 0; j < kParts; ++j) {
+                e[j] = ml[j * kBQ + q];
+                M = fmaxf(M, e[j].x);
             }
-            corr_prev = corr;
-        }
-        if (ok) ok = fold_o(nck - 1, corr_prev);
-        // merge the two key halves: every P.V product is complete, so the P
-        // tiles are free to carry each half's (m, l) and the accumulator
-        // channels the other half writes out
-        float *xs = reinterpret_cast<float *>(pbuf);  // [2 halves][128 rows][34]
-        const bool all_ok = __all_sync(0xffffffffu, ok);
-        // static register indices only: split acc by half with branches
-        float keep[32], give[32];
-        if (half == 0) {
+            float f[kParts], L = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                keep[i] = acc[i];
-                give[i] = acc[32 + i];
+            for (int j = 0; j < kParts; ++j) {
+                f[j] = e[j].x == -INFINITY ? 0.f : ex2(e[j].x - M);
+                L += e[j].y * f[j];
             }
-        } else {
+            const float inv = 1.f / L;
+            // channels [16 part, 16 part + 16) of the four accumulators, two at a time
+            float y[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                keep[i] = acc[32 + i];
-                give[i] = acc[i];
+            for (int i = 0; i < 16; ++i) y[i] = 0.f;
+#pragma unroll
+            for (int j0 = 0; j0 < kParts; j0 += 2) {
+                uint32_t o0[16], o1[16];
+                tmem_ld16(lane_base + kTmemO + 64 * j0 + 16 * part, o0);
+                tmem_ld16(lane_base + kTmemO + 64 * (j0 + 1) + 16 * part, o1);
+                tmem_ld_wait();
+                const float f0 = f[j0] * inv, f1 = f[j0 + 1] * inv;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    y[i] = fmaf(__uint_as_float(o1[i]), f1, fmaf(__uint_as_float(o0[i]), f0, y[i]));
             }
-        }
-        if (all_ok) {
-            float *mine = xs + (half * kBQ + q) * 34;
-            mine[0] = m;
-            mine[1] = l;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mine[2 + i] = give[i];
-        }
-        named_bar_sync(1, kWorkers);
-        if (all_ok && qq < nr) {
-            const float *other = xs + ((1 - half) * kBQ + q) * 34;
-            const float pm = other[0], pl = other[1];
-            const float M = fmaxf(m, pm);
-            const float f = m == -INFINITY ? 0.f : ex2(m - M);
-            const float pf = pm == -INFINITY ? 0.f : ex2(pm - M);
-            const float inv = 1.f / (l * f + pl * pf);
-            T *out = reinterpret_cast<T *>(p.O) + ((long long)bh * g.n + r + (long long)g.s * qq) * 64 +
-                     half * 32;
-            uint4 *o4 = reinterpret_cast<uint4 *>(out);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    y[e] = (keep[8 * u + e] * f + other[2 + 8 * u + e] * pf) * inv;
-                o4[u] = make_uint4(pack2<T>(y[0], y[1]), pack2<T>(y[2], y[3]), pack2<T>(y[4], y[5]),
+            tc_fence_before();   // O may be overwritten once this warp's next P tile is signalled
+            if (qq < tl.nr) {
+                const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * qq;
+                uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + row * 64 + 16 * part);
+                o4[0] = make_uint4(pack2<T>(y[0], y[1]), pack2<T>(y[2], y[3]), pack2<T>(y[4], y[5]),
                                    pack2<T>(y[6], y[7]));
+                o4[1] = make_uint4(pack2<T>(y[8], y[9]), pack2<T>(y[10], y[11]),
+                                   pack2<T>(y[12], y[13]), pack2<T>(y[14], y[15]));
+                if (p.lse && part == 0) p.lse[row] = M * 0.6931471805599453f + logf(L);
             }
-            if (p.lse && half == 0)
-                p.lse[(long long)bh * g.n + r + (long long)g.s * qq] =
-                    M * 0.6931471805599453f + logf(l * f + pl * pf);
+            ++it;
         }
     }
     tc_fence_before();
@@ -422,8 +543,10 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
 template <typename T>
 cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const AttnArgs &a,
                      cudaStream_t st) {
-    const int tiles = (a.g.nsub + kBQ - 1) / kBQ;
-    dim3 grid(tiles, a.g.s, a.g.BH);
+    const long long tiles = (long long)((a.g.nsub + kBQ - 1) / kBQ) * a.g.s * a.g.BH;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = (int)(tiles < sms ? tiles : sms);
     cudaError_t e = cudaFuncSetAttribute(k_band_attention_fwd<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;

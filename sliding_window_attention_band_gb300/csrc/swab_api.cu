@@ -209,6 +209,22 @@ swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, co
 }
 
 }  // namespace
+
+// Number of SMs of the current device (cached per device); 0 on error.
+int device_sm_count() {
+    static std::mutex mu;
+    static int cache[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
 }  // namespace swab
 
 using namespace swab;

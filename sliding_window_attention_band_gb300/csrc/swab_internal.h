@@ -139,6 +139,8 @@ cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const Tmap
                                          const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,
                                          cudaStream_t st);
 cudaError_t launch_band_attention_bwd_f32(const BwdArgs &a, cudaStream_t st);
+// SM count of the current device (swab_api.cu); 0 on error
+int device_sm_count();
 // the module-scope delta scratch of band_attention_bwd_noalloc (k_attention_bwd.cu)
 cudaError_t noalloc_delta_scratch(float **out);
 // fp32 FFMA paths
