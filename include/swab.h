@@ -164,20 +164,30 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
  *   P = exp(scale*Q.K^T - lse), dP = dO.V^T, delta_i = dO_i . O_i,
  *   dS = P*(dP - delta), dQ = scale*dS.K, dK = scale*dS^T.Q, dV = P^T.dO
  * on the used slots (the two backward products of the TVM thread, post 6,
- * with the textbook softmax derivative).  Deterministic (no atomics).
+ * with the textbook softmax derivative).
  * `workspace` is caller-owned device memory of band_attention_bwd_workspace()
- * bytes (the per-row delta, fp32); its contents on entry do not matter.
+ * bytes, 16-byte aligned; its contents on entry do not matter.  For fp16 /
+ * bf16 it holds the per-row delta and an fp32 dQ accumulator: dK and dV have
+ * one writer per row, while dQ is summed over key tiles with fp32 atomic
+ * additions, so dQ may differ in its last bits from run to run (within the
+ * rounding of one fp32 sum; band_attention_bwd_noalloc is bitwise
+ * repeatable).  For fp32 it holds the delta only and every output is
+ * repeatable.
  * Global tokens are not supported here (n_global must be 0). */
 SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, const void *Q,
                                         const void *K, const void *V, const void *O,
                                         const void *dO, const float *lse, void *dQ, void *dK,
                                         void *dV, void *workspace, void *stream);
 
-/* Bytes of workspace band_attention_bwd needs for `desc` (0 if desc is NULL). */
+/* Bytes of workspace band_attention_bwd needs for `desc` (0 if desc is NULL):
+ * fp16 / bf16: round_up(b*h*n*4, 256) + b*h*n*64*4;  fp32: round_up(b*h*n*4, 256). */
 SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc);
 
 /* band_attention_bwd for callers that cannot allocate device memory: the same
- * computation, arguments and results, minus the workspace.  Some callers have
+ * computation and arguments, minus the workspace.  It needs only the per-row
+ * delta as scratch because it computes dQ in a kernel of its own (one writer
+ * per row) instead of summing it in an fp32 accumulator, so its results agree
+ * with band_attention_bwd within rounding and repeat bitwise.  Some callers have
  * no way to obtain a device buffer of their own -- code running under an
  * allocator or memory pool they do not control, plugins handed only input and
  * output pointers, or contexts where a cudaMalloc would synchronise or is

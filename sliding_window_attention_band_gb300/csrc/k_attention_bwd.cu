@@ -149,6 +149,28 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
         const long long R = warp_row0 + 4 * k + (lane >> 3);
         if ((lane & 7) == 0 && R < rows) p.delta[R] = v;
     }
+    if (p.dqacc) {
+        // the one-pass backward adds dQ contributions into an fp32 accumulator:
+        // clear this warp's rows of it (16 rows x 64 floats)
+        float4 *acc = reinterpret_cast<float4 *>(p.dqacc);
+#pragma unroll
+        for (int k = 0; k < kDeltaRowsPerWarp * 16 / 32; ++k) {
+            const int idx = k * 32 + lane;
+            const long long R = warp_row0 + idx / 16;
+            if (R < rows) acc[R * 16 + (idx & 15)] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
+// dQ = accumulator (already scaled), rounded to the output type: 8 channels per thread
+template <typename T>
+__global__ void __launch_bounds__(256) k_bwd_dq_out(const BwdArgs p) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8-channel group
+    if (i >= (long long)p.g.BH * p.g.n * 8) return;
+    const float4 *acc = reinterpret_cast<const float4 *>(p.dqacc) + 2 * i;
+    const float4 a = acc[0], b = acc[1];
+    reinterpret_cast<uint4 *>(p.dQ)[i] =
+        make_uint4(pack2<T>(a.x, a.y), pack2<T>(a.z, a.w), pack2<T>(b.x, b.y), pack2<T>(b.z, b.w));
 }
 
 // ---------------------------------------------------------------------------
@@ -587,6 +609,461 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// One-pass backward: dK, dV and dQ from one persistent kernel.
+// Tile = 128 keys of one residue; for each 128-query chunk of its band:
+//   S^T = K Q_c^T, dP^T = V dO_c^T               (tcgen05, TMEM lane = key)
+//   P^T, dS^T per key row (16 warps: 4 per TMEM lane quarter, each owning 32
+//   query columns), written as K-major 128-B-swizzled operands
+//   dV += P^T dO_c, dK += dS^T Q_c                (TMEM, lane = key)
+//   dQ_c = dS K: the dS^T tile read as an MN-major A operand (M = queries),
+//   the K tile as an MN-major B operand, into one of two TMEM buffers
+//   (lane = query); the softmax warps add scale * dQ_c into an fp32
+//   accumulator with vector reductions one chunk later.
+// The per-query lse and delta of a chunk are staged into shared memory by the
+// producer warp next to the chunk's Q and dO tiles.  The accumulation order of
+// dQ across key tiles is not fixed, so dQ may differ in the last bits between
+// runs; dK and dV have one writer per row.
+// ---------------------------------------------------------------------------
+namespace fused {
+constexpr int kParts = 4;
+constexpr int kWorkers = 32 * 4 * kParts;       // 512
+constexpr int kThreads = 64 + kWorkers;
+constexpr int kKV = 2 * kTile;                  // K and V of a key tile: 32 KB
+constexpr int kQS = 2 * kTile;                  // Q and dO of a query chunk: 32 KB
+constexpr int kSmem = 2 * kKV + 2 * kQS + 2 * kOpBytes + 2 * 2 * kB * 4 + 1024 + 1024;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+
+struct KTile {
+    int a0, r, bh, nr, qb_lo, qb_hi, nck;
+};
+
+__device__ __forceinline__ bool decode_ktile(const Geom &g, int t, int xt, KTile &tl) {
+    tl.a0 = (t % xt) * kB;
+    const int rest = t / xt;
+    tl.r = rest % g.s;
+    tl.bh = rest / g.s;
+    tl.nr = residue_len(g.n, g.s, tl.r);
+    if (tl.a0 >= tl.nr) return false;
+    // key b is attended by the queries a with b in [a - w, a + w_upper]
+    tl.qb_lo = max(tl.a0 - g.wu, 0);
+    tl.qb_hi = min(tl.a0 + kB - 1 + g.w, tl.nr - 1);
+    tl.nck = (tl.qb_hi - tl.qb_lo + kB) / kB;
+    return true;
+}
+}  // namespace fused
+
+template <typename T>
+__global__ void __launch_bounds__(fused::kThreads, 1)
+    k_bwd_fused(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
+                const __grid_constant__ TmapSet mapV, const __grid_constant__ TmapSet mapdO,
+                const BwdArgs p) {
+    using namespace fused;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *kvbuf = base;                      // [2] key tiles: K at +0, V at +kTile
+    uint8_t *qsbuf = kvbuf + 2 * kKV;           // [2] query chunks: Q at +0, dO at +kTile
+    uint8_t *pt_op = qsbuf + 2 * kQS;           // P^T  [128 keys x 128 queries]
+    uint8_t *dst_op = pt_op + kOpBytes;         // dS^T
+    float *qstat = reinterpret_cast<float *>(dst_op + kOpBytes);  // [2][lse*log2e | delta][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(qstat + 2 * 2 * kB);
+    uint64_t *kvfull = bars;           // [2]
+    uint64_t *kvempty = kvfull + 2;    // [2]
+    uint64_t *qfull = kvempty + 2;     // [2]
+    uint64_t *qempty = qfull + 2;      // [2]
+    uint64_t *qsfull = qempty + 2;     // [2] count 32 (producer lanes)
+    uint64_t *sfull = qsfull + 2;      // 1
+    uint64_t *sempty = sfull + 1;      // 1, count fused::kWorkers
+    uint64_t *opfull = sempty + 1;     // 1, count fused::kWorkers
+    uint64_t *opempty = opfull + 1;    // 1
+    uint64_t *dqfull = opempty + 1;    // [2]
+    uint64_t *dqempty = dqfull + 2;    // [2], count fused::kWorkers
+    uint64_t *accfull = dqempty + 2;   // 1
+    uint64_t *accempty = accfull + 1;  // 1, count fused::kWorkers
+    uint64_t *mmadone = accempty + 1;  // 1
+    uint64_t *drain = mmadone + 1;     // a flag word that is never set
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *no_abort = reinterpret_cast<volatile int *>(drain);
+
+    const Geom &g = p.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int xt = (g.nsub + kB - 1) / kB;
+    const int ntiles = xt * g.s * g.BH;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kvfull[i], 1);
+            mbar_init(&kvempty[i], 1);
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+            mbar_init(&qsfull[i], 32);
+            mbar_init(&dqfull[i], 1);
+            mbar_init(&dqempty[i], fused::kWorkers);
+        }
+        mbar_init(sfull, 1);
+        mbar_init(sempty, fused::kWorkers);
+        mbar_init(opfull, fused::kWorkers);
+        mbar_init(opempty, 1);
+        mbar_init(accfull, 1);
+        mbar_init(accempty, fused::kWorkers);
+        mbar_init(mmadone, 1);
+        *no_abort = 0;
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- producer (warp-uniform; lane 0 issues the copies) ----------------
+        uint32_t gc = 0, it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            KTile tl;
+            if (!decode_ktile(g, t, xt, tl)) continue;
+            const CUtensorMap *mq = &mapQ.m[tl.r], *mk = &mapK.m[tl.r], *mv = &mapV.m[tl.r],
+                              *mo = &mapdO.m[tl.r];
+            const int tb = it & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&kvempty[tb], ((it >> 1) & 1) ^ 1, abort_flag, p.err)))
+                break;
+            if (lane == 0) {
+                tma_prefetch_desc(mq);
+                tma_prefetch_desc(mk);
+                tma_prefetch_desc(mv);
+                tma_prefetch_desc(mo);
+                mbar_arrive_expect_tx(&kvfull[tb], kKV);
+                tma_load_3d(kvbuf + tb * kKV, mk, &kvfull[tb], 0, tl.a0, tl.bh);
+                tma_load_3d(kvbuf + tb * kKV + kTile, mv, &kvfull[tb], 0, tl.a0, tl.bh);
+            }
+            __syncwarp();
+            ++it;
+            for (int c = 0; c < tl.nck; ++c) {
+                const int qs = gc & 1;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&qempty[qs], ((gc >> 1) & 1) ^ 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                const int qbase = tl.qb_lo + c * kB;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&qfull[qs], kQS);
+                    tma_load_3d(qsbuf + qs * kQS, mq, &qfull[qs], 0, qbase, tl.bh);
+                    tma_load_3d(qsbuf + qs * kQS + kTile, mo, &qfull[qs], 0, qbase, tl.bh);
+                }
+                // lse (log2 units) and delta of the chunk's 128 queries, 4 per lane
+                float lv[4], dv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int qq = qbase + 4 * lane + e;
+                    const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * qq;
+                    lv[e] = qq < tl.nr ? p.lse[row] * kLog2e : 0.f;
+                    dv[e] = qq < tl.nr ? p.delta[row] : 0.f;
+                }
+                float4 *st4 = reinterpret_cast<float4 *>(qstat + qs * 2 * kB);
+                st4[lane] = make_float4(lv[0], lv[1], lv[2], lv[3]);
+                st4[kB / 4 + lane] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+                mbar_arrive(&qsfull[qs]);
+                ++gc;
+            }
+        }
+        // every copy issued lands before the CTA may exit
+        for (uint32_t k = it > 2u ? it - 2 : 0; k < it; ++k)
+            mbar_wait(&kvfull[k & 1], (k >> 1) & 1, no_abort, nullptr, 100000000ull);
+        for (uint32_t k = gc > 2u ? gc - 2 : 0; k < gc; ++k)
+            mbar_wait(&qfull[k & 1], (k >> 1) & 1, no_abort, nullptr, 100000000ull);
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (warp-uniform; lane 0 issues) ----------------
+        constexpr bool kBf16 = !std::is_same<T, __half>::value;
+        constexpr uint32_t id_s = idesc_f16(kB, kB, kBf16, false, false);  // S^T, dP^T
+        constexpr uint32_t id_g = idesc_f16(kB, 64, kBf16, false, true);   // dV, dK
+        constexpr uint32_t id_q = idesc_f16(kB, 64, kBf16, true, true);    // dQ
+        // descriptors of buffer 0; a buffer / K step adds (bytes >> 4)
+        const uint64_t d_k = sdesc_sw128(smem_u32(kvbuf), 16, 1024);           // K, K-major
+        const uint64_t d_v = sdesc_sw128(smem_u32(kvbuf + kTile), 16, 1024);   // V, K-major
+        const uint64_t d_kmn = sdesc_sw128(smem_u32(kvbuf), 1024, 1024);       // K as MN-major B
+        const uint64_t d_q = sdesc_sw128(smem_u32(qsbuf), 16, 1024);           // Q, K-major
+        const uint64_t d_o = sdesc_sw128(smem_u32(qsbuf + kTile), 16, 1024);   // dO, K-major
+        const uint64_t d_qmn = sdesc_sw128(smem_u32(qsbuf), 1024, 1024);       // Q as MN-major B
+        const uint64_t d_omn = sdesc_sw128(smem_u32(qsbuf + kTile), 1024, 1024);  // dO as MN-major B
+        const uint64_t d_pt = sdesc_sw128(smem_u32(pt_op), 16, 1024);          // P^T, K-major A
+        const uint64_t d_dst = sdesc_sw128(smem_u32(dst_op), 16, 1024);        // dS^T, K-major A
+        // dS^T read as dS (M = queries): 64-query blocks kOpBytes/2 apart,
+        // 8-key groups 1024 B apart
+        const uint64_t d_dsmn = sdesc_sw128(smem_u32(dst_op), kOpBytes / 2, 1024);
+        auto issue_grad = [&](uint32_t gg, bool first, bool last, int tb, uint32_t itt) -> bool {
+            const int qs = gg & 1;
+            bool w = mbar_wait(opfull, gg & 1, abort_flag, p.err) &&
+                     mbar_wait(&dqempty[qs], ((gg >> 1) & 1) ^ 1, abort_flag, p.err);
+            if (first) w = w && mbar_wait(accempty, (itt & 1) ^ 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, w)) return false;
+            tc_fence_after();
+            const uint64_t qoff = (uint64_t)((qs * kQS) >> 4), toff = (uint64_t)((tb * kKV) >> 4);
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < kB / 16; ++k) {
+                    // K step k = queries 16k.. (dV, dK) or keys 16k.. (dQ)
+                    const uint64_t aop = (uint64_t)((((k >> 2) * (kOpBytes / 2)) + (k & 3) * 32) >> 4);
+                    const uint64_t rows = (uint64_t)((2048 * k) >> 4);
+                    const uint32_t acc = (first && k == 0) ? 0u : 1u;
+                    mma_f16_ss(tmem + kColDV, d_pt + aop, d_omn + qoff + rows, id_g, acc);
+                    mma_f16_ss(tmem + kColDK, d_dst + aop, d_qmn + qoff + rows, id_g, acc);
+                    mma_f16_ss(tmem + kColDQ + 64 * qs, d_dsmn + rows, d_kmn + toff + rows, id_q,
+                               k > 0 ? 1u : 0u);
+                }
+                mma_commit(opempty);
+                mma_commit(&qempty[qs]);
+                mma_commit(&dqfull[qs]);
+                if (last) {
+                    mma_commit(accfull);
+                    mma_commit(&kvempty[tb]);
+                }
+            }
+            __syncwarp();
+            return true;
+        };
+        uint32_t gc = 0, it = 0, prev = 0, prev_it = 0;
+        int prev_tb = 0;
+        bool ok = true, have_prev = false, prev_first = false, prev_last = false;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            KTile tl;
+            if (!decode_ktile(g, t, xt, tl)) continue;
+            // the previous tile's last gradient products go first: its
+            // epilogue need not wait for this tile's loads
+            if (have_prev) {
+                have_prev = false;
+                if (!issue_grad(prev, prev_first, prev_last, prev_tb, prev_it)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const int tb = it & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&kvfull[tb], (it >> 1) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            const uint64_t toff = (uint64_t)((tb * kKV) >> 4);
+            for (int c = 0; c < tl.nck; ++c, ++gc) {
+                const int qs = gc & 1;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&qfull[qs], (gc >> 1) & 1, abort_flag, p.err) &&
+                                    mbar_wait(sempty, (gc & 1) ^ 1, abort_flag, p.err));
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t qoff = (uint64_t)((qs * kQS) >> 4);
+                if (lane == 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16_ss(tmem + kColS, d_k + toff + 2 * k, d_q + qoff + 2 * k, id_s, k > 0);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16_ss(tmem + kColDP, d_v + toff + 2 * k, d_o + qoff + 2 * k, id_s, k > 0);
+                    mma_commit(sfull);
+                }
+                __syncwarp();
+                if (have_prev && !issue_grad(prev, prev_first, prev_last, prev_tb, prev_it)) {
+                    ok = false;
+                    break;
+                }
+                have_prev = true;
+                prev = gc;
+                prev_first = c == 0;
+                prev_last = c == tl.nck - 1;
+                prev_tb = tb;
+                prev_it = it;
+            }
+            ++it;
+        }
+        if (ok && have_prev) issue_grad(prev, prev_first, prev_last, prev_tb, prev_it);
+        if (lane == 0) mma_commit(mmadone);
+        __syncwarp();
+        mbar_wait(mmadone, 0, no_abort, nullptr, 100000000ull);
+    } else {
+        // ---------------- softmax warps: thread = key row ----------------
+        const int quarter = warp & 3;
+        const int part = (warp - 2) >> 2;        // query columns [32 part, 32 part + 32)
+        const int m = quarter * 32 + lane;       // TMEM lane: key of the tile / query of a dQ chunk
+        const float xscale = p.scale * kLog2e;
+        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
+        const uint32_t prow = smem_u32(pt_op) + (part >> 1) * (kOpBytes / 2) + m * 128;
+        const uint32_t drow = smem_u32(dst_op) + (part >> 1) * (kOpBytes / 2) + m * 128;
+        uint32_t gc = 0, it = 0;
+        bool ok = true;
+        // the dQ chunk waiting to be added to the accumulator
+        bool dq_pend = false;
+        uint32_t dq_g = 0;
+        long long dq_row = 0;
+        bool dq_ok = false;
+        auto drain_dq = [&]() -> bool {
+            const int qs = dq_g & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&dqfull[qs], (dq_g >> 1) & 1, abort_flag, p.err)))
+                return false;
+            tc_fence_after();
+            uint32_t v[16];
+            tmem_ld16(lane_base + kColDQ + 64 * qs + 16 * part, v);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&dqempty[qs]);
+            if (dq_ok) {
+                float *dst = p.dqacc + dq_row * 64 + 16 * part;
+                const float sc = p.scale;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    red_add4(dst + 4 * u, sc * __uint_as_float(v[4 * u]), sc * __uint_as_float(v[4 * u + 1]),
+                             sc * __uint_as_float(v[4 * u + 2]), sc * __uint_as_float(v[4 * u + 3]));
+            }
+            dq_pend = false;
+            return true;
+        };
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            KTile tl;
+            if (!decode_ktile(g, t, xt, tl)) continue;
+            const int kk = tl.a0 + m;
+            for (int c = 0; c < tl.nck; ++c, ++gc) {
+                const int qs = gc & 1;
+                const int qbase = tl.qb_lo + c * kB;
+                const int cbase = qbase + 32 * part;
+                // this key's queries inside the part: columns [jlo, jhi]
+                const int jlo = max(kk - g.wu - cbase, 0);
+                const int jhi = min(min(kk + g.w, tl.nr - 1) - cbase, 31);
+                const uint32_t vmask =
+                    (kk >= tl.nr || jlo > jhi) ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
+                const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
+                const bool empty = __all_sync(0xffffffffu, vmask == 0u);
+                if (!__all_sync(0xffffffffu, mbar_wait(sfull, gc & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (!empty &&
+                    !__all_sync(0xffffffffu, mbar_wait(&qsfull[qs], (gc >> 1) & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                const float4 *l4 = reinterpret_cast<const float4 *>(qstat + qs * 2 * kB + 32 * part);
+                const float4 *d4 = reinterpret_cast<const float4 *>(qstat + qs * 2 * kB + kB + 32 * part);
+                const uint64_t xs2 = f2(xscale, xscale);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // columns [16h, 16h + 16) of the part
+                    uint32_t sv[16], dv[16];
+                    tmem_ld16(lane_base + kColS + 32 * part + 16 * h, sv);
+                    tmem_ld16(lane_base + kColDP + 32 * part + 16 * h, dv);
+                    tmem_ld_wait();
+                    if (h == 1) {
+                        tc_fence_before();
+                        mbar_arrive(sempty);   // S^T and dP^T are in registers
+                    }
+                    if (empty) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) pk[8 * h + i] = dk[8 * h + i] = 0u;
+                        continue;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 lq = l4[4 * h + u], dq = d4[4 * h + u];
+                        const int i = 4 * u;           // within the half
+                        const int j = 16 * h + i;      // within the part
+                        float p0, p1, p2, p3;
+                        {
+                            float y0, y1, y2, y3;
+                            f2split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), xs2, f2(-lq.x, -lq.y)), y0, y1);
+                            f2split(fma2(f2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), xs2, f2(-lq.z, -lq.w)), y2, y3);
+                            p0 = ex2(y0);
+                            p1 = ex2(y1);
+                            p2 = ex2(y2);
+                            p3 = ex2(y3);
+                        }
+                        if (!full) {
+                            if (!((vmask >> j) & 1u)) p0 = 0.f;
+                            if (!((vmask >> (j + 1)) & 1u)) p1 = 0.f;
+                            if (!((vmask >> (j + 2)) & 1u)) p2 = 0.f;
+                            if (!((vmask >> (j + 3)) & 1u)) p3 = 0.f;
+                        }
+                        float s0, s1, s2, s3;
+                        f2split(mul2(f2(p0, p1), sub2(f2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), f2(dq.x, dq.y))), s0, s1);
+                        f2split(mul2(f2(p2, p3), sub2(f2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2(dq.z, dq.w))), s2, s3);
+                        pk[8 * h + 2 * u] = pack2<T>(p0, p1);
+                        pk[8 * h + 2 * u + 1] = pack2<T>(p2, p3);
+                        dk[8 * h + 2 * u] = pack2<T>(s0, s1);
+                        dk[8 * h + 2 * u + 1] = pack2<T>(s2, s3);
+                    }
+                }
+                // the operands of chunk gc-1 have been consumed
+                if (!__all_sync(0xffffffffu, mbar_wait(opempty, (gc & 1) ^ 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t off = (uint32_t)((((part & 1) * 4 + u) ^ (m & 7)) << 4);
+                    sts16(prow + off, make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+                    sts16(drow + off, make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(opfull);
+                if (dq_pend && !drain_dq()) {
+                    ok = false;
+                    break;
+                }
+                dq_pend = true;
+                dq_g = gc;
+                const int dq_q = qbase + m;
+                dq_ok = dq_q < tl.nr;
+                dq_row = (long long)tl.bh * g.n + tl.r + (long long)g.s * dq_q;
+            }
+            if (!ok) break;
+            // ---------------- tile epilogue: dV, dK of these 128 keys ----------------
+            if (!__all_sync(0xffffffffu, mbar_wait(accfull, it & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t a[16], b[16];
+            tmem_ld16(lane_base + kColDV + 16 * part, a);
+            tmem_ld16(lane_base + kColDK + 16 * part, b);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(accempty);
+            if (kk < tl.nr) {
+                const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * kk;
+                uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + row * 64 + 16 * part);
+                uint4 *k4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dK) + row * 64 + 16 * part);
+                const float sc = p.scale;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int i = 8 * u;
+                    v4[u] = make_uint4(pack2<T>(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
+                                       pack2<T>(__uint_as_float(a[i + 2]), __uint_as_float(a[i + 3])),
+                                       pack2<T>(__uint_as_float(a[i + 4]), __uint_as_float(a[i + 5])),
+                                       pack2<T>(__uint_as_float(a[i + 6]), __uint_as_float(a[i + 7])));
+                    k4[u] = make_uint4(pack2<T>(sc * __uint_as_float(b[i]), sc * __uint_as_float(b[i + 1])),
+                                       pack2<T>(sc * __uint_as_float(b[i + 2]), sc * __uint_as_float(b[i + 3])),
+                                       pack2<T>(sc * __uint_as_float(b[i + 4]), sc * __uint_as_float(b[i + 5])),
+                                       pack2<T>(sc * __uint_as_float(b[i + 6]), sc * __uint_as_float(b[i + 7])));
+                }
+            }
+            ++it;
+        }
+        if (ok && dq_pend) drain_dq();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // exact fp32 path: one CTA per row, one thread per channel; the backward of the
 // fp32 fused forward, recomputing each slot's probability from lse.
 //   dQ pass (rows = queries), then dK / dV pass (rows = keys).
@@ -676,7 +1153,37 @@ cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, co
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const TmapSet &mo,
+                           const BwdArgs &a, cudaStream_t st) {
+    const long long rows = (long long)a.g.BH * a.g.n;
+    const long long per_block = 8LL * kDeltaRowsPerWarp;
+    k_bwd_delta<T><<<(unsigned)((rows + per_block - 1) / per_block), 256, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long tiles = (long long)((a.g.nsub + kB - 1) / kB) * a.g.s * a.g.BH;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    e = cudaFuncSetAttribute(k_bwd_fused<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, fused::kSmem);
+    if (e != cudaSuccess) return e;
+    k_bwd_fused<T><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long groups = rows * 8;
+    k_bwd_dq_out<T><<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const TmapSet &mk,
+                                            const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,
+                                            cudaStream_t st) {
+    if (!a.dqacc) return cudaErrorInvalidValue;
+    if (dt == kF16) return launch_fused_t<__half>(mq, mk, mv, mo, a, st);
+    return launch_fused_t<__nv_bfloat16>(mq, mk, mv, mo, a, st);
+}
 
 cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const TmapSet &mk,
                                          const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,

@@ -402,7 +402,11 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
 
 SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc) {
     if (!desc || desc->b < 1 || desc->h < 1 || desc->n < 1) return 0;
-    return (size_t)desc->b * desc->h * desc->n * sizeof(float);
+    const size_t rows = (size_t)desc->b * desc->h * desc->n;
+    const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
+    if (desc->dtype == SWAB_F32) return delta;
+    // fp16 / bf16: the per-row delta, then the fp32 dQ accumulator [rows, 64]
+    return delta + rows * 64 * sizeof(float);
 }
 
 SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, const void *Q,
@@ -424,7 +428,10 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
         return SWAB_ERR_CUDA;
     a.err = status_word();
     if (!a.err) return SWAB_ERR_CUDA;
-    return from_cuda(launch_band_attention_bwd_tc(dt, mq, mk, mv, mo, a, st));
+    const size_t rows = (size_t)g.BH * g.n;
+    a.dqacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                        (rows * sizeof(float) + 255) / 256 * 256);
+    return from_cuda(launch_band_attention_bwd_fused(dt, mq, mk, mv, mo, a, st));
 }
 
 SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float scale, const void *Q,

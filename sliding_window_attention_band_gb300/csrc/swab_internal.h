@@ -115,6 +115,7 @@ struct BwdArgs {      // fused backward
     float *delta;     // workspace [BH, n]
     void *dQ, *dK, *dV;
     unsigned *err;
+    float *dqacc;     // fused tensor-core path: fp32 dQ accumulator [BH, n, 64], or null
 };
 
 struct DenseArgs {    // fp32 FFMA path
@@ -139,6 +140,10 @@ cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const Tmap
                                          const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,
                                          cudaStream_t st);
 cudaError_t launch_band_attention_bwd_f32(const BwdArgs &a, cudaStream_t st);
+// one-pass backward (dK, dV and dQ in one persistent kernel; needs a.dqacc)
+cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const TmapSet &mk,
+                                            const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,
+                                            cudaStream_t st);
 // SM count of the current device (swab_api.cu); 0 on error
 int device_sm_count();
 // the module-scope delta scratch of band_attention_bwd_noalloc (k_attention_bwd.cu)
