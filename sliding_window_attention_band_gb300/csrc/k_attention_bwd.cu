@@ -162,15 +162,16 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
     }
 }
 
-// dQ = accumulator (already scaled), rounded to the output type: 8 channels per thread
+// dQ = scale * accumulator, rounded to the output type: 8 channels per thread
 template <typename T>
 __global__ void __launch_bounds__(256) k_bwd_dq_out(const BwdArgs p) {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8-channel group
     if (i >= (long long)p.g.BH * p.g.n * 8) return;
     const float4 *acc = reinterpret_cast<const float4 *>(p.dqacc) + 2 * i;
     const float4 a = acc[0], b = acc[1];
-    reinterpret_cast<uint4 *>(p.dQ)[i] =
-        make_uint4(pack2<T>(a.x, a.y), pack2<T>(a.z, a.w), pack2<T>(b.x, b.y), pack2<T>(b.z, b.w));
+    const float c = p.scale;
+    reinterpret_cast<uint4 *>(p.dQ)[i] = make_uint4(pack2<T>(c * a.x, c * a.y), pack2<T>(c * a.z, c * a.w),
+                                                    pack2<T>(c * b.x, c * b.y), pack2<T>(c * b.z, c * b.w));
 }
 
 // ---------------------------------------------------------------------------
@@ -612,26 +613,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 // One-pass backward: dK, dV and dQ from one persistent kernel.
 // Tile = 128 keys of one residue; for each 128-query chunk of its band:
 //   S^T = K Q_c^T, dP^T = V dO_c^T               (tcgen05, TMEM lane = key)
-//   P^T, dS^T per key row (16 warps: 4 per TMEM lane quarter, each owning 32
-//   query columns), written as K-major 128-B-swizzled operands
-//   dV += P^T dO_c, dK += dS^T Q_c                (TMEM, lane = key)
+//   P^T, dS^T per key row (16 softmax warps: 4 per TMEM lane quarter, each
+//   owning 32 query columns): P^T into tensor memory (packed 16-bit pairs),
+//   dS^T as a K-major 128-B-swizzled shared-memory operand
+//   dV += P^T dO_c (A from TMEM), dK += dS^T Q_c   (TMEM, lane = key)
 //   dQ_c = dS K: the dS^T tile read as an MN-major A operand (M = queries),
-//   the K tile as an MN-major B operand, into one of two TMEM buffers
-//   (lane = query); the softmax warps add scale * dQ_c into an fp32
-//   accumulator with vector reductions one chunk later.
-// The per-query lse and delta of a chunk are staged into shared memory by the
-// producer warp next to the chunk's Q and dO tiles.  The accumulation order of
-// dQ across key tiles is not fixed, so dQ may differ in the last bits between
-// runs; dK and dV have one writer per row.
+//   the K tile as an MN-major B operand, into a TMEM buffer (lane = query).
+//   One chunk later the softmax warps copy dQ_c into a swizzled fp32
+//   staging tile and a reducer warp adds it into the fp32 accumulator with
+//   two TMA reduce-add stores (the final scale and rounding happen in
+//   k_bwd_dq_out).  K and V are double-buffered across tiles, and the chunk
+//   sequence runs on across tile boundaries: a tile's dV and dK are read out
+//   of TMEM during the next tile's first chunk, once its products are done.
+// Each softmax warp loads the lse and delta of its 32 query columns itself
+// (one of each per lane) and shares them through a per-warp shared slot.
+// The accumulation order of dQ across key tiles is not fixed, so dQ may
+// differ in the last bits between runs; dK and dV have one writer per row.
 // ---------------------------------------------------------------------------
 namespace fused {
 constexpr int kParts = 4;
-constexpr int kWorkers = 32 * 4 * kParts;       // 512
-constexpr int kThreads = 64 + kWorkers;
+constexpr int kWorkerWarps = 4 * kParts;        // 16
+constexpr int kWorkers = 32 * kWorkerWarps;     // 512
+constexpr int kReducerWarp = 2 + kWorkerWarps;  // 18
+constexpr int kThreads = 32 * (kReducerWarp + 1);
 constexpr int kKV = 2 * kTile;                  // K and V of a key tile: 32 KB
 constexpr int kQS = 2 * kTile;                  // Q and dO of a query chunk: 32 KB
-constexpr int kSmem = 2 * kKV + 2 * kQS + 2 * kOpBytes + 2 * 2 * kB * 4 + 1024 + 1024;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr int kStage = 128 * 64 * 4;            // fp32 dQ staging: two 128 x 32 swizzled halves
+constexpr int kSlot = 2 * 32 * 4;               // per softmax warp: lse*log2e, delta of 32 queries
+constexpr int kSmem = 2 * kKV + 2 * kQS + kOpBytes + kStage + kWorkerWarps * kSlot + 1024 + 1024;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColP = 448;
 
 struct KTile {
     int a0, r, bh, nr, qb_lo, qb_hi, nck;
@@ -656,30 +666,29 @@ template <typename T>
 __global__ void __launch_bounds__(fused::kThreads, 1)
     k_bwd_fused(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
                 const __grid_constant__ TmapSet mapV, const __grid_constant__ TmapSet mapdO,
-                const BwdArgs p) {
+                const __grid_constant__ TmapSet mapAcc, const BwdArgs p) {
     using namespace fused;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *kvbuf = base;                      // [2] key tiles: K at +0, V at +kTile
     uint8_t *qsbuf = kvbuf + 2 * kKV;           // [2] query chunks: Q at +0, dO at +kTile
-    uint8_t *pt_op = qsbuf + 2 * kQS;           // P^T  [128 keys x 128 queries]
-    uint8_t *dst_op = pt_op + kOpBytes;         // dS^T
-    float *qstat = reinterpret_cast<float *>(dst_op + kOpBytes);  // [2][lse*log2e | delta][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(qstat + 2 * 2 * kB);
+    uint8_t *dst_op = qsbuf + 2 * kQS;          // dS^T [128 keys x 128 queries]
+    uint8_t *stage = dst_op + kOpBytes;         // fp32 dQ: channels [0,32) at +0, [32,64) at +16 KB
+    float *slots = reinterpret_cast<float *>(stage + kStage);  // [16 warps][lse | delta][32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(slots + kWorkerWarps * 64);
     uint64_t *kvfull = bars;           // [2]
     uint64_t *kvempty = kvfull + 2;    // [2]
     uint64_t *qfull = kvempty + 2;     // [2]
     uint64_t *qempty = qfull + 2;      // [2]
-    uint64_t *qsfull = qempty + 2;     // [2] count 32 (producer lanes)
-    uint64_t *sfull = qsfull + 2;      // 1
+    uint64_t *sfull = qempty + 2;      // 1
     uint64_t *sempty = sfull + 1;      // 1, count fused::kWorkers
     uint64_t *opfull = sempty + 1;     // 1, count fused::kWorkers
-    uint64_t *opempty = opfull + 1;    // 1
-    uint64_t *dqfull = opempty + 1;    // [2]
-    uint64_t *dqempty = dqfull + 2;    // [2], count fused::kWorkers
-    uint64_t *accfull = dqempty + 2;   // 1
-    uint64_t *accempty = accfull + 1;  // 1, count fused::kWorkers
+    uint64_t *opempty = opfull + 1;    // 1 (also: dQ of that chunk is in TMEM)
+    uint64_t *dqempty = opempty + 1;   // 1, count fused::kWorkers: dQ read out of TMEM
+    uint64_t *stfull = dqempty + 1;    // 1, count fused::kWorkers
+    uint64_t *stempty = stfull + 1;    // 1
+    uint64_t *accempty = stempty + 1;  // 1, count fused::kWorkers: dV, dK of a tile read out
     uint64_t *mmadone = accempty + 1;  // 1
     uint64_t *drain = mmadone + 1;     // a flag word that is never set
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
@@ -693,19 +702,18 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&kvfull[i], 1);
-            mbar_init(&kvempty[i], 1);
             mbar_init(&qfull[i], 1);
             mbar_init(&qempty[i], 1);
-            mbar_init(&qsfull[i], 32);
-            mbar_init(&dqfull[i], 1);
-            mbar_init(&dqempty[i], fused::kWorkers);
+            mbar_init(&kvfull[i], 1);
+            mbar_init(&kvempty[i], 1);
         }
+        mbar_init(dqempty, fused::kWorkers);
         mbar_init(sfull, 1);
         mbar_init(sempty, fused::kWorkers);
         mbar_init(opfull, fused::kWorkers);
         mbar_init(opempty, 1);
-        mbar_init(accfull, 1);
+        mbar_init(stfull, fused::kWorkers);
+        mbar_init(stempty, 1);
         mbar_init(accempty, fused::kWorkers);
         mbar_init(mmadone, 1);
         *no_abort = 0;
@@ -744,33 +752,20 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             }
             __syncwarp();
             ++it;
-            for (int c = 0; c < tl.nck; ++c) {
+            for (int c = 0; c < tl.nck; ++c, ++gc) {
                 const int qs = gc & 1;
                 if (!__all_sync(0xffffffffu,
                                 mbar_wait(&qempty[qs], ((gc >> 1) & 1) ^ 1, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
-                const int qbase = tl.qb_lo + c * kB;
                 if (lane == 0) {
+                    const int qbase = tl.qb_lo + c * kB;
                     mbar_arrive_expect_tx(&qfull[qs], kQS);
                     tma_load_3d(qsbuf + qs * kQS, mq, &qfull[qs], 0, qbase, tl.bh);
                     tma_load_3d(qsbuf + qs * kQS + kTile, mo, &qfull[qs], 0, qbase, tl.bh);
                 }
-                // lse (log2 units) and delta of the chunk's 128 queries, 4 per lane
-                float lv[4], dv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int qq = qbase + 4 * lane + e;
-                    const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * qq;
-                    lv[e] = qq < tl.nr ? p.lse[row] * kLog2e : 0.f;
-                    dv[e] = qq < tl.nr ? p.delta[row] : 0.f;
-                }
-                float4 *st4 = reinterpret_cast<float4 *>(qstat + qs * 2 * kB);
-                st4[lane] = make_float4(lv[0], lv[1], lv[2], lv[3]);
-                st4[kB / 4 + lane] = make_float4(dv[0], dv[1], dv[2], dv[3]);
-                mbar_arrive(&qsfull[qs]);
-                ++gc;
+                __syncwarp();
             }
         }
         // every copy issued lands before the CTA may exit
@@ -792,15 +787,16 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         const uint64_t d_o = sdesc_sw128(smem_u32(qsbuf + kTile), 16, 1024);   // dO, K-major
         const uint64_t d_qmn = sdesc_sw128(smem_u32(qsbuf), 1024, 1024);       // Q as MN-major B
         const uint64_t d_omn = sdesc_sw128(smem_u32(qsbuf + kTile), 1024, 1024);  // dO as MN-major B
-        const uint64_t d_pt = sdesc_sw128(smem_u32(pt_op), 16, 1024);          // P^T, K-major A
         const uint64_t d_dst = sdesc_sw128(smem_u32(dst_op), 16, 1024);        // dS^T, K-major A
         // dS^T read as dS (M = queries): 64-query blocks kOpBytes/2 apart,
         // 8-key groups 1024 B apart
         const uint64_t d_dsmn = sdesc_sw128(smem_u32(dst_op), kOpBytes / 2, 1024);
         auto issue_grad = [&](uint32_t gg, bool first, bool last, int tb, uint32_t itt) -> bool {
             const int qs = gg & 1;
+            // the softmax warps read dQ of chunk gg-1 out of TMEM in chunk gg
+            // (phase gg of dqempty), before they signal its operands
             bool w = mbar_wait(opfull, gg & 1, abort_flag, p.err) &&
-                     mbar_wait(&dqempty[qs], ((gg >> 1) & 1) ^ 1, abort_flag, p.err);
+                     mbar_wait(dqempty, gg & 1, abort_flag, p.err);
             if (first) w = w && mbar_wait(accempty, (itt & 1) ^ 1, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, w)) return false;
             tc_fence_after();
@@ -812,18 +808,13 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                     const uint64_t aop = (uint64_t)((((k >> 2) * (kOpBytes / 2)) + (k & 3) * 32) >> 4);
                     const uint64_t rows = (uint64_t)((2048 * k) >> 4);
                     const uint32_t acc = (first && k == 0) ? 0u : 1u;
-                    mma_f16_ss(tmem + kColDV, d_pt + aop, d_omn + qoff + rows, id_g, acc);
+                    mma_f16_ts(tmem + kColDV, tmem + kColP + 8 * k, d_omn + qoff + rows, id_g, acc);
                     mma_f16_ss(tmem + kColDK, d_dst + aop, d_qmn + qoff + rows, id_g, acc);
-                    mma_f16_ss(tmem + kColDQ + 64 * qs, d_dsmn + rows, d_kmn + toff + rows, id_q,
-                               k > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + kColDQ, d_dsmn + rows, d_kmn + toff + rows, id_q, k > 0 ? 1u : 0u);
                 }
-                mma_commit(opempty);
+                mma_commit(opempty);   // also: dV, dK of the tile are complete after its last chunk
                 mma_commit(&qempty[qs]);
-                mma_commit(&dqfull[qs]);
-                if (last) {
-                    mma_commit(accfull);
-                    mma_commit(&kvempty[tb]);
-                }
+                if (last) mma_commit(&kvempty[tb]);
             }
             __syncwarp();
             return true;
@@ -834,15 +825,6 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             KTile tl;
             if (!decode_ktile(g, t, xt, tl)) continue;
-            // the previous tile's last gradient products go first: its
-            // epilogue need not wait for this tile's loads
-            if (have_prev) {
-                have_prev = false;
-                if (!issue_grad(prev, prev_first, prev_last, prev_tb, prev_it)) {
-                    ok = false;
-                    break;
-                }
-            }
             const int tb = it & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&kvfull[tb], (it >> 1) & 1, abort_flag, p.err))) {
                 ok = false;
@@ -884,6 +866,32 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         if (lane == 0) mma_commit(mmadone);
         __syncwarp();
         mbar_wait(mmadone, 0, no_abort, nullptr, 100000000ull);
+    } else if (warp == kReducerWarp) {
+        // ---------------- reducer: staged dQ tiles into the accumulator ----------------
+        uint32_t gc = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            KTile tl;
+            if (!decode_ktile(g, t, xt, tl)) continue;
+            const CUtensorMap *ma = &mapAcc.m[tl.r];
+            for (int c = 0; c < tl.nck; ++c, ++gc) {
+                if (!__all_sync(0xffffffffu, mbar_wait(stfull, gc & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const int qbase = tl.qb_lo + c * kB;
+                    tma_reduce_add_3d(ma, stage, 0, qbase, tl.bh);
+                    tma_reduce_add_3d(ma, stage + kStage / 2, 32, qbase, tl.bh);
+                    bulk_commit();
+                    bulk_wait_read();
+                    mbar_arrive(stempty);
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     } else {
         // ---------------- softmax warps: thread = key row ----------------
         const int quarter = warp & 3;
@@ -891,151 +899,27 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         const int m = quarter * 32 + lane;       // TMEM lane: key of the tile / query of a dQ chunk
         const float xscale = p.scale * kLog2e;
         const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
-        const uint32_t prow = smem_u32(pt_op) + (part >> 1) * (kOpBytes / 2) + m * 128;
         const uint32_t drow = smem_u32(dst_op) + (part >> 1) * (kOpBytes / 2) + m * 128;
+        const uint32_t srow = smem_u32(stage) + (part >> 1) * (kStage / 2) + m * 128;
+        float *slot = slots + (warp - 2) * 64;
         uint32_t gc = 0, it = 0;
         bool ok = true;
-        // the dQ chunk waiting to be added to the accumulator
-        bool dq_pend = false;
+        bool dq_pend = false;   // the dQ of chunk dq_g (in TMEM) waits to be staged
         uint32_t dq_g = 0;
-        long long dq_row = 0;
-        bool dq_ok = false;
-        auto drain_dq = [&]() -> bool {
-            const int qs = dq_g & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&dqfull[qs], (dq_g >> 1) & 1, abort_flag, p.err)))
-                return false;
-            tc_fence_after();
-            uint32_t v[16];
-            tmem_ld16(lane_base + kColDQ + 64 * qs + 16 * part, v);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&dqempty[qs]);
-            if (dq_ok) {
-                float *dst = p.dqacc + dq_row * 64 + 16 * part;
-                const float sc = p.scale;
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    red_add4(dst + 4 * u, sc * __uint_as_float(v[4 * u]), sc * __uint_as_float(v[4 * u + 1]),
-                             sc * __uint_as_float(v[4 * u + 2]), sc * __uint_as_float(v[4 * u + 3]));
-            }
-            dq_pend = false;
-            return true;
-        };
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            KTile tl;
-            if (!decode_ktile(g, t, xt, tl)) continue;
-            const int kk = tl.a0 + m;
-            for (int c = 0; c < tl.nck; ++c, ++gc) {
-                const int qs = gc & 1;
-                const int qbase = tl.qb_lo + c * kB;
-                const int cbase = qbase + 32 * part;
-                // this key's queries inside the part: columns [jlo, jhi]
-                const int jlo = max(kk - g.wu - cbase, 0);
-                const int jhi = min(min(kk + g.w, tl.nr - 1) - cbase, 31);
-                const uint32_t vmask =
-                    (kk >= tl.nr || jlo > jhi) ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
-                const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
-                const bool empty = __all_sync(0xffffffffu, vmask == 0u);
-                if (!__all_sync(0xffffffffu, mbar_wait(sfull, gc & 1, abort_flag, p.err))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (!empty &&
-                    !__all_sync(0xffffffffu, mbar_wait(&qsfull[qs], (gc >> 1) & 1, abort_flag, p.err))) {
-                    ok = false;
-                    break;
-                }
-                const float4 *l4 = reinterpret_cast<const float4 *>(qstat + qs * 2 * kB + 32 * part);
-                const float4 *d4 = reinterpret_cast<const float4 *>(qstat + qs * 2 * kB + kB + 32 * part);
-                const uint64_t xs2 = f2(xscale, xscale);
-                uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // columns [16h, 16h + 16) of the part
-                    uint32_t sv[16], dv[16];
-                    tmem_ld16(lane_base + kColS + 32 * part + 16 * h, sv);
-                    tmem_ld16(lane_base + kColDP + 32 * part + 16 * h, dv);
-                    tmem_ld_wait();
-                    if (h == 1) {
-                        tc_fence_before();
-                        mbar_arrive(sempty);   // S^T and dP^T are in registers
-                    }
-                    if (empty) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) pk[8 * h + i] = dk[8 * h + i] = 0u;
-                        continue;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float4 lq = l4[4 * h + u], dq = d4[4 * h + u];
-                        const int i = 4 * u;           // within the half
-                        const int j = 16 * h + i;      // within the part
-                        float p0, p1, p2, p3;
-                        {
-                            float y0, y1, y2, y3;
-                            f2split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), xs2, f2(-lq.x, -lq.y)), y0, y1);
-                            f2split(fma2(f2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), xs2, f2(-lq.z, -lq.w)), y2, y3);
-                            p0 = ex2(y0);
-                            p1 = ex2(y1);
-                            p2 = ex2(y2);
-                            p3 = ex2(y3);
-                        }
-                        if (!full) {
-                            if (!((vmask >> j) & 1u)) p0 = 0.f;
-                            if (!((vmask >> (j + 1)) & 1u)) p1 = 0.f;
-                            if (!((vmask >> (j + 2)) & 1u)) p2 = 0.f;
-                            if (!((vmask >> (j + 3)) & 1u)) p3 = 0.f;
-                        }
-                        float s0, s1, s2, s3;
-                        f2split(mul2(f2(p0, p1), sub2(f2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), f2(dq.x, dq.y))), s0, s1);
-                        f2split(mul2(f2(p2, p3), sub2(f2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2(dq.z, dq.w))), s2, s3);
-                        pk[8 * h + 2 * u] = pack2<T>(p0, p1);
-                        pk[8 * h + 2 * u + 1] = pack2<T>(p2, p3);
-                        dk[8 * h + 2 * u] = pack2<T>(s0, s1);
-                        dk[8 * h + 2 * u + 1] = pack2<T>(s2, s3);
-                    }
-                }
-                // the operands of chunk gc-1 have been consumed
-                if (!__all_sync(0xffffffffu, mbar_wait(opempty, (gc & 1) ^ 1, abort_flag, p.err))) {
-                    ok = false;
-                    break;
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t off = (uint32_t)((((part & 1) * 4 + u) ^ (m & 7)) << 4);
-                    sts16(prow + off, make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
-                    sts16(drow + off, make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(opfull);
-                if (dq_pend && !drain_dq()) {
-                    ok = false;
-                    break;
-                }
-                dq_pend = true;
-                dq_g = gc;
-                const int dq_q = qbase + m;
-                dq_ok = dq_q < tl.nr;
-                dq_row = (long long)tl.bh * g.n + tl.r + (long long)g.s * dq_q;
-            }
-            if (!ok) break;
-            // ---------------- tile epilogue: dV, dK of these 128 keys ----------------
-            if (!__all_sync(0xffffffffu, mbar_wait(accfull, it & 1, abort_flag, p.err))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
+        bool acc_pend = false, acc_ok = false;   // a tile's dV, dK wait to be read out
+        long long acc_row = 0;
+        // dV, dK of key row acc_row (channels [16 part, +16)); the caller has
+        // waited for the tile's last products
+        auto drain_acc = [&]() {
             uint32_t a[16], b[16];
             tmem_ld16(lane_base + kColDV + 16 * part, a);
             tmem_ld16(lane_base + kColDK + 16 * part, b);
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(accempty);
-            if (kk < tl.nr) {
-                const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * kk;
-                uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + row * 64 + 16 * part);
-                uint4 *k4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dK) + row * 64 + 16 * part);
+            if (acc_ok) {
+                uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + acc_row * 64 + 16 * part);
+                uint4 *k4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dK) + acc_row * 64 + 16 * part);
                 const float sc = p.scale;
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -1050,9 +934,161 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                                        pack2<T>(sc * __uint_as_float(b[i + 6]), sc * __uint_as_float(b[i + 7])));
                 }
             }
+        };
+
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            KTile tl;
+            if (!decode_ktile(g, t, xt, tl)) continue;
+            const int kk = tl.a0 + m;
+            for (int c = 0; c < tl.nck; ++c, ++gc) {
+                const int qbase = tl.qb_lo + c * kB;
+                const int cbase = qbase + 32 * part;
+                // this key's queries inside the part: columns [jlo, jhi]
+                const int jlo = max(kk - g.wu - cbase, 0);
+                const int jhi = min(min(kk + g.w, tl.nr - 1) - cbase, 31);
+                const uint32_t vmask =
+                    (kk >= tl.nr || jlo > jhi) ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
+                const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
+                const bool empty = __all_sync(0xffffffffu, vmask == 0u);
+                // lse (log2 units) and delta of query column `lane` of the part
+                float lq = 0.f, dq = 0.f;
+                if (!empty && cbase + lane < tl.nr) {
+                    const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * (cbase + lane);
+                    lq = p.lse[row] * kLog2e;
+                    dq = p.delta[row];
+                }
+                if (!__all_sync(0xffffffffu, mbar_wait(sfull, gc & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                __syncwarp();   // the previous chunk's reads of the slot are done
+                slot[lane] = lq;
+                slot[32 + lane] = dq;
+                __syncwarp();
+                const float4 *l4 = reinterpret_cast<const float4 *>(slot);
+                const float4 *d4 = reinterpret_cast<const float4 *>(slot + 32);
+                const uint64_t xs2 = f2(xscale, xscale);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    // columns [8h, 8h + 8) of the part
+                    uint32_t sv[8], dv[8];
+                    tmem_ld8(lane_base + kColS + 32 * part + 8 * h, sv);
+                    tmem_ld8(lane_base + kColDP + 32 * part + 8 * h, dv);
+                    tmem_ld_wait();
+                    if (h == 3) {
+                        tc_fence_before();
+                        mbar_arrive(sempty);   // S^T and dP^T are in registers
+                    }
+                    if (empty) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) pk[4 * h + i] = dk[4 * h + i] = 0u;
+                        continue;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float4 lv = l4[2 * h + u], dl = d4[2 * h + u];
+                        const int i = 4 * u;           // within the step
+                        const int j = 8 * h + i;       // within the part
+                        float p0, p1, p2, p3;
+                        {
+                            float y0, y1, y2, y3;
+                            f2split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), xs2, f2(-lv.x, -lv.y)), y0, y1);
+                            f2split(fma2(f2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), xs2, f2(-lv.z, -lv.w)), y2, y3);
+                            p0 = ex2(y0);
+                            p1 = ex2(y1);
+                            p2 = ex2(y2);
+                            p3 = ex2(y3);
+                        }
+                        if (!full) {
+                            if (!((vmask >> j) & 1u)) p0 = 0.f;
+                            if (!((vmask >> (j + 1)) & 1u)) p1 = 0.f;
+                            if (!((vmask >> (j + 2)) & 1u)) p2 = 0.f;
+                            if (!((vmask >> (j + 3)) & 1u)) p3 = 0.f;
+                        }
+                        float s0, s1, s2, s3;
+                        f2split(mul2(f2(p0, p1), sub2(f2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), f2(dl.x, dl.y))), s0, s1);
+                        f2split(mul2(f2(p2, p3), sub2(f2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2(dl.z, dl.w))), s2, s3);
+                        pk[4 * h + 2 * u] = pack2<T>(p0, p1);
+                        pk[4 * h + 2 * u + 1] = pack2<T>(p2, p3);
+                        dk[4 * h + 2 * u] = pack2<T>(s0, s1);
+                        dk[4 * h + 2 * u + 1] = pack2<T>(s2, s3);
+                    }
+                }
+                // the products of chunk gc-1 are done: its operands are free,
+                // its dQ is in TMEM and, at a tile boundary, the previous
+                // tile's dV and dK are complete
+                if (!__all_sync(0xffffffffu, mbar_wait(opempty, (gc & 1) ^ 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // P^T: query columns [32 part, +32) are TMEM columns [16 part, +16) of the P region
+                tmem_st16(lane_base + kColP + 16 * part, pk);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t off = (uint32_t)((((part & 1) * 4 + u) ^ (m & 7)) << 4);
+                    sts16(drow + off, make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
+                }
+                tmem_st_wait();
+                if (acc_pend) {
+                    drain_acc();
+                    acc_pend = false;
+                }
+                uint32_t dqv[16];
+                if (dq_pend) {
+                    tmem_ld16(lane_base + kColDQ + 16 * part, dqv);
+                    tmem_ld_wait();
+                }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                mbar_arrive(dqempty);
+                mbar_arrive(opfull);
+                if (dq_pend) {
+                    // dQ of chunk dq_g (channels [16 part, +16) of query row m) into
+                    // the staging tile, once the reducer has read the previous one
+                    if (!__all_sync(0xffffffffu, mbar_wait(stempty, (dq_g & 1) ^ 1, abort_flag, p.err))) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        sts16(srow + ((((part & 1) * 4 + u) ^ (m & 7)) << 4),
+                              make_uint4(dqv[4 * u], dqv[4 * u + 1], dqv[4 * u + 2], dqv[4 * u + 3]));
+                    fence_proxy_async_smem();
+                    mbar_arrive(stfull);
+                }
+                dq_pend = true;
+                dq_g = gc;
+            }
+            if (!ok) break;
+            // dV, dK of these keys: read out during the next chunk (or at the end)
+            acc_pend = true;
+            acc_ok = kk < tl.nr;
+            acc_row = (long long)tl.bh * g.n + tl.r + (long long)g.s * kk;
             ++it;
         }
-        if (ok && dq_pend) drain_dq();
+        if (ok && dq_pend) {
+            // the last chunk's products (opempty phase gc-1): its dQ and the
+            // last tile's dV, dK
+            if (__all_sync(0xffffffffu, mbar_wait(opempty, (gc - 1) & 1, abort_flag, p.err))) {
+                tc_fence_after();
+                if (acc_pend) drain_acc();
+                uint32_t dqv[16];
+                tmem_ld16(lane_base + kColDQ + 16 * part, dqv);
+                tmem_ld_wait();
+                tc_fence_before();
+                if (__all_sync(0xffffffffu, mbar_wait(stempty, (dq_g & 1) ^ 1, abort_flag, p.err))) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        sts16(srow + ((((part & 1) * 4 + u) ^ (m & 7)) << 4),
+                              make_uint4(dqv[4 * u], dqv[4 * u + 1], dqv[4 * u + 2], dqv[4 * u + 3]));
+                    fence_proxy_async_smem();
+                    mbar_arrive(stfull);
+                }
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -1155,7 +1191,7 @@ cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, co
 
 template <typename T>
 cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const TmapSet &mo,
-                           const BwdArgs &a, cudaStream_t st) {
+                           const TmapSet &macc, const BwdArgs &a, cudaStream_t st) {
     const long long rows = (long long)a.g.BH * a.g.n;
     const long long per_block = 8LL * kDeltaRowsPerWarp;
     k_bwd_delta<T><<<(unsigned)((rows + per_block - 1) / per_block), 256, 0, st>>>(a);
@@ -1167,7 +1203,7 @@ cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &
     const int grid = (int)(tiles < sms ? tiles : sms);
     e = cudaFuncSetAttribute(k_bwd_fused<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, fused::kSmem);
     if (e != cudaSuccess) return e;
-    k_bwd_fused<T><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, a);
+    k_bwd_fused<T><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, macc, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long groups = rows * 8;
@@ -1178,11 +1214,11 @@ cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &
 }  // namespace
 
 cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const TmapSet &mk,
-                                            const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,
-                                            cudaStream_t st) {
+                                            const TmapSet &mv, const TmapSet &mo, const TmapSet &macc,
+                                            const BwdArgs &a, cudaStream_t st) {
     if (!a.dqacc) return cudaErrorInvalidValue;
-    if (dt == kF16) return launch_fused_t<__half>(mq, mk, mv, mo, a, st);
-    return launch_fused_t<__nv_bfloat16>(mq, mk, mv, mo, a, st);
+    if (dt == kF16) return launch_fused_t<__half>(mq, mk, mv, mo, macc, a, st);
+    return launch_fused_t<__nv_bfloat16>(mq, mk, mv, mo, macc, a, st);
 }
 
 cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const TmapSet &mk,

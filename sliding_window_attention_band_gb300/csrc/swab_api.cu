@@ -134,6 +134,29 @@ bool build_rows_maps(TmapSet *set, const void *base, const Geom &g, DType dt, in
     return true;
 }
 
+// One map per residue r over an fp32 [BH, n, 64] accumulator: box = 32 floats
+// (128 B) x 128 rows, 128-byte swizzle; the one-pass backward adds its dQ
+// tiles into it with TMA reduce-add stores.
+bool build_acc_maps(TmapSet *set, float *base, const Geom &g) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    std::memset(set, 0, sizeof(*set));
+    for (int r = 0; r < g.s; ++r) {
+        int nr = residue_len(g.n, g.s, r);
+        const int rr = nr > 0 ? r : 0;
+        if (nr == 0) nr = 1;
+        cuuint64_t dims[3] = {64, (cuuint64_t)nr, (cuuint64_t)g.BH};
+        cuuint64_t strides[2] = {(cuuint64_t)g.s * 64 * 4, (cuuint64_t)g.n * 64 * 4};
+        cuuint32_t box[3] = {32, 128, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult res = enc(&set->m[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base + (size_t)rr * 64, dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (res != CUDA_SUCCESS) return false;
+    }
+    return true;
+}
+
 // Address of the status word on the current device (cached per device).
 unsigned *status_word() {
     static std::mutex mu;
@@ -431,7 +454,9 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
     const size_t rows = (size_t)g.BH * g.n;
     a.dqacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                         (rows * sizeof(float) + 255) / 256 * 256);
-    return from_cuda(launch_band_attention_bwd_fused(dt, mq, mk, mv, mo, a, st));
+    TmapSet macc;
+    if (!build_acc_maps(&macc, a.dqacc, g)) return SWAB_ERR_CUDA;
+    return from_cuda(launch_band_attention_bwd_fused(dt, mq, mk, mv, mo, macc, a, st));
 }
 
 SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float scale, const void *Q,

@@ -142,8 +142,8 @@ cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const Tmap
 cudaError_t launch_band_attention_bwd_f32(const BwdArgs &a, cudaStream_t st);
 // one-pass backward (dK, dV and dQ in one persistent kernel; needs a.dqacc)
 cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const TmapSet &mk,
-                                            const TmapSet &mv, const TmapSet &mo, const BwdArgs &a,
-                                            cudaStream_t st);
+                                            const TmapSet &mv, const TmapSet &mo, const TmapSet &macc,
+                                            const BwdArgs &a, cudaStream_t st);
 // SM count of the current device (swab_api.cu); 0 on error
 int device_sm_count();
 // the module-scope delta scratch of band_attention_bwd_noalloc (k_attention_bwd.cu)
