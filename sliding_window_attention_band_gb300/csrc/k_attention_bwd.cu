@@ -622,9 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   One chunk later the softmax warps copy dQ_c into a swizzled fp32
 //   staging tile and a reducer warp adds it into the fp32 accumulator with
 //   two TMA reduce-add stores (the final scale and rounding happen in
-//   k_bwd_dq_out).  K and V are double-buffered across tiles, and the chunk
-//   sequence runs on across tile boundaries: a tile's dV and dK are read out
-//   of TMEM during the next tile's first chunk, once its products are done.
+//   k_bwd_dq_out).  The chunk sequence runs on across tile boundaries: a
+//   tile's dV and dK are read out of TMEM during the next tile's first chunk,
+//   once its products are done.  K is double-buffered across tiles (dQ of a
+//   tile's last chunk still reads it while the next tile's scores are
+//   computed); V, read only by the dP^T product, has one buffer that is
+//   reloaded after the tile's last dP^T; Q and dO chunks use a 3-stage ring,
+//   so each chunk's load has a whole gradient phase to land.
 // Each softmax warp loads the lse and delta of its 32 query columns itself
 // (one of each per lane) and shares them through a per-warp shared slot.
 // The accumulation order of dQ across key tiles is not fixed, so dQ may
@@ -636,11 +640,11 @@ constexpr int kWorkerWarps = 4 * kParts;        // 16
 constexpr int kWorkers = 32 * kWorkerWarps;     // 512
 constexpr int kReducerWarp = 2 + kWorkerWarps;  // 18
 constexpr int kThreads = 32 * (kReducerWarp + 1);
-constexpr int kKV = 2 * kTile;                  // K and V of a key tile: 32 KB
 constexpr int kQS = 2 * kTile;                  // Q and dO of a query chunk: 32 KB
+constexpr int kQStages = 3;
 constexpr int kStage = 128 * 64 * 4;            // fp32 dQ staging: two 128 x 32 swizzled halves
 constexpr int kSlot = 2 * 32 * 4;               // per softmax warp: lse*log2e, delta of 32 queries
-constexpr int kSmem = 2 * kKV + 2 * kQS + kOpBytes + kStage + kWorkerWarps * kSlot + 1024 + 1024;
+constexpr int kSmem = 3 * kTile + kQStages * kQS + kOpBytes + kStage + kWorkerWarps * kSlot + 1024 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColP = 448;
 
 struct KTile {
@@ -671,17 +675,20 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *kvbuf = base;                      // [2] key tiles: K at +0, V at +kTile
-    uint8_t *qsbuf = kvbuf + 2 * kKV;           // [2] query chunks: Q at +0, dO at +kTile
-    uint8_t *dst_op = qsbuf + 2 * kQS;          // dS^T [128 keys x 128 queries]
+    uint8_t *kbuf = base;                       // [2] K tiles
+    uint8_t *vbuf = kbuf + 2 * kTile;           // V tile
+    uint8_t *qsbuf = vbuf + kTile;              // [kQStages] query chunks: Q at +0, dO at +kTile
+    uint8_t *dst_op = qsbuf + kQStages * kQS;   // dS^T [128 keys x 128 queries]
     uint8_t *stage = dst_op + kOpBytes;         // fp32 dQ: channels [0,32) at +0, [32,64) at +16 KB
     float *slots = reinterpret_cast<float *>(stage + kStage);  // [16 warps][lse | delta][32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(slots + kWorkerWarps * 64);
-    uint64_t *kvfull = bars;           // [2]
-    uint64_t *kvempty = kvfull + 2;    // [2]
-    uint64_t *qfull = kvempty + 2;     // [2]
-    uint64_t *qempty = qfull + 2;      // [2]
-    uint64_t *sfull = qempty + 2;      // 1
+    uint64_t *kfull = bars;            // [2]
+    uint64_t *kempty = kfull + 2;      // [2]
+    uint64_t *vfull = kempty + 2;      // 1
+    uint64_t *vempty = vfull + 1;      // 1
+    uint64_t *qfull = vempty + 1;      // [kQStages]
+    uint64_t *qempty = qfull + kQStages;  // [kQStages]
+    uint64_t *sfull = qempty + kQStages;  // 1
     uint64_t *sempty = sfull + 1;      // 1, count fused::kWorkers
     uint64_t *opfull = sempty + 1;     // 1, count fused::kWorkers
     uint64_t *opempty = opfull + 1;    // 1 (also: dQ of that chunk is in TMEM)
@@ -701,12 +708,16 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
     const int ntiles = xt * g.s * g.BH;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQStages; ++i) {
             mbar_init(&qfull[i], 1);
             mbar_init(&qempty[i], 1);
-            mbar_init(&kvfull[i], 1);
-            mbar_init(&kvempty[i], 1);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&kempty[i], 1);
+        }
+        mbar_init(vfull, 1);
+        mbar_init(vempty, 1);
         mbar_init(dqempty, fused::kWorkers);
         mbar_init(sfull, 1);
         mbar_init(sempty, fused::kWorkers);
@@ -739,23 +750,27 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             const CUtensorMap *mq = &mapQ.m[tl.r], *mk = &mapK.m[tl.r], *mv = &mapV.m[tl.r],
                               *mo = &mapdO.m[tl.r];
             const int tb = it & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&kvempty[tb], ((it >> 1) & 1) ^ 1, abort_flag, p.err)))
+            // K: buffer tb was last read by the last products of tile it-2;
+            // V: its one buffer was last read by the last dP^T of tile it-1
+            if (!__all_sync(0xffffffffu, mbar_wait(&kempty[tb], ((it >> 1) & 1) ^ 1, abort_flag, p.err) &&
+                                             mbar_wait(vempty, (it & 1) ^ 1, abort_flag, p.err)))
                 break;
             if (lane == 0) {
                 tma_prefetch_desc(mq);
                 tma_prefetch_desc(mk);
                 tma_prefetch_desc(mv);
                 tma_prefetch_desc(mo);
-                mbar_arrive_expect_tx(&kvfull[tb], kKV);
-                tma_load_3d(kvbuf + tb * kKV, mk, &kvfull[tb], 0, tl.a0, tl.bh);
-                tma_load_3d(kvbuf + tb * kKV + kTile, mv, &kvfull[tb], 0, tl.a0, tl.bh);
+                mbar_arrive_expect_tx(&kfull[tb], kTile);
+                tma_load_3d(kbuf + tb * kTile, mk, &kfull[tb], 0, tl.a0, tl.bh);
+                mbar_arrive_expect_tx(vfull, kTile);
+                tma_load_3d(vbuf, mv, vfull, 0, tl.a0, tl.bh);
             }
             __syncwarp();
             ++it;
             for (int c = 0; c < tl.nck; ++c, ++gc) {
-                const int qs = gc & 1;
+                const int qs = gc % kQStages;
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait(&qempty[qs], ((gc >> 1) & 1) ^ 1, abort_flag, p.err))) {
+                                mbar_wait(&qempty[qs], ((gc / kQStages) & 1) ^ 1, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
@@ -770,9 +785,10 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         }
         // every copy issued lands before the CTA may exit
         for (uint32_t k = it > 2u ? it - 2 : 0; k < it; ++k)
-            mbar_wait(&kvfull[k & 1], (k >> 1) & 1, no_abort, nullptr, 100000000ull);
-        for (uint32_t k = gc > 2u ? gc - 2 : 0; k < gc; ++k)
-            mbar_wait(&qfull[k & 1], (k >> 1) & 1, no_abort, nullptr, 100000000ull);
+            mbar_wait(&kfull[k & 1], (k >> 1) & 1, no_abort, nullptr, 100000000ull);
+        if (it > 0) mbar_wait(vfull, (it - 1) & 1, no_abort, nullptr, 100000000ull);
+        for (uint32_t k = gc > (uint32_t)kQStages ? gc - kQStages : 0; k < gc; ++k)
+            mbar_wait(&qfull[k % kQStages], (k / kQStages) & 1, no_abort, nullptr, 100000000ull);
     } else if (warp == 1) {
         // ---------------- MMA issuer (warp-uniform; lane 0 issues) ----------------
         constexpr bool kBf16 = !std::is_same<T, __half>::value;
@@ -780,9 +796,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         constexpr uint32_t id_g = idesc_f16(kB, 64, kBf16, false, true);   // dV, dK
         constexpr uint32_t id_q = idesc_f16(kB, 64, kBf16, true, true);    // dQ
         // descriptors of buffer 0; a buffer / K step adds (bytes >> 4)
-        const uint64_t d_k = sdesc_sw128(smem_u32(kvbuf), 16, 1024);           // K, K-major
-        const uint64_t d_v = sdesc_sw128(smem_u32(kvbuf + kTile), 16, 1024);   // V, K-major
-        const uint64_t d_kmn = sdesc_sw128(smem_u32(kvbuf), 1024, 1024);       // K as MN-major B
+        const uint64_t d_k = sdesc_sw128(smem_u32(kbuf), 16, 1024);            // K, K-major
+        const uint64_t d_v = sdesc_sw128(smem_u32(vbuf), 16, 1024);            // V, K-major
+        const uint64_t d_kmn = sdesc_sw128(smem_u32(kbuf), 1024, 1024);        // K as MN-major B
         const uint64_t d_q = sdesc_sw128(smem_u32(qsbuf), 16, 1024);           // Q, K-major
         const uint64_t d_o = sdesc_sw128(smem_u32(qsbuf + kTile), 16, 1024);   // dO, K-major
         const uint64_t d_qmn = sdesc_sw128(smem_u32(qsbuf), 1024, 1024);       // Q as MN-major B
@@ -792,7 +808,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         // 8-key groups 1024 B apart
         const uint64_t d_dsmn = sdesc_sw128(smem_u32(dst_op), kOpBytes / 2, 1024);
         auto issue_grad = [&](uint32_t gg, bool first, bool last, int tb, uint32_t itt) -> bool {
-            const int qs = gg & 1;
+            const int qs = gg % kQStages;
             // the softmax warps read dQ of chunk gg-1 out of TMEM in chunk gg
             // (phase gg of dqempty), before they signal its operands
             bool w = mbar_wait(opfull, gg & 1, abort_flag, p.err) &&
@@ -800,7 +816,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             if (first) w = w && mbar_wait(accempty, (itt & 1) ^ 1, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, w)) return false;
             tc_fence_after();
-            const uint64_t qoff = (uint64_t)((qs * kQS) >> 4), toff = (uint64_t)((tb * kKV) >> 4);
+            const uint64_t qoff = (uint64_t)((qs * kQS) >> 4), toff = (uint64_t)((tb * kTile) >> 4);
             if (lane == 0) {
 #pragma unroll
                 for (int k = 0; k < kB / 16; ++k) {
@@ -814,7 +830,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 }
                 mma_commit(opempty);   // also: dV, dK of the tile are complete after its last chunk
                 mma_commit(&qempty[qs]);
-                if (last) mma_commit(&kvempty[tb]);
+                if (last) mma_commit(&kempty[tb]);
             }
             __syncwarp();
             return true;
@@ -826,15 +842,16 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             KTile tl;
             if (!decode_ktile(g, t, xt, tl)) continue;
             const int tb = it & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&kvfull[tb], (it >> 1) & 1, abort_flag, p.err))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&kfull[tb], (it >> 1) & 1, abort_flag, p.err) &&
+                                             mbar_wait(vfull, it & 1, abort_flag, p.err))) {
                 ok = false;
                 break;
             }
-            const uint64_t toff = (uint64_t)((tb * kKV) >> 4);
+            const uint64_t toff = (uint64_t)((tb * kTile) >> 4);
             for (int c = 0; c < tl.nck; ++c, ++gc) {
-                const int qs = gc & 1;
+                const int qs = gc % kQStages;
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&qfull[qs], (gc >> 1) & 1, abort_flag, p.err) &&
+                                mbar_wait(&qfull[qs], (gc / kQStages) & 1, abort_flag, p.err) &&
                                     mbar_wait(sempty, (gc & 1) ^ 1, abort_flag, p.err));
                 if (!ok) break;
                 tc_fence_after();
@@ -845,7 +862,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                         mma_f16_ss(tmem + kColS, d_k + toff + 2 * k, d_q + qoff + 2 * k, id_s, k > 0);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_f16_ss(tmem + kColDP, d_v + toff + 2 * k, d_o + qoff + 2 * k, id_s, k > 0);
+                        mma_f16_ss(tmem + kColDP, d_v + 2 * k, d_o + qoff + 2 * k, id_s, k > 0);
+                    if (c == tl.nck - 1) mma_commit(vempty);   // the tile's last read of V
                     mma_commit(sfull);
                 }
                 __syncwarp();
