@@ -160,12 +160,13 @@ class Step:
 
 class FusedStep(Step):
     """Forward + backward with the scores kept on chip: band_attention (O, lse),
-    then band_attention_bwd (dQ, dK, dV; its delta, dK/dV and dQ kernels)."""
+    then band_attention_bwd (dQ, dK, dV: its row-sum kernel, the one-pass
+    dK/dV/dQ kernel and the dQ rounding kernel)."""
 
     NAMES = ["band_attention", "band_attention_bwd"]
     LAUNCHES = 4
     DESCRIPTION = ("fused fwd+bwd: band_attention (O, lse), band_attention_bwd "
-                   "(delta, dK/dV and dQ kernels)")
+                   "(row sums, one-pass dK/dV/dQ kernel, dQ rounding)")
 
     def __init__(self, wl, device):
         super().__init__(wl, device)
@@ -454,6 +455,9 @@ def main():
     ap.add_argument("--step", default="fused", choices=["fused", "materialised"],
                     help="fused: band_attention + band_attention_bwd; materialised: the "
                          "eight band_qk / softmax / band_pv / band_t calls")
+    ap.add_argument("--no-also", action="store_true",
+                    help="skip the companion timings (other step variant, dilation 3, long "
+                         "causal forward); used for short profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -513,7 +517,7 @@ def main():
     # fused forward on the long causal workload
     also = {}
     n_also = max(3, args.steps // 2)
-    for cls in (FusedStep, Step):
+    for cls in (() if args.no_also else (FusedStep, Step)):
         for w_ in (WORKLOADS[MAIN_CFG], WORKLOADS[ALSO_CFG]):
             if cls is step_cls and w_ is wl:
                 continue
@@ -522,8 +526,9 @@ def main():
             also[f"{'fused' if cls is FusedStep else 'materialised'}:{w_.name}"] = \
                 step_summary(w_, st, ps, pk, peaks)
             del st
-    wl5 = WORKLOADS[5]
-    also[f"band_attention:{wl5.name}"] = fused_forward(wl5, device, n_also, 3, flush, peaks)
+    if not args.no_also:
+        wl5 = WORKLOADS[5]
+        also[f"band_attention:{wl5.name}"] = fused_forward(wl5, device, n_also, 3, flush, peaks)
     if swab.device_status(reset=True) != 0:
         raise SystemExit("a kernel raised the device status word during the benchmark")
 
