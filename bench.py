@@ -133,8 +133,21 @@ class Step:
             lambda: s.band_pv_bwd_t(d, 1.0, self.P, self.dO, self.dV),
         ]
 
-    def run(self, events=None):
-        for k, fn in enumerate(self.launches()):
+    def capture(self):
+        """Capture each API call once into its own CUDA graph; run() then replays
+        them: the same kernels, with no host work between the launches."""
+        self.graphs = []
+        for fn in self.launches():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                fn()
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def run(self, events=None, eager=False):
+        graphs = getattr(self, "graphs", None)
+        fns = self.launches() if eager or not graphs else [g.replay for g in graphs]
+        for k, fn in enumerate(fns):
             if events is not None:
                 events[k].record()
             fn()
@@ -192,11 +205,14 @@ def step_summary(wl, step, per_step, per_kernel, peaks):
 
 
 def time_steps(step, steps, warmup, flush):
-    """Per-step device times (ms) and per-kernel times (ms) over `steps` steps."""
+    """Per-step device times (ms) and per-call times (ms) over `steps` steps: the
+    calls run eagerly for the warm-up, are captured once into CUDA graphs, and
+    the timed steps replay them."""
     for _ in range(warmup):
         flush.zero_()
-        step.run()
+        step.run(eager=True)
     torch.cuda.synchronize()
+    step.capture()
     nk = len(step.NAMES)
     per_step, per_kernel = [], [[] for _ in range(nk)]
     for _ in range(steps):
@@ -220,12 +236,17 @@ def fused_forward(wl, device, steps, warmup, flush, peaks):
     lse = torch.empty((wl.BH, wl.n), dtype=torch.float32, device=device)
     for _ in range(warmup):
         swab.band_attention(d, wl.scale, Q, K, V, O, lse)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()   # captured once, replayed in the timed runs
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        swab.band_attention(d, wl.scale, Q, K, V, O, lse)
+    torch.cuda.synchronize()
     ts = []
     for _ in range(steps):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        swab.band_attention(d, wl.scale, Q, K, V, O, lse)
+        g.replay()
         b.record()
         torch.cuda.synchronize()
         ts.append(a.elapsed_time(b))
@@ -244,7 +265,7 @@ def fused_forward(wl, device, steps, warmup, flush, peaks):
 def time_e2e(step, steps, warmup, flush):
     for _ in range(warmup):
         step.h2d()
-        step.run()
+        step.run(eager=True)
         step.d2h()
     torch.cuda.synchronize()
     times = []
@@ -253,7 +274,7 @@ def time_e2e(step, steps, warmup, flush):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         step.h2d()
-        step.run()
+        step.run(eager=True)   # the calls a user makes, host work included
         step.d2h()
         b.record()
         torch.cuda.synchronize()
@@ -540,6 +561,8 @@ def main():
         "config": {**wl.describe(), "parallelism": f"replicas x{world}" if world > 1 else "none",
                    "l2": "flushed (256 MB write) before every timed step",
                    "step": step.DESCRIPTION, "flops_per_step": flops,
+                   "launch": "each API call captured once into a CUDA graph and replayed in the "
+                             "timed steps; e2e calls the API eagerly",
                    "flops_counted": "6 banded contractions x 2*head_dim per valid pair"},
         "per_call_us": {f"{i}:{nm}": round(statistics.mean(t) * 1e3, 2)
                         for i, (nm, t) in enumerate(zip(step.NAMES, per_kernel))},

@@ -27,7 +27,11 @@
 // Tile epilogue: the four parts of a row exchange (m_j, l_j) through shared
 // memory; part j then reads channels [16j, 16j+16) of all four accumulators,
 // combines them (O = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j) and
-// writes them out; lse = M ln 2 + ln L.
+// writes them out; lse = M ln 2 + ln L.  The chunk sequence runs on across
+// tiles: a tile's epilogue runs in the next tile's first chunk, after that
+// chunk's softmax and before its P tile is signalled (its P.V product
+// overwrites the accumulators), so the next tile's first Q.K^T and softmax
+// overlap the tile's last P.V.
 //
 // Warps: 0 = TMA producer (Q double-buffered, K and V chunks into a 3-stage
 // ring), 1 = TMEM owner + MMA issuer, 2..17 = softmax / epilogue.  Every
@@ -246,15 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             Tile tl;
             if (!decode_tile(g, t, xt, tl)) continue;
-            // the last product of the previous tile goes first: its epilogue
-            // need not wait for this tile's loads
-            if (have_prev) {
-                have_prev = false;
-                if (!issue_pv(prev, prev_first)) {
-                    ok = false;
-                    break;
-                }
-            }
             const int qb = it & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&qfull[qb], (it >> 1) & 1, abort_flag, p.err))) {
                 ok = false;
@@ -304,6 +299,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t o_mine = lane_base + kTmemO + 64 * part;
         uint32_t gc = 0, it = 0;
         bool ok = true;
+        bool epi_pend = false, epi_ok = false;
+        float epi_m = 0.f, epi_l = 0.f;
+        long long epi_row = 0;
+        uint32_t epi_it = 0;
+        // the epilogue of tile epi_it (row epi_row, this part's (epi_m, epi_l));
+        // the caller has waited for the tile's last P.V product
+        auto epilogue = [&]() -> bool {
+            epi_pend = false;
+            float2 *ml = mlx + (epi_it & 1) * kParts * kBQ;
+            ml[part * kBQ + q] = make_float2(epi_m, epi_l);
+            mbar_arrive(&mlbar[quarter]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&mlbar[quarter], epi_it & 1, abort_flag, p.err)))
+                return false;
+            float M = -INFINITY;
+            float2 e[kParts];
+#pragma unroll
+            for (int j = 0; j < kParts; ++j) {
+                e[j] = ml[j * kBQ + q];
+                M = fmaxf(M, e[j].x);
+            }
+            float f[kParts], L = 0.f;
+#pragma unroll
+            for (int j = 0; j < kParts; ++j) {
+                f[j] = e[j].x == -INFINITY ? 0.f : ex2(e[j].x - M);
+                L += e[j].y * f[j];
+            }
+            const float inv = 1.f / L;
+            // channels [16 part, 16 part + 16) of the four accumulators, two at a time
+            float y[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = 0.f;
+#pragma unroll
+            for (int j0 = 0; j0 < kParts; j0 += 2) {
+                uint32_t o0[16], o1[16];
+                tmem_ld16(lane_base + kTmemO + 64 * j0 + 16 * part, o0);
+                tmem_ld16(lane_base + kTmemO + 64 * (j0 + 1) + 16 * part, o1);
+                tmem_ld_wait();
+                const float f0 = f[j0] * inv, f1 = f[j0 + 1] * inv;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    y[i] = fmaf(__uint_as_float(o1[i]), f1, fmaf(__uint_as_float(o0[i]), f0, y[i]));
+            }
+            tc_fence_before();   // O may be overwritten once this warp's next P tile is signalled
+            if (epi_ok) {
+                const long long row = epi_row;
+                uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + row * 64 + 16 * part);
+                o4[0] = make_uint4(pack2<T>(y[0], y[1]), pack2<T>(y[2], y[3]), pack2<T>(y[4], y[5]),
+                                   pack2<T>(y[6], y[7]));
+                o4[1] = make_uint4(pack2<T>(y[8], y[9]), pack2<T>(y[10], y[11]),
+                                   pack2<T>(y[12], y[13]), pack2<T>(y[14], y[15]));
+                if (p.lse && part == 0) p.lse[row] = M * 0.6931471805599453f + logf(L);
+            }
+            return true;
+        };
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             Tile tl;
             if (!decode_tile(g, t, xt, tl)) continue;
@@ -385,10 +434,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool rescale = raise && m != -INFINITY;
                 const float corr = rescale ? ex2(m - mref) : 1.f;
                 l = l * corr + lc;
-                if (c > 0) {
-                    // the product of chunk gc-1 has landed in O: it may be rescaled
+                if (c > 0 || epi_pend) {
+                    // the product of chunk gc-1 has landed in O: it may be
+                    // rescaled, or (first chunk of a tile) the previous tile's
+                    // accumulators are final
                     w_ok = mbar_wait(ofull, (gc - 1) & 1, abort_flag, p.err);
                     if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+                }
+                if (epi_pend) {
+                    tc_fence_after();
+                    if (!epilogue()) { ok = false; break; }
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
                     tc_fence_after();
@@ -409,55 +464,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = mref;
             }
             if (!ok) break;
-            // ---------------- tile epilogue ----------------
-            bool w_ok = mbar_wait(ofull, (gc - 1) & 1, abort_flag, p.err);
-            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-            tc_fence_after();
-            float2 *ml = mlx + (it & 1) * kParts * kBQ;
-            ml[part * kBQ + q] = make_float2(m, l);
-            mbar_arrive(&mlbar[quarter]);
-            w_ok = mbar_wait(&mlbar[quarter], it & 1, abort_flag, p.err);
-            if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-            float M = -INFINITY;
-            float2 e[kParts];
-#pragma unroll
-            for (int j = 0; j < kParts; ++j) {
-                e[j] = ml[j * kBQ + q];
-                M = fmaxf(M, e[j].x);
-            }
-            float f[kParts], L = 0.f;
-#pragma unroll
-            for (int j = 0; j < kParts; ++j) {
-                f[j] = e[j].x == -INFINITY ? 0.f : ex2(e[j].x - M);
-                L += e[j].y * f[j];
-            }
-            const float inv = 1.f / L;
-            // channels [16 part, 16 part + 16) of the four accumulators, two at a time
-            float y[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = 0.f;
-#pragma unroll
-            for (int j0 = 0; j0 < kParts; j0 += 2) {
-                uint32_t o0[16], o1[16];
-                tmem_ld16(lane_base + kTmemO + 64 * j0 + 16 * part, o0);
-                tmem_ld16(lane_base + kTmemO + 64 * (j0 + 1) + 16 * part, o1);
-                tmem_ld_wait();
-                const float f0 = f[j0] * inv, f1 = f[j0 + 1] * inv;
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    y[i] = fmaf(__uint_as_float(o1[i]), f1, fmaf(__uint_as_float(o0[i]), f0, y[i]));
-            }
-            tc_fence_before();   // O may be overwritten once this warp's next P tile is signalled
-            if (qq < tl.nr) {
-                const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * qq;
-                uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + row * 64 + 16 * part);
-                o4[0] = make_uint4(pack2<T>(y[0], y[1]), pack2<T>(y[2], y[3]), pack2<T>(y[4], y[5]),
-                                   pack2<T>(y[6], y[7]));
-                o4[1] = make_uint4(pack2<T>(y[8], y[9]), pack2<T>(y[10], y[11]),
-                                   pack2<T>(y[12], y[13]), pack2<T>(y[14], y[15]));
-                if (p.lse && part == 0) p.lse[row] = M * 0.6931471805599453f + logf(L);
-            }
+            // the epilogue of this tile runs in the next tile's first chunk
+            epi_pend = true;
+            epi_m = m;
+            epi_l = l;
+            epi_ok = qq < tl.nr;
+            epi_row = (long long)tl.bh * g.n + tl.r + (long long)g.s * qq;
+            epi_it = it;
             ++it;
+        }
+        if (ok && epi_pend) {
+            // the last tile's epilogue: its last P.V product is phase gc-1 of ofull
+            if (__all_sync(0xffffffffu, mbar_wait(ofull, (gc - 1) & 1, abort_flag, p.err))) {
+                tc_fence_after();
+                epilogue();
+            }
         }
     }
     tc_fence_before();
@@ -517,8 +538,7 @@ cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, co
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    cudaError_t e = cudaFuncSetAttribute(k_band_attention_fwd<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_attention_fwd<T>), kSmemBytes);
     if (e != cudaSuccess) return e;
     k_band_attention_fwd<T><<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, a);
     return cudaGetLastError();

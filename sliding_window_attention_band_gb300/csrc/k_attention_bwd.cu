@@ -988,17 +988,23 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 const float4 *d4 = reinterpret_cast<const float4 *>(slot + 32);
                 const uint64_t xs2 = f2(xscale, xscale);
                 uint32_t pk[16], dk[16];
+                // columns [8h, 8h + 8) of the part in four steps; the next
+                // step's loads are in flight while a step is computed
+                uint32_t svb[2][8], dvb[2][8];
+                tmem_ld8(lane_base + kColS + 32 * part, svb[0]);
+                tmem_ld8(lane_base + kColDP + 32 * part, dvb[0]);
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    // columns [8h, 8h + 8) of the part
-                    uint32_t sv[8], dv[8];
-                    tmem_ld8(lane_base + kColS + 32 * part + 8 * h, sv);
-                    tmem_ld8(lane_base + kColDP + 32 * part + 8 * h, dv);
-                    tmem_ld_wait();
-                    if (h == 3) {
+                    tmem_ld_wait();   // step h (the only loads outstanding)
+                    if (h < 3) {
+                        tmem_ld8(lane_base + kColS + 32 * part + 8 * (h + 1), svb[(h + 1) & 1]);
+                        tmem_ld8(lane_base + kColDP + 32 * part + 8 * (h + 1), dvb[(h + 1) & 1]);
+                    } else {
                         tc_fence_before();
                         mbar_arrive(sempty);   // S^T and dP^T are in registers
                     }
+                    const uint32_t (&sv)[8] = svb[h & 1];
+                    const uint32_t (&dv)[8] = dvb[h & 1];
                     if (empty) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) pk[4 * h + i] = dk[4 * h + i] = 0u;
@@ -1196,12 +1202,12 @@ cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, co
     if (e != cudaSuccess) return e;
     const int tiles = (a.g.nsub + kB - 1) / kB;
     dim3 grid(tiles, a.g.s, a.g.BH);
-    e = cudaFuncSetAttribute(k_bwd_dkdv<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDKDV);
+    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_dkdv<T>), kSmemDKDV);
     if (e != cudaSuccess) return e;
     k_bwd_dkdv<T><<<grid, kThreads, kSmemDKDV, st>>>(mq, mk, mv, mo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_bwd_dq<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDQ);
+    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_dq<T>), kSmemDQ);
     if (e != cudaSuccess) return e;
     k_bwd_dq<T><<<grid, kThreads, kSmemDQ, st>>>(mq, mk, mv, mo, a);
     return cudaGetLastError();
@@ -1219,7 +1225,7 @@ cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    e = cudaFuncSetAttribute(k_bwd_fused<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, fused::kSmem);
+    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T>), fused::kSmem);
     if (e != cudaSuccess) return e;
     k_bwd_fused<T><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, macc, a);
     e = cudaGetLastError();

@@ -408,8 +408,7 @@ cudaError_t launch_gather(const TmapSet &mapB, const GatherArgs &a, cudaStream_t
     const int tiles = (a.g.nsub + kBM - 1) / kBM;
     dim3 grid(tiles, a.g.s, a.g.BH);
     const size_t smem = kSmemBytes + (kGlob ? gather_glob_smem(a.g.n, a.gl.G) : 0);
-    cudaError_t e = cudaFuncSetAttribute(k_band_gather_tc<T, kTrans, kGlob>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_gather_tc<T, kTrans, kGlob>), (int)smem);
     if (e != cudaSuccess) return e;
     k_band_gather_tc<T, kTrans, kGlob><<<grid, kThreads, smem, st>>>(mapB, a);
     return cudaGetLastError();

@@ -362,8 +362,7 @@ template <typename T, bool kRows>
 cudaError_t launch_qk(const TmapSet &mapA, const TmapSet &mapB, const QKArgs &a, cudaStream_t st) {
     const int tiles = (a.g.nsub + kBN - 1) / kBN;
     dim3 grid(tiles, a.g.s, a.g.BH);
-    cudaError_t e = cudaFuncSetAttribute(k_band_qk_tc<T, kRows>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_qk_tc<T, kRows>), kSmemBytes);
     if (e != cudaSuccess) return e;
     k_band_qk_tc<T, kRows><<<grid, kThreads, kSmemBytes, st>>>(mapA, mapB, a);
     return cudaGetLastError();

@@ -394,8 +394,7 @@ size_t bitmap_bytes(int n) { return (size_t)((n + 31) / 32) * 4; }
 template <typename T>
 cudaError_t launch_scores_t(const GlobScoreArgs &a, cudaStream_t st) {
     const size_t smem = (size_t)(2 * kTile + 2 * a.gl.G) * kPad * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_glob_scores<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_glob_scores<T>), (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.g.n + kTile - 1) / kTile, a.g.BH);
     k_glob_scores<T><<<grid, kThreads, smem, st>>>(a);
@@ -407,13 +406,11 @@ cudaError_t launch_softmax_t(const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st
     const size_t smem = bitmap_bytes(a.g.n);
     const unsigned grid = grid_rows((long long)a.g.BH * a.g.n);
     if (bwd) {
-        cudaError_t e = cudaFuncSetAttribute(k_softmax_bwd_glob<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_softmax_bwd_glob<T>), (int)smem);
         if (e != cudaSuccess) return e;
         k_softmax_bwd_glob<T><<<grid, kThreads, smem, st>>>(a);
     } else {
-        cudaError_t e = cudaFuncSetAttribute(k_softmax_glob<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_softmax_glob<T>), (int)smem);
         if (e != cudaSuccess) return e;
         k_softmax_glob<T><<<grid, kThreads, smem, st>>>(a);
     }
@@ -431,13 +428,11 @@ template <typename T>
 cudaError_t launch_reduce_t(const GlobReduceArgs &a, bool cols, cudaStream_t st) {
     const size_t smem = (size_t)2 * kTile * kPad * sizeof(float) + (cols ? bitmap_bytes(a.g.n) : 0);
     if (cols) {
-        cudaError_t e = cudaFuncSetAttribute(k_glob_reduce<T, true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_glob_reduce<T, true>), (int)smem);
         if (e != cudaSuccess) return e;
         k_glob_reduce<T, true><<<a.g.BH, kThreads, smem, st>>>(a);
     } else {
-        cudaError_t e = cudaFuncSetAttribute(k_glob_reduce<T, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_glob_reduce<T, false>), (int)smem);
         if (e != cudaSuccess) return e;
         k_glob_reduce<T, false><<<a.g.BH, kThreads, smem, st>>>(a);
     }
@@ -470,13 +465,11 @@ cudaError_t launch_band_f32_glob(const DenseGlobArgs &a, bool transposed, cudaSt
     const long long rows = (long long)a.g.BH * a.g.n;
     const size_t smem = bitmap_bytes(a.g.n);
     if (transposed) {
-        cudaError_t e = cudaFuncSetAttribute(k_band_t_f32_glob, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_t_f32_glob), (int)smem);
         if (e != cudaSuccess) return e;
         k_band_t_f32_glob<<<(unsigned)rows, 128, smem, st>>>(a);
     } else {
-        cudaError_t e = cudaFuncSetAttribute(k_band_pv_f32_glob, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_pv_f32_glob), (int)smem);
         if (e != cudaSuccess) return e;
         k_band_pv_f32_glob<<<(unsigned)rows, 128, smem, st>>>(a);
     }

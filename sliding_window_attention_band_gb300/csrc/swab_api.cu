@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "swab_internal.h"
@@ -232,6 +233,23 @@ swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, co
 }
 
 }  // namespace
+
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`; cudaFuncSetAttribute runs only when the limit recorded for
+// (kernel, device) is lower, so repeated launches (and stream capture) skip it.
+cudaError_t ensure_smem(const void *kernel, int bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    int &have = done[std::make_pair(kernel, dev)];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
+}
 
 // Number of SMs of the current device (cached per device); 0 on error.
 int device_sm_count() {

@@ -146,6 +146,8 @@ cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const T
                                             const BwdArgs &a, cudaStream_t st);
 // SM count of the current device (swab_api.cu); 0 on error
 int device_sm_count();
+// dynamic shared-memory limit of a kernel, set once per (kernel, device) (swab_api.cu)
+cudaError_t ensure_smem(const void *kernel, int bytes);
 // the module-scope delta scratch of band_attention_bwd_noalloc (k_attention_bwd.cu)
 cudaError_t noalloc_delta_scratch(float **out);
 // fp32 FFMA paths
