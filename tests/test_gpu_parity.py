@@ -394,7 +394,7 @@ def test_band_attention_bwd_unit(case):
     check_fused_bwd(d, Q, K, V, dO, 0.125, range(BH), dtype == torch.float32)
 
 
-@pytest.mark.parametrize("cfg,slices", [(1, (0, 1)), (2, (0, 11)), (3, (6,))])
+@pytest.mark.parametrize("cfg,slices", [(1, (0, 1)), (2, (0, 11)), (3, (6,)), (5, (3,))])
 def test_band_attention_bwd_config(cfg, slices):
     wl = WORKLOADS[cfg]
     Q, K, V, dO = workload_inputs(wl)
