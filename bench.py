@@ -437,6 +437,17 @@ def cpu_baseline(wl, budget_s=15.0):
                       f"{t:.2f} s"}
 
 
+def job_value(dev_ms, world, steps, flops_per_step, dist=None, device=None):
+    """Whole-job throughput over N ranks that each run the same workload (weak
+    scaling, replicas): the slowest rank's timed region (max over ranks) and
+    the flops of all ranks divided by it, in TFLOP/s."""
+    if dist is not None and world > 1:
+        t = torch.tensor([float(dev_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_ms = float(t.item())
+    return dev_ms, world * flops_per_step * steps / (dev_ms * 1e-3) / 1e12
+
+
 def run_reference(args):
     import oracle
 
@@ -523,14 +534,9 @@ def main():
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
 
-    dev_ms = sum(per_step)
-    if dist:
-        t = torch.tensor([dev_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_ms = float(t.item())
-    ms_per_step = dev_ms / args.steps
     flops = step_flops(wl)
-    value = world * flops * args.steps / (dev_ms * 1e-3) / 1e12
+    dev_ms, value = job_value(sum(per_step), world, args.steps, flops, dist, device)
+    ms_per_step = dev_ms / args.steps
     e2e_ms = time_e2e(step, max(3, args.steps // 2), 3, flush)
     e2e_val = world * flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
 
