@@ -49,12 +49,12 @@ def _load():
         p = ctypes.c_void_p
         _lib.orc_num_threads.restype = i
         _lib.orc_band_qk.argtypes = [i, i, i, i, i, i, d, d, p, p, p, i, p, p, p]
-        _lib.orc_band_softmax.argtypes = [i, i, i, i, i, p, p, p, i, p, p, p, p, p]
+        _lib.orc_band_softmax.argtypes = [i, i, i, i, i, p, p, p, i, p, p, p, p, p, p]
         _lib.orc_band_pv.argtypes = [i, i, i, i, i, i, d, p, p, p, i, p, p, p]
         _lib.orc_band_t.argtypes = [i, i, i, i, i, i, d, p, p, p, i, p, p, p]
         _lib.orc_band_softmax_bwd.argtypes = [i, i, i, i, i, p, p, p, i, p, p, p, p, p, p, p]
-        _lib.orc_attention_fwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, i, p]
-        _lib.orc_attention_bwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, p, p, i, p]
+        _lib.orc_attention_fwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, i, p, p]
+        _lib.orc_attention_bwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, p, p, i, p, p]
         for f in ("orc_band_qk", "orc_band_softmax", "orc_band_pv", "orc_band_t",
                   "orc_band_softmax_bwd", "orc_attention_fwd", "orc_attention_bwd"):
             getattr(_lib, f).restype = i
@@ -100,10 +100,22 @@ def band_qk(A, B, w, w_upper, dilation=0, alpha=1.0, padding=0.0, global_idx=Non
     return (S, Sg, Sr) if G else S
 
 
-def band_softmax(S, w, w_upper, dilation=0, global_idx=None, Sg=None, Sr=None):
-    """Masked row softmax.  Returns (P, lse) or (P, lse, Pg, Pr) with globals."""
+def _kbias(key_bias, BH, n):
+    """Key bias given per slice [BH, n] (callers expand a [b, n] bias over the heads)."""
+    if key_bias is None:
+        return None
+    kb = _f64(key_bias)
+    if kb.shape != (BH, n):
+        raise ValueError(f"key_bias must be [BH, n] = {(BH, n)}, got {kb.shape}")
+    return kb
+
+
+def band_softmax(S, w, w_upper, dilation=0, global_idx=None, Sg=None, Sr=None, key_bias=None):
+    """Masked row softmax (key_bias[bh, j] added to the score of key j).  Returns
+    (P, lse) or (P, lse, Pg, Pr) with globals."""
     S = _f64(S)
     BH, n, D = S.shape
+    kb = _kbias(key_bias, BH, n)
     G, g = _gidx(global_idx)
     P = np.empty_like(S)
     lse = np.empty((BH, n))
@@ -112,7 +124,7 @@ def band_softmax(S, w, w_upper, dilation=0, global_idx=None, Sg=None, Sr=None):
     Sg = _f64(Sg) if G else None
     Sr = _f64(Sr) if G else None
     _check(_load().orc_band_softmax(BH, n, w, w_upper, dilation, _ptr(S), _ptr(P), _ptr(lse),
-                                    G, _ptr(g), _ptr(Sg), _ptr(Sr), _ptr(Pg), _ptr(Pr)),
+                                    G, _ptr(g), _ptr(Sg), _ptr(Sr), _ptr(Pg), _ptr(Pr), _ptr(kb)),
            "band_softmax")
     return (P, lse, Pg, Pr) if G else (P, lse)
 
@@ -162,28 +174,32 @@ def band_softmax_bwd(P, dP, w, w_upper, dilation=0, global_idx=None, Pg=None, dP
     return (dS, dSg, dSr) if G else dS
 
 
-def attention_fwd(Q, K, V, w, w_upper, dilation=0, scale=None, global_idx=None):
-    """Attention on explicit key sets.  Returns (O, lse)."""
+def attention_fwd(Q, K, V, w, w_upper, dilation=0, scale=None, global_idx=None, key_bias=None):
+    """Attention on explicit key sets (key_bias[bh, j] added to the scaled score of
+    key j).  Returns (O, lse)."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     BH, n, hd = Q.shape
+    kb = _kbias(key_bias, BH, n)
     scale = 1.0 / np.sqrt(hd) if scale is None else scale
     G, g = _gidx(global_idx)
     O = np.empty((BH, n, hd))
     lse = np.empty((BH, n))
     _check(_load().orc_attention_fwd(BH, n, hd, w, w_upper, dilation, scale, _ptr(Q),
-                                     _ptr(K), _ptr(V), _ptr(O), _ptr(lse), G, _ptr(g)),
+                                     _ptr(K), _ptr(V), _ptr(O), _ptr(lse), G, _ptr(g), _ptr(kb)),
            "attention_fwd")
     return O, lse
 
 
-def attention_bwd(Q, K, V, dO, w, w_upper, dilation=0, scale=None, global_idx=None):
+def attention_bwd(Q, K, V, dO, w, w_upper, dilation=0, scale=None, global_idx=None,
+                  key_bias=None):
     """Gradients of attention_fwd's O.  Returns (dQ, dK, dV)."""
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
     BH, n, hd = Q.shape
+    kb = _kbias(key_bias, BH, n)
     scale = 1.0 / np.sqrt(hd) if scale is None else scale
     G, g = _gidx(global_idx)
     dQ, dK, dV = (np.empty((BH, n, hd)) for _ in range(3))
     _check(_load().orc_attention_bwd(BH, n, hd, w, w_upper, dilation, scale, _ptr(Q),
                                      _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK),
-                                     _ptr(dV), G, _ptr(g)), "attention_bwd")
+                                     _ptr(dV), G, _ptr(g), _ptr(kb)), "attention_bwd")
     return dQ, dK, dV

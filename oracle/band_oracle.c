@@ -162,17 +162,29 @@ int orc_band_qk(int BH, int n, int hd, int w, int wu, int dil, double alpha,
  * --------------------------------------------------------------------- */
 int orc_band_softmax(int BH, int n, int w, int wu, int dil, const double *S,
                      double *P, double *lse, int G, const int *gidx,
-                     const double *Sg, const double *Sr, double *Pg, double *Pr) {
+                     const double *Sg, const double *Sr, double *Pg, double *Pr,
+                     const double *kbias) {
     if (check_geom(BH, n, 1, w, wu, dil)) return -1;
+    if (G > 0 && kbias) return -4;  /* key bias with global tokens: not defined here */
     const int D = w + wu + 1, s = dil + 1;
     unsigned char *gm; int *gp;
     int rc = build_gmask(n, G, gidx, &gm, &gp);
     if (rc) return rc;
     const unsigned char *gmask = G > 0 ? gm : NULL;
-#pragma omp parallel for collapse(2) schedule(static)
+#pragma omp parallel
+    {
+    /* the row's scores plus the key bias of each slot's key (nvFuser issue,
+     * fusion 1: the additive mask term is added to the scaled score) */
+    double *xb = (double *)malloc(sizeof(double) * (size_t)D);
+#pragma omp for collapse(2) schedule(static)
     for (int bh = 0; bh < BH; ++bh) {
         for (int i = 0; i < n; ++i) {
-            const double *srow = S + ((size_t)bh * n + i) * D;
+            const double *srow0 = S + ((size_t)bh * n + i) * D;
+            for (int t = 0; t < D; ++t) {
+                const long long j = (long long)i + (long long)(t - w) * s;
+                xb[t] = srow0[t] + ((kbias && j >= 0 && j < n) ? kbias[(size_t)bh * n + j] : 0.0);
+            }
+            const double *srow = xb;
             double *prow = P + ((size_t)bh * n + i) * D;
             if (gmask && gmask[i]) {
                 const int g = gp[i];
@@ -202,6 +214,8 @@ int orc_band_softmax(int BH, int n, int w, int wu, int dil, const double *S,
             }
             if (lse) lse[(size_t)bh * n + i] = m + log(z);
         }
+    }
+    free(xb);
     }
     free(gm); free(gp);
     return 0;
@@ -401,8 +415,9 @@ static int build_keysets(int n, int w, int wu, int dil, int G, const int *gidx,
 
 int orc_attention_fwd(int BH, int n, int hd, int w, int wu, int dil, double scale,
                       const double *Q, const double *K, const double *V, double *O,
-                      double *lse, int G, const int *gidx) {
+                      double *lse, int G, const int *gidx, const double *kbias) {
     if (check_geom(BH, n, hd, w, wu, dil)) return -1;
+    if (G > 0 && kbias) return -4;
     unsigned char *gm; int *gp;
     int rc = build_gmask(n, G, gidx, &gm, &gp);
     if (rc) return rc;
@@ -419,7 +434,8 @@ int orc_attention_fwd(int BH, int n, int hd, int w, int wu, int dil, double scal
                 const long long b0 = ks.off[i], cnt = ks.off[i + 1] - b0;
                 double m = -INFINITY, z = 0.0;
                 for (long long u = 0; u < cnt; ++u) {
-                    x[u] = scale * dot(q, K + ((size_t)bh * n + ks.key[b0 + u]) * hd, hd);
+                    x[u] = scale * dot(q, K + ((size_t)bh * n + ks.key[b0 + u]) * hd, hd) +
+                           (kbias ? kbias[(size_t)bh * n + ks.key[b0 + u]] : 0.0);
                     m = fmax(m, x[u]);
                 }
                 for (long long u = 0; u < cnt; ++u) z += exp(x[u] - m);
@@ -448,8 +464,9 @@ int orc_attention_fwd(int BH, int n, int hd, int w, int wu, int dil, double scal
 int orc_attention_bwd(int BH, int n, int hd, int w, int wu, int dil, double scale,
                       const double *Q, const double *K, const double *V,
                       const double *dO, double *dQ, double *dK, double *dV, int G,
-                      const int *gidx) {
+                      const int *gidx, const double *kbias) {
     if (check_geom(BH, n, hd, w, wu, dil)) return -1;
+    if (G > 0 && kbias) return -4;
     unsigned char *gm; int *gp;
     int rc = build_gmask(n, G, gidx, &gm, &gp);
     if (rc) return rc;
@@ -476,7 +493,8 @@ int orc_attention_bwd(int BH, int n, int hd, int w, int wu, int dil, double scal
                 double *ds = sbuf + (size_t)bh * nnz + b0;
                 double m = -INFINITY, z = 0.0, delta = 0.0;
                 for (long long u = 0; u < cnt; ++u) {
-                    x[u] = scale * dot(q, K + ((size_t)bh * n + ks.key[b0 + u]) * hd, hd);
+                    x[u] = scale * dot(q, K + ((size_t)bh * n + ks.key[b0 + u]) * hd, hd) +
+                           (kbias ? kbias[(size_t)bh * n + ks.key[b0 + u]] : 0.0);
                     m = fmax(m, x[u]);
                 }
                 for (long long u = 0; u < cnt; ++u) z += exp(x[u] - m);

@@ -764,6 +764,15 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 tma_load_3d(kbuf + tb * kTile, mk, &kfull[tb], 0, tl.a0, tl.bh);
                 mbar_arrive_expect_tx(vfull, kTile);
                 tma_load_3d(vbuf, mv, vfull, 0, tl.a0, tl.bh);
+                // the next tile's K and V into L2: V is reloaded within one
+                // gradient phase at the tile boundary
+                for (int t2 = t + gridDim.x; t2 < ntiles; t2 += gridDim.x) {
+                    KTile nx;
+                    if (!decode_ktile(g, t2, xt, nx)) continue;
+                    tma_prefetch_l2_3d(&mapK.m[nx.r], 0, nx.a0, nx.bh);
+                    tma_prefetch_l2_3d(&mapV.m[nx.r], 0, nx.a0, nx.bh);
+                    break;
+                }
             }
             __syncwarp();
             ++it;
@@ -990,21 +999,16 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 uint32_t pk[16], dk[16];
                 // columns [8h, 8h + 8) of the part in four steps; the next
                 // step's loads are in flight while a step is computed
-                uint32_t svb[2][8], dvb[2][8];
-                tmem_ld8(lane_base + kColS + 32 * part, svb[0]);
-                tmem_ld8(lane_base + kColDP + 32 * part, dvb[0]);
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    tmem_ld_wait();   // step h (the only loads outstanding)
-                    if (h < 3) {
-                        tmem_ld8(lane_base + kColS + 32 * part + 8 * (h + 1), svb[(h + 1) & 1]);
-                        tmem_ld8(lane_base + kColDP + 32 * part + 8 * (h + 1), dvb[(h + 1) & 1]);
-                    } else {
+                    uint32_t sv[8], dv[8];
+                    tmem_ld8(lane_base + kColS + 32 * part + 8 * h, sv);
+                    tmem_ld8(lane_base + kColDP + 32 * part + 8 * h, dv);
+                    tmem_ld_wait();
+                    if (h == 3) {
                         tc_fence_before();
-                        mbar_arrive(sempty);   // S^T and dP^T are in registers
+                        mbar_arrive(sempty);
                     }
-                    const uint32_t (&sv)[8] = svb[h & 1];
-                    const uint32_t (&dv)[8] = dvb[h & 1];
                     if (empty) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) pk[4 * h + i] = dk[4 * h + i] = 0u;

@@ -364,6 +364,87 @@ def test_bad_global_index_rejected():
 # --------------------------------------------------------------------------
 # planted mistakes: every mutant of the oracle must fail at least one pin
 # --------------------------------------------------------------------------
+# ---------------------------------------------------------------------------
+# key-padding bias: nvFuser issue "HuggingFace BertForMaskedLM - Log Softmax
+# Fusion with Autocast has bad perf", fusion 1 adds (1 - mask) * -10000 per key
+# to the scaled scores before the softmax
+# ---------------------------------------------------------------------------
+BIAS_CASES = [  # n, hd, w, w_upper, dilation
+    (41, 6, 4, 2, 0),
+    (45, 4, 2, 5, 3),
+    (24, 8, 30, 30, 0),
+]
+
+
+def key_bias(BH, n, seed):
+    """(1 - mask) * -10000 for a random 0/1 key mask, plus small per-key terms."""
+    rng = np.random.default_rng(seed)
+    keep = rng.random((BH, n)) > 0.25
+    return np.where(keep, 0.0, -10000.0) + 0.3 * rng.standard_normal((BH, n))
+
+
+def torch_attention_bias(Q, K, V, mask, scale, kb):
+    s = scale * Q @ K.transpose(-1, -2) + kb[:, None, :]
+    s = s.masked_fill(~mask, float("-inf"))
+    return torch.softmax(s, -1) @ V, torch.logsumexp(s, -1)
+
+
+def pin_bias(n, hd, w, wu, d):
+    Q, K, V, dO = (randn(3, n, hd, seed=s) for s in (61, 62, 63, 64))
+    kb = key_bias(3, n, seed=65)
+    scale = 1.0 / np.sqrt(hd)
+    mask = dense_mask(n, w, wu, d)
+    tQ, tK, tV, tb = (torch.from_numpy(x) for x in (Q, K, V, kb))
+    O_t, lse_t = torch_attention_bias(tQ, tK, tV, mask, scale, tb)
+    O, lse = oracle.attention_fwd(Q, K, V, w, wu, d, scale, key_bias=kb)
+    np.testing.assert_allclose(O, O_t.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_t.numpy(), rtol=1e-12, atol=1e-9)
+    # the materialised chain with the bias in band_softmax
+    S = oracle.band_qk(Q, K, w, wu, d, alpha=scale, padding=11.0)
+    P, lse2 = oracle.band_softmax(S, w, wu, d, key_bias=kb)
+    O2 = oracle.band_pv(P, V, w, wu, d, 1.0)
+    np.testing.assert_allclose(O2, O_t.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse_t.numpy(), rtol=1e-12, atol=1e-9)
+    # gradients against autograd of the dense reference
+    t = [x.clone().requires_grad_(True) for x in (tQ, tK, tV)]
+    O_a, _ = torch_attention_bias(*t, mask, scale, tb)
+    O_a.backward(torch.from_numpy(dO))
+    got = oracle.attention_bwd(Q, K, V, dO, w, wu, d, scale, key_bias=kb)
+    for g, r in zip(got, t):
+        np.testing.assert_allclose(g, r.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("n,hd,w,wu,d", BIAS_CASES)
+def test_key_bias_vs_torch(n, hd, w, wu, d):
+    pin_bias(n, hd, w, wu, d)
+
+
+def test_key_bias_constant_is_a_shift():
+    """A bias equal for every key leaves P and O unchanged and shifts lse by it."""
+    n, hd, w, wu, d = 33, 5, 3, 4, 1
+    Q, K, V = (randn(2, n, hd, seed=s) for s in (66, 67, 68))
+    O0, lse0 = oracle.attention_fwd(Q, K, V, w, wu, d, 0.4)
+    O1, lse1 = oracle.attention_fwd(Q, K, V, w, wu, d, 0.4, key_bias=np.full((2, n), 2.5))
+    np.testing.assert_allclose(O1, O0, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse1, lse0 + 2.5, rtol=1e-13, atol=1e-12)
+
+
+def test_key_bias_huge_negative_removes_keys():
+    """A bias of -1e6 on a key removes it from every row's key set."""
+    n, hd, w, wu, d = 30, 4, 5, 5, 0
+    Q, K, V = (randn(1, n, hd, seed=s) for s in (69, 70, 71))
+    gone = [3, 4, 17]
+    kb = np.zeros((1, n))
+    kb[0, gone] = -1e6
+    mask = dense_mask(n, w, wu, d)
+    mask[:, gone] = False
+    mask[gone, :] = mask[gone, :] | torch.eye(n, dtype=torch.bool)[gone]  # keep rows non-empty
+    O, _ = oracle.attention_fwd(Q, K, V, w, wu, d, 0.5, key_bias=kb)
+    rows = [i for i in range(n) if i not in gone]
+    O_t, _ = torch_attention(*(torch.from_numpy(x) for x in (Q, K, V)), mask, 0.5)
+    np.testing.assert_allclose(O[:, rows], O_t.numpy()[:, rows], rtol=1e-12, atol=1e-13)
+
+
 MUTANTS = {
     "key_offset": ("(long long)(t - w) * s;", "(long long)(t - w + 1) * s;"),
     "stride": ("const int D = w + wu + 1, s = dil + 1;",
@@ -379,6 +460,9 @@ MUTANTS = {
     "global_cols_dropped_from_sum": (
         "for (int q = 0; q < G; ++q) z += exp(Sg[((size_t)bh * n + i) * G + q] - m);", ""),
     "global_key_not_excluded": ("if (gmask && gmask[j]) return 0;", ""),
+    "key_bias_ignored": ("(kbias ? kbias[(size_t)bh * n + ks.key[b0 + u]] : 0.0)", "0.0"),
+    "softmax_key_bias_ignored": ("((kbias && j >= 0 && j < n) ? kbias[(size_t)bh * n + j] : 0.0)",
+                                 "0.0"),
     "qk_transposed": ("srow[t] = alpha * dot(a, B + ((size_t)bh * n + j) * hd, hd);",
                       "srow[t] = alpha * dot(B + ((size_t)bh * n + i) * hd,"
                       " A + ((size_t)bh * n + j) * hd, hd);"),
@@ -396,6 +480,8 @@ def run_all_pins():
     pin_adjoint(gidx=(0, 5, 17))
     for c in GRAD_CASES:
         pin_grads(*c)
+    for c in BIAS_CASES:
+        pin_bias(*c)
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
