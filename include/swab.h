@@ -93,6 +93,15 @@ typedef struct swab_desc {
     int32_t dtype;             /* swab_dtype of every tensor except lse */
     int32_t n_global;          /* G, 0..SWAB_MAX_GLOBAL; 0 = no global tokens */
     const int32_t *global_idx; /* HOST array of G sorted unique positions in [0,n) */
+    /* Optional key-padding bias (nvFuser issue "HuggingFace BertForMaskedLM -
+     * Log Softmax Fusion...", fusion 1, adds (1 - mask) * -10000 per key to the
+     * scaled scores): DEVICE array of b*n fp32, 4-byte aligned, row bb holding
+     * the term added to the score of every query of batch bb with key j
+     * before the softmax; NULL for none.  Read by band_softmax, band_attention
+     * and band_attention_bwd (the other calls do not depend on it); with
+     * n_global > 0, and by band_attention_bwd_noalloc, it is
+     * SWAB_ERR_UNSUPPORTED. */
+    const float *key_bias;
 } swab_desc;
 
 /* Companion of a band tensor when n_global > 0 (device pointers, dtype of the

@@ -44,7 +44,8 @@ class _Desc(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("w", ctypes.c_int32),
                 ("w_upper", ctypes.c_int32), ("dilation", ctypes.c_int32),
                 ("padding", ctypes.c_float), ("dtype", ctypes.c_int32),
-                ("n_global", ctypes.c_int32), ("global_idx", ctypes.POINTER(ctypes.c_int32))]
+                ("n_global", ctypes.c_int32), ("global_idx", ctypes.POINTER(ctypes.c_int32)),
+                ("key_bias", ctypes.c_void_p)]
 
 
 class _Glob(ctypes.Structure):
@@ -55,7 +56,7 @@ class Desc:
     """Problem description (swab_desc).  Keeps the host global index alive."""
 
     def __init__(self, b, h, n, head_dim, w, w_upper, dilation=0, padding=0.0,
-                 dtype=torch.float16, global_idx=None):
+                 dtype=torch.float16, global_idx=None, key_bias=None):
         if dtype not in _DTYPES:
             raise ValueError(f"unsupported dtype {dtype}")
         self.b, self.h, self.n, self.head_dim = int(b), int(h), int(n), int(head_dim)
@@ -65,9 +66,17 @@ class Desc:
         gi = list(global_idx) if global_idx is not None else []
         self.global_idx = tuple(int(x) for x in gi)
         self._gi = (ctypes.c_int32 * max(1, len(gi)))(*gi) if gi else None
+        # key-padding bias: a [b, n] fp32 CUDA tensor (kept alive here), or None
+        if key_bias is not None:
+            if (key_bias.dtype != torch.float32 or tuple(key_bias.shape) != (self.b, self.n)
+                    or not key_bias.is_contiguous()):
+                raise ValueError(f"key_bias must be a contiguous float32 [b, n] = "
+                                 f"{(self.b, self.n)} tensor")
+        self.key_bias = key_bias
         self.c = _Desc(self.b, self.h, self.n, self.head_dim, self.w, self.w_upper,
                        self.dilation, self.padding, _DTYPES[dtype], len(gi),
-                       ctypes.cast(self._gi, ctypes.POINTER(ctypes.c_int32)) if gi else None)
+                       ctypes.cast(self._gi, ctypes.POINTER(ctypes.c_int32)) if gi else None,
+                       key_bias.data_ptr() if key_bias is not None else None)
 
     @property
     def BH(self):

@@ -56,7 +56,9 @@ constexpr int kKBytes = kBK * 128;              // 16 KB
 constexpr int kStageBytes = 2 * kKBytes;        // K and V: 32 KB
 constexpr int kPBytes = kBQ * kBK * 2;          // 32 KB (two 64-key K-atoms)
 constexpr int kMlBytes = 2 * kParts * kBQ * 8;  // (m, l) exchange, two tile parities
-constexpr int kSmemBytes = 2 * kQBytes + kStages * kStageBytes + 2 * kPBytes + kMlBytes + 1024 + 1024;
+constexpr int kBiasSlotBytes = kWorkerWarps * 32 * 4;  // key bias of each warp's 32 keys
+constexpr int kSmemBytes =
+    2 * kQBytes + kStages * kStageBytes + 2 * kPBytes + kMlBytes + kBiasSlotBytes + 1024 + 1024;
 constexpr uint32_t kTmemCols = 512;             // S: 2 x 128, O: 4 parts x 64
 constexpr uint32_t kTmemO = 256;                // O of part j at 256 + 64 j
 constexpr float kSlack = 8.f;                   // log2 headroom of the reference max
@@ -101,7 +103,7 @@ __device__ __forceinline__ bool decode_tile(const Geom &g, int t, int xt, Tile &
     return true;
 }
 
-template <typename T>
+template <typename T, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     k_band_attention_fwd(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
                          const __grid_constant__ TmapSet mapV, const AttnArgs p) {
@@ -112,7 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *kv = base + 2 * kQBytes;                    // stage st: K at +0, V at +kKBytes
     uint8_t *pbuf = kv + kStages * kStageBytes;          // 2 x 32 KB
     float2 *mlx = reinterpret_cast<float2 *>(pbuf + 2 * kPBytes);  // [2][kParts][kBQ]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(pbuf + 2 * kPBytes + kMlBytes);
+    float *bslots = reinterpret_cast<float *>(pbuf + 2 * kPBytes + kMlBytes);  // [16 warps][32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(pbuf + 2 * kPBytes + kMlBytes + kBiasSlotBytes);
     uint64_t *qfull = bars;                  // [2]
     uint64_t *qempty = qfull + 2;            // [2]
     uint64_t *kvfull = qempty + 2;           // [kStages]
@@ -367,6 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t vmask = jlo > jhi ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
                 const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
                 const bool empty = __all_sync(0xffffffffu, vmask == 0u);
+                float kb = 0.f;   // key bias (log2 units) of this part's key `lane`
+                if constexpr (kBias) {
+                    if (!empty && kbase + lane < tl.nr)
+                        kb = __ldg(g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * (kbase + lane)) *
+                             1.4426950408889634f;
+                }
                 bool w_ok = mbar_wait(&sfull[b], (gc >> 1) & 1, abort_flag, p.err);
                 if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
                 tc_fence_after();
@@ -390,23 +399,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sts16(prow + ((piece ^ (q & 7)) << 4), make_uint4(0u, 0u, 0u, 0u));
                     }
                 } else {
+                    if constexpr (kBias) {
+                        // scaled score plus the key bias, in log2 units: the
+                        // scale is folded in here, so the passes below see
+                        // scale 1
+                        float *slot = bslots + (warp - 2) * 32;
+                        slot[lane] = kb;
+                        __syncwarp();
+                        const float4 *b4 = reinterpret_cast<const float4 *>(slot);
+                        const uint64_t xs2 = f2(xscale, xscale);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const float4 bb = b4[u];
+                            f2split(fma2(f2(x[4 * u], x[4 * u + 1]), xs2, f2(bb.x, bb.y)), x[4 * u], x[4 * u + 1]);
+                            f2split(fma2(f2(x[4 * u + 2], x[4 * u + 3]), xs2, f2(bb.z, bb.w)), x[4 * u + 2],
+                                    x[4 * u + 3]);
+                        }
+                        __syncwarp();
+                    }
                     // chunk max of the scaled scores from the raw ones: the
                     // largest raw score for a positive scale, the smallest
                     // for a negative one; columns outside the band are
                     // replaced by the value that never wins
+                    const bool neg = kBias ? false : neg_scale;
                     if (!full) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (!((vmask >> i) & 1u)) x[i] = neg_scale ? INFINITY : -INFINITY;
+                            if (!((vmask >> i) & 1u)) x[i] = neg ? INFINITY : -INFINITY;
                     }
-                    const float vm = neg_scale ? reduce32<true>(x) : reduce32<false>(x);
-                    cmax = vmask == 0u ? -INFINITY : vm * xscale;
+                    const float vm = neg ? reduce32<true>(x) : reduce32<false>(x);
+                    cmax = vmask == 0u ? -INFINITY : vm * (kBias ? 1.f : xscale);
                 }
                 const bool raise = m == -INFINITY || cmax > m + kSlack;
                 const float mref = raise ? cmax : m;
                 if (!empty) {
                     const float mb = mref == -INFINITY ? 0.f : mref;
-                    const uint64_t xs2 = f2(xscale, xscale), nb2 = f2(-mb, -mb);
+                    const float xs_eff = kBias ? 1.f : xscale;   // the bias path holds scaled scores
+                    const uint64_t xs2 = f2(xs_eff, xs_eff), nb2 = f2(-mb, -mb);
                     uint64_t lc2 = f2(0.f, 0.f);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -519,7 +548,8 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
         float sdot = 0.f;
         for (int k = 0; k < nw; ++k) sdot += part[k];
         __syncthreads();
-        const float sc = sdot * p.scale;
+        const float sc = sdot * p.scale +
+                         (g.kbias ? g.kbias[(size_t)(bh / g.h) * g.n + (size_t)j] : 0.f);
         const float m_new = fmaxf(m, sc);
         const float corr = (m == -INFINITY) ? 0.f : expf(m - m_new);
         const float pv = expf(sc - m_new);
@@ -531,16 +561,16 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
     if (c == 0 && p.lse) p.lse[R] = m + logf(l);
 }
 
-template <typename T>
+template <typename T, bool kBias>
 cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const AttnArgs &a,
                      cudaStream_t st) {
     const long long tiles = (long long)((a.g.nsub + kBQ - 1) / kBQ) * a.g.s * a.g.BH;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_attention_fwd<T>), kSmemBytes);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_attention_fwd<T, kBias>), kSmemBytes);
     if (e != cudaSuccess) return e;
-    k_band_attention_fwd<T><<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, a);
+    k_band_attention_fwd<T, kBias><<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, a);
     return cudaGetLastError();
 }
 
@@ -555,8 +585,11 @@ cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st) {
 
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                      const TmapSet &mapV, const AttnArgs &a, cudaStream_t st) {
-    if (dt == kF16) return launch_t<__half>(mapQ, mapK, mapV, a, st);
-    return launch_t<__nv_bfloat16>(mapQ, mapK, mapV, a, st);
+    const bool bias = a.g.kbias != nullptr;
+    if (dt == kF16)
+        return bias ? launch_t<__half, true>(mapQ, mapK, mapV, a, st) : launch_t<__half, false>(mapQ, mapK, mapV, a, st);
+    return bias ? launch_t<__nv_bfloat16, true>(mapQ, mapK, mapV, a, st)
+                : launch_t<__nv_bfloat16, false>(mapQ, mapK, mapV, a, st);
 }
 
 }  // namespace swab

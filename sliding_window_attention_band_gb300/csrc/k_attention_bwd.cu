@@ -666,7 +666,7 @@ __device__ __forceinline__ bool decode_ktile(const Geom &g, int t, int xt, KTile
 }
 }  // namespace fused
 
-template <typename T>
+template <typename T, bool kBias>
 __global__ void __launch_bounds__(fused::kThreads, 1)
     k_bwd_fused(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
                 const __grid_constant__ TmapSet mapV, const __grid_constant__ TmapSet mapdO,
@@ -967,6 +967,14 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             KTile tl;
             if (!decode_ktile(g, t, xt, tl)) continue;
             const int kk = tl.a0 + m;
+            // key bias of this thread's key (log2 units), the same for every query
+            uint64_t kb2 = f2(0.f, 0.f);
+            if constexpr (kBias) {
+                if (kk < tl.nr) {
+                    const float kb = __ldg(g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * kk) * kLog2e;
+                    kb2 = f2(kb, kb);
+                }
+            }
             for (int c = 0; c < tl.nck; ++c, ++gc) {
                 const int qbase = tl.qb_lo + c * kB;
                 const int cbase = qbase + 32 * part;
@@ -1022,8 +1030,11 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                         float p0, p1, p2, p3;
                         {
                             float y0, y1, y2, y3;
-                            f2split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), xs2, f2(-lv.x, -lv.y)), y0, y1);
-                            f2split(fma2(f2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), xs2, f2(-lv.z, -lv.w)), y2, y3);
+                            // x * scale * log2e (+ key bias) - lse * log2e
+                            const uint64_t c01 = kBias ? sub2(kb2, f2(lv.x, lv.y)) : f2(-lv.x, -lv.y);
+                            const uint64_t c23 = kBias ? sub2(kb2, f2(lv.z, lv.w)) : f2(-lv.z, -lv.w);
+                            f2split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), xs2, c01), y0, y1);
+                            f2split(fma2(f2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), xs2, c23), y2, y3);
                             p0 = ex2(y0);
                             p1 = ex2(y1);
                             p2 = ex2(y2);
@@ -1167,7 +1178,8 @@ __global__ void __launch_bounds__(128) k_bwd_f32(const BwdArgs p, int pass) {
         const long long i = pass == 0 ? x : y, j = pass == 0 ? y : x;
         const float sdot = block_dot(on ? Q[i * g.hd + c] * K[j * g.hd + c] : 0.f, part);
         const float pdot = block_dot(on ? dO[i * g.hd + c] * V[j * g.hd + c] : 0.f, part);
-        const float pr = expf(p.scale * sdot - lse[i]);
+        const float kb = g.kbias ? g.kbias[(size_t)(bh / g.h) * g.n + (size_t)j] : 0.f;
+        const float pr = expf(p.scale * sdot + kb - lse[i]);
         const float ds = pr * (pdot - delta[i]);
         if (!on) continue;
         if (pass == 0) {
@@ -1217,7 +1229,7 @@ cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, co
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool kBias>
 cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const TmapSet &mo,
                            const TmapSet &macc, const BwdArgs &a, cudaStream_t st) {
     const long long rows = (long long)a.g.BH * a.g.n;
@@ -1229,9 +1241,9 @@ cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T>), fused::kSmem);
+    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, kBias>), fused::kSmem);
     if (e != cudaSuccess) return e;
-    k_bwd_fused<T><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, macc, a);
+    k_bwd_fused<T, kBias><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, macc, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long groups = rows * 8;
@@ -1245,8 +1257,12 @@ cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const T
                                             const TmapSet &mv, const TmapSet &mo, const TmapSet &macc,
                                             const BwdArgs &a, cudaStream_t st) {
     if (!a.dqacc) return cudaErrorInvalidValue;
-    if (dt == kF16) return launch_fused_t<__half>(mq, mk, mv, mo, macc, a, st);
-    return launch_fused_t<__nv_bfloat16>(mq, mk, mv, mo, macc, a, st);
+    const bool bias = a.g.kbias != nullptr;
+    if (dt == kF16)
+        return bias ? launch_fused_t<__half, true>(mq, mk, mv, mo, macc, a, st)
+                    : launch_fused_t<__half, false>(mq, mk, mv, mo, macc, a, st);
+    return bias ? launch_fused_t<__nv_bfloat16, true>(mq, mk, mv, mo, macc, a, st)
+                : launch_fused_t<__nv_bfloat16, false>(mq, mk, mv, mo, macc, a, st);
 }
 
 cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const TmapSet &mk,

@@ -111,6 +111,23 @@ __device__ __forceinline__ bool all_valid(int x0, int n, const Row &rw) {
     return x0 >= rw.xlo && x0 + n - 1 <= rw.xhi;
 }
 
+// Key-padding bias row of row R's batch (null without a bias).
+__device__ __forceinline__ const float *bias_row(const Geom &g, int R) {
+    return g.kbias ? g.kbias + (size_t)(R / g.n / g.h) * g.n : nullptr;
+}
+
+// Adds the key bias to the valid elements of a piece: element x is slot
+// t = x - lead, whose key is i + (t - w) * s.
+template <int N>
+__device__ __forceinline__ void add_key_bias(float (&x)[N], int x0, const Row &rw, const float *brow,
+                                             int i, const Geom &g) {
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+        const int xx = x0 + u;
+        if (xx >= rw.xlo && xx <= rw.xhi) x[u] += __ldg(brow + i + (xx - rw.lead - g.w) * g.s);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // register-resident rows
 // ---------------------------------------------------------------------------
@@ -123,6 +140,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
     const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
     if (R >= g.BH * g.n) return;
     const Row rw = make_row<T>(g, R);
+    const float *brow = bias_row(g, R);
+    const int qi = R % g.n;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
     uint4 raw[NCH];
 #pragma unroll
@@ -136,6 +155,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
         const int x0 = (lane + 32 * k) * N;
         float x[N];
         unpack<T>(raw[k], x);
+        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
         if (all_valid(x0, N, rw)) {
 #pragma unroll
             for (int u = 0; u < N; ++u) m = fmaxf(m, x[u]);
@@ -155,6 +175,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
         const int x0 = (lane + 32 * k) * N;
         float x[N];
         unpack<T>(raw[k], x);
+        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
         const bool full = all_valid(x0, N, rw);
 #pragma unroll
         for (int u = 0; u < N; ++u) {
@@ -180,6 +201,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
         } else {
             float x[N];
             unpack<T>(raw[k], x);
+            if (brow) add_key_bias(x, x0, rw, brow, qi, g);
             const bool full = all_valid(x0, N, rw);
 #pragma unroll
             for (int u = 0; u < N; ++u) {
@@ -258,6 +280,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
     const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
     if (R >= g.BH * g.n) return;
     const Row rw = make_row<T>(g, R);
+    const float *brow = bias_row(g, R);
+    const int qi = R % g.n;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
     // pass 1: per-lane running max (log2 units) and sum, one rescale per piece
     float m = -INFINITY, z = 0.f;
@@ -265,6 +289,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
         float x[N];
         unpack<T>(ldg16(src + pc), x);
         const int x0 = pc * N;
+        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
         float pm = -INFINITY;
 #pragma unroll
         for (int u = 0; u < N; ++u) {
@@ -293,6 +318,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
         float x[N];
         unpack<T>(ldg16(src + pc), x);
         const int x0 = pc * N;
+        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
 #pragma unroll
         for (int u = 0; u < N; ++u) {
             const bool v = x0 + u >= rw.xlo && x0 + u <= rw.xhi;

@@ -60,6 +60,10 @@ swab_status check_desc(const swab_desc *d, Geom *g, DType *dt) {
         }
     }
     if (d->dilation > SWAB_MAX_DILATION) return SWAB_ERR_UNSUPPORTED;
+    if (d->key_bias) {
+        if (reinterpret_cast<uintptr_t>(d->key_bias) % 4 != 0) return SWAB_ERR_MISALIGNED;
+        if (d->n_global > 0) return SWAB_ERR_UNSUPPORTED;  // key bias with global tokens
+    }
     const long long BH = (long long)d->b * d->h;
     const long long D = (long long)d->w + d->w_upper + 1;
     if (BH > 65535) return SWAB_ERR_UNSUPPORTED;          // grid z
@@ -79,6 +83,8 @@ swab_status check_desc(const swab_desc *d, Geom *g, DType *dt) {
     g->D = (int)D;
     g->nsub = (d->n + g->s - 1) / g->s;
     g->padding = d->padding;
+    g->h = d->h;
+    g->kbias = d->key_bias;
     *dt = static_cast<DType>(d->dtype);
     return SWAB_OK;
 }
@@ -487,6 +493,7 @@ SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float sca
     if (s != SWAB_OK) return s;
     if ((s = check_no_globals(desc)) != SWAB_OK) return s;
     if ((long long)g.BH * g.n > (long long)SWAB_NOALLOC_MAX_ROWS) return SWAB_ERR_UNSUPPORTED;
+    if (desc->key_bias) return SWAB_ERR_UNSUPPORTED;  // the two-kernel path has no key bias
     if ((s = check_ptrs({Q, K, V, O, dO, lse, dQ, dK, dV})) != SWAB_OK) return s;
     float *scratch = nullptr;
     if (noalloc_delta_scratch(&scratch) != cudaSuccess) return SWAB_ERR_CUDA;

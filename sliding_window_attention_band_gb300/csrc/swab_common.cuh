@@ -39,6 +39,8 @@ struct Geom {
     int D;        // band slots w + wu + 1
     int nsub;     // ceil(n / s): longest residue subsequence
     float padding;
+    int h;                // heads: slice bh belongs to batch bh / h
+    const float *kbias;   // [b, n] key-padding bias added to scaled scores, or null
 };
 
 __host__ __device__ __forceinline__ int residue_len(int n, int s, int r) {

@@ -211,3 +211,25 @@ def test_binding_checks_companion_shapes():
     bad = (torch.zeros(2, 256, 3, dtype=torch.float16), torch.zeros(2, 2, 256, dtype=torch.float16))
     with pytest.raises(ValueError):
         B._glob(bad, d, "Sg")
+
+
+def test_key_bias_validation(lib):
+    """The key-padding bias must be 4-byte aligned, is not combined with global
+    tokens, and the allocation-free backward does not take it."""
+    d = desc()
+    d.c.key_bias = FAKE + 2
+    assert call(lib, "band_softmax", d, FAKE, FAKE) == MISALIGNED
+    dg = desc(n=512, global_idx=[0, 5])
+    dg.c.key_bias = FAKE
+    assert call(lib, "band_qk", dg, FAKE, FAKE, FAKE) == UNSUPPORTED
+    d.c.key_bias = FAKE
+    P = ctypes.c_void_p
+    assert lib.band_attention_bwd_noalloc(ctypes.byref(d.c), 0.125, *(P(FAKE) for _ in range(9)),
+                                          None) == UNSUPPORTED
+
+
+def test_binding_key_bias_shape():
+    with pytest.raises(ValueError):
+        B.Desc(2, 3, 64, 64, 4, 4, key_bias=torch.zeros(3, 64))
+    with pytest.raises(ValueError):
+        B.Desc(2, 3, 64, 64, 4, 4, key_bias=torch.zeros(2, 64, dtype=torch.float16))
