@@ -53,8 +53,14 @@ def _load():
         _lib.orc_band_pv.argtypes = [i, i, i, i, i, i, d, p, p, p, i, p, p, p]
         _lib.orc_band_t.argtypes = [i, i, i, i, i, i, d, p, p, p, i, p, p, p]
         _lib.orc_band_softmax_bwd.argtypes = [i, i, i, i, i, p, p, p, i, p, p, p, p, p, p, p]
-        _lib.orc_attention_fwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, i, p, p]
-        _lib.orc_attention_bwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, p, p, i, p, p]
+        u64 = ctypes.c_uint64
+        _lib.orc_attention_fwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, i, p, p, u64, i]
+        _lib.orc_attention_bwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, p, p, i, p, p,
+                                           u64, i]
+        _lib.orc_philox4x64.argtypes = [p, p, p]
+        _lib.orc_philox4x64.restype = i
+        _lib.orc_dropout_factor.argtypes = [u64, i, i, i, i, i, ctypes.POINTER(ctypes.c_double)]
+        _lib.orc_dropout_factor.restype = i
         for f in ("orc_band_qk", "orc_band_softmax", "orc_band_pv", "orc_band_t",
                   "orc_band_softmax_bwd", "orc_attention_fwd", "orc_attention_bwd"):
             getattr(_lib, f).restype = i
@@ -174,9 +180,28 @@ def band_softmax_bwd(P, dP, w, w_upper, dilation=0, global_idx=None, Pg=None, dP
     return (dS, dSg, dSr) if G else dS
 
 
-def attention_fwd(Q, K, V, w, w_upper, dilation=0, scale=None, global_idx=None, key_bias=None):
+def philox4x64(counter, key):
+    """Philox4x64-10 block of a 4-word counter and 2-word key (uint64)."""
+    c = np.ascontiguousarray(counter, dtype=np.uint64)
+    k = np.ascontiguousarray(key, dtype=np.uint64)
+    out = np.empty(4, dtype=np.uint64)
+    _check(_load().orc_philox4x64(_ptr(c), _ptr(k), _ptr(out)), "philox4x64")
+    return out
+
+
+def dropout_factor(seed, drop_t, bh, i, j, s):
+    """Keep-and-scale factor of element (bh, i, j): 0 or 256 / (256 - drop_t)."""
+    out = ctypes.c_double()
+    _check(_load().orc_dropout_factor(seed, drop_t, bh, i, j, s, ctypes.byref(out)),
+           "dropout_factor")
+    return out.value
+
+
+def attention_fwd(Q, K, V, w, w_upper, dilation=0, scale=None, global_idx=None, key_bias=None,
+                  drop_t=0, seed=0):
     """Attention on explicit key sets (key_bias[bh, j] added to the scaled score of
-    key j).  Returns (O, lse)."""
+    key j; dropout of the probabilities with threshold byte drop_t).  Returns
+    (O, lse)."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     BH, n, hd = Q.shape
     kb = _kbias(key_bias, BH, n)
@@ -185,13 +210,13 @@ def attention_fwd(Q, K, V, w, w_upper, dilation=0, scale=None, global_idx=None, 
     O = np.empty((BH, n, hd))
     lse = np.empty((BH, n))
     _check(_load().orc_attention_fwd(BH, n, hd, w, w_upper, dilation, scale, _ptr(Q),
-                                     _ptr(K), _ptr(V), _ptr(O), _ptr(lse), G, _ptr(g), _ptr(kb)),
-           "attention_fwd")
+                                     _ptr(K), _ptr(V), _ptr(O), _ptr(lse), G, _ptr(g), _ptr(kb),
+                                     seed, drop_t), "attention_fwd")
     return O, lse
 
 
 def attention_bwd(Q, K, V, dO, w, w_upper, dilation=0, scale=None, global_idx=None,
-                  key_bias=None):
+                  key_bias=None, drop_t=0, seed=0):
     """Gradients of attention_fwd's O.  Returns (dQ, dK, dV)."""
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
     BH, n, hd = Q.shape
@@ -201,5 +226,6 @@ def attention_bwd(Q, K, V, dO, w, w_upper, dilation=0, scale=None, global_idx=No
     dQ, dK, dV = (np.empty((BH, n, hd)) for _ in range(3))
     _check(_load().orc_attention_bwd(BH, n, hd, w, w_upper, dilation, scale, _ptr(Q),
                                      _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK),
-                                     _ptr(dV), G, _ptr(g), _ptr(kb)), "attention_bwd")
+                                     _ptr(dV), G, _ptr(g), _ptr(kb), seed, drop_t),
+           "attention_bwd")
     return dQ, dK, dV

@@ -41,6 +41,7 @@
  * Every function returns 0 on success and a negative code on bad arguments.
  */
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -377,6 +378,65 @@ typedef struct {
     int *key;
 } keysets;
 
+/* ---------------------------------------------------------------------
+ * Dropout mask from the counter-based generator Philox4x64-10 (Salmon,
+ * Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ * SC'11): ten rounds of two 64x64->128 multiplies with the published
+ * multipliers, the key bumped by the published Weyl constants between
+ * rounds.  Element (slice bh, query i, key j) with b = floor(j / s) reads byte
+ * (b mod 32) of the block at counter (floor(b / 32), i, bh, 0) and key
+ * (seed, 0), bytes taken little-endian from the four output words; it is
+ * kept when that byte is >= drop_t (keep probability 1 - drop_t/256) and
+ * then scaled by 256 / (256 - drop_t) (nvFuser issue, fusion 1: dropout with
+ * 1/(1-p) scaling).
+ * --------------------------------------------------------------------- */
+static void mulhilo64(uint64_t a, uint64_t b, uint64_t *hi, uint64_t *lo) {
+    const uint64_t a0 = a & 0xffffffffu, a1 = a >> 32, b0 = b & 0xffffffffu, b1 = b >> 32;
+    const uint64_t p00 = a0 * b0, p01 = a0 * b1, p10 = a1 * b0, p11 = a1 * b1;
+    const uint64_t mid = (p00 >> 32) + (p01 & 0xffffffffu) + (p10 & 0xffffffffu);
+    *lo = a * b;
+    *hi = p11 + (p01 >> 32) + (p10 >> 32) + (mid >> 32);
+}
+
+int orc_philox4x64(const uint64_t *ctr, const uint64_t *key, uint64_t *out) {
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B97F4A7C15ull;
+            k1 += 0xBB67AE8584CAA73Bull;
+        }
+        uint64_t hi0, lo0, hi1, lo1;
+        mulhilo64(0xD2E7470EE14C6C93ull, c0, &hi0, &lo0);
+        mulhilo64(0xCA5A826395121157ull, c2, &hi1, &lo1);
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+    return 0;
+}
+
+/* keep-and-scale factor of element (bh, i, j): 0 or 256 / (256 - drop_t) */
+static double drop_factor(uint64_t seed, int drop_t, int bh, int i, int j, int s) {
+    if (drop_t <= 0) return 1.0;
+    const uint64_t b = (uint64_t)(j / s);
+    const uint64_t ctr[4] = {b / 32, (uint64_t)i, (uint64_t)bh, 0};
+    const uint64_t key[2] = {seed, 0};
+    uint64_t out[4];
+    orc_philox4x64(ctr, key, out);
+    const int k = (int)(b % 32);
+    const int byte = (int)((out[k / 8] >> (8 * (k % 8))) & 0xffu);
+    return byte >= drop_t ? 256.0 / (256.0 - drop_t) : 0.0;
+}
+
+int orc_dropout_factor(uint64_t seed, int drop_t, int bh, int i, int j, int s, double *out) {
+    if (drop_t < 0 || drop_t > 255 || s < 1) return -1;
+    *out = drop_factor(seed, drop_t, bh, i, j, s);
+    return 0;
+}
+
 static int build_keysets(int n, int w, int wu, int dil, int G, const int *gidx,
                          const unsigned char *gmask, keysets *ks) {
     const int s = dil + 1;
@@ -415,9 +475,12 @@ static int build_keysets(int n, int w, int wu, int dil, int G, const int *gidx,
 
 int orc_attention_fwd(int BH, int n, int hd, int w, int wu, int dil, double scale,
                       const double *Q, const double *K, const double *V, double *O,
-                      double *lse, int G, const int *gidx, const double *kbias) {
+                      double *lse, int G, const int *gidx, const double *kbias, uint64_t seed,
+                      int drop_t) {
     if (check_geom(BH, n, hd, w, wu, dil)) return -1;
     if (G > 0 && kbias) return -4;
+    if (drop_t < 0 || drop_t > 255 || (G > 0 && drop_t > 0)) return -4;
+    const int s_ = dil + 1;
     unsigned char *gm; int *gp;
     int rc = build_gmask(n, G, gidx, &gm, &gp);
     if (rc) return rc;
@@ -442,7 +505,8 @@ int orc_attention_fwd(int BH, int n, int hd, int w, int wu, int dil, double scal
                 double *o = O + ((size_t)bh * n + i) * hd;
                 for (int c = 0; c < hd; ++c) o[c] = 0.0;
                 for (long long u = 0; u < cnt; ++u) {
-                    const double p = exp(x[u] - m) / z;
+                    const double p = exp(x[u] - m) / z *
+                                     drop_factor(seed, drop_t, bh, i, ks.key[b0 + u], s_);
                     const double *v = V + ((size_t)bh * n + ks.key[b0 + u]) * hd;
                     for (int c = 0; c < hd; ++c) o[c] += p * v[c];
                 }
@@ -464,9 +528,11 @@ int orc_attention_fwd(int BH, int n, int hd, int w, int wu, int dil, double scal
 int orc_attention_bwd(int BH, int n, int hd, int w, int wu, int dil, double scale,
                       const double *Q, const double *K, const double *V,
                       const double *dO, double *dQ, double *dK, double *dV, int G,
-                      const int *gidx, const double *kbias) {
+                      const int *gidx, const double *kbias, uint64_t seed, int drop_t) {
     if (check_geom(BH, n, hd, w, wu, dil)) return -1;
     if (G > 0 && kbias) return -4;
+    if (drop_t < 0 || drop_t > 255 || (G > 0 && drop_t > 0)) return -4;
+    const int s_ = dil + 1;
     unsigned char *gm; int *gp;
     int rc = build_gmask(n, G, gidx, &gm, &gp);
     if (rc) return rc;
@@ -498,15 +564,20 @@ int orc_attention_bwd(int BH, int n, int hd, int w, int wu, int dil, double scal
                     m = fmax(m, x[u]);
                 }
                 for (long long u = 0; u < cnt; ++u) z += exp(x[u] - m);
+                /* with dropout the product uses p * f (f the keep-and-scale
+                 * factor): dP~ = f dP, delta = sum p f dP = dO . O, and
+                 * dS = p (f dP - delta); dV takes p f */
                 for (long long u = 0; u < cnt; ++u) {
+                    const double f = drop_factor(seed, drop_t, bh, i, ks.key[b0 + u], s_);
                     p[u] = exp(x[u] - m) / z;
-                    ds[u] = dot(go, V + ((size_t)bh * n + ks.key[b0 + u]) * hd, hd);
+                    ds[u] = f * dot(go, V + ((size_t)bh * n + ks.key[b0 + u]) * hd, hd);
                     delta += p[u] * ds[u];
                 }
                 double *gq = dQ + ((size_t)bh * n + i) * hd;
                 for (int c = 0; c < hd; ++c) gq[c] = 0.0;
                 for (long long u = 0; u < cnt; ++u) {
                     ds[u] = p[u] * (ds[u] - delta);
+                    p[u] *= drop_factor(seed, drop_t, bh, i, ks.key[b0 + u], s_);
                     const double *k = K + ((size_t)bh * n + ks.key[b0 + u]) * hd;
                     for (int c = 0; c < hd; ++c) gq[c] += scale * ds[u] * k[c];
                 }

@@ -445,6 +445,96 @@ def test_key_bias_huge_negative_removes_keys():
     np.testing.assert_allclose(O[:, rows], O_t.numpy()[:, rows], rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------------------
+# dropout of the probabilities (nvFuser issue, fusion 1: p with 1/(1-p)
+# scaling) from the counter-based generator Philox4x64-10 (Salmon et al.,
+# SC'11), pinned to numpy's implementation of the same generator
+# ---------------------------------------------------------------------------
+def numpy_philox_block(counter, key):
+    """The Philox4x64-10 block at `counter` from numpy (which advances the
+    counter before producing a block)."""
+    c = np.array(counter, dtype=np.uint64)
+    c[0] -= np.uint64(1)  # the tests use counter[0] >= 1
+    bg = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=c)
+    return bg.random_raw(4).astype(np.uint64)
+
+
+@pytest.mark.parametrize("counter,key", [((1, 0, 0, 0), (0, 0)), ((5, 7, 3, 0), (2024, 0)),
+                                         ((1 << 40, 99, 12, 0), (0xDEADBEEF12345678, 0))])
+def test_philox_matches_numpy(counter, key):
+    np.testing.assert_array_equal(oracle.philox4x64(counter, key), numpy_philox_block(counter, key))
+
+
+def test_dropout_factor_definition():
+    """Element (bh, i, j): byte (b mod 32) of the block at (b // 32, i, bh, 0),
+    b = j // s, little-endian bytes of the four words; kept iff byte >= t."""
+    rng = np.random.default_rng(5)
+    for _ in range(40):
+        seed, t = int(rng.integers(1, 1 << 62)), int(rng.integers(1, 256))
+        bh, i, s = int(rng.integers(0, 50)), int(rng.integers(0, 5000)), int(rng.integers(1, 4))
+        j = int(rng.integers(32 * s, 5000))
+        b = j // s
+        blk = numpy_philox_block((b // 32, i, bh, 0), (seed, 0))
+        k = b % 32
+        byte = (int(blk[k // 8]) >> (8 * (k % 8))) & 0xFF
+        want = 256.0 / (256.0 - t) if byte >= t else 0.0
+        assert oracle.dropout_factor(seed, t, bh, i, j, s) == want
+
+
+def test_dropout_keep_fraction():
+    t, seed, kept, tot = 26, 77, 0, 0
+    for i in range(64):
+        for j in range(0, 2048, 3):
+            kept += oracle.dropout_factor(seed, t, 1, i, j, 1) > 0
+            tot += 1
+    frac = kept / tot
+    expect = 1 - t / 256
+    assert abs(frac - expect) < 5 * np.sqrt(expect * (1 - expect) / tot)
+
+
+def dense_drop_factors(BH, n, s, seed, t):
+    F = np.ones((BH, n, n))
+    for bh in range(BH):
+        for i in range(n):
+            for j in range(n):
+                F[bh, i, j] = oracle.dropout_factor(seed, t, bh, i, j, s)
+    return F
+
+
+DROP_CASES = [  # n, hd, w, w_upper, dilation, threshold
+    (37, 5, 4, 3, 0, 26),
+    (41, 4, 3, 5, 2, 77),
+]
+
+
+@pytest.mark.parametrize("n,hd,w,wu,d,t", DROP_CASES)
+def test_dropout_attention_vs_torch(n, hd, w, wu, d, t):
+    Q, K, V, dO = (randn(2, n, hd, seed=sd) for sd in (81, 82, 83, 84))
+    scale, seed = 0.4, 1234567
+    F = torch.from_numpy(dense_drop_factors(2, n, d + 1, seed, t))
+    mask = dense_mask(n, w, wu, d)
+    t_in = [torch.from_numpy(x).clone().requires_grad_(True) for x in (Q, K, V)]
+    sc = scale * t_in[0] @ t_in[1].transpose(-1, -2)
+    sc = sc.masked_fill(~mask, float("-inf"))
+    O_t = (torch.softmax(sc, -1) * F) @ t_in[2]
+    O_t.backward(torch.from_numpy(dO))
+    O, lse = oracle.attention_fwd(Q, K, V, w, wu, d, scale, drop_t=t, seed=seed)
+    np.testing.assert_allclose(O, O_t.detach().numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(sc, -1).detach().numpy(), rtol=1e-12,
+                               atol=1e-12)
+    got = oracle.attention_bwd(Q, K, V, dO, w, wu, d, scale, drop_t=t, seed=seed)
+    for g, r in zip(got, t_in):
+        np.testing.assert_allclose(g, r.grad.numpy(), rtol=1e-9, atol=1e-11)
+    # threshold 0 is no dropout
+    O0, _ = oracle.attention_fwd(Q, K, V, w, wu, d, scale, drop_t=0, seed=seed)
+    O1, _ = oracle.attention_fwd(Q, K, V, w, wu, d, scale)
+    np.testing.assert_array_equal(O0, O1)
+
+
+def pin_dropout():
+    test_dropout_attention_vs_torch(*DROP_CASES[0])
+
+
 MUTANTS = {
     "key_offset": ("(long long)(t - w) * s;", "(long long)(t - w + 1) * s;"),
     "stride": ("const int D = w + wu + 1, s = dil + 1;",
@@ -463,6 +553,10 @@ MUTANTS = {
     "key_bias_ignored": ("(kbias ? kbias[(size_t)bh * n + ks.key[b0 + u]] : 0.0)", "0.0"),
     "softmax_key_bias_ignored": ("((kbias && j >= 0 && j < n) ? kbias[(size_t)bh * n + j] : 0.0)",
                                  "0.0"),
+    "dropout_factor_dropped": ("""                    const double p = exp(x[u] - m) / z *
+                                     drop_factor(seed, drop_t, bh, i, ks.key[b0 + u], s_);""",
+                               """                    const double p = exp(x[u] - m) / z;"""),
+    "dropout_byte_order": ("(out[k / 8] >> (8 * (k % 8)))", "(out[k % 4] >> (8 * (k / 4)))"),
     "qk_transposed": ("srow[t] = alpha * dot(a, B + ((size_t)bh * n + j) * hd, hd);",
                       "srow[t] = alpha * dot(B + ((size_t)bh * n + i) * hd,"
                       " A + ((size_t)bh * n + j) * hd, hd);"),
@@ -482,6 +576,8 @@ def run_all_pins():
         pin_grads(*c)
     for c in BIAS_CASES:
         pin_bias(*c)
+    pin_dropout()
+    test_dropout_factor_definition()
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
