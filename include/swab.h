@@ -102,6 +102,19 @@ typedef struct swab_desc {
      * n_global > 0, and by band_attention_bwd_noalloc, it is
      * SWAB_ERR_UNSUPPORTED. */
     const float *key_bias;
+    /* Optional dropout of the attention probabilities (the nvFuser fusion 1
+     * dropout, p with 1/(1-p) scaling), in band_attention and
+     * band_attention_bwd (pass the same values to both): dropout_p in [0, 1) is
+     * rounded to t = round(256 * dropout_p) (at most 255); an element is kept
+     * with probability 1 - t/256 and then scaled by 256 / (256 - t).  Element
+     * (slice bh, query i, key j) is kept iff byte (b mod 32), b = floor(j / s),
+     * of the Philox4x64-10 block at counter (floor(b / 32), i, bh, 0) and key
+     * (dropout_seed, 0) -- bytes little-endian from the four output words --
+     * is >= t.  lse is that of the probabilities before dropout.  With t > 0,
+     * band_softmax, global tokens and band_attention_bwd_noalloc return
+     * SWAB_ERR_UNSUPPORTED; the other calls do not depend on it. */
+    float dropout_p;
+    uint64_t dropout_seed;
 } swab_desc;
 
 /* Companion of a band tensor when n_global > 0 (device pointers, dtype of the

@@ -45,7 +45,8 @@ class _Desc(ctypes.Structure):
                 ("w_upper", ctypes.c_int32), ("dilation", ctypes.c_int32),
                 ("padding", ctypes.c_float), ("dtype", ctypes.c_int32),
                 ("n_global", ctypes.c_int32), ("global_idx", ctypes.POINTER(ctypes.c_int32)),
-                ("key_bias", ctypes.c_void_p)]
+                ("key_bias", ctypes.c_void_p), ("dropout_p", ctypes.c_float),
+                ("dropout_seed", ctypes.c_uint64)]
 
 
 class _Glob(ctypes.Structure):
@@ -56,7 +57,8 @@ class Desc:
     """Problem description (swab_desc).  Keeps the host global index alive."""
 
     def __init__(self, b, h, n, head_dim, w, w_upper, dilation=0, padding=0.0,
-                 dtype=torch.float16, global_idx=None, key_bias=None):
+                 dtype=torch.float16, global_idx=None, key_bias=None, dropout_p=0.0,
+                 dropout_seed=0):
         if dtype not in _DTYPES:
             raise ValueError(f"unsupported dtype {dtype}")
         self.b, self.h, self.n, self.head_dim = int(b), int(h), int(n), int(head_dim)
@@ -73,10 +75,17 @@ class Desc:
                 raise ValueError(f"key_bias must be a contiguous float32 [b, n] = "
                                  f"{(self.b, self.n)} tensor")
         self.key_bias = key_bias
+        self.dropout_p, self.dropout_seed = float(dropout_p), int(dropout_seed)
         self.c = _Desc(self.b, self.h, self.n, self.head_dim, self.w, self.w_upper,
                        self.dilation, self.padding, _DTYPES[dtype], len(gi),
                        ctypes.cast(self._gi, ctypes.POINTER(ctypes.c_int32)) if gi else None,
-                       key_bias.data_ptr() if key_bias is not None else None)
+                       key_bias.data_ptr() if key_bias is not None else None, self.dropout_p,
+                       self.dropout_seed)
+
+    @property
+    def drop_t(self):
+        """Dropout threshold byte: round(256 * dropout_p), at most 255."""
+        return min(255, int(round(256.0 * self.dropout_p)))
 
     @property
     def BH(self):

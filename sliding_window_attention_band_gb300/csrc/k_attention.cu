@@ -97,13 +97,15 @@ __device__ __forceinline__ bool decode_tile(const Geom &g, int t, int xt, Tile &
     tl.bh = rest / g.s;
     tl.nr = residue_len(g.n, g.s, tl.r);
     if (tl.a0 >= tl.nr) return false;
-    tl.kb_lo = max(tl.a0 - g.w, 0);
+    // the key range starts on a multiple of 32 (keys before the band are
+    // masked), so each softmax warp's 32 keys of a chunk are one dropout block
+    tl.kb_lo = max(tl.a0 - g.w, 0) & ~31;
     tl.kb_hi = min(tl.a0 + kBQ - 1 + g.wu, tl.nr - 1);
     tl.nck = (tl.kb_hi - tl.kb_lo + kBK) / kBK;
     return true;
 }
 
-template <typename T, bool kBias>
+template <typename T, bool kBias, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     k_band_attention_fwd(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
                          const __grid_constant__ TmapSet mapV, const AttnArgs p) {
@@ -298,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = quarter * 32 + lane;
         const float xscale = p.scale * 1.4426950408889634f;
         const bool neg_scale = xscale < 0.f;
+        const float dscale = 256.f / (256.f - (float)g.drop_t);   // kept values' scale
         const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
         const uint32_t o_mine = lane_base + kTmemO + 64 * part;
         uint32_t gc = 0, it = 0;
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 f[j] = e[j].x == -INFINITY ? 0.f : ex2(e[j].x - M);
                 L += e[j].y * f[j];
             }
-            const float inv = 1.f / L;
+            const float inv = (kDrop ? dscale : 1.f) / L;   // kept values scaled once, here
             // channels [16 part, 16 part + 16) of the four accumulators, two at a time
             float y[16];
 #pragma unroll
@@ -370,6 +373,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t vmask = jlo > jhi ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
                 const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
                 const bool empty = __all_sync(0xffffffffu, vmask == 0u);
+                // dropout keep bits of this row's 32 keys (one Philox block:
+                // kbase is a multiple of 32)
+                uint32_t keep = 0xffffffffu;
+                if constexpr (kDrop) {
+                    if (!empty && qq < tl.nr) {
+                        unsigned long long wv[4];
+                        philox4x64_10((unsigned long long)(kbase / 32),
+                                      (unsigned long long)(tl.r + (long long)g.s * qq),
+                                      (unsigned long long)tl.bh, 0, g.seed, 0, wv);
+                        keep = keep_bits32(wv, g.drop_t);
+                    }
+                }
                 float kb = 0.f;   // key bias (log2 units) of this part's key `lane`
                 if constexpr (kBias) {
                     if (!empty && kbase + lane < tl.nr)
@@ -450,7 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (!((vmask >> i) & 1u)) p0 = 0.f;
                                 if (!((vmask >> (i + 1)) & 1u)) p1 = 0.f;
                             }
-                            lc2 = add2(lc2, f2(p0, p1));
+                            lc2 = add2(lc2, f2(p0, p1));   // the row sum is before dropout
+                            if constexpr (kDrop) {   // dropped: 0 (kept: scaled in the epilogue)
+                                if (!((keep >> i) & 1u)) p0 = 0.f;
+                                if (!((keep >> (i + 1)) & 1u)) p1 = 0.f;
+                            }
                             pk[e] = pack2<T>(p0, p1);
                         }
                         const int piece = (part & 1) * 4 + u;
@@ -553,24 +572,25 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
         const float m_new = fmaxf(m, sc);
         const float corr = (m == -INFINITY) ? 0.f : expf(m - m_new);
         const float pv = expf(sc - m_new);
-        l = l * corr + pv;
-        if (c < g.hd) acc = acc * corr + pv * V[j * g.hd + c];
+        l = l * corr + pv;   // the row sum is before dropout
+        if (c < g.hd) acc = acc * corr + pv * drop_factor(g, bh, i, j) * V[j * g.hd + c];
         m = m_new;
     }
     if (c < g.hd) p.O[R * g.hd + c] = acc / l;
     if (c == 0 && p.lse) p.lse[R] = m + logf(l);
 }
 
-template <typename T, bool kBias>
+template <typename T, bool kBias, bool kDrop>
 cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const AttnArgs &a,
                      cudaStream_t st) {
     const long long tiles = (long long)((a.g.nsub + kBQ - 1) / kBQ) * a.g.s * a.g.BH;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_attention_fwd<T, kBias>), kSmemBytes);
+    cudaError_t e =
+        ensure_smem(reinterpret_cast<const void *>(k_band_attention_fwd<T, kBias, kDrop>), kSmemBytes);
     if (e != cudaSuccess) return e;
-    k_band_attention_fwd<T, kBias><<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, a);
+    k_band_attention_fwd<T, kBias, kDrop><<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, a);
     return cudaGetLastError();
 }
 
@@ -585,11 +605,21 @@ cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st) {
 
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                      const TmapSet &mapV, const AttnArgs &a, cudaStream_t st) {
-    const bool bias = a.g.kbias != nullptr;
-    if (dt == kF16)
-        return bias ? launch_t<__half, true>(mapQ, mapK, mapV, a, st) : launch_t<__half, false>(mapQ, mapK, mapV, a, st);
-    return bias ? launch_t<__nv_bfloat16, true>(mapQ, mapK, mapV, a, st)
-                : launch_t<__nv_bfloat16, false>(mapQ, mapK, mapV, a, st);
+    const int v = (a.g.kbias ? 1 : 0) + (a.g.drop_t > 0 ? 2 : 0);
+    if (dt == kF16) {
+        switch (v) {
+            case 0: return launch_t<__half, false, false>(mapQ, mapK, mapV, a, st);
+            case 1: return launch_t<__half, true, false>(mapQ, mapK, mapV, a, st);
+            case 2: return launch_t<__half, false, true>(mapQ, mapK, mapV, a, st);
+            default: return launch_t<__half, true, true>(mapQ, mapK, mapV, a, st);
+        }
+    }
+    switch (v) {
+        case 0: return launch_t<__nv_bfloat16, false, false>(mapQ, mapK, mapV, a, st);
+        case 1: return launch_t<__nv_bfloat16, true, false>(mapQ, mapK, mapV, a, st);
+        case 2: return launch_t<__nv_bfloat16, false, true>(mapQ, mapK, mapV, a, st);
+        default: return launch_t<__nv_bfloat16, true, true>(mapQ, mapK, mapV, a, st);
+    }
 }
 
 }  // namespace swab

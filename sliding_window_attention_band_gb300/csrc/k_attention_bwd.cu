@@ -666,7 +666,7 @@ __device__ __forceinline__ bool decode_ktile(const Geom &g, int t, int xt, KTile
 }
 }  // namespace fused
 
-template <typename T, bool kBias>
+template <typename T, bool kBias, bool kDrop>
 __global__ void __launch_bounds__(fused::kThreads, 1)
     k_bwd_fused(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
                 const __grid_constant__ TmapSet mapV, const __grid_constant__ TmapSet mapdO,
@@ -925,6 +925,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         const int part = (warp - 2) >> 2;        // query columns [32 part, 32 part + 32)
         const int m = quarter * 32 + lane;       // TMEM lane: key of the tile / query of a dQ chunk
         const float xscale = p.scale * kLog2e;
+        const float dscale = 256.f / (256.f - (float)g.drop_t);   // kept values' scale
         const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
         const uint32_t drow = smem_u32(dst_op) + (part >> 1) * (kOpBytes / 2) + m * 128;
         const uint32_t srow = smem_u32(stage) + (part >> 1) * (kStage / 2) + m * 128;
@@ -985,6 +986,25 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                     (kk >= tl.nr || jlo > jhi) ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
                 const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
                 const bool empty = __all_sync(0xffffffffu, vmask == 0u);
+                // dropout: bit j = keep(query column j of the part, this key).
+                // Lane l draws the block of query column l for the warp's 32
+                // keys (one block: the warp's keys start on a multiple of 32)
+                // and 32 ballots transpose the bits to the key rows.
+                uint32_t keepcol = 0xffffffffu;
+                if constexpr (kDrop) {
+                    if (!empty) {
+                        unsigned long long wv[4];
+                        philox4x64_10((unsigned long long)((tl.a0 + 32 * quarter) / 32),
+                                      (unsigned long long)(tl.r + (long long)g.s * (cbase + lane)),
+                                      (unsigned long long)tl.bh, 0, g.seed, 0, wv);
+                        const uint32_t row = keep_bits32(wv, g.drop_t);
+#pragma unroll
+                        for (int l = 0; l < 32; ++l) {
+                            const uint32_t col = __ballot_sync(0xffffffffu, (row >> l) & 1u);
+                            if (l == lane) keepcol = col;
+                        }
+                    }
+                }
                 // lse (log2 units) and delta of query column `lane` of the part
                 float lq = 0.f, dq = 0.f;
                 if (!empty && cbase + lane < tl.nr) {
@@ -1047,8 +1067,22 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                             if (!((vmask >> (j + 3)) & 1u)) p3 = 0.f;
                         }
                         float s0, s1, s2, s3;
-                        f2split(mul2(f2(p0, p1), sub2(f2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), f2(dl.x, dl.y))), s0, s1);
-                        f2split(mul2(f2(p2, p3), sub2(f2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2(dl.z, dl.w))), s2, s3);
+                        if constexpr (kDrop) {
+                            // dS = p (f dP - delta), and dV takes p f
+                            const float f0 = ((keepcol >> j) & 1u) ? dscale : 0.f;
+                            const float f1 = ((keepcol >> (j + 1)) & 1u) ? dscale : 0.f;
+                            const float f2_ = ((keepcol >> (j + 2)) & 1u) ? dscale : 0.f;
+                            const float f3 = ((keepcol >> (j + 3)) & 1u) ? dscale : 0.f;
+                            f2split(mul2(f2(p0, p1), fma2(f2(f0, f1), f2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), f2(-dl.x, -dl.y))), s0, s1);
+                            f2split(mul2(f2(p2, p3), fma2(f2(f2_, f3), f2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2(-dl.z, -dl.w))), s2, s3);
+                            p0 *= f0;
+                            p1 *= f1;
+                            p2 *= f2_;
+                            p3 *= f3;
+                        } else {
+                            f2split(mul2(f2(p0, p1), sub2(f2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), f2(dl.x, dl.y))), s0, s1);
+                            f2split(mul2(f2(p2, p3), sub2(f2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2(dl.z, dl.w))), s2, s3);
+                        }
                         pk[4 * h + 2 * u] = pack2<T>(p0, p1);
                         pk[4 * h + 2 * u + 1] = pack2<T>(p2, p3);
                         dk[4 * h + 2 * u] = pack2<T>(s0, s1);
@@ -1180,13 +1214,14 @@ __global__ void __launch_bounds__(128) k_bwd_f32(const BwdArgs p, int pass) {
         const float pdot = block_dot(on ? dO[i * g.hd + c] * V[j * g.hd + c] : 0.f, part);
         const float kb = g.kbias ? g.kbias[(size_t)(bh / g.h) * g.n + (size_t)j] : 0.f;
         const float pr = expf(p.scale * sdot + kb - lse[i]);
-        const float ds = pr * (pdot - delta[i]);
+        const float f = drop_factor(g, bh, i, j);   // dropout keep-and-scale factor
+        const float ds = pr * (f * pdot - delta[i]);
         if (!on) continue;
         if (pass == 0) {
             acc_a = fmaf(ds, K[j * g.hd + c], acc_a);
         } else {
             acc_a = fmaf(ds, Q[i * g.hd + c], acc_a);   // dK
-            acc_b = fmaf(pr, dO[i * g.hd + c], acc_b);  // dV
+            acc_b = fmaf(pr * f, dO[i * g.hd + c], acc_b);  // dV
         }
     }
     if (!on) return;
@@ -1229,7 +1264,7 @@ cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, co
     return cudaGetLastError();
 }
 
-template <typename T, bool kBias>
+template <typename T, bool kBias, bool kDrop>
 cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const TmapSet &mo,
                            const TmapSet &macc, const BwdArgs &a, cudaStream_t st) {
     const long long rows = (long long)a.g.BH * a.g.n;
@@ -1241,9 +1276,9 @@ cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, kBias>), fused::kSmem);
+    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, kBias, kDrop>), fused::kSmem);
     if (e != cudaSuccess) return e;
-    k_bwd_fused<T, kBias><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, macc, a);
+    k_bwd_fused<T, kBias, kDrop><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, macc, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long groups = rows * 8;
@@ -1257,12 +1292,21 @@ cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const T
                                             const TmapSet &mv, const TmapSet &mo, const TmapSet &macc,
                                             const BwdArgs &a, cudaStream_t st) {
     if (!a.dqacc) return cudaErrorInvalidValue;
-    const bool bias = a.g.kbias != nullptr;
-    if (dt == kF16)
-        return bias ? launch_fused_t<__half, true>(mq, mk, mv, mo, macc, a, st)
-                    : launch_fused_t<__half, false>(mq, mk, mv, mo, macc, a, st);
-    return bias ? launch_fused_t<__nv_bfloat16, true>(mq, mk, mv, mo, macc, a, st)
-                : launch_fused_t<__nv_bfloat16, false>(mq, mk, mv, mo, macc, a, st);
+    const int v = (a.g.kbias ? 1 : 0) + (a.g.drop_t > 0 ? 2 : 0);
+    if (dt == kF16) {
+        switch (v) {
+            case 0: return launch_fused_t<__half, false, false>(mq, mk, mv, mo, macc, a, st);
+            case 1: return launch_fused_t<__half, true, false>(mq, mk, mv, mo, macc, a, st);
+            case 2: return launch_fused_t<__half, false, true>(mq, mk, mv, mo, macc, a, st);
+            default: return launch_fused_t<__half, true, true>(mq, mk, mv, mo, macc, a, st);
+        }
+    }
+    switch (v) {
+        case 0: return launch_fused_t<__nv_bfloat16, false, false>(mq, mk, mv, mo, macc, a, st);
+        case 1: return launch_fused_t<__nv_bfloat16, true, false>(mq, mk, mv, mo, macc, a, st);
+        case 2: return launch_fused_t<__nv_bfloat16, false, true>(mq, mk, mv, mo, macc, a, st);
+        default: return launch_fused_t<__nv_bfloat16, true, true>(mq, mk, mv, mo, macc, a, st);
+    }
 }
 
 cudaError_t launch_band_attention_bwd_tc(DType dt, const TmapSet &mq, const TmapSet &mk,

@@ -5,6 +5,8 @@
 // cudaGetDriverEntryPointByVersion, so it loads on a machine without a GPU.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -64,6 +66,9 @@ swab_status check_desc(const swab_desc *d, Geom *g, DType *dt) {
         if (reinterpret_cast<uintptr_t>(d->key_bias) % 4 != 0) return SWAB_ERR_MISALIGNED;
         if (d->n_global > 0) return SWAB_ERR_UNSUPPORTED;  // key bias with global tokens
     }
+    if (!(d->dropout_p >= 0.f && d->dropout_p < 1.f)) return SWAB_ERR_INVALID_ARG;  // NaN too
+    const int drop_t = (int)std::min(255.f, std::nearbyint(d->dropout_p * 256.f));
+    if (drop_t > 0 && d->n_global > 0) return SWAB_ERR_UNSUPPORTED;  // dropout with globals
     const long long BH = (long long)d->b * d->h;
     const long long D = (long long)d->w + d->w_upper + 1;
     if (BH > 65535) return SWAB_ERR_UNSUPPORTED;          // grid z
@@ -85,6 +90,8 @@ swab_status check_desc(const swab_desc *d, Geom *g, DType *dt) {
     g->padding = d->padding;
     g->h = d->h;
     g->kbias = d->key_bias;
+    g->drop_t = drop_t;
+    g->seed = d->dropout_seed;
     *dt = static_cast<DType>(d->dtype);
     return SWAB_OK;
 }
@@ -346,6 +353,7 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
+    if (g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;  // dropout lives in the fused kernels
     GlobArgs gl;
     if ((s = check_globals(desc, {Sg, Pg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({S, P})) != SWAB_OK) return s;
@@ -494,6 +502,7 @@ SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float sca
     if ((s = check_no_globals(desc)) != SWAB_OK) return s;
     if ((long long)g.BH * g.n > (long long)SWAB_NOALLOC_MAX_ROWS) return SWAB_ERR_UNSUPPORTED;
     if (desc->key_bias) return SWAB_ERR_UNSUPPORTED;  // the two-kernel path has no key bias
+    if (g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;    // nor dropout
     if ((s = check_ptrs({Q, K, V, O, dO, lse, dQ, dK, dV})) != SWAB_OK) return s;
     float *scratch = nullptr;
     if (noalloc_delta_scratch(&scratch) != cudaSuccess) return SWAB_ERR_CUDA;

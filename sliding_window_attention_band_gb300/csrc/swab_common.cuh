@@ -41,6 +41,8 @@ struct Geom {
     float padding;
     int h;                // heads: slice bh belongs to batch bh / h
     const float *kbias;   // [b, n] key-padding bias added to scaled scores, or null
+    int drop_t;           // dropout threshold byte (0 = no dropout)
+    unsigned long long seed;  // dropout key
 };
 
 __host__ __device__ __forceinline__ int residue_len(int n, int s, int r) {
@@ -405,6 +407,63 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
     float r;
     asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC'11): ten rounds of two 64x64->128 products with the
+// published multipliers, the key bumped by the published Weyl constants
+// between rounds.  The dropout keep byte of element (slice bh, query i, key j)
+// is byte (b mod 32), b = floor(j / s), of the block at counter
+// (floor(b / 32), i, bh, 0) and key (seed, 0), bytes little-endian from the
+// four words.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void philox4x64_10(unsigned long long c0, unsigned long long c1,
+                                              unsigned long long c2, unsigned long long c3,
+                                              unsigned long long k0, unsigned long long k1,
+                                              unsigned long long (&out)[4]) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B97F4A7C15ull;
+            k1 += 0xBB67AE8584CAA73Bull;
+        }
+        const unsigned long long hi0 = __umul64hi(0xD2E7470EE14C6C93ull, c0), lo0 = 0xD2E7470EE14C6C93ull * c0;
+        const unsigned long long hi1 = __umul64hi(0xCA5A826395121157ull, c2), lo1 = 0xCA5A826395121157ull * c2;
+        const unsigned long long n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+// 32 keep bits of a block: bit k = (byte k >= t), bytes little-endian.
+__device__ __forceinline__ uint32_t keep_bits32(const unsigned long long (&w)[4], int t) {
+    const uint32_t t4 = 0x01010101u * (uint32_t)t;
+    uint32_t bits = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t word = (uint32_t)(w[k >> 1] >> (32 * (k & 1)));
+        const uint32_t ge = __vcmpgeu4(word, t4) & 0x01010101u;   // 1 per byte >= t
+        bits |= ((ge * 0x01020408u) >> 24 & 0xFu) << (4 * k);      // bytes 4k..4k+3 -> bits
+    }
+    return bits;
+}
+
+// keep-and-scale factor of one element (the exact fp32 paths)
+__device__ __forceinline__ float drop_factor(const Geom &g, long long bh, long long i, long long j) {
+    if (g.drop_t <= 0) return 1.f;
+    const unsigned long long b = (unsigned long long)(j / g.s);
+    unsigned long long w[4];
+    philox4x64_10(b / 32, (unsigned long long)i, (unsigned long long)bh, 0, g.seed, 0, w);
+    const int k = (int)(b % 32);
+    const int byte = (int)((w[k >> 3] >> (8 * (k & 7))) & 0xffu);
+    return byte >= g.drop_t ? 256.f / (256.f - (float)g.drop_t) : 0.f;
 }
 
 // fp32 add of 4 values into global memory (one vector reduction, sm_90+)

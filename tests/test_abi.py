@@ -233,3 +233,20 @@ def test_binding_key_bias_shape():
         B.Desc(2, 3, 64, 64, 4, 4, key_bias=torch.zeros(3, 64))
     with pytest.raises(ValueError):
         B.Desc(2, 3, 64, 64, 4, 4, key_bias=torch.zeros(2, 64, dtype=torch.float16))
+
+
+def test_dropout_validation(lib):
+    """dropout_p must lie in [0, 1); band_softmax, global tokens and the
+    allocation-free backward do not take dropout."""
+    P = ctypes.c_void_p
+    for bad in (-0.1, 1.0, float("nan")):
+        d = desc()
+        d.c.dropout_p = bad
+        assert call(lib, "band_attention", d, FAKE, FAKE, FAKE, FAKE) == INVALID
+    d = desc(dropout_p=0.1)
+    assert call(lib, "band_softmax", d, FAKE, FAKE) == UNSUPPORTED
+    assert lib.band_attention_bwd_noalloc(ctypes.byref(d.c), 0.125, *(P(FAKE) for _ in range(9)),
+                                          None) == UNSUPPORTED
+    dg = desc(n=512, global_idx=[0, 5], dropout_p=0.1)
+    assert call(lib, "band_qk", dg, FAKE, FAKE, FAKE) == UNSUPPORTED
+    assert desc(dropout_p=0.1).drop_t == 26 and desc(dropout_p=0.999).drop_t == 255
