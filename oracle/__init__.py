@@ -49,11 +49,12 @@ def _load():
         p = ctypes.c_void_p
         _lib.orc_num_threads.restype = i
         _lib.orc_band_qk.argtypes = [i, i, i, i, i, i, d, d, p, p, p, i, p, p, p]
-        _lib.orc_band_softmax.argtypes = [i, i, i, i, i, p, p, p, i, p, p, p, p, p, p]
+        u64 = ctypes.c_uint64
+        _lib.orc_band_softmax.argtypes = [i, i, i, i, i, p, p, p, i, p, p, p, p, p, p, u64, i, p]
         _lib.orc_band_pv.argtypes = [i, i, i, i, i, i, d, p, p, p, i, p, p, p]
         _lib.orc_band_t.argtypes = [i, i, i, i, i, i, d, p, p, p, i, p, p, p]
-        _lib.orc_band_softmax_bwd.argtypes = [i, i, i, i, i, p, p, p, i, p, p, p, p, p, p, p]
-        u64 = ctypes.c_uint64
+        _lib.orc_band_softmax_bwd.argtypes = [i, i, i, i, i, p, p, p, i, p, p, p, p, p, p, p, u64,
+                                              i]
         _lib.orc_attention_fwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, i, p, p, u64, i]
         _lib.orc_attention_bwd.argtypes = [i, i, i, i, i, i, d, p, p, p, p, p, p, p, i, p, p,
                                            u64, i]
@@ -116,22 +117,28 @@ def _kbias(key_bias, BH, n):
     return kb
 
 
-def band_softmax(S, w, w_upper, dilation=0, global_idx=None, Sg=None, Sr=None, key_bias=None):
+def band_softmax(S, w, w_upper, dilation=0, global_idx=None, Sg=None, Sr=None, key_bias=None,
+                 drop_t=0, seed=0):
     """Masked row softmax (key_bias[bh, j] added to the score of key j).  Returns
-    (P, lse) or (P, lse, Pg, Pr) with globals."""
+    (P, lse) or (P, lse, Pg, Pr) with globals; with dropout (threshold byte
+    drop_t > 0) (P, lse, Pd), Pd the dropped and rescaled probabilities."""
     S = _f64(S)
     BH, n, D = S.shape
     kb = _kbias(key_bias, BH, n)
     G, g = _gidx(global_idx)
     P = np.empty_like(S)
+    Pd = np.empty_like(S) if drop_t else None
     lse = np.empty((BH, n))
     Pg = np.empty((BH, n, G)) if G else None
     Pr = np.empty((BH, G, n)) if G else None
     Sg = _f64(Sg) if G else None
     Sr = _f64(Sr) if G else None
     _check(_load().orc_band_softmax(BH, n, w, w_upper, dilation, _ptr(S), _ptr(P), _ptr(lse),
-                                    G, _ptr(g), _ptr(Sg), _ptr(Sr), _ptr(Pg), _ptr(Pr), _ptr(kb)),
+                                    G, _ptr(g), _ptr(Sg), _ptr(Sr), _ptr(Pg), _ptr(Pr), _ptr(kb),
+                                    seed, drop_t, _ptr(Pd)),
            "band_softmax")
+    if drop_t:
+        return P, lse, Pd
     return (P, lse, Pg, Pr) if G else (P, lse)
 
 
@@ -162,8 +169,10 @@ def band_t(Bd, Y, w, w_upper, dilation=0, alpha=1.0, global_idx=None, Bg=None, B
 
 
 def band_softmax_bwd(P, dP, w, w_upper, dilation=0, global_idx=None, Pg=None, dPg=None,
-                     Pr=None, dPr=None):
-    """dS = P * (dP - rowsum(P * dP)).  Returns dS or (dS, dSg, dSr)."""
+                     Pr=None, dPr=None, drop_t=0, seed=0):
+    """dS = P * (f dP - rowsum(P * f dP)), f the dropout keep-and-scale factor
+    (1 without dropout; dP is then the gradient of the dropped probabilities).
+    Returns dS or (dS, dSg, dSr)."""
     P, dP = _f64(P), _f64(dP)
     BH, n, D = P.shape
     G, g = _gidx(global_idx)
@@ -176,7 +185,8 @@ def band_softmax_bwd(P, dP, w, w_upper, dilation=0, global_idx=None, Pg=None, dP
         dSg = dSr = None
     _check(_load().orc_band_softmax_bwd(BH, n, w, w_upper, dilation, _ptr(P), _ptr(dP),
                                         _ptr(dS), G, _ptr(g), _ptr(Pg), _ptr(dPg), _ptr(dSg),
-                                        _ptr(Pr), _ptr(dPr), _ptr(dSr)), "band_softmax_bwd")
+                                        _ptr(Pr), _ptr(dPr), _ptr(dSr), seed, drop_t),
+           "band_softmax_bwd")
     return (dS, dSg, dSr) if G else dS
 
 

@@ -161,12 +161,15 @@ int orc_band_qk(int BH, int n, int hd, int w, int wu, int dil, double alpha,
  *                 P[i,:] = 0, Pg[i,:] = 0
  *   lse[i] = m + log Z.
  * --------------------------------------------------------------------- */
+static double drop_factor(uint64_t seed, int drop_t, int bh, int i, int j, int s);
+
 int orc_band_softmax(int BH, int n, int w, int wu, int dil, const double *S,
                      double *P, double *lse, int G, const int *gidx,
                      const double *Sg, const double *Sr, double *Pg, double *Pr,
-                     const double *kbias) {
+                     const double *kbias, uint64_t seed, int drop_t, double *Pd) {
     if (check_geom(BH, n, 1, w, wu, dil)) return -1;
     if (G > 0 && kbias) return -4;  /* key bias with global tokens: not defined here */
+    if (drop_t < 0 || drop_t > 255 || (drop_t > 0 && (G > 0 || !Pd))) return -4;
     const int D = w + wu + 1, s = dil + 1;
     unsigned char *gm; int *gp;
     int rc = build_gmask(n, G, gidx, &gm, &gp);
@@ -209,6 +212,14 @@ int orc_band_softmax(int BH, int n, int w, int wu, int dil, const double *S,
             for (int q = 0; q < G; ++q) z += exp(Sg[((size_t)bh * n + i) * G + q] - m);
             for (int t = 0; t < D; ++t)
                 prow[t] = slot_used(i, t, w, s, n, gmask) ? exp(srow[t] - m) / z : 0.0;
+            /* dropped probabilities: the keep-and-scale factor of the slot's key */
+            if (Pd) {
+                double *drow = Pd + ((size_t)bh * n + i) * D;
+                for (int t = 0; t < D; ++t)
+                    drow[t] = slot_used(i, t, w, s, n, gmask)
+                                  ? drop_factor(seed, drop_t, bh, i, i + (t - w) * s, s) * prow[t]
+                                  : 0.0;
+            }
             for (int q = 0; q < G; ++q) {
                 size_t k = ((size_t)bh * n + i) * G + q;
                 Pg[k] = exp(Sg[k] - m) / z;
@@ -329,8 +340,10 @@ int orc_band_t(int BH, int n, int hd, int w, int wu, int dil, double alpha,
 int orc_band_softmax_bwd(int BH, int n, int w, int wu, int dil, const double *P,
                          const double *dP, double *dS, int G, const int *gidx,
                          const double *Pg, const double *dPg, double *dSg,
-                         const double *Pr, const double *dPr, double *dSr) {
+                         const double *Pr, const double *dPr, double *dSr,
+                         uint64_t seed, int drop_t) {
     if (check_geom(BH, n, 1, w, wu, dil)) return -1;
+    if (drop_t < 0 || drop_t > 255 || (drop_t > 0 && G > 0)) return -4;
     const int D = w + wu + 1, s = dil + 1;
     unsigned char *gm; int *gp;
     int rc = build_gmask(n, G, gidx, &gm, &gp);
@@ -349,13 +362,19 @@ int orc_band_softmax_bwd(int BH, int n, int w, int wu, int dil, const double *P,
                 for (int q = 0; q < G; ++q) dSg[r * G + q] = 0.0;
                 continue;
             }
+            /* with dropout the forward's output is f*P and dP is its gradient:
+             * the gradient reaching P is f*dP (f the slot key's keep-and-scale
+             * factor, 1 without dropout) */
             double delta = 0.0;
             for (int t = 0; t < D; ++t)
-                if (slot_used(i, t, w, s, n, gmask)) delta += P[r * D + t] * dP[r * D + t];
+                if (slot_used(i, t, w, s, n, gmask))
+                    delta += P[r * D + t] * drop_factor(seed, drop_t, bh, i, i + (t - w) * s, s) *
+                             dP[r * D + t];
             for (int q = 0; q < G; ++q) delta += Pg[r * G + q] * dPg[r * G + q];
             for (int t = 0; t < D; ++t)
                 dS[r * D + t] = slot_used(i, t, w, s, n, gmask)
-                                    ? P[r * D + t] * (dP[r * D + t] - delta)
+                                    ? P[r * D + t] * (drop_factor(seed, drop_t, bh, i, i + (t - w) * s, s) *
+                                                      dP[r * D + t] - delta)
                                     : 0.0;
             for (int q = 0; q < G; ++q)
                 dSg[r * G + q] = Pg[r * G + q] * (dPg[r * G + q] - delta);

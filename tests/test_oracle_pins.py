@@ -525,6 +525,19 @@ def test_dropout_attention_vs_torch(n, hd, w, wu, d, t):
     got = oracle.attention_bwd(Q, K, V, dO, w, wu, d, scale, drop_t=t, seed=seed)
     for g, r in zip(got, t_in):
         np.testing.assert_allclose(g, r.grad.numpy(), rtol=1e-9, atol=1e-11)
+    # the materialised chain: band_softmax writes P and the dropped Pd, P.V
+    # uses Pd, and band_softmax_bwd takes P with the gradient of Pd
+    S = oracle.band_qk(Q, K, w, wu, d, alpha=scale, padding=-3.0)
+    P, lse2, Pd = oracle.band_softmax(S, w, wu, d, drop_t=t, seed=seed)
+    np.testing.assert_allclose(oracle.band_pv(Pd, V, w, wu, d), O_t.detach().numpy(),
+                               rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-13, atol=1e-13)
+    dPd = oracle.band_qk(dO, V, w, wu, d)
+    dS = oracle.band_softmax_bwd(P, dPd, w, wu, d, drop_t=t, seed=seed)
+    chain = (oracle.band_pv(dS, K, w, wu, d, alpha=scale), oracle.band_t(dS, Q, w, wu, d, scale),
+             oracle.band_t(Pd, dO, w, wu, d))
+    for g, r in zip(chain, t_in):
+        np.testing.assert_allclose(g, r.grad.numpy(), rtol=1e-9, atol=1e-11)
     # threshold 0 is no dropout
     O0, _ = oracle.attention_fwd(Q, K, V, w, wu, d, scale, drop_t=0, seed=seed)
     O1, _ = oracle.attention_fwd(Q, K, V, w, wu, d, scale)
@@ -543,8 +556,13 @@ MUTANTS = {
     "pv_alpha_dropped": ("for (int c = 0; c < hd; ++c) o[c] *= alpha;", ""),
     "t_operand": ("x[(size_t)j * hd + c] += alpha * b[t] * yi;",
                   "x[(size_t)j * hd + c] += alpha * b[t] * y[(size_t)j * hd + c];"),
-    "softmax_bwd_sign": ("? P[r * D + t] * (dP[r * D + t] - delta)",
-                         "? P[r * D + t] * (dP[r * D + t] + delta)"),
+    "softmax_bwd_sign": ("dP[r * D + t] - delta)", "dP[r * D + t] + delta)"),
+    "softmax_bwd_dropout_delta": (
+        """delta += P[r * D + t] * drop_factor(seed, drop_t, bh, i, i + (t - w) * s, s) *
+                             dP[r * D + t];""", "delta += P[r * D + t] * dP[r * D + t];"),
+    "softmax_dropped_unscaled": ("? drop_factor(seed, drop_t, bh, i, i + (t - w) * s, s) * prow[t]",
+                                 "? (drop_factor(seed, drop_t, bh, i, i + (t - w) * s, s) > 0) *"
+                                 " prow[t]"),
     "bwd_dk_scale": ("+= scale * sbuf[(size_t)bh * nnz + u] * qi;",
                      "+= sbuf[(size_t)bh * nnz + u] * qi;"),
     "global_cols_dropped_from_sum": (
@@ -599,7 +617,7 @@ def test_planted_mistake_fails_pins(name):
             mut = ctypes.CDLL(so)
             for fname in ("orc_num_threads", "orc_band_qk", "orc_band_softmax", "orc_band_pv",
                           "orc_band_t", "orc_band_softmax_bwd", "orc_attention_fwd",
-                          "orc_attention_bwd"):
+                          "orc_attention_bwd", "orc_philox4x64", "orc_dropout_factor"):
                 src_f, dst_f = getattr(oracle._lib, fname), getattr(mut, fname)
                 dst_f.argtypes, dst_f.restype = src_f.argtypes, src_f.restype
             oracle._lib = mut
