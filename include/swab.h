@@ -110,9 +110,11 @@ typedef struct swab_desc {
      * (slice bh, query i, key j) is kept iff byte (b mod 32), b = floor(j / s),
      * of the Philox4x64-10 block at counter (floor(b / 32), i, bh, 0) and key
      * (dropout_seed, 0) -- bytes little-endian from the four output words --
-     * is >= t.  lse is that of the probabilities before dropout.  With t > 0,
-     * band_softmax, global tokens and band_attention_bwd_noalloc return
-     * SWAB_ERR_UNSUPPORTED; the other calls do not depend on it. */
+     * is >= t.  lse is that of the probabilities before dropout.  Read by
+     * band_softmax_dropout, band_softmax_bwd, band_attention and
+     * band_attention_bwd; with t > 0, band_softmax (use band_softmax_dropout),
+     * global tokens and band_attention_bwd_noalloc return SWAB_ERR_UNSUPPORTED;
+     * the other calls do not depend on it. */
     float dropout_p;
     uint64_t dropout_seed;
 } swab_desc;
@@ -145,6 +147,22 @@ SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, 
 SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const swab_glob *Sg,
                                   void *P, const swab_glob *Pg, float *lse, void *stream);
 
+/* Masked row softmax followed by dropout (nvFuser issue "HuggingFace
+ * BertForMaskedLM - Log Softmax Fusion...", fusion 1, whose outputs include
+ * both the probabilities and the dropped, rescaled probabilities):
+ *   P[i,t]  as band_softmax (before dropout; P may be NULL if not needed);
+ *   Pd[i,t] = f(i,t) * P[i,t], f = 256/(256-t) or 0 the keep-and-scale factor
+ *             of the slot's key under the descriptor's dropout (f = 1 when
+ *             dropout_p rounds to 0); 0 on unused slots;
+ *   lse[i]  as band_softmax (before dropout; may be NULL).
+ * The forward product is then O = band_pv(Pd, V); for the backward,
+ * band_softmax_bwd with the same descriptor takes P and the gradient of Pd.
+ * The keep decisions are recomputed from the descriptor, never stored.
+ * No global tokens (SWAB_ERR_UNSUPPORTED); D <= 65536 (else
+ * SWAB_ERR_UNSUPPORTED). */
+SWAB_API swab_status band_softmax_dropout(const swab_desc *desc, const void *S, void *P, void *Pd,
+                                          float *lse, void *stream);
+
 /* Band x dense product (TVM thread, post 6: transpose_t1 = 0, t1d3 = 2w+1):
  *   O[i,c] = alpha * sum over used slots t of P[i,t] * V[j(i,t), c]
  *            (+ alpha * sum_g Pg->cols[i,g] * V[G[g],c]);
@@ -167,7 +185,11 @@ SWAB_API swab_status band_pv_bwd_t(const swab_desc *desc, float alpha, const voi
 /* Softmax backward on the band (derivative of band_softmax):
  *   dS[i,t] = P[i,t] * (dP[i,t] - delta_i) on used slots, 0 elsewhere,
  *   delta_i = sum over used slots of P*dP (+ sum_g Pg*dPg);
- * global pieces likewise (dSg->cols, dSg->rows). */
+ * global pieces likewise (dSg->cols, dSg->rows).  With the descriptor's
+ * dropout (derivative of band_softmax_dropout's Pd): P is the probabilities
+ * before dropout, dP the gradient of Pd, and
+ *   dS[i,t] = P[i,t] * (f(i,t) dP[i,t] - delta_i), delta_i = sum P*f*dP
+ * (D <= 65536, else SWAB_ERR_UNSUPPORTED). */
 SWAB_API swab_status band_softmax_bwd(const swab_desc *desc, const void *P, const swab_glob *Pg,
                                       const void *dP, const swab_glob *dPg, void *dS,
                                       const swab_glob *dSg, void *stream);

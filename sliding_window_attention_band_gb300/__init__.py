@@ -9,11 +9,13 @@ from ._binding import (API_FUNCTIONS, Desc, SwabError, band_attention,  # noqa: 
                        band_attention_bwd, band_attention_bwd_noalloc,
                        band_attention_bwd_workspace, band_pv,
                        band_pv_bwd_t, band_qk, band_qk_bwd_t, band_softmax, band_softmax_bwd,
+                       band_softmax_dropout,
                        device_status, library_path, load, selftest_wait_timeout,
                        status_string, version)
 from .inputs import WORKLOADS, Workload, seeded_qkvo, workload_inputs  # noqa: F401
 
-__all__ = ["Desc", "SwabError", "band_qk", "band_softmax", "band_pv", "band_qk_bwd_t",
+__all__ = ["Desc", "SwabError", "band_qk", "band_softmax", "band_softmax_dropout", "band_pv",
+           "band_qk_bwd_t",
            "band_pv_bwd_t", "band_softmax_bwd", "band_attention", "band_attention_bwd",
            "band_attention_bwd_noalloc",
            "band_attention_bwd_workspace", "device_status", "selftest_wait_timeout", "load",

@@ -24,7 +24,7 @@ MAX_DILATION = 15
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # every symbol the header declares
-API_FUNCTIONS = ("band_qk", "band_softmax", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
+API_FUNCTIONS = ("band_qk", "band_softmax", "band_softmax_dropout", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
                  "band_softmax_bwd", "band_attention", "band_attention_bwd",
                  "band_attention_bwd_workspace", "band_attention_bwd_noalloc",
                  "swab_status_string", "swab_device_status",
@@ -130,6 +130,7 @@ def load():
             sigs = {
                 "band_qk": [D, f, P, P, P, Gp, P],
                 "band_softmax": [D, P, Gp, P, Gp, P, P],
+                "band_softmax_dropout": [D, P, P, P, P, P],
                 "band_pv": [D, f, P, Gp, P, P, P],
                 "band_qk_bwd_t": [D, f, P, Gp, P, P, P],
                 "band_pv_bwd_t": [D, f, P, Gp, P, P, P],
@@ -247,6 +248,17 @@ def band_softmax(desc: Desc, S, P, lse=None, Sg=None, Pg=None, stream=None):
     _call("band_softmax", ctypes.byref(desc.c), _ptr(S), _glob(Sg, desc, "Sg"), _ptr(P),
           _glob(Pg, desc, "Pg"),
           _ptr(lse), _stream(stream, P))
+
+
+def band_softmax_dropout(desc: Desc, S, Pd, P=None, lse=None, stream=None):
+    """Pd = dropout of the masked row softmax of S (the descriptor's dropout);
+    P (optional) = the probabilities before dropout; lse (optional)."""
+    _check_shape("S", S, _band(desc), desc.dtype)
+    _check_shape("Pd", Pd, _band(desc), desc.dtype)
+    _check_shape("P", P, _band(desc), desc.dtype)
+    _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
+    _call("band_softmax_dropout", ctypes.byref(desc.c), _ptr(S), _ptr(P), _ptr(Pd), _ptr(lse),
+          _stream(stream, Pd))
 
 
 def band_pv(desc: Desc, alpha, P, V, O, Pg=None, stream=None):

@@ -8,6 +8,12 @@
 // with the valid range in closed form: t_lo = max(0, w - floor(i/s)),
 // t_hi = min(D-1, w + floor((n-1-i)/s)).
 // Backward:  dS = P * (dP - delta_i), delta_i = sum over valid slots P*dP.
+// Dropout (nvFuser issue, fusion 1: the kept probabilities scaled by
+// 1/(1-p)): the forward also writes Pd = f * P, f the keep-and-scale factor of
+// the slot's key, and the backward, given P and the gradient dP of Pd, forms
+// dS = P * (f dP - delta_i), delta_i = sum P*f*dP.  A row's keep bits come
+// from one Philox4x64-10 block per 32 keys of its residue (the lanes draw the
+// blocks, one word of 32 bits each, into shared memory).
 //
 // One warp per band row.  A row of D elements starts at an arbitrary element
 // boundary, so the warp walks the row's aligned 16-byte pieces (128-bit
@@ -128,10 +134,71 @@ __device__ __forceinline__ void add_key_bias(float (&x)[N], int x0, const Row &r
     }
 }
 
+// Dropout keep bits of one row: element x (piece coordinates) of the row has
+// key sub-index b = x + a - w - lead (a = floor(i/s)); bit (b - 32 kb0) of the
+// word table holds its keep decision.
+struct Keep {
+    const uint32_t *words;
+    int off;   // x + off = b - 32 kb0
+    float scale;
+};
+
+// Words per row the table needs: the valid keys span at most D, so at most
+// (D - 1) / 32 + 2 blocks.
+__host__ __device__ __forceinline__ int keep_words(int D) { return (D - 1) / 32 + 2; }
+
+// Draws row R's keep bits into this warp's table (all lanes take part).
+__device__ __forceinline__ Keep make_keep(const Geom &g, int R, const Row &rw, uint32_t *words,
+                                          int lane) {
+    const int i = R % g.n, bh = R / g.n, a = i / g.s;
+    const int b_lo = a - g.w + (rw.xlo - rw.lead), b_hi = a - g.w + (rw.xhi - rw.lead);
+    const int kb0 = b_lo >> 5, nkb = (b_hi >> 5) - kb0 + 1;
+    for (int k = lane; k < nkb; k += 32) {
+        unsigned long long wv[4];
+        philox4x64_10((unsigned long long)(kb0 + k), (unsigned long long)i, (unsigned long long)bh,
+                      0, g.seed, 0, wv);
+        words[k] = keep_bits32(wv, g.drop_t);
+    }
+    __syncwarp();
+    Keep kp;
+    kp.words = words;
+    kp.off = a - g.w - rw.lead - 32 * kb0;
+    kp.scale = 256.f / (256.f - (float)g.drop_t);
+    return kp;
+}
+
+// Keep-and-scale factor of valid element x.
+__device__ __forceinline__ float keep_factor(const Keep &kp, int x) {
+    const int b = x + kp.off;
+    return ((kp.words[b >> 5] >> (b & 31)) & 1u) ? kp.scale : 0.f;
+}
+
+// dP -> f * dP on the valid elements of a piece (the gradient reaching P
+// through the dropout).
+template <int N>
+__device__ __forceinline__ void apply_keep(float (&y)[N], int x0, const Row &rw, const Keep &kp) {
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+        if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) y[u] *= keep_factor(kp, x0 + u);
+}
+
+// Stores f * y for a piece of probabilities (0 on invalid slots).
+template <typename T>
+__device__ __forceinline__ void store_dropped(uint4 *out, int pc, const Row &rw, const Keep &kp,
+                                              const float (&y)[Vec<T>::N]) {
+    constexpr int N = Vec<T>::N;
+    const int x0 = pc * N;
+    float yd[N];
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+        yd[u] = (x0 + u >= rw.xlo && x0 + u <= rw.xhi) ? y[u] * keep_factor(kp, x0 + u) : 0.f;
+    store_piece<T>(out, pc, rw, yd);
+}
+
 // ---------------------------------------------------------------------------
 // register-resident rows
 // ---------------------------------------------------------------------------
-template <typename T, int NCH>
+template <typename T, int NCH, bool kDrop>
 __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const SoftmaxArgs p) {
     constexpr int N = Vec<T>::N;
     constexpr bool kKeep = NCH * N <= 32;  // keep exp() values in registers
@@ -149,6 +216,11 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
         const int pc = lane + 32 * k;
         raw[k] = pc < rw.npieces ? ldg16(src + pc) : make_uint4(0, 0, 0, 0);
     }
+    // the keep bits are drawn while the row's loads are in flight
+    extern __shared__ uint32_t keep_smem[];
+    Keep kp{};
+    if constexpr (kDrop)
+        kp = make_keep(g, R, rw, keep_smem + (threadIdx.x >> 5) * keep_words(g.D), lane);
     float m = -INFINITY;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
@@ -189,6 +261,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     const float inv = 1.f / z;
     uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
+    uint4 *dstd = reinterpret_cast<uint4 *>(p.Pd) + rw.piece0;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
         const int pc = lane + 32 * k;
@@ -209,12 +282,17 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
                 y[u] = v ? ex2(fmaf(x[u], kLog2e, -mb)) * inv : 0.f;
             }
         }
-        store_piece<T>(dst, pc, rw, y);
+        if constexpr (kDrop) {
+            if (p.P) store_piece<T>(dst, pc, rw, y);
+            store_dropped<T>(dstd, pc, rw, kp, y);
+        } else {
+            store_piece<T>(dst, pc, rw, y);
+        }
     }
     if (p.lse && lane == 0) p.lse[R] = m + logf(z);
 }
 
-template <typename T, int NCH>
+template <typename T, int NCH, bool kDrop>
 __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const SoftmaxArgs p) {
     constexpr int N = Vec<T>::N;
     const Geom &g = p.g;
@@ -232,6 +310,11 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const So
         rp[k] = in ? ldg16(sp + pc) : make_uint4(0, 0, 0, 0);
         rd[k] = in ? ldg16(sd + pc) : make_uint4(0, 0, 0, 0);
     }
+    // the keep bits are drawn while the row's loads are in flight
+    extern __shared__ uint32_t keep_smem[];
+    Keep kp{};
+    if constexpr (kDrop)
+        kp = make_keep(g, R, rw, keep_smem + (threadIdx.x >> 5) * keep_words(g.D), lane);
     float delta = 0.f;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
@@ -239,6 +322,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const So
         float x[N], y[N];
         unpack<T>(rp[k], x);
         unpack<T>(rd[k], y);
+        if constexpr (kDrop) apply_keep<N>(y, x0, rw, kp);
         if (all_valid(x0, N, rw)) {
 #pragma unroll
             for (int u = 0; u < N; ++u) delta = fmaf(x[u], y[u], delta);
@@ -259,6 +343,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const So
         float x[N], y[N];
         unpack<T>(rp[k], x);
         unpack<T>(rd[k], y);
+        if constexpr (kDrop) apply_keep<N>(y, x0, rw, kp);
         const bool full = all_valid(x0, N, rw);
 #pragma unroll
         for (int u = 0; u < N; ++u) {
@@ -282,6 +367,10 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
     const Row rw = make_row<T>(g, R);
     const float *brow = bias_row(g, R);
     const int qi = R % g.n;
+    const bool drop = p.Pd != nullptr;
+    extern __shared__ uint32_t keep_smem[];
+    Keep kp{};
+    if (drop) kp = make_keep(g, R, rw, keep_smem + (threadIdx.x >> 5) * keep_words(g.D), lane);
     const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
     // pass 1: per-lane running max (log2 units) and sum, one rescale per piece
     float m = -INFINITY, z = 0.f;
@@ -314,6 +403,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
     }
     const float inv = 1.f / z;
     uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
+    uint4 *dstd = reinterpret_cast<uint4 *>(p.Pd) + rw.piece0;
     for (int pc = lane; pc < rw.npieces; pc += 32) {
         float x[N];
         unpack<T>(ldg16(src + pc), x);
@@ -324,7 +414,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
             const bool v = x0 + u >= rw.xlo && x0 + u <= rw.xhi;
             x[u] = v ? ex2(fmaf(x[u], kLog2e, -m)) * inv : 0.f;
         }
-        store_piece<T>(dst, pc, rw, x);
+        if (p.P) store_piece<T>(dst, pc, rw, x);
+        if (drop) store_dropped<T>(dstd, pc, rw, kp, x);
     }
     if (p.lse && lane == 0) p.lse[R] = m / kLog2e + logf(z);
 }
@@ -337,6 +428,10 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const
     const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
     if (R >= g.BH * g.n) return;
     const Row rw = make_row<T>(g, R);
+    const bool drop = g.drop_t > 0;
+    extern __shared__ uint32_t keep_smem[];
+    Keep kp{};
+    if (drop) kp = make_keep(g, R, rw, keep_smem + (threadIdx.x >> 5) * keep_words(g.D), lane);
     const uint4 *sp = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
     const uint4 *sd = reinterpret_cast<const uint4 *>(p.S2) + rw.piece0;
     float delta = 0.f;
@@ -345,6 +440,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const
         unpack<T>(ldg16(sp + pc), x);
         unpack<T>(ldg16(sd + pc), y);
         const int x0 = pc * N;
+        if (drop) apply_keep<N>(y, x0, rw, kp);
 #pragma unroll
         for (int u = 0; u < N; ++u)
             if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) delta = fmaf(x[u], y[u], delta);
@@ -357,6 +453,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const
         unpack<T>(ldg16(sp + pc), x);
         unpack<T>(ldg16(sd + pc), y);
         const int x0 = pc * N;
+        if (drop) apply_keep<N>(y, x0, rw, kp);
 #pragma unroll
         for (int u = 0; u < N; ++u) {
             const bool v = x0 + u >= rw.xlo && x0 + u <= rw.xhi;
@@ -366,31 +463,39 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const
     }
 }
 
-template <typename T>
-cudaError_t launch_sm(const SoftmaxArgs &a, bool bwd, cudaStream_t st) {
+template <typename T, bool kDrop>
+cudaError_t launch_sm_v(const SoftmaxArgs &a, bool bwd, cudaStream_t st) {
     constexpr int N = Vec<T>::N;
     const long long rows = (long long)a.g.BH * a.g.n;
-    const unsigned blocks = (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+    const dim3 grd((unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock));
     const dim3 blk(kRowsPerBlock * 32);
     const long long pieces = (a.g.D + N - 1) / N + 1;  // most pieces a row touches
     const long long per_lane = (pieces + 31) / 32;
+    // dropout: each warp's keep-bit table for its row
+    const size_t smem = kDrop ? (size_t)kRowsPerBlock * keep_words(a.g.D) * sizeof(uint32_t) : 0;
     if (bwd) {
-        if (per_lane <= 1) k_softmax_bwd_reg<T, 1><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 2) k_softmax_bwd_reg<T, 2><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 3) k_softmax_bwd_reg<T, 3><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 4) k_softmax_bwd_reg<T, 4><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 8) k_softmax_bwd_reg<T, 8><<<blocks, blk, 0, st>>>(a);
-        else k_softmax_bwd_stream<T><<<blocks, blk, 0, st>>>(a);
+        if (per_lane <= 1) k_softmax_bwd_reg<T, 1, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 2) k_softmax_bwd_reg<T, 2, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 3) k_softmax_bwd_reg<T, 3, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 4) k_softmax_bwd_reg<T, 4, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 8) k_softmax_bwd_reg<T, 8, kDrop><<<grd, blk, smem, st>>>(a);
+        else k_softmax_bwd_stream<T><<<grd, blk, smem, st>>>(a);
     } else {
-        if (per_lane <= 1) k_softmax_reg<T, 1><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 2) k_softmax_reg<T, 2><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 3) k_softmax_reg<T, 3><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 4) k_softmax_reg<T, 4><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 8) k_softmax_reg<T, 8><<<blocks, blk, 0, st>>>(a);
-        else if (per_lane <= 17) k_softmax_reg<T, 17><<<blocks, blk, 0, st>>>(a);
-        else k_softmax_stream<T><<<blocks, blk, 0, st>>>(a);
+        if (per_lane <= 1) k_softmax_reg<T, 1, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 2) k_softmax_reg<T, 2, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 3) k_softmax_reg<T, 3, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 4) k_softmax_reg<T, 4, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 8) k_softmax_reg<T, 8, kDrop><<<grd, blk, smem, st>>>(a);
+        else if (per_lane <= 17) k_softmax_reg<T, 17, kDrop><<<grd, blk, smem, st>>>(a);
+        else k_softmax_stream<T><<<grd, blk, smem, st>>>(a);
     }
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_sm(const SoftmaxArgs &a, bool bwd, cudaStream_t st) {
+    const bool drop = bwd ? a.g.drop_t > 0 : a.Pd != nullptr;
+    return drop ? launch_sm_v<T, true>(a, bwd, st) : launch_sm_v<T, false>(a, bwd, st);
 }
 
 }  // namespace

@@ -353,7 +353,7 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
-    if (g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;  // dropout lives in the fused kernels
+    if (g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;  // the dropped output: band_softmax_dropout
     GlobArgs gl;
     if ((s = check_globals(desc, {Sg, Pg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({S, P})) != SWAB_OK) return s;
@@ -364,6 +364,25 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
         return from_cuda(launch_softmax_glob(dt, a, false, as_stream(stream)));
     }
     SoftmaxArgs a{g, S, nullptr, P, lse, nullptr};
+    return from_cuda(launch_band_softmax(dt, a, as_stream(stream)));
+}
+
+// Largest band the softmax kernels take with dropout: the per-row keep bits
+// (one word per 32 keys, four rows per block) stay within 32 KB of shared memory.
+constexpr int kMaxDropBand = 65536;
+
+SWAB_API swab_status band_softmax_dropout(const swab_desc *desc, const void *S, void *P, void *Pd,
+                                          float *lse, void *stream) {
+    Geom g;
+    DType dt;
+    swab_status s = check_desc(desc, &g, &dt);
+    if (s != SWAB_OK) return s;
+    if (desc->n_global > 0) return SWAB_ERR_UNSUPPORTED;
+    if ((s = check_ptrs({S, Pd})) != SWAB_OK) return s;
+    if (P && !aligned16(P)) return SWAB_ERR_MISALIGNED;
+    if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
+    if (g.D > kMaxDropBand) return SWAB_ERR_UNSUPPORTED;
+    SoftmaxArgs a{g, S, nullptr, P, lse, nullptr, Pd};
     return from_cuda(launch_band_softmax(dt, a, as_stream(stream)));
 }
 
@@ -421,6 +440,7 @@ SWAB_API swab_status band_softmax_bwd(const swab_desc *desc, const void *P, cons
     GlobArgs gl;
     if ((s = check_globals(desc, {Pg, dPg, dSg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({P, dP, dS})) != SWAB_OK) return s;
+    if (g.drop_t > 0 && g.D > kMaxDropBand) return SWAB_ERR_UNSUPPORTED;
     if (gl.G > 0) {
         SoftmaxGlobArgs a{g, gl, P, dP, Pg->cols, dPg->cols, Pg->rows, dPg->rows,
                           dS, dSg->cols, dSg->rows, nullptr};

@@ -86,9 +86,10 @@ struct SoftmaxArgs {
     Geom g;
     const void *S;    // fwd: scores; bwd: P
     const void *S2;   // bwd: dP
-    void *P;          // fwd: probabilities; bwd: dS
+    void *P;          // fwd: probabilities (may be null with Pd); bwd: dS
     float *lse;       // fwd only, may be null
     unsigned *err;
+    void *Pd;         // fwd with dropout: dropped, rescaled probabilities; else null
 };
 
 struct AttnArgs {     // fused forward, tensor-core path

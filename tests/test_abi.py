@@ -250,3 +250,26 @@ def test_dropout_validation(lib):
     dg = desc(n=512, global_idx=[0, 5], dropout_p=0.1)
     assert call(lib, "band_qk", dg, FAKE, FAKE, FAKE) == UNSUPPORTED
     assert desc(dropout_p=0.1).drop_t == 26 and desc(dropout_p=0.999).drop_t == 255
+
+
+def test_softmax_dropout_validation(lib):
+    """band_softmax_dropout: S and Pd required and aligned, P and lse optional
+    but aligned, no global tokens, bands of at most 65536 slots."""
+    P = ctypes.c_void_p
+    f = lib.band_softmax_dropout
+    d = desc(dropout_p=0.1)
+    assert f(None, P(FAKE), P(FAKE), P(FAKE), None, None) == INVALID
+    assert f(ctypes.byref(d.c), None, None, P(FAKE), None, None) == INVALID
+    assert f(ctypes.byref(d.c), P(FAKE), None, None, None, None) == INVALID
+    assert f(ctypes.byref(d.c), P(FAKE), None, P(FAKE + 2), None, None) == MISALIGNED
+    assert f(ctypes.byref(d.c), P(FAKE), P(FAKE + 8), P(FAKE), None, None) == MISALIGNED
+    assert f(ctypes.byref(d.c), P(FAKE), None, P(FAKE), P(FAKE + 4), None) == MISALIGNED
+    dg = desc(n=512, global_idx=[0, 5])
+    assert f(ctypes.byref(dg.c), P(FAKE), None, P(FAKE), None, None) == UNSUPPORTED
+    big = desc(n=256, w=40000, w_upper=30000, dropout_p=0.1)
+    assert f(ctypes.byref(big.c), P(FAKE), None, P(FAKE), None, None) == UNSUPPORTED
+    assert call(lib, "band_softmax_bwd", big, FAKE, FAKE, FAKE) == UNSUPPORTED
+    # without dropout the long band is fine for band_softmax_bwd's validation
+    big0 = desc(n=256, w=40000, w_upper=30000)
+    if not torch.cuda.is_available():
+        assert call(lib, "band_softmax_bwd", big0, FAKE, FAKE, FAKE) == CUDA
