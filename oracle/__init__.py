@@ -62,7 +62,9 @@ def _load():
         _lib.orc_philox4x64.restype = i
         _lib.orc_dropout_factor.argtypes = [u64, i, i, i, i, i, ctypes.POINTER(ctypes.c_double)]
         _lib.orc_dropout_factor.restype = i
-        for f in ("orc_band_qk", "orc_band_softmax", "orc_band_pv", "orc_band_t",
+        _lib.orc_add_bias_transpose.argtypes = [i, i, i, i, i, p, p, p]
+        for f in ("orc_add_bias_transpose", "orc_band_qk", "orc_band_softmax", "orc_band_pv",
+                  "orc_band_t",
                   "orc_band_softmax_bwd", "orc_attention_fwd", "orc_attention_bwd"):
             getattr(_lib, f).restype = i
     return _lib
@@ -239,3 +241,16 @@ def attention_bwd(Q, K, V, dO, w, w_upper, dilation=0, scale=None, global_idx=No
                                      _ptr(dV), G, _ptr(g), _ptr(kb), seed, drop_t),
            "attention_bwd")
     return dQ, dK, dV
+
+
+def add_bias_transpose(X, bias=None):
+    """X [b, n, M, h, hd] (+ bias [M, h, hd]) -> Y [M, b, h, n, hd]."""
+    X = _f64(X)
+    b, n, M, h, hd = X.shape
+    bias = _f64(bias) if bias is not None else None
+    if bias is not None and bias.shape != (M, h, hd):
+        raise ValueError(f"bias must be [M, h, hd] = {(M, h, hd)}")
+    Y = np.empty((M, b, h, n, hd))
+    _check(_load().orc_add_bias_transpose(b, n, M, h, hd, _ptr(X), _ptr(bias), _ptr(Y)),
+           "add_bias_transpose")
+    return Y

@@ -625,3 +625,25 @@ int orc_attention_bwd(int BH, int n, int hd, int w, int wu, int dil, double scal
     free(pbuf); free(sbuf); free(ks.off); free(ks.key); free(gm); free(gp);
     return 0;
 }
+
+/* ---------------------------------------------------------------------
+ * AddBiasTranspose (ONNX Runtime issue "[WIP] Improve LongformerAttention
+ * performance", item (2): bias add and transpose after the merged
+ * projection): X holds rows of [b, n, M, h, hd] (M projections side by
+ * side), bias is [M, h, hd] (or NULL), Y is [M, b, h, n, hd]:
+ *   Y[m][bb][hh][i][c] = X[bb][i][m][hh][c] + bias[m][hh][c].
+ * --------------------------------------------------------------------- */
+int orc_add_bias_transpose(int b, int n, int M, int h, int hd, const double *X,
+                           const double *bias, double *Y) {
+    if (b < 1 || n < 1 || M < 1 || h < 1 || hd < 1) return -1;
+    for (int m = 0; m < M; ++m)
+        for (int bb = 0; bb < b; ++bb)
+            for (int hh = 0; hh < h; ++hh)
+                for (int i = 0; i < n; ++i)
+                    for (int c = 0; c < hd; ++c) {
+                        const size_t src = ((((size_t)bb * n + i) * M + m) * h + hh) * hd + c;
+                        const size_t dst = ((((size_t)m * b + bb) * h + hh) * n + i) * hd + c;
+                        Y[dst] = X[src] + (bias ? bias[((size_t)m * h + hh) * hd + c] : 0.0);
+                    }
+    return 0;
+}

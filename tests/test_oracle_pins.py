@@ -548,6 +548,40 @@ def pin_dropout():
     test_dropout_attention_vs_torch(*DROP_CASES[0])
 
 
+# ---------------------------------------------------------------------------
+# AddBiasTranspose (ONNX Runtime issue, item (2)) against numpy broadcasting and
+# an axis permutation
+# ---------------------------------------------------------------------------
+ABT_CASES = [(1, 7, 3, 2, 4), (2, 5, 1, 3, 8), (3, 4, 2, 1, 2)]  # b, n, M, h, hd
+
+
+@pytest.mark.parametrize("b,n,M,h,hd", ABT_CASES)
+def test_add_bias_transpose_vs_numpy(b, n, M, h, hd):
+    rng = np.random.default_rng(b * 100 + n)
+    X = rng.standard_normal((b, n, M, h, hd))
+    bias = rng.standard_normal((M, h, hd))
+    want = np.transpose(X + bias[None, None], (2, 0, 3, 1, 4))
+    np.testing.assert_array_equal(oracle.add_bias_transpose(X, bias), want)
+    np.testing.assert_array_equal(oracle.add_bias_transpose(X), np.transpose(X, (2, 0, 3, 1, 4)))
+
+
+def test_add_bias_transpose_is_a_permutation():
+    """Without a bias every input value lands in exactly one place: distinct
+    integers come out as the same multiset, each at its own index."""
+    b, n, M, h, hd = 2, 3, 3, 2, 4
+    X = np.arange(b * n * M * h * hd, dtype=np.float64).reshape(b, n, M, h, hd)
+    Y = oracle.add_bias_transpose(X)
+    np.testing.assert_array_equal(np.sort(Y.ravel()), X.ravel())
+    for (m, bb, hh, i, c) in [(0, 0, 0, 0, 0), (2, 1, 1, 2, 3), (1, 0, 1, 2, 0)]:
+        assert Y[m, bb, hh, i, c] == (((bb * n + i) * M + m) * h + hh) * hd + c
+
+
+def pin_add_bias_transpose():
+    for c in ABT_CASES:
+        test_add_bias_transpose_vs_numpy(*c)
+    test_add_bias_transpose_is_a_permutation()
+
+
 MUTANTS = {
     "key_offset": ("(long long)(t - w) * s;", "(long long)(t - w + 1) * s;"),
     "stride": ("const int D = w + wu + 1, s = dil + 1;",
@@ -574,6 +608,9 @@ MUTANTS = {
     "dropout_factor_dropped": ("""                    const double p = exp(x[u] - m) / z *
                                      drop_factor(seed, drop_t, bh, i, ks.key[b0 + u], s_);""",
                                """                    const double p = exp(x[u] - m) / z;"""),
+    "abt_m_h_swapped": ("const size_t src = ((((size_t)bb * n + i) * M + m) * h + hh) * hd + c;",
+                        "const size_t src = ((((size_t)bb * n + i) * h + hh) * M + m) * hd + c;"),
+    "abt_bias_index": ("bias[((size_t)m * h + hh) * hd + c]", "bias[((size_t)hh * M + m) * hd + c]"),
     "dropout_byte_order": ("(out[k / 8] >> (8 * (k % 8)))", "(out[k % 4] >> (8 * (k / 4)))"),
     "qk_transposed": ("srow[t] = alpha * dot(a, B + ((size_t)bh * n + j) * hd, hd);",
                       "srow[t] = alpha * dot(B + ((size_t)bh * n + i) * hd,"
@@ -596,6 +633,7 @@ def run_all_pins():
         pin_bias(*c)
     pin_dropout()
     test_dropout_factor_definition()
+    pin_add_bias_transpose()
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
@@ -617,7 +655,8 @@ def test_planted_mistake_fails_pins(name):
             mut = ctypes.CDLL(so)
             for fname in ("orc_num_threads", "orc_band_qk", "orc_band_softmax", "orc_band_pv",
                           "orc_band_t", "orc_band_softmax_bwd", "orc_attention_fwd",
-                          "orc_attention_bwd", "orc_philox4x64", "orc_dropout_factor"):
+                          "orc_attention_bwd", "orc_philox4x64", "orc_dropout_factor",
+                          "orc_add_bias_transpose"):
                 src_f, dst_f = getattr(oracle._lib, fname), getattr(mut, fname)
                 dst_f.argtypes, dst_f.restype = src_f.argtypes, src_f.restype
             oracle._lib = mut
