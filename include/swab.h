@@ -117,6 +117,21 @@ typedef struct swab_desc {
      * the other calls do not depend on it. */
     float dropout_p;
     uint64_t dropout_seed;
+    /* Optional strided layout of the dense tensors in band_attention and
+     * band_attention_bwd (ONNX Runtime issue "[WIP] Improve LongformerAttention
+     * performance": the merged QKV projection leaves rows of [b, n, 3, h,
+     * head_dim]).  0 = the contiguous [b, h, n, head_dim] layout.  Otherwise
+     * the row stride in elements: element (batch bb, head hh, position i,
+     * channel c) is at (bb * n + i) * stride + hh * head_dim + c, i.e. rows of
+     * [b, n, stride] with the heads side by side; stride >= h * head_dim and a
+     * multiple of 16 bytes (else SWAB_ERR_INVALID_ARG / SWAB_ERR_MISALIGNED).
+     * qkv_row_stride applies to Q, K, V, dQ, dK, dV (3 h head_dim reads Q, K, V
+     * straight from the merged projection: pass its base, base + h head_dim and
+     * base + 2 h head_dim); out_row_stride to O and dO.  lse stays [b, h, n].
+     * The other calls (materialised band products, band_attention_bwd_noalloc)
+     * take the contiguous layout only (SWAB_ERR_UNSUPPORTED). */
+    int64_t qkv_row_stride;
+    int64_t out_row_stride;
 } swab_desc;
 
 /* Companion of a band tensor when n_global > 0 (device pointers, dtype of the
@@ -162,6 +177,19 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
  * SWAB_ERR_UNSUPPORTED). */
 SWAB_API swab_status band_softmax_dropout(const swab_desc *desc, const void *S, void *P, void *Pd,
                                           float *lse, void *stream);
+
+/* AddBiasTranspose (ONNX Runtime issue "[WIP] Improve LongformerAttention
+ * performance", item (2): the bias add and the transpose after the merged
+ * projection in one kernel, with the widest vector loads, conclusion (g)):
+ *   Y[m, bb, hh, i, c] = X[bb, i, m, hh, c] + bias[m, hh, c]
+ * for M matrices side by side in each row of X (M = 3: Q, K, V), i.e.
+ * X = rows of [b, n, M, h, head_dim] -> Y = M tensors [b, h, n, head_dim].
+ * b, h, n, head_dim and dtype come from desc (head_dim * element size a
+ * multiple of 16 bytes); the sum is rounded once to the dtype (correctly
+ * rounded).  bias ([M, h, head_dim]) may be NULL: a pure transpose.  X, Y,
+ * bias device pointers, 16-byte aligned; Y must not overlap X. */
+SWAB_API swab_status add_bias_transpose(const swab_desc *desc, int32_t M, const void *X,
+                                        const void *bias, void *Y, void *stream);
 
 /* Band x dense product (TVM thread, post 6: transpose_t1 = 0, t1d3 = 2w+1):
  *   O[i,c] = alpha * sum over used slots t of P[i,t] * V[j(i,t), c]

@@ -5,7 +5,8 @@ built into ``_lib/libswab.so`` by ``build.build()``); this package is the thin
 ctypes binding over it plus the seeded input generators.  Nothing here
 computes attention on the host.
 """
-from ._binding import (API_FUNCTIONS, Desc, SwabError, band_attention,  # noqa: F401
+from ._binding import (API_FUNCTIONS, Desc, SwabError, add_bias_transpose,  # noqa: F401
+                       band_attention,
                        band_attention_bwd, band_attention_bwd_noalloc,
                        band_attention_bwd_workspace, band_pv,
                        band_pv_bwd_t, band_qk, band_qk_bwd_t, band_softmax, band_softmax_bwd,
@@ -14,8 +15,8 @@ from ._binding import (API_FUNCTIONS, Desc, SwabError, band_attention,  # noqa: 
                        status_string, version)
 from .inputs import WORKLOADS, Workload, seeded_qkvo, workload_inputs  # noqa: F401
 
-__all__ = ["Desc", "SwabError", "band_qk", "band_softmax", "band_softmax_dropout", "band_pv",
-           "band_qk_bwd_t",
+__all__ = ["Desc", "SwabError", "add_bias_transpose", "band_qk", "band_softmax",
+           "band_softmax_dropout", "band_pv", "band_qk_bwd_t",
            "band_pv_bwd_t", "band_softmax_bwd", "band_attention", "band_attention_bwd",
            "band_attention_bwd_noalloc",
            "band_attention_bwd_workspace", "device_status", "selftest_wait_timeout", "load",

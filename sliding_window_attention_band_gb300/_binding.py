@@ -24,7 +24,7 @@ MAX_DILATION = 15
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # every symbol the header declares
-API_FUNCTIONS = ("band_qk", "band_softmax", "band_softmax_dropout", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
+API_FUNCTIONS = ("add_bias_transpose", "band_qk", "band_softmax", "band_softmax_dropout", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
                  "band_softmax_bwd", "band_attention", "band_attention_bwd",
                  "band_attention_bwd_workspace", "band_attention_bwd_noalloc",
                  "swab_status_string", "swab_device_status",
@@ -46,7 +46,8 @@ class _Desc(ctypes.Structure):
                 ("padding", ctypes.c_float), ("dtype", ctypes.c_int32),
                 ("n_global", ctypes.c_int32), ("global_idx", ctypes.POINTER(ctypes.c_int32)),
                 ("key_bias", ctypes.c_void_p), ("dropout_p", ctypes.c_float),
-                ("dropout_seed", ctypes.c_uint64)]
+                ("dropout_seed", ctypes.c_uint64), ("qkv_row_stride", ctypes.c_int64),
+                ("out_row_stride", ctypes.c_int64)]
 
 
 class _Glob(ctypes.Structure):
@@ -58,7 +59,7 @@ class Desc:
 
     def __init__(self, b, h, n, head_dim, w, w_upper, dilation=0, padding=0.0,
                  dtype=torch.float16, global_idx=None, key_bias=None, dropout_p=0.0,
-                 dropout_seed=0):
+                 dropout_seed=0, qkv_row_stride=0, out_row_stride=0):
         if dtype not in _DTYPES:
             raise ValueError(f"unsupported dtype {dtype}")
         self.b, self.h, self.n, self.head_dim = int(b), int(h), int(n), int(head_dim)
@@ -76,11 +77,13 @@ class Desc:
                                  f"{(self.b, self.n)} tensor")
         self.key_bias = key_bias
         self.dropout_p, self.dropout_seed = float(dropout_p), int(dropout_seed)
+        # strided dense layout of the fused calls: rows of [b, n, stride]
+        self.qkv_row_stride, self.out_row_stride = int(qkv_row_stride), int(out_row_stride)
         self.c = _Desc(self.b, self.h, self.n, self.head_dim, self.w, self.w_upper,
                        self.dilation, self.padding, _DTYPES[dtype], len(gi),
                        ctypes.cast(self._gi, ctypes.POINTER(ctypes.c_int32)) if gi else None,
                        key_bias.data_ptr() if key_bias is not None else None, self.dropout_p,
-                       self.dropout_seed)
+                       self.dropout_seed, self.qkv_row_stride, self.out_row_stride)
 
     @property
     def drop_t(self):
@@ -131,6 +134,7 @@ def load():
                 "band_qk": [D, f, P, P, P, Gp, P],
                 "band_softmax": [D, P, Gp, P, Gp, P, P],
                 "band_softmax_dropout": [D, P, P, P, P, P],
+                "add_bias_transpose": [D, i32, P, P, P, P],
                 "band_pv": [D, f, P, Gp, P, P, P],
                 "band_qk_bwd_t": [D, f, P, Gp, P, P, P],
                 "band_pv_bwd_t": [D, f, P, Gp, P, P, P],
@@ -299,13 +303,30 @@ def band_softmax_bwd(desc: Desc, P, dP, dS, Pg=None, dPg=None, dSg=None, stream=
           _glob(dPg, desc, "dPg"), _ptr(dS), _glob(dSg, desc, "dSg"), _stream(stream, dS))
 
 
+def _dense_ptr(desc: Desc, name, t, stride):
+    """Pointer to a dense tensor of a fused call: contiguous [b*h, n, hd] (or
+    any contiguous shape of that size) when stride == 0, else a [b, n, h, hd]
+    view whose rows are `stride` elements apart (e.g. a slice of the merged
+    projection output [b, n, 3, h, hd])."""
+    if stride == 0:
+        _check_shape(name, t, _dense(desc), desc.dtype)
+        return _ptr(t)
+    want_shape = (desc.b, desc.n, desc.h, desc.head_dim)
+    want_strides = (desc.n * stride, stride, desc.head_dim, 1)
+    if t.dtype != desc.dtype or tuple(t.shape) != want_shape or tuple(t.stride()) != want_strides:
+        raise ValueError(f"{name}: expected a {want_shape} view with strides {want_strides}, got "
+                         f"{tuple(t.shape)} / {tuple(t.stride())} {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def band_attention(desc: Desc, scale, Q, K, V, O, lse=None, stream=None):
     """Fused forward: O (and lse) of band_qk -> band_softmax -> band_pv, scores on chip."""
-    for n_, t in (("Q", Q), ("K", K), ("V", V), ("O", O)):
-        _check_shape(n_, t, _dense(desc), desc.dtype)
+    ps, os_ = desc.qkv_row_stride, desc.out_row_stride
+    args = [_dense_ptr(desc, "Q", Q, ps), _dense_ptr(desc, "K", K, ps),
+            _dense_ptr(desc, "V", V, ps), _dense_ptr(desc, "O", O, os_)]
     _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
-    _call("band_attention", ctypes.byref(desc.c), float(scale), _ptr(Q), _ptr(K), _ptr(V),
-          _ptr(O), _ptr(lse), _stream(stream, O))
+    _call("band_attention", ctypes.byref(desc.c), float(scale), *args, _ptr(lse),
+          _stream(stream, O))
 
 
 def band_attention_bwd_workspace(desc: Desc) -> int:
@@ -316,15 +337,29 @@ def band_attention_bwd_workspace(desc: Desc) -> int:
 def band_attention_bwd(desc: Desc, scale, Q, K, V, O, dO, lse, dQ, dK, dV, workspace,
                        stream=None):
     """Fused backward: dQ, dK, dV from Q, K, V, O, dO and the forward's lse."""
-    for n_, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO), ("dQ", dQ), ("dK", dK),
-                  ("dV", dV)):
-        _check_shape(n_, t, _dense(desc), desc.dtype)
+    ps, os_ = desc.qkv_row_stride, desc.out_row_stride
+    args = [_dense_ptr(desc, n_, t, st) for n_, t, st in
+            (("Q", Q, ps), ("K", K, ps), ("V", V, ps), ("O", O, os_), ("dO", dO, os_))]
+    outs = [_dense_ptr(desc, n_, t, ps) for n_, t in (("dQ", dQ), ("dK", dK), ("dV", dV))]
     _check_shape("lse", lse, (desc.BH, desc.n), torch.float32)
     if workspace.numel() * workspace.element_size() < band_attention_bwd_workspace(desc):
         raise ValueError("workspace too small")
-    _call("band_attention_bwd", ctypes.byref(desc.c), float(scale), _ptr(Q), _ptr(K), _ptr(V),
-          _ptr(O), _ptr(dO), _ptr(lse), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
-          _stream(stream, dQ))
+    _call("band_attention_bwd", ctypes.byref(desc.c), float(scale), *args, _ptr(lse), *outs,
+          _ptr(workspace), _stream(stream, dQ))
+
+
+def add_bias_transpose(desc: Desc, X, bias, Y, stream=None):
+    """Y[m] = transpose of X[:, :, m] + bias[m]: X rows of [b, n, M, h, hd] (the
+    merged projection output), bias [M, h, hd] or None, Y [M, b, h, n, hd]."""
+    if X.dim() != 5 or X.shape[0] != desc.b or X.shape[1] != desc.n or X.shape[3] != desc.h \
+            or X.shape[4] != desc.head_dim:
+        raise ValueError(f"X: expected [b, n, M, h, hd], got {tuple(X.shape)}")
+    M = int(X.shape[2])
+    _check_shape("X", X, tuple(X.shape), desc.dtype)
+    _check_shape("bias", bias, (M, desc.h, desc.head_dim), desc.dtype)
+    _check_shape("Y", Y, (M, desc.b, desc.h, desc.n, desc.head_dim), desc.dtype)
+    _call("add_bias_transpose", ctypes.byref(desc.c), M, _ptr(X), _ptr(bias), _ptr(Y),
+          _stream(stream, Y))
 
 
 def selftest_wait_timeout(limit_us: int = 20000, stream=None):

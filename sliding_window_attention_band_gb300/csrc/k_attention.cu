@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(mk);
                 tma_prefetch_desc(mv);
                 mbar_arrive_expect_tx(&qfull[qb], kQBytes);
-                tma_load_3d(qtile + qb * kQBytes, mq, &qfull[qb], 0, tl.a0, tl.bh);
+                tma_load_dense(qtile + qb * kQBytes, mq, &qfull[qb], tl.a0, tl.bh, g.h, g.rs_p != 0);
             }
             __syncwarp();
             ++it;
@@ -198,8 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&kvfull[st], kStageBytes);
                     uint8_t *stage = kv + st * kStageBytes;
-                    tma_load_3d(stage, mk, &kvfull[st], 0, tl.kb_lo + c * kBK, tl.bh);
-                    tma_load_3d(stage + kKBytes, mv, &kvfull[st], 0, tl.kb_lo + c * kBK, tl.bh);
+                    tma_load_dense(stage, mk, &kvfull[st], tl.kb_lo + c * kBK, tl.bh, g.h, g.rs_p != 0);
+                    tma_load_dense(stage + kKBytes, mv, &kvfull[st], tl.kb_lo + c * kBK, tl.bh, g.h,
+                                   g.rs_p != 0);
                 }
                 __syncwarp();
                 ++gc;
@@ -350,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();   // O may be overwritten once this warp's next P tile is signalled
             if (epi_ok) {
                 const long long row = epi_row;
-                uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + row * 64 + 16 * part);
+                uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + dense_row(g, row, g.rs_o) +
+                                                      16 * part);
                 o4[0] = make_uint4(pack2<T>(y[0], y[1]), pack2<T>(y[2], y[3]), pack2<T>(y[4], y[5]),
                                    pack2<T>(y[6], y[7]));
                 o4[1] = make_uint4(pack2<T>(y[8], y[9]), pack2<T>(y[10], y[11]),
@@ -550,16 +552,17 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
     const int c = threadIdx.x;
     const int lane = c & 31, wid = c >> 5, nw = (blockDim.x + 31) >> 5;
     __shared__ float part[4];
-    const float *Q = p.Q + R * g.hd;
-    const float *K = p.K + bh * g.n * g.hd;
-    const float *V = p.V + bh * g.n * g.hd;
+    const float *Q = p.Q + dense_row(g, R, g.rs_p);
+    const float *K = p.K + dense_row(g, bh * g.n, g.rs_p);   // row j of the slice: j * ks
+    const float *V = p.V + dense_row(g, bh * g.n, g.rs_p);
+    const long long ks = g.rs_p ? g.rs_p : g.hd;
     const float qc = c < g.hd ? Q[c] : 0.f;
     const int t_lo = max(0, g.w - i / g.s);
     const int t_hi = min(g.D - 1, g.w + (g.n - 1 - i) / g.s);
     float m = -INFINITY, l = 0.f, acc = 0.f;
     for (int t = t_lo; t <= t_hi; ++t) {
         const long long j = (long long)i + (long long)(t - g.w) * g.s;
-        float x = c < g.hd ? qc * K[j * g.hd + c] : 0.f;
+        float x = c < g.hd ? qc * K[j * ks + c] : 0.f;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
         if (lane == 0) part[wid] = x;
@@ -573,10 +576,10 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
         const float corr = (m == -INFINITY) ? 0.f : expf(m - m_new);
         const float pv = expf(sc - m_new);
         l = l * corr + pv;   // the row sum is before dropout
-        if (c < g.hd) acc = acc * corr + pv * drop_factor(g, bh, i, j) * V[j * g.hd + c];
+        if (c < g.hd) acc = acc * corr + pv * drop_factor(g, bh, i, j) * V[j * ks + c];
         m = m_new;
     }
-    if (c < g.hd) p.O[R * g.hd + c] = acc / l;
+    if (c < g.hd) p.O[dense_row(g, R, g.rs_o) + c] = acc / l;
     if (c == 0 && p.lse) p.lse[R] = m + logf(l);
 }
 

@@ -130,8 +130,9 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
     for (int k = 0; k < kDeltaRowsPerWarp / 4; ++k) {
         const long long R = warp_row0 + 4 * k + (lane >> 3);
         if (R < rows) {
-            o[k] = ldg16(O + R * 8 + (lane & 7));
-            d[k] = ldg16(dO + R * 8 + (lane & 7));
+            const long long off = dense_row(p.g, R, p.g.rs_o) / 8;   // 8 elements per 16 bytes
+            o[k] = ldg16(O + off + (lane & 7));
+            d[k] = ldg16(dO + off + (lane & 7));
         } else {
             o[k] = d[k] = make_uint4(0, 0, 0, 0);
         }
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(256) k_bwd_dq_out(const BwdArgs p) {
     const float4 *acc = reinterpret_cast<const float4 *>(p.dqacc) + 2 * i;
     const float4 a = acc[0], b = acc[1];
     const float c = p.scale;
-    reinterpret_cast<uint4 *>(p.dQ)[i] = make_uint4(pack2<T>(c * a.x, c * a.y), pack2<T>(c * a.z, c * a.w),
+    const long long off = dense_row(p.g, i >> 3, p.g.rs_p) / 8 + (i & 7);   // row i / 8, group i % 8
+    reinterpret_cast<uint4 *>(p.dQ)[off] = make_uint4(pack2<T>(c * a.x, c * a.y), pack2<T>(c * a.z, c * a.w),
                                                     pack2<T>(c * b.x, c * b.y), pack2<T>(c * b.z, c * b.w));
 }
 
@@ -761,16 +763,16 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 tma_prefetch_desc(mv);
                 tma_prefetch_desc(mo);
                 mbar_arrive_expect_tx(&kfull[tb], kTile);
-                tma_load_3d(kbuf + tb * kTile, mk, &kfull[tb], 0, tl.a0, tl.bh);
+                tma_load_dense(kbuf + tb * kTile, mk, &kfull[tb], tl.a0, tl.bh, g.h, g.rs_p != 0);
                 mbar_arrive_expect_tx(vfull, kTile);
-                tma_load_3d(vbuf, mv, vfull, 0, tl.a0, tl.bh);
+                tma_load_dense(vbuf, mv, vfull, tl.a0, tl.bh, g.h, g.rs_p != 0);
                 // the next tile's K and V into L2: V is reloaded within one
                 // gradient phase at the tile boundary
                 for (int t2 = t + gridDim.x; t2 < ntiles; t2 += gridDim.x) {
                     KTile nx;
                     if (!decode_ktile(g, t2, xt, nx)) continue;
-                    tma_prefetch_l2_3d(&mapK.m[nx.r], 0, nx.a0, nx.bh);
-                    tma_prefetch_l2_3d(&mapV.m[nx.r], 0, nx.a0, nx.bh);
+                    tma_prefetch_dense(&mapK.m[nx.r], nx.a0, nx.bh, g.h, g.rs_p != 0);
+                    tma_prefetch_dense(&mapV.m[nx.r], nx.a0, nx.bh, g.h, g.rs_p != 0);
                     break;
                 }
             }
@@ -786,8 +788,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 if (lane == 0) {
                     const int qbase = tl.qb_lo + c * kB;
                     mbar_arrive_expect_tx(&qfull[qs], kQS);
-                    tma_load_3d(qsbuf + qs * kQS, mq, &qfull[qs], 0, qbase, tl.bh);
-                    tma_load_3d(qsbuf + qs * kQS + kTile, mo, &qfull[qs], 0, qbase, tl.bh);
+                    tma_load_dense(qsbuf + qs * kQS, mq, &qfull[qs], qbase, tl.bh, g.h, g.rs_p != 0);
+                    tma_load_dense(qsbuf + qs * kQS + kTile, mo, &qfull[qs], qbase, tl.bh, g.h,
+                                   g.rs_o != 0);
                 }
                 __syncwarp();
             }
@@ -935,7 +938,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         bool dq_pend = false;   // the dQ of chunk dq_g (in TMEM) waits to be staged
         uint32_t dq_g = 0;
         bool acc_pend = false, acc_ok = false;   // a tile's dV, dK wait to be read out
-        long long acc_row = 0;
+        unsigned acc_row = 0;   // row bh * n + key of dK, dV (below 2^31)
         // dV, dK of key row acc_row (channels [16 part, +16)); the caller has
         // waited for the tile's last products
         auto drain_acc = [&]() {
@@ -946,8 +949,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             tc_fence_before();
             mbar_arrive(accempty);
             if (acc_ok) {
-                uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + acc_row * 64 + 16 * part);
-                uint4 *k4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dK) + acc_row * 64 + 16 * part);
+                const long long off = dense_row(g, acc_row, g.rs_p) + 16 * part;
+                uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + off);
+                uint4 *k4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dK) + off);
                 const float sc = p.scale;
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -1139,7 +1143,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             // dV, dK of these keys: read out during the next chunk (or at the end)
             acc_pend = true;
             acc_ok = kk < tl.nr;
-            acc_row = (long long)tl.bh * g.n + tl.r + (long long)g.s * kk;
+            acc_row = (unsigned)(tl.bh * g.n + tl.r + g.s * kk);
             ++it;
         }
         if (ok && dq_pend) {
@@ -1196,10 +1200,12 @@ __global__ void __launch_bounds__(128) k_bwd_f32(const BwdArgs p, int pass) {
     const long long bh = R / g.n;
     const int c = threadIdx.x;
     __shared__ float part[4];
-    const float *Q = reinterpret_cast<const float *>(p.Q) + bh * g.n * g.hd;
-    const float *K = reinterpret_cast<const float *>(p.K) + bh * g.n * g.hd;
-    const float *V = reinterpret_cast<const float *>(p.V) + bh * g.n * g.hd;
-    const float *dO = reinterpret_cast<const float *>(p.dO) + bh * g.n * g.hd;
+    // row y of the slice is at y * ps (Q, K, V) or y * os (dO) from row 0
+    const long long ps = g.rs_p ? g.rs_p : g.hd, os = g.rs_o ? g.rs_o : g.hd;
+    const float *Q = reinterpret_cast<const float *>(p.Q) + dense_row(g, bh * g.n, g.rs_p);
+    const float *K = reinterpret_cast<const float *>(p.K) + dense_row(g, bh * g.n, g.rs_p);
+    const float *V = reinterpret_cast<const float *>(p.V) + dense_row(g, bh * g.n, g.rs_p);
+    const float *dO = reinterpret_cast<const float *>(p.dO) + dense_row(g, bh * g.n, g.rs_o);
     const float *lse = p.lse + bh * g.n;
     const float *delta = p.delta + bh * g.n;
     const bool on = c < g.hd;
@@ -1210,26 +1216,27 @@ __global__ void __launch_bounds__(128) k_bwd_f32(const BwdArgs p, int pass) {
                                       : (long long)x - (long long)(t - g.w) * g.s;
         if (y < 0 || y >= g.n) continue;
         const long long i = pass == 0 ? x : y, j = pass == 0 ? y : x;
-        const float sdot = block_dot(on ? Q[i * g.hd + c] * K[j * g.hd + c] : 0.f, part);
-        const float pdot = block_dot(on ? dO[i * g.hd + c] * V[j * g.hd + c] : 0.f, part);
+        const float sdot = block_dot(on ? Q[i * ps + c] * K[j * ps + c] : 0.f, part);
+        const float pdot = block_dot(on ? dO[i * os + c] * V[j * ps + c] : 0.f, part);
         const float kb = g.kbias ? g.kbias[(size_t)(bh / g.h) * g.n + (size_t)j] : 0.f;
         const float pr = expf(p.scale * sdot + kb - lse[i]);
         const float f = drop_factor(g, bh, i, j);   // dropout keep-and-scale factor
         const float ds = pr * (f * pdot - delta[i]);
         if (!on) continue;
         if (pass == 0) {
-            acc_a = fmaf(ds, K[j * g.hd + c], acc_a);
+            acc_a = fmaf(ds, K[j * ps + c], acc_a);
         } else {
-            acc_a = fmaf(ds, Q[i * g.hd + c], acc_a);   // dK
-            acc_b = fmaf(pr * f, dO[i * g.hd + c], acc_b);  // dV
+            acc_a = fmaf(ds, Q[i * ps + c], acc_a);   // dK
+            acc_b = fmaf(pr * f, dO[i * os + c], acc_b);  // dV
         }
     }
     if (!on) return;
+    const long long out = dense_row(g, R, g.rs_p) + c;
     if (pass == 0) {
-        reinterpret_cast<float *>(p.dQ)[R * g.hd + c] = p.scale * acc_a;
+        reinterpret_cast<float *>(p.dQ)[out] = p.scale * acc_a;
     } else {
-        reinterpret_cast<float *>(p.dK)[R * g.hd + c] = p.scale * acc_a;
-        reinterpret_cast<float *>(p.dV)[R * g.hd + c] = acc_b;
+        reinterpret_cast<float *>(p.dK)[out] = p.scale * acc_a;
+        reinterpret_cast<float *>(p.dV)[out] = acc_b;
     }
 }
 
@@ -1237,8 +1244,8 @@ __global__ void __launch_bounds__(128) k_bwd_delta_f32(const BwdArgs p) {
     const long long R = blockIdx.x;
     const int c = threadIdx.x;
     __shared__ float part[4];
-    const float *O = reinterpret_cast<const float *>(p.O) + R * p.g.hd;
-    const float *dO = reinterpret_cast<const float *>(p.dO) + R * p.g.hd;
+    const float *O = reinterpret_cast<const float *>(p.O) + dense_row(p.g, R, p.g.rs_o);
+    const float *dO = reinterpret_cast<const float *>(p.dO) + dense_row(p.g, R, p.g.rs_o);
     const float v = block_dot(c < p.g.hd ? O[c] * dO[c] : 0.f, part);
     if (c == 0) p.delta[R] = v;
 }

@@ -92,6 +92,17 @@ swab_status check_desc(const swab_desc *d, Geom *g, DType *dt) {
     g->kbias = d->key_bias;
     g->drop_t = drop_t;
     g->seed = d->dropout_seed;
+    // strided dense layout: rows of [b, n, rs] (heads side by side); the TMA
+    // maps need 16-byte row strides
+    const long long hw = (long long)d->h * d->head_dim;
+    const long long vec = 16 / (long long)elt_size(static_cast<DType>(d->dtype));
+    for (const int64_t rs : {d->qkv_row_stride, d->out_row_stride}) {
+        if (rs < 0 || (rs > 0 && rs < hw)) return SWAB_ERR_INVALID_ARG;
+        if (rs % vec != 0) return SWAB_ERR_MISALIGNED;
+        if (rs > 0 && (long long)d->n * rs * vec > (1ll << 40)) return SWAB_ERR_UNSUPPORTED;
+    }
+    g->rs_p = d->qkv_row_stride;
+    g->rs_o = d->out_row_stride;
     *dt = static_cast<DType>(d->dtype);
     return SWAB_OK;
 }
@@ -141,6 +152,52 @@ bool build_rows_maps(TmapSet *set, const void *base, const Geom &g, DType dt, in
         cuuint32_t estr[3] = {1, 1, 1};
         void *ptr = const_cast<char *>(static_cast<const char *>(base)) + (size_t)rr * 64 * es;
         CUresult res = enc(&set->m[r], ty, 3, ptr, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (res != CUDA_SUCCESS) return false;
+    }
+    return true;
+}
+
+// Maps of the fused kernels' dense tensors, one per residue r: 4-D with
+// increasing strides (TMA coordinates in tma_load_dense).  rs == 0: the
+// contiguous [b, h, n, 64] layout as {64, rows, h, b}; rs > 0: rows of
+// [b, n, rs] with head hh at column 64 hh, as {64, h, rows, b}.  Box = 64
+// elements x box_rows rows of one (b, h) slice, 128-byte swizzle.
+bool build_dense_maps(TmapSet *set, const void *base, const Geom &g, DType dt, int box_rows,
+                      long long rs) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const size_t es = elt_size(dt);
+    const CUtensorMapDataType ty =
+        dt == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int b = g.BH / g.h;
+    std::memset(set, 0, sizeof(*set));
+    for (int r = 0; r < g.s; ++r) {
+        int nr = residue_len(g.n, g.s, r);
+        const int rr = nr > 0 ? r : 0;  // empty residue: never loaded, encode a valid map
+        if (nr == 0) nr = 1;
+        cuuint64_t dims[4], strides[3];
+        cuuint32_t box[4];
+        size_t first;
+        if (rs == 0) {
+            dims[0] = 64; dims[1] = (cuuint64_t)nr; dims[2] = (cuuint64_t)g.h; dims[3] = (cuuint64_t)b;
+            strides[0] = (cuuint64_t)g.s * 64 * es;
+            strides[1] = (cuuint64_t)g.n * 64 * es;
+            strides[2] = (cuuint64_t)g.h * g.n * 64 * es;
+            box[0] = 64; box[1] = (cuuint32_t)box_rows; box[2] = 1; box[3] = 1;
+            first = (size_t)rr * 64 * es;
+        } else {
+            dims[0] = 64; dims[1] = (cuuint64_t)g.h; dims[2] = (cuuint64_t)nr; dims[3] = (cuuint64_t)b;
+            strides[0] = 64 * es;
+            strides[1] = (cuuint64_t)g.s * rs * es;
+            strides[2] = (cuuint64_t)g.n * rs * es;
+            box[0] = 64; box[1] = 1; box[2] = (cuuint32_t)box_rows; box[3] = 1;
+            first = (size_t)rr * rs * es;
+        }
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        void *ptr = const_cast<char *>(static_cast<const char *>(base)) + first;
+        CUresult res = enc(&set->m[r], ty, 4, ptr, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (res != CUDA_SUCCESS) return false;
@@ -217,6 +274,7 @@ swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, co
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
+    if (g.rs_p || g.rs_o) return SWAB_ERR_UNSUPPORTED;  // dense tensors contiguous here
     GlobArgs gl;
     if ((s = check_globals(desc, {Bg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({Bd, Y, X})) != SWAB_OK) return s;
@@ -322,6 +380,7 @@ SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, 
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
+    if (g.rs_p || g.rs_o) return SWAB_ERR_UNSUPPORTED;  // dense tensors contiguous here
     GlobArgs gl;
     if ((s = check_globals(desc, {Sg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({A, B, S})) != SWAB_OK) return s;
@@ -367,6 +426,29 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
     return from_cuda(launch_band_softmax(dt, a, as_stream(stream)));
 }
 
+SWAB_API swab_status add_bias_transpose(const swab_desc *desc, int32_t M, const void *X,
+                                        const void *bias, void *Y, void *stream) {
+    if (!desc || M < 1) return SWAB_ERR_INVALID_ARG;
+    if (desc->b < 1 || desc->h < 1 || desc->n < 1 || desc->head_dim < 1) return SWAB_ERR_INVALID_ARG;
+    if (desc->dtype != SWAB_F32 && desc->dtype != SWAB_F16 && desc->dtype != SWAB_BF16)
+        return SWAB_ERR_INVALID_ARG;
+    const DType dt = static_cast<DType>(desc->dtype);
+    const long long row_bytes = (long long)desc->head_dim * (long long)elt_size(dt);
+    if (row_bytes % 16 != 0) return SWAB_ERR_UNSUPPORTED;
+    swab_status s;
+    if ((s = check_ptrs({X, Y})) != SWAB_OK) return s;
+    if (bias && !aligned16(bias)) return SWAB_ERR_MISALIGNED;
+    BiasTransposeArgs a{X, bias, Y, (long long)desc->b * desc->n, desc->b, desc->n, desc->h, M,
+                        row_bytes / 16};
+    const long long total = a.rows * a.M * a.h * row_bytes;
+    if (a.rows > 0x7fffffffLL || a.M * a.h * a.cpr > (1LL << 30)) return SWAB_ERR_UNSUPPORTED;
+    if (total / row_bytes / a.rows / a.M != a.h) return SWAB_ERR_UNSUPPORTED;  // overflow
+    // Y must not overlap X
+    const char *x0 = static_cast<const char *>(X), *y0 = static_cast<const char *>(Y);
+    if (x0 < y0 + total && y0 < x0 + total) return SWAB_ERR_INVALID_ARG;
+    return from_cuda(launch_add_bias_transpose(dt, a, as_stream(stream)));
+}
+
 // Largest band the softmax kernels take with dropout: the per-row keep bits
 // (one word per 32 keys, four rows per block) stay within 32 KB of shared memory.
 constexpr int kMaxDropBand = 65536;
@@ -392,6 +474,7 @@ SWAB_API swab_status band_pv(const swab_desc *desc, float alpha, const void *P,
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
+    if (g.rs_p || g.rs_o) return SWAB_ERR_UNSUPPORTED;  // dense tensors contiguous here
     GlobArgs gl;
     if ((s = check_globals(desc, {Pg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({P, V, O})) != SWAB_OK) return s;
@@ -466,8 +549,9 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
         return from_cuda(launch_band_attention_f32(a, as_stream(stream)));
     }
     TmapSet mq, mk, mv;
-    if (!build_rows_maps(&mq, Q, g, dt, kQKBoxRows) || !build_rows_maps(&mk, K, g, dt, kQKBoxRows) ||
-        !build_rows_maps(&mv, V, g, dt, kQKBoxRows))
+    if (!build_dense_maps(&mq, Q, g, dt, kQKBoxRows, g.rs_p) ||
+        !build_dense_maps(&mk, K, g, dt, kQKBoxRows, g.rs_p) ||
+        !build_dense_maps(&mv, V, g, dt, kQKBoxRows, g.rs_p))
         return SWAB_ERR_CUDA;
     unsigned *err = status_word();
     if (!err) return SWAB_ERR_CUDA;
@@ -498,8 +582,10 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
     BwdArgs a{g, scale, Q, K, V, O, dO, lse, static_cast<float *>(workspace), dQ, dK, dV, nullptr};
     if (dt == kF32) return from_cuda(launch_band_attention_bwd_f32(a, st));
     TmapSet mq, mk, mv, mo;
-    if (!build_rows_maps(&mq, Q, g, dt, kQKBoxRows) || !build_rows_maps(&mk, K, g, dt, kQKBoxRows) ||
-        !build_rows_maps(&mv, V, g, dt, kQKBoxRows) || !build_rows_maps(&mo, dO, g, dt, kQKBoxRows))
+    if (!build_dense_maps(&mq, Q, g, dt, kQKBoxRows, g.rs_p) ||
+        !build_dense_maps(&mk, K, g, dt, kQKBoxRows, g.rs_p) ||
+        !build_dense_maps(&mv, V, g, dt, kQKBoxRows, g.rs_p) ||
+        !build_dense_maps(&mo, dO, g, dt, kQKBoxRows, g.rs_o))
         return SWAB_ERR_CUDA;
     a.err = status_word();
     if (!a.err) return SWAB_ERR_CUDA;
@@ -523,6 +609,7 @@ SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float sca
     if ((long long)g.BH * g.n > (long long)SWAB_NOALLOC_MAX_ROWS) return SWAB_ERR_UNSUPPORTED;
     if (desc->key_bias) return SWAB_ERR_UNSUPPORTED;  // the two-kernel path has no key bias
     if (g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;    // nor dropout
+    if (g.rs_p || g.rs_o) return SWAB_ERR_UNSUPPORTED;  // nor the strided layout
     if ((s = check_ptrs({Q, K, V, O, dO, lse, dQ, dK, dV})) != SWAB_OK) return s;
     float *scratch = nullptr;
     if (noalloc_delta_scratch(&scratch) != cudaSuccess) return SWAB_ERR_CUDA;

@@ -43,7 +43,20 @@ struct Geom {
     const float *kbias;   // [b, n] key-padding bias added to scaled scores, or null
     int drop_t;           // dropout threshold byte (0 = no dropout)
     unsigned long long seed;  // dropout key
+    // Row strides (elements) of the dense tensors in the fused entry points:
+    // 0 = contiguous [b, h, n, hd]; otherwise rows of [b, n, rs] with the heads
+    // side by side (head hh at hh * hd).  rs_p: Q, K, V, dQ, dK, dV; rs_o: O, dO.
+    long long rs_p, rs_o;
 };
+
+// Element offset of dense row R = bh * n + i under row stride rs (R < 2^31:
+// the descriptor check bounds b*h*n, so the divisions are 32-bit).
+__host__ __device__ __forceinline__ long long dense_row(const Geom &g, long long R, long long rs) {
+    if (rs == 0) return R * g.hd;
+    const unsigned r = (unsigned)R, bh = r / (unsigned)g.n, i = r - bh * (unsigned)g.n;
+    const unsigned b = bh / (unsigned)g.h, hh = bh - b * (unsigned)g.h;
+    return ((long long)b * g.n + i) * rs + (long long)hh * g.hd;
+}
 
 __host__ __device__ __forceinline__ int residue_len(int n, int s, int r) {
     return r < n ? (n - r + s - 1) / s : 0;
@@ -191,6 +204,36 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+// Dense-tensor maps of the fused kernels are 4-D with increasing strides:
+// {64, rows, h, b} for the contiguous layout, {64, h, rows, b} for rows of
+// [b, n, rs]; `row` is the index within the map's residue.
+__device__ __forceinline__ void tma_load_dense(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                               int row, int bh, int h, bool strided) {
+    const int b = bh / h, hh = bh - b * h;
+    if (strided) tma_load_4d(dst, map, bar, 0, hh, row, b);
+    else tma_load_4d(dst, map, bar, 0, row, hh, b);
+}
+__device__ __forceinline__ void tma_prefetch_dense(const CUtensorMap *map, int row, int bh, int h,
+                                                   bool strided) {
+    const int b = bh / h, hh = bh - b * h;
+    if (strided) tma_prefetch_l2_4d(map, 0, hh, row, b);
+    else tma_prefetch_l2_4d(map, 0, row, hh, b);
 }
 
 // TMA reduce-add of a shared-memory tile into global memory (bulk group)

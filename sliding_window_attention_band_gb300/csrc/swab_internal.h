@@ -162,6 +162,16 @@ cudaError_t launch_softmax_glob(DType dt, const SoftmaxGlobArgs &a, bool bwd, cu
 cudaError_t launch_glob_reduce(DType dt, const GlobReduceArgs &a, bool cols, cudaStream_t st);
 cudaError_t launch_band_f32_glob(const DenseGlobArgs &a, bool transposed, cudaStream_t st);
 // softmax forward / backward (all dtypes)
+struct BiasTransposeArgs {   // AddBiasTranspose
+    const void *X;     // rows of [b, n, M, h, hd]
+    const void *bias;  // [M, h, hd] or null
+    void *Y;           // [M, b, h, n, hd]
+    long long rows;    // b * n
+    long long b, n, h, M;
+    long long cpr;     // 16-byte chunks per head row (hd * size / 16)
+};
+cudaError_t launch_add_bias_transpose(DType dt, const BiasTransposeArgs &a, cudaStream_t st);
+
 cudaError_t launch_band_softmax(DType dt, const SoftmaxArgs &a, cudaStream_t st);
 cudaError_t launch_band_softmax_bwd(DType dt, const SoftmaxArgs &a, cudaStream_t st);
 

@@ -273,3 +273,50 @@ def test_softmax_dropout_validation(lib):
     big0 = desc(n=256, w=40000, w_upper=30000)
     if not torch.cuda.is_available():
         assert call(lib, "band_softmax_bwd", big0, FAKE, FAKE, FAKE) == CUDA
+
+
+def test_strided_layout_validation(lib):
+    """Row strides: >= h * head_dim, 16-byte multiples; the materialised band
+    products and the allocation-free backward take the contiguous layout only."""
+    P = ctypes.c_void_p
+    for kw, want in ((dict(qkv_row_stride=-8), INVALID), (dict(qkv_row_stride=64), INVALID),
+                     (dict(out_row_stride=100), INVALID), (dict(qkv_row_stride=132), MISALIGNED),
+                     (dict(out_row_stride=136, dtype=torch.float32), OK)):
+        d = desc(**kw)   # h = 2, head_dim = 64: h * head_dim = 128
+        rc = call(lib, "band_attention", d, FAKE, FAKE, FAKE, FAKE)
+        if want == OK:
+            assert rc in (OK, CUDA)   # valid; without a GPU the launch fails cleanly
+        else:
+            assert rc == want, kw
+    d = desc(qkv_row_stride=384)
+    for name in ("band_qk", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t"):
+        assert call(lib, name, d, FAKE, FAKE, FAKE) == UNSUPPORTED, name
+    d = desc(out_row_stride=256)
+    assert lib.band_attention_bwd_noalloc(ctypes.byref(d.c), 0.125, *(P(FAKE) for _ in range(9)),
+                                          None) == UNSUPPORTED
+
+
+def test_add_bias_transpose_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.add_bias_transpose
+    d = desc()
+    assert f(None, 3, P(FAKE), None, P(FAKE * 16), None) == INVALID
+    assert f(ctypes.byref(d.c), 0, P(FAKE), None, P(FAKE * 16), None) == INVALID
+    assert f(ctypes.byref(d.c), 3, None, None, P(FAKE * 16), None) == INVALID
+    assert f(ctypes.byref(d.c), 3, P(FAKE + 8), None, P(FAKE * 16), None) == MISALIGNED
+    assert f(ctypes.byref(d.c), 3, P(FAKE), P(FAKE + 2), P(FAKE * 16), None) == MISALIGNED
+    assert f(ctypes.byref(d.c), 3, P(FAKE), None, P(FAKE + 4096), None) == INVALID  # overlap
+    odd = desc(head_dim=12)   # 24 bytes per head row: not whole 16-byte chunks
+    assert f(ctypes.byref(odd.c), 3, P(FAKE), None, P(FAKE * 16), None) == UNSUPPORTED
+
+
+def test_binding_strided_views():
+    d = desc(b=2, h=3, n=40, qkv_row_stride=3 * 3 * 64)
+    qkv = torch.zeros(2, 40, 3, 3, 64, dtype=torch.float16)
+    ptr = B._dense_ptr(d, "Q", qkv[:, :, 0], d.qkv_row_stride)
+    assert ptr.value == qkv.data_ptr()
+    with pytest.raises(ValueError):
+        B._dense_ptr(d, "Q", qkv[:, :, 0].contiguous(), d.qkv_row_stride)
+    with pytest.raises(ValueError):
+        B.add_bias_transpose(d, torch.zeros(2, 40, 3, 2, 64, dtype=torch.float16), None,
+                             torch.zeros(3, 2, 3, 40, 64, dtype=torch.float16))
