@@ -63,7 +63,9 @@ def _load():
         _lib.orc_dropout_factor.argtypes = [u64, i, i, i, i, i, ctypes.POINTER(ctypes.c_double)]
         _lib.orc_dropout_factor.restype = i
         _lib.orc_add_bias_transpose.argtypes = [i, i, i, i, i, p, p, p]
-        for f in ("orc_add_bias_transpose", "orc_band_qk", "orc_band_softmax", "orc_band_pv",
+        _lib.orc_global_attention_fwd.argtypes = [i, i, i, i, d, p, p, p, p, p]
+        _lib.orc_global_attention_bwd.argtypes = [i, i, i, i, d, p, p, p, p, p, p, p]
+        for f in ("orc_add_bias_transpose", "orc_global_attention_fwd", "orc_global_attention_bwd", "orc_band_qk", "orc_band_softmax", "orc_band_pv",
                   "orc_band_t",
                   "orc_band_softmax_bwd", "orc_attention_fwd", "orc_attention_bwd"):
             getattr(_lib, f).restype = i
@@ -254,3 +256,29 @@ def add_bias_transpose(X, bias=None):
     _check(_load().orc_add_bias_transpose(b, n, M, h, hd, _ptr(X), _ptr(bias), _ptr(Y)),
            "add_bias_transpose")
     return Y
+
+
+def global_attention_fwd(Qg, Kg, Vg, scale):
+    """Compact global queries Qg [BH, G, hd] over every key of Kg, Vg [BH, n, hd].
+    Returns (Og [BH, G, hd], lseg [BH, G])."""
+    Qg, Kg, Vg = _f64(Qg), _f64(Kg), _f64(Vg)
+    BH, G, hd = Qg.shape
+    n = Kg.shape[1]
+    Og = np.empty((BH, G, hd))
+    lseg = np.empty((BH, G))
+    _check(_load().orc_global_attention_fwd(BH, G, n, hd, scale, _ptr(Qg), _ptr(Kg), _ptr(Vg),
+                                            _ptr(Og), _ptr(lseg)), "global_attention_fwd")
+    return Og, lseg
+
+
+def global_attention_bwd(Qg, Kg, Vg, dOg, scale):
+    """Gradients of global_attention_fwd's Og.  Returns (dQg, dKg, dVg)."""
+    Qg, Kg, Vg, dOg = _f64(Qg), _f64(Kg), _f64(Vg), _f64(dOg)
+    BH, G, hd = Qg.shape
+    n = Kg.shape[1]
+    dQg = np.empty((BH, G, hd))
+    dKg, dVg = np.empty((BH, n, hd)), np.empty((BH, n, hd))
+    _check(_load().orc_global_attention_bwd(BH, G, n, hd, scale, _ptr(Qg), _ptr(Kg), _ptr(Vg),
+                                            _ptr(dOg), _ptr(dQg), _ptr(dKg), _ptr(dVg)),
+           "global_attention_bwd")
+    return dQg, dKg, dVg

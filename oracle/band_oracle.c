@@ -647,3 +647,85 @@ int orc_add_bias_transpose(int b, int n, int M, int h, int hd, const double *X,
                     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------
+ * Global queries with their own projections (ONNX Runtime issue, item (3):
+ * the global_q projection computed only for the global tokens, i.e. a
+ * compact Qg; separate global key / value projections Kg, Vg over every
+ * position).  Per slice bh and global query g:
+ *   p_gj = exp(scale * Qg[g].Kg[j] - m_g) / Z_g over all j in [0, n)
+ *   Og[g] = sum_j p_gj Vg[j],   lseg[g] = m_g + log Z_g.
+ * Backward (dOg given): delta_g = dOg[g].Og[g],
+ *   ds_gj = p_gj (dOg[g].Vg[j] - delta_g),
+ *   dQg[g] = scale sum_j ds_gj Kg[j],  dKg[j] = scale sum_g ds_gj Qg[g],
+ *   dVg[j] = sum_g p_gj dOg[g].
+ * --------------------------------------------------------------------- */
+int orc_global_attention_fwd(int BH, int G, int n, int hd, double scale, const double *Qg,
+                             const double *Kg, const double *Vg, double *Og, double *lseg) {
+    if (BH < 1 || G < 1 || n < 1 || hd < 1) return -1;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int bh = 0; bh < BH; ++bh) {
+        for (int g = 0; g < G; ++g) {
+            const double *q = Qg + ((size_t)bh * G + g) * hd;
+            const double *K = Kg + (size_t)bh * n * hd, *V = Vg + (size_t)bh * n * hd;
+            double *o = Og + ((size_t)bh * G + g) * hd;
+            double m = -INFINITY, z = 0.0;
+            for (int j = 0; j < n; ++j) m = fmax(m, scale * dot(q, K + (size_t)j * hd, hd));
+            for (int c = 0; c < hd; ++c) o[c] = 0.0;
+            for (int j = 0; j < n; ++j) {
+                const double e = exp(scale * dot(q, K + (size_t)j * hd, hd) - m);
+                z += e;
+                for (int c = 0; c < hd; ++c) o[c] += e * V[(size_t)j * hd + c];
+            }
+            for (int c = 0; c < hd; ++c) o[c] /= z;
+            lseg[(size_t)bh * G + g] = m + log(z);
+        }
+    }
+    return 0;
+}
+
+int orc_global_attention_bwd(int BH, int G, int n, int hd, double scale, const double *Qg,
+                             const double *Kg, const double *Vg, const double *dOg, double *dQg,
+                             double *dKg, double *dVg) {
+    if (BH < 1 || G < 1 || n < 1 || hd < 1) return -1;
+#pragma omp parallel for schedule(static)
+    for (int bh = 0; bh < BH; ++bh) {
+        const double *K = Kg + (size_t)bh * n * hd, *V = Vg + (size_t)bh * n * hd;
+        double *dK = dKg + (size_t)bh * n * hd, *dV = dVg + (size_t)bh * n * hd;
+        for (size_t e = 0; e < (size_t)n * hd; ++e) dK[e] = dV[e] = 0.0;
+        double *p = (double *)malloc(sizeof(double) * (size_t)n);
+        double *o = (double *)malloc(sizeof(double) * (size_t)hd);
+        for (int g = 0; g < G; ++g) {
+            const double *q = Qg + ((size_t)bh * G + g) * hd;
+            const double *dO = dOg + ((size_t)bh * G + g) * hd;
+            double *dq = dQg + ((size_t)bh * G + g) * hd;
+            /* the probabilities of this global query and its output */
+            double m = -INFINITY, z = 0.0;
+            for (int j = 0; j < n; ++j) {
+                p[j] = scale * dot(q, K + (size_t)j * hd, hd);
+                m = fmax(m, p[j]);
+            }
+            for (int j = 0; j < n; ++j) {
+                p[j] = exp(p[j] - m);
+                z += p[j];
+            }
+            for (int c = 0; c < hd; ++c) o[c] = 0.0;
+            for (int j = 0; j < n; ++j) {
+                p[j] /= z;
+                for (int c = 0; c < hd; ++c) o[c] += p[j] * V[(size_t)j * hd + c];
+            }
+            const double delta = dot(dO, o, hd);
+            for (int c = 0; c < hd; ++c) dq[c] = 0.0;
+            for (int j = 0; j < n; ++j) {
+                const double ds = p[j] * (dot(dO, V + (size_t)j * hd, hd) - delta);
+                for (int c = 0; c < hd; ++c) {
+                    dq[c] += scale * ds * K[(size_t)j * hd + c];
+                    dK[(size_t)j * hd + c] += scale * ds * q[c];
+                    dV[(size_t)j * hd + c] += p[j] * dO[c];
+                }
+            }
+        }
+        free(p); free(o);
+    }
+    return 0;
+}

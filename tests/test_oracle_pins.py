@@ -582,6 +582,86 @@ def pin_add_bias_transpose():
     test_add_bias_transpose_is_a_permutation()
 
 
+# ---------------------------------------------------------------------------
+# global queries with their own projections (ONNX Runtime issue, item (3) and
+# the compact global_q): dense attention of G compact queries over every key
+# ---------------------------------------------------------------------------
+GA_CASES = [(2, 3, 17, 5), (1, 1, 9, 4), (3, 4, 23, 8)]  # BH, G, n, hd
+
+
+@pytest.mark.parametrize("BH,G,n,hd", GA_CASES)
+def test_global_attention_vs_torch(BH, G, n, hd):
+    rng = np.random.default_rng(BH * 97 + n)
+    Qg, dOg = rng.standard_normal((BH, G, hd)), rng.standard_normal((BH, G, hd))
+    Kg, Vg = rng.standard_normal((BH, n, hd)), rng.standard_normal((BH, n, hd))
+    scale = 0.3
+    t = [torch.from_numpy(x).clone().requires_grad_(True) for x in (Qg, Kg, Vg)]
+    sc = scale * t[0] @ t[1].transpose(-1, -2)
+    O_t = torch.softmax(sc, -1) @ t[2]
+    O_t.backward(torch.from_numpy(dOg))
+    Og, lseg = oracle.global_attention_fwd(Qg, Kg, Vg, scale)
+    np.testing.assert_allclose(Og, O_t.detach().numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lseg, torch.logsumexp(sc, -1).detach().numpy(), rtol=1e-12,
+                               atol=1e-12)
+    got = oracle.global_attention_bwd(Qg, Kg, Vg, dOg, scale)
+    for g, r in zip(got, t):
+        np.testing.assert_allclose(g, r.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_global_attention_equals_shared_projection_rows():
+    """With Qg = Q[G], Kg = K, Vg = V the global queries' outputs are the global
+    rows of the attention with global tokens (key sets on explicit lists)."""
+    BH, n, hd, w, wu = 2, 40, 6, 3, 2
+    gidx = [0, 7, 31]
+    Q, K, V = (randn(BH, n, hd, seed=s) for s in (91, 92, 93))
+    O, lse = oracle.attention_fwd(Q, K, V, w, wu, 0, 0.4, global_idx=gidx)
+    Og, lseg = oracle.global_attention_fwd(Q[:, gidx], K, V, 0.4)
+    np.testing.assert_allclose(Og, O[:, gidx], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lseg, lse[:, gidx], rtol=1e-13, atol=1e-13)
+
+
+def test_separate_global_projections_composition():
+    """Longformer-style attention with separate global projections: local rows
+    attend to their band keys outside G plus G (projections Q, K, V); global
+    rows attend to every key through Qg (compact), Kg, Vg.  The composition --
+    the band path with global_idx for the local rows, global_attention for the
+    global rows, and in the backward dO's global rows zeroed for the band path
+    and handed to global_attention_bwd -- equals dense torch attention under
+    autograd."""
+    BH, n, hd, w, wu, d = 2, 36, 5, 3, 4, 1
+    gidx = [1, 12, 30]
+    Q, K, V, dO = (randn(BH, n, hd, seed=s) for s in (101, 102, 103, 104))
+    Qg = randn(BH, len(gidx), hd, seed=105)
+    Kg, Vg = randn(BH, n, hd, seed=106), randn(BH, n, hd, seed=107)
+    scale = 0.45
+    t = [torch.from_numpy(x).clone().requires_grad_(True) for x in (Q, K, V, Qg, Kg, Vg)]
+    mask = dense_mask(n, w, wu, d, gidx)
+    local, _ = torch_attention(t[0], t[1], t[2], mask, scale)
+    glob = torch.softmax(scale * t[3] @ t[4].transpose(-1, -2), -1) @ t[5]
+    is_g = torch.zeros(n, dtype=torch.bool)
+    is_g[gidx] = True
+    out = local.clone()
+    out[:, gidx] = glob
+    out.backward(torch.from_numpy(dO))
+    O, _ = oracle.attention_fwd(Q, K, V, w, wu, d, scale, global_idx=gidx)
+    Og, _ = oracle.global_attention_fwd(Qg, Kg, Vg, scale)
+    O[:, gidx] = Og
+    np.testing.assert_allclose(O, out.detach().numpy(), rtol=1e-10, atol=1e-12)
+    dO_local = dO.copy()
+    dO_local[:, gidx] = 0.0
+    grads = (oracle.attention_bwd(Q, K, V, dO_local, w, wu, d, scale, global_idx=gidx) +
+             oracle.global_attention_bwd(Qg, Kg, Vg, dO[:, gidx], scale))
+    for g, r in zip(grads, t):
+        np.testing.assert_allclose(g, r.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def pin_global_attention():
+    for c in GA_CASES:
+        test_global_attention_vs_torch(*c)
+    test_global_attention_equals_shared_projection_rows()
+    test_separate_global_projections_composition()
+
+
 MUTANTS = {
     "key_offset": ("(long long)(t - w) * s;", "(long long)(t - w + 1) * s;"),
     "stride": ("const int D = w + wu + 1, s = dil + 1;",
@@ -611,6 +691,9 @@ MUTANTS = {
     "abt_m_h_swapped": ("const size_t src = ((((size_t)bb * n + i) * M + m) * h + hh) * hd + c;",
                         "const size_t src = ((((size_t)bb * n + i) * h + hh) * M + m) * hd + c;"),
     "abt_bias_index": ("bias[((size_t)m * h + hh) * hd + c]", "bias[((size_t)hh * M + m) * hd + c]"),
+    "global_attention_delta": ("const double delta = dot(dO, o, hd);", "const double delta = 0.0;"),
+    "global_attention_dk_scale": ("dK[(size_t)j * hd + c] += scale * ds * q[c];",
+                                  "dK[(size_t)j * hd + c] += ds * q[c];"),
     "dropout_byte_order": ("(out[k / 8] >> (8 * (k % 8)))", "(out[k % 4] >> (8 * (k / 4)))"),
     "qk_transposed": ("srow[t] = alpha * dot(a, B + ((size_t)bh * n + j) * hd, hd);",
                       "srow[t] = alpha * dot(B + ((size_t)bh * n + i) * hd,"
@@ -634,6 +717,7 @@ def run_all_pins():
     pin_dropout()
     test_dropout_factor_definition()
     pin_add_bias_transpose()
+    pin_global_attention()
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
@@ -656,7 +740,8 @@ def test_planted_mistake_fails_pins(name):
             for fname in ("orc_num_threads", "orc_band_qk", "orc_band_softmax", "orc_band_pv",
                           "orc_band_t", "orc_band_softmax_bwd", "orc_attention_fwd",
                           "orc_attention_bwd", "orc_philox4x64", "orc_dropout_factor",
-                          "orc_add_bias_transpose"):
+                          "orc_add_bias_transpose", "orc_global_attention_fwd",
+                          "orc_global_attention_bwd"):
                 src_f, dst_f = getattr(oracle._lib, fname), getattr(mut, fname)
                 dst_f.argtypes, dst_f.restype = src_f.argtypes, src_f.restype
             oracle._lib = mut
