@@ -191,6 +191,36 @@ SWAB_API swab_status band_softmax_dropout(const swab_desc *desc, const void *S, 
 SWAB_API swab_status add_bias_transpose(const swab_desc *desc, int32_t M, const void *X,
                                         const void *bias, void *Y, void *stream);
 
+/* Global queries with their own projections (ONNX Runtime issue "[WIP]
+ * Improve LongformerAttention performance", item (3) and its "compact
+ * global_q"): the G = desc->n_global global queries, given compact as
+ * Qg [b, h, G, 64] (the global_q projection of the global tokens only), attend
+ * to every position through separate global key / value projections
+ * Kg, Vg [b, h, n, 64]:
+ *   Og[g] = sum_j p_gj Vg[j],  p_gj = softmax_j(scale * Qg[g].Kg[j]),
+ *   lseg[g] = log sum_j exp(scale * Qg[g].Kg[j])   ([b, h, G] fp32, may be NULL).
+ * Together with the band path this gives attention with separate global
+ * projections: run the band calls with global_idx (local rows attend to their
+ * band keys outside G plus G, with Q, K, V), then replace O's global rows
+ * O[G[g]] by Og[g].  In the backward, give the band calls dO with its global
+ * rows set to 0 and global_attention_bwd dOg[g] = dO[G[g]].
+ * head_dim 64, contiguous layout, no key bias or dropout.  workspace:
+ * global_attention_workspace(desc) bytes of device memory, 16-byte aligned,
+ * shared by the forward and the backward (not concurrently). */
+SWAB_API size_t global_attention_workspace(const swab_desc *desc);
+SWAB_API swab_status global_attention(const swab_desc *desc, float scale, const void *Qg,
+                                      const void *Kg, const void *Vg, void *Og, float *lseg,
+                                      void *workspace, void *stream);
+/* Backward of global_attention: with delta_g = dOg[g].Og[g] and
+ * ds_gj = p_gj (dOg[g].Vg[j] - delta_g):
+ *   dQg = scale ds Kg,  dKg = scale ds^T Qg,  dVg = p^T dOg.
+ * lseg is the forward's (required).  dKg, dVg rows have one writer each;
+ * dQg sums per-tile partials in a fixed order (bitwise repeatable). */
+SWAB_API swab_status global_attention_bwd(const swab_desc *desc, float scale, const void *Qg,
+                                          const void *Kg, const void *Vg, const void *Og,
+                                          const void *dOg, const float *lseg, void *dQg,
+                                          void *dKg, void *dVg, void *workspace, void *stream);
+
 /* Band x dense product (TVM thread, post 6: transpose_t1 = 0, t1d3 = 2w+1):
  *   O[i,c] = alpha * sum over used slots t of P[i,t] * V[j(i,t), c]
  *            (+ alpha * sum_g Pg->cols[i,g] * V[G[g],c]);

@@ -11,12 +11,14 @@ from ._binding import (API_FUNCTIONS, Desc, SwabError, add_bias_transpose,  # no
                        band_attention_bwd_workspace, band_pv,
                        band_pv_bwd_t, band_qk, band_qk_bwd_t, band_softmax, band_softmax_bwd,
                        band_softmax_dropout,
-                       device_status, library_path, load, selftest_wait_timeout,
+                       device_status, global_attention, global_attention_bwd,
+                       global_attention_workspace, library_path, load, selftest_wait_timeout,
                        status_string, version)
 from .inputs import WORKLOADS, Workload, seeded_qkvo, workload_inputs  # noqa: F401
 
 __all__ = ["Desc", "SwabError", "add_bias_transpose", "band_qk", "band_softmax",
-           "band_softmax_dropout", "band_pv", "band_qk_bwd_t",
+           "band_softmax_dropout", "band_pv", "band_qk_bwd_t", "global_attention",
+           "global_attention_bwd", "global_attention_workspace",
            "band_pv_bwd_t", "band_softmax_bwd", "band_attention", "band_attention_bwd",
            "band_attention_bwd_noalloc",
            "band_attention_bwd_workspace", "device_status", "selftest_wait_timeout", "load",

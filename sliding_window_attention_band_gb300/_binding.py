@@ -24,7 +24,8 @@ MAX_DILATION = 15
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # every symbol the header declares
-API_FUNCTIONS = ("add_bias_transpose", "band_qk", "band_softmax", "band_softmax_dropout", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
+API_FUNCTIONS = ("add_bias_transpose", "global_attention", "global_attention_bwd",
+                 "global_attention_workspace", "band_qk", "band_softmax", "band_softmax_dropout", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
                  "band_softmax_bwd", "band_attention", "band_attention_bwd",
                  "band_attention_bwd_workspace", "band_attention_bwd_noalloc",
                  "swab_status_string", "swab_device_status",
@@ -135,6 +136,8 @@ def load():
                 "band_softmax": [D, P, Gp, P, Gp, P, P],
                 "band_softmax_dropout": [D, P, P, P, P, P],
                 "add_bias_transpose": [D, i32, P, P, P, P],
+                "global_attention": [D, f, P, P, P, P, P, P, P],
+                "global_attention_bwd": [D, f, P, P, P, P, P, P, P, P, P, P, P],
                 "band_pv": [D, f, P, Gp, P, P, P],
                 "band_qk_bwd_t": [D, f, P, Gp, P, P, P],
                 "band_pv_bwd_t": [D, f, P, Gp, P, P, P],
@@ -149,6 +152,8 @@ def load():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int
+            lib.global_attention_workspace.argtypes = [D]
+            lib.global_attention_workspace.restype = ctypes.c_size_t
             lib.band_attention_bwd_workspace.argtypes = [D]
             lib.band_attention_bwd_workspace.restype = ctypes.c_size_t
             lib.swab_status_string.restype = ctypes.c_char_p
@@ -346,6 +351,43 @@ def band_attention_bwd(desc: Desc, scale, Q, K, V, O, dO, lse, dQ, dK, dV, works
         raise ValueError("workspace too small")
     _call("band_attention_bwd", ctypes.byref(desc.c), float(scale), *args, _ptr(lse), *outs,
           _ptr(workspace), _stream(stream, dQ))
+
+
+def global_attention_workspace(desc: Desc) -> int:
+    """Bytes of device workspace global_attention / global_attention_bwd need."""
+    return int(load().global_attention_workspace(ctypes.byref(desc.c)))
+
+
+def _global_shapes(desc: Desc):
+    return (desc.BH, desc.G, desc.head_dim), (desc.BH, desc.n, desc.head_dim)
+
+
+def global_attention(desc: Desc, scale, Qg, Kg, Vg, Og, lseg, workspace, stream=None):
+    """Global queries Qg [b*h, G, 64] over every key of their own projections
+    Kg, Vg [b*h, n, 64]: Og [b*h, G, 64], lseg [b*h, G] (may be None)."""
+    gs, ns = _global_shapes(desc)
+    for n_, t, sh in (("Qg", Qg, gs), ("Kg", Kg, ns), ("Vg", Vg, ns), ("Og", Og, gs)):
+        _check_shape(n_, t, sh, desc.dtype)
+    _check_shape("lseg", lseg, (desc.BH, desc.G), torch.float32)
+    if workspace.numel() * workspace.element_size() < global_attention_workspace(desc):
+        raise ValueError("workspace too small")
+    _call("global_attention", ctypes.byref(desc.c), float(scale), _ptr(Qg), _ptr(Kg), _ptr(Vg),
+          _ptr(Og), _ptr(lseg), _ptr(workspace), _stream(stream, Og))
+
+
+def global_attention_bwd(desc: Desc, scale, Qg, Kg, Vg, Og, dOg, lseg, dQg, dKg, dVg, workspace,
+                         stream=None):
+    """Gradients of global_attention: dQg [b*h, G, 64], dKg, dVg [b*h, n, 64]."""
+    gs, ns = _global_shapes(desc)
+    for n_, t, sh in (("Qg", Qg, gs), ("Kg", Kg, ns), ("Vg", Vg, ns), ("Og", Og, gs),
+                      ("dOg", dOg, gs), ("dQg", dQg, gs), ("dKg", dKg, ns), ("dVg", dVg, ns)):
+        _check_shape(n_, t, sh, desc.dtype)
+    _check_shape("lseg", lseg, (desc.BH, desc.G), torch.float32)
+    if workspace.numel() * workspace.element_size() < global_attention_workspace(desc):
+        raise ValueError("workspace too small")
+    _call("global_attention_bwd", ctypes.byref(desc.c), float(scale), _ptr(Qg), _ptr(Kg), _ptr(Vg),
+          _ptr(Og), _ptr(dOg), _ptr(lseg), _ptr(dQg), _ptr(dKg), _ptr(dVg), _ptr(workspace),
+          _stream(stream, dQg))
 
 
 def add_bias_transpose(desc: Desc, X, bias, Y, stream=None):

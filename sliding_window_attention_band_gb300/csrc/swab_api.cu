@@ -449,6 +449,68 @@ SWAB_API swab_status add_bias_transpose(const swab_desc *desc, int32_t M, const 
     return from_cuda(launch_add_bias_transpose(dt, a, as_stream(stream)));
 }
 
+// shared checks of the global-query calls; fills the kernel arguments
+static swab_status global_proj_setup(const swab_desc *desc, float scale, GlobalProjArgs *a,
+                                     DType *dt) {
+    Geom g;
+    swab_status s = check_desc(desc, &g, dt);
+    if (s != SWAB_OK) return s;
+    if (desc->n_global < 1) return SWAB_ERR_INVALID_ARG;
+    if (desc->head_dim != 64) return SWAB_ERR_UNSUPPORTED;
+    if (g.rs_p || g.rs_o) return SWAB_ERR_UNSUPPORTED;
+    *a = GlobalProjArgs{};
+    a->BH = g.BH;
+    a->G = desc->n_global;
+    a->n = g.n;
+    a->scale = scale;
+    return SWAB_OK;
+}
+
+SWAB_API size_t global_attention_workspace(const swab_desc *desc) {
+    if (!desc || desc->b < 1 || desc->h < 1 || desc->n < 1 || desc->n_global < 1) return 0;
+    return global_proj_workspace_bytes((long long)desc->b * desc->h, desc->n_global, desc->n);
+}
+
+SWAB_API swab_status global_attention(const swab_desc *desc, float scale, const void *Qg,
+                                      const void *Kg, const void *Vg, void *Og, float *lseg,
+                                      void *workspace, void *stream) {
+    GlobalProjArgs a;
+    DType dt;
+    swab_status s = global_proj_setup(desc, scale, &a, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_ptrs({Qg, Kg, Vg, Og, workspace})) != SWAB_OK) return s;
+    if (lseg && !aligned16(lseg)) return SWAB_ERR_MISALIGNED;
+    a.Qg = Qg;
+    a.Kg = Kg;
+    a.Vg = Vg;
+    a.Og = Og;
+    a.lseg = lseg;
+    a.ws = static_cast<float *>(workspace);
+    return from_cuda(launch_global_proj(dt, a, false, as_stream(stream)));
+}
+
+SWAB_API swab_status global_attention_bwd(const swab_desc *desc, float scale, const void *Qg,
+                                          const void *Kg, const void *Vg, const void *Og,
+                                          const void *dOg, const float *lseg, void *dQg,
+                                          void *dKg, void *dVg, void *workspace, void *stream) {
+    GlobalProjArgs a;
+    DType dt;
+    swab_status s = global_proj_setup(desc, scale, &a, &dt);
+    if (s != SWAB_OK) return s;
+    if ((s = check_ptrs({Qg, Kg, Vg, Og, dOg, lseg, dQg, dKg, dVg, workspace})) != SWAB_OK) return s;
+    a.Qg = Qg;
+    a.Kg = Kg;
+    a.Vg = Vg;
+    a.Og = const_cast<void *>(Og);
+    a.dOg = dOg;
+    a.lseg = const_cast<float *>(lseg);
+    a.dQg = dQg;
+    a.dKg = dKg;
+    a.dVg = dVg;
+    a.ws = static_cast<float *>(workspace);
+    return from_cuda(launch_global_proj(dt, a, true, as_stream(stream)));
+}
+
 // Largest band the softmax kernels take with dropout: the per-row keep bits
 // (one word per 32 keys, four rows per block) stay within 32 KB of shared memory.
 constexpr int kMaxDropBand = 65536;

@@ -172,6 +172,22 @@ struct BiasTransposeArgs {   // AddBiasTranspose
 };
 cudaError_t launch_add_bias_transpose(DType dt, const BiasTransposeArgs &a, cudaStream_t st);
 
+struct GlobalProjArgs {   // global queries with their own projections
+    long long BH;
+    int G, n;
+    float scale;
+    const void *Qg;        // [BH, G, 64] compact global queries
+    const void *Kg, *Vg;   // [BH, n, 64] global key / value projections
+    void *Og;              // fwd: output [BH, G, 64]; bwd: the forward's output
+    const void *dOg;       // bwd: [BH, G, 64]
+    float *lseg;           // [BH, G]: fwd output (may be null), bwd input
+    void *dQg, *dKg, *dVg; // bwd outputs
+    float *ws;             // workspace (partials)
+    int nchunks;           // set by the launcher
+};
+size_t global_proj_workspace_bytes(long long BH, int G, int n);
+cudaError_t launch_global_proj(DType dt, const GlobalProjArgs &a, bool bwd, cudaStream_t st);
+
 cudaError_t launch_band_softmax(DType dt, const SoftmaxArgs &a, cudaStream_t st);
 cudaError_t launch_band_softmax_bwd(DType dt, const SoftmaxArgs &a, cudaStream_t st);
 

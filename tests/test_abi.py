@@ -320,3 +320,25 @@ def test_binding_strided_views():
     with pytest.raises(ValueError):
         B.add_bias_transpose(d, torch.zeros(2, 40, 3, 2, 64, dtype=torch.float16), None,
                              torch.zeros(3, 2, 3, 40, 64, dtype=torch.float16))
+
+
+def test_global_attention_validation(lib):
+    P = ctypes.c_void_p
+    f, fb = lib.global_attention, lib.global_attention_bwd
+    d = desc(n=512, global_idx=[0, 3, 9])
+    assert lib.global_attention_workspace(ctypes.byref(d.c)) > 0
+    assert lib.global_attention_workspace(ctypes.byref(desc().c)) == 0   # no global tokens
+    assert f(ctypes.byref(desc().c), 0.1, *(P(FAKE) for _ in range(4)), None, P(FAKE), None) == \
+        INVALID
+    assert f(ctypes.byref(d.c), 0.1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, None, None) == \
+        INVALID   # no workspace
+    assert f(ctypes.byref(d.c), 0.1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE + 4), P(FAKE),
+             None) == MISALIGNED
+    d32 = desc(n=512, global_idx=[0, 3], dtype=torch.float32, head_dim=32)
+    assert f(ctypes.byref(d32.c), 0.1, *(P(FAKE) for _ in range(4)), None, P(FAKE), None) == \
+        UNSUPPORTED
+    ds = desc(n=512, global_idx=[0, 3], qkv_row_stride=384)
+    assert f(ctypes.byref(ds.c), 0.1, *(P(FAKE) for _ in range(4)), None, P(FAKE), None) == \
+        UNSUPPORTED
+    assert fb(ctypes.byref(d.c), 0.1, *(P(FAKE) for _ in range(5)), None,
+              *(P(FAKE) for _ in range(4)), None) == INVALID   # lseg required
