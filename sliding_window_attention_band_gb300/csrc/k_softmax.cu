@@ -196,19 +196,49 @@ __device__ __forceinline__ void store_dropped(uint4 *out, int pc, const Row &rw,
 }
 
 // ---------------------------------------------------------------------------
-// register-resident rows
+// register-resident rows: CTA (4 rows of one slice, slice) -- the grid gives
+// the row's position directly, no division by n.  Invalid elements are
+// replaced once, right after the unpack (-inf in the forward, 0 in the
+// backward), so every later step is uniform packed fp32x2 arithmetic.
 // ---------------------------------------------------------------------------
+// Row geometry of position i of slice bh (s == 1 skips the divisions).
+template <typename T>
+__device__ __forceinline__ Row make_row_at(const Geom &g, long long R, int i) {
+    constexpr int N = Vec<T>::N;
+    Row rw;
+    const int a = g.s == 1 ? i : i / g.s, b = g.s == 1 ? g.n - 1 - i : (g.n - 1 - i) / g.s;
+    const int t_lo = max(0, g.w - a);
+    const int t_hi = min(g.D - 1, g.w + b);
+    const long long e0 = R * g.D;
+    rw.lead = (int)(e0 & (N - 1));
+    rw.piece0 = e0 / N;
+    rw.npieces = (rw.lead + g.D + N - 1) / N;
+    rw.xlo = t_lo + rw.lead;
+    rw.xhi = t_hi + rw.lead;
+    rw.xend = rw.lead + g.D;
+    return rw;
+}
+
+// x[u] = fill where element x0 + u is outside the valid range
+template <int N>
+__device__ __forceinline__ void mask_piece(float (&x)[N], int x0, const Row &rw, float fill) {
+    if (all_valid(x0, N, rw)) return;
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+        if (x0 + u < rw.xlo || x0 + u > rw.xhi) x[u] = fill;
+}
+
 template <typename T, int NCH, bool kDrop>
 __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const SoftmaxArgs p) {
     constexpr int N = Vec<T>::N;
-    constexpr bool kKeep = NCH * N <= 32;  // keep exp() values in registers
+    constexpr bool kKeep = NCH * N <= 32;  // keep the row's values in registers
     const Geom &g = p.g;
     const int lane = threadIdx.x & 31;
-    const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (R >= g.BH * g.n) return;
-    const Row rw = make_row<T>(g, R);
-    const float *brow = bias_row(g, R);
-    const int qi = R % g.n;
+    const int qi = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (qi >= g.n) return;
+    const long long R = (long long)blockIdx.y * g.n + qi;
+    const Row rw = make_row_at<T>(g, R, qi);
+    const float *brow = g.kbias ? g.kbias + (size_t)(blockIdx.y / g.h) * g.n : nullptr;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
     uint4 raw[NCH];
 #pragma unroll
@@ -220,68 +250,82 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
     extern __shared__ uint32_t keep_smem[];
     Keep kp{};
     if constexpr (kDrop)
-        kp = make_keep(g, R, rw, keep_smem + (threadIdx.x >> 5) * keep_words(g.D), lane);
+        kp = make_keep(g, (int)R, rw, keep_smem + (threadIdx.x >> 5) * keep_words(g.D), lane);
+    // scores (plus the key bias), invalid elements -inf
+    auto scores = [&](int k, float (&x)[N]) {
+        const int x0 = (lane + 32 * k) * N;
+        unpack<T>(raw[k], x);
+        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
+        mask_piece<N>(x, x0, rw, -INFINITY);
+    };
+    float xs[kKeep ? NCH * N : 1];
     float m = -INFINITY;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
-        const int x0 = (lane + 32 * k) * N;
         float x[N];
-        unpack<T>(raw[k], x);
-        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
-        if (all_valid(x0, N, rw)) {
+        scores(k, x);
 #pragma unroll
-            for (int u = 0; u < N; ++u) m = fmaxf(m, x[u]);
-        } else {
+        for (int u = 0; u < N; u += 2) m = max3(m, x[u], x[u + 1]);
+        if constexpr (kKeep) {
 #pragma unroll
-            for (int u = 0; u < N; ++u)
-                if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) m = fmaxf(m, x[u]);
+            for (int u = 0; u < N; ++u) xs[k * N + u] = x[u];
         }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     const float mb = m * kLog2e;
-    float z = 0.f;
-    float e[kKeep ? NCH * N : 1];
+    const uint64_t l2 = f2(kLog2e, kLog2e), nb2 = f2(-mb, -mb);
+    // e = 2^(x log2e - m log2e) of a piece (0 on invalid elements)
+    auto expo = [&](float (&x)[N]) {
+#pragma unroll
+        for (int u = 0; u < N; u += 2) {
+            float y0, y1;
+            f2split(fma2(f2(x[u], x[u + 1]), l2, nb2), y0, y1);
+            x[u] = ex2(y0);
+            x[u + 1] = ex2(y1);
+        }
+    };
+    uint64_t z2 = f2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
-        const int x0 = (lane + 32 * k) * N;
         float x[N];
-        unpack<T>(raw[k], x);
-        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
-        const bool full = all_valid(x0, N, rw);
+        if constexpr (kKeep) {
 #pragma unroll
-        for (int u = 0; u < N; ++u) {
-            const bool v = full || (x0 + u >= rw.xlo && x0 + u <= rw.xhi);
-            const float ev = v ? ex2(fmaf(x[u], kLog2e, -mb)) : 0.f;
-            z += ev;
-            if constexpr (kKeep) e[k * N + u] = ev;
+            for (int u = 0; u < N; ++u) x[u] = xs[k * N + u];
+        } else {
+            scores(k, x);
+        }
+        expo(x);
+#pragma unroll
+        for (int u = 0; u < N; u += 2) z2 = add2(z2, f2(x[u], x[u + 1]));
+        if constexpr (kKeep) {
+#pragma unroll
+            for (int u = 0; u < N; ++u) xs[k * N + u] = x[u];
         }
     }
+    float z0, z1;
+    f2split(z2, z0, z1);
+    float z = z0 + z1;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     const float inv = 1.f / z;
+    const uint64_t inv2 = f2(inv, inv);
     uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
     uint4 *dstd = reinterpret_cast<uint4 *>(p.Pd) + rw.piece0;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
         const int pc = lane + 32 * k;
         if (pc >= rw.npieces) break;
-        const int x0 = pc * N;
         float y[N];
         if constexpr (kKeep) {
 #pragma unroll
-            for (int u = 0; u < N; ++u) y[u] = e[k * N + u] * inv;
+            for (int u = 0; u < N; ++u) y[u] = xs[k * N + u];
         } else {
-            float x[N];
-            unpack<T>(raw[k], x);
-            if (brow) add_key_bias(x, x0, rw, brow, qi, g);
-            const bool full = all_valid(x0, N, rw);
-#pragma unroll
-            for (int u = 0; u < N; ++u) {
-                const bool v = full || (x0 + u >= rw.xlo && x0 + u <= rw.xhi);
-                y[u] = v ? ex2(fmaf(x[u], kLog2e, -mb)) * inv : 0.f;
-            }
+            scores(k, y);
+            expo(y);
         }
+#pragma unroll
+        for (int u = 0; u < N; u += 2) f2split(mul2(f2(y[u], y[u + 1]), inv2), y[u], y[u + 1]);
         if constexpr (kDrop) {
             if (p.P) store_piece<T>(dst, pc, rw, y);
             store_dropped<T>(dstd, pc, rw, kp, y);
@@ -297,9 +341,10 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const So
     constexpr int N = Vec<T>::N;
     const Geom &g = p.g;
     const int lane = threadIdx.x & 31;
-    const int R = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (R >= g.BH * g.n) return;
-    const Row rw = make_row<T>(g, R);
+    const int qi = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (qi >= g.n) return;
+    const long long R = (long long)blockIdx.y * g.n + qi;
+    const Row rw = make_row_at<T>(g, R, qi);
     const uint4 *sp = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
     const uint4 *sd = reinterpret_cast<const uint4 *>(p.S2) + rw.piece0;
     uint4 rp[NCH], rd[NCH];
@@ -314,42 +359,41 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const So
     extern __shared__ uint32_t keep_smem[];
     Keep kp{};
     if constexpr (kDrop)
-        kp = make_keep(g, R, rw, keep_smem + (threadIdx.x >> 5) * keep_words(g.D), lane);
-    float delta = 0.f;
-#pragma unroll
-    for (int k = 0; k < NCH; ++k) {
+        kp = make_keep(g, (int)R, rw, keep_smem + (threadIdx.x >> 5) * keep_words(g.D), lane);
+    // P and the gradient reaching P (f dP with dropout) of a piece, both 0 on
+    // invalid elements (whatever those slots hold)
+    auto operands = [&](int k, float (&x)[N], float (&y)[N]) {
         const int x0 = (lane + 32 * k) * N;
-        float x[N], y[N];
         unpack<T>(rp[k], x);
         unpack<T>(rd[k], y);
         if constexpr (kDrop) apply_keep<N>(y, x0, rw, kp);
-        if (all_valid(x0, N, rw)) {
+        mask_piece<N>(x, x0, rw, 0.f);
+        mask_piece<N>(y, x0, rw, 0.f);
+    };
+    uint64_t d2 = f2(0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < N; ++u) delta = fmaf(x[u], y[u], delta);
-        } else {
+    for (int k = 0; k < NCH; ++k) {
+        float x[N], y[N];
+        operands(k, x, y);
 #pragma unroll
-            for (int u = 0; u < N; ++u)
-                if (x0 + u >= rw.xlo && x0 + u <= rw.xhi) delta = fmaf(x[u], y[u], delta);
-        }
+        for (int u = 0; u < N; u += 2) d2 = fma2(f2(x[u], x[u + 1]), f2(y[u], y[u + 1]), d2);
     }
+    float d0, d1;
+    f2split(d2, d0, d1);
+    float delta = d0 + d1;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
+    const uint64_t nd2 = f2(-delta, -delta);
     uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
         const int pc = lane + 32 * k;
         if (pc >= rw.npieces) break;
-        const int x0 = pc * N;
         float x[N], y[N];
-        unpack<T>(rp[k], x);
-        unpack<T>(rd[k], y);
-        if constexpr (kDrop) apply_keep<N>(y, x0, rw, kp);
-        const bool full = all_valid(x0, N, rw);
+        operands(k, x, y);
 #pragma unroll
-        for (int u = 0; u < N; ++u) {
-            const bool v = full || (x0 + u >= rw.xlo && x0 + u <= rw.xhi);
-            x[u] = v ? x[u] * (y[u] - delta) : 0.f;
-        }
+        for (int u = 0; u < N; u += 2)
+            f2split(mul2(f2(x[u], x[u + 1]), add2(f2(y[u], y[u + 1]), nd2)), x[u], x[u + 1]);
         store_piece<T>(dst, pc, rw, x);
     }
 }
@@ -467,26 +511,27 @@ template <typename T, bool kDrop>
 cudaError_t launch_sm_v(const SoftmaxArgs &a, bool bwd, cudaStream_t st) {
     constexpr int N = Vec<T>::N;
     const long long rows = (long long)a.g.BH * a.g.n;
-    const dim3 grd((unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock));
+    const dim3 grd((unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock));   // streaming kernels
+    const dim3 grd2((unsigned)((a.g.n + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)a.g.BH);
     const dim3 blk(kRowsPerBlock * 32);
     const long long pieces = (a.g.D + N - 1) / N + 1;  // most pieces a row touches
     const long long per_lane = (pieces + 31) / 32;
     // dropout: each warp's keep-bit table for its row
     const size_t smem = kDrop ? (size_t)kRowsPerBlock * keep_words(a.g.D) * sizeof(uint32_t) : 0;
     if (bwd) {
-        if (per_lane <= 1) k_softmax_bwd_reg<T, 1, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 2) k_softmax_bwd_reg<T, 2, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 3) k_softmax_bwd_reg<T, 3, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 4) k_softmax_bwd_reg<T, 4, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 8) k_softmax_bwd_reg<T, 8, kDrop><<<grd, blk, smem, st>>>(a);
+        if (per_lane <= 1) k_softmax_bwd_reg<T, 1, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 2) k_softmax_bwd_reg<T, 2, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 3) k_softmax_bwd_reg<T, 3, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 4) k_softmax_bwd_reg<T, 4, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 8) k_softmax_bwd_reg<T, 8, kDrop><<<grd2, blk, smem, st>>>(a);
         else k_softmax_bwd_stream<T><<<grd, blk, smem, st>>>(a);
     } else {
-        if (per_lane <= 1) k_softmax_reg<T, 1, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 2) k_softmax_reg<T, 2, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 3) k_softmax_reg<T, 3, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 4) k_softmax_reg<T, 4, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 8) k_softmax_reg<T, 8, kDrop><<<grd, blk, smem, st>>>(a);
-        else if (per_lane <= 17) k_softmax_reg<T, 17, kDrop><<<grd, blk, smem, st>>>(a);
+        if (per_lane <= 1) k_softmax_reg<T, 1, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 2) k_softmax_reg<T, 2, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 3) k_softmax_reg<T, 3, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 4) k_softmax_reg<T, 4, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 8) k_softmax_reg<T, 8, kDrop><<<grd2, blk, smem, st>>>(a);
+        else if (per_lane <= 17) k_softmax_reg<T, 17, kDrop><<<grd2, blk, smem, st>>>(a);
         else k_softmax_stream<T><<<grd, blk, smem, st>>>(a);
     }
     return cudaGetLastError();
