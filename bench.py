@@ -196,6 +196,121 @@ class FusedStep(Step):
         ]
 
 
+class FusedVariantStep(FusedStep):
+    """The fused step with one of the optional features of the fused calls:
+    dropout of the probabilities (p = 0.1), a key-padding bias (a quarter of
+    the keys masked with -10000), or the strided layout (Q, K, V read from a
+    merged [b, n, 3, h, 64] projection buffer, dQ, dK, dV written into one)."""
+
+    def __init__(self, wl, device, feature):
+        import sliding_window_attention_band_gb300 as swab
+
+        super().__init__(wl, device)
+        self.feature = feature
+        self.DESCRIPTION = f"fused fwd+bwd with {feature}"
+        kw = {}
+        if feature == "dropout p=0.1":
+            kw = dict(dropout_p=0.1, dropout_seed=1234)
+        elif feature == "key bias":
+            g = torch.Generator().manual_seed(77)
+            keep = torch.rand(wl.b, wl.n, generator=g) > 0.25
+            self.kbias = torch.where(keep, 0.0, -10000.0).to(device)
+            kw = dict(key_bias=self.kbias)
+        elif feature == "strided qkv":
+            b, h, n, hd = wl.b, wl.h, wl.n, wl.head_dim
+            self.qkv = torch.empty(b, n, 3, h, hd, dtype=wl.dtype, device=device)
+            for m, x in enumerate((self.Q, self.K, self.V)):
+                self.qkv[:, :, m] = x.view(b, h, n, hd).permute(0, 2, 1, 3)
+            self.dqkv = torch.empty_like(self.qkv)
+            self.Os = torch.empty(b, n, h, hd, dtype=wl.dtype, device=device)
+            self.dOs = self.dO.view(b, h, n, hd).permute(0, 2, 1, 3).contiguous()
+            kw = dict(qkv_row_stride=3 * h * hd, out_row_stride=h * hd)
+        else:
+            raise ValueError(feature)
+        self.d = swab.Desc(wl.b, wl.h, wl.n, wl.head_dim, wl.w, wl.w_upper, wl.dilation,
+                           wl.padding, wl.dtype, **kw)
+
+    def launches(self):
+        if self.feature != "strided qkv":
+            return super().launches()
+        s, d, sc = self.swab, self.d, self.wl.scale
+        Q, K, V = (self.qkv[:, :, m] for m in range(3))
+        dQ, dK, dV = (self.dqkv[:, :, m] for m in range(3))
+        return [
+            lambda: s.band_attention(d, sc, Q, K, V, self.Os, self.lse),
+            lambda: s.band_attention_bwd(d, sc, Q, K, V, self.Os, self.dOs, self.lse, dQ, dK, dV,
+                                         self.ws),
+        ]
+
+
+def time_graph(fn, steps, warmup, flush):
+    """Mean device time (ms) of one call captured into a CUDA graph, L2 flushed
+    before every timed replay."""
+    for _ in range(warmup):
+        flush_l2(flush)
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush_l2(flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.mean(ts)
+
+
+def prologue_and_globals(device, steps, flush, peaks):
+    """add_bias_transpose on the merged Q, K, V projection of the Longformer-base
+    shape, and the global queries with their own projections on the training
+    shape (b = 12, h = 12, n = 4096, 16 global tokens, bf16)."""
+    import sliding_window_attention_band_gb300 as swab
+
+    out = {}
+    wl = WORKLOADS[MAIN_CFG]
+    g = torch.Generator().manual_seed(5)
+    X = torch.randn(wl.b, wl.n, 3, wl.h, wl.head_dim, generator=g).to(wl.dtype).to(device)
+    bias = torch.randn(3, wl.h, wl.head_dim, generator=g).to(wl.dtype).to(device)
+    Y = torch.empty(3, wl.b, wl.h, wl.n, wl.head_dim, dtype=wl.dtype, device=device)
+    d = swab.Desc(wl.b, wl.h, wl.n, wl.head_dim, wl.w, wl.w_upper, dtype=wl.dtype)
+    ms = time_graph(lambda: swab.add_bias_transpose(d, X, bias, Y), steps, 3, flush)
+    nbytes = 2 * X.numel() * X.element_size() + bias.numel() * bias.element_size()
+    out[f"add_bias_transpose:{wl.name}"] = {
+        "ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
+        "roofline_frac": round(nbytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3), 4),
+        "bytes": nbytes}
+    w4 = WORKLOADS[4]
+    dg = swab.Desc.from_workload(w4)
+    G, BH, n = dg.G, w4.BH, w4.n
+    mk = lambda *sh: torch.randn(*sh, generator=g).to(w4.dtype).to(device)  # noqa: E731
+    Qg, dOg, Kg, Vg = mk(BH, G, 64), mk(BH, G, 64), mk(BH, n, 64), mk(BH, n, 64)
+    Og, dQg, dKg, dVg = (torch.empty_like(x) for x in (Qg, Qg, Kg, Vg))
+    lseg = torch.empty(BH, G, dtype=torch.float32, device=device)
+    ws = torch.empty(swab.global_attention_workspace(dg) // 4 + 4, dtype=torch.float32,
+                     device=device)
+    fwd = time_graph(lambda: swab.global_attention(dg, w4.scale, Qg, Kg, Vg, Og, lseg, ws),
+                     steps, 3, flush)
+    bwd = time_graph(lambda: swab.global_attention_bwd(dg, w4.scale, Qg, Kg, Vg, Og, dOg, lseg,
+                                                       dQg, dKg, dVg, ws), steps, 3, flush)
+    es = Kg.element_size()
+    fb = 2 * BH * n * 64 * es                      # Kg, Vg read
+    bb = 2 * fb                                    # Kg, Vg read, dKg, dVg written
+    out[f"global_attention:{w4.name}"] = {
+        "fwd_ms": round(fwd, 4), "bwd_ms": round(bwd, 4),
+        "fwd_tflops": round(4.0 * BH * G * n * 64 / (fwd * 1e-3) / 1e12, 2),
+        "bwd_tflops": round(10.0 * BH * G * n * 64 / (bwd * 1e-3) / 1e12, 2),
+        "bound": "hbm", "fwd_roofline_frac": round(fb / (peaks["hbm_gbs"] * 1e9) / (fwd * 1e-3), 4),
+        "bwd_roofline_frac": round(bb / (peaks["hbm_gbs"] * 1e9) / (bwd * 1e-3), 4),
+        "note": "FFMA kernels (G = 16 is one dimension of every product)"}
+    return out
+
+
 def step_summary(wl, step, per_step, per_kernel, peaks):
     return {"ms_per_step": round(statistics.mean(per_step), 4),
             "tflops": round(step_flops(wl) / (statistics.mean(per_step) * 1e-3) / 1e12, 3),
@@ -571,6 +686,12 @@ def main():
     if not args.no_also:
         wl5 = WORKLOADS[5]
         also[f"band_attention:{wl5.name}"] = fused_forward(wl5, device, n_also, 3, flush, peaks)
+        for feature in ("dropout p=0.1", "key bias", "strided qkv"):
+            st = FusedVariantStep(wl, device, feature)
+            ps, pk = time_steps(st, n_also, 3, flush)
+            also[f"fused+{feature.replace(' ', '_')}:{wl.name}"] = step_summary(wl, st, ps, pk, peaks)
+            del st
+        also.update(prologue_and_globals(device, n_also, flush, peaks))
     if swab.device_status(reset=True) != 0:
         raise SystemExit("a kernel raised the device status word during the benchmark")
 
