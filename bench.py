@@ -307,7 +307,7 @@ def prologue_and_globals(device, steps, flush, peaks):
         "bwd_tflops": round(10.0 * BH * G * n * 64 / (bwd * 1e-3) / 1e12, 2),
         "bound": "hbm", "fwd_roofline_frac": round(fb / (peaks["hbm_gbs"] * 1e9) / (fwd * 1e-3), 4),
         "bwd_roofline_frac": round(bb / (peaks["hbm_gbs"] * 1e9) / (bwd * 1e-3), 4),
-        "note": "FFMA kernels (G = 16 is one dimension of every product)"}
+        "note": "tcgen05 kernels, one CTA per 128-key tile (keys as the M dimension)"}
     return out
 
 

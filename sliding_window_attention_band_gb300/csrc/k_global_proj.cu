@@ -7,14 +7,17 @@
 //   backward: delta_g = dOg[g].Og[g];  ds_gj = p_gj (dOg[g].Vg[j] - delta_g)
 //             dQg = scale ds Kg,  dKg = scale ds^T Qg,  dVg = p^T dOg
 //
-// G is a handful of tokens, so every product has G as one dimension and costs
-// G * n * 64 multiply-adds per slice: FFMA with fp32 operands staged in shared
-// memory (a 16-query chunk against 64-key tiles).  Parallelism comes from the
-// keys: the forward splits them into chunks of kChunkKeys with per-chunk
-// partial (max, sum, accumulator) merged by a second kernel; the backward
-// gives each CTA one 64-key tile and every global query, so dKg, dVg rows have
-// one writer, and its dQg partials are summed by a second kernel.  Both
-// partial sets live in the caller's workspace.
+// G is a handful of tokens, so every product has G as one dimension.  The
+// 16-bit paths run on the tensor cores with the keys as the M dimension: one
+// CTA per (128-key tile, slice) computes S^T = Kg Qg^T (N = 16 queries per
+// chunk) into tensor memory; the forward writes a (max, sum, output) partial
+// per tile that a second kernel merges, the backward forms dVg, dKg (one
+// writer per key row) and per-tile dQg partials summed by a second kernel in
+// a fixed order.  fp32 runs FFMA kernels on operands staged in shared memory
+// (256-key chunks in the forward, 64-key tiles in the backward).  Partials
+// live in the caller's workspace.
+#include <type_traits>
+
 #include "swab_internal.h"
 
 namespace swab {
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) k_gproj_combine(const GlobalProjArgs
 }
 
 // ---------------------------------------------------------------------------
-// backward: CTA (key tile, slice) over every global query
+// backward, fp32 operands (FFMA): CTA (64-key tile, slice) over every global query
 // ---------------------------------------------------------------------------
 // shared memory of the backward (floats): K, V tiles; Qg, dOg chunks; p, ds
 // of the chunk; lse, delta of the chunk
@@ -367,6 +370,463 @@ __global__ void __launch_bounds__(kThreads) k_gproj_bwd(const GlobalProjArgs p) 
     }
 }
 
+// ---------------------------------------------------------------------------
+// backward on the tensor cores: CTA (128-key tile, slice), every global query
+// in chunks of 16.  With the keys as the M dimension every product has a
+// tcgen05 shape (M = 128):
+//   S^T  = Kg Qg_c^T,  dP^T = Vg dOg_c^T          (N = 16, K = 64)
+//   dVg += P_c^T dOg_c, dKg += dS_c^T Qg_c         (N = 64, K = 16)
+//   dQg_c^T = Kg^T dS_c                           (K = 128 keys; Kg read as an
+//        MN-major A of 128 rows whose second 64-row block is the V tile: those
+//        32 output lanes are never read)
+// Warp 0 loads (TMA), warp 1 owns tensor memory and issues the products,
+// warps 2-5 (lane = key) turn S^T, dP^T into P and dS and read the results.
+// ---------------------------------------------------------------------------
+constexpr int kTcThreads = 192;
+constexpr int kTcKeys = 128;
+constexpr uint32_t kTcTmemCols = 256;
+constexpr uint32_t kColS = 0, kColDP = 16, kColDQ = 32, kColDV = 64, kColDK = 128;
+constexpr int kTile16 = kTcKeys * 128;   // a 128 x 64 16-bit tile, bytes
+
+// shared memory of the tensor-core backward for nch query chunks (bytes)
+__host__ __device__ constexpr int tc_bwd_smem(int nch) {
+    return 1024 /* alignment */ + 2 * kTile16 /* K, V */ + 2 * nch * 2048 /* Qg, dOg */ +
+           2 * kTile16 /* P, dS (keys x queries) */ + 2 * 2048 /* dS (queries x keys) */ +
+           2 * 256 * 4 /* lse, delta */ + 256 /* barriers, flags */;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_gproj_bwd_tc(const __grid_constant__ TmapSet mapK, const __grid_constant__ TmapSet mapV,
+                   const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapO,
+                   const GlobalProjArgs p) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const int G = p.G, n = p.n, nch = (G + kGC - 1) / kGC;
+    uint8_t *kbuf = base;                    // K tile; the V tile follows at +kTile16
+    uint8_t *vbuf = kbuf + kTile16;
+    uint8_t *qbuf = vbuf + kTile16;          // [nch] Qg chunks, 16 rows x 128 B
+    uint8_t *obuf = qbuf + nch * 2048;       // [nch] dOg chunks
+    uint8_t *pa = obuf + nch * 2048;         // P  [128 keys][16 queries], 128-B swizzled rows
+    uint8_t *dsa = pa + kTile16;             // dS [128 keys][16 queries]
+    uint8_t *dsb = dsa + kTile16;            // dS [16 queries][128 keys]: two 64-key blocks
+    float *lse2 = reinterpret_cast<float *>(dsb + 2 * 2048);   // [256] lse * log2e
+    float *del = lse2 + 256;                                    // [256] delta
+    uint64_t *bars = reinterpret_cast<uint64_t *>(del + 256);
+    uint64_t *ldfull = bars, *sfull = bars + 1, *pfull = bars + 2, *qfull = bars + 3, *qdone = bars + 4;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 6);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *no_abort = reinterpret_cast<volatile int *>(tmem_holder + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kt = blockIdx.x, bh = blockIdx.y, j0 = kt * kTcKeys;
+    if (threadIdx.x == 0) {
+        mbar_init(ldfull, 1);
+        mbar_init(sfull, 1);
+        mbar_init(pfull, 128);
+        mbar_init(qfull, 1);
+        mbar_init(qdone, 128);
+        mbar_init(qdone + 1, 1);   // every product complete
+        *abort_flag = 0;
+        *no_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTcTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ---------------- loads: the key tile and every query chunk, once ----------------
+        if (lane == 0) {
+            mbar_arrive_expect_tx(ldfull, 2 * kTile16 + 2 * nch * 2048);
+            tma_load_3d(kbuf, &mapK.m[0], ldfull, 0, j0, bh);
+            tma_load_3d(vbuf, &mapV.m[0], ldfull, 0, j0, bh);
+            for (int c = 0; c < nch; ++c) {
+                tma_load_3d(qbuf + c * 2048, &mapQ.m[0], ldfull, 0, c * kGC, bh);
+                tma_load_3d(obuf + c * 2048, &mapO.m[0], ldfull, 0, c * kGC, bh);
+            }
+        }
+        __syncwarp();
+        // the copies land before the CTA may exit
+        mbar_wait(ldfull, 0, no_abort, nullptr, 100000000ull);
+    } else if (warp == 1) {
+        // ---------------- products (lane 0 issues) ----------------
+        constexpr bool kBf16 = !std::is_same<T, __half>::value;
+        constexpr uint32_t id_s = idesc_f16(kTcKeys, kGC, kBf16, false, false);   // S^T, dP^T
+        constexpr uint32_t id_g = idesc_f16(kTcKeys, 64, kBf16, false, true);     // dV, dK
+        constexpr uint32_t id_q = idesc_f16(kTcKeys, kGC, kBf16, true, false);    // dQ^T
+        const uint64_t d_k = sdesc_sw128(smem_u32(kbuf), 16, 1024);
+        const uint64_t d_v = sdesc_sw128(smem_u32(vbuf), 16, 1024);
+        const uint64_t d_kmn = sdesc_sw128(smem_u32(kbuf), kTile16, 1024);   // K^T, MN-major A
+        const uint64_t d_pa = sdesc_sw128(smem_u32(pa), 16, 1024);
+        const uint64_t d_dsa = sdesc_sw128(smem_u32(dsa), 16, 1024);
+        const uint64_t d_dsb = sdesc_sw128(smem_u32(dsb), 16, 1024);
+        ok = __all_sync(0xffffffffu, mbar_wait(ldfull, 0, abort_flag, p.err));
+        for (int c = 0; c < nch && ok; ++c) {
+            if (c > 0 && !__all_sync(0xffffffffu, mbar_wait(qdone, (c - 1) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t qoff = (uint64_t)((c * 2048) >> 4);
+            const uint64_t d_q = sdesc_sw128(smem_u32(qbuf), 16, 1024) + qoff;
+            const uint64_t d_o = sdesc_sw128(smem_u32(obuf), 16, 1024) + qoff;
+            const uint64_t d_qmn = sdesc_sw128(smem_u32(qbuf), 1024, 1024) + qoff;
+            const uint64_t d_omn = sdesc_sw128(smem_u32(obuf), 1024, 1024) + qoff;
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    mma_f16_ss(tmem + kColS, d_k + 2 * k, d_q + 2 * k, id_s, k > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + kColDP, d_v + 2 * k, d_o + 2 * k, id_s, k > 0 ? 1u : 0u);
+                }
+                mma_commit(sfull);
+            }
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, mbar_wait(pfull, c & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                mma_f16_ss(tmem + kColDV, d_pa, d_omn, id_g, c > 0 ? 1u : 0u);
+                mma_f16_ss(tmem + kColDK, d_dsa, d_qmn, id_g, c > 0 ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < kTcKeys / 16; ++k) {
+                    const uint64_t a = d_kmn + (uint64_t)((2048 * k) >> 4);
+                    const uint64_t b = d_dsb + (uint64_t)((((k >> 2) * 2048) + (k & 3) * 32) >> 4);
+                    mma_f16_ss(tmem + kColDQ, a, b, id_q, k > 0 ? 1u : 0u);
+                }
+                mma_commit(qfull);
+            }
+            __syncwarp();
+        }
+        // the products issued complete before tensor memory is freed
+        if (lane == 0) mma_commit(qdone + 1);
+        __syncwarp();
+    } else {
+        // ---------------- workers: lane = key m of the tile ----------------
+        const int quarter = warp & 3, m = quarter * 32 + lane, t = threadIdx.x - 64;
+        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
+        const T *Og = reinterpret_cast<const T *>(p.Og) + (long long)bh * G * 64;
+        const T *dOg = reinterpret_cast<const T *>(p.dOg) + (long long)bh * G * 64;
+        for (int gg = t; gg < G; gg += 128) {
+            lse2[gg] = p.lseg[(long long)bh * G + gg] * kLog2e;
+            float d = 0.f;
+            for (int c = 0; c < 64; ++c)
+                d = fmaf(Elt<T>::to_f(Og[(long long)gg * 64 + c]), Elt<T>::to_f(dOg[(long long)gg * 64 + c]), d);
+            del[gg] = d;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // the workers' lse, delta
+        const bool kvalid = j0 + m < n;
+        const float xs = p.scale * kLog2e;
+        const uint32_t pa_row = smem_u32(pa) + m * 128, dsa_row = smem_u32(dsa) + m * 128;
+        for (int c = 0; c < nch && ok; ++c) {
+            if (!__all_sync(0xffffffffu, mbar_wait(sfull, c & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[16], dv[16];
+            tmem_ld16(lane_base + kColS, sv);
+            tmem_ld16(lane_base + kColDP, dv);
+            tmem_ld_wait();
+            float pv[16], dsv[16];
+#pragma unroll
+            for (int q = 0; q < kGC; ++q) {
+                const int gg = c * kGC + q;
+                const bool live = kvalid && gg < G;
+                const float pr = live ? ex2(__uint_as_float(sv[q]) * xs - lse2[gg < G ? gg : 0]) : 0.f;
+                pv[q] = pr;
+                dsv[q] = pr * (__uint_as_float(dv[q]) - (gg < G ? del[gg] : 0.f));
+            }
+            // P and dS rows (queries 0-15 of the chunk: the first two 16-byte
+            // pieces of the row, swizzled), and dS as [query][key]
+            sts16(pa_row + ((0 ^ (m & 7)) << 4), make_uint4(pack2<T>(pv[0], pv[1]), pack2<T>(pv[2], pv[3]),
+                                                            pack2<T>(pv[4], pv[5]), pack2<T>(pv[6], pv[7])));
+            sts16(pa_row + ((1 ^ (m & 7)) << 4), make_uint4(pack2<T>(pv[8], pv[9]), pack2<T>(pv[10], pv[11]),
+                                                            pack2<T>(pv[12], pv[13]), pack2<T>(pv[14], pv[15])));
+            sts16(dsa_row + ((0 ^ (m & 7)) << 4), make_uint4(pack2<T>(dsv[0], dsv[1]), pack2<T>(dsv[2], dsv[3]),
+                                                             pack2<T>(dsv[4], dsv[5]), pack2<T>(dsv[6], dsv[7])));
+            sts16(dsa_row + ((1 ^ (m & 7)) << 4), make_uint4(pack2<T>(dsv[8], dsv[9]), pack2<T>(dsv[10], dsv[11]),
+                                                             pack2<T>(dsv[12], dsv[13]), pack2<T>(dsv[14], dsv[15])));
+            {
+                uint16_t *blk = reinterpret_cast<uint16_t *>(dsb + (m >> 6) * 2048);
+                const int col = m & 63;   // key within the 64-key block
+#pragma unroll
+                for (int q = 0; q < kGC; q += 2) {
+                    const uint32_t w2 = pack2<T>(dsv[q], dsv[q + 1]);
+                    blk[q * 64 + ((((col >> 3) ^ (q & 7))) << 3) + (col & 7)] = (uint16_t)(w2 & 0xffffu);
+                    blk[(q + 1) * 64 + ((((col >> 3) ^ ((q + 1) & 7))) << 3) + (col & 7)] = (uint16_t)(w2 >> 16);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(pfull);
+            if (!__all_sync(0xffffffffu, mbar_wait(qfull, c & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (quarter < 2) {   // TMEM lanes 0-63: the 64 channels of dQ^T
+                uint32_t qv[16];
+                tmem_ld16(lane_base + kColDQ, qv);
+                tmem_ld_wait();
+                float *part = p.ws + ((long long)bh * p.nchunks + kt) * G * 64 + m;
+#pragma unroll
+                for (int q = 0; q < kGC; ++q) {
+                    const int gg = c * kGC + q;
+                    if (gg < G) part[(long long)gg * 64] = p.scale * __uint_as_float(qv[q]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(qdone);
+        }
+        // dV, dK rows of this key (the last chunk's products are complete)
+        if (ok) {
+            tc_fence_after();
+            T *dV = reinterpret_cast<T *>(p.dVg) + ((long long)bh * n + j0 + m) * 64;
+            T *dK = reinterpret_cast<T *>(p.dKg) + ((long long)bh * n + j0 + m) * 64;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const float mul = which ? p.scale : 1.f;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_base + (which ? kColDK : kColDV) + 32 * h, v);
+                    tmem_ld_wait();
+                    if (kvalid) {
+                        uint4 *o4 = reinterpret_cast<uint4 *>((which ? dK : dV) + 32 * h);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            o4[u] = make_uint4(
+                                pack2<T>(mul * __uint_as_float(v[8 * u]), mul * __uint_as_float(v[8 * u + 1])),
+                                pack2<T>(mul * __uint_as_float(v[8 * u + 2]), mul * __uint_as_float(v[8 * u + 3])),
+                                pack2<T>(mul * __uint_as_float(v[8 * u + 4]), mul * __uint_as_float(v[8 * u + 5])),
+                                pack2<T>(mul * __uint_as_float(v[8 * u + 6]), mul * __uint_as_float(v[8 * u + 7])));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        // every product issued has completed (its commit arrived) before the free
+        mbar_wait(qdone + 1, 0, no_abort, nullptr, 100000000ull);
+        __syncwarp();
+        tmem_dealloc(tmem, kTcTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// forward on the tensor cores: CTA (128-key tile, slice), every global query
+// in chunks of 16.  S^T = Kg Qg_c^T (M = 128 keys, N = 16); the workers (lane
+// = key) take each query's max and sum over the tile's keys, write
+// P = 2^(s - max) as [query][key], and O_c^T = Vg^T P (K = 128 keys; Vg read as
+// an MN-major A of 128 rows whose second 64-row block is the K tile stored
+// right after it: those output lanes are never read) gives the tile's
+// unnormalised output.  The partial (max, sum,
+// output) of every (slice, tile, query) goes to the workspace; the combine
+// kernel merges the tiles.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kFColS = 0, kFColO = 32;
+
+__host__ __device__ constexpr int tc_fwd_smem(int nch) {
+    return 1024 + 2 * kTile16 /* K, V */ + nch * 2048 /* Qg */ + 2 * 2048 /* P [query][key] */ +
+           2 * 4 * kGC * 4 /* per-warp max, sum */ + 256;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_gproj_fwd_tc(const __grid_constant__ TmapSet mapK, const __grid_constant__ TmapSet mapV,
+                   const __grid_constant__ TmapSet mapQ, const GlobalProjArgs p) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const int G = p.G, n = p.n, nch = (G + kGC - 1) / kGC;
+    uint8_t *vbuf = base;                    // V tile; the K tile follows at +kTile16
+    uint8_t *kbuf = vbuf + kTile16;
+    uint8_t *qbuf = kbuf + kTile16;          // [nch] Qg chunks
+    uint8_t *pb = qbuf + nch * 2048;         // P [16 queries][128 keys]: two 64-key blocks
+    float *wmax = reinterpret_cast<float *>(pb + 2 * 2048);   // [4 warps][16]
+    float *wsum = wmax + 4 * kGC;                               // [4 warps][16]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(wsum + 4 * kGC);
+    uint64_t *ldfull = bars, *sfull = bars + 1, *pfull = bars + 2, *ofull = bars + 3, *odone = bars + 4,
+             *alldone = bars + 5;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 6);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *no_abort = reinterpret_cast<volatile int *>(tmem_holder + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kt = blockIdx.x, bh = blockIdx.y, j0 = kt * kTcKeys;
+    if (threadIdx.x == 0) {
+        mbar_init(ldfull, 1);
+        mbar_init(sfull, 1);
+        mbar_init(pfull, 128);
+        mbar_init(ofull, 1);
+        mbar_init(odone, 128);
+        mbar_init(alldone, 1);
+        *abort_flag = 0;
+        *no_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTcTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    bool ok = true;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(ldfull, 2 * kTile16 + nch * 2048);
+            tma_load_3d(kbuf, &mapK.m[0], ldfull, 0, j0, bh);
+            tma_load_3d(vbuf, &mapV.m[0], ldfull, 0, j0, bh);
+            for (int c = 0; c < nch; ++c) tma_load_3d(qbuf + c * 2048, &mapQ.m[0], ldfull, 0, c * kGC, bh);
+        }
+        __syncwarp();
+        mbar_wait(ldfull, 0, no_abort, nullptr, 100000000ull);
+    } else if (warp == 1) {
+        constexpr bool kBf16 = !std::is_same<T, __half>::value;
+        constexpr uint32_t id_s = idesc_f16(kTcKeys, kGC, kBf16, false, false);   // S^T
+        constexpr uint32_t id_o = idesc_f16(kTcKeys, kGC, kBf16, true, false);    // O^T
+        const uint64_t d_k = sdesc_sw128(smem_u32(kbuf), 16, 1024);
+        const uint64_t d_vmn = sdesc_sw128(smem_u32(vbuf), kTile16, 1024);   // V^T, MN-major A
+        const uint64_t d_pb = sdesc_sw128(smem_u32(pb), 16, 1024);
+        ok = __all_sync(0xffffffffu, mbar_wait(ldfull, 0, abort_flag, p.err));
+        for (int c = 0; c < nch && ok; ++c) {
+            if (c > 0 && !__all_sync(0xffffffffu, mbar_wait(odone, (c - 1) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t d_q = sdesc_sw128(smem_u32(qbuf), 16, 1024) + (uint64_t)((c * 2048) >> 4);
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mma_f16_ss(tmem + kFColS, d_k + 2 * k, d_q + 2 * k, id_s, k > 0 ? 1u : 0u);
+                mma_commit(sfull);
+            }
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, mbar_wait(pfull, c & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < kTcKeys / 16; ++k) {
+                    const uint64_t a = d_vmn + (uint64_t)((2048 * k) >> 4);
+                    const uint64_t b = d_pb + (uint64_t)((((k >> 2) * 2048) + (k & 3) * 32) >> 4);
+                    mma_f16_ss(tmem + kFColO, a, b, id_o, k > 0 ? 1u : 0u);
+                }
+                mma_commit(ofull);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) mma_commit(alldone);
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3, wi = warp - 2, m = quarter * 32 + lane, t = threadIdx.x - 64;
+        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
+        const bool kvalid = j0 + m < n;
+        const float xs = p.scale * kLog2e;
+        for (int c = 0; c < nch && ok; ++c) {
+            if (!__all_sync(0xffffffffu, mbar_wait(sfull, c & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[16];
+            tmem_ld16(lane_base + kFColS, sv);
+            tmem_ld_wait();
+            float x[16];
+#pragma unroll
+            for (int q = 0; q < kGC; ++q) x[q] = kvalid ? __uint_as_float(sv[q]) * xs : -INFINITY;
+            // max over the tile's 128 keys of every query: warp, then the 4 warps
+#pragma unroll
+            for (int q = 0; q < kGC; ++q) {
+                float v = x[q];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                if (lane == q) wmax[wi * kGC + q] = v;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            float pr[16];
+#pragma unroll
+            for (int q = 0; q < kGC; ++q) {
+                const float mx = max3(wmax[q], wmax[kGC + q], fmaxf(wmax[2 * kGC + q], wmax[3 * kGC + q]));
+                pr[q] = ex2(x[q] - mx);   // 0 for keys past the end (the tile has one key < n)
+            }
+            // P as [query][key] (two 64-key blocks, 128-byte swizzled rows)
+            {
+                uint16_t *blk = reinterpret_cast<uint16_t *>(pb + (m >> 6) * 2048);
+                const int col = m & 63;
+#pragma unroll
+                for (int q = 0; q < kGC; q += 2) {
+                    const uint32_t w2 = pack2<T>(pr[q], pr[q + 1]);
+                    blk[q * 64 + ((((col >> 3) ^ (q & 7))) << 3) + (col & 7)] = (uint16_t)(w2 & 0xffffu);
+                    blk[(q + 1) * 64 + ((((col >> 3) ^ ((q + 1) & 7))) << 3) + (col & 7)] = (uint16_t)(w2 >> 16);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(pfull);
+            // sums over the keys (of the fp32 values; the product uses them rounded)
+#pragma unroll
+            for (int q = 0; q < kGC; ++q) {
+                float v = pr[q];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == q) wsum[wi * kGC + q] = v;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            // the partial of (slice, tile, query): [max (log2 units), sum, O[64]]
+            float *part = p.ws + ((long long)bh * p.nchunks + kt) * G * 66;
+            if (t < kGC && c * kGC + t < G) {
+                const int gg = c * kGC + t;
+                part[(long long)gg * 66] = max3(wmax[t], wmax[kGC + t], fmaxf(wmax[2 * kGC + t], wmax[3 * kGC + t]));
+                part[(long long)gg * 66 + 1] = (wsum[t] + wsum[kGC + t]) + (wsum[2 * kGC + t] + wsum[3 * kGC + t]);
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(ofull, c & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (quarter < 2) {   // TMEM lanes 0-63: the 64 channels of O^T
+                uint32_t ov[16];
+                tmem_ld16(lane_base + kFColO, ov);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < kGC; ++q) {
+                    const int gg = c * kGC + q;
+                    if (gg < G) part[(long long)gg * 66 + 2 + m] = __uint_as_float(ov[q]);
+                }
+            }
+            tc_fence_before();
+            // the next chunk's maxima and sums overwrite these slots
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            mbar_arrive(odone);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        mbar_wait(alldone, 0, no_abort, nullptr, 100000000ull);
+        __syncwarp();
+        tmem_dealloc(tmem, kTcTmemCols);
+    }
+}
+
 // dQg = sum of the key tiles' partials (fixed order): a thread per (slice,
 // query, channel), eight loads in flight
 template <typename T>
@@ -404,6 +864,40 @@ cudaError_t launch_fwd_t(GlobalProjArgs a, cudaStream_t st) {
 }
 
 template <typename T>
+cudaError_t launch_fwd_tc_t(const TmapSet &mk, const TmapSet &mv, const TmapSet &mq, GlobalProjArgs a,
+                            cudaStream_t st) {
+    a.nchunks = (a.n + kTcKeys - 1) / kTcKeys;
+    const int nch = (a.G + kGC - 1) / kGC;
+    const size_t smem = (size_t)max(tc_fwd_smem(nch), 80 * 1024);   // two CTAs per SM (TMEM)
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gproj_fwd_tc<T>), smem);
+    if (e != cudaSuccess) return e;
+    k_gproj_fwd_tc<T><<<dim3(a.nchunks, a.BH), kTcThreads, smem, st>>>(mk, mv, mq, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long warps = (long long)a.BH * a.G;
+    const long long per_block = kThreads / 32;
+    k_gproj_combine<T><<<(unsigned)((warps + per_block - 1) / per_block), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_bwd_tc_t(const TmapSet &mk, const TmapSet &mv, const TmapSet &mq, const TmapSet &mo,
+                            GlobalProjArgs a, cudaStream_t st) {
+    a.nchunks = (a.n + kTcKeys - 1) / kTcKeys;
+    const int nch = (a.G + kGC - 1) / kGC;
+    // at least 80 KB: two CTAs per SM, as many as tensor memory holds (256 columns each)
+    const size_t smem = (size_t)max(tc_bwd_smem(nch), 80 * 1024);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gproj_bwd_tc<T>), smem);
+    if (e != cudaSuccess) return e;
+    k_gproj_bwd_tc<T><<<dim3(a.nchunks, a.BH), kTcThreads, smem, st>>>(mk, mv, mq, mo, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long outs = (long long)a.BH * a.G * 64;
+    k_gproj_dq<T><<<(unsigned)((outs + kThreads - 1) / kThreads), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
 cudaError_t launch_bwd_t(GlobalProjArgs a, cudaStream_t st) {
     a.nchunks = (a.n + kKT - 1) / kKT;
     const dim3 grid(a.nchunks, a.BH);
@@ -421,9 +915,26 @@ cudaError_t launch_bwd_t(GlobalProjArgs a, cudaStream_t st) {
 }  // namespace
 
 size_t global_proj_workspace_bytes(long long BH, int G, int n) {
-    const size_t fwd = (size_t)BH * ((n + kChunkKeys - 1) / kChunkKeys) * G * 66 * sizeof(float);
+    // forward partials per 128-key tile (tensor cores) or 256-key chunk (FFMA)
+    const size_t fwd = (size_t)BH * ((n + kTcKeys - 1) / kTcKeys) * G * 66 * sizeof(float);
     const size_t bwd = (size_t)BH * ((n + kKT - 1) / kKT) * G * 64 * sizeof(float);
     return fwd > bwd ? fwd : bwd;
+}
+
+cudaError_t launch_global_proj_bwd_tc(DType dt, const TmapSet &mk, const TmapSet &mv, const TmapSet &mq,
+                                      const TmapSet &mo, const GlobalProjArgs &a, cudaStream_t st) {
+    if (a.BH > 65535 || a.G > 256) return cudaErrorInvalidValue;
+    if (dt == kF16) return launch_bwd_tc_t<__half>(mk, mv, mq, mo, a, st);
+    if (dt == kBF16) return launch_bwd_tc_t<__nv_bfloat16>(mk, mv, mq, mo, a, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_global_proj_fwd_tc(DType dt, const TmapSet &mk, const TmapSet &mv, const TmapSet &mq,
+                                      const GlobalProjArgs &a, cudaStream_t st) {
+    if (a.BH > 65535 || a.G > 256) return cudaErrorInvalidValue;
+    if (dt == kF16) return launch_fwd_tc_t<__half>(mk, mv, mq, a, st);
+    if (dt == kBF16) return launch_fwd_tc_t<__nv_bfloat16>(mk, mv, mq, a, st);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_global_proj(DType dt, const GlobalProjArgs &a, bool bwd, cudaStream_t st) {

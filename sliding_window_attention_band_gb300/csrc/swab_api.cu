@@ -486,7 +486,19 @@ SWAB_API swab_status global_attention(const swab_desc *desc, float scale, const 
     a.Og = Og;
     a.lseg = lseg;
     a.ws = static_cast<float *>(workspace);
-    return from_cuda(launch_global_proj(dt, a, false, as_stream(stream)));
+    if (dt == kF32) return from_cuda(launch_global_proj(dt, a, false, as_stream(stream)));
+    Geom gk{}, gq{};
+    gk.BH = gq.BH = (int)a.BH;
+    gk.s = gq.s = 1;
+    gk.n = a.n;
+    gq.n = a.G;
+    TmapSet mk, mv, mq;
+    if (!build_rows_maps(&mk, Kg, gk, dt, 128) || !build_rows_maps(&mv, Vg, gk, dt, 128) ||
+        !build_rows_maps(&mq, Qg, gq, dt, 16))
+        return SWAB_ERR_CUDA;
+    a.err = status_word();
+    if (!a.err) return SWAB_ERR_CUDA;
+    return from_cuda(launch_global_proj_fwd_tc(dt, mk, mv, mq, a, as_stream(stream)));
 }
 
 SWAB_API swab_status global_attention_bwd(const swab_desc *desc, float scale, const void *Qg,
@@ -508,7 +520,20 @@ SWAB_API swab_status global_attention_bwd(const swab_desc *desc, float scale, co
     a.dKg = dKg;
     a.dVg = dVg;
     a.ws = static_cast<float *>(workspace);
-    return from_cuda(launch_global_proj(dt, a, true, as_stream(stream)));
+    if (dt == kF32) return from_cuda(launch_global_proj(dt, a, true, as_stream(stream)));
+    // tensor-core path: [n, 64] slices of Kg, Vg and [G, 64] slices of Qg, dOg
+    Geom gk{}, gq{};
+    gk.BH = gq.BH = (int)a.BH;
+    gk.s = gq.s = 1;
+    gk.n = a.n;
+    gq.n = a.G;
+    TmapSet mk, mv, mq, mo;
+    if (!build_rows_maps(&mk, Kg, gk, dt, 128) || !build_rows_maps(&mv, Vg, gk, dt, 128) ||
+        !build_rows_maps(&mq, Qg, gq, dt, 16) || !build_rows_maps(&mo, dOg, gq, dt, 16))
+        return SWAB_ERR_CUDA;
+    a.err = status_word();
+    if (!a.err) return SWAB_ERR_CUDA;
+    return from_cuda(launch_global_proj_bwd_tc(dt, mk, mv, mq, mo, a, as_stream(stream)));
 }
 
 // Largest band the softmax kernels take with dropout: the per-row keep bits

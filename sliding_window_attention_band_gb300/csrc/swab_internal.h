@@ -184,9 +184,17 @@ struct GlobalProjArgs {   // global queries with their own projections
     void *dQg, *dKg, *dVg; // bwd outputs
     float *ws;             // workspace (partials)
     int nchunks;           // set by the launcher
+    unsigned *err;         // device status word (tensor-core backward)
 };
 size_t global_proj_workspace_bytes(long long BH, int G, int n);
 cudaError_t launch_global_proj(DType dt, const GlobalProjArgs &a, bool bwd, cudaStream_t st);
+// tensor-core forward (f16 / bf16): maps of Kg, Vg (128-row boxes) and Qg (16-row boxes)
+cudaError_t launch_global_proj_fwd_tc(DType dt, const TmapSet &mk, const TmapSet &mv, const TmapSet &mq,
+                                      const GlobalProjArgs &a, cudaStream_t st);
+// tensor-core backward (f16 / bf16): maps of Kg, Vg (128-row boxes) and of
+// Qg, dOg (16-row boxes), one slice per third coordinate
+cudaError_t launch_global_proj_bwd_tc(DType dt, const TmapSet &mk, const TmapSet &mv, const TmapSet &mq,
+                                      const TmapSet &mo, const GlobalProjArgs &a, cudaStream_t st);
 
 cudaError_t launch_band_softmax(DType dt, const SoftmaxArgs &a, cudaStream_t st);
 cudaError_t launch_band_softmax_bwd(DType dt, const SoftmaxArgs &a, cudaStream_t st);
