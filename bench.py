@@ -62,6 +62,25 @@ def valid_pairs(wl) -> int:
     return int((t_hi - t_lo + 1).sum()) * wl.BH
 
 
+def valid_pairs_globals(wl) -> int:
+    """(query, key) pairs with global tokens: a local row's band keys outside G
+    plus the G global keys; a global row's n keys."""
+    s = wl.dilation + 1
+    i = np.arange(wl.n, dtype=np.int64)
+    t_lo = np.maximum(0, wl.w - i // s)
+    t_hi = np.minimum(wl.D - 1, wl.w + (wl.n - 1 - i) // s)
+    per_row = t_hi - t_lo + 1
+    gl = np.array(wl.global_idx, dtype=np.int64)
+    for p_ in gl:   # rows whose band holds global key p_
+        k = np.arange(-wl.w, wl.w_upper + 1, dtype=np.int64)
+        rows = p_ - k * s
+        rows = rows[(rows >= 0) & (rows < wl.n)]
+        per_row[rows] -= 1
+    per_row += len(gl)
+    per_row[gl] = wl.n
+    return int(per_row.sum()) * wl.BH
+
+
 def step_flops(wl) -> float:
     return float(N_CONTRACTIONS * 2 * wl.head_dim * valid_pairs(wl))
 
@@ -286,6 +305,18 @@ def prologue_and_globals(device, steps, flush, peaks):
         "roofline_frac": round(nbytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3), 4),
         "bytes": nbytes}
     w4 = WORKLOADS[4]
+    # the fused forward with global tokens on the training shape
+    Q4, K4, V4 = (x.to(device) for x in workload_inputs(w4, count=3))
+    O4 = torch.empty_like(Q4)
+    lse4 = torch.empty(w4.BH, w4.n, dtype=torch.float32, device=device)
+    d4 = swab.Desc.from_workload(w4)
+    ms4 = time_graph(lambda: swab.band_attention(d4, w4.scale, Q4, K4, V4, O4, lse4), steps, 3, flush)
+    fl4 = 2 * 2.0 * w4.head_dim * valid_pairs_globals(w4)
+    out[f"band_attention+globals:{w4.name}"] = {
+        "ms": round(ms4, 4), "tflops": round(fl4 / (ms4 * 1e-3) / 1e12, 2),
+        "roofline_frac": round(fl4 / (peaks["bf16_tflops"] * 1e12) / (ms4 * 1e-3), 4), "bound": "tensor",
+        "note": "band part (global keys masked) + global columns merged + global rows"}
+    del Q4, K4, V4, O4
     dg = swab.Desc.from_workload(w4)
     G, BH, n = dg.G, w4.BH, w4.n
     mk = lambda *sh: torch.randn(*sh, generator=g).to(w4.dtype).to(device)  # noqa: E731

@@ -254,7 +254,12 @@ SWAB_API swab_status band_softmax_bwd(const swab_desc *desc, const void *P, cons
 
 /* Fused forward: the same O (and lse, may be NULL) as band_qk(scale) ->
  * band_softmax -> band_pv, with the scores kept on chip (never written to
- * memory).  Global tokens are not supported here (n_global must be 0). */
+ * memory).  With global tokens (f16 / bf16, contiguous layout, lse required,
+ * n <= 188416): local rows attend to their band keys outside G plus G, global
+ * rows to every key, as in the materialised calls; computed as the band part
+ * (global keys masked), the global columns merged into the local rows by
+ * log-sum-exp, and the global rows' dense attention.  fp32 or the strided
+ * layout with global tokens: SWAB_ERR_UNSUPPORTED. */
 SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const void *Q,
                                     const void *K, const void *V, void *O, float *lse,
                                     void *stream);

@@ -105,10 +105,11 @@ __device__ __forceinline__ bool decode_tile(const Geom &g, int t, int xt, Tile &
     return true;
 }
 
-template <typename T, bool kBias, bool kDrop>
+template <typename T, bool kBias, bool kDrop, bool kGlob>
 __global__ void __launch_bounds__(kThreads, 1)
     k_band_attention_fwd(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
-                         const __grid_constant__ TmapSet mapV, const AttnArgs p) {
+                         const __grid_constant__ TmapSet mapV, const AttnArgs p,
+                         const __grid_constant__ GlobArgs gl) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -132,11 +133,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *no_abort = reinterpret_cast<volatile int *>(drain);
+    // global tokens: bit j of gbits marks position j as global (the band
+    // excludes those keys; they are attended through their own columns)
+    uint32_t *gbits = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(bars) + 1024);
 
     const Geom &g = p.g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int xt = (g.nsub + kBQ - 1) / kBQ;
     const int ntiles = xt * g.s * g.BH;
+
+    if constexpr (kGlob) {
+        for (int w = threadIdx.x; w < (g.n + 31) / 32; w += kThreads) gbits[w] = 0u;
+        __syncthreads();
+        for (int k = threadIdx.x; k < gl.G; k += kThreads)
+            atomicOr(&gbits[gl.idx[k] >> 5], 1u << (gl.idx[k] & 31));
+        // visible to every thread after the barrier below
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -372,7 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this row's band inside the part: columns [max(jlo,0), min(jhi,31)]
                 const int jlo = max(qq - g.w - kbase, 0);
                 const int jhi = min(min(qq + g.wu, tl.kb_hi) - kbase, 31);
-                const uint32_t vmask = jlo > jhi ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
+                uint32_t vmask = jlo > jhi ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
+                if constexpr (kGlob) {
+                    // column `lane` of the part is key kbase + lane of the residue
+                    const int sub = kbase + lane;
+                    const int key = tl.r + g.s * sub;
+                    const bool isg = sub < tl.nr && ((gbits[key >> 5] >> (key & 31)) & 1u);
+                    vmask &= ~__ballot_sync(0xffffffffu, isg);
+                }
                 const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
                 const bool empty = __all_sync(0xffffffffu, vmask == 0u);
                 // dropout keep bits of this row's 32 keys (one Philox block:
@@ -583,17 +602,20 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
     if (c == 0 && p.lse) p.lse[R] = m + logf(l);
 }
 
-template <typename T, bool kBias, bool kDrop>
+template <typename T, bool kBias, bool kDrop, bool kGlob = false>
 cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const AttnArgs &a,
-                     cudaStream_t st) {
+                     cudaStream_t st, const GlobArgs *gl = nullptr) {
     const long long tiles = (long long)((a.g.nsub + kBQ - 1) / kBQ) * a.g.s * a.g.BH;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(tiles < sms ? tiles : sms);
+    const size_t smem = kSmemBytes + (kGlob ? (size_t)((a.g.n + 31) / 32) * 4 : 0);
     cudaError_t e =
-        ensure_smem(reinterpret_cast<const void *>(k_band_attention_fwd<T, kBias, kDrop>), kSmemBytes);
+        ensure_smem(reinterpret_cast<const void *>(k_band_attention_fwd<T, kBias, kDrop, kGlob>), smem);
     if (e != cudaSuccess) return e;
-    k_band_attention_fwd<T, kBias, kDrop><<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, a);
+    GlobArgs none;
+    none.G = 0;
+    k_band_attention_fwd<T, kBias, kDrop, kGlob><<<grid, kThreads, smem, st>>>(mq, mk, mv, a, gl ? *gl : none);
     return cudaGetLastError();
 }
 
@@ -604,6 +626,13 @@ cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st) {
     const int threads = ((a.g.hd + 31) / 32) * 32;
     k_band_attention_f32<<<(unsigned)rows, threads, 0, st>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_band_attention_glob(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
+                                       const TmapSet &mapV, const AttnArgs &a, const GlobArgs &gl,
+                                       cudaStream_t st) {
+    if (dt == kF16) return launch_t<__half, false, false, true>(mapQ, mapK, mapV, a, st, &gl);
+    return launch_t<__nv_bfloat16, false, false, true>(mapQ, mapK, mapV, a, st, &gl);
 }
 
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,

@@ -439,9 +439,194 @@ cudaError_t launch_reduce_t(const GlobReduceArgs &a, bool cols, cudaStream_t st)
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Companions of the fused forward with global tokens.  The fused kernel
+// attends each query to its band keys outside G; then
+//  * k_fused_glob_cols merges, into every local row, its attention over the G
+//    global keys (columns): O and lse of the two disjoint key sets combine by
+//    log-sum-exp;
+//  * k_fused_glob_rows computes every global query's dense attention over all
+//    n keys, overwriting those rows.
+// ---------------------------------------------------------------------------
+struct FusedGlobArgs {
+    Geom g;
+    GlobArgs gl;
+    float scale;
+    const void *Q, *K, *V;
+    void *O;
+    float *lse;
+};
+
+// warp per local row; the slice's global K, V rows staged once per block
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_fused_glob_cols(const FusedGlobArgs p) {
+    extern __shared__ float sm[];
+    const GlobArgs &gl = p.gl;
+    const int G = gl.G, n = p.g.n, bh = blockIdx.y;
+    float *kg = sm;                     // [G][kPad]
+    float *vg = kg + G * kPad;          // [G][64]
+    float *qs = vg + G * 64;            // [8 warps][64]
+    const T *Q = reinterpret_cast<const T *>(p.Q) + (long long)bh * n * 64;
+    const T *K = reinterpret_cast<const T *>(p.K) + (long long)bh * n * 64;
+    const T *V = reinterpret_cast<const T *>(p.V) + (long long)bh * n * 64;
+    for (int e = threadIdx.x; e < G * 64; e += kThreads) {
+        const int gg = e >> 6, c = e & 63;
+        kg[gg * kPad + c] = ld(K + (long long)gl.idx[gg] * 64 + c);
+        vg[gg * 64 + c] = ld(V + (long long)gl.idx[gg] * 64 + c);
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * (kThreads / 32) + warp;
+    if (i >= n) return;
+    // global rows are written by k_fused_glob_rows
+    int lo = 0, hi = G;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (gl.idx[mid] < i) lo = mid + 1; else hi = mid;
+    }
+    if (lo < G && gl.idx[lo] == i) return;
+    float *q = qs + warp * 64;
+    q[lane] = ld(Q + (long long)i * 64 + lane);
+    q[lane + 32] = ld(Q + (long long)i * 64 + lane + 32);
+    __syncwarp();
+    // scores of the global keys: lane owns keys lane, lane + 32, ... (log2 units)
+    constexpr int kMaxPer = kMaxGlobal / 32;
+    float sc[kMaxPer];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kMaxPer; ++u) {
+        const int gg = lane + 32 * u;
+        sc[u] = -INFINITY;
+        if (gg < G) {
+            float d = 0.f;
+#pragma unroll 16
+            for (int c = 0; c < 64; ++c) d = fmaf(q[c], kg[gg * kPad + c], d);
+            sc[u] = d * p.scale * kLog2e;
+            mx = fmaxf(mx, sc[u]);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float l = 0.f;
+#pragma unroll
+    for (int u = 0; u < kMaxPer; ++u) {
+        sc[u] = lane + 32 * u < G ? ex2(sc[u] - mx) : 0.f;
+        l += sc[u];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    // the global keys' unnormalised output, channels lane and lane + 32
+    float o0 = 0.f, o1 = 0.f;
+    for (int gg = 0; gg < G; ++gg) {
+        float pg = 0.f;
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u)
+            if ((gg >> 5) == u) pg = __shfl_sync(0xffffffffu, sc[u], gg & 31);
+        o0 = fmaf(pg, vg[gg * 64 + lane], o0);
+        o1 = fmaf(pg, vg[gg * 64 + lane + 32], o1);
+    }
+    // merge with the band part (O, lse of the keys outside G)
+    const long long row = (long long)bh * n + i;
+    const float lse_a = p.lse[row];
+    const float lse_b = mx / kLog2e + logf(l);
+    const float m2 = fmaxf(lse_a, lse_b);
+    const float wa = expf(lse_a - m2), wb = expf(lse_b - m2);
+    const float den = wa + wb;
+    T *o = reinterpret_cast<T *>(p.O) + row * 64;
+    const float a0 = ld(o + lane), a1 = ld(o + lane + 32);
+    const float fb = wb / (l * den), fa = wa / den;
+    o[lane] = Elt<T>::from_f(a0 * fa + o0 * fb);
+    o[lane + 32] = Elt<T>::from_f(a1 * fa + o1 * fb);
+    if (lane == 0) p.lse[row] = m2 + logf(den);
+}
+
+// CTA per (global query, slice): 16 key groups of 16 threads, 4 channels each
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArgs p) {
+    __shared__ float qs[64];
+    __shared__ float red[16][66];
+    const int gg = blockIdx.x, bh = blockIdx.y, n = p.g.n;
+    const int i = p.gl.idx[gg];
+    const T *K = reinterpret_cast<const T *>(p.K) + (long long)bh * n * 64;
+    const T *V = reinterpret_cast<const T *>(p.V) + (long long)bh * n * 64;
+    if (threadIdx.x < 64) qs[threadIdx.x] = ld(reinterpret_cast<const T *>(p.Q) + ((long long)bh * n + i) * 64 + threadIdx.x);
+    __syncthreads();
+    const int kg = threadIdx.x >> 4, cq = threadIdx.x & 15;
+    const float q0 = qs[4 * cq], q1 = qs[4 * cq + 1], q2 = qs[4 * cq + 2], q3 = qs[4 * cq + 3];
+    const float xs = p.scale * kLog2e;
+    float m = -INFINITY, l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    // the trip count is the same for every lane (the shuffles take the whole
+    // warp); a group's key past the end contributes nothing
+    for (int jb = 0; jb < n; jb += 16) {
+        const int j = jb + kg;
+        const bool live = j < n;
+        const T *kr = K + (long long)(live ? j : 0) * 64 + 4 * cq, *vr = V + (long long)(live ? j : 0) * 64 + 4 * cq;
+        float d = live ? q0 * ld(kr) + q1 * ld(kr + 1) + q2 * ld(kr + 2) + q3 * ld(kr + 3) : 0.f;
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        if (!live) continue;
+        const float x = d * xs;
+        const float mn = fmaxf(m, x);
+        const float corr = m == -INFINITY ? 0.f : ex2(m - mn);
+        const float pj = ex2(x - mn);
+        l = l * corr + pj;
+        a0 = a0 * corr + pj * ld(vr);
+        a1 = a1 * corr + pj * ld(vr + 1);
+        a2 = a2 * corr + pj * ld(vr + 2);
+        a3 = a3 * corr + pj * ld(vr + 3);
+        m = mn;
+    }
+    // merge the 16 key groups
+    red[kg][2 + 4 * cq] = a0;
+    red[kg][3 + 4 * cq] = a1;
+    red[kg][4 + 4 * cq] = a2;
+    red[kg][5 + 4 * cq] = a3;
+    if (cq == 0) {
+        red[kg][0] = m;
+        red[kg][1] = l;
+    }
+    __syncthreads();
+    if (threadIdx.x < 64) {
+        const int c = threadIdx.x;
+        float M = -INFINITY;
+        for (int k = 0; k < 16; ++k) M = fmaxf(M, red[k][0]);
+        float L = 0.f, o = 0.f;
+        for (int k = 0; k < 16; ++k) {
+            const float f = red[k][0] == -INFINITY ? 0.f : ex2(red[k][0] - M);
+            L = fmaf(red[k][1], f, L);
+            o = fmaf(red[k][2 + c], f, o);
+        }
+        const long long row = (long long)bh * n + i;
+        reinterpret_cast<T *>(p.O)[row * 64 + c] = Elt<T>::from_f(o / L);
+        if (c == 0) p.lse[row] = M / kLog2e + logf(L);
+    }
+}
+
+template <typename T>
+cudaError_t launch_fused_glob_t(const FusedGlobArgs &a, cudaStream_t st) {
+    const int G = a.gl.G;
+    const size_t smem = (size_t)(G * kPad + G * 64 + (kThreads / 32) * 64) * sizeof(float);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_fused_glob_cols<T>), (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid_c((unsigned)((a.g.n + kThreads / 32 - 1) / (kThreads / 32)), (unsigned)a.g.BH);
+    k_fused_glob_cols<T><<<grid_c, kThreads, smem, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_fused_glob_rows<T><<<dim3((unsigned)G, (unsigned)a.g.BH), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t glob_bitmap_bytes(int n) { return bitmap_bytes(n); }
+
+cudaError_t launch_fused_glob(DType dt, const Geom &g, const GlobArgs &gl, float scale, const void *Q,
+                              const void *K, const void *V, void *O, float *lse, cudaStream_t st) {
+    FusedGlobArgs a{g, gl, scale, Q, K, V, O, lse};
+    if (dt == kF16) return launch_fused_glob_t<__half>(a, st);
+    if (dt == kBF16) return launch_fused_glob_t<__nv_bfloat16>(a, st);
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_glob_scores(DType dt, const GlobScoreArgs &a, cudaStream_t st) {
     if (dt == kF32) return launch_scores_t<float>(a, st);

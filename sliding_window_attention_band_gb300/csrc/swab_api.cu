@@ -627,9 +627,29 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
-    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
     if ((s = check_ptrs({Q, K, V, O})) != SWAB_OK) return s;
     if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
+    if (desc->n_global > 0) {
+        // band keys outside G by the fused kernel, then the global columns
+        // merged into local rows (needs lse) and the global rows
+        if (dt == kF32 || g.rs_p || g.rs_o) return SWAB_ERR_UNSUPPORTED;
+        if (!lse) return SWAB_ERR_INVALID_ARG;
+        if ((long long)(g.n + 31) / 32 * 4 > 23 * 1024) return SWAB_ERR_UNSUPPORTED;   // key bitmap
+        GlobArgs gl;
+        gl.G = desc->n_global;
+        for (int k = 0; k < gl.G; ++k) gl.idx[k] = desc->global_idx[k];
+        TmapSet mq, mk, mv;
+        if (!build_dense_maps(&mq, Q, g, dt, kQKBoxRows, 0) || !build_dense_maps(&mk, K, g, dt, kQKBoxRows, 0) ||
+            !build_dense_maps(&mv, V, g, dt, kQKBoxRows, 0))
+            return SWAB_ERR_CUDA;
+        unsigned *err = status_word();
+        if (!err) return SWAB_ERR_CUDA;
+        AttnArgs a{g, scale, O, lse, err};
+        cudaStream_t st = as_stream(stream);
+        cudaError_t e = launch_band_attention_glob(dt, mq, mk, mv, a, gl, st);
+        if (e == cudaSuccess) e = launch_fused_glob(dt, g, gl, scale, Q, K, V, O, lse, st);
+        return from_cuda(e);
+    }
     if (dt == kF32) {
         AttnArgsF32 a{g, scale, static_cast<const float *>(Q), static_cast<const float *>(K),
                       static_cast<const float *>(V), static_cast<float *>(O), lse};

@@ -134,6 +134,13 @@ cudaError_t launch_band_gather_tc(DType dt, bool transposed, const TmapSet &mapB
                                   const GatherArgs &a, cudaStream_t st);
 size_t gather_glob_smem(int n, int G);      // extra shared memory with global tokens
 size_t gather_smem_bytes(int n, int G);     // total shared memory of the gather kernel
+// fused forward with global tokens: the band kernel with global keys masked,
+// then the global columns merged into local rows and the global rows
+cudaError_t launch_band_attention_glob(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
+                                       const TmapSet &mapV, const AttnArgs &a, const GlobArgs &gl,
+                                       cudaStream_t st);
+cudaError_t launch_fused_glob(DType dt, const Geom &g, const GlobArgs &gl, float scale, const void *Q,
+                              const void *K, const void *V, void *O, float *lse, cudaStream_t st);
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                      const TmapSet &mapV, const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st);

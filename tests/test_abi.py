@@ -199,11 +199,25 @@ def test_globals_need_head_dim_64(lib):
                        None) == UNSUPPORTED
 
 
-def test_fused_forward_rejects_globals(lib):
-    d = desc(global_idx=[1])
+def test_fused_forward_global_rules(lib):
+    """With global tokens the fused forward needs lse (the global columns are
+    merged by log-sum-exp), f16 / bf16 and the contiguous layout."""
     P = ctypes.c_void_p
+    d = desc(global_idx=[1])
     assert lib.band_attention(ctypes.byref(d.c), 1.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None,
-                              None) == UNSUPPORTED
+                              None) == INVALID
+    d32 = desc(global_idx=[1], dtype=torch.float32)
+    assert lib.band_attention(ctypes.byref(d32.c), 1.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                              P(FAKE), None) == UNSUPPORTED
+    ds = desc(global_idx=[1], qkv_row_stride=384)
+    assert lib.band_attention(ctypes.byref(ds.c), 1.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                              P(FAKE), None) == UNSUPPORTED
+    big = desc(n=200000, global_idx=[1])
+    assert lib.band_attention(ctypes.byref(big.c), 1.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                              P(FAKE), None) == UNSUPPORTED
+    # the fused backward still takes no global tokens
+    assert lib.band_attention_bwd(ctypes.byref(d.c), 1.0, *(P(FAKE) for _ in range(10)),
+                                  None) == UNSUPPORTED
 
 
 def test_binding_checks_companion_shapes():

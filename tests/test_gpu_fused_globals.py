@@ -1,0 +1,81 @@
+"""The fused forward with global tokens (ONNX Runtime issue "[WIP] Improve
+LongformerAttention performance", item (1)): band_attention gives the same O
+and lse as the attention with global tokens on explicit key sets (the fp64
+oracle) -- local rows over their band keys outside G plus G, global rows over
+every key.  Tolerances as in test_gpu_parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sliding_window_attention_band_gb300 as swab
+from sliding_window_attention_band_gb300.inputs import WORKLOADS, seeded_qkvo, workload_inputs
+
+from test_gpu_parity import f64, within_abs
+
+pytestmark = pytest.mark.gpu
+
+CASES = [  # BH, n, w, w_upper, dilation, dtype, global idx
+    (2, 1000, 64, 64, 0, torch.float16, (0, 1, 7, 500, 999)),
+    (3, 777, 100, 37, 2, torch.bfloat16, (3, 20, 21, 400)),
+    (1, 640, 0, 127, 1, torch.float16, tuple(range(16))),
+    (2, 515, 3, 3, 3, torch.float16, (64,)),
+    (1, 1100, 300, 300, 0, torch.bfloat16, tuple(range(0, 1100, 37))),
+]
+
+
+def ids(c):
+    return f"BH{c[0]}-n{c[1]}-w{c[2]}-wu{c[3]}-d{c[4]}-{str(c[5]).split('.')[-1]}-G{len(c[6])}"
+
+
+def run(d, Q, K, V, scale):
+    O = torch.empty(d.BH, d.n, 64, dtype=d.dtype, device="cuda")
+    lse = torch.empty(d.BH, d.n, dtype=torch.float32, device="cuda")
+    swab.band_attention(d, scale, Q.cuda(), K.cuda(), V.cuda(), O, lse)
+    torch.cuda.synchronize()
+    return O, lse
+
+
+def check(d, Q, K, V, scale, slices):
+    O, lse = run(d, Q, K, V, scale)
+    sl = list(slices)
+    rO, rl = oracle.attention_fwd(f64(Q[sl]), f64(K[sl]), f64(V[sl]), d.w, d.w_upper, d.dilation,
+                                  scale, list(d.global_idx))
+    assert within_abs(f64(O[sl].cpu()), rO, d.dtype)
+    np.testing.assert_allclose(f64(lse[sl].cpu()), rl, rtol=1e-4, atol=2e-3)
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_fused_forward_globals(case):
+    BH, n, w, wu, dil, dtype, gidx = case
+    d = swab.Desc(1, BH, n, 64, w, wu, dil, 0.0, dtype, gidx)
+    Q, K, V, _ = seeded_qkvo(BH, n, 64, dtype, seed=n + 71)
+    check(d, Q, K, V, 0.125, range(BH))
+
+
+def test_fused_forward_globals_matches_materialised():
+    """The fused forward and the materialised chain agree with global tokens."""
+    BH, n, gidx = 2, 900, (0, 5, 450, 899)
+    d = swab.Desc(1, BH, n, 64, 128, 128, 0, 0.0, torch.float16, gidx)
+    Q, K, V, _ = (x.cuda() for x in seeded_qkvo(BH, n, 64, torch.float16, seed=3))
+    O, lse = run(d, Q, K, V, 0.125)
+    S = torch.empty(BH, n, d.D, dtype=torch.float16, device="cuda")
+    Sg = (torch.empty(BH, n, d.G, dtype=torch.float16, device="cuda"),
+          torch.empty(BH, d.G, n, dtype=torch.float16, device="cuda"))
+    Pg = tuple(torch.empty_like(x) for x in Sg)
+    P = torch.empty_like(S)
+    O2 = torch.empty_like(O)
+    lse2 = torch.empty_like(lse)
+    swab.band_qk(d, 0.125, Q, K, S, Sg)
+    swab.band_softmax(d, S, P, lse2, Sg=Sg, Pg=Pg)
+    swab.band_pv(d, 1.0, P, V, O2, Pg=Pg)
+    torch.cuda.synchronize()
+    assert float((O.float() - O2.float()).abs().max()) <= 1e-2
+    assert float((lse - lse2).abs().max()) <= 2e-3
+
+
+def test_fused_forward_globals_training_workload_sampled():
+    """b = 12, h = 12, n = 4096, w = 256, 16 global tokens, bf16 (slices 0, 77, 143)."""
+    wl = WORKLOADS[4]
+    Q, K, V = workload_inputs(wl, count=3)
+    check(swab.Desc.from_workload(wl), Q, K, V, wl.scale, (0, 77, 143))
