@@ -24,3 +24,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="module")
+def device_status_guard():
+    """Builds and loads the library, clears its device status word before the
+    module's tests and checks afterwards that no kernel raised it (a bounded
+    wait that gave up)."""
+    import sliding_window_attention_band_gb300 as swab
+    from sliding_window_attention_band_gb300 import build as swab_build
+
+    swab_build.build()
+    swab.load()
+    swab.device_status(reset=True)
+    yield
+    assert swab.device_status(reset=True) == 0, "a kernel raised the device status word"

@@ -13,7 +13,7 @@ from sliding_window_attention_band_gb300.inputs import WORKLOADS, seeded_qkvo, w
 
 from test_gpu_parity import f64, within_abs
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("device_status_guard")]
 
 CASES = [  # BH, n, w, w_upper, dilation, dtype, global idx
     (2, 1000, 64, 64, 0, torch.float16, (0, 1, 7, 500, 999)),

@@ -17,7 +17,7 @@ from sliding_window_attention_band_gb300.inputs import WORKLOADS, seeded_qkvo
 from test_gpu_globals import gpu_chain_globals
 from test_gpu_parity import F32_TOL, f64, normwise, within_abs
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("device_status_guard")]
 
 CASES = [  # BH, n, G, dtype
     (2, 1000, 16, torch.float16),

@@ -12,7 +12,7 @@ from sliding_window_attention_band_gb300.inputs import WORKLOADS, seeded_qkvo, w
 
 from test_gpu_parity import F32_TOL, empty_dense, f64, normwise, within_abs
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("device_status_guard")]
 
 CASES = [  # b, h, n, w, w_upper, dilation, dtype
     (2, 2, 700, 64, 64, 0, torch.float16),

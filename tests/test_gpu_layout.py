@@ -21,7 +21,7 @@ import sliding_window_attention_band_gb300 as swab
 
 from test_gpu_parity import F32_TOL, f64, normwise, within_abs
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("device_status_guard")]
 
 DTYPES = [torch.float16, torch.bfloat16, torch.float32]
 

@@ -19,7 +19,7 @@ from test_gpu_parity import (ABS_TOL, F32_TOL, UNIT_CASES, empty_band, empty_den
                              normwise, poison_invalid, score_tol, unit_ids, valid_mask,
                              within_abs)
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("device_status_guard")]
 
 P_DROP = 0.1
 SEED = 0x5EED1234ABCD
