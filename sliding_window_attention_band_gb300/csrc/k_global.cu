@@ -10,6 +10,8 @@
 // Every product here has G (a handful of tokens) as one of its dimensions and
 // costs G*n*64 multiply-adds per slice, a few percent of the banded products;
 // they run on FFMA with operands staged in shared memory.
+#include <type_traits>
+
 #include "swab_internal.h"
 
 namespace swab {
@@ -457,26 +459,28 @@ struct FusedGlobArgs {
     float *lse;
 };
 
-// warp per local row; the slice's global K, V rows staged once per block
+// Thread per local row (its query and a 64-channel accumulator in
+// registers), the slice's global K, V rows staged once per block and read by
+// every lane at once (shared-memory broadcasts).
+constexpr int kGlobColThreads = 128;
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads) k_fused_glob_cols(const FusedGlobArgs p) {
-    extern __shared__ float sm[];
+__global__ void __launch_bounds__(kGlobColThreads) k_fused_glob_cols(const FusedGlobArgs p) {
+    extern __shared__ __align__(16) float sm[];
     const GlobArgs &gl = p.gl;
     const int G = gl.G, n = p.g.n, bh = blockIdx.y;
-    float *kg = sm;                     // [G][kPad]
-    float *vg = kg + G * kPad;          // [G][64]
-    float *qs = vg + G * 64;            // [8 warps][64]
+    float *kg = sm;             // [G][64]
+    float *vg = kg + G * 64;    // [G][64]
     const T *Q = reinterpret_cast<const T *>(p.Q) + (long long)bh * n * 64;
     const T *K = reinterpret_cast<const T *>(p.K) + (long long)bh * n * 64;
     const T *V = reinterpret_cast<const T *>(p.V) + (long long)bh * n * 64;
-    for (int e = threadIdx.x; e < G * 64; e += kThreads) {
+    for (int e = threadIdx.x; e < G * 64; e += kGlobColThreads) {
         const int gg = e >> 6, c = e & 63;
-        kg[gg * kPad + c] = ld(K + (long long)gl.idx[gg] * 64 + c);
-        vg[gg * 64 + c] = ld(V + (long long)gl.idx[gg] * 64 + c);
+        kg[e] = ld(K + (long long)gl.idx[gg] * 64 + c);
+        vg[e] = ld(V + (long long)gl.idx[gg] * 64 + c);
     }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = blockIdx.x * (kThreads / 32) + warp;
+    const int i = blockIdx.x * kGlobColThreads + threadIdx.x;
     if (i >= n) return;
     // global rows are written by k_fused_glob_rows
     int lo = 0, hi = G;
@@ -485,59 +489,73 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_cols(const FusedGlobArg
         if (gl.idx[mid] < i) lo = mid + 1; else hi = mid;
     }
     if (lo < G && gl.idx[lo] == i) return;
-    float *q = qs + warp * 64;
-    q[lane] = ld(Q + (long long)i * 64 + lane);
-    q[lane + 32] = ld(Q + (long long)i * 64 + lane + 32);
-    __syncwarp();
-    // scores of the global keys: lane owns keys lane, lane + 32, ... (log2 units)
-    constexpr int kMaxPer = kMaxGlobal / 32;
-    float sc[kMaxPer];
-    float mx = -INFINITY;
+    float q[64];
+    {
+        const uint4 *qr = reinterpret_cast<const uint4 *>(Q + (long long)i * 64);
 #pragma unroll
-    for (int u = 0; u < kMaxPer; ++u) {
-        const int gg = lane + 32 * u;
-        sc[u] = -INFINITY;
-        if (gg < G) {
-            float d = 0.f;
-#pragma unroll 16
-            for (int c = 0; c < 64; ++c) d = fmaf(q[c], kg[gg * kPad + c], d);
-            sc[u] = d * p.scale * kLog2e;
-            mx = fmaxf(mx, sc[u]);
+        for (int k = 0; k < 64 * (int)sizeof(T) / 16; ++k) {
+            const uint4 v = ldg16(qr + k);
+            if constexpr (sizeof(T) == 2) {
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    q[8 * k + 2 * u] = lo16<T>(w[u]);
+                    q[8 * k + 2 * u + 1] = hi16<T>(w[u]);
+                }
+            }
         }
     }
+    // online softmax over the G global keys (log2 units)
+    const float xs = p.scale * kLog2e;
+    float m = -INFINITY, l = 0.f, acc[64];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float l = 0.f;
-#pragma unroll
-    for (int u = 0; u < kMaxPer; ++u) {
-        sc[u] = lane + 32 * u < G ? ex2(sc[u] - mx) : 0.f;
-        l += sc[u];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    // the global keys' unnormalised output, channels lane and lane + 32
-    float o0 = 0.f, o1 = 0.f;
+    for (int c = 0; c < 64; ++c) acc[c] = 0.f;
     for (int gg = 0; gg < G; ++gg) {
-        float pg = 0.f;
+        const float4 *kr = reinterpret_cast<const float4 *>(kg + gg * 64);
+        float d = 0.f;
 #pragma unroll
-        for (int u = 0; u < kMaxPer; ++u)
-            if ((gg >> 5) == u) pg = __shfl_sync(0xffffffffu, sc[u], gg & 31);
-        o0 = fmaf(pg, vg[gg * 64 + lane], o0);
-        o1 = fmaf(pg, vg[gg * 64 + lane + 32], o1);
+        for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 k4 = kr[c4];
+            d = fmaf(q[4 * c4 + 3], k4.w, fmaf(q[4 * c4 + 2], k4.z, fmaf(q[4 * c4 + 1], k4.y, fmaf(q[4 * c4], k4.x, d))));
+        }
+        const float x = d * xs;
+        const float mn = fmaxf(m, x);
+        const float corr = ex2(m - mn);   // 0 for the first key (m = -inf)
+        const float pg = ex2(x - mn);
+        l = fmaf(l, corr, pg);
+        const float4 *vr = reinterpret_cast<const float4 *>(vg + gg * 64);
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 v4 = vr[c4];
+            acc[4 * c4] = fmaf(acc[4 * c4], corr, pg * v4.x);
+            acc[4 * c4 + 1] = fmaf(acc[4 * c4 + 1], corr, pg * v4.y);
+            acc[4 * c4 + 2] = fmaf(acc[4 * c4 + 2], corr, pg * v4.z);
+            acc[4 * c4 + 3] = fmaf(acc[4 * c4 + 3], corr, pg * v4.w);
+        }
+        m = mn;
     }
     // merge with the band part (O, lse of the keys outside G)
     const long long row = (long long)bh * n + i;
     const float lse_a = p.lse[row];
-    const float lse_b = mx / kLog2e + logf(l);
+    const float lse_b = m / kLog2e + logf(l);
     const float m2 = fmaxf(lse_a, lse_b);
     const float wa = expf(lse_a - m2), wb = expf(lse_b - m2);
     const float den = wa + wb;
-    T *o = reinterpret_cast<T *>(p.O) + row * 64;
-    const float a0 = ld(o + lane), a1 = ld(o + lane + 32);
-    const float fb = wb / (l * den), fa = wa / den;
-    o[lane] = Elt<T>::from_f(a0 * fa + o0 * fb);
-    o[lane + 32] = Elt<T>::from_f(a1 * fa + o1 * fb);
-    if (lane == 0) p.lse[row] = m2 + logf(den);
+    const float fa = wa / den, fb = wb / (l * den);
+    uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + row * 64);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint4 a = o4[k];
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+        uint32_t r[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = 8 * k + 2 * u;
+            r[u] = pack2<T>(fmaf(lo16<T>(w[u]), fa, acc[c] * fb), fmaf(hi16<T>(w[u]), fa, acc[c + 1] * fb));
+        }
+        o4[k] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+    p.lse[row] = m2 + logf(den);
 }
 
 // CTA per (global query, slice): 16 key groups of 16 threads, 4 channels each
@@ -557,24 +575,35 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArg
     float m = -INFINITY, l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     // the trip count is the same for every lane (the shuffles take the whole
     // warp); a group's key past the end contributes nothing
-    for (int jb = 0; jb < n; jb += 16) {
-        const int j = jb + kg;
-        const bool live = j < n;
-        const T *kr = K + (long long)(live ? j : 0) * 64 + 4 * cq, *vr = V + (long long)(live ? j : 0) * 64 + 4 * cq;
-        float d = live ? q0 * ld(kr) + q1 * ld(kr + 1) + q2 * ld(kr + 2) + q3 * ld(kr + 3) : 0.f;
+    // four keys per step (their loads in flight together), 8 bytes per load
+    for (int jb = 0; jb < n; jb += 64) {
+        uint2 kw[4], vw[4];
 #pragma unroll
-        for (int off = 8; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-        if (!live) continue;
-        const float x = d * xs;
-        const float mn = fmaxf(m, x);
-        const float corr = m == -INFINITY ? 0.f : ex2(m - mn);
-        const float pj = ex2(x - mn);
-        l = l * corr + pj;
-        a0 = a0 * corr + pj * ld(vr);
-        a1 = a1 * corr + pj * ld(vr + 1);
-        a2 = a2 * corr + pj * ld(vr + 2);
-        a3 = a3 * corr + pj * ld(vr + 3);
-        m = mn;
+        for (int u = 0; u < 4; ++u) {
+            const int j = jb + 16 * u + kg;
+            const long long off = (long long)(j < n ? j : 0) * 64 + 4 * cq;
+            kw[u] = *reinterpret_cast<const uint2 *>(K + off);
+            vw[u] = *reinterpret_cast<const uint2 *>(V + off);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const bool live = jb + 16 * u + kg < n;
+            float d = q0 * lo16<T>(kw[u].x) + q1 * hi16<T>(kw[u].x) + q2 * lo16<T>(kw[u].y) +
+                      q3 * hi16<T>(kw[u].y);
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+            if (!live) continue;
+            const float x = d * xs;
+            const float mn = fmaxf(m, x);
+            const float corr = m == -INFINITY ? 0.f : ex2(m - mn);
+            const float pj = ex2(x - mn);
+            l = l * corr + pj;
+            a0 = a0 * corr + pj * lo16<T>(vw[u].x);
+            a1 = a1 * corr + pj * hi16<T>(vw[u].x);
+            a2 = a2 * corr + pj * lo16<T>(vw[u].y);
+            a3 = a3 * corr + pj * hi16<T>(vw[u].y);
+            m = mn;
+        }
     }
     // merge the 16 key groups
     red[kg][2 + 4 * cq] = a0;
@@ -605,13 +634,20 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArg
 template <typename T>
 cudaError_t launch_fused_glob_t(const FusedGlobArgs &a, cudaStream_t st) {
     const int G = a.gl.G;
-    const size_t smem = (size_t)(G * kPad + G * 64 + (kThreads / 32) * 64) * sizeof(float);
+    const size_t smem = (size_t)(2 * G * 64) * sizeof(float);
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_fused_glob_cols<T>), (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid_c((unsigned)((a.g.n + kThreads / 32 - 1) / (kThreads / 32)), (unsigned)a.g.BH);
-    k_fused_glob_cols<T><<<grid_c, kThreads, smem, st>>>(a);
+    const dim3 grid_c((unsigned)((a.g.n + kGlobColThreads - 1) / kGlobColThreads), (unsigned)a.g.BH);
+    k_fused_glob_cols<T><<<grid_c, kGlobColThreads, smem, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // dense global rows: a CTA per 16 global queries of a slice (each K, V tile
+    // read once for them) when those CTAs fill the GPU, else a CTA per query
+    const int sms = device_sm_count();
+    if (sms > 0 && 2LL * ((G + 15) / 16) * a.g.BH >= sms) {
+        GlobalRowsArgs r{a.g.BH, a.g.n, a.scale, a.Q, a.K, a.V, a.O, a.lse, a.gl};
+        return launch_fused_glob_rows_chunk(std::is_same<T, __half>::value ? kF16 : kBF16, r, st);
+    }
     k_fused_glob_rows<T><<<dim3((unsigned)G, (unsigned)a.g.BH), kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }

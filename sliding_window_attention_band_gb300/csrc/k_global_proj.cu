@@ -202,6 +202,93 @@ __global__ void __launch_bounds__(kThreads, 2) k_gproj_fwd(const GlobalProjArgs 
     part[5 + 4 * sub] = acc.w;
 }
 
+// Dense rows of the global queries of the fused forward, for problems with
+// enough (query chunk, slice) pairs to fill the GPU: CTA per (16 global
+// queries, slice) over every key (64-key tiles, the next tile's loads in
+// flight), so each K, V tile is read once for the 16 queries; writes the
+// final O rows at the global positions and their lse.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) k_fused_glob_rows_chunk(const GlobalRowsArgs p) {
+    __shared__ __align__(16) float qs[kGC * kPad], ks[kKT * kPad], vs[kKT * kPad], ps[kGC * kPad];
+    const int gc = blockIdx.x, bh = blockIdx.y;
+    const int G = p.gl.G, n = p.n, t = threadIdx.x;
+    const int g = t >> 4, sub = t & 15;
+    const T *Q = reinterpret_cast<const T *>(p.Q) + (long long)bh * n * 64;
+    const T *Kg = reinterpret_cast<const T *>(p.K) + (long long)bh * n * 64;
+    const T *Vg = reinterpret_cast<const T *>(p.V) + (long long)bh * n * 64;
+    for (int e = t; e < kGC * 64; e += kThreads) {
+        const int r = e >> 6, c = e & 63, gg = gc * kGC + r;
+        qs[r * kPad + c] = gg < G ? Elt<T>::to_f(Q[(long long)p.gl.idx[gg] * 64 + c]) : 0.f;
+    }
+    const float xs = p.scale * kLog2e;
+    float m = -INFINITY, l = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // channels 4 sub .. + 3
+    TileRegs<T> kr, vr;
+    fetch_tile(kr, Kg, 0, n);
+    fetch_tile(vr, Vg, 0, n);
+    for (int j0 = 0; j0 < n; j0 += kKT) {
+        __syncthreads();   // the previous tile's readers are done (and qs is written)
+        store_tile(ks, kr);
+        store_tile(vs, vr);
+        if (j0 + kKT < n) {
+            fetch_tile(kr, Kg, j0 + kKT, n);
+            fetch_tile(vr, Vg, j0 + kKT, n);
+        }
+        __syncthreads();
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, tmax = -INFINITY;
+#pragma unroll 4
+        for (int c = 0; c < 64; c += 4) {
+            const float4 q4 = lds4(qs + g * kPad + c);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s[u] = dot4(q4, lds4(ks + (sub + 16 * u) * kPad + c), s[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            s[u] = j0 + sub + 16 * u < n ? s[u] * xs : -INFINITY;
+            tmax = fmaxf(tmax, s[u]);
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+        const float mn = fmaxf(m, tmax);
+        const float corr = m == -INFINITY ? 0.f : ex2(m - mn);
+        float psum = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float pv = ex2(s[u] - mn);
+            ps[g * kPad + sub + 16 * u] = pv;
+            psum += pv;
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+        l = l * corr + psum;
+        m = mn;
+        __syncthreads();
+        acc.x *= corr;
+        acc.y *= corr;
+        acc.z *= corr;
+        acc.w *= corr;
+#pragma unroll 4
+        for (int j = 0; j < kKT; j += 4) {
+            const float4 p4 = lds4(ps + g * kPad + j);
+            const float *vrow = vs + j * kPad + 4 * sub;
+            axpy4(acc, p4.x, lds4(vrow));
+            axpy4(acc, p4.y, lds4(vrow + kPad));
+            axpy4(acc, p4.z, lds4(vrow + 2 * kPad));
+            axpy4(acc, p4.w, lds4(vrow + 3 * kPad));
+        }
+    }
+    const int gg = gc * kGC + g;
+    if (gg >= G) return;
+    const long long row = (long long)bh * n + p.gl.idx[gg];
+    const float inv = 1.f / l;
+    T *o = reinterpret_cast<T *>(p.O) + row * 64 + 4 * sub;
+    o[0] = Elt<T>::from_f(acc.x * inv);
+    o[1] = Elt<T>::from_f(acc.y * inv);
+    o[2] = Elt<T>::from_f(acc.z * inv);
+    o[3] = Elt<T>::from_f(acc.w * inv);
+    if (sub == 0) p.lse[row] = m / kLog2e + logf(l);
+}
+
 // merge the chunks: a warp per (slice, query); lane k < nchunks reads chunk
 // k's (max, sum) at once, then every lane merges two channels over the chunks
 // with eight loads in flight
@@ -935,6 +1022,14 @@ cudaError_t launch_global_proj_fwd_tc(DType dt, const TmapSet &mk, const TmapSet
     if (dt == kF16) return launch_fwd_tc_t<__half>(mk, mv, mq, a, st);
     if (dt == kBF16) return launch_fwd_tc_t<__nv_bfloat16>(mk, mv, mq, a, st);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fused_glob_rows_chunk(DType dt, const GlobalRowsArgs &a, cudaStream_t st) {
+    const dim3 grid((unsigned)((a.gl.G + kGC - 1) / kGC), (unsigned)a.BH);
+    if (dt == kF16) k_fused_glob_rows_chunk<__half><<<grid, kThreads, 0, st>>>(a);
+    else if (dt == kBF16) k_fused_glob_rows_chunk<__nv_bfloat16><<<grid, kThreads, 0, st>>>(a);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_global_proj(DType dt, const GlobalProjArgs &a, bool bwd, cudaStream_t st) {

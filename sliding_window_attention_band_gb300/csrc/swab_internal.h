@@ -139,6 +139,16 @@ size_t gather_smem_bytes(int n, int G);     // total shared memory of the gather
 cudaError_t launch_band_attention_glob(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                        const TmapSet &mapV, const AttnArgs &a, const GlobArgs &gl,
                                        cudaStream_t st);
+struct GlobalRowsArgs {   // dense rows of the global queries (fused forward)
+    long long BH;
+    int n;
+    float scale;
+    const void *Q, *K, *V;   // [BH, n, 64]
+    void *O;                 // [BH, n, 64]: rows at the global positions written
+    float *lse;              // [BH, n]
+    GlobArgs gl;
+};
+cudaError_t launch_fused_glob_rows_chunk(DType dt, const GlobalRowsArgs &a, cudaStream_t st);
 cudaError_t launch_fused_glob(DType dt, const Geom &g, const GlobArgs &gl, float scale, const void *Q,
                               const void *K, const void *V, void *O, float *lse, cudaStream_t st);
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
