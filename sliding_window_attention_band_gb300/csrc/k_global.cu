@@ -632,20 +632,23 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArg
 }
 
 template <typename T>
-cudaError_t launch_fused_glob_t(const FusedGlobArgs &a, cudaStream_t st) {
+cudaError_t launch_fused_glob_t(const FusedGlobArgs &a, bool cols_done, cudaStream_t st) {
     const int G = a.gl.G;
-    const size_t smem = (size_t)(2 * G * 64) * sizeof(float);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_fused_glob_cols<T>), (int)smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid_c((unsigned)((a.g.n + kGlobColThreads - 1) / kGlobColThreads), (unsigned)a.g.BH);
-    k_fused_glob_cols<T><<<grid_c, kGlobColThreads, smem, st>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
+    if (!cols_done) {
+        const size_t smem = (size_t)(2 * G * 64) * sizeof(float);
+        e = ensure_smem(reinterpret_cast<const void *>(k_fused_glob_cols<T>), (int)smem);
+        if (e != cudaSuccess) return e;
+        const dim3 grid_c((unsigned)((a.g.n + kGlobColThreads - 1) / kGlobColThreads), (unsigned)a.g.BH);
+        k_fused_glob_cols<T><<<grid_c, kGlobColThreads, smem, st>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     // dense global rows: a CTA per 16 global queries of a slice (each K, V tile
     // read once for them) when those CTAs fill the GPU, else a CTA per query
     const int sms = device_sm_count();
     if (sms > 0 && 2LL * ((G + 15) / 16) * a.g.BH >= sms) {
-        GlobalRowsArgs r{a.g.BH, a.g.n, a.scale, a.Q, a.K, a.V, a.O, a.lse, a.gl};
+        GlobalRowsArgs r{a.g.BH, a.g.n, a.scale, a.Q, a.K, a.V, a.O, a.lse, a.gl, nullptr};
         return launch_fused_glob_rows_chunk(std::is_same<T, __half>::value ? kF16 : kBF16, r, st);
     }
     k_fused_glob_rows<T><<<dim3((unsigned)G, (unsigned)a.g.BH), kThreads, 0, st>>>(a);
@@ -657,10 +660,11 @@ cudaError_t launch_fused_glob_t(const FusedGlobArgs &a, cudaStream_t st) {
 size_t glob_bitmap_bytes(int n) { return bitmap_bytes(n); }
 
 cudaError_t launch_fused_glob(DType dt, const Geom &g, const GlobArgs &gl, float scale, const void *Q,
-                              const void *K, const void *V, void *O, float *lse, cudaStream_t st) {
+                              const void *K, const void *V, void *O, float *lse, bool cols_done,
+                              cudaStream_t st) {
     FusedGlobArgs a{g, gl, scale, Q, K, V, O, lse};
-    if (dt == kF16) return launch_fused_glob_t<__half>(a, st);
-    if (dt == kBF16) return launch_fused_glob_t<__nv_bfloat16>(a, st);
+    if (dt == kF16) return launch_fused_glob_t<__half>(a, cols_done, st);
+    if (dt == kBF16) return launch_fused_glob_t<__nv_bfloat16>(a, cols_done, st);
     return cudaErrorInvalidValue;
 }
 

@@ -914,6 +914,216 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Global columns of the fused forward with global tokens, on the tensor
+// cores (G <= 64): CTA per (128-query tile, slice).  S = Q_tile K_G^T
+// (N = G rounded up to 16), each worker lane owns a query row and takes the
+// softmax over the global keys in registers, O_B = P V_G (K = G rounded up),
+// and the row's (O_B, lse_B) is merged into the band part's (O, lse) by
+// log-sum-exp.  The Q tile arrives by TMA; the few K_G, V_G rows are loaded
+// by warp 0 and written into the swizzled layout (zeros past G).  Rows in G
+// are left to the dense rows.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kCColS = 0, kCColO = 64;
+constexpr uint32_t kCTmemCols = 128;
+
+__host__ __device__ constexpr int tc_cols_smem() {
+    return 1024 + kTile16 /* Q tile */ + 2 * 64 * 128 /* K_G, V_G: 64 rows */ + kTile16 /* P */ + 128;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_fused_glob_cols_tc(const __grid_constant__ TmapSet mapQ, const GlobalRowsArgs p) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const int G = p.gl.G, n = p.n, gp = (G + 15) & ~15;   // global keys, rounded up to 16
+    uint8_t *qbuf = base;                    // Q tile [128 x 64]
+    uint8_t *kgb = qbuf + kTile16;           // K_G [gp rows x 64]
+    uint8_t *vgb = kgb + 64 * 128;           // V_G [gp rows x 64]
+    uint8_t *pa = vgb + 64 * 128;            // P [128 queries][gp keys], 128-byte swizzled rows
+    uint64_t *bars = reinterpret_cast<uint64_t *>(pa + kTile16);
+    uint64_t *ldfull = bars, *sfull = bars + 1, *pfull = bars + 2, *ofull = bars + 3;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *no_abort = reinterpret_cast<volatile int *>(tmem_holder + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, bh = blockIdx.y, a0 = qt * kTcKeys;
+    if (threadIdx.x == 0) {
+        mbar_init(ldfull, 1 + 32);   // the Q copy, and warp 0's lanes after K_G, V_G
+        mbar_init(sfull, 1);
+        mbar_init(pfull, 128);
+        mbar_init(ofull, 1);
+        *abort_flag = 0;
+        *no_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kCTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    bool ok = true;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(ldfull, kTile16);
+            tma_load_3d(qbuf, &mapQ.m[0], ldfull, 0, a0, bh);
+        }
+        // K_G, V_G rows (zeros past G) written straight into the 128-byte
+        // swizzled layout: 16-byte piece c of row r at r * 128 + ((c ^ (r & 7)) << 4)
+        const T *Kb = reinterpret_cast<const T *>(p.K) + (long long)bh * n * 64;
+        const T *Vb = reinterpret_cast<const T *>(p.V) + (long long)bh * n * 64;
+        for (int e = lane; e < gp * 8; e += 32) {
+            const int r = e >> 3, c = e & 7;
+            uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+            if (r < G) {
+                kv = ldg16(Kb + (long long)p.gl.idx[r] * 64 + 8 * c);
+                vv = ldg16(Vb + (long long)p.gl.idx[r] * 64 + 8 * c);
+            }
+            const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+            sts16(smem_u32(kgb) + off, kv);
+            sts16(smem_u32(vgb) + off, vv);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(ldfull);
+        mbar_wait(ldfull, 0, no_abort, nullptr, 100000000ull);
+    } else if (warp == 1) {
+        constexpr bool kBf16 = !std::is_same<T, __half>::value;
+        const uint32_t id_s = idesc_f16(kTcKeys, gp, kBf16, false, false);
+        constexpr uint32_t id_o = idesc_f16(kTcKeys, 64, kBf16, false, true);
+        const uint64_t d_q = sdesc_sw128(smem_u32(qbuf), 16, 1024);
+        const uint64_t d_kg = sdesc_sw128(smem_u32(kgb), 16, 1024);
+        const uint64_t d_vmn = sdesc_sw128(smem_u32(vgb), 1024, 1024);   // V_G as MN-major B
+        const uint64_t d_pa = sdesc_sw128(smem_u32(pa), 16, 1024);
+        ok = __all_sync(0xffffffffu, mbar_wait(ldfull, 0, abort_flag, p.err));
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mma_f16_ss(tmem + kCColS, d_q + 2 * k, d_kg + 2 * k, id_s, k > 0 ? 1u : 0u);
+                mma_commit(sfull);
+            }
+            __syncwarp();
+            ok = __all_sync(0xffffffffu, mbar_wait(pfull, 0, abort_flag, p.err));
+        }
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0) {
+                for (int k = 0; k < gp / 16; ++k)
+                    mma_f16_ss(tmem + kCColO, d_pa + 2 * k, d_vmn + (uint64_t)((2048 * k) >> 4), id_o, k > 0 ? 1u : 0u);
+                mma_commit(ofull);
+            }
+            __syncwarp();
+        } else if (lane == 0) {
+            mma_commit(ofull);   // the products issued complete before the free
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3, m = quarter * 32 + lane;
+        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
+        const int i = a0 + m;
+        bool write = i < n;
+        if (write) {
+            int lo = 0, hi = G;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (p.gl.idx[mid] < i) lo = mid + 1; else hi = mid;
+            }
+            write = !(lo < G && p.gl.idx[lo] == i);
+        }
+        const float xs = p.scale * kLog2e;
+        float mb = 0.f, lb = 1.f;
+        if (__all_sync(0xffffffffu, mbar_wait(sfull, 0, abort_flag, p.err))) {
+            tc_fence_after();
+            // every index compile-time (registers), the columns past gp unused
+            float x[64];
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                if (c0 < gp) {   // warp-uniform
+                    uint32_t v[16];
+                    tmem_ld16(lane_base + kCColS + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) x[c0 + u] = __uint_as_float(v[u]);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) x[c0 + u] = 0.f;
+                }
+            }
+            mb = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                x[c] = c < G ? x[c] * xs : -INFINITY;
+                mb = fmaxf(mb, x[c]);
+            }
+            lb = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                x[c] = ex2(x[c] - mb);   // 0 past G
+                lb += x[c];
+            }
+            // P row m: keys 0..gp-1 = the first gp / 8 swizzled 16-byte pieces
+            const uint32_t prow = smem_u32(pa) + m * 128;
+#pragma unroll
+            for (int c = 0; c < 64; c += 8)
+                if (c < gp)
+                    sts16(prow + ((((c >> 3)) ^ (m & 7)) << 4),
+                          make_uint4(pack2<T>(x[c], x[c + 1]), pack2<T>(x[c + 2], x[c + 3]),
+                                     pack2<T>(x[c + 4], x[c + 5]), pack2<T>(x[c + 6], x[c + 7])));
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(pfull);
+        } else {
+            ok = false;
+        }
+        if (ok && __all_sync(0xffffffffu, mbar_wait(ofull, 0, abort_flag, p.err))) {
+            tc_fence_after();
+            uint32_t ov[32];
+            const long long row = (long long)bh * n + (write ? i : 0);
+            const float lse_a = write ? p.lse[row] : 0.f;
+            const float lse_b = mb / kLog2e + logf(lb);
+            const float m2 = fmaxf(lse_a, lse_b);
+            const float wa = expf(lse_a - m2), wb = expf(lse_b - m2);
+            const float den = wa + wb;
+            const float fa = wa / den, fb = wb / (lb * den);
+            uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + row * 64);
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                tmem_ld32(lane_base + kCColO + 32 * h, ov);
+                tmem_ld_wait();
+                if (write) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 a = o4[4 * h + k];
+                        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+                        uint32_t r[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int c = 8 * k + 2 * u;
+                            r[u] = pack2<T>(fmaf(lo16<T>(w[u]), fa, __uint_as_float(ov[c]) * fb),
+                                            fmaf(hi16<T>(w[u]), fa, __uint_as_float(ov[c + 1]) * fb));
+                        }
+                        o4[4 * h + k] = make_uint4(r[0], r[1], r[2], r[3]);
+                    }
+                }
+            }
+            if (write) p.lse[row] = m2 + logf(den);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        mbar_wait(ofull, 0, no_abort, nullptr, 100000000ull);
+        __syncwarp();
+        tmem_dealloc(tmem, kCTmemCols);
+    }
+}
+
 // dQg = sum of the key tiles' partials (fixed order): a thread per (slice,
 // query, channel), eight loads in flight
 template <typename T>
@@ -1022,6 +1232,25 @@ cudaError_t launch_global_proj_fwd_tc(DType dt, const TmapSet &mk, const TmapSet
     if (dt == kF16) return launch_fwd_tc_t<__half>(mk, mv, mq, a, st);
     if (dt == kBF16) return launch_fwd_tc_t<__nv_bfloat16>(mk, mv, mq, a, st);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fused_glob_cols_tc(DType dt, const TmapSet &mq, const GlobalRowsArgs &a, cudaStream_t st) {
+    if (a.gl.G > 64 || a.BH > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((a.n + kTcKeys - 1) / kTcKeys), (unsigned)a.BH);
+    const size_t smem = (size_t)tc_cols_smem();
+    cudaError_t e;
+    if (dt == kF16) {
+        e = ensure_smem(reinterpret_cast<const void *>(k_fused_glob_cols_tc<__half>), smem);
+        if (e != cudaSuccess) return e;
+        k_fused_glob_cols_tc<__half><<<grid, kTcThreads, smem, st>>>(mq, a);
+    } else if (dt == kBF16) {
+        e = ensure_smem(reinterpret_cast<const void *>(k_fused_glob_cols_tc<__nv_bfloat16>), smem);
+        if (e != cudaSuccess) return e;
+        k_fused_glob_cols_tc<__nv_bfloat16><<<grid, kTcThreads, smem, st>>>(mq, a);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_fused_glob_rows_chunk(DType dt, const GlobalRowsArgs &a, cudaStream_t st) {

@@ -647,7 +647,20 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
         AttnArgs a{g, scale, O, lse, err};
         cudaStream_t st = as_stream(stream);
         cudaError_t e = launch_band_attention_glob(dt, mq, mk, mv, a, gl, st);
-        if (e == cudaSuccess) e = launch_fused_glob(dt, g, gl, scale, Q, K, V, O, lse, st);
+        bool cols_done = false;
+        if (e == cudaSuccess && gl.G <= 64) {
+            // the global columns on the tensor cores (Q in 128-row boxes)
+            Geom gr{};
+            gr.BH = g.BH;
+            gr.n = g.n;
+            gr.s = 1;
+            TmapSet mq1;
+            if (!build_rows_maps(&mq1, Q, gr, dt, 128)) return SWAB_ERR_CUDA;
+            GlobalRowsArgs r{g.BH, g.n, scale, Q, K, V, O, lse, gl, err};
+            e = launch_fused_glob_cols_tc(dt, mq1, r, st);
+            cols_done = true;
+        }
+        if (e == cudaSuccess) e = launch_fused_glob(dt, g, gl, scale, Q, K, V, O, lse, cols_done, st);
         return from_cuda(e);
     }
     if (dt == kF32) {

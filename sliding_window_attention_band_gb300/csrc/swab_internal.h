@@ -147,10 +147,16 @@ struct GlobalRowsArgs {   // dense rows of the global queries (fused forward)
     void *O;                 // [BH, n, 64]: rows at the global positions written
     float *lse;              // [BH, n]
     GlobArgs gl;
+    unsigned *err;           // device status word (tensor-core kernel)
 };
 cudaError_t launch_fused_glob_rows_chunk(DType dt, const GlobalRowsArgs &a, cudaStream_t st);
+// global columns on the tensor cores (G <= 64): map of Q (128-row boxes),
+// contiguous [BH, n, 64]
+cudaError_t launch_fused_glob_cols_tc(DType dt, const TmapSet &mq, const GlobalRowsArgs &a, cudaStream_t st);
+// cols_done: the global columns were merged already (tensor-core kernel)
 cudaError_t launch_fused_glob(DType dt, const Geom &g, const GlobArgs &gl, float scale, const void *Q,
-                              const void *K, const void *V, void *O, float *lse, cudaStream_t st);
+                              const void *K, const void *V, void *O, float *lse, bool cols_done,
+                              cudaStream_t st);
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                      const TmapSet &mapV, const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st);
