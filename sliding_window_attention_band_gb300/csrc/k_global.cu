@@ -449,6 +449,9 @@ cudaError_t launch_reduce_t(const GlobReduceArgs &a, bool cols, cudaStream_t st)
 //    log-sum-exp;
 //  * k_fused_glob_rows computes every global query's dense attention over all
 //    n keys, overwriting those rows.
+// The tensor-core kernels take both for G <= 64 (columns) and when the
+// (16-query chunk, slice) CTAs of the rows fill the GPU; these two are the
+// general forms.
 // ---------------------------------------------------------------------------
 struct FusedGlobArgs {
     Geom g;
@@ -632,7 +635,7 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArg
 }
 
 template <typename T>
-cudaError_t launch_fused_glob_t(const FusedGlobArgs &a, bool cols_done, cudaStream_t st) {
+cudaError_t launch_fused_glob_t(const FusedGlobArgs &a, bool cols_done, bool rows_done, cudaStream_t st) {
     const int G = a.gl.G;
     cudaError_t e;
     if (!cols_done) {
@@ -644,13 +647,8 @@ cudaError_t launch_fused_glob_t(const FusedGlobArgs &a, bool cols_done, cudaStre
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    // dense global rows: a CTA per 16 global queries of a slice (each K, V tile
-    // read once for them) when those CTAs fill the GPU, else a CTA per query
-    const int sms = device_sm_count();
-    if (sms > 0 && 2LL * ((G + 15) / 16) * a.g.BH >= sms) {
-        GlobalRowsArgs r{a.g.BH, a.g.n, a.scale, a.Q, a.K, a.V, a.O, a.lse, a.gl, nullptr};
-        return launch_fused_glob_rows_chunk(std::is_same<T, __half>::value ? kF16 : kBF16, r, st);
-    }
+    if (rows_done) return cudaSuccess;
+    // dense global rows: a CTA per (global query, slice)
     k_fused_glob_rows<T><<<dim3((unsigned)G, (unsigned)a.g.BH), kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
@@ -661,10 +659,10 @@ size_t glob_bitmap_bytes(int n) { return bitmap_bytes(n); }
 
 cudaError_t launch_fused_glob(DType dt, const Geom &g, const GlobArgs &gl, float scale, const void *Q,
                               const void *K, const void *V, void *O, float *lse, bool cols_done,
-                              cudaStream_t st) {
+                              bool rows_done, cudaStream_t st) {
     FusedGlobArgs a{g, gl, scale, Q, K, V, O, lse};
-    if (dt == kF16) return launch_fused_glob_t<__half>(a, cols_done, st);
-    if (dt == kBF16) return launch_fused_glob_t<__nv_bfloat16>(a, cols_done, st);
+    if (dt == kF16) return launch_fused_glob_t<__half>(a, cols_done, rows_done, st);
+    if (dt == kBF16) return launch_fused_glob_t<__nv_bfloat16>(a, cols_done, rows_done, st);
     return cudaErrorInvalidValue;
 }
 

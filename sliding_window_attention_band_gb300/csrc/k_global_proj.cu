@@ -202,93 +202,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_gproj_fwd(const GlobalProjArgs 
     part[5 + 4 * sub] = acc.w;
 }
 
-// Dense rows of the global queries of the fused forward, for problems with
-// enough (query chunk, slice) pairs to fill the GPU: CTA per (16 global
-// queries, slice) over every key (64-key tiles, the next tile's loads in
-// flight), so each K, V tile is read once for the 16 queries; writes the
-// final O rows at the global positions and their lse.
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 2) k_fused_glob_rows_chunk(const GlobalRowsArgs p) {
-    __shared__ __align__(16) float qs[kGC * kPad], ks[kKT * kPad], vs[kKT * kPad], ps[kGC * kPad];
-    const int gc = blockIdx.x, bh = blockIdx.y;
-    const int G = p.gl.G, n = p.n, t = threadIdx.x;
-    const int g = t >> 4, sub = t & 15;
-    const T *Q = reinterpret_cast<const T *>(p.Q) + (long long)bh * n * 64;
-    const T *Kg = reinterpret_cast<const T *>(p.K) + (long long)bh * n * 64;
-    const T *Vg = reinterpret_cast<const T *>(p.V) + (long long)bh * n * 64;
-    for (int e = t; e < kGC * 64; e += kThreads) {
-        const int r = e >> 6, c = e & 63, gg = gc * kGC + r;
-        qs[r * kPad + c] = gg < G ? Elt<T>::to_f(Q[(long long)p.gl.idx[gg] * 64 + c]) : 0.f;
-    }
-    const float xs = p.scale * kLog2e;
-    float m = -INFINITY, l = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // channels 4 sub .. + 3
-    TileRegs<T> kr, vr;
-    fetch_tile(kr, Kg, 0, n);
-    fetch_tile(vr, Vg, 0, n);
-    for (int j0 = 0; j0 < n; j0 += kKT) {
-        __syncthreads();   // the previous tile's readers are done (and qs is written)
-        store_tile(ks, kr);
-        store_tile(vs, vr);
-        if (j0 + kKT < n) {
-            fetch_tile(kr, Kg, j0 + kKT, n);
-            fetch_tile(vr, Vg, j0 + kKT, n);
-        }
-        __syncthreads();
-        float s[4] = {0.f, 0.f, 0.f, 0.f}, tmax = -INFINITY;
-#pragma unroll 4
-        for (int c = 0; c < 64; c += 4) {
-            const float4 q4 = lds4(qs + g * kPad + c);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) s[u] = dot4(q4, lds4(ks + (sub + 16 * u) * kPad + c), s[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            s[u] = j0 + sub + 16 * u < n ? s[u] * xs : -INFINITY;
-            tmax = fmaxf(tmax, s[u]);
-        }
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-        const float mn = fmaxf(m, tmax);
-        const float corr = m == -INFINITY ? 0.f : ex2(m - mn);
-        float psum = 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float pv = ex2(s[u] - mn);
-            ps[g * kPad + sub + 16 * u] = pv;
-            psum += pv;
-        }
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
-        l = l * corr + psum;
-        m = mn;
-        __syncthreads();
-        acc.x *= corr;
-        acc.y *= corr;
-        acc.z *= corr;
-        acc.w *= corr;
-#pragma unroll 4
-        for (int j = 0; j < kKT; j += 4) {
-            const float4 p4 = lds4(ps + g * kPad + j);
-            const float *vrow = vs + j * kPad + 4 * sub;
-            axpy4(acc, p4.x, lds4(vrow));
-            axpy4(acc, p4.y, lds4(vrow + kPad));
-            axpy4(acc, p4.z, lds4(vrow + 2 * kPad));
-            axpy4(acc, p4.w, lds4(vrow + 3 * kPad));
-        }
-    }
-    const int gg = gc * kGC + g;
-    if (gg >= G) return;
-    const long long row = (long long)bh * n + p.gl.idx[gg];
-    const float inv = 1.f / l;
-    T *o = reinterpret_cast<T *>(p.O) + row * 64 + 4 * sub;
-    o[0] = Elt<T>::from_f(acc.x * inv);
-    o[1] = Elt<T>::from_f(acc.y * inv);
-    o[2] = Elt<T>::from_f(acc.z * inv);
-    o[3] = Elt<T>::from_f(acc.w * inv);
-    if (sub == 0) p.lse[row] = m / kLog2e + logf(l);
-}
-
 // merge the chunks: a warp per (slice, query); lane k < nchunks reads chunk
 // k's (max, sum) at once, then every lane merges two channels over the chunks
 // with eight loads in flight
@@ -1124,6 +1037,274 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Dense global rows of the fused forward on the tensor cores: CTA per (16
+// global queries, slice) over every key, no workspace.  As in the global
+// projections the keys are the M side: S^T = K_c Q^T gives each worker lane
+// one key with the 16 queries' scores in its columns.  Pass 1 walks the
+// 128-key chunks for every query's maximum; pass 2 recomputes S^T, forms
+// P = 2^(s - max) and accumulates O^T += V_c^T P^T in tensor memory while each
+// lane sums its keys' P.  The maximum is final before pass 2, so nothing is
+// rescaled, and the sums are merged once at the end.  K (pass 1) or K and V
+// (pass 2) chunks arrive by TMA through a four-stage ring; S^T and P are
+// double-buffered so a chunk's softmax overlaps the next chunk's product.
+// ---------------------------------------------------------------------------
+constexpr int kRStages = 4;
+constexpr uint32_t kRColS = 0, kRColO = 32;   // S^T buffers at columns 0 and 16, O^T at 32
+constexpr uint32_t kRTmemCols = 64;
+
+__host__ __device__ constexpr int tc_rows_smem() {
+    return 1024 + kRStages * 2 * kTile16 /* V, K ring */ + 2048 /* Q */ + 2 * 4096 /* P */ +
+           2 * 4 * kGC * 4 /* per-warp max, sum */ + 256;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_fused_glob_rows_tc(const __grid_constant__ TmapSet mapK, const __grid_constant__ TmapSet mapV,
+                         const GlobalRowsArgs p) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const int G = p.gl.G, n = p.n, nck = (n + kTcKeys - 1) / kTcKeys, steps = 2 * nck;
+    uint8_t *ring = base;                            // stage b: V at +0, K at +kTile16
+    uint8_t *qbuf = ring + kRStages * 2 * kTile16;   // Q [16 queries][64]
+    uint8_t *pbuf = qbuf + 2048;                     // two P [16 queries][128 keys]
+    float *wmax = reinterpret_cast<float *>(pbuf + 2 * 4096);   // [4 warps][16]
+    float *wsum = wmax + 4 * kGC;                                // [4 warps][16]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(wsum + 4 * kGC);
+    uint64_t *kvfull = bars, *kvempty = bars + kRStages, *sfull = bars + 2 * kRStages, *sempty = sfull + 2,
+             *pfull = sempty + 2, *pempty = pfull + 2, *ofull = pempty + 2, *red = ofull + 1;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(red + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *no_abort = reinterpret_cast<volatile int *>(tmem_holder + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gc = blockIdx.x, bh = blockIdx.y;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRStages; ++i) {
+            mbar_init(&kvfull[i], 1);
+            mbar_init(&kvempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sempty[i], 128);
+            mbar_init(&pfull[i], 128);
+            mbar_init(&pempty[i], 1);
+        }
+        mbar_init(ofull, 1);
+        mbar_init(red, 128);
+        *abort_flag = 0;
+        *no_abort = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x >= 64) {
+        // the 16 queries' rows into the swizzled Q tile, zeros past G
+        const int t = threadIdx.x - 64, j = t >> 3, c = t & 7, gg = gc * kGC + j;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (gg < G) v = ldg16(reinterpret_cast<const T *>(p.Q) + ((long long)bh * n + p.gl.idx[gg]) * 64 + 8 * c);
+        sts16(smem_u32(qbuf) + j * 128 + ((c ^ (j & 7)) << 4), v);
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kRTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    bool ok = true;
+
+    if (warp == 0) {
+        int issued = 0;
+        for (int st = 0; st < steps && ok; ++st) {
+            const int b = st % kRStages, c = st < nck ? st : st - nck;
+            if (!__all_sync(0xffffffffu, mbar_wait(&kvempty[b], ((st / kRStages) & 1) ^ 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                uint8_t *stage = ring + b * 2 * kTile16;
+                mbar_arrive_expect_tx(&kvfull[b], st < nck ? kTile16 : 2 * kTile16);
+                tma_load_3d(stage + kTile16, &mapK.m[0], &kvfull[b], 0, c * kTcKeys, bh);
+                if (st >= nck) tma_load_3d(stage, &mapV.m[0], &kvfull[b], 0, c * kTcKeys, bh);
+            }
+            __syncwarp();
+            ++issued;
+        }
+        // the copies still in flight land before the CTA ends
+        for (int k = issued > kRStages ? issued - kRStages : 0; k < issued; ++k)
+            mbar_wait(&kvfull[k % kRStages], (k / kRStages) & 1, no_abort, nullptr, 100000000ull);
+    } else if (warp == 1) {
+        constexpr bool kBf16 = !std::is_same<T, __half>::value;
+        constexpr uint32_t id_s = idesc_f16(kTcKeys, kGC, kBf16, false, false);   // S^T = K Q^T
+        constexpr uint32_t id_o = idesc_f16(kTcKeys, kGC, kBf16, true, false);    // O^T += V^T P^T
+        const uint64_t d_q = sdesc_sw128(smem_u32(qbuf), 16, 1024);
+        const uint64_t d_k = sdesc_sw128(smem_u32(ring + kTile16), 16, 1024);
+        // V^T as an MN-major A of 128 rows: its second 64-row block is the
+        // stage's K tile, and those output lanes are never read
+        const uint64_t d_vmn = sdesc_sw128(smem_u32(ring), kTile16, 1024);
+        const uint64_t d_p = sdesc_sw128(smem_u32(pbuf), 16, 1024);
+        // O^T += V_c^T P_c^T for the pass-2 step u, once its P is written
+        auto pv = [&](int u) -> bool {
+            const int c2 = u - nck, pi = c2 & 1, bu = u % kRStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&pfull[pi], (c2 >> 1) & 1, abort_flag, p.err))) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t voff = (uint64_t)((bu * 2 * kTile16) >> 4);
+#pragma unroll
+                for (int k = 0; k < kTcKeys / 16; ++k) {
+                    const uint64_t a = d_vmn + voff + (uint64_t)((2048 * k) >> 4);
+                    const uint64_t b = d_p + (uint64_t)((pi * 4096 + (k >> 2) * 2048 + (k & 3) * 32) >> 4);
+                    mma_f16_ss(tmem + kRColO, a, b, id_o, (c2 > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(&pempty[pi]);
+                mma_commit(&kvempty[bu]);
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int st = 0; st < steps && ok; ++st) {
+            const int b = st % kRStages, sb = st & 1;
+            bool w = mbar_wait(&kvfull[b], (st / kRStages) & 1, abort_flag, p.err);
+            w = w && mbar_wait(&sempty[sb], ((st >> 1) & 1) ^ 1, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, w)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t koff = (uint64_t)((b * 2 * kTile16) >> 4);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_f16_ss(tmem + kRColS + 16 * sb, d_k + koff + 2 * k, d_q + 2 * k, id_s, k > 0 ? 1u : 0u);
+                mma_commit(&sfull[sb]);
+                if (st < nck) mma_commit(&kvempty[b]);   // pass 1 needs only K
+            }
+            __syncwarp();
+            // the previous chunk's product, issued after this one's scores
+            if (st > nck && !pv(st - 1)) ok = false;
+        }
+        if (ok && !pv(steps - 1)) ok = false;
+        if (lane == 0) mma_commit(ofull);   // also: every product issued is complete
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3, wi = warp - 2, m = quarter * 32 + lane;
+        const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
+        const float xs = p.scale * kLog2e;
+        float mx[kGC], ls[kGC];
+#pragma unroll
+        for (int q = 0; q < kGC; ++q) {
+            mx[q] = -INFINITY;
+            ls[q] = 0.f;
+        }
+        for (int st = 0; st < steps && ok; ++st) {
+            const int sb = st & 1, c = st < nck ? st : st - nck;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sfull[sb], (st >> 1) & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[16];
+            tmem_ld16(lane_base + kRColS + 16 * sb, sv);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&sempty[sb]);   // the scores are in registers
+            const bool kvalid = c * kTcKeys + m < n;
+            if (st < nck) {
+                if (kvalid) {
+#pragma unroll
+                    for (int q = 0; q < kGC; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(sv[q]) * xs);
+                }
+                if (st == nck - 1) {
+                    // every query's maximum: the warp's keys, then the four warps
+#pragma unroll
+                    for (int q = 0; q < kGC; ++q) {
+                        float v = mx[q];
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                        if (lane == q) wmax[wi * kGC + q] = v;
+                    }
+                    mbar_arrive(red);
+                    if (!__all_sync(0xffffffffu, mbar_wait(red, 0, abort_flag, p.err))) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int q = 0; q < kGC; ++q)
+                        mx[q] = max3(wmax[q], wmax[kGC + q], fmaxf(wmax[2 * kGC + q], wmax[3 * kGC + q]));
+                }
+            } else {
+                const int c2 = st - nck, pi = c2 & 1;
+                float pr[kGC];
+#pragma unroll
+                for (int q = 0; q < kGC; ++q) {
+                    pr[q] = kvalid ? ex2(__uint_as_float(sv[q]) * xs - mx[q]) : 0.f;
+                    ls[q] += pr[q];
+                }
+                if (!__all_sync(0xffffffffu, mbar_wait(&pempty[pi], ((c2 >> 1) & 1) ^ 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                // key m's column of P [query][key] (two 64-key blocks, 128-byte swizzled rows)
+                uint16_t *blk = reinterpret_cast<uint16_t *>(pbuf + pi * 4096 + (m >> 6) * 2048);
+                const int col = m & 63;
+#pragma unroll
+                for (int q = 0; q < kGC; q += 2) {
+                    const uint32_t w2 = pack2<T>(pr[q], pr[q + 1]);
+                    blk[q * 64 + (((col >> 3) ^ (q & 7)) << 3) + (col & 7)] = (uint16_t)(w2 & 0xffffu);
+                    blk[(q + 1) * 64 + (((col >> 3) ^ ((q + 1) & 7)) << 3) + (col & 7)] = (uint16_t)(w2 >> 16);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&pfull[pi]);
+            }
+        }
+        if (ok) {
+            // every query's sum over the keys: the warp's lanes, then the four warps
+#pragma unroll
+            for (int q = 0; q < kGC; ++q) {
+                float v = ls[q];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == q) wsum[wi * kGC + q] = v;
+            }
+            mbar_arrive(red);
+            ok = __all_sync(0xffffffffu, mbar_wait(red, 1, abort_flag, p.err));
+        }
+        if (ok && __all_sync(0xffffffffu, mbar_wait(ofull, 0, abort_flag, p.err))) {
+            tc_fence_after();
+            float inv[kGC];
+#pragma unroll
+            for (int q = 0; q < kGC; ++q) {
+                const float l = (wsum[q] + wsum[kGC + q]) + (wsum[2 * kGC + q] + wsum[3 * kGC + q]);
+                inv[q] = 1.f / l;
+                const int gg = gc * kGC + q;
+                if (wi == 0 && lane == q && gg < G)
+                    p.lse[(long long)bh * n + p.gl.idx[gg]] = mx[q] / kLog2e + logf(l);
+            }
+            if (quarter < 2) {   // TMEM lanes 0-63: the 64 channels of O^T
+                uint32_t ov[16];
+                tmem_ld16(lane_base + kRColO, ov);
+                tmem_ld_wait();
+                T *O = reinterpret_cast<T *>(p.O);
+#pragma unroll
+                for (int q = 0; q < kGC; ++q) {
+                    const int gg = gc * kGC + q;
+                    if (gg < G)
+                        O[((long long)bh * n + p.gl.idx[gg]) * 64 + m] = Elt<T>::from_f(__uint_as_float(ov[q]) * inv[q]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        mbar_wait(ofull, 0, no_abort, nullptr, 100000000ull);
+        __syncwarp();
+        tmem_dealloc(tmem, kRTmemCols);
+    }
+}
+
 // dQg = sum of the key tiles' partials (fixed order): a thread per (slice,
 // query, channel), eight loads in flight
 template <typename T>
@@ -1253,11 +1434,23 @@ cudaError_t launch_fused_glob_cols_tc(DType dt, const TmapSet &mq, const GlobalR
     return cudaGetLastError();
 }
 
-cudaError_t launch_fused_glob_rows_chunk(DType dt, const GlobalRowsArgs &a, cudaStream_t st) {
+cudaError_t launch_fused_glob_rows_tc(DType dt, const TmapSet &mk, const TmapSet &mv, const GlobalRowsArgs &a,
+                                      cudaStream_t st) {
+    if (a.BH > 65535) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)((a.gl.G + kGC - 1) / kGC), (unsigned)a.BH);
-    if (dt == kF16) k_fused_glob_rows_chunk<__half><<<grid, kThreads, 0, st>>>(a);
-    else if (dt == kBF16) k_fused_glob_rows_chunk<__nv_bfloat16><<<grid, kThreads, 0, st>>>(a);
-    else return cudaErrorInvalidValue;
+    const size_t smem = (size_t)tc_rows_smem();
+    cudaError_t e;
+    if (dt == kF16) {
+        e = ensure_smem(reinterpret_cast<const void *>(k_fused_glob_rows_tc<__half>), smem);
+        if (e != cudaSuccess) return e;
+        k_fused_glob_rows_tc<__half><<<grid, kTcThreads, smem, st>>>(mk, mv, a);
+    } else if (dt == kBF16) {
+        e = ensure_smem(reinterpret_cast<const void *>(k_fused_glob_rows_tc<__nv_bfloat16>), smem);
+        if (e != cudaSuccess) return e;
+        k_fused_glob_rows_tc<__nv_bfloat16><<<grid, kTcThreads, smem, st>>>(mk, mv, a);
+    } else {
+        return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

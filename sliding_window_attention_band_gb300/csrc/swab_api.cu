@@ -647,20 +647,30 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
         AttnArgs a{g, scale, O, lse, err};
         cudaStream_t st = as_stream(stream);
         cudaError_t e = launch_band_attention_glob(dt, mq, mk, mv, a, gl, st);
-        bool cols_done = false;
+        Geom gr{};   // rows of [BH, n, 64] in 128-row boxes
+        gr.BH = g.BH;
+        gr.n = g.n;
+        gr.s = 1;
+        GlobalRowsArgs r{g.BH, g.n, scale, Q, K, V, O, lse, gl, err};
+        bool cols_done = false, rows_done = false;
         if (e == cudaSuccess && gl.G <= 64) {
-            // the global columns on the tensor cores (Q in 128-row boxes)
-            Geom gr{};
-            gr.BH = g.BH;
-            gr.n = g.n;
-            gr.s = 1;
+            // the global columns on the tensor cores
             TmapSet mq1;
             if (!build_rows_maps(&mq1, Q, gr, dt, 128)) return SWAB_ERR_CUDA;
-            GlobalRowsArgs r{g.BH, g.n, scale, Q, K, V, O, lse, gl, err};
             e = launch_fused_glob_cols_tc(dt, mq1, r, st);
             cols_done = true;
         }
-        if (e == cudaSuccess) e = launch_fused_glob(dt, g, gl, scale, Q, K, V, O, lse, cols_done, st);
+        const int sms = device_sm_count();
+        if (e == cudaSuccess && sms > 0 && 2LL * ((gl.G + 15) / 16) * g.BH >= sms) {
+            // the dense global rows on the tensor cores, when their (16-query
+            // chunk, slice) CTAs fill the GPU
+            TmapSet mk1, mv1;
+            if (!build_rows_maps(&mk1, K, gr, dt, 128) || !build_rows_maps(&mv1, V, gr, dt, 128))
+                return SWAB_ERR_CUDA;
+            e = launch_fused_glob_rows_tc(dt, mk1, mv1, r, st);
+            rows_done = true;
+        }
+        if (e == cudaSuccess) e = launch_fused_glob(dt, g, gl, scale, Q, K, V, O, lse, cols_done, rows_done, st);
         return from_cuda(e);
     }
     if (dt == kF32) {

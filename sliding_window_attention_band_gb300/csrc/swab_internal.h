@@ -149,14 +149,18 @@ struct GlobalRowsArgs {   // dense rows of the global queries (fused forward)
     GlobArgs gl;
     unsigned *err;           // device status word (tensor-core kernel)
 };
-cudaError_t launch_fused_glob_rows_chunk(DType dt, const GlobalRowsArgs &a, cudaStream_t st);
 // global columns on the tensor cores (G <= 64): map of Q (128-row boxes),
 // contiguous [BH, n, 64]
 cudaError_t launch_fused_glob_cols_tc(DType dt, const TmapSet &mq, const GlobalRowsArgs &a, cudaStream_t st);
-// cols_done: the global columns were merged already (tensor-core kernel)
+// dense global rows on the tensor cores: maps of K, V (128-row boxes),
+// contiguous [BH, n, 64]; f16/bf16
+cudaError_t launch_fused_glob_rows_tc(DType dt, const TmapSet &mk, const TmapSet &mv, const GlobalRowsArgs &a,
+                                      cudaStream_t st);
+// cols_done / rows_done: the global columns were merged / the dense global
+// rows written already (tensor-core kernels)
 cudaError_t launch_fused_glob(DType dt, const Geom &g, const GlobArgs &gl, float scale, const void *Q,
                               const void *K, const void *V, void *O, float *lse, bool cols_done,
-                              cudaStream_t st);
+                              bool rows_done, cudaStream_t st);
 cudaError_t launch_band_attention_tc(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                      const TmapSet &mapV, const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st);

@@ -53,6 +53,27 @@ def test_fused_forward_globals(case):
     check(d, Q, K, V, 0.125, range(BH))
 
 
+# enough (16-query chunk, slice) pairs to fill the GPU, so the dense global
+# rows run on the tensor-core kernel: ragged key tails (777 = 6 x 128 + 9,
+# 129 = 128 + 1), a single key chunk (n = 50), a partial last query chunk
+# (G = 21) and four query chunks (G = 63); three slices checked
+TC_ROWS_CASES = [
+    (80, 777, 100, 37, 2, torch.bfloat16, (0, 3, 20, 21, 400) + tuple(range(500, 776, 18))),
+    (96, 129, 0, 0, 0, torch.float16, (0, 128)),
+    (100, 50, 10, 10, 0, torch.float16, (3, 49)),
+    (24, 1000, 64, 64, 0, torch.float16, tuple(range(0, 1000, 16))[:64]),
+]
+
+
+@pytest.mark.parametrize("case", TC_ROWS_CASES, ids=ids)
+def test_fused_forward_globals_tensor_core_rows(case):
+    BH, n, w, wu, dil, dtype, gidx = case
+    assert 2 * ((len(gidx) + 15) // 16) * BH >= torch.cuda.get_device_properties(0).multi_processor_count
+    d = swab.Desc(1, BH, n, 64, w, wu, dil, 0.0, dtype, gidx)
+    Q, K, V, _ = seeded_qkvo(BH, n, 64, dtype, seed=n + 5)
+    check(d, Q, K, V, 0.125, (0, BH // 2 + 1, BH - 1))
+
+
 def test_fused_forward_globals_matches_materialised():
     """The fused forward and the materialised chain agree with global tokens."""
     BH, n, gidx = 2, 900, (0, 5, 450, 899)
