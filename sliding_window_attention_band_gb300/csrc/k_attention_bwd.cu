@@ -75,10 +75,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ void named_bar(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // Write 32 packed values (16 words) of row `row` into a K-major 128-B-swizzled
 // 128 x 128 operand at key/query group `grp` (32 columns).
 __device__ __forceinline__ void store_op_row(uint32_t op_addr, int row, int grp,
@@ -204,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *opfull = sempty + 1;            // 1, count 128
     uint64_t *opempty = opfull + 1;           // 1
     uint64_t *accfull = opempty + 1;          // 1
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(accfull + 1);
+    uint64_t *statbar = accfull + 1;          // 1, count kWorkers: a chunk's lse, delta written
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(statbar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const Geom &g = p.g;
@@ -228,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(opfull, kWorkers);
         mbar_init(opempty, 1);
         mbar_init(accfull, 1);
+        mbar_init(statbar, kWorkers);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -316,7 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (tid < kB) ql[qi] = qq < nr ? p.lse[row] * kLog2e : INFINITY;
                 else ql[kB + qi] = qq < nr ? p.delta[row] : 0.f;
             }
-            named_bar(1, kWorkers);
+            // every worker's statistics are in (a bounded wait: a timeout
+            // anywhere lets every warp leave)
+            mbar_arrive(statbar);
+            if (!__all_sync(0xffffffffu, mbar_wait(statbar, c & 1, abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
             // this key's queries inside the chunk: columns [jlo, jhi]
             const int jlo = max(kk - g.wu - qbase, 0);
             const int jhi = min(min(kk + g.w, qb_hi) - qbase, kB - 1);

@@ -658,8 +658,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float *wsum = wmax + 4 * kGC;                               // [4 warps][16]
     uint64_t *bars = reinterpret_cast<uint64_t *>(wsum + 4 * kGC);
     uint64_t *ldfull = bars, *sfull = bars + 1, *pfull = bars + 2, *ofull = bars + 3, *odone = bars + 4,
-             *alldone = bars + 5;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 6);
+             *alldone = bars + 5, *wbar = bars + 6;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 7);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *no_abort = reinterpret_cast<volatile int *>(tmem_holder + 2);
 
@@ -672,6 +672,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(ofull, 1);
         mbar_init(odone, 128);
         mbar_init(alldone, 1);
+        mbar_init(wbar, 128);
         *abort_flag = 0;
         *no_abort = 0;
         fence_barrier_init();
@@ -739,6 +740,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
         const bool kvalid = j0 + m < n;
         const float xs = p.scale * kLog2e;
+        // the four worker warps meet on wbar (bounded waits, so a timeout
+        // anywhere lets every warp leave); nb counts its phases
+        uint32_t nb = 0;
+        auto meet = [&]() -> bool {
+            mbar_arrive(wbar);
+            return __all_sync(0xffffffffu, mbar_wait(wbar, (nb++) & 1, abort_flag, p.err));
+        };
         for (int c = 0; c < nch && ok; ++c) {
             if (!__all_sync(0xffffffffu, mbar_wait(sfull, c & 1, abort_flag, p.err))) {
                 ok = false;
@@ -759,7 +767,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
                 if (lane == q) wmax[wi * kGC + q] = v;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (!meet()) {
+                ok = false;
+                break;
+            }
             float pr[16];
 #pragma unroll
             for (int q = 0; q < kGC; ++q) {
@@ -788,7 +799,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
                 if (lane == q) wsum[wi * kGC + q] = v;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (!meet()) {
+                ok = false;
+                break;
+            }
             // the partial of (slice, tile, query): [max (log2 units), sum, O[64]]
             float *part = p.ws + ((long long)bh * p.nchunks + kt) * G * 66;
             if (t < kGC && c * kGC + t < G) {
@@ -813,7 +827,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_before();
             // the next chunk's maxima and sums overwrite these slots
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (!meet()) {
+                ok = false;
+                break;
+            }
             mbar_arrive(odone);
         }
     }
