@@ -108,6 +108,13 @@ __device__ __forceinline__ void mma_tiles(uint32_t d, uint32_t a_addr, uint32_t 
                    idesc, k > 0);
 }
 
+// Programmatic dependent launch: a kernel launched with the stream
+// serialization attribute may start while the kernel before it runs; it
+// waits for that kernel's completion (and its memory) before reading what it
+// wrote.  Without the attribute both instructions do nothing.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------------------
 // delta_i = dO_i . O_i: 8 lanes per row, 16-byte loads, each warp keeps 4
 // groups of 4 rows (16 rows, 8 loads per lane) in flight before reducing.
@@ -116,6 +123,7 @@ constexpr int kDeltaRowsPerWarp = 16;
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
+    pdl_trigger();   // the one-pass kernel may start its loads
     const long long rows = (long long)p.g.BH * p.g.n;
     const int lane = threadIdx.x & 31;
     const long long warp_row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kDeltaRowsPerWarp;
@@ -162,6 +170,7 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
 // dQ = scale * accumulator, rounded to the output type: 8 channels per thread
 template <typename T>
 __global__ void __launch_bounds__(256) k_bwd_dq_out(const BwdArgs p) {
+    pdl_wait();   // every dQ addition of the one-pass kernel has landed
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8-channel group
     if (i >= (long long)p.g.BH * p.g.n * 8) return;
     const float4 *acc = reinterpret_cast<const float4 *>(p.dqacc) + 2 * i;
@@ -737,6 +746,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    pdl_trigger();   // the dQ rounding may be scheduled (it waits for this grid)
     if (warp == 1) {
         tmem_alloc(tmem_holder, kTmemCols);
         tmem_relinquish();
@@ -902,6 +912,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         mbar_wait(mmadone, 0, no_abort, nullptr, 100000000ull);
     } else if (warp == kReducerWarp) {
         // ---------------- reducer: staged dQ tiles into the accumulator ----------------
+        pdl_wait();   // the row-sum kernel has cleared the accumulator
         uint32_t gc = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -928,6 +939,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         __syncwarp();
     } else {
         // ---------------- softmax warps: thread = key row ----------------
+        pdl_wait();   // the row sums delta are written
         const int quarter = warp & 3;
         const int part = (warp - 2) >> 2;        // query columns [32 part, 32 part + 32)
         const int m = quarter * 32 + lane;       // TMEM lane: key of the tile / query of a dQ chunk
@@ -1289,12 +1301,25 @@ cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &
     const int grid = (int)(tiles < sms ? tiles : sms);
     e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, kBias, kDrop>), fused::kSmem);
     if (e != cudaSuccess) return e;
-    k_bwd_fused<T, kBias, kDrop><<<grid, fused::kThreads, fused::kSmem, st>>>(mq, mk, mv, mo, macc, a);
-    e = cudaGetLastError();
+    // the one-pass kernel and the dQ rounding start early (programmatic
+    // dependent launch) and wait inside for what the kernel before wrote
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(fused::kThreads);
+    cfg.dynamicSmemBytes = fused::kSmem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_bwd_fused<T, kBias, kDrop>, mq, mk, mv, mo, macc, a);
     if (e != cudaSuccess) return e;
     const long long groups = rows * 8;
-    k_bwd_dq_out<T><<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(a);
-    return cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)((groups + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, k_bwd_dq_out<T>, a);
 }
 
 }  // namespace
