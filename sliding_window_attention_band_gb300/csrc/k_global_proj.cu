@@ -637,6 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // kernel merges the tiles.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kFColS = 0, kFColO = 32;
+constexpr uint32_t kFTmemCols = 64;   // S^T at columns 0-15, O^T at 32-47
 
 __host__ __device__ constexpr int tc_fwd_smem(int nch) {
     return 1024 + 2 * kTile16 /* K, V */ + nch * 2048 /* Qg */ + 2 * 2048 /* P [query][key] */ +
@@ -644,7 +645,7 @@ __host__ __device__ constexpr int tc_fwd_smem(int nch) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 4)
     k_gproj_fwd_tc(const __grid_constant__ TmapSet mapK, const __grid_constant__ TmapSet mapV,
                    const __grid_constant__ TmapSet mapQ, const GlobalProjArgs p) {
     extern __shared__ uint8_t smraw[];
@@ -678,7 +679,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, kTcTmemCols);
+        tmem_alloc(tmem_holder, kFTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -840,7 +841,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) {
         mbar_wait(alldone, 0, no_abort, nullptr, 100000000ull);
         __syncwarp();
-        tmem_dealloc(tmem, kTcTmemCols);
+        tmem_dealloc(tmem, kFTmemCols);
     }
 }
 
@@ -1363,7 +1364,7 @@ cudaError_t launch_fwd_tc_t(const TmapSet &mk, const TmapSet &mv, const TmapSet 
                             cudaStream_t st) {
     a.nchunks = (a.n + kTcKeys - 1) / kTcKeys;
     const int nch = (a.G + kGC - 1) / kGC;
-    const size_t smem = (size_t)max(tc_fwd_smem(nch), 80 * 1024);   // two CTAs per SM (TMEM)
+    const size_t smem = (size_t)tc_fwd_smem(nch);   // up to four CTAs per SM (64 TMEM columns each)
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gproj_fwd_tc<T>), smem);
     if (e != cudaSuccess) return e;
     k_gproj_fwd_tc<T><<<dim3(a.nchunks, a.BH), kTcThreads, smem, st>>>(mk, mv, mq, a);
