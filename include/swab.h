@@ -280,6 +280,10 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
  * rounding of one fp32 sum; band_attention_bwd_noalloc is bitwise
  * repeatable).  For fp32 it holds the delta only and every output is
  * repeatable.
+ * For fp16 / bf16 the call launches three kernels.  The last two are launched
+ * as programmatic dependents: they may start while the one before runs and
+ * wait inside for what it wrote.  For the caller the call stays ordered on
+ * the stream like any kernel launch.
  * Global tokens are not supported here (n_global must be 0). */
 SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, const void *Q,
                                         const void *K, const void *V, const void *O,
