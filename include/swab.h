@@ -12,7 +12,7 @@
  *   Post 6 names three modes of one kernel: the forward product (dense x
  *   dense^T -> band, t3d3 = 2w+1) and two backward products (band x dense,
  *   transpose_t1 = 0, and band^T x dense, transpose_t1 = 1).  The author
- *   merged them into one function only because he could not put several
+ *   merged them into one function only because they could not put several
  *   kernels into one .so; here they are separate entry points.
  *
  * Global tokens ("[WIP] Improve LongformerAttention performance", ONNX
