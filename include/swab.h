@@ -275,10 +275,11 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
  * `workspace` is caller-owned device memory of band_attention_bwd_workspace()
  * bytes, 16-byte aligned; its contents on entry do not matter.  For fp16 /
  * bf16 it holds the per-row delta and an fp32 dQ accumulator: dK and dV have
- * one writer per row, while dQ is summed over key tiles with fp32 atomic
- * additions, so dQ may differ in its last bits from run to run (within the
- * rounding of one fp32 sum; band_attention_bwd_noalloc is bitwise
- * repeatable).  For fp32 it holds the delta only and every output is
+ * one writer per row, while each key tile's contribution to dQ is added into
+ * the accumulator by TMA reduce-add stores (cp.reduce.async.bulk.tensor, fp32
+ * additions in the memory system) in an order that varies between runs, so
+ * dQ may differ in its last bits from run to run (within the rounding of one
+ * fp32 sum; band_attention_bwd_noalloc is bitwise repeatable).  For fp32 it holds the delta only and every output is
  * repeatable.
  * For fp16 / bf16 the call launches three kernels.  The last two are launched
  * as programmatic dependents: they may start while the one before runs and
@@ -310,7 +311,11 @@ SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc);
  *     SWAB_ERR_UNSUPPORTED (use band_attention_bwd with a workspace).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  A first call made while `stream` is being captured
+ *     returns SWAB_ERR_UNSUPPORTED and launches nothing.
+ *   - The cached address belongs to the device's context at the first call:
+ *     resetting the device (cudaDeviceReset) after that call is not
+ *     supported, since later calls would use the old address.
  *   - All calls share the one array, which keeps the last call's contents
  *     (every call overwrites what it reads before reading it).  Calls whose
  *     executions overlap on the GPU -- on different streams, or from different

@@ -39,8 +39,10 @@ static __device__ __align__(256) float g_noalloc_delta[SWAB_NOALLOC_MAX_ROWS];
 // Device address of g_noalloc_delta on the current device.  In host code the
 // array's name only stands in for the symbol, so the address is looked up
 // with cudaGetSymbolAddress, once per device (the first call on a device does
-// it) and cached.
-cudaError_t noalloc_delta_scratch(float **out) {
+// it) and cached.  The lookup may load the module, which must not happen
+// while `st` is being captured: a first call under capture is refused
+// (cudaErrorStreamCaptureUnsupported) before anything is looked up.
+cudaError_t noalloc_delta_scratch(float **out, cudaStream_t st) {
     static std::mutex mu;
     static float *cache[128] = {};
     int dev = 0;
@@ -49,6 +51,10 @@ cudaError_t noalloc_delta_scratch(float **out) {
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!cache[dev]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(st, &cs);
+        if (e != cudaSuccess) return e;
+        if (cs != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
         void *ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_delta);
         if (e != cudaSuccess) return e;

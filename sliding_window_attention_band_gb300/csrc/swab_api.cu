@@ -741,9 +741,11 @@ SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float sca
     if (g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;    // nor dropout
     if (g.rs_p || g.rs_o) return SWAB_ERR_UNSUPPORTED;  // nor the strided layout
     if ((s = check_ptrs({Q, K, V, O, dO, lse, dQ, dK, dV})) != SWAB_OK) return s;
-    float *scratch = nullptr;
-    if (noalloc_delta_scratch(&scratch) != cudaSuccess) return SWAB_ERR_CUDA;
     cudaStream_t st = as_stream(stream);
+    float *scratch = nullptr;
+    const cudaError_t se = noalloc_delta_scratch(&scratch, st);
+    if (se == cudaErrorStreamCaptureUnsupported) return SWAB_ERR_UNSUPPORTED;
+    if (se != cudaSuccess) return SWAB_ERR_CUDA;
     BwdArgs a{g, scale, Q, K, V, O, dO, lse, scratch, dQ, dK, dV, nullptr};
     if (dt == kF32) return from_cuda(launch_band_attention_bwd_f32(a, st));
     TmapSet mq, mk, mv, mo;

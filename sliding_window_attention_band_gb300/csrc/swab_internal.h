@@ -176,8 +176,10 @@ cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const T
 int device_sm_count();
 // dynamic shared-memory limit of a kernel, set once per (kernel, device) (swab_api.cu)
 cudaError_t ensure_smem(const void *kernel, int bytes);
-// the module-scope delta scratch of band_attention_bwd_noalloc (k_attention_bwd.cu)
-cudaError_t noalloc_delta_scratch(float **out);
+// the module-scope delta scratch of band_attention_bwd_noalloc (k_attention_bwd.cu);
+// cudaErrorStreamCaptureUnsupported when the first lookup on a device would
+// run while `st` is being captured
+cudaError_t noalloc_delta_scratch(float **out, cudaStream_t st);
 // fp32 FFMA paths
 cudaError_t launch_band_qk_f32(const DenseArgs &a, cudaStream_t st);
 cudaError_t launch_band_pv_f32(const DenseArgs &a, cudaStream_t st);
