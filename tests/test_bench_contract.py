@@ -28,6 +28,10 @@ def test_reference_arm_json_line():
     assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["config"]["workload"] == "longformer_base_fp16_n4096_w256_d0"
     assert d["value"] > 0
+    # the line reports the work it timed: value = the step's flops / its time
+    fl = d["config"]["flops_per_step"]
+    assert d["config"]["slices_per_step"] == 1
+    assert abs(fl / (d["ms_per_step"] * 1e-3) / 1e12 - d["value"]) <= 1e-3 * d["value"] + 1e-6
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert cb["sample"]
