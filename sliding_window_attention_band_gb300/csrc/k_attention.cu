@@ -9,34 +9,39 @@
 // (rows r + s*a, a in [a0, a0+128)).  The kernel is persistent: one CTA per
 // SM walks the tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...; a per-CTA
 // chunk counter runs across tiles, so the K/V ring, the score and P buffers
-// and their barriers carry straight on from one tile into the next (the
-// next tile's Q and K/V loads and its first Q.K^T product overlap the
-// current tile's epilogue).  For chunk c (128 keys) of a tile:
-//   1. MMA warp: S_c = Q . K_c^T (tcgen05, M = 128 queries, N = 128 keys,
-//      K = 64) into TMEM score buffer c%2;
-//   2. softmax warps: four per TMEM lane quarter, warp part j owning chunk
-//      columns [32j, 32j+32) of its 32 rows (thread = query row).  Each keeps
-//      its own reference max m (log2 domain) and sum l; m is raised only when
-//      the chunk's largest score exceeds it by more than 2^8, so p = 2^(x-m)
-//      <= 2^8 stays well inside fp16/bf16.  p is written as the K-major,
-//      128-B-swizzled A operand of the next product;
-//   3. MMA warp: O_j += P_c[:, part j] . V_c[part j] into part j's own fp32
-//      accumulator in TMEM (4 x 64 columns), so no accumulator lives in
-//      registers; when a part raises m it rescales its own accumulator rows
-//      in place (tcgen05.ld / st) before the product that uses the new m.
-// Tile epilogue: the four parts of a row exchange (m_j, l_j) through shared
-// memory; part j then reads channels [16j, 16j+16) of all four accumulators,
-// combines them (O = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j) and
-// writes them out; lse = M ln 2 + ln L.  The chunk sequence runs on across
-// tiles: a tile's epilogue runs in the next tile's first chunk, after that
-// chunk's softmax and before its P tile is signalled (its P.V product
-// overwrites the accumulators), so the next tile's first Q.K^T and softmax
-// overlap the tile's last P.V.
+// and their barriers carry straight on from one tile into the next.  For
+// chunk c (128 keys) of a tile, with b = c mod 2:
+//   1. MMA thread: S_b = Q . K_c^T (tcgen05, M = 128 queries, N = 128 keys,
+//      K = 64) into tensor-memory score buffer b;
+//   2. softmax warps, two per TMEM lane quarter: the warp of half h owns keys
+//      [64h, 64h+64) of the chunk for its 32 query rows (thread = row).  It
+//      copies its 64 scores to registers (which frees S_b for chunk c+2),
+//      applies the band as per-32-key masks (warp-uniform fast paths for
+//      groups that are full or empty for the whole warp), takes the max and
+//      p = 2^(x*scale*log2e - m_h) with packed fp32x2 arithmetic and ex2,
+//      and packs p to 16 bits into its 32 columns of the tensor-memory P
+//      buffer b.  Each half keeps its own reference max m_h and sum l_h, and
+//      raises m_h only when a chunk's largest score exceeds it by more than
+//      2^8 (p <= 2^8 stays inside fp16 / bf16); its accumulator rows are
+//      rescaled in place then (rare);
+//   3. MMA thread: O_h += P_b[:, half h] . V_c[half h] for h = 0, 1 (A read
+//      from tensor memory, B = V rows from shared memory, N = 64) into the
+//      half's own fp32 accumulator.
+// S and P are double-buffered, so a chunk's softmax overlaps the next
+// chunk's Q.K^T and the previous chunk's P.V; nothing waits for the previous
+// P.V except a rescale and the tile's epilogue.  The epilogue (in the next
+// tile's first chunk, after its P is written and before it is signalled)
+// exchanges (m_h, l_h) between the two halves of a row through shared memory
+// and writes O = sum_h 2^(m_h - M) O_h / sum_h 2^(m_h - M) l_h, each half 32
+// channels, and lse = M ln 2 + ln L.
 //
-// Warps: 0 = TMA producer (Q double-buffered, K and V chunks into a 3-stage
-// ring), 1 = TMEM owner + MMA issuer, 2..17 = softmax / epilogue.  Every
-// wait is a bounded mbarrier wait (no bar.sync inside the loops), so a
-// timeout anywhere lets every warp leave.
+// Warps: 0 = TMA producer (Q double-buffered, K and V chunks into a 4-stage
+// ring), 1 = TMEM owner + MMA issuer, 2..9 = softmax / epilogue.  In the
+// producer and MMA warps one lane does the work and the others go straight
+// to the final barrier.  (The two roles do not share a warp: a lane spinning
+// on a barrier starves a diverged lane of the same warp.)  Every wait is a
+// bounded mbarrier wait (no bar.sync inside the loops), so a timeout
+// anywhere lets every thread leave.
 #include <type_traits>
 
 #include "swab_internal.h"
@@ -46,22 +51,23 @@ namespace {
 
 constexpr int kBQ = 128;        // queries per tile (M)
 constexpr int kBK = 128;        // keys per chunk (N of S, K of P.V)
-constexpr int kStages = 3;      // K/V ring
-constexpr int kParts = 4;       // key parts of a chunk: 32 keys each
-constexpr int kWorkerWarps = 4 * kParts;
-constexpr int kWorkers = 32 * kWorkerWarps;     // 512
+constexpr int kHalf = 64;       // keys of a chunk per softmax thread
+constexpr int kStages = 4;      // K/V ring
+constexpr int kWorkerWarps = 8; // two per TMEM lane quarter
+constexpr int kWorkers = 32 * kWorkerWarps;     // 256
 constexpr int kThreads = 64 + kWorkers;         // producer, MMA, softmax warps
-constexpr int kQBytes = kBQ * 128;              // 16 KB
-constexpr int kKBytes = kBK * 128;              // 16 KB
-constexpr int kStageBytes = 2 * kKBytes;        // K and V: 32 KB
-constexpr int kPBytes = kBQ * kBK * 2;          // 32 KB (two 64-key K-atoms)
-constexpr int kMlBytes = 2 * kParts * kBQ * 8;  // (m, l) exchange, two tile parities
-constexpr int kBiasSlotBytes = kWorkerWarps * 32 * 4;  // key bias of each warp's 32 keys
-constexpr int kSmemBytes =
-    2 * kQBytes + kStages * kStageBytes + 2 * kPBytes + kMlBytes + kBiasSlotBytes + 1024 + 1024;
-constexpr uint32_t kTmemCols = 512;             // S: 2 x 128, O: 4 parts x 64
-constexpr uint32_t kTmemO = 256;                // O of part j at 256 + 64 j
-constexpr float kSlack = 8.f;                   // log2 headroom of the reference max
+constexpr int kTileBytes = kBQ * 128;           // 16 KB: 128 rows x 64 16-bit values
+constexpr int kStageBytes = 2 * kTileBytes;     // K and V of a chunk
+constexpr int kMlBytes = 2 * 2 * kBQ * 8;       // (m, l) exchange, two tile parities x two halves
+constexpr int kBiasBytes = kWorkerWarps * kHalf * 4;   // each softmax warp's key bias of a chunk
+constexpr int kBarBytes = 256;
+constexpr int kSmemBytes = 2 * kTileBytes + kStages * kStageBytes + kMlBytes + kBiasBytes + kBarBytes + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;     // S_b at 128 b
+constexpr uint32_t kColP = 256;   // P_b at 256 + 64 b (half h at + 32 h)
+constexpr uint32_t kColO = 384;   // O_h at 384 + 64 h
+constexpr float kSlack = 8.f;     // log2 headroom of the reference max
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -69,17 +75,20 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Largest (kMin: smallest) of 32 values: four independent 8-value chains.
+// Largest (kMin: smallest) of the 32 values v[0..31] (fp32 bit patterns):
+// four independent chains of three-input max.
 template <bool kMin>
-__device__ __forceinline__ float reduce32(const float (&x)[32]) {
+__device__ __forceinline__ float reduce32(const uint32_t *v) {
     float c[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float *y = x + 8 * k;
-        float a = kMin ? min3(y[0], y[1], y[2]) : max3(y[0], y[1], y[2]);
-        a = kMin ? min3(a, y[3], y[4]) : max3(a, y[3], y[4]);
-        a = kMin ? min3(a, y[5], y[6]) : max3(a, y[5], y[6]);
-        c[k] = kMin ? fminf(a, y[7]) : fmaxf(a, y[7]);
+        const uint32_t *y = v + 8 * k;
+#define F(i) __uint_as_float(y[i])
+        float a = kMin ? min3(F(0), F(1), F(2)) : max3(F(0), F(1), F(2));
+        a = kMin ? min3(a, F(3), F(4)) : max3(a, F(3), F(4));
+        a = kMin ? min3(a, F(5), F(6)) : max3(a, F(5), F(6));
+        c[k] = kMin ? fminf(a, F(7)) : fmaxf(a, F(7));
+#undef F
     }
     return kMin ? fminf(min3(c[0], c[1], c[2]), c[3]) : fmaxf(max3(c[0], c[1], c[2]), c[3]);
 }
@@ -98,7 +107,7 @@ __device__ __forceinline__ bool decode_tile(const Geom &g, int t, int xt, Tile &
     tl.nr = residue_len(g.n, g.s, tl.r);
     if (tl.a0 >= tl.nr) return false;
     // the key range starts on a multiple of 32 (keys before the band are
-    // masked), so each softmax warp's 32 keys of a chunk are one dropout block
+    // masked), so each 32-key group of a chunk is one dropout block
     tl.kb_lo = max(tl.a0 - g.w, 0) & ~31;
     tl.kb_hi = min(tl.a0 + kBQ - 1 + g.wu, tl.nr - 1);
     tl.nck = (tl.kb_hi - tl.kb_lo + kBK) / kBK;
@@ -113,21 +122,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *qtile = base;                               // 2 x 16 KB
-    uint8_t *kv = base + 2 * kQBytes;                    // stage st: K at +0, V at +kKBytes
-    uint8_t *pbuf = kv + kStages * kStageBytes;          // 2 x 32 KB
-    float2 *mlx = reinterpret_cast<float2 *>(pbuf + 2 * kPBytes);  // [2][kParts][kBQ]
-    float *bslots = reinterpret_cast<float *>(pbuf + 2 * kPBytes + kMlBytes);  // [16 warps][32]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(pbuf + 2 * kPBytes + kMlBytes + kBiasSlotBytes);
+    uint8_t *qtile = base;                                   // [2] x 16 KB
+    uint8_t *kv = qtile + 2 * kTileBytes;                    // stage st: K at +0, V at +kTileBytes
+    float2 *mlx = reinterpret_cast<float2 *>(kv + kStages * kStageBytes);   // [2 parities][2 halves][kBQ]
+    float *bslots = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(mlx) + kMlBytes);  // [8 warps][64]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(bslots) + kBiasBytes);
     uint64_t *qfull = bars;                  // [2]
     uint64_t *qempty = qfull + 2;            // [2]
     uint64_t *kvfull = qempty + 2;           // [kStages]
     uint64_t *kvempty = kvfull + kStages;    // [kStages]
-    uint64_t *sfull = kvempty + kStages;     // [2]
-    uint64_t *sempty = sfull + 2;            // [2] count kWorkers
-    uint64_t *pfull = sempty + 2;            // [2] count kWorkers
-    uint64_t *ofull = pfull + 2;             // 1: P.V product of a chunk done
-    uint64_t *mlbar = ofull + 1;             // [4] per lane quarter, count 128
+    uint64_t *sfull = kvempty + kStages;     // [2]: S_b is in TMEM
+    uint64_t *sempty = sfull + 2;            // [2], count kWorkers: S_b copied to registers
+    uint64_t *pfull = sempty + 2;            // [2], count kWorkers: P_b (and a rescaled O) in TMEM
+    uint64_t *pempty = pfull + 2;            // [2]: the P.V product that read P_b is done
+    uint64_t *mlbar = pempty + 2;            // [4] per lane quarter, count 64
     uint64_t *mmadone = mlbar + 4;           // 1: drain of the MMA pipe at exit
     uint64_t *drain = mmadone + 1;           // 1 int: never set (drain waits ignore aborts)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
@@ -135,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *no_abort = reinterpret_cast<volatile int *>(drain);
     // global tokens: bit j of gbits marks position j as global (the band
     // excludes those keys; they are attended through their own columns)
-    uint32_t *gbits = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(bars) + 1024);
+    uint32_t *gbits = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(bars) + kBarBytes);
 
     const Geom &g = p.g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,13 +165,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sfull[i], 1);
             mbar_init(&sempty[i], kWorkers);
             mbar_init(&pfull[i], kWorkers);
+            mbar_init(&pempty[i], 1);
         }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&kvfull[i], 1);
             mbar_init(&kvempty[i], 1);
         }
-        mbar_init(ofull, 1);
-        for (int i = 0; i < 4; ++i) mbar_init(&mlbar[i], 128);
+        for (int i = 0; i < 4; ++i) mbar_init(&mlbar[i], 64);
         mbar_init(mmadone, 1);
         *no_abort = 0;
         *abort_flag = 0;
@@ -178,10 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    // The producer and MMA warps run their loops warp-uniformly (every lane
-    // walks the tiles and waits on the barriers) and only lane 0 issues the
-    // copies, products and commits.
-    if (warp == 0) {
+    if (warp == 0 && lane == 0) {
         uint32_t gc = 0, it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -189,33 +194,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!decode_tile(g, t, xt, tl)) continue;
             const CUtensorMap *mq = &mapQ.m[tl.r], *mk = &mapK.m[tl.r], *mv = &mapV.m[tl.r];
             const int qb = it & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&qempty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.err)))
-                break;
-            if (lane == 0) {
-                tma_prefetch_desc(mq);
-                tma_prefetch_desc(mk);
-                tma_prefetch_desc(mv);
-                mbar_arrive_expect_tx(&qfull[qb], kQBytes);
-                tma_load_dense(qtile + qb * kQBytes, mq, &qfull[qb], tl.a0, tl.bh, g.h, g.rs_p != 0);
-            }
-            __syncwarp();
+            if (!mbar_wait(&qempty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+            tma_prefetch_desc(mq);
+            tma_prefetch_desc(mk);
+            tma_prefetch_desc(mv);
+            mbar_arrive_expect_tx(&qfull[qb], kTileBytes);
+            tma_load_dense(qtile + qb * kTileBytes, mq, &qfull[qb], tl.a0, tl.bh, g.h, g.rs_p != 0);
             ++it;
-            for (int c = 0; c < tl.nck; ++c) {
+            for (int c = 0; c < tl.nck; ++c, ++gc) {
                 const int st = gc % kStages;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&kvempty[st], ((gc / kStages) & 1) ^ 1, abort_flag, p.err))) {
+                if (!mbar_wait(&kvempty[st], ((gc / kStages) & 1) ^ 1, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&kvfull[st], kStageBytes);
-                    uint8_t *stage = kv + st * kStageBytes;
-                    tma_load_dense(stage, mk, &kvfull[st], tl.kb_lo + c * kBK, tl.bh, g.h, g.rs_p != 0);
-                    tma_load_dense(stage + kKBytes, mv, &kvfull[st], tl.kb_lo + c * kBK, tl.bh, g.h,
-                                   g.rs_p != 0);
-                }
-                __syncwarp();
-                ++gc;
+                uint8_t *stage = kv + st * kStageBytes;
+                const int row = tl.kb_lo + c * kBK;
+                mbar_arrive_expect_tx(&kvfull[st], kStageBytes);
+                tma_load_dense(stage, mk, &kvfull[st], row, tl.bh, g.h, g.rs_p != 0);
+                tma_load_dense(stage + kTileBytes, mv, &kvfull[st], row, tl.bh, g.h, g.rs_p != 0);
             }
         }
         // every copy issued lands before the CTA may exit (the last use of
@@ -224,43 +220,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&kvfull[k % kStages], (k / kStages) & 1, no_abort, nullptr, 100000000ull);
         for (uint32_t k = it > 2u ? it - 2 : 0; k < it; ++k)
             mbar_wait(&qfull[k & 1], (k >> 1) & 1, no_abort, nullptr, 100000000ull);
-    } else if (warp == 1) {
+    } else if (warp == 1 && lane == 0) {
         constexpr bool kBf16 = !std::is_same<T, __half>::value;
         constexpr uint32_t idesc_s = idesc_f16(kBQ, kBK, kBf16, false, false);
         constexpr uint32_t idesc_o = idesc_f16(kBQ, 64, kBf16, false, true);
         // Shared-memory descriptors are built once; a buffer, stage or K step
-        // only moves the start address field (address >> 4, which stays below
-        // 2^14 for any shared-memory address), so each one is a 64-bit add of
-        // a compile-time offset.
+        // only moves the start address field (address >> 4, below 2^14 for any
+        // shared-memory address), so each one is a 64-bit add.
         const uint64_t qdesc = sdesc_sw128(smem_u32(qtile), 16, 1024);
         const uint64_t kdesc = sdesc_sw128(smem_u32(kv), 16, 1024);
-        const uint64_t vdesc = sdesc_sw128(smem_u32(kv + kKBytes), 1024, 1024);
-        const uint64_t pdesc = sdesc_sw128(smem_u32(pbuf), 16, 1024);
-        // O_j (+)= P[:, part j] . V[part j]: the P.V product of chunk gg
+        const uint64_t vdesc = sdesc_sw128(smem_u32(kv + kTileBytes), 1024, 1024);
+        // O_h (+)= P_b[:, half h] . V[half h], the product of chunk gg: per
+        // half 4 steps of 16 keys, A from tensor memory (8 columns a step), B
+        // = 16 V rows (MN-major, 2 KB a step)
         auto issue_pv = [&](uint32_t gg, bool first) -> bool {
             const int st = gg % kStages;
             const int b = gg & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&pfull[b], (gg >> 1) & 1, abort_flag, p.err)))
-                return false;
+            if (!mbar_wait(&pfull[b], (gg >> 1) & 1, abort_flag, p.err)) return false;
             tc_fence_after();
-            const uint64_t pa = pdesc + (uint64_t)((b * kPBytes) >> 4);
             const uint64_t va = vdesc + (uint64_t)((st * kStageBytes) >> 4);
-            if (lane == 0) {
 #pragma unroll
-                for (int j = 0; j < kParts; ++j) {
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        // keys 32j + 16kk ..: atom j/2 of P, rows 32j + 16kk.. of V
-                        mma_f16_ss(tmem + kTmemO + 64 * j,
-                                   pa + (((j >> 1) * (kPBytes / 2) + (j & 1) * 64 + kk * 32) >> 4),
-                                   va + (((2 * j + kk) * 2048) >> 4), idesc_o,
-                                   (first && kk == 0) ? 0u : 1u);
-                    }
-                }
-                mma_commit(ofull);
-                mma_commit(&kvempty[st]);
+                for (int k = 0; k < kHalf / 16; ++k)
+                    mma_f16_ts(tmem + kColO + 64 * h, tmem + kColP + 64 * b + 32 * h + 8 * k,
+                               va + (uint64_t)((2048 * (4 * h + k)) >> 4), idesc_o, (first && k == 0) ? 0u : 1u);
             }
-            __syncwarp();
+            mma_commit(&pempty[b]);
+            mma_commit(&kvempty[st]);
             return true;
         };
         uint32_t gc = 0, it = 0, prev = 0;
@@ -269,28 +256,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             Tile tl;
             if (!decode_tile(g, t, xt, tl)) continue;
             const int qb = it & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&qfull[qb], (it >> 1) & 1, abort_flag, p.err))) {
+            if (!mbar_wait(&qfull[qb], (it >> 1) & 1, abort_flag, p.err)) {
                 ok = false;
                 break;
             }
-            const uint64_t qa = qdesc + (uint64_t)((qb * kQBytes) >> 4);
+            const uint64_t qa = qdesc + (uint64_t)((qb * kTileBytes) >> 4);
             for (int c = 0; c < tl.nck; ++c, ++gc) {
                 const int st = gc % kStages;
                 const int b = gc & 1;
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&kvfull[st], (gc / kStages) & 1, abort_flag, p.err) &&
-                                    mbar_wait(&sempty[b], ((gc >> 1) & 1) ^ 1, abort_flag, p.err));
+                ok = mbar_wait(&kvfull[st], (gc / kStages) & 1, abort_flag, p.err) &&
+                     mbar_wait(&sempty[b], ((gc >> 1) & 1) ^ 1, abort_flag, p.err);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t ka = kdesc + (uint64_t)((st * kStageBytes) >> 4);
-                if (lane == 0) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_f16_ss(tmem + b * kBK, qa + 2 * k, ka + 2 * k, idesc_s, k > 0);
-                    if (c == tl.nck - 1) mma_commit(&qempty[qb]);
-                    mma_commit(&sfull[b]);
-                }
-                __syncwarp();
+                for (int k = 0; k < 4; ++k) mma_f16_ss(tmem + kColS + kBK * b, qa + 2 * k, ka + 2 * k, idesc_s, k > 0);
+                if (c == tl.nck - 1) mma_commit(&qempty[qb]);
+                mma_commit(&sfull[b]);
                 if (have_prev && !issue_pv(prev, prev_first)) {
                     ok = false;
                     break;
@@ -303,73 +285,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && have_prev) issue_pv(prev, prev_first);
         // every product issued is complete before the accumulators are freed
-        if (lane == 0) mma_commit(mmadone);
-        __syncwarp();
+        mma_commit(mmadone);
         mbar_wait(mmadone, 0, no_abort, nullptr, 100000000ull);
-    } else {
-        // ---------------- softmax warps: thread = query row ----------------
+    } else if (warp >= 2) {
+        // ---------------- softmax warps: thread = query row, half h of the keys ----------------
         const int quarter = warp & 3;
-        const int part = (warp - 2) >> 2;
+        const int half = (warp - 2) >> 2;
         const int q = quarter * 32 + lane;
-        const float xscale = p.scale * 1.4426950408889634f;
+        const float xscale = p.scale * kLog2e;
         const bool neg_scale = xscale < 0.f;
         const float dscale = 256.f / (256.f - (float)g.drop_t);   // kept values' scale
         const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
-        const uint32_t o_mine = lane_base + kTmemO + 64 * part;
+        const uint32_t o_mine = lane_base + kColO + 64 * half;
+        float *bslot = bslots + (warp - 2) * kHalf;
         uint32_t gc = 0, it = 0;
         bool ok = true;
         bool epi_pend = false, epi_ok = false;
         float epi_m = 0.f, epi_l = 0.f;
         long long epi_row = 0;
         uint32_t epi_it = 0;
-        // the epilogue of tile epi_it (row epi_row, this part's (epi_m, epi_l));
+        // the epilogue of tile epi_it (row epi_row, this half's (epi_m, epi_l));
         // the caller has waited for the tile's last P.V product
         auto epilogue = [&]() -> bool {
             epi_pend = false;
-            float2 *ml = mlx + (epi_it & 1) * kParts * kBQ;
-            ml[part * kBQ + q] = make_float2(epi_m, epi_l);
+            float2 *ml = mlx + (epi_it & 1) * 2 * kBQ;
+            ml[half * kBQ + q] = make_float2(epi_m, epi_l);
             mbar_arrive(&mlbar[quarter]);
             if (!__all_sync(0xffffffffu, mbar_wait(&mlbar[quarter], epi_it & 1, abort_flag, p.err)))
                 return false;
-            float M = -INFINITY;
-            float2 e[kParts];
-#pragma unroll
-            for (int j = 0; j < kParts; ++j) {
-                e[j] = ml[j * kBQ + q];
-                M = fmaxf(M, e[j].x);
-            }
-            float f[kParts], L = 0.f;
-#pragma unroll
-            for (int j = 0; j < kParts; ++j) {
-                f[j] = e[j].x == -INFINITY ? 0.f : ex2(e[j].x - M);
-                L += e[j].y * f[j];
-            }
+            const float2 e0 = ml[q], e1 = ml[kBQ + q];
+            const float M = fmaxf(e0.x, e1.x);
+            const float f0 = e0.x == -INFINITY ? 0.f : ex2(e0.x - M);
+            const float f1 = e1.x == -INFINITY ? 0.f : ex2(e1.x - M);
+            const float L = e0.y * f0 + e1.y * f1;
             const float inv = (kDrop ? dscale : 1.f) / L;   // kept values scaled once, here
-            // channels [16 part, 16 part + 16) of the four accumulators, two at a time
-            float y[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = 0.f;
-#pragma unroll
-            for (int j0 = 0; j0 < kParts; j0 += 2) {
+            const float g0 = f0 * inv, g1 = f1 * inv;
+            // channels [32 half, 32 half + 32) of both accumulators, 16 at a time
+            uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + dense_row(g, epi_row, g.rs_o) +
+                                                  32 * half);
+#pragma unroll 1
+            for (int v = 0; v < 2; ++v) {
                 uint32_t o0[16], o1[16];
-                tmem_ld16(lane_base + kTmemO + 64 * j0 + 16 * part, o0);
-                tmem_ld16(lane_base + kTmemO + 64 * (j0 + 1) + 16 * part, o1);
+                tmem_ld16(lane_base + kColO + 32 * half + 16 * v, o0);
+                tmem_ld16(lane_base + kColO + 64 + 32 * half + 16 * v, o1);
                 tmem_ld_wait();
-                const float f0 = f[j0] * inv, f1 = f[j0 + 1] * inv;
+                if (epi_ok) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    y[i] = fmaf(__uint_as_float(o1[i]), f1, fmaf(__uint_as_float(o0[i]), f0, y[i]));
+                    for (int u = 0; u < 2; ++u) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 8 * u + 2 * e;
+                            w4[e] = pack2<T>(fmaf(__uint_as_float(o1[i]), g1, __uint_as_float(o0[i]) * g0),
+                                             fmaf(__uint_as_float(o1[i + 1]), g1, __uint_as_float(o0[i + 1]) * g0));
+                        }
+                        o4[2 * v + u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
             }
-            tc_fence_before();   // O may be overwritten once this warp's next P tile is signalled
             if (epi_ok) {
-                const long long row = epi_row;
-                uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + dense_row(g, row, g.rs_o) +
-                                                      16 * part);
-                o4[0] = make_uint4(pack2<T>(y[0], y[1]), pack2<T>(y[2], y[3]), pack2<T>(y[4], y[5]),
-                                   pack2<T>(y[6], y[7]));
-                o4[1] = make_uint4(pack2<T>(y[8], y[9]), pack2<T>(y[10], y[11]),
-                                   pack2<T>(y[12], y[13]), pack2<T>(y[14], y[15]));
-                if (p.lse && part == 0) p.lse[row] = M * 0.6931471805599453f + logf(L);
+                if (p.lse && half == 0) p.lse[epi_row] = M * 0.6931471805599453f + logf(L);
             }
             return true;
         };
@@ -380,156 +355,192 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m = -INFINITY, l = 0.f;
             for (int c = 0; c < tl.nck; ++c, ++gc) {
                 const int b = gc & 1;
-                const int kbase = tl.kb_lo + c * kBK + 32 * part;
-                // this row's band inside the part: columns [max(jlo,0), min(jhi,31)]
-                const int jlo = max(qq - g.w - kbase, 0);
-                const int jhi = min(min(qq + g.wu, tl.kb_hi) - kbase, 31);
-                uint32_t vmask = jlo > jhi ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
-                if constexpr (kGlob) {
-                    // column `lane` of the part is key kbase + lane of the residue
-                    const int sub = kbase + lane;
-                    const int key = tl.r + g.s * sub;
-                    const bool isg = sub < tl.nr && ((gbits[key >> 5] >> (key & 31)) & 1u);
-                    vmask &= ~__ballot_sync(0xffffffffu, isg);
+                const int kbase = tl.kb_lo + c * kBK + kHalf * half;   // this half's first key
+                // this row's band inside the half: columns [jlo, jhi]
+                const int jlo = qq - g.w - kbase;
+                const int jhi = min(qq + g.wu, tl.kb_hi) - kbase;
+                // group gi (keys kbase + 32 gi ..) is full / empty for every row
+                // of the warp (rows wq0 .. wq0 + 31): warp-uniform, no vote
+                const int wq0 = tl.a0 + 32 * quarter;
+                const int wlo_last = wq0 + 31 - g.w - kbase;                 // largest jlo of the warp
+                const int whi_first = min(wq0 + g.wu, tl.kb_hi) - kbase;    // smallest jhi
+                const int wlo_first = wq0 - g.w - kbase;                     // smallest jlo
+                const int whi_last = min(wq0 + 31 + g.wu, tl.kb_hi) - kbase; // largest jhi
+                uint32_t vm[2];
+                bool gfull[2], gempty[2];
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi) {
+                    gfull[gi] = wlo_last <= 32 * gi && whi_first >= 32 * gi + 31;
+                    gempty[gi] = whi_last < 32 * gi || wlo_first > 32 * gi + 31;
+                    const int lo = max(jlo - 32 * gi, 0), hi = min(jhi - 32 * gi, 31);
+                    vm[gi] = lo > hi ? 0u : ((2u << hi) - 1u) & (0xffffffffu << lo);
+                    if constexpr (kGlob) {
+                        // key `lane` of the group is kbase + 32 gi + lane of the residue
+                        const int sub = kbase + 32 * gi + lane;
+                        const int key = tl.r + g.s * sub;
+                        const bool isg = sub < tl.nr && ((gbits[key >> 5] >> (key & 31)) & 1u);
+                        const uint32_t gm = __ballot_sync(0xffffffffu, isg);
+                        vm[gi] &= ~gm;
+                        if (gm != 0u) gfull[gi] = false;   // the masks then drop the global keys
+                    }
                 }
-                const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
-                const bool empty = __all_sync(0xffffffffu, vmask == 0u);
-                // dropout keep bits of this row's 32 keys (one Philox block:
-                // kbase is a multiple of 32)
-                uint32_t keep = 0xffffffffu;
+                // dropout keep bits of this row's keys, one Philox block per group
+                uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
                 if constexpr (kDrop) {
-                    if (!empty && qq < tl.nr) {
-                        unsigned long long wv[4];
-                        philox4x64_10((unsigned long long)(kbase / 32),
-                                      (unsigned long long)(tl.r + (long long)g.s * qq),
-                                      (unsigned long long)tl.bh, 0, g.seed, 0, wv);
-                        keep = keep_bits32(wv, g.drop_t);
+#pragma unroll
+                    for (int gi = 0; gi < 2; ++gi) {
+                        if (vm[gi] != 0u && qq < tl.nr) {
+                            unsigned long long wv[4];
+                            philox4x64_10((unsigned long long)((kbase + 32 * gi) / 32),
+                                          (unsigned long long)(tl.r + (long long)g.s * qq),
+                                          (unsigned long long)tl.bh, 0, g.seed, 0, wv);
+                            keep[gi] = keep_bits32(wv, g.drop_t);
+                        }
                     }
                 }
-                float kb = 0.f;   // key bias (log2 units) of this part's key `lane`
                 if constexpr (kBias) {
-                    if (!empty && kbase + lane < tl.nr)
-                        kb = __ldg(g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * (kbase + lane)) *
-                             1.4426950408889634f;
-                }
-                bool w_ok = mbar_wait(&sfull[b], (gc >> 1) & 1, abort_flag, p.err);
-                if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-                tc_fence_after();
-                float x[32];
-                {
-                    uint32_t v[32];
-                    tmem_ld32(lane_base + b * kBK + 32 * part, v);
-                    tmem_ld_wait();
+                    // the half's key bias (log2 units) into this warp's slot
+                    __syncwarp();   // the previous chunk's reads of the slot are done
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
-                }
-                tc_fence_before();
-                mbar_arrive(&sempty[b]);   // the scores are in registers
-                // P tile b last fed the product of chunk gc-2, which is done
-                const uint32_t prow = smem_u32(pbuf + b * kPBytes) + (part >> 1) * (kPBytes / 2) + q * 128;
-                float cmax = -INFINITY, lc = 0.f;
-                if (empty) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int piece = (part & 1) * 4 + u;
-                        sts16(prow + ((piece ^ (q & 7)) << 4), make_uint4(0u, 0u, 0u, 0u));
+                    for (int u = 0; u < 2; ++u) {
+                        const int sub = kbase + 32 * u + lane;
+                        float kb = 0.f;
+                        if (!gempty[u] && sub < tl.nr)
+                            kb = __ldg(g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * sub) * kLog2e;
+                        bslot[32 * u + lane] = kb;
                     }
-                } else {
+                    __syncwarp();
+                }
+                if (!__all_sync(0xffffffffu, mbar_wait(&sfull[b], (gc >> 1) & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t x[kHalf];
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi) {
+                    if (gempty[gi]) continue;
+                    uint32_t (&xg)[32] = *reinterpret_cast<uint32_t (*)[32]>(x + 32 * gi);
+                    tmem_ld32(lane_base + kColS + kBK * b + kHalf * half + 32 * gi, xg);
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&sempty[b]);   // the scores are in registers: S_b may be rewritten
+                const bool neg = kBias ? false : neg_scale;
+                const float never = neg ? INFINITY : -INFINITY;   // the masked value that never wins
+                float ext = never;
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi) {
+                    if (gempty[gi]) continue;
+                    uint32_t *xg = x + 32 * gi;
                     if constexpr (kBias) {
                         // scaled score plus the key bias, in log2 units: the
-                        // scale is folded in here, so the passes below see
-                        // scale 1
-                        float *slot = bslots + (warp - 2) * 32;
-                        slot[lane] = kb;
-                        __syncwarp();
-                        const float4 *b4 = reinterpret_cast<const float4 *>(slot);
+                        // passes below see scale 1
+                        const float4 *b4 = reinterpret_cast<const float4 *>(bslot + 32 * gi);
                         const uint64_t xs2 = f2(xscale, xscale);
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             const float4 bb = b4[u];
-                            f2split(fma2(f2(x[4 * u], x[4 * u + 1]), xs2, f2(bb.x, bb.y)), x[4 * u], x[4 * u + 1]);
-                            f2split(fma2(f2(x[4 * u + 2], x[4 * u + 3]), xs2, f2(bb.z, bb.w)), x[4 * u + 2],
-                                    x[4 * u + 3]);
+                            float y0, y1, y2, y3;
+                            f2split(fma2(f2(__uint_as_float(xg[4 * u]), __uint_as_float(xg[4 * u + 1])), xs2,
+                                         f2(bb.x, bb.y)), y0, y1);
+                            f2split(fma2(f2(__uint_as_float(xg[4 * u + 2]), __uint_as_float(xg[4 * u + 3])), xs2,
+                                         f2(bb.z, bb.w)), y2, y3);
+                            xg[4 * u] = __float_as_uint(y0);
+                            xg[4 * u + 1] = __float_as_uint(y1);
+                            xg[4 * u + 2] = __float_as_uint(y2);
+                            xg[4 * u + 3] = __float_as_uint(y3);
                         }
-                        __syncwarp();
                     }
-                    // chunk max of the scaled scores from the raw ones: the
-                    // largest raw score for a positive scale, the smallest
-                    // for a negative one; columns outside the band are
-                    // replaced by the value that never wins
-                    const bool neg = kBias ? false : neg_scale;
-                    if (!full) {
+                    if (!gfull[gi]) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (!((vmask >> i) & 1u)) x[i] = neg ? INFINITY : -INFINITY;
+                            if (!((vm[gi] >> i) & 1u)) xg[i] = __float_as_uint(never);
                     }
-                    const float vm = neg ? reduce32<true>(x) : reduce32<false>(x);
-                    cmax = vmask == 0u ? -INFINITY : vm * (kBias ? 1.f : xscale);
+                    ext = neg ? fminf(ext, reduce32<true>(xg)) : fmaxf(ext, reduce32<false>(xg));
                 }
+                const float cmax = (vm[0] | vm[1]) != 0u ? ext * (kBias ? 1.f : xscale) : -INFINITY;
                 const bool raise = m == -INFINITY || cmax > m + kSlack;
                 const float mref = raise ? cmax : m;
-                if (!empty) {
-                    const float mb = mref == -INFINITY ? 0.f : mref;
-                    const float xs_eff = kBias ? 1.f : xscale;   // the bias path holds scaled scores
-                    const uint64_t xs2 = f2(xs_eff, xs_eff), nb2 = f2(-mb, -mb);
-                    uint64_t lc2 = f2(0.f, 0.f);
+                const float mb = mref == -INFINITY ? 0.f : mref;
+                const float xs_eff = kBias ? 1.f : xscale;   // the bias path holds scaled scores
+                // P_b last fed the product of chunk gc-2, which must be done
+                if (gc >= 2) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&pempty[b], ((gc >> 1) & 1) ^ 1, abort_flag, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                const uint64_t xs2 = f2(xs_eff, xs_eff), nb2 = f2(-mb, -mb);
+                uint64_t lc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};   // partial row sums (two chains)
+                // p of each 32-key group, packed, into its 16 columns of P_b
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint32_t pk[4];
+                for (int gi = 0; gi < 2; ++gi) {
+                    uint32_t pk[16];
+                    if (gempty[gi]) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 8 * u + 2 * e;
+                        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                    } else {
+                        const uint32_t *xg = x + 32 * gi;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
                             float y0, y1;
-                            f2split(fma2(f2(x[i], x[i + 1]), xs2, nb2), y0, y1);
+                            f2split(fma2(f2(__uint_as_float(xg[2 * e]), __uint_as_float(xg[2 * e + 1])), xs2, nb2),
+                                    y0, y1);
                             float p0 = ex2(y0), p1 = ex2(y1);
-                            if (!full) {
-                                if (!((vmask >> i) & 1u)) p0 = 0.f;
-                                if (!((vmask >> (i + 1)) & 1u)) p1 = 0.f;
+                            if (!gfull[gi]) {
+                                if (!((vm[gi] >> (2 * e)) & 1u)) p0 = 0.f;
+                                if (!((vm[gi] >> (2 * e + 1)) & 1u)) p1 = 0.f;
                             }
-                            lc2 = add2(lc2, f2(p0, p1));   // the row sum is before dropout
+                            lc2[e & 1] = add2(lc2[e & 1], f2(p0, p1));   // the row sum is before dropout
                             if constexpr (kDrop) {   // dropped: 0 (kept: scaled in the epilogue)
-                                if (!((keep >> i) & 1u)) p0 = 0.f;
-                                if (!((keep >> (i + 1)) & 1u)) p1 = 0.f;
+                                if (!((keep[gi] >> (2 * e)) & 1u)) p0 = 0.f;
+                                if (!((keep[gi] >> (2 * e + 1)) & 1u)) p1 = 0.f;
                             }
                             pk[e] = pack2<T>(p0, p1);
                         }
-                        const int piece = (part & 1) * 4 + u;
-                        sts16(prow + ((piece ^ (q & 7)) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
                     }
-                    float l0, l1;
-                    f2split(lc2, l0, l1);
-                    lc = l0 + l1;
+                    tmem_st16(lane_base + kColP + 64 * b + 32 * half + 16 * gi, pk);
                 }
+                float l0, l1;
+                f2split(add2(lc2[0], lc2[1]), l0, l1);
                 const bool rescale = raise && m != -INFINITY;
                 const float corr = rescale ? ex2(m - mref) : 1.f;
-                l = l * corr + lc;
-                if (c > 0 || epi_pend) {
-                    // the product of chunk gc-1 has landed in O: it may be
-                    // rescaled, or (first chunk of a tile) the previous tile's
-                    // accumulators are final
-                    w_ok = mbar_wait(ofull, (gc - 1) & 1, abort_flag, p.err);
-                    if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-                }
-                if (epi_pend) {
+                l = l * corr + (l0 + l1);
+                const bool resc_any = __any_sync(0xffffffffu, rescale);
+                if ((resc_any || epi_pend) && gc >= 1) {
+                    // the product of chunk gc-1 (the last one of the previous
+                    // tile, in a tile's first chunk) is done: O may be
+                    // rescaled or read out
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&pempty[b ^ 1], ((gc - 1) >> 1) & 1, abort_flag, p.err))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    if (!epilogue()) { ok = false; break; }
                 }
-                if (__any_sync(0xffffffffu, rescale)) {
-                    tc_fence_after();
+                // a rescale never happens in a tile's first chunk (m is -inf
+                // there), so never together with the epilogue
+                if (resc_any) {
 #pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
+                    for (int hh = 0; hh < 2; ++hh) {
                         uint32_t o[32];
-                        tmem_ld32(o_mine + 32 * h, o);
+                        tmem_ld32(o_mine + 32 * hh, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-                        tmem_st32(o_mine + 32 * h, o);
+                        tmem_st32(o_mine + 32 * hh, o);
                     }
-                    tmem_st_wait();
                 }
+                // the previous tile's O stays in place until this chunk's P is signalled
+                if (epi_pend && !epilogue()) {
+                    ok = false;
+                    break;
+                }
+                tmem_st_wait();
                 tc_fence_before();
-                fence_proxy_async_smem();
-                mbar_arrive(&pfull[b]);    // P tile b (and the rescaled O) are ready
+                mbar_arrive(&pfull[b]);    // P_b (and the rescaled O) are in tensor memory
                 m = mref;
             }
             if (!ok) break;
@@ -542,9 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             epi_it = it;
             ++it;
         }
-        if (ok && epi_pend) {
-            // the last tile's epilogue: its last P.V product is phase gc-1 of ofull
-            if (__all_sync(0xffffffffu, mbar_wait(ofull, (gc - 1) & 1, abort_flag, p.err))) {
+        if (ok && epi_pend && gc >= 1) {
+            // the last tile's epilogue: its last P.V product read P_{(gc-1) mod 2}
+            if (__all_sync(0xffffffffu, mbar_wait(&pempty[(gc - 1) & 1], ((gc - 1) >> 1) & 1, abort_flag, p.err))) {
                 tc_fence_after();
                 epilogue();
             }
@@ -608,11 +619,17 @@ cudaError_t launch_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, co
     const long long tiles = (long long)((a.g.nsub + kBQ - 1) / kBQ) * a.g.s * a.g.BH;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const int grid = (int)(tiles < sms ? tiles : sms);
+    const void *fn = reinterpret_cast<const void *>(k_band_attention_fwd<T, kBias, kDrop, kGlob>);
     const size_t smem = kSmemBytes + (kGlob ? (size_t)((a.g.n + 31) / 32) * 4 : 0);
-    cudaError_t e =
-        ensure_smem(reinterpret_cast<const void *>(k_band_attention_fwd<T, kBias, kDrop, kGlob>), smem);
+    cudaError_t e = ensure_smem(fn, (int)smem);
     if (e != cudaSuccess) return e;
+    // persistent CTAs: as many as fit at once (one per SM), at most one per tile
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const long long slots = (long long)sms * per_sm;
+    const int grid = (int)(tiles < slots ? tiles : slots);
     GlobArgs none;
     none.G = 0;
     k_band_attention_fwd<T, kBias, kDrop, kGlob><<<grid, kThreads, smem, st>>>(mq, mk, mv, a, gl ? *gl : none);
