@@ -318,7 +318,23 @@ def prologue_and_globals(device, steps, flush, peaks):
         "ms": round(ms4, 4), "tflops": round(fl4 / (ms4 * 1e-3) / 1e12, 2),
         "roofline_frac": round(fl4 / (peaks["bf16_tflops"] * 1e12) / (ms4 * 1e-3), 4), "bound": "tensor",
         "note": "band part (global keys masked) + global columns merged + global rows"}
-    del Q4, K4, V4, O4
+    # the fused training step with global tokens: forward, then the backward
+    # (band pass with global keys and queries left out, global columns, global
+    # rows), on the same shape
+    dO4 = workload_inputs(w4)[3].to(device)
+    dQ4, dK4, dV4 = (torch.empty_like(Q4) for _ in range(3))
+    ws4 = torch.empty(swab.band_attention_bwd_workspace(d4) // 4 + 4, dtype=torch.float32, device=device)
+    msb = time_graph(lambda: swab.band_attention_bwd(d4, w4.scale, Q4, K4, V4, O4, dO4, lse4, dQ4, dK4, dV4, ws4),
+                     steps, 3, flush)
+    fl4b = 2 * fl4
+    out[f"fused+globals:{w4.name}"] = {
+        "ms_per_step": round(ms4 + msb, 4), "fwd_ms": round(ms4, 4), "bwd_ms": round(msb, 4),
+        "tflops": round((fl4 + fl4b) / ((ms4 + msb) * 1e-3) / 1e12, 2),
+        "roofline_frac": round((fl4 + fl4b) / (peaks["bf16_tflops"] * 1e12) / ((ms4 + msb) * 1e-3), 4),
+        "bound": "tensor",
+        "note": "band_attention then band_attention_bwd with 16 global tokens, bf16; flops = 6 contractions x "
+                "2 x head_dim over the attended (query, key) pairs"}
+    del Q4, K4, V4, O4, dO4, dQ4, dK4, dV4, ws4
     dg = swab.Desc.from_workload(w4)
     G, BH, n = dg.G, w4.BH, w4.n
     mk = lambda *sh: torch.randn(*sh, generator=g).to(w4.dtype).to(device)  # noqa: E731

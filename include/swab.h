@@ -285,14 +285,26 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
  * as programmatic dependents: they may start while the one before runs and
  * wait inside for what it wrote.  For the caller the call stays ordered on
  * the stream like any kernel launch.
- * Global tokens are not supported here (n_global must be 0). */
+ * Global tokens (f16 / bf16, contiguous layout, no key bias or dropout,
+ * n <= 98304; else SWAB_ERR_UNSUPPORTED): the gradients of the attention with
+ * global tokens of band_attention -- local rows over their band keys outside G
+ * plus G, global rows over every key.  The call then runs the band (global
+ * keys and global queries left out), the global columns (every local row
+ * against the G global keys, gathered into the workspace) and the global
+ * rows (the global_attention_bwd computation with the shared Q, K, V as the
+ * global projections), the dK, dV terms of all three added in fp32 before one
+ * rounding; the workspace (band_attention_bwd_workspace) then also holds the
+ * gathered rows and keys and the global rows' dK, dV terms. */
 SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, const void *Q,
                                         const void *K, const void *V, const void *O,
                                         const void *dO, const float *lse, void *dQ, void *dK,
                                         void *dV, void *workspace, void *stream);
 
 /* Bytes of workspace band_attention_bwd needs for `desc` (0 if desc is NULL):
- * fp16 / bf16: round_up(b*h*n*4, 256) + b*h*n*64*4;  fp32: round_up(b*h*n*4, 256). */
+ * fp16 / bf16: round_up(b*h*n*4, 256) + b*h*n*64*4, plus with global tokens
+ * the sections of the gathered global rows, keys and values and the global
+ * rows' dK, dV terms (about 2*b*h*n*64*2 bytes more);
+ * fp32: round_up(b*h*n*4, 256). */
 SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc);
 
 /* band_attention_bwd for callers that cannot allocate device memory: the same

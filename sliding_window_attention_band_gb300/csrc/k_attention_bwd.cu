@@ -687,11 +687,21 @@ __device__ __forceinline__ bool decode_ktile(const Geom &g, int t, int xt, KTile
 }
 }  // namespace fused
 
-template <typename T, bool kBias, bool kDrop>
+// kMode 0: the band.  kMode 1: the band with global tokens -- global keys and
+// global queries are left out (a local row's global keys and a global row's
+// keys are attended through their own columns and rows), and the dK, dV drain
+// adds the global rows' terms (a.gdK, a.gdV, every key) and, at a global key,
+// the global columns' terms (a.cdK, a.cdV).  kMode 2: the global columns --
+// one "key tile" per slice holding the G global keys (gathered, zero past G;
+// mapK / mapV over [BH, 128, 64]) against every local query (chunks over the
+// whole sequence, stride 1); dQ is added into the accumulator as in the band
+// pass and the tile's dK (scaled), dV are written to a.cdK, a.cdV.
+template <typename T, bool kBias, bool kDrop, int kMode = 0>
 __global__ void __launch_bounds__(fused::kThreads, 1)
     k_bwd_fused(const __grid_constant__ TmapSet mapQ, const __grid_constant__ TmapSet mapK,
                 const __grid_constant__ TmapSet mapV, const __grid_constant__ TmapSet mapdO,
-                const __grid_constant__ TmapSet mapAcc, const BwdArgs p) {
+                const __grid_constant__ TmapSet mapAcc, const BwdArgs p,
+                const __grid_constant__ GlobArgs gl) {
     using namespace fused;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
@@ -723,10 +733,39 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *no_abort = reinterpret_cast<volatile int *>(drain);
 
+    // global tokens: bit j of gbits marks position j as global
+    uint32_t *gbits = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(bars) + 1024);
+
     const Geom &g = p.g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int xt = (g.nsub + kB - 1) / kB;
-    const int ntiles = xt * g.s * g.BH;
+    const int gtiles = (gl.G + kB - 1) / kB;   // kMode 2: key tiles of gathered global keys per slice
+    const int xt = kMode == 2 ? 1 : (g.nsub + kB - 1) / kB;
+    const int ntiles = kMode == 2 ? g.BH * gtiles : xt * g.s * g.BH;
+
+    if constexpr (kMode != 0) {
+        for (int w = threadIdx.x; w < (g.n + 31) / 32; w += fused::kThreads) gbits[w] = 0u;
+        __syncthreads();
+        for (int k = threadIdx.x; k < gl.G; k += fused::kThreads)
+            atomicOr(&gbits[gl.idx[k] >> 5], 1u << (gl.idx[k] & 31));
+        // visible to every thread after the barrier below
+    }
+    auto is_global = [&](int pos) -> bool { return (gbits[pos >> 5] >> (pos & 31)) & 1u; };
+    // tile t: kMode 2 has ceil(G / 128) tiles per slice, their keys the
+    // gathered global keys and their queries the whole sequence
+    auto decode = [&](int t, KTile &tl) -> bool {
+        if constexpr (kMode == 2) {
+            tl.a0 = (t % gtiles) * kB;
+            tl.r = 0;
+            tl.bh = t / gtiles;
+            tl.nr = g.n;
+            tl.qb_lo = 0;
+            tl.qb_hi = g.n - 1;
+            tl.nck = (g.n + kB - 1) / kB;
+            return true;
+        } else {
+            return decode_ktile(g, t, xt, tl);
+        }
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kQStages; ++i) {
@@ -768,7 +807,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             KTile tl;
-            if (!decode_ktile(g, t, xt, tl)) continue;
+            if (!decode(t, tl)) continue;
             const CUtensorMap *mq = &mapQ.m[tl.r], *mk = &mapK.m[tl.r], *mv = &mapV.m[tl.r],
                               *mo = &mapdO.m[tl.r];
             const int tb = it & 1;
@@ -790,7 +829,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 // gradient phase at the tile boundary
                 for (int t2 = t + gridDim.x; t2 < ntiles; t2 += gridDim.x) {
                     KTile nx;
-                    if (!decode_ktile(g, t2, xt, nx)) continue;
+                    if (!decode(t2, nx)) continue;
                     tma_prefetch_dense(&mapK.m[nx.r], nx.a0, nx.bh, g.h, g.rs_p != 0);
                     tma_prefetch_dense(&mapV.m[nx.r], nx.a0, nx.bh, g.h, g.rs_p != 0);
                     break;
@@ -872,7 +911,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         bool ok = true, have_prev = false, prev_first = false, prev_last = false;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             KTile tl;
-            if (!decode_ktile(g, t, xt, tl)) continue;
+            if (!decode(t, tl)) continue;
             const int tb = it & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&kfull[tb], (it >> 1) & 1, abort_flag, p.err) &&
                                              mbar_wait(vfull, it & 1, abort_flag, p.err))) {
@@ -923,7 +962,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             KTile tl;
-            if (!decode_ktile(g, t, xt, tl)) continue;
+            if (!decode(t, tl)) continue;
             const CUtensorMap *ma = &mapAcc.m[tl.r];
             for (int c = 0; c < tl.nck; ++c, ++gc) {
                 if (!__all_sync(0xffffffffu, mbar_wait(stfull, gc & 1, abort_flag, p.err))) {
@@ -960,7 +999,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         bool dq_pend = false;   // the dQ of chunk dq_g (in TMEM) waits to be staged
         uint32_t dq_g = 0;
         bool acc_pend = false, acc_ok = false;   // a tile's dV, dK wait to be read out
-        unsigned acc_row = 0;   // row bh * n + key of dK, dV (below 2^31)
+        unsigned acc_row = 0;   // row bh * n + key of dK, dV (below 2^31); kMode 2: the key's index in G
+        int acc_bh = 0;         // kMode 2: the slice
+        int acc_gi = -1;        // kMode 1: index in G of a global key, else -1
         // dV, dK of key row acc_row (channels [16 part, +16)); the caller has
         // waited for the tile's last products
         auto drain_acc = [&]() {
@@ -970,6 +1011,67 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(accempty);
+            if constexpr (kMode == 2) {
+                // the global columns' dK (scaled), dV of global key acc_row
+                // (its index in G) of slice acc_bh, fp32
+                if (acc_ok) {
+                    float4 *cv = reinterpret_cast<float4 *>(p.cdV + ((size_t)acc_bh * gl.G + acc_row) * 64 + 16 * part);
+                    float4 *ck = reinterpret_cast<float4 *>(p.cdK + ((size_t)acc_bh * gl.G + acc_row) * 64 + 16 * part);
+                    const float sc = p.scale;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = 4 * u;
+                        cv[u] = make_float4(__uint_as_float(a[i]), __uint_as_float(a[i + 1]),
+                                            __uint_as_float(a[i + 2]), __uint_as_float(a[i + 3]));
+                        ck[u] = make_float4(sc * __uint_as_float(b[i]), sc * __uint_as_float(b[i + 1]),
+                                            sc * __uint_as_float(b[i + 2]), sc * __uint_as_float(b[i + 3]));
+                    }
+                }
+                return;
+            }
+            if constexpr (kMode == 1) {
+                // the global rows' terms (every key) and, at a global key, the
+                // global columns' terms, added before the one rounding
+                if (acc_ok) {
+                    const float sc = p.scale;
+                    const size_t goff = (size_t)acc_row * 64 + 16 * part;   // contiguous layout
+                    const uint4 *gv = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.gdV) + goff);
+                    const uint4 *gk = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.gdK) + goff);
+                    float fv[16], fk[16];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint4 wv = gv[u], wk = gk[u];
+                        const uint32_t v32[4] = {wv.x, wv.y, wv.z, wv.w}, k32[4] = {wk.x, wk.y, wk.z, wk.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            fv[8 * u + 2 * e] = __uint_as_float(a[8 * u + 2 * e]) + lo16<T>(v32[e]);
+                            fv[8 * u + 2 * e + 1] = __uint_as_float(a[8 * u + 2 * e + 1]) + hi16<T>(v32[e]);
+                            fk[8 * u + 2 * e] = fmaf(sc, __uint_as_float(b[8 * u + 2 * e]), lo16<T>(k32[e]));
+                            fk[8 * u + 2 * e + 1] = fmaf(sc, __uint_as_float(b[8 * u + 2 * e + 1]), hi16<T>(k32[e]));
+                        }
+                    }
+                    if (acc_gi >= 0) {
+                        const float *cv = p.cdV + ((size_t)acc_bh * gl.G + acc_gi) * 64 + 16 * part;
+                        const float *ck = p.cdK + ((size_t)acc_bh * gl.G + acc_gi) * 64 + 16 * part;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            fv[i] += cv[i];
+                            fk[i] += ck[i];
+                        }
+                    }
+                    uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + goff);
+                    uint4 *k4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dK) + goff);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = 8 * u;
+                        v4[u] = make_uint4(pack2<T>(fv[i], fv[i + 1]), pack2<T>(fv[i + 2], fv[i + 3]),
+                                           pack2<T>(fv[i + 4], fv[i + 5]), pack2<T>(fv[i + 6], fv[i + 7]));
+                        k4[u] = make_uint4(pack2<T>(fk[i], fk[i + 1]), pack2<T>(fk[i + 2], fk[i + 3]),
+                                           pack2<T>(fk[i + 4], fk[i + 5]), pack2<T>(fk[i + 6], fk[i + 7]));
+                    }
+                }
+                return;
+            }
             if (acc_ok) {
                 const long long off = dense_row(g, acc_row, g.rs_p) + 16 * part;
                 uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + off);
@@ -992,7 +1094,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
 
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             KTile tl;
-            if (!decode_ktile(g, t, xt, tl)) continue;
+            if (!decode(t, tl)) continue;
             const int kk = tl.a0 + m;
             // key bias of this thread's key (log2 units), the same for every query
             uint64_t kb2 = f2(0.f, 0.f);
@@ -1002,14 +1104,26 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                     kb2 = f2(kb, kb);
                 }
             }
+            // kMode 1: a global key takes no band query; kMode 2: the rows past
+            // the G gathered keys are padding
+            bool key_off = kk >= tl.nr;
+            if constexpr (kMode == 1) key_off = key_off || is_global(tl.r + g.s * kk);
+            if constexpr (kMode == 2) key_off = kk >= gl.G;
             for (int c = 0; c < tl.nck; ++c, ++gc) {
                 const int qbase = tl.qb_lo + c * kB;
                 const int cbase = qbase + 32 * part;
-                // this key's queries inside the part: columns [jlo, jhi]
-                const int jlo = max(kk - g.wu - cbase, 0);
-                const int jhi = min(min(kk + g.w, tl.nr - 1) - cbase, 31);
-                const uint32_t vmask =
-                    (kk >= tl.nr || jlo > jhi) ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
+                // this key's queries inside the part: columns [jlo, jhi] (kMode
+                // 2: every query of the sequence)
+                const int jlo = kMode == 2 ? 0 : max(kk - g.wu - cbase, 0);
+                const int jhi = kMode == 2 ? min(tl.nr - 1 - cbase, 31) : min(min(kk + g.w, tl.nr - 1) - cbase, 31);
+                uint32_t vmask = (key_off || jlo > jhi) ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
+                if constexpr (kMode != 0) {
+                    // global queries (query column `lane` of the part) take no band
+                    // or global-column keys: their rows are dense, done apart
+                    const int qsub = cbase + lane;
+                    const bool qg = qsub < tl.nr && is_global(tl.r + g.s * qsub);
+                    vmask &= ~__ballot_sync(0xffffffffu, qg);
+                }
                 const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
                 const bool empty = __all_sync(0xffffffffu, vmask == 0u);
                 // dropout: bit j = keep(query column j of the part, this key).
@@ -1166,6 +1280,25 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             acc_pend = true;
             acc_ok = kk < tl.nr;
             acc_row = (unsigned)(tl.bh * g.n + tl.r + g.s * kk);
+            if constexpr (kMode == 2) {
+                acc_ok = kk < gl.G;
+                acc_row = (unsigned)kk;
+                acc_bh = tl.bh;
+            }
+            if constexpr (kMode == 1) {
+                acc_gi = -1;
+                const int pos = tl.r + g.s * kk;
+                if (acc_ok && is_global(pos)) {
+                    int lo = 0, hi = gl.G - 1;   // the index is sorted
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (gl.idx[mid] < pos) lo = mid + 1;
+                        else hi = mid;
+                    }
+                    acc_gi = lo;
+                    acc_bh = tl.bh;
+                }
+            }
             ++it;
         }
         if (ok && dq_pend) {
@@ -1319,7 +1452,9 @@ cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_bwd_fused<T, kBias, kDrop>, mq, mk, mv, mo, macc, a);
+    GlobArgs none;
+    none.G = 0;
+    e = cudaLaunchKernelEx(&cfg, k_bwd_fused<T, kBias, kDrop>, mq, mk, mv, mo, macc, a, none);
     if (e != cudaSuccess) return e;
     const long long groups = rows * 8;
     cfg.gridDim = dim3((unsigned)((groups + 255) / 256));
@@ -1328,7 +1463,139 @@ cudaError_t launch_fused_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &
     return cudaLaunchKernelEx(&cfg, k_bwd_dq_out<T>, a);
 }
 
+// ---------------------------------------------------------------------------
+// global tokens: gather the G global rows of Q, O, dO, lse into compact
+// buffers (the global rows' backward) and the global keys / values into
+// ceil(G / 128) [128, 64] tiles per slice, zero past G (the global columns'
+// "key tiles").
+// Contiguous layout; one CTA per slice.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) k_glob_gather(const BwdArgs p, const __grid_constant__ GlobArgs gl,
+                                                     const GlobBwdBufs gb) {
+    const long long bh = blockIdx.x;
+    const int n = p.g.n, G = gl.G;
+    const uint4 *K4 = reinterpret_cast<const uint4 *>(p.K), *V4 = reinterpret_cast<const uint4 *>(p.V);
+    const uint4 *Q4 = reinterpret_cast<const uint4 *>(p.Q), *O4 = reinterpret_cast<const uint4 *>(p.O);
+    const uint4 *dO4 = reinterpret_cast<const uint4 *>(p.dO);
+    uint4 *KG4 = reinterpret_cast<uint4 *>(gb.KG), *VG4 = reinterpret_cast<uint4 *>(gb.VG);
+    const int grows = (G + kB - 1) / kB * kB;   // whole 128-key tiles
+    for (int i = threadIdx.x; i < grows * 8; i += blockDim.x) {
+        const int row = i >> 3, c = i & 7;   // 8 x 16 bytes per 64-element row
+        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+        if (row < G) {
+            const size_t src = ((size_t)bh * n + gl.idx[row]) * 8 + c;
+            kv = K4[src];
+            vv = V4[src];
+        }
+        KG4[((size_t)bh * grows + row) * 8 + c] = kv;
+        VG4[((size_t)bh * grows + row) * 8 + c] = vv;
+    }
+    uint4 *Qg4 = reinterpret_cast<uint4 *>(gb.Qg), *Og4 = reinterpret_cast<uint4 *>(gb.Og);
+    uint4 *dOg4 = reinterpret_cast<uint4 *>(gb.dOg);
+    for (int i = threadIdx.x; i < G * 8; i += blockDim.x) {
+        const int row = i >> 3, c = i & 7;
+        const size_t src = ((size_t)bh * n + gl.idx[row]) * 8 + c, dst = ((size_t)bh * G + row) * 8 + c;
+        Qg4[dst] = Q4[src];
+        Og4[dst] = O4[src];
+        dOg4[dst] = dO4[src];
+    }
+    for (int k = threadIdx.x; k < G; k += blockDim.x) gb.lseg[bh * G + k] = p.lse[bh * n + gl.idx[k]];
+}
+
+// the global rows' dQ (computed by the global-query backward) into dQ
+__global__ void __launch_bounds__(256) k_glob_dq_rows(const BwdArgs p, const __grid_constant__ GlobArgs gl,
+                                                      const void *dQg) {
+    const long long bh = blockIdx.x;
+    const uint4 *src = reinterpret_cast<const uint4 *>(dQg);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.dQ);
+    for (int i = threadIdx.x; i < gl.G * 8; i += blockDim.x) {
+        const int row = i >> 3, c = i & 7;
+        dst[((size_t)bh * p.g.n + gl.idx[row]) * 8 + c] = src[((size_t)bh * gl.G + row) * 8 + c];
+    }
+}
+
+template <typename T>
+cudaError_t launch_glob_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const TmapSet &mo,
+                          const TmapSet &macc, const TmapSet &mq1, const TmapSet &mo1, const TmapSet &mkc,
+                          const TmapSet &mvc, const TmapSet &macc1, const GlobArgs &gl, const GlobBwdBufs &gb,
+                          const BwdArgs &a, const GlobalProjArgs &gp, const TmapSet &gmk, const TmapSet &gmv,
+                          const TmapSet &gmq, const TmapSet &gmo, cudaStream_t st) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const long long rows = (long long)a.g.BH * a.g.n;
+    // 1. delta for every row; the dQ accumulator cleared
+    const long long per_block = 8LL * kDeltaRowsPerWarp;
+    k_bwd_delta<T><<<(unsigned)((rows + per_block - 1) / per_block), 256, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // 2. the global rows and the global keys / values gathered
+    k_glob_gather<T><<<(unsigned)a.g.BH, 256, 0, st>>>(a, gl, gb);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 3. the global rows: dense attention of the G global queries over every
+    //    key (dQ of those rows into gb.dQg, their dK, dV terms into a.gdK, a.gdV)
+    if ((e = launch_global_proj_bwd_tc(std::is_same<T, __half>::value ? kF16 : kBF16, gmk, gmv, gmq, gmo, gp, st)) !=
+        cudaSuccess)
+        return e;
+    const size_t smem = fused::kSmem + (size_t)((a.g.n + 31) / 32) * 4;
+    // 4. the global columns: every local query against the G global keys
+    {
+        BwdArgs ac = a;
+        ac.g.s = 1;
+        ac.g.nsub = a.g.n;
+        e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, false, false, 2>), (int)smem);
+        if (e != cudaSuccess) return e;
+        const int ctiles = a.g.BH * ((gl.G + kB - 1) / kB);
+        const int grid = ctiles < sms ? ctiles : sms;
+        k_bwd_fused<T, false, false, 2><<<grid, fused::kThreads, smem, st>>>(mq1, mkc, mvc, mo1, macc1, ac, gl);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // 5. the band (global keys and queries left out), its dK, dV drain adding
+    //    the global terms; 6. the dQ rounding -- both programmatic dependents
+    const long long tiles = (long long)((a.g.nsub + kB - 1) / kB) * a.g.s * a.g.BH;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, false, false, 1>), (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(fused::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_bwd_fused<T, false, false, 1>, mq, mk, mv, mo, macc, a, gl);
+    if (e != cudaSuccess) return e;
+    const long long groups = rows * 8;
+    cfg.gridDim = dim3((unsigned)((groups + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    if ((e = cudaLaunchKernelEx(&cfg, k_bwd_dq_out<T>, a)) != cudaSuccess) return e;
+    // 7. the global rows' dQ
+    k_glob_dq_rows<<<(unsigned)a.g.BH, 256, 0, st>>>(a, gl, gb.dQg);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_band_attention_bwd_glob(DType dt, const TmapSet &mq, const TmapSet &mk, const TmapSet &mv,
+                                           const TmapSet &mo, const TmapSet &macc, const TmapSet &mq1,
+                                           const TmapSet &mo1, const TmapSet &mkc, const TmapSet &mvc,
+                                           const TmapSet &macc1, const GlobArgs &gl, const GlobBwdBufs &gb,
+                                           const BwdArgs &a, const GlobalProjArgs &gp, const TmapSet &gmk,
+                                           const TmapSet &gmv, const TmapSet &gmq, const TmapSet &gmo,
+                                           cudaStream_t st) {
+    if (!a.dqacc || gl.G < 1 || a.g.BH > 65535) return cudaErrorInvalidValue;
+    if (dt == kF16)
+        return launch_glob_t<__half>(mq, mk, mv, mo, macc, mq1, mo1, mkc, mvc, macc1, gl, gb, a, gp, gmk, gmv, gmq,
+                                     gmo, st);
+    if (dt == kBF16)
+        return launch_glob_t<__nv_bfloat16>(mq, mk, mv, mo, macc, mq1, mo1, mkc, mvc, macc1, gl, gb, a, gp, gmk,
+                                            gmv, gmq, gmo, st);
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_band_attention_bwd_fused(DType dt, const TmapSet &mq, const TmapSet &mk,
                                             const TmapSet &mv, const TmapSet &mo, const TmapSet &macc,

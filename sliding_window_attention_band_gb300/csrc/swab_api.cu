@@ -689,13 +689,123 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
     return from_cuda(launch_band_attention_tc(dt, mq, mk, mv, a, as_stream(stream)));
 }
 
+// Workspace of band_attention_bwd with global tokens, after the per-row delta
+// and the fp32 dQ accumulator: byte offsets of each section (256-aligned).
+struct BwdGlobLayout {
+    size_t Qg, Og, dOg, dQg, lseg, KG, VG, gdK, gdV, cdK, cdV, gp, end;
+};
+static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+static BwdGlobLayout bwd_glob_layout(const swab_desc *desc, size_t start) {
+    const size_t BH = (size_t)desc->b * desc->h, n = desc->n, G = desc->n_global, es = 2;
+    BwdGlobLayout L;
+    size_t o = up256(start);
+    auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
+    L.Qg = take(BH * G * 64 * es);
+    L.Og = take(BH * G * 64 * es);
+    L.dOg = take(BH * G * 64 * es);
+    L.dQg = take(BH * G * 64 * es);
+    L.lseg = take(BH * G * 4);
+    const size_t grows = (G + 127) / 128 * 128;   // whole 128-key tiles of gathered global keys
+    L.KG = take(BH * grows * 64 * es);
+    L.VG = take(BH * grows * 64 * es);
+    L.gdK = take(BH * n * 64 * es);
+    L.gdV = take(BH * n * 64 * es);
+    L.cdK = take(BH * G * 64 * 4);
+    L.cdV = take(BH * G * 64 * 4);
+    L.gp = take(global_proj_workspace_bytes((long long)BH, (int)G, (int)n));
+    L.end = o;
+    return L;
+}
+
 SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc) {
     if (!desc || desc->b < 1 || desc->h < 1 || desc->n < 1) return 0;
     const size_t rows = (size_t)desc->b * desc->h * desc->n;
     const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
     if (desc->dtype == SWAB_F32) return delta;
     // fp16 / bf16: the per-row delta, then the fp32 dQ accumulator [rows, 64]
-    return delta + rows * 64 * sizeof(float);
+    const size_t base = delta + rows * 64 * sizeof(float);
+    if (desc->n_global > 0 && desc->n_global <= SWAB_MAX_GLOBAL) return bwd_glob_layout(desc, base).end;
+    return base;
+}
+
+// band_attention_bwd with global tokens (f16 / bf16, contiguous layout, no key
+// bias or dropout): the band pass with global keys and queries left out, the
+// global columns as a pass of the same kernel over the gathered global keys,
+// and the global rows through the global-query backward (the shared Q, K, V
+// are their projections); all scratch in the caller's workspace.
+static swab_status bwd_with_globals(const swab_desc *desc, const Geom &g, DType dt, BwdArgs a, cudaStream_t st) {
+    GlobArgs gl;
+    swab_status s = check_globals(desc, {}, &gl);
+    if (s != SWAB_OK) return s;
+    if (dt == kF32 || g.rs_p || g.rs_o || g.kbias || g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;
+    if ((long long)(g.n + 31) / 32 * 4 > 12 * 1024) return SWAB_ERR_UNSUPPORTED;   // key bitmap in shared memory
+    const size_t rows = (size_t)g.BH * g.n;
+    char *ws = static_cast<char *>(static_cast<void *>(a.delta));
+    a.dqacc = reinterpret_cast<float *>(ws + up256(rows * sizeof(float)));
+    const BwdGlobLayout L = bwd_glob_layout(desc, up256(rows * sizeof(float)) + rows * 64 * sizeof(float));
+    GlobBwdBufs gb;
+    gb.Qg = ws + L.Qg;
+    gb.Og = ws + L.Og;
+    gb.dOg = ws + L.dOg;
+    gb.dQg = ws + L.dQg;
+    gb.lseg = reinterpret_cast<float *>(ws + L.lseg);
+    gb.KG = ws + L.KG;
+    gb.VG = ws + L.VG;
+    a.G = gl.G;
+    a.gdK = ws + L.gdK;
+    a.gdV = ws + L.gdV;
+    a.cdK = reinterpret_cast<float *>(ws + L.cdK);
+    a.cdV = reinterpret_cast<float *>(ws + L.cdV);
+    a.err = status_word();
+    if (!a.err) return SWAB_ERR_CUDA;
+    // band pass: the per-residue maps
+    TmapSet mq, mk, mv, mo, macc;
+    if (!build_dense_maps(&mq, a.Q, g, dt, kQKBoxRows, 0) || !build_dense_maps(&mk, a.K, g, dt, kQKBoxRows, 0) ||
+        !build_dense_maps(&mv, a.V, g, dt, kQKBoxRows, 0) || !build_dense_maps(&mo, a.dO, g, dt, kQKBoxRows, 0) ||
+        !build_acc_maps(&macc, a.dqacc, g))
+        return SWAB_ERR_CUDA;
+    // global columns: Q, dO and the accumulator with stride 1; the gathered
+    // global keys / values as [b, h, 128 x ceil(G / 128), 64]
+    Geom g1 = g;
+    g1.s = 1;
+    g1.nsub = g.n;
+    Geom gk = g;
+    gk.s = 1;
+    gk.n = (gl.G + 127) / 128 * 128;
+    gk.nsub = gk.n;
+    TmapSet mq1, mo1, mkc, mvc, macc1;
+    if (!build_dense_maps(&mq1, a.Q, g1, dt, kQKBoxRows, 0) || !build_dense_maps(&mo1, a.dO, g1, dt, kQKBoxRows, 0) ||
+        !build_dense_maps(&mkc, gb.KG, gk, dt, kQKBoxRows, 0) || !build_dense_maps(&mvc, gb.VG, gk, dt, kQKBoxRows, 0) ||
+        !build_acc_maps(&macc1, a.dqacc, g1))
+        return SWAB_ERR_CUDA;
+    // global rows: the global-query backward with Kg = K, Vg = V
+    GlobalProjArgs gp{};
+    gp.BH = g.BH;
+    gp.G = gl.G;
+    gp.n = g.n;
+    gp.scale = a.scale;
+    gp.Qg = gb.Qg;
+    gp.Kg = a.K;
+    gp.Vg = a.V;
+    gp.Og = gb.Og;
+    gp.dOg = gb.dOg;
+    gp.lseg = gb.lseg;
+    gp.dQg = gb.dQg;
+    gp.dKg = const_cast<void *>(a.gdK);
+    gp.dVg = const_cast<void *>(a.gdV);
+    gp.ws = reinterpret_cast<float *>(ws + L.gp);
+    gp.err = a.err;
+    Geom gkr{}, gqr{};
+    gkr.BH = gqr.BH = g.BH;
+    gkr.s = gqr.s = 1;
+    gkr.n = g.n;
+    gqr.n = gl.G;
+    TmapSet gmk, gmv, gmq, gmo;
+    if (!build_rows_maps(&gmk, a.K, gkr, dt, 128) || !build_rows_maps(&gmv, a.V, gkr, dt, 128) ||
+        !build_rows_maps(&gmq, gb.Qg, gqr, dt, 16) || !build_rows_maps(&gmo, gb.dOg, gqr, dt, 16))
+        return SWAB_ERR_CUDA;
+    return from_cuda(launch_band_attention_bwd_glob(dt, mq, mk, mv, mo, macc, mq1, mo1, mkc, mvc, macc1, gl, gb, a,
+                                                    gp, gmk, gmv, gmq, gmo, st));
 }
 
 SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, const void *Q,
@@ -706,10 +816,10 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
     DType dt;
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
-    if ((s = check_no_globals(desc)) != SWAB_OK) return s;
     if ((s = check_ptrs({Q, K, V, O, dO, lse, dQ, dK, dV, workspace})) != SWAB_OK) return s;
     cudaStream_t st = as_stream(stream);
     BwdArgs a{g, scale, Q, K, V, O, dO, lse, static_cast<float *>(workspace), dQ, dK, dV, nullptr};
+    if (desc->n_global > 0) return bwd_with_globals(desc, g, dt, a, st);
     if (dt == kF32) return from_cuda(launch_band_attention_bwd_f32(a, st));
     TmapSet mq, mk, mv, mo;
     if (!build_dense_maps(&mq, Q, g, dt, kQKBoxRows, g.rs_p) ||

@@ -117,6 +117,10 @@ struct BwdArgs {      // fused backward
     void *dQ, *dK, *dV;
     unsigned *err;
     float *dqacc;     // fused tensor-core path: fp32 dQ accumulator [BH, n, 64], or null
+    // global tokens (fused tensor-core path with n_global > 0)
+    int G;
+    const void *gdK, *gdV;   // [BH, n, 64]: the global rows' dK, dV terms (every key)
+    float *cdK, *cdV;        // [BH, G, 64] fp32: the global columns' dK (scaled), dV terms
 };
 
 struct DenseArgs {    // fp32 FFMA path
@@ -224,6 +228,26 @@ cudaError_t launch_global_proj_fwd_tc(DType dt, const TmapSet &mk, const TmapSet
 // Qg, dOg (16-row boxes), one slice per third coordinate
 cudaError_t launch_global_proj_bwd_tc(DType dt, const TmapSet &mk, const TmapSet &mv, const TmapSet &mq,
                                       const TmapSet &mo, const GlobalProjArgs &a, cudaStream_t st);
+// the fused backward with global tokens (f16 / bf16, contiguous layout).  The
+// workspace sections are set by the caller (swab_api.cu); maps:
+//   band pass: mq, mk, mv, mo, macc as for launch_band_attention_bwd_fused;
+//   global columns: mq1, mo1 (Q, dO with stride 1), mkc, mvc (the gathered
+//   global keys / values, [BH, 128 ceil(G / 128), 64]), macc1 (the
+//   accumulator, stride 1);
+//   global rows: gp (Qg, Og, dOg, lseg, dQg, dKg = a.gdK, dVg = a.gdV, ws set)
+//   with its maps gmk, gmv (K, V 128-row boxes), gmq, gmo (Qg, dOg 16-row boxes).
+struct GlobBwdBufs {
+    void *Qg, *Og, *dOg, *dQg;   // [BH, G, 64] gathered / the global rows' dQ
+    float *lseg;                 // [BH, G]
+    void *KG, *VG;               // [BH, 128 ceil(G / 128), 64]: the global keys, values, zero past G
+};
+cudaError_t launch_band_attention_bwd_glob(DType dt, const TmapSet &mq, const TmapSet &mk, const TmapSet &mv,
+                                           const TmapSet &mo, const TmapSet &macc, const TmapSet &mq1,
+                                           const TmapSet &mo1, const TmapSet &mkc, const TmapSet &mvc,
+                                           const TmapSet &macc1, const GlobArgs &gl, const GlobBwdBufs &gb,
+                                           const BwdArgs &a, const GlobalProjArgs &gp, const TmapSet &gmk,
+                                           const TmapSet &gmv, const TmapSet &gmq, const TmapSet &gmo,
+                                           cudaStream_t st);
 
 cudaError_t launch_band_softmax(DType dt, const SoftmaxArgs &a, cudaStream_t st);
 cudaError_t launch_band_softmax_bwd(DType dt, const SoftmaxArgs &a, cudaStream_t st);

@@ -215,9 +215,20 @@ def test_fused_forward_global_rules(lib):
     big = desc(n=200000, global_idx=[1])
     assert lib.band_attention(ctypes.byref(big.c), 1.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
                               P(FAKE), None) == UNSUPPORTED
-    # the fused backward still takes no global tokens
-    assert lib.band_attention_bwd(ctypes.byref(d.c), 1.0, *(P(FAKE) for _ in range(10)),
-                                  None) == UNSUPPORTED
+    # the fused backward takes global tokens in f16 / bf16 with the contiguous
+    # layout and a key bitmap that fits in shared memory; the rest is refused
+    # before anything is launched
+    for bad in (d32, ds, desc(n=120000, global_idx=[1])):
+        assert lib.band_attention_bwd(ctypes.byref(bad.c), 1.0, *(P(FAKE) for _ in range(10)),
+                                      None) == UNSUPPORTED
+    # the allocation-free backward takes no global tokens
+    assert lib.band_attention_bwd_noalloc(ctypes.byref(d.c), 1.0, *(P(FAKE) for _ in range(9)),
+                                          None) == UNSUPPORTED
+    # with global tokens the workspace grows by the gathered rows, the global
+    # keys' tiles and the global rows' dK, dV terms
+    plain = desc()
+    assert lib.band_attention_bwd_workspace(ctypes.byref(d.c)) > \
+        lib.band_attention_bwd_workspace(ctypes.byref(plain.c))
 
 
 def test_binding_checks_companion_shapes():

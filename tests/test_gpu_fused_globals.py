@@ -100,3 +100,57 @@ def test_fused_forward_globals_training_workload_sampled():
     wl = WORKLOADS[4]
     Q, K, V = workload_inputs(wl, count=3)
     check(swab.Desc.from_workload(wl), Q, K, V, wl.scale, (0, 77, 143))
+
+
+# ---------------------------------------------------------------------------
+# the fused backward with global tokens: band_attention_bwd gives the dQ, dK,
+# dV of the attention with global tokens on explicit key sets (the fp64
+# oracle's scatter) -- the band with global keys and queries left out, the
+# global columns and the global rows
+# ---------------------------------------------------------------------------
+def run_bwd(d, Q, K, V, dO, scale):
+    q, k, v, go = (x.cuda() for x in (Q, K, V, dO))
+    O = torch.empty_like(q)
+    lse = torch.empty(d.BH, d.n, dtype=torch.float32, device="cuda")
+    swab.band_attention(d, scale, q, k, v, O, lse)
+    dQ, dK, dV = (torch.full_like(q, float("nan")) for _ in range(3))
+    ws = torch.empty(swab.band_attention_bwd_workspace(d) // 4, dtype=torch.float32, device="cuda")
+    ws.fill_(float("nan"))  # contents on entry must not matter
+    swab.band_attention_bwd(d, scale, q, k, v, O, go, lse, dQ, dK, dV, ws)
+    torch.cuda.synchronize()
+    return dQ, dK, dV
+
+
+def check_bwd(d, Q, K, V, dO, scale, slices):
+    dQ, dK, dV = run_bwd(d, Q, K, V, dO, scale)
+    for b in slices:
+        sl = slice(b, b + 1)
+        refs = oracle.attention_bwd(f64(Q[sl]), f64(K[sl]), f64(V[sl]), f64(dO[sl]), d.w, d.w_upper,
+                                    d.dilation, scale, list(d.global_idx))
+        for name, got, ref in (("dQ", dQ, refs[0]), ("dK", dK, refs[1]), ("dV", dV, refs[2])):
+            assert within_abs(f64(got[sl].cpu()), ref, d.dtype), (name, b)
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_fused_backward_globals(case):
+    BH, n, w, wu, dil, dtype, gidx = case
+    d = swab.Desc(1, BH, n, 64, w, wu, dil, 0.0, dtype, gidx)
+    Q, K, V, dO = seeded_qkvo(BH, n, 64, dtype, seed=n + 91)
+    check_bwd(d, Q, K, V, dO, 0.125, range(BH))
+
+
+def test_fused_backward_globals_more_than_128():
+    """G = 150 global tokens: the global columns take two tiles of gathered
+    keys per slice (the second one ragged); with dilation."""
+    BH, n, gidx = 2, 900, tuple(range(0, 900, 6))
+    assert len(gidx) == 150
+    d = swab.Desc(1, BH, n, 64, 40, 40, 1, 0.0, torch.float16, gidx)
+    Q, K, V, dO = seeded_qkvo(BH, n, 64, torch.float16, seed=17)
+    check_bwd(d, Q, K, V, dO, 0.125, range(BH))
+
+
+def test_fused_backward_globals_training_workload_sampled():
+    """b = 12, h = 12, n = 4096, w = 256, 16 global tokens, bf16 (slices 0, 77, 143)."""
+    wl = WORKLOADS[4]
+    Q, K, V, dO = workload_inputs(wl)
+    check_bwd(swab.Desc.from_workload(wl), Q, K, V, dO, wl.scale, (0, 77, 143))
