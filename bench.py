@@ -193,6 +193,35 @@ class Step:
         return sum(x.numel() * x.element_size() for x in self.out_host)
 
 
+class GlobStep(Step):
+    """The materialised eight-call step with global tokens: every band tensor
+    has its two dense companions (cols [b, h, n, G], rows [b, h, G, n])."""
+
+    DESCRIPTION = ("materialised fwd+bwd with global tokens: band_qk, band_softmax, band_pv, "
+                   "band_qk(dO,V), band_softmax_bwd, band_pv(dS,K), band_qk_bwd_t, band_pv_bwd_t, "
+                   "each with its cols / rows companions")
+
+    def __init__(self, wl, device):
+        super().__init__(wl, device)
+        G = len(wl.global_idx)
+        mk = lambda: (torch.empty(wl.BH, wl.n, G, dtype=wl.dtype, device=device),  # noqa: E731
+                      torch.empty(wl.BH, G, wl.n, dtype=wl.dtype, device=device))
+        self.Sg, self.Pg, self.dPg, self.dSg = mk(), mk(), mk(), mk()
+
+    def launches(self):
+        s, d, sc = self.swab, self.d, self.wl.scale
+        return [
+            lambda: s.band_qk(d, sc, self.Q, self.K, self.S, self.Sg),
+            lambda: s.band_softmax(d, self.S, self.P, self.lse, Sg=self.Sg, Pg=self.Pg),
+            lambda: s.band_pv(d, 1.0, self.P, self.V, self.O, Pg=self.Pg),
+            lambda: s.band_qk(d, 1.0, self.dO, self.V, self.dP, self.dPg),
+            lambda: s.band_softmax_bwd(d, self.P, self.dP, self.dS, Pg=self.Pg, dPg=self.dPg, dSg=self.dSg),
+            lambda: s.band_pv(d, sc, self.dS, self.K, self.dQ, Pg=self.dSg),
+            lambda: s.band_qk_bwd_t(d, sc, self.dS, self.Q, self.dK, self.dSg),
+            lambda: s.band_pv_bwd_t(d, 1.0, self.P, self.dO, self.dV, self.Pg),
+        ]
+
+
 class FusedStep(Step):
     """Forward + backward with the scores kept on chip: band_attention (O, lse),
     then band_attention_bwd (dQ, dK, dV: its row-sum kernel, the one-pass
@@ -802,6 +831,19 @@ def main():
             also[f"fused+{feature.replace(' ', '_')}:{wl.name}"] = step_summary(wl, st, ps, pk, peaks)
             del st
         also.update(prologue_and_globals(device, n_also, flush, peaks))
+        # the training workload with global tokens through the materialised calls
+        w4 = WORKLOADS[4]
+        st = GlobStep(w4, device)
+        ps, pk = time_steps(st, max(3, n_also // 4), 3, flush)
+        ms = statistics.mean(ps)
+        fl = 6 * 2.0 * w4.head_dim * valid_pairs_globals(w4)
+        also[f"materialised+globals:{w4.name}"] = {
+            "ms_per_step": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+            "per_call_us": {f"{i}:{nm}": round(statistics.mean(t) * 1e3, 1)
+                            for i, (nm, t) in enumerate(zip(st.NAMES, pk))},
+            "note": "eight materialised calls with global tokens (16), bf16; flops = 6 contractions x "
+                    "2 x head_dim over the attended pairs"}
+        del st
     if swab.device_status(reset=True) != 0:
         raise SystemExit("a kernel raised the device status word during the benchmark")
 

@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libswab.so")
 SOURCES = ["swab_api.cu", "k_band_qk.cu", "k_band_gather.cu", "k_softmax.cu", "k_attention.cu", "k_attention_bwd.cu",
-           "k_global.cu", "k_bias_transpose.cu", "k_global_proj.cu"]
+           "k_global.cu", "k_bias_transpose.cu", "k_global_proj.cu",
+           "k_global_tc.cu"]
 HEADERS = ["swab_common.cuh", "swab_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -43,6 +43,10 @@ constexpr int kThreads = 32 * (2 + kGW);
 constexpr int kATile = kBM * kKC * 2;    // 16 KB
 constexpr int kBTile = kKC * 64 * 2;     // 8 KB (64 rows x 64 halves)
 constexpr int kSmemBytes = kStages * (kATile + kBTile) + 1024 + 1024;
+// up to this many global tokens the global term runs on the tensor cores as
+// one more chunk of the pipeline (K = G rounded up to 16); beyond it, FFMA in
+// the epilogue
+constexpr int kGlobTc = 64;
 constexpr uint32_t kTmemCols = 64;
 
 // bytes [2e, 2e + 16) of the 32-byte value (lo, hi), e in [0, 8)
@@ -139,9 +143,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
         for (int k = threadIdx.x; k < p.gl.G; k += blockDim.x)
             atomicOr(&gbits[p.gl.idx[k] >> 5], 1u << (p.gl.idx[k] & 31));
-        const T *ysrc = reinterpret_cast<const T *>(p.gy) + (long long)bh * g.n * 64;
-        for (int e = threadIdx.x; e < p.gl.G * 64; e += blockDim.x)
-            gyrows[e] = Elt<T>::to_f(ysrc[(long long)p.gl.idx[e >> 6] * 64 + (e & 63)]);
+        if (p.gl.G > kGlobTc) {   // the FFMA epilogue's global rows of Y
+            const T *ysrc = reinterpret_cast<const T *>(p.gy) + (long long)bh * g.n * 64;
+            for (int e = threadIdx.x; e < p.gl.G * 64; e += blockDim.x)
+                gyrows[e] = Elt<T>::to_f(ysrc[(long long)p.gl.idx[e >> 6] * 64 + (e & 63)]);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -152,12 +158,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             const CUtensorMap *mb = &mapB.m[r];
             tma_prefetch_desc(mb);
+            bool okp = true;
             for (int c = 0; c < nck; ++c) {
                 const int st = c % kStages;
                 const uint32_t ph = (c / kStages) & 1;
-                if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err)) break;
+                if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err)) { okp = false; break; }
                 mbar_arrive_expect_tx(&bfull[st], kBTile);
                 tma_load_3d(btile + st * kBTile, mb, &bfull[st], 0, k_lo + c * kKC, bh);
+            }
+            if (kGlob && p.gl.G <= kGlobTc && okp) {
+                // the global chunk: the gather warps write its B tile too
+                const int st = nck % kStages;
+                if (mbar_wait(&empty[st], ((nck / kStages) & 1) ^ 1, abort_flag, p.err)) mbar_arrive(&bfull[st]);
             }
         }
     } else if (warp == 1) {
@@ -165,7 +177,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             constexpr bool kBf16 = !std::is_same<T, __half>::value;
             const uint32_t idesc = idesc_f16(kBM, 64, kBf16, kTrans, true);
             bool ok = true;
-            for (int c = 0; c < nck && ok; ++c) {
+            // chunk nck (global tokens, G <= kGlobTc): the G weights of every
+            // output row against the G global rows of the dense operand
+            const int nall = nck + ((kGlob && p.gl.G <= kGlobTc) ? 1 : 0);
+            for (int c = 0; c < nall && ok; ++c) {
                 const int st = c % kStages;
                 const uint32_t ph = (c / kStages) & 1;
                 ok = mbar_wait(&bfull[st], ph, abort_flag, p.err) &&
@@ -174,8 +189,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(atile + st * kATile);
                 const uint32_t b_addr = smem_u32(btile + st * kBTile);
+                const int ksteps = c < nck ? kKC / 16 : (p.gl.G + 15) / 16;
 #pragma unroll
                 for (int k = 0; k < kKC / 16; ++k) {
+                    if (k >= ksteps) break;
                     // A: K-major (band_pv) advances 32 B per K=16 step inside the
                     // 128-B swizzle row; MN-major (band_t) advances 16 lines of
                     // 128 B.  B (dense rows, MN-major) advances 16 lines.
@@ -300,6 +317,51 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[st]);
         }
+        if (kGlob && p.gl.G <= kGlobTc && ok) {
+            // the global chunk, in the layouts of a band chunk (K = global
+            // index q):
+            //   A  band_pv: line m (output row), W = cols[row, q];
+            //      band_t: line q, the two 64-row halves 8 KB apart, W = rows[q, row]
+            //   B  line q: the global row G[q] of the dense operand
+            // zero past G (and, for band_pv, at a global output row)
+            const int st = nck % kStages;
+            const uint32_t ph = (nck / kStages) & 1;
+            ok = mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err);
+            if (__all_sync(0xffffffffu, ok)) {
+                uint8_t *at = atile + st * kATile, *bt = btile + st * kBTile;
+                const int G = p.gl.G;
+                const int t = gw * 32 + lane;
+                const T *W = reinterpret_cast<const T *>(p.gw);
+                for (int e = t; e < kBM * kKC; e += kGW * 32) {
+                    const int m = e / kKC, q = e % kKC, row = a0 + m;
+                    const long long ri = r + (long long)g.s * row;
+                    T v = Elt<T>::from_f(0.f);
+                    if (q < G && row < nr) {
+                        if (!kTrans) {
+                            if (!is_global(ri)) v = W[((long long)bh * g.n + ri) * G + q];
+                        } else {
+                            v = W[((long long)bh * G + q) * g.n + ri];
+                        }
+                    }
+                    const uint32_t off = !kTrans ? (uint32_t)(m * 128 + ((((q >> 3) ^ (m & 7))) << 4) + (q & 7) * 2)
+                                                 : (uint32_t)((m >> 6) * (kKC * 128) + q * 128 +
+                                                              ((((m & 63) >> 3) ^ (q & 7)) << 4) + (m & 7) * 2);
+                    *reinterpret_cast<T *>(at + off) = v;
+                }
+                const T *Y = reinterpret_cast<const T *>(p.gy) + (long long)bh * g.n * 64;
+                for (int e = t; e < kKC * 8; e += kGW * 32) {
+                    const int q = e >> 3, c = e & 7;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (q < G) v = *reinterpret_cast<const uint4 *>(Y + (long long)p.gl.idx[q] * 64 + 8 * c);
+                    *reinterpret_cast<uint4 *>(bt + q * 128 + ((c ^ (q & 7)) << 4)) = v;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[st]);
+            } else {
+                ok = false;
+            }
+        }
         // ---------------- epilogue ----------------
         const bool acc_ok = ok && mbar_wait(accfull, 0, abort_flag, p.err);
         if (__all_sync(0xffffffffu, acc_ok)) {
@@ -311,9 +373,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_ld32(tmem_addr(tmem, quarter * 32, half * 32), v);
             tmem_ld_wait();
             const int row = a0 + m;
-            if (kGlob && row < nr) {
+            if (kGlob && row < nr && p.gl.G > kGlobTc) {
                 // band_pv: + sum_g cols[i,g] V[G[g]] for a local query row i;
-                // band_t:  + sum_g rows[g,j] Y[G[g]] for key j.
+                // band_t:  + sum_g rows[g,j] Y[G[g]] for key j (on FFMA here
+                // past kGlobTc global tokens; up to it, the global chunk has
+                // added them on the tensor cores).
                 const long long ri = r + (long long)g.s * row;  // row index in the slice
                 if (!kTrans && is_global(ri)) {
 #pragma unroll
@@ -334,6 +398,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[i]);
                 }
+            }
+            if (kGlob && !kTrans && row < nr && p.gl.G <= kGlobTc && is_global(r + (long long)g.s * row)) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0u;   // a global query's row is dense, written apart
             }
             if (row < nr) {
                 T *out = reinterpret_cast<T *>(p.out) +
@@ -423,7 +491,7 @@ cudaError_t launch_gather2(const TmapSet &mapB, const GatherArgs &a, cudaStream_
 }  // namespace
 
 size_t gather_glob_smem(int n, int G) {
-    return (size_t)((n + 31) / 32) * 4 + (size_t)G * 64 * sizeof(float);
+    return (size_t)((n + 31) / 32) * 4 + (G > kGlobTc ? (size_t)G * 64 * sizeof(float) : 0);
 }
 
 size_t gather_smem_bytes(int n, int G) { return kSmemBytes + (G > 0 ? gather_glob_smem(n, G) : 0); }

@@ -267,6 +267,20 @@ swab_status check_no_globals(const swab_desc *d) {
     return d->n_global > 0 ? SWAB_ERR_UNSUPPORTED : SWAB_OK;
 }
 
+// The sums over the sequence for the G global outputs: tensor cores for f16 /
+// bf16 (the dense operand Y in 64-row boxes, stride 1), exact FFMA for fp32.
+cudaError_t glob_reduce(DType dt, const GlobReduceArgs &r, bool cols, cudaStream_t st) {
+    if (dt == kF32) return launch_glob_reduce(dt, r, cols, st);
+    Geom g1 = r.g;
+    g1.s = 1;
+    g1.nsub = r.g.n;
+    TmapSet my;
+    if (!build_rows_maps(&my, r.Y, g1, dt, 64)) return cudaErrorInvalidValue;
+    unsigned *err = status_word();
+    if (!err) return cudaErrorInvalidValue;
+    return launch_glob_reduce_tc(dt, my, r, cols, err, st);
+}
+
 // The two transposed-product names share this body.
 swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, const swab_glob *Bg,
                           const void *Y, void *X, void *stream) {
@@ -298,7 +312,7 @@ swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, co
     }
     if (e == cudaSuccess && gl.G > 0) {
         GlobReduceArgs r{g, gl, alpha, Bg->cols, Y, X};
-        e = launch_glob_reduce(dt, r, true, st);
+        e = glob_reduce(dt, r, true, st);
     }
     return from_cuda(e);
 }
@@ -401,7 +415,19 @@ SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, 
     }
     if (e == cudaSuccess && gl.G > 0) {
         GlobScoreArgs a{g, gl, alpha, A, B, Sg->cols, Sg->rows};
-        e = launch_glob_scores(dt, a, st);
+        if (dt == kF32) {
+            e = launch_glob_scores(dt, a, st);
+        } else {
+            // tensor cores: 128-row tiles of A and B in sequence order
+            Geom g1 = g;
+            g1.s = 1;
+            g1.nsub = g.n;
+            TmapSet ma, mb;
+            if (!build_rows_maps(&ma, A, g1, dt, 128) || !build_rows_maps(&mb, B, g1, dt, 128)) return SWAB_ERR_CUDA;
+            a.err = status_word();
+            if (!a.err) return SWAB_ERR_CUDA;
+            e = launch_glob_scores_tc(dt, ma, mb, a, st);
+        }
     }
     return from_cuda(e);
 }
@@ -585,7 +611,7 @@ SWAB_API swab_status band_pv(const swab_desc *desc, float alpha, const void *P,
     }
     if (e == cudaSuccess && gl.G > 0) {
         GlobReduceArgs r{g, gl, alpha, Pg->rows, V, O};
-        e = launch_glob_reduce(dt, r, false, st);
+        e = glob_reduce(dt, r, false, st);
     }
     return from_cuda(e);
 }

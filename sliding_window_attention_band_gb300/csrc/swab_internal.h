@@ -52,6 +52,7 @@ struct GlobScoreArgs {  // dense score pieces of band_qk
     float alpha;
     const void *A, *B;
     void *cols, *rows;
+    unsigned *err;     // device status word (tensor-core kernel)
 };
 
 struct SoftmaxGlobArgs {
@@ -193,6 +194,12 @@ size_t glob_bitmap_bytes(int n);
 cudaError_t launch_glob_scores(DType dt, const GlobScoreArgs &a, cudaStream_t st);
 cudaError_t launch_softmax_glob(DType dt, const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st);
 cudaError_t launch_glob_reduce(DType dt, const GlobReduceArgs &a, bool cols, cudaStream_t st);
+// the same two on the tensor cores (f16 / bf16; k_global_tc.cu): maps of A, B
+// (scores) or Y (reductions) over [BH, n, 64] with stride 1, 128- / 64-row boxes
+cudaError_t launch_glob_scores_tc(DType dt, const TmapSet &mapA, const TmapSet &mapB, const GlobScoreArgs &a,
+                                  cudaStream_t st);
+cudaError_t launch_glob_reduce_tc(DType dt, const TmapSet &mapY, const GlobReduceArgs &a, bool cols, unsigned *err,
+                                  cudaStream_t st);
 cudaError_t launch_band_f32_glob(const DenseGlobArgs &a, bool transposed, cudaStream_t st);
 // softmax forward / backward (all dtypes)
 struct BiasTransposeArgs {   // AddBiasTranspose

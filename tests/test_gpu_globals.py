@@ -37,6 +37,8 @@ CASES = [  # BH, n, w, w_upper, dilation, dtype, global idx
     (1, 640, 0, 127, 1, torch.float16, tuple(range(16))),
     (2, 300, 20, 20, 0, torch.float32, (0, 150, 299)),
     (1, 129, 1, 2, 0, torch.bfloat16, (64,)),
+    # more than 64 global tokens: the band products' global term on FFMA
+    (1, 700, 30, 30, 0, torch.float16, tuple(range(0, 700, 9))),
 ]
 
 
