@@ -1092,6 +1092,18 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             }
         };
 
+        // lse, delta of query column `lane` of the part starting at query cb
+        auto load_rowstats = [&](const KTile &tl, int cb, float &l, float &d) {
+            l = 0.f;
+            d = 0.f;
+            if (cb + lane < tl.nr) {
+                const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * (cb + lane);
+                l = p.lse[row];
+                d = p.delta[row];
+            }
+        };
+        float lq_next = 0.f, dq_next = 0.f;
+
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             KTile tl;
             if (!decode(t, tl)) continue;
@@ -1145,20 +1157,24 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                         }
                     }
                 }
-                // lse (log2 units) and delta of query column `lane` of the part
-                float lq = 0.f, dq = 0.f;
-                if (!empty && cbase + lane < tl.nr) {
-                    const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * (cbase + lane);
-                    lq = p.lse[row] * kLog2e;
-                    dq = p.delta[row];
+                // lse and delta of query column `lane` of the part: loaded one
+                // chunk ahead (the first chunk of a tile here), so that their
+                // latency is hidden behind the previous chunk
+                float lq, dq;
+                if (c == 0) {
+                    load_rowstats(tl, cbase, lq, dq);
+                } else {
+                    lq = lq_next;
+                    dq = dq_next;
                 }
+                if (c + 1 < tl.nck) load_rowstats(tl, cbase + kB, lq_next, dq_next);
                 if (!__all_sync(0xffffffffu, mbar_wait(sfull, gc & 1, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 __syncwarp();   // the previous chunk's reads of the slot are done
-                slot[lane] = lq;
+                slot[lane] = lq * kLog2e;
                 slot[32 + lane] = dq;
                 __syncwarp();
                 const float4 *l4 = reinterpret_cast<const float4 *>(slot);
