@@ -132,10 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *kvfull = qempty + 2;           // [kStages]
     uint64_t *kvempty = kvfull + kStages;    // [kStages]
     uint64_t *sfull = kvempty + kStages;     // [2]: S_b is in TMEM
-    uint64_t *sempty = sfull + 2;            // [2], count kWorkers: S_b copied to registers
-    uint64_t *pfull = sempty + 2;            // [2], count kWorkers: P_b (and a rescaled O) in TMEM
+    uint64_t *sempty = sfull + 2;            // [2], one arrival per softmax warp: S_b copied to registers
+    uint64_t *pfull = sempty + 2;            // [2], one arrival per softmax warp: P_b (and a rescaled O) in TMEM
     uint64_t *pempty = pfull + 2;            // [2]: the P.V product that read P_b is done
-    uint64_t *mlbar = pempty + 2;            // [4] per lane quarter, count 64
+    uint64_t *mlbar = pempty + 2;            // [4] per lane quarter, one arrival per warp (2)
     uint64_t *mmadone = mlbar + 4;           // 1: drain of the MMA pipe at exit
     uint64_t *drain = mmadone + 1;           // 1 int: never set (drain waits ignore aborts)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
@@ -163,15 +163,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&qfull[i], 1);
             mbar_init(&qempty[i], 1);
             mbar_init(&sfull[i], 1);
-            mbar_init(&sempty[i], kWorkers);
-            mbar_init(&pfull[i], kWorkers);
+            mbar_init(&sempty[i], kWorkers / 32);   // one arrival per softmax warp
+            mbar_init(&pfull[i], kWorkers / 32);
             mbar_init(&pempty[i], 1);
         }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&kvfull[i], 1);
             mbar_init(&kvempty[i], 1);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(&mlbar[i], 64);
+        for (int i = 0; i < 4; ++i) mbar_init(&mlbar[i], 2);   // the two warps of a lane quarter
         mbar_init(mmadone, 1);
         *no_abort = 0;
         *abort_flag = 0;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             epi_pend = false;
             float2 *ml = mlx + (epi_it & 1) * 2 * kBQ;
             ml[half * kBQ + q] = make_float2(epi_m, epi_l);
-            mbar_arrive(&mlbar[quarter]);
+            mbar_arrive_warp(&mlbar[quarter]);
             if (!__all_sync(0xffffffffu, mbar_wait(&mlbar[quarter], epi_it & 1, abort_flag, p.err)))
                 return false;
             const float2 e0 = ml[q], e1 = ml[kBQ + q];
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&sempty[b]);   // the scores are in registers: S_b may be rewritten
+                mbar_arrive_warp(&sempty[b]);   // the scores are in registers: S_b may be rewritten
                 const bool neg = kBias ? false : neg_scale;
                 const float never = neg ? INFINITY : -INFINITY;   // the masked value that never wins
                 float ext = never;
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&pfull[b]);    // P_b (and the rescaled O) are in tensor memory
+                mbar_arrive_warp(&pfull[b]);    // P_b (and the rescaled O) are in tensor memory
                 m = mref;
             }
             if (!ok) break;

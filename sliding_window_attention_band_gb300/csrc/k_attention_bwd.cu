@@ -634,8 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // One-pass backward: dK, dV and dQ from one persistent kernel.
 // Tile = 128 keys of one residue; for each 128-query chunk of its band:
 //   S^T = K Q_c^T, dP^T = V dO_c^T               (tcgen05, TMEM lane = key)
-//   P^T, dS^T per key row (16 softmax warps: 4 per TMEM lane quarter, each
-//   owning 32 query columns): P^T into tensor memory (packed 16-bit pairs),
+//   P^T, dS^T per key row (8 softmax warps: 2 per TMEM lane quarter, each
+//   owning 64 query columns): P^T into tensor memory (packed 16-bit pairs),
 //   dS^T as a K-major 128-B-swizzled shared-memory operand
 //   dV += P^T dO_c (A from TMEM), dK += dS^T Q_c   (TMEM, lane = key)
 //   dQ_c = dS K: the dS^T tile read as an MN-major A operand (M = queries),
@@ -650,21 +650,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   computed); V, read only by the dP^T product, has one buffer that is
 //   reloaded after the tile's last dP^T; Q and dO chunks use a 3-stage ring,
 //   so each chunk's load has a whole gradient phase to land.
-// Each softmax warp loads the lse and delta of its 32 query columns itself
-// (one of each per lane) and shares them through a per-warp shared slot.
+// Each softmax warp loads the lse and delta of its 64 query columns itself
+// (two of each per lane, one chunk ahead) and shares them through a per-warp
+// shared slot.  Eight softmax warps (two per scheduler, beside the producer,
+// MMA and reducer warps) leave each thread 168 registers and the MMA warp's
+// scheduler two busy warps to share with.
 // The accumulation order of dQ across key tiles is not fixed, so dQ may
 // differ in the last bits between runs; dK and dV have one writer per row.
 // ---------------------------------------------------------------------------
 namespace fused {
-constexpr int kParts = 4;
-constexpr int kWorkerWarps = 4 * kParts;        // 16
-constexpr int kWorkers = 32 * kWorkerWarps;     // 512
-constexpr int kReducerWarp = 2 + kWorkerWarps;  // 18
+constexpr int kParts = 2;                       // 64 query columns per softmax warp
+constexpr int kWorkerWarps = 4 * kParts;        // 8
+constexpr int kWorkers = 32 * kWorkerWarps;     // 256
+constexpr int kReducerWarp = 2 + kWorkerWarps;  // 10
 constexpr int kThreads = 32 * (kReducerWarp + 1);
 constexpr int kQS = 2 * kTile;                  // Q and dO of a query chunk: 32 KB
 constexpr int kQStages = 3;
 constexpr int kStage = 128 * 64 * 4;            // fp32 dQ staging: two 128 x 32 swizzled halves
-constexpr int kSlot = 2 * 32 * 4;               // per softmax warp: lse*log2e, delta of 32 queries
+constexpr int kSlot = 2 * 64 * 4;               // per softmax warp: lse*log2e, delta of 64 queries
 constexpr int kSmem = 3 * kTile + kQStages * kQS + kOpBytes + kStage + kWorkerWarps * kSlot + 1024 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColP = 448;
 
@@ -711,8 +714,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
     uint8_t *qsbuf = vbuf + kTile;              // [kQStages] query chunks: Q at +0, dO at +kTile
     uint8_t *dst_op = qsbuf + kQStages * kQS;   // dS^T [128 keys x 128 queries]
     uint8_t *stage = dst_op + kOpBytes;         // fp32 dQ: channels [0,32) at +0, [32,64) at +16 KB
-    float *slots = reinterpret_cast<float *>(stage + kStage);  // [16 warps][lse | delta][32]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(slots + kWorkerWarps * 64);
+    float *slots = reinterpret_cast<float *>(stage + kStage);  // [8 warps][lse | delta][64]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(slots + kWorkerWarps * (kSlot / 4));
     uint64_t *kfull = bars;            // [2]
     uint64_t *kempty = kfull + 2;      // [2]
     uint64_t *vfull = kempty + 2;      // 1
@@ -720,13 +723,13 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
     uint64_t *qfull = vempty + 1;      // [kQStages]
     uint64_t *qempty = qfull + kQStages;  // [kQStages]
     uint64_t *sfull = qempty + kQStages;  // 1
-    uint64_t *sempty = sfull + 1;      // 1, count fused::kWorkers
-    uint64_t *opfull = sempty + 1;     // 1, count fused::kWorkers
+    uint64_t *sempty = sfull + 1;      // 1, count fused::kWorkerWarps
+    uint64_t *opfull = sempty + 1;     // 1, count fused::kWorkerWarps
     uint64_t *opempty = opfull + 1;    // 1 (also: dQ of that chunk is in TMEM)
-    uint64_t *dqempty = opempty + 1;   // 1, count fused::kWorkers: dQ read out of TMEM
-    uint64_t *stfull = dqempty + 1;    // 1, count fused::kWorkers
+    uint64_t *dqempty = opempty + 1;   // 1, count fused::kWorkerWarps: dQ read out of TMEM
+    uint64_t *stfull = dqempty + 1;    // 1, count fused::kWorkerWarps
     uint64_t *stempty = stfull + 1;    // 1
-    uint64_t *accempty = stempty + 1;  // 1, count fused::kWorkers: dV, dK of a tile read out
+    uint64_t *accempty = stempty + 1;  // 1, count fused::kWorkerWarps: dV, dK of a tile read out
     uint64_t *mmadone = accempty + 1;  // 1
     uint64_t *drain = mmadone + 1;     // a flag word that is never set
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
@@ -778,14 +781,14 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         }
         mbar_init(vfull, 1);
         mbar_init(vempty, 1);
-        mbar_init(dqempty, fused::kWorkers);
+        mbar_init(dqempty, fused::kWorkerWarps);
         mbar_init(sfull, 1);
-        mbar_init(sempty, fused::kWorkers);
-        mbar_init(opfull, fused::kWorkers);
+        mbar_init(sempty, fused::kWorkerWarps);
+        mbar_init(opfull, fused::kWorkerWarps);
         mbar_init(opempty, 1);
-        mbar_init(stfull, fused::kWorkers);
+        mbar_init(stfull, fused::kWorkerWarps);
         mbar_init(stempty, 1);
-        mbar_init(accempty, fused::kWorkers);
+        mbar_init(accempty, fused::kWorkerWarps);
         mbar_init(mmadone, 1);
         *no_abort = 0;
         *abort_flag = 0;
@@ -986,14 +989,16 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         // ---------------- softmax warps: thread = key row ----------------
         pdl_wait();   // the row sums delta are written
         const int quarter = warp & 3;
-        const int part = (warp - 2) >> 2;        // query columns [32 part, 32 part + 32)
+        const int part = (warp - 2) >> 2;        // query columns [64 part, 64 part + 64)
         const int m = quarter * 32 + lane;       // TMEM lane: key of the tile / query of a dQ chunk
         const float xscale = p.scale * kLog2e;
         const float dscale = 256.f / (256.f - (float)g.drop_t);   // kept values' scale
         const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
-        const uint32_t drow = smem_u32(dst_op) + (part >> 1) * (kOpBytes / 2) + m * 128;
-        const uint32_t srow = smem_u32(stage) + (part >> 1) * (kStage / 2) + m * 128;
-        float *slot = slots + (warp - 2) * 64;
+        // dS^T: the part's 64 queries are one 64-query block of the operand;
+        // fp32 dQ staging: the part's 32 channels are one half of the tile
+        const uint32_t drow = smem_u32(dst_op) + part * (kOpBytes / 2) + m * 128;
+        const uint32_t srow = smem_u32(stage) + part * (kStage / 2) + m * 128;
+        float *slot = slots + (warp - 2) * (kSlot / 4);   // lse (64 queries) | delta (64)
         uint32_t gc = 0, it = 0;
         bool ok = true;
         bool dq_pend = false;   // the dQ of chunk dq_g (in TMEM) waits to be staged
@@ -1002,21 +1007,14 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         unsigned acc_row = 0;   // row bh * n + key of dK, dV (below 2^31); kMode 2: the key's index in G
         int acc_bh = 0;         // kMode 2: the slice
         int acc_gi = -1;        // kMode 1: index in G of a global key, else -1
-        // dV, dK of key row acc_row (channels [16 part, +16)); the caller has
-        // waited for the tile's last products
-        auto drain_acc = [&]() {
-            uint32_t a[16], b[16];
-            tmem_ld16(lane_base + kColDV + 16 * part, a);
-            tmem_ld16(lane_base + kColDK + 16 * part, b);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(accempty);
+        // dV (a), dK (b) of key row acc_row, channels [ch0, ch0 + 16)
+        auto drain16 = [&](const uint32_t (&a)[16], const uint32_t (&b)[16], int ch0) {
             if constexpr (kMode == 2) {
                 // the global columns' dK (scaled), dV of global key acc_row
                 // (its index in G) of slice acc_bh, fp32
                 if (acc_ok) {
-                    float4 *cv = reinterpret_cast<float4 *>(p.cdV + ((size_t)acc_bh * gl.G + acc_row) * 64 + 16 * part);
-                    float4 *ck = reinterpret_cast<float4 *>(p.cdK + ((size_t)acc_bh * gl.G + acc_row) * 64 + 16 * part);
+                    float4 *cv = reinterpret_cast<float4 *>(p.cdV + ((size_t)acc_bh * gl.G + acc_row) * 64 + ch0);
+                    float4 *ck = reinterpret_cast<float4 *>(p.cdK + ((size_t)acc_bh * gl.G + acc_row) * 64 + ch0);
                     const float sc = p.scale;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -1034,7 +1032,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 // global columns' terms, added before the one rounding
                 if (acc_ok) {
                     const float sc = p.scale;
-                    const size_t goff = (size_t)acc_row * 64 + 16 * part;   // contiguous layout
+                    const size_t goff = (size_t)acc_row * 64 + ch0;   // contiguous layout
                     const uint4 *gv = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.gdV) + goff);
                     const uint4 *gk = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.gdK) + goff);
                     float fv[16], fk[16];
@@ -1051,8 +1049,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                         }
                     }
                     if (acc_gi >= 0) {
-                        const float *cv = p.cdV + ((size_t)acc_bh * gl.G + acc_gi) * 64 + 16 * part;
-                        const float *ck = p.cdK + ((size_t)acc_bh * gl.G + acc_gi) * 64 + 16 * part;
+                        const float *cv = p.cdV + ((size_t)acc_bh * gl.G + acc_gi) * 64 + ch0;
+                        const float *ck = p.cdK + ((size_t)acc_bh * gl.G + acc_gi) * 64 + ch0;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             fv[i] += cv[i];
@@ -1073,7 +1071,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 return;
             }
             if (acc_ok) {
-                const long long off = dense_row(g, acc_row, g.rs_p) + 16 * part;
+                const long long off = dense_row(g, acc_row, g.rs_p) + ch0;
                 uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + off);
                 uint4 *k4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dK) + off);
                 const float sc = p.scale;
@@ -1091,18 +1089,46 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 }
             }
         };
-
-        // lse, delta of query column `lane` of the part starting at query cb
-        auto load_rowstats = [&](const KTile &tl, int cb, float &l, float &d) {
-            l = 0.f;
-            d = 0.f;
-            if (cb + lane < tl.nr) {
-                const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * (cb + lane);
-                l = p.lse[row];
-                d = p.delta[row];
+        // dV, dK of key row acc_row (channels [32 part, +32)) out of TMEM;
+        // the caller has waited for the tile's last products
+        auto drain_acc = [&]() {
+            uint32_t a0[16], b0[16], a1[16], b1[16];
+            tmem_ld16(lane_base + kColDV + 32 * part, a0);
+            tmem_ld16(lane_base + kColDK + 32 * part, b0);
+            tmem_ld16(lane_base + kColDV + 32 * part + 16, a1);
+            tmem_ld16(lane_base + kColDK + 32 * part + 16, b1);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive_warp(accempty);
+            drain16(a0, b0, 32 * part);
+            drain16(a1, b1, 32 * part + 16);
+        };
+        // lse, delta of the queries cb + lane and cb + 32 + lane
+        auto load_rowstats = [&](const KTile &tl, int cb, float (&l)[2], float (&d)[2]) {
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                l[w] = 0.f;
+                d[w] = 0.f;
+                if (cb + 32 * w + lane < tl.nr) {
+                    const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * (cb + 32 * w + lane);
+                    l[w] = p.lse[row];
+                    d[w] = p.delta[row];
+                }
             }
         };
-        float lq_next = 0.f, dq_next = 0.f;
+        float lq_next[2] = {0.f, 0.f}, dq_next[2] = {0.f, 0.f};
+        // dQ of chunk dq_g (channels [32 part, +32) of query row m) into the
+        // staging tile, once the reducer has read the previous one
+        auto stage_dq = [&](const uint32_t (&dqv)[32]) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(stempty, (dq_g & 1) ^ 1, abort_flag, p.err))) return false;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                sts16(srow + ((u ^ (m & 7)) << 4),
+                      make_uint4(dqv[4 * u], dqv[4 * u + 1], dqv[4 * u + 2], dqv[4 * u + 3]));
+            fence_proxy_async_smem();
+            mbar_arrive_warp(stfull);
+            return true;
+        };
 
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             KTile tl;
@@ -1123,49 +1149,59 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             if constexpr (kMode == 2) key_off = kk >= gl.G;
             for (int c = 0; c < tl.nck; ++c, ++gc) {
                 const int qbase = tl.qb_lo + c * kB;
-                const int cbase = qbase + 32 * part;
-                // this key's queries inside the part: columns [jlo, jhi] (kMode
-                // 2: every query of the sequence)
-                const int jlo = kMode == 2 ? 0 : max(kk - g.wu - cbase, 0);
-                const int jhi = kMode == 2 ? min(tl.nr - 1 - cbase, 31) : min(min(kk + g.w, tl.nr - 1) - cbase, 31);
-                uint32_t vmask = (key_off || jlo > jhi) ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
-                if constexpr (kMode != 0) {
-                    // global queries (query column `lane` of the part) take no band
-                    // or global-column keys: their rows are dense, done apart
-                    const int qsub = cbase + lane;
-                    const bool qg = qsub < tl.nr && is_global(tl.r + g.s * qsub);
-                    vmask &= ~__ballot_sync(0xffffffffu, qg);
+                const int cbase = qbase + 64 * part;
+                // vm[w]: this key's queries among the columns [32 w, 32 w + 32)
+                // of the part (kMode 2: every query of the sequence)
+                uint32_t vm[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int cb = cbase + 32 * w;
+                    const int jlo = kMode == 2 ? 0 : max(kk - g.wu - cb, 0);
+                    const int jhi = kMode == 2 ? min(tl.nr - 1 - cb, 31) : min(min(kk + g.w, tl.nr - 1) - cb, 31);
+                    vm[w] = (key_off || jlo > jhi) ? 0u : ((2u << jhi) - 1u) & (0xffffffffu << jlo);
+                    if constexpr (kMode != 0) {
+                        // global queries (query column `lane` of the word) take no
+                        // band or global-column keys: their rows are dense, done apart
+                        const int qsub = cb + lane;
+                        const bool qg = qsub < tl.nr && is_global(tl.r + g.s * qsub);
+                        vm[w] &= ~__ballot_sync(0xffffffffu, qg);
+                    }
                 }
-                const bool full = __all_sync(0xffffffffu, vmask == 0xffffffffu);
-                const bool empty = __all_sync(0xffffffffu, vmask == 0u);
-                // dropout: bit j = keep(query column j of the part, this key).
-                // Lane l draws the block of query column l for the warp's 32
-                // keys (one block: the warp's keys start on a multiple of 32)
-                // and 32 ballots transpose the bits to the key rows.
-                uint32_t keepcol = 0xffffffffu;
+                const bool full = __all_sync(0xffffffffu, (vm[0] & vm[1]) == 0xffffffffu);
+                const bool empty = __all_sync(0xffffffffu, (vm[0] | vm[1]) == 0u);
+                // dropout: bit j of keepcol[w] = keep(query column 32 w + j of the
+                // part, this key).  Lane l draws the block of query column 32 w + l
+                // for the warp's 32 keys (one block: the warp's keys start on a
+                // multiple of 32) and 32 ballots transpose the bits to the key rows.
+                uint32_t keepcol[2] = {0xffffffffu, 0xffffffffu};
                 if constexpr (kDrop) {
                     if (!empty) {
-                        unsigned long long wv[4];
-                        philox4x64_10((unsigned long long)((tl.a0 + 32 * quarter) / 32),
-                                      (unsigned long long)(tl.r + (long long)g.s * (cbase + lane)),
-                                      (unsigned long long)tl.bh, 0, g.seed, 0, wv);
-                        const uint32_t row = keep_bits32(wv, g.drop_t);
 #pragma unroll
-                        for (int l = 0; l < 32; ++l) {
-                            const uint32_t col = __ballot_sync(0xffffffffu, (row >> l) & 1u);
-                            if (l == lane) keepcol = col;
+                        for (int w = 0; w < 2; ++w) {
+                            unsigned long long wv[4];
+                            philox4x64_10((unsigned long long)((tl.a0 + 32 * quarter) / 32),
+                                          (unsigned long long)(tl.r + (long long)g.s * (cbase + 32 * w + lane)),
+                                          (unsigned long long)tl.bh, 0, g.seed, 0, wv);
+                            const uint32_t row = keep_bits32(wv, g.drop_t);
+#pragma unroll
+                            for (int l = 0; l < 32; ++l) {
+                                const uint32_t col = __ballot_sync(0xffffffffu, (row >> l) & 1u);
+                                if (l == lane) keepcol[w] = col;
+                            }
                         }
                     }
                 }
-                // lse and delta of query column `lane` of the part: loaded one
-                // chunk ahead (the first chunk of a tile here), so that their
-                // latency is hidden behind the previous chunk
-                float lq, dq;
+                // lse and delta of the part's queries: loaded one chunk ahead
+                // (the first chunk of a tile here), so that their latency is
+                // hidden behind the previous chunk
+                float lq[2], dq[2];
                 if (c == 0) {
                     load_rowstats(tl, cbase, lq, dq);
                 } else {
-                    lq = lq_next;
-                    dq = dq_next;
+                    lq[0] = lq_next[0];
+                    lq[1] = lq_next[1];
+                    dq[0] = dq_next[0];
+                    dq[1] = dq_next[1];
                 }
                 if (c + 1 < tl.nck) load_rowstats(tl, cbase + kB, lq_next, dq_next);
                 if (!__all_sync(0xffffffffu, mbar_wait(sfull, gc & 1, abort_flag, p.err))) {
@@ -1174,35 +1210,41 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 }
                 tc_fence_after();
                 __syncwarp();   // the previous chunk's reads of the slot are done
-                slot[lane] = lq * kLog2e;
-                slot[32 + lane] = dq;
+                slot[lane] = lq[0] * kLog2e;
+                slot[32 + lane] = lq[1] * kLog2e;
+                slot[64 + lane] = dq[0];
+                slot[96 + lane] = dq[1];
                 __syncwarp();
                 const float4 *l4 = reinterpret_cast<const float4 *>(slot);
-                const float4 *d4 = reinterpret_cast<const float4 *>(slot + 32);
+                const float4 *d4 = reinterpret_cast<const float4 *>(slot + 64);
                 const uint64_t xs2 = f2(xscale, xscale);
-                uint32_t pk[16], dk[16];
-                // columns [8h, 8h + 8) of the part in four steps; the next
-                // step's loads are in flight while a step is computed
+                // packed P^T and dS^T of the part's columns: [32 w + 2 q, +2) in
+                // word q of pk[w], dk[w]
+                uint32_t pk[2][16], dk[2][16];
+                // columns [8h, 8h + 8) of the part in eight steps
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
+                for (int h = 0; h < 8; ++h) {
+                    const int w = h >> 2;                 // word of the step's columns
+                    const uint32_t vmask = vm[w], keep = keepcol[w];
                     uint32_t sv[8], dv[8];
-                    tmem_ld8(lane_base + kColS + 32 * part + 8 * h, sv);
-                    tmem_ld8(lane_base + kColDP + 32 * part + 8 * h, dv);
+                    tmem_ld8(lane_base + kColS + 64 * part + 8 * h, sv);
+                    tmem_ld8(lane_base + kColDP + 64 * part + 8 * h, dv);
                     tmem_ld_wait();
-                    if (h == 3) {
+                    if (h == 7) {
                         tc_fence_before();
-                        mbar_arrive(sempty);
+                        mbar_arrive_warp(sempty);
                     }
                     if (empty) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) pk[4 * h + i] = dk[4 * h + i] = 0u;
+                        for (int i = 0; i < 4; ++i) pk[w][4 * (h & 3) + i] = dk[w][4 * (h & 3) + i] = 0u;
                         continue;
                     }
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const float4 lv = l4[2 * h + u], dl = d4[2 * h + u];
-                        const int i = 4 * u;           // within the step
-                        const int j = 8 * h + i;       // within the part
+                        const int i = 4 * u;                  // within the step
+                        const int j = 8 * (h & 3) + i;        // within the word
+                        const int q = 4 * (h & 3) + 2 * u;    // packed word of pk[w], dk[w]
                         float p0, p1, p2, p3;
                         {
                             float y0, y1, y2, y3;
@@ -1225,10 +1267,10 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                         float s0, s1, s2, s3;
                         if constexpr (kDrop) {
                             // dS = p (f dP - delta), and dV takes p f
-                            const float f0 = ((keepcol >> j) & 1u) ? dscale : 0.f;
-                            const float f1 = ((keepcol >> (j + 1)) & 1u) ? dscale : 0.f;
-                            const float f2_ = ((keepcol >> (j + 2)) & 1u) ? dscale : 0.f;
-                            const float f3 = ((keepcol >> (j + 3)) & 1u) ? dscale : 0.f;
+                            const float f0 = ((keep >> j) & 1u) ? dscale : 0.f;
+                            const float f1 = ((keep >> (j + 1)) & 1u) ? dscale : 0.f;
+                            const float f2_ = ((keep >> (j + 2)) & 1u) ? dscale : 0.f;
+                            const float f3 = ((keep >> (j + 3)) & 1u) ? dscale : 0.f;
                             f2split(mul2(f2(p0, p1), fma2(f2(f0, f1), f2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), f2(-dl.x, -dl.y))), s0, s1);
                             f2split(mul2(f2(p2, p3), fma2(f2(f2_, f3), f2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2(-dl.z, -dl.w))), s2, s3);
                             p0 *= f0;
@@ -1239,10 +1281,10 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                             f2split(mul2(f2(p0, p1), sub2(f2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), f2(dl.x, dl.y))), s0, s1);
                             f2split(mul2(f2(p2, p3), sub2(f2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), f2(dl.z, dl.w))), s2, s3);
                         }
-                        pk[4 * h + 2 * u] = pack2<T>(p0, p1);
-                        pk[4 * h + 2 * u + 1] = pack2<T>(p2, p3);
-                        dk[4 * h + 2 * u] = pack2<T>(s0, s1);
-                        dk[4 * h + 2 * u + 1] = pack2<T>(s2, s3);
+                        pk[w][q] = pack2<T>(p0, p1);
+                        pk[w][q + 1] = pack2<T>(p2, p3);
+                        dk[w][q] = pack2<T>(s0, s1);
+                        dk[w][q + 1] = pack2<T>(s2, s3);
                     }
                 }
                 // the products of chunk gc-1 are done: its operands are free,
@@ -1253,40 +1295,33 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                // P^T: query columns [32 part, +32) are TMEM columns [16 part, +16) of the P region
-                tmem_st16(lane_base + kColP + 16 * part, pk);
+                // P^T: query columns [64 part, +64) are TMEM columns [32 part, +32) of the P region
+                tmem_st16(lane_base + kColP + 32 * part, pk[0]);
+                tmem_st16(lane_base + kColP + 32 * part + 16, pk[1]);
+                // dS^T: columns 8u.. of the part are 16-byte chunk u of the key row
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t off = (uint32_t)((((part & 1) * 4 + u) ^ (m & 7)) << 4);
-                    sts16(drow + off, make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]));
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t off = (uint32_t)((u ^ (m & 7)) << 4);
+                    const int w = u >> 2, q = 4 * (u & 3);
+                    sts16(drow + off, make_uint4(dk[w][q], dk[w][q + 1], dk[w][q + 2], dk[w][q + 3]));
                 }
                 tmem_st_wait();
                 if (acc_pend) {
                     drain_acc();
                     acc_pend = false;
                 }
-                uint32_t dqv[16];
+                uint32_t dqv[32];
                 if (dq_pend) {
-                    tmem_ld16(lane_base + kColDQ + 16 * part, dqv);
+                    tmem_ld32(lane_base + kColDQ + 32 * part, dqv);
                     tmem_ld_wait();
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
-                mbar_arrive(dqempty);
-                mbar_arrive(opfull);
-                if (dq_pend) {
-                    // dQ of chunk dq_g (channels [16 part, +16) of query row m) into
-                    // the staging tile, once the reducer has read the previous one
-                    if (!__all_sync(0xffffffffu, mbar_wait(stempty, (dq_g & 1) ^ 1, abort_flag, p.err))) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        sts16(srow + ((((part & 1) * 4 + u) ^ (m & 7)) << 4),
-                              make_uint4(dqv[4 * u], dqv[4 * u + 1], dqv[4 * u + 2], dqv[4 * u + 3]));
-                    fence_proxy_async_smem();
-                    mbar_arrive(stfull);
+                mbar_arrive_warp(dqempty);
+                mbar_arrive_warp(opfull);
+                if (dq_pend && !stage_dq(dqv)) {
+                    ok = false;
+                    break;
                 }
                 dq_pend = true;
                 dq_g = gc;
@@ -1323,18 +1358,11 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             if (__all_sync(0xffffffffu, mbar_wait(opempty, (gc - 1) & 1, abort_flag, p.err))) {
                 tc_fence_after();
                 if (acc_pend) drain_acc();
-                uint32_t dqv[16];
-                tmem_ld16(lane_base + kColDQ + 16 * part, dqv);
+                uint32_t dqv[32];
+                tmem_ld32(lane_base + kColDQ + 32 * part, dqv);
                 tmem_ld_wait();
                 tc_fence_before();
-                if (__all_sync(0xffffffffu, mbar_wait(stempty, (dq_g & 1) ^ 1, abort_flag, p.err))) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        sts16(srow + ((((part & 1) * 4 + u) ^ (m & 7)) << 4),
-                              make_uint4(dqv[4 * u], dqv[4 * u + 1], dqv[4 * u + 2], dqv[4 * u + 3]));
-                    fence_proxy_async_smem();
-                    mbar_arrive(stfull);
-                }
+                stage_dq(dqv);
             }
         }
     }
