@@ -883,6 +883,23 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         const uint64_t d_dsmn = sdesc_sw128(smem_u32(dst_op), kOpBytes / 2, 1024);
         auto issue_grad = [&](uint32_t gg, bool first, bool last, int tb, uint32_t itt) -> bool {
             const int qs = gg % kQStages;
+            const uint64_t qoff = (uint64_t)((qs * kQS) >> 4), toff = (uint64_t)((tb * kTile) >> 4);
+            // the chunk's operand descriptors, formed before the waits so that
+            // the 24 products issue back to back
+            uint64_t dv_b[8], dk_a[8], dk_b[8], dq_a[8], dq_b[8];
+#pragma unroll
+            for (int k = 0; k < kB / 16; ++k) {
+                // K step k = queries 16k.. (dV, dK) or keys 16k.. (dQ)
+                const uint64_t aop = (uint64_t)((((k >> 2) * (kOpBytes / 2)) + (k & 3) * 32) >> 4);
+                const uint64_t rows = (uint64_t)((2048 * k) >> 4);
+                dv_b[k] = d_omn + qoff + rows;
+                dk_a[k] = d_dst + aop;
+                dk_b[k] = d_qmn + qoff + rows;
+                dq_a[k] = d_dsmn + rows;
+                dq_b[k] = d_kmn + toff + rows;
+                asm volatile("" ::"l"(dv_b[k]), "l"(dk_b[k]), "l"(dq_b[k]));
+            }
+            const uint32_t acc0 = first ? 0u : 1u;
             // the softmax warps read dQ of chunk gg-1 out of TMEM in chunk gg
             // (phase gg of dqempty), before they signal its operands
             bool w = mbar_wait(opfull, gg & 1, abort_flag, p.err) &&
@@ -890,17 +907,13 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             if (first) w = w && mbar_wait(accempty, (itt & 1) ^ 1, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, w)) return false;
             tc_fence_after();
-            const uint64_t qoff = (uint64_t)((qs * kQS) >> 4), toff = (uint64_t)((tb * kTile) >> 4);
             if (lane == 0) {
 #pragma unroll
                 for (int k = 0; k < kB / 16; ++k) {
-                    // K step k = queries 16k.. (dV, dK) or keys 16k.. (dQ)
-                    const uint64_t aop = (uint64_t)((((k >> 2) * (kOpBytes / 2)) + (k & 3) * 32) >> 4);
-                    const uint64_t rows = (uint64_t)((2048 * k) >> 4);
-                    const uint32_t acc = (first && k == 0) ? 0u : 1u;
-                    mma_f16_ts(tmem + kColDV, tmem + kColP + 8 * k, d_omn + qoff + rows, id_g, acc);
-                    mma_f16_ss(tmem + kColDK, d_dst + aop, d_qmn + qoff + rows, id_g, acc);
-                    mma_f16_ss(tmem + kColDQ, d_dsmn + rows, d_kmn + toff + rows, id_q, k > 0 ? 1u : 0u);
+                    const uint32_t acc = k == 0 ? acc0 : 1u;
+                    mma_f16_ts(tmem + kColDV, tmem + kColP + 8 * k, dv_b[k], id_g, acc);
+                    mma_f16_ss(tmem + kColDK, dk_a[k], dk_b[k], id_g, acc);
+                    mma_f16_ss(tmem + kColDQ, dq_a[k], dq_b[k], id_q, k > 0 ? 1u : 0u);
                 }
                 mma_commit(opempty);   // also: dV, dK of the tile are complete after its last chunk
                 mma_commit(&qempty[qs]);
