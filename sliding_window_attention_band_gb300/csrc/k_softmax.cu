@@ -399,6 +399,186 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const So
 }
 
 // ---------------------------------------------------------------------------
+// long rows: one CTA of kWideThreads per row (grid (position, slice)), each
+// thread holding at most NCH pieces -- the row is read once, one exp per
+// element, and the max and sum reductions go across the CTA's warps
+// through shared memory.  A warp per row would hold up to 17 pieces a lane
+// and recompute the exponentials; spread over eight warps the row stays in
+// registers.
+// ---------------------------------------------------------------------------
+constexpr int kWideThreads = 256;
+constexpr int kWideWarps = kWideThreads / 32;
+
+// max (kMax) or sum over the CTA; `red` holds kWideWarps floats
+template <bool kMax>
+__device__ __forceinline__ float block_reduce(float v, float *red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = kMax ? fmaxf(v, o) : v + o;
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < kWideWarps; ++w) r = kMax ? fmaxf(r, red[w]) : r + red[w];
+    __syncthreads();   // `red` is reused by the next reduction
+    return r;
+}
+
+// The row's keep bits drawn by the whole CTA (the warp version's table).
+__device__ __forceinline__ Keep make_keep_block(const Geom &g, int R, const Row &rw, uint32_t *words) {
+    const int i = R % g.n, bh = R / g.n, a = i / g.s;
+    const int b_lo = a - g.w + (rw.xlo - rw.lead), b_hi = a - g.w + (rw.xhi - rw.lead);
+    const int kb0 = b_lo >> 5, nkb = (b_hi >> 5) - kb0 + 1;
+    for (int k = threadIdx.x; k < nkb; k += blockDim.x) {
+        unsigned long long wv[4];
+        philox4x64_10((unsigned long long)(kb0 + k), (unsigned long long)i, (unsigned long long)bh,
+                      0, g.seed, 0, wv);
+        words[k] = keep_bits32(wv, g.drop_t);
+    }
+    __syncthreads();
+    Keep kp;
+    kp.words = words;
+    kp.off = a - g.w - rw.lead - 32 * kb0;
+    kp.scale = 256.f / (256.f - (float)g.drop_t);
+    return kp;
+}
+
+template <typename T, int NCH, bool kDrop>
+__global__ void __launch_bounds__(kWideThreads) k_softmax_wide(const SoftmaxArgs p) {
+    constexpr int N = Vec<T>::N;
+    static_assert(NCH * N <= 32, "the row's values stay in registers");
+    const Geom &g = p.g;
+    const int tid = threadIdx.x;
+    const int qi = blockIdx.x;
+    const long long R = (long long)blockIdx.y * g.n + qi;
+    const Row rw = make_row_at<T>(g, R, qi);
+    const float *brow = g.kbias ? g.kbias + (size_t)(blockIdx.y / g.h) * g.n : nullptr;
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
+    uint4 raw[NCH];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const int pc = tid + kWideThreads * k;
+        raw[k] = pc < rw.npieces ? ldg16(src + pc) : make_uint4(0, 0, 0, 0);
+    }
+    __shared__ float red[kWideWarps];
+    extern __shared__ uint32_t keep_smem[];
+    Keep kp{};
+    if constexpr (kDrop) kp = make_keep_block(g, (int)R, rw, keep_smem);
+    // scores (plus the key bias), invalid elements -inf
+    float xs[NCH * N];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        float x[N];
+        const int x0 = (tid + kWideThreads * k) * N;
+        unpack<T>(raw[k], x);
+        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
+        mask_piece<N>(x, x0, rw, -INFINITY);
+#pragma unroll
+        for (int u = 0; u < N; u += 2) m = max3(m, x[u], x[u + 1]);
+#pragma unroll
+        for (int u = 0; u < N; ++u) xs[k * N + u] = x[u];
+    }
+    m = block_reduce<true>(m, red);
+    const float mb = m * kLog2e;
+    const uint64_t l2 = f2(kLog2e, kLog2e), nb2 = f2(-mb, -mb);
+    uint64_t z2 = f2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < NCH * N; u += 2) {
+        float y0, y1;
+        f2split(fma2(f2(xs[u], xs[u + 1]), l2, nb2), y0, y1);
+        xs[u] = ex2(y0);
+        xs[u + 1] = ex2(y1);
+        z2 = add2(z2, f2(xs[u], xs[u + 1]));
+    }
+    float z0, z1;
+    f2split(z2, z0, z1);
+    const float z = block_reduce<false>(z0 + z1, red);
+    const float inv = 1.f / z;
+    const uint64_t inv2 = f2(inv, inv);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
+    uint4 *dstd = reinterpret_cast<uint4 *>(p.Pd) + rw.piece0;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const int pc = tid + kWideThreads * k;
+        if (pc >= rw.npieces) break;
+        float y[N];
+#pragma unroll
+        for (int u = 0; u < N; u += 2) f2split(mul2(f2(xs[k * N + u], xs[k * N + u + 1]), inv2), y[u], y[u + 1]);
+        if constexpr (kDrop) {
+            if (p.P) store_piece<T>(dst, pc, rw, y);
+            store_dropped<T>(dstd, pc, rw, kp, y);
+        } else {
+            store_piece<T>(dst, pc, rw, y);
+        }
+    }
+    if (p.lse && tid == 0) p.lse[R] = m + logf(z);
+}
+
+template <typename T, int NCH, bool kDrop>
+__global__ void __launch_bounds__(kWideThreads) k_softmax_bwd_wide(const SoftmaxArgs p) {
+    constexpr int N = Vec<T>::N;
+    static_assert(NCH * N <= 32, "the row's values stay in registers");
+    const Geom &g = p.g;
+    const int tid = threadIdx.x;
+    const int qi = blockIdx.x;
+    const long long R = (long long)blockIdx.y * g.n + qi;
+    const Row rw = make_row_at<T>(g, R, qi);
+    const uint4 *sp = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
+    const uint4 *sd = reinterpret_cast<const uint4 *>(p.S2) + rw.piece0;
+    uint4 rp[NCH], rd[NCH];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const int pc = tid + kWideThreads * k;
+        const bool in = pc < rw.npieces;
+        rp[k] = in ? ldg16(sp + pc) : make_uint4(0, 0, 0, 0);
+        rd[k] = in ? ldg16(sd + pc) : make_uint4(0, 0, 0, 0);
+    }
+    __shared__ float red[kWideWarps];
+    extern __shared__ uint32_t keep_smem[];
+    Keep kp{};
+    if constexpr (kDrop) kp = make_keep_block(g, (int)R, rw, keep_smem);
+    // P and the gradient reaching P (f dP with dropout), 0 on invalid elements
+    float xp[NCH * N], yd[NCH * N];
+    uint64_t d2 = f2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        float x[N], y[N];
+        const int x0 = (tid + kWideThreads * k) * N;
+        unpack<T>(rp[k], x);
+        unpack<T>(rd[k], y);
+        if constexpr (kDrop) apply_keep<N>(y, x0, rw, kp);
+        mask_piece<N>(x, x0, rw, 0.f);
+        mask_piece<N>(y, x0, rw, 0.f);
+#pragma unroll
+        for (int u = 0; u < N; u += 2) d2 = fma2(f2(x[u], x[u + 1]), f2(y[u], y[u + 1]), d2);
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            xp[k * N + u] = x[u];
+            yd[k * N + u] = y[u];
+        }
+    }
+    float d0, d1;
+    f2split(d2, d0, d1);
+    const float delta = block_reduce<false>(d0 + d1, red);
+    const uint64_t nd2 = f2(-delta, -delta);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const int pc = tid + kWideThreads * k;
+        if (pc >= rw.npieces) break;
+        float x[N];
+#pragma unroll
+        for (int u = 0; u < N; u += 2)
+            f2split(mul2(f2(xp[k * N + u], xp[k * N + u + 1]), add2(f2(yd[k * N + u], yd[k * N + u + 1]), nd2)),
+                    x[u], x[u + 1]);
+        store_piece<T>(dst, pc, rw, x);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // streaming rows (longer than the register path holds): two reads
 // ---------------------------------------------------------------------------
 template <typename T>
@@ -518,6 +698,25 @@ cudaError_t launch_sm_v(const SoftmaxArgs &a, bool bwd, cudaStream_t st) {
     const long long per_lane = (pieces + 31) / 32;
     // dropout: each warp's keep-bit table for its row
     const size_t smem = kDrop ? (size_t)kRowsPerBlock * keep_words(a.g.D) * sizeof(uint32_t) : 0;
+    // rows past four pieces a lane: a CTA per row while its pieces fit the
+    // CTA's registers (at most 32 values a thread)
+    const long long per_thread = (pieces + kWideThreads - 1) / kWideThreads;
+    if (per_lane > 4 && per_thread * N <= 32) {
+        const dim3 grw((unsigned)a.g.n, (unsigned)a.g.BH);
+        const size_t smw = kDrop ? (size_t)keep_words(a.g.D) * sizeof(uint32_t) : 0;
+        if (bwd) {
+            if (per_thread <= 1) k_softmax_bwd_wide<T, 1, kDrop><<<grw, kWideThreads, smw, st>>>(a);
+            else if (per_thread <= 2) k_softmax_bwd_wide<T, 2, kDrop><<<grw, kWideThreads, smw, st>>>(a);
+            else if (per_thread <= 4) k_softmax_bwd_wide<T, 4, kDrop><<<grw, kWideThreads, smw, st>>>(a);
+            else k_softmax_bwd_wide<T, 32 / N, kDrop><<<grw, kWideThreads, smw, st>>>(a);
+        } else {
+            if (per_thread <= 1) k_softmax_wide<T, 1, kDrop><<<grw, kWideThreads, smw, st>>>(a);
+            else if (per_thread <= 2) k_softmax_wide<T, 2, kDrop><<<grw, kWideThreads, smw, st>>>(a);
+            else if (per_thread <= 4) k_softmax_wide<T, 4, kDrop><<<grw, kWideThreads, smw, st>>>(a);
+            else k_softmax_wide<T, 32 / N, kDrop><<<grw, kWideThreads, smw, st>>>(a);
+        }
+        return cudaGetLastError();
+    }
     if (bwd) {
         if (per_lane <= 1) k_softmax_bwd_reg<T, 1, kDrop><<<grd2, blk, smem, st>>>(a);
         else if (per_lane <= 2) k_softmax_bwd_reg<T, 2, kDrop><<<grd2, blk, smem, st>>>(a);
