@@ -403,6 +403,17 @@ cudaError_t launch_scores_t(const GlobScoreArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// the dense softmax of the global rows, a warp per row
+template <typename T>
+cudaError_t launch_rows_softmax_t(const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st) {
+    const unsigned rgrid = (unsigned)(((long long)a.g.BH * a.gl.G + (kThreads / 32) - 1) / (kThreads / 32));
+    if (bwd)
+        k_glob_rows_softmax_bwd<T><<<rgrid, kThreads, 0, st>>>(a);
+    else
+        k_glob_rows_softmax<T><<<rgrid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_softmax_t(const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st) {
     const size_t smem = bitmap_bytes(a.g.n);
@@ -418,12 +429,7 @@ cudaError_t launch_softmax_t(const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const unsigned rgrid = (unsigned)(((long long)a.g.BH * a.gl.G + (kThreads / 32) - 1) / (kThreads / 32));
-    if (bwd)
-        k_glob_rows_softmax_bwd<T><<<rgrid, kThreads, 0, st>>>(a);
-    else
-        k_glob_rows_softmax<T><<<rgrid, kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_rows_softmax_t<T>(a, bwd, st);
 }
 
 template <typename T>
@@ -673,6 +679,14 @@ cudaError_t launch_glob_scores(DType dt, const GlobScoreArgs &a, cudaStream_t st
 }
 
 cudaError_t launch_softmax_glob(DType dt, const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st) {
+    bool rows_done = false;
+    cudaError_t e = cudaSuccess;
+    if (launch_softmax_glob_fast(dt, a, bwd, &rows_done, st, &e)) {
+        if (e != cudaSuccess || rows_done) return e;
+        if (dt == kF32) return launch_rows_softmax_t<float>(a, bwd, st);
+        if (dt == kF16) return launch_rows_softmax_t<__half>(a, bwd, st);
+        return launch_rows_softmax_t<__nv_bfloat16>(a, bwd, st);
+    }
     if (dt == kF32) return launch_softmax_t<float>(a, bwd, st);
     if (dt == kF16) return launch_softmax_t<__half>(a, bwd, st);
     return launch_softmax_t<__nv_bfloat16>(a, bwd, st);

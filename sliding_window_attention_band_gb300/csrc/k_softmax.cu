@@ -687,6 +687,343 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const
     }
 }
 
+// ---------------------------------------------------------------------------
+// Softmax with global tokens ("[WIP] Improve LongformerAttention performance",
+// ONNX Runtime issue, item (1)).  A local row i takes its band slots whose key
+// is in the sequence and not global, plus its G values at the global keys
+// (the cols piece [BH, n, G]); a global row's band and cols rows are zero (its
+// softmax is the dense row, [BH, G, n], done apart).  Warp per band row,
+// 16-byte pieces in registers as in the plain kernels; a piece tests its keys
+// against the global index only when its key span reaches the index's range.
+// ---------------------------------------------------------------------------
+constexpr int kColsPerLane = (kMaxGlobal + 31) / 32;
+
+template <typename T> __device__ __forceinline__ float ld(const T *p) { return Elt<T>::to_f(*p); }
+
+__device__ __forceinline__ bool is_global_pos(const GlobArgs &gl, long long j) {
+    if (j < gl.idx[0] || j > gl.idx[gl.G - 1]) return false;
+    int lo = 0, hi = gl.G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (gl.idx[mid] < j) lo = mid + 1;
+        else hi = mid;
+    }
+    return gl.idx[lo] == j;
+}
+
+// x[u] = fill where element x0 + u's key (i + (x - lead - w) s) is global
+template <int N>
+__device__ __forceinline__ void mask_global_keys(float (&x)[N], int x0, const Row &rw, int i, const Geom &g,
+                                                 const GlobArgs &gl, float fill) {
+    const long long j0 = (long long)i + (long long)(x0 - rw.lead - g.w) * g.s;
+    const long long j1 = j0 + (long long)(N - 1) * g.s;
+    if (j1 < gl.idx[0] || j0 > gl.idx[gl.G - 1]) return;
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+        if (is_global_pos(gl, j0 + (long long)u * g.s)) x[u] = fill;
+}
+
+template <typename T, int NCH>
+__global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_glob_reg(const SoftmaxGlobArgs p) {
+    constexpr int N = Vec<T>::N;
+    static_assert(NCH * N <= 32, "the row's values stay in registers");
+    const Geom &g = p.g;
+    const GlobArgs &gl = p.gl;
+    const int lane = threadIdx.x & 31;
+    const int qi = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (qi >= g.n) return;
+    const long long R = (long long)blockIdx.y * g.n + qi;
+    const Row rw = make_row_at<T>(g, R, qi);
+    const int G = gl.G;
+    uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
+    T *pcol = reinterpret_cast<T *>(p.Pcols) + R * G;
+    if (is_global_pos(gl, qi)) {
+        float zero[N];
+#pragma unroll
+        for (int u = 0; u < N; ++u) zero[u] = 0.f;
+        for (int pc = lane; pc < rw.npieces; pc += 32) store_piece<T>(dst, pc, rw, zero);
+        for (int q = lane; q < G; q += 32) pcol[q] = Elt<T>::from_f(0.f);
+        return;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
+    uint4 raw[NCH];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const int pc = lane + 32 * k;
+        raw[k] = pc < rw.npieces ? ldg16(src + pc) : make_uint4(0, 0, 0, 0);
+    }
+    const T *scol = reinterpret_cast<const T *>(p.Scols) + R * G;
+    float cv[kColsPerLane];
+#pragma unroll
+    for (int k = 0; k < kColsPerLane; ++k) {
+        const int q = lane + 32 * k;
+        cv[k] = q < G ? ld(scol + q) : -INFINITY;
+    }
+    float xs[NCH * N];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        float x[N];
+        const int x0 = (lane + 32 * k) * N;
+        unpack<T>(raw[k], x);
+        mask_piece<N>(x, x0, rw, -INFINITY);
+        mask_global_keys<N>(x, x0, rw, qi, g, gl, -INFINITY);
+#pragma unroll
+        for (int u = 0; u < N; u += 2) m = max3(m, x[u], x[u + 1]);
+#pragma unroll
+        for (int u = 0; u < N; ++u) xs[k * N + u] = x[u];
+    }
+#pragma unroll
+    for (int k = 0; k < kColsPerLane; ++k) m = fmaxf(m, cv[k]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float mb = m * kLog2e;
+    const uint64_t l2 = f2(kLog2e, kLog2e), nb2 = f2(-mb, -mb);
+    uint64_t z2 = f2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < NCH * N; u += 2) {
+        float y0, y1;
+        f2split(fma2(f2(xs[u], xs[u + 1]), l2, nb2), y0, y1);
+        xs[u] = ex2(y0);
+        xs[u + 1] = ex2(y1);
+        z2 = add2(z2, f2(xs[u], xs[u + 1]));
+    }
+    float z0, z1;
+    f2split(z2, z0, z1);
+    float z = z0 + z1;
+#pragma unroll
+    for (int k = 0; k < kColsPerLane; ++k) {
+        cv[k] = ex2(fmaf(cv[k], kLog2e, -mb));
+        z += cv[k];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    const float inv = 1.f / z;
+    const uint64_t inv2 = f2(inv, inv);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const int pc = lane + 32 * k;
+        if (pc >= rw.npieces) break;
+        float y[N];
+#pragma unroll
+        for (int u = 0; u < N; u += 2) f2split(mul2(f2(xs[k * N + u], xs[k * N + u + 1]), inv2), y[u], y[u + 1]);
+        store_piece<T>(dst, pc, rw, y);
+    }
+#pragma unroll
+    for (int k = 0; k < kColsPerLane; ++k) {
+        const int q = lane + 32 * k;
+        if (q < G) pcol[q] = Elt<T>::from_f(cv[k] * inv);
+    }
+    if (p.lse && lane == 0) p.lse[R] = m + logf(z);
+}
+
+// dS = P (dP - delta) on the used slots and dSc = Pc (dPc - delta) on the
+// cols, delta = sum over both of P dP; a global row's band and cols rows are 0
+template <typename T, int NCH>
+__global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_glob_reg(const SoftmaxGlobArgs p) {
+    constexpr int N = Vec<T>::N;
+    static_assert(NCH * N <= 32, "the row's values stay in registers");
+    const Geom &g = p.g;
+    const GlobArgs &gl = p.gl;
+    const int lane = threadIdx.x & 31;
+    const int qi = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (qi >= g.n) return;
+    const long long R = (long long)blockIdx.y * g.n + qi;
+    const Row rw = make_row_at<T>(g, R, qi);
+    const int G = gl.G;
+    uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
+    T *dscol = reinterpret_cast<T *>(p.Pcols) + R * G;
+    if (is_global_pos(gl, qi)) {
+        float zero[N];
+#pragma unroll
+        for (int u = 0; u < N; ++u) zero[u] = 0.f;
+        for (int pc = lane; pc < rw.npieces; pc += 32) store_piece<T>(dst, pc, rw, zero);
+        for (int q = lane; q < G; q += 32) dscol[q] = Elt<T>::from_f(0.f);
+        return;
+    }
+    const uint4 *sp = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
+    const uint4 *sd = reinterpret_cast<const uint4 *>(p.S2) + rw.piece0;
+    uint4 rp[NCH], rd[NCH];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const int pc = lane + 32 * k;
+        const bool in = pc < rw.npieces;
+        rp[k] = in ? ldg16(sp + pc) : make_uint4(0, 0, 0, 0);
+        rd[k] = in ? ldg16(sd + pc) : make_uint4(0, 0, 0, 0);
+    }
+    const T *pcol = reinterpret_cast<const T *>(p.Scols) + R * G;
+    const T *dpcol = reinterpret_cast<const T *>(p.S2cols) + R * G;
+    float pv[kColsPerLane], dv[kColsPerLane];
+#pragma unroll
+    for (int k = 0; k < kColsPerLane; ++k) {
+        const int q = lane + 32 * k;
+        pv[k] = q < G ? ld(pcol + q) : 0.f;
+        dv[k] = q < G ? ld(dpcol + q) : 0.f;
+    }
+    float xp[NCH * N], yd[NCH * N];
+    uint64_t d2 = f2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        float x[N], y[N];
+        const int x0 = (lane + 32 * k) * N;
+        unpack<T>(rp[k], x);
+        unpack<T>(rd[k], y);
+        mask_piece<N>(x, x0, rw, 0.f);
+        mask_piece<N>(y, x0, rw, 0.f);
+        mask_global_keys<N>(x, x0, rw, qi, g, gl, 0.f);
+        mask_global_keys<N>(y, x0, rw, qi, g, gl, 0.f);
+#pragma unroll
+        for (int u = 0; u < N; u += 2) d2 = fma2(f2(x[u], x[u + 1]), f2(y[u], y[u + 1]), d2);
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            xp[k * N + u] = x[u];
+            yd[k * N + u] = y[u];
+        }
+    }
+    float d0, d1;
+    f2split(d2, d0, d1);
+    float delta = d0 + d1;
+#pragma unroll
+    for (int k = 0; k < kColsPerLane; ++k) delta = fmaf(pv[k], dv[k], delta);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
+    const uint64_t nd2 = f2(-delta, -delta);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+        const int pc = lane + 32 * k;
+        if (pc >= rw.npieces) break;
+        float x[N];
+#pragma unroll
+        for (int u = 0; u < N; u += 2)
+            f2split(mul2(f2(xp[k * N + u], xp[k * N + u + 1]), add2(f2(yd[k * N + u], yd[k * N + u + 1]), nd2)),
+                    x[u], x[u + 1]);
+        store_piece<T>(dst, pc, rw, x);
+    }
+#pragma unroll
+    for (int k = 0; k < kColsPerLane; ++k) {
+        const int q = lane + 32 * k;
+        if (q < G) dscol[q] = Elt<T>::from_f(pv[k] * (dv[k] - delta));
+    }
+}
+
+// Dense softmax (and its backward) of the G global query rows [BH, G, n]: a
+// CTA of kWideThreads per row, 16-byte pieces (n a multiple of a piece), at
+// most NCH pieces a thread.
+template <typename T, int NCH, bool kBwd>
+__global__ void __launch_bounds__(kWideThreads) k_glob_rows_wide(const SoftmaxGlobArgs p) {
+    constexpr int N = Vec<T>::N;
+    static_assert(NCH * N <= 32, "the row's values stay in registers");
+    const Geom &g = p.g;
+    const GlobArgs &gl = p.gl;
+    const int tid = threadIdx.x;
+    const long long W = blockIdx.x;   // (slice, g)
+    const int np = g.n / N;
+    __shared__ float red[kWideWarps];
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(p.Srows) + W * np;
+    uint4 *y4 = reinterpret_cast<uint4 *>(p.Prows) + W * np;
+    float xs[NCH * N];
+    if constexpr (!kBwd) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) {
+            const int pc = tid + kWideThreads * k;
+            float x[N];
+            unpack<T>(pc < np ? ldg16(x4 + pc) : make_uint4(0, 0, 0, 0), x);
+#pragma unroll
+            for (int u = 0; u < N; ++u) {
+                xs[k * N + u] = pc < np ? x[u] : -INFINITY;
+                m = fmaxf(m, xs[k * N + u]);
+            }
+        }
+        m = block_reduce<true>(m, red);
+        const float mb = m * kLog2e;
+        float z = 0.f;
+#pragma unroll
+        for (int u = 0; u < NCH * N; ++u) {
+            xs[u] = ex2(fmaf(xs[u], kLog2e, -mb));
+            z += xs[u];
+        }
+        z = block_reduce<false>(z, red);
+        const float inv = 1.f / z;
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) {
+            const int pc = tid + kWideThreads * k;
+            if (pc >= np) break;
+            float y[N];
+#pragma unroll
+            for (int u = 0; u < N; ++u) y[u] = xs[k * N + u] * inv;
+            y4[pc] = pack<T>(y);
+        }
+        if (p.lse && tid == 0) p.lse[(W / gl.G) * g.n + gl.idx[W % gl.G]] = m + logf(z);
+    } else {
+        const uint4 *d4 = reinterpret_cast<const uint4 *>(p.S2rows) + W * np;
+        float ys[NCH * N];
+        float delta = 0.f;
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) {
+            const int pc = tid + kWideThreads * k;
+            float x[N], y[N];
+            unpack<T>(pc < np ? ldg16(x4 + pc) : make_uint4(0, 0, 0, 0), x);
+            unpack<T>(pc < np ? ldg16(d4 + pc) : make_uint4(0, 0, 0, 0), y);
+#pragma unroll
+            for (int u = 0; u < N; ++u) {
+                xs[k * N + u] = x[u];
+                ys[k * N + u] = y[u];
+                delta = fmaf(x[u], y[u], delta);
+            }
+        }
+        delta = block_reduce<false>(delta, red);
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) {
+            const int pc = tid + kWideThreads * k;
+            if (pc >= np) break;
+            float y[N];
+#pragma unroll
+            for (int u = 0; u < N; ++u) y[u] = xs[k * N + u] * (ys[k * N + u] - delta);
+            y4[pc] = pack<T>(y);
+        }
+    }
+}
+
+template <typename T>
+bool launch_glob_fast_t(const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st, cudaError_t *err,
+                        bool *rows_done) {
+    constexpr int N = Vec<T>::N;
+    const long long pieces = (a.g.D + N - 1) / N + 1;
+    const long long per_lane = (pieces + 31) / 32;
+    if (per_lane * N > 32 || a.gl.G < 1) return false;
+    const int rp = a.g.n / N;
+    const bool rows_fast = a.g.n % N == 0 && (rp + kWideThreads - 1) / kWideThreads * N <= 32;
+    const dim3 grd2((unsigned)((a.g.n + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)a.g.BH);
+    const dim3 blk(kRowsPerBlock * 32);
+    constexpr int kMaxNch = 32 / N;
+    if (bwd) {
+        if (per_lane <= 1) k_softmax_bwd_glob_reg<T, 1><<<grd2, blk, 0, st>>>(a);
+        else if (per_lane <= 2) k_softmax_bwd_glob_reg<T, 2><<<grd2, blk, 0, st>>>(a);
+        else k_softmax_bwd_glob_reg<T, kMaxNch><<<grd2, blk, 0, st>>>(a);
+    } else {
+        if (per_lane <= 1) k_softmax_glob_reg<T, 1><<<grd2, blk, 0, st>>>(a);
+        else if (per_lane <= 2) k_softmax_glob_reg<T, 2><<<grd2, blk, 0, st>>>(a);
+        else k_softmax_glob_reg<T, kMaxNch><<<grd2, blk, 0, st>>>(a);
+    }
+    *err = cudaGetLastError();
+    *rows_done = rows_fast;
+    if (*err != cudaSuccess || !rows_fast) return true;   // the dense rows: done by the caller
+    const unsigned rows = (unsigned)((long long)a.g.BH * a.gl.G);
+    const int per_thread = (rp + kWideThreads - 1) / kWideThreads;
+    if (bwd) {
+        if (per_thread <= 1) k_glob_rows_wide<T, 1, true><<<rows, kWideThreads, 0, st>>>(a);
+        else if (per_thread <= 2) k_glob_rows_wide<T, 2, true><<<rows, kWideThreads, 0, st>>>(a);
+        else k_glob_rows_wide<T, kMaxNch, true><<<rows, kWideThreads, 0, st>>>(a);
+    } else {
+        if (per_thread <= 1) k_glob_rows_wide<T, 1, false><<<rows, kWideThreads, 0, st>>>(a);
+        else if (per_thread <= 2) k_glob_rows_wide<T, 2, false><<<rows, kWideThreads, 0, st>>>(a);
+        else k_glob_rows_wide<T, kMaxNch, false><<<rows, kWideThreads, 0, st>>>(a);
+    }
+    *err = cudaGetLastError();
+    return true;
+}
+
 template <typename T, bool kDrop>
 cudaError_t launch_sm_v(const SoftmaxArgs &a, bool bwd, cudaStream_t st) {
     constexpr int N = Vec<T>::N;
@@ -754,6 +1091,14 @@ cudaError_t launch_band_softmax_bwd(DType dt, const SoftmaxArgs &a, cudaStream_t
     if (dt == kF32) return launch_sm<float>(a, true, st);
     if (dt == kF16) return launch_sm<__half>(a, true, st);
     return launch_sm<__nv_bfloat16>(a, true, st);
+}
+
+bool launch_softmax_glob_fast(DType dt, const SoftmaxGlobArgs &a, bool bwd, bool *rows_done,
+                              cudaStream_t st, cudaError_t *err) {
+    *rows_done = false;
+    if (dt == kF32) return launch_glob_fast_t<float>(a, bwd, st, err, rows_done);
+    if (dt == kF16) return launch_glob_fast_t<__half>(a, bwd, st, err, rows_done);
+    return launch_glob_fast_t<__nv_bfloat16>(a, bwd, st, err, rows_done);
 }
 
 }  // namespace swab

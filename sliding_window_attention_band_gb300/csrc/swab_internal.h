@@ -193,6 +193,12 @@ cudaError_t launch_band_t_f32(const DenseArgs &a, cudaStream_t st);
 size_t glob_bitmap_bytes(int n);
 cudaError_t launch_glob_scores(DType dt, const GlobScoreArgs &a, cudaStream_t st);
 cudaError_t launch_softmax_glob(DType dt, const SoftmaxGlobArgs &a, bool bwd, cudaStream_t st);
+// The vectorised softmax with global tokens (band rows of at most 32 values a
+// lane; the dense global rows too when n is a multiple of a 16-byte piece and
+// fits a CTA's registers).  Returns false, launching nothing, where it does
+// not apply; *rows_done tells whether it also did the dense rows.
+bool launch_softmax_glob_fast(DType dt, const SoftmaxGlobArgs &a, bool bwd, bool *rows_done,
+                              cudaStream_t st, cudaError_t *err);
 cudaError_t launch_glob_reduce(DType dt, const GlobReduceArgs &a, bool cols, cudaStream_t st);
 // the same two on the tensor cores (f16 / bf16; k_global_tc.cu): maps of A, B
 // (scores) or Y (reductions) over [BH, n, 64] with stride 1, 128- / 64-row boxes
