@@ -337,21 +337,51 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
                 const int G = p.gl.G;
                 const int t = gw * 32 + lane;
                 const T *W = reinterpret_cast<const T *>(p.gw);
-                for (int e = t; e < kBM * kKC; e += kGW * 32) {
-                    const int m = e / kKC, q = e % kKC, row = a0 + m;
-                    const long long ri = r + (long long)g.s * row;
-                    T v = Elt<T>::from_f(0.f);
-                    if (q < G && row < nr) {
-                        if (!kTrans) {
-                            if (!is_global(ri)) v = W[((long long)bh * g.n + ri) * G + q];
-                        } else {
-                            v = W[((long long)bh * G + q) * g.n + ri];
+                // 16-byte chunks of 8 K indices (band_pv) or of 8 lines' rows
+                // (band_t); a chunk is one 16-byte load where the weights are
+                // contiguous and aligned, else it is gathered element-wise
+                if (!kTrans) {
+                    for (int e = t; e < kBM * 8; e += kGW * 32) {
+                        const int m = e >> 3, c = e & 7, row = a0 + m;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (8 * c < G && row < nr) {
+                            const long long ri = r + (long long)g.s * row;
+                            if (!is_global(ri)) {
+                                const T *wp = W + ((long long)bh * g.n + ri) * G + 8 * c;
+                                if ((G & 7) == 0 && (reinterpret_cast<uintptr_t>(wp) & 15) == 0) {
+                                    v = *reinterpret_cast<const uint4 *>(wp);
+                                } else {
+                                    float f[8];
+#pragma unroll
+                                    for (int u = 0; u < 8; ++u) f[u] = 8 * c + u < G ? Elt<T>::to_f(wp[u]) : 0.f;
+                                    v = make_uint4(pack2<T>(f[0], f[1]), pack2<T>(f[2], f[3]),
+                                                   pack2<T>(f[4], f[5]), pack2<T>(f[6], f[7]));
+                                }
+                            }
                         }
+                        sts16(smem_u32(at) + m * 128 + ((c ^ (m & 7)) << 4), v);
                     }
-                    const uint32_t off = !kTrans ? (uint32_t)(m * 128 + ((((q >> 3) ^ (m & 7))) << 4) + (q & 7) * 2)
-                                                 : (uint32_t)((m >> 6) * (kKC * 128) + q * 128 +
-                                                              ((((m & 63) >> 3) ^ (q & 7)) << 4) + (m & 7) * 2);
-                    *reinterpret_cast<T *>(at + off) = v;
+                } else {
+                    for (int e = t; e < kKC * (kBM / 8); e += kGW * 32) {
+                        const int q = e >> 4, m0 = 8 * (e & 15);
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (q < G) {
+                            const T *wp = W + ((long long)bh * G + q) * g.n + r + (long long)g.s * (a0 + m0);
+                            if (g.s == 1 && a0 + m0 + 8 <= nr &&
+                                (reinterpret_cast<uintptr_t>(wp) & 15) == 0) {
+                                v = *reinterpret_cast<const uint4 *>(wp);
+                            } else {
+                                float f[8];
+#pragma unroll
+                                for (int u = 0; u < 8; ++u)
+                                    f[u] = a0 + m0 + u < nr ? Elt<T>::to_f(wp[(long long)g.s * u]) : 0.f;
+                                v = make_uint4(pack2<T>(f[0], f[1]), pack2<T>(f[2], f[3]),
+                                               pack2<T>(f[4], f[5]), pack2<T>(f[6], f[7]));
+                            }
+                        }
+                        sts16(smem_u32(at) + (m0 >> 6) * (kKC * 128) + q * 128 +
+                                  ((((m0 & 63) >> 3) ^ (q & 7)) << 4), v);
+                    }
                 }
                 const T *Y = reinterpret_cast<const T *>(p.gy) + (long long)bh * g.n * 64;
                 for (int e = t; e < kKC * 8; e += kGW * 32) {

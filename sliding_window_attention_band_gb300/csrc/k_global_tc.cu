@@ -138,19 +138,41 @@ constexpr int kATile = kRows * 128;        // 16 KB: W chunk (rows: 128 x 64 K-m
 constexpr int kBTile = kChunk * 128;       // 8 KB: Y chunk, 64 rows x 64
 constexpr int kStageBytes = kATile + kBTile;
 
+// The sequence is split over a cluster of kSplit CTAs (one slice and 128
+// global positions a cluster): each CTA sums its share of the chunks into
+// tensor memory, the partial sums meet in shared memory, and each CTA of the
+// cluster finishes 1/kSplit of the rows from every CTA's partial (read through
+// distributed shared memory).  One CTA a slice walked the whole sequence
+// alone and took 0.28 ms at b*h = 144, n = 4096.
+constexpr int kSplit = 8;
+constexpr int kPartStride = 65;   // floats a row of the partial (bank-conflict free)
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_peer_f32(const float *local, int rank) {
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
+    return v;
+}
+
 template <typename T, bool kCols>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
     k_glob_reduce_tc(const __grid_constant__ TmapSet mapY, const GlobReduceArgs p, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint32_t *bm = reinterpret_cast<uint32_t *>(base + 2 * kStageBytes);   // cols: global positions
+    float *part = reinterpret_cast<float *>(base);   // the partial sums, once the stages are idle
     __shared__ uint64_t full[2], empty[2], done;
     __shared__ uint32_t tmem_holder;
     __shared__ int abort_flag;
     const Geom &g = p.g;
     const GlobArgs &gl = p.gl;
-    const int n = g.n, G = gl.G, bh = blockIdx.x, q0 = blockIdx.y * kRows;
+    const int rank = blockIdx.x;   // rank in the cluster = share of the sequence
+    const int n = g.n, G = gl.G, bh = blockIdx.y, q0 = blockIdx.z * kRows;
     const int qn = min(kRows, G - q0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -181,18 +203,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_holder;
     const T *W = reinterpret_cast<const T *>(p.W);
     const int nch = (n + kChunk - 1) / kChunk;
+    const int cps = (nch + kSplit - 1) / kSplit;
+    const int c0 = rank * cps, c1 = min(nch, c0 + cps);
     constexpr bool kBf16 = !std::is_same<T, __half>::value;
     // A: rows mode K-major (line = global position, 64 sequence elements);
     // cols mode MN-major (line = sequence position, 64 global positions; the
     // two 64-position halves of M sit kATile / 2 apart).  B = Y rows, MN-major.
     const uint32_t idesc = idesc_f16(kRows, 64, kBf16, kCols, true);
     bool ok = true;
-    for (int c = 0; c < nch && ok; ++c) {
-        const int st = c & 1;
+    for (int c = c0; c < c1 && ok; ++c) {
+        const int lc = c - c0;
+        const int st = lc & 1;
         uint8_t *at = base + st * kStageBytes, *btile = at + kATile;
-        // the stage was last read by the products of chunk c - 2
-        if (c >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((c >> 1) - 1) & 1, &abort_flag, err)) &&
-                         ok;
+        // the stage was last read by the products of chunk lc - 2
+        if (lc >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((lc >> 1) - 1) & 1, &abort_flag, err)) &&
+                          ok;
         ok = __syncthreads_and(ok);
         if (!ok) break;
         const int j0 = c * kChunk;
@@ -200,27 +225,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&full[st], kBTile);
             tma_load_3d(btile, &mapY.m[0], &full[st], 0, j0, bh);
         }
+        // 16-byte pieces of 8 consecutive W elements: one 16-byte load where
+        // they are in range and aligned, else element by element
+        auto piece = [&](const T *src, int cnt) -> uint4 {
+            if (cnt >= 8 && (reinterpret_cast<uintptr_t>(src) & 15) == 0)
+                return *reinterpret_cast<const uint4 *>(src);
+            float f[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) f[u] = u < cnt ? Elt<T>::to_f(src[u]) : 0.f;
+            return make_uint4(pack2<T>(f[0], f[1]), pack2<T>(f[2], f[3]), pack2<T>(f[4], f[5]),
+                              pack2<T>(f[6], f[7]));
+        };
         if constexpr (!kCols) {
             // line q: W[q0 + q, j0 .. j0 + 63]
-            for (int e = threadIdx.x; e < qn * kChunk; e += kThreads) {
-                const int q = e / kChunk, jj = e % kChunk, j = j0 + jj;
-                const T v = j < n ? W[((size_t)bh * G + q0 + q) * n + j] : Elt<T>::from_f(0.f);
-                reinterpret_cast<T *>(at + sw128(q, jj >> 3))[jj & 7] = v;
+            for (int e = threadIdx.x; e < qn * (kChunk / 8); e += kThreads) {
+                const int q = e >> 3, c8 = e & 7, j = j0 + 8 * c8;
+                const uint4 v = j < n ? piece(W + ((size_t)bh * G + q0 + q) * n + j, n - j)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                sts16(smem_u32(at + sw128(q, c8)), v);
             }
         } else {
             // line jj: W[j0 + jj, q0 .. q0 + 127], zero at a global row
-            for (int e = threadIdx.x; e < kChunk * qn; e += kThreads) {
-                const int jj = e / qn, q = e % qn, j = j0 + jj;
+            const int qp = (qn + 7) / 8;
+            for (int e = threadIdx.x; e < kChunk * qp; e += kThreads) {
+                const int jj = e / qp, c8 = e % qp, j = j0 + jj, q = 8 * c8;
                 const bool use = j < n && !((bm[j >> 5] >> (j & 31)) & 1u);
-                const T v = use ? W[((size_t)bh * n + j) * G + q0 + q] : Elt<T>::from_f(0.f);
+                const uint4 v = use ? piece(W + ((size_t)bh * n + j) * G + q0 + q, qn - q)
+                                    : make_uint4(0u, 0u, 0u, 0u);
                 uint8_t *half = at + (q >> 6) * (kATile / 2);
-                reinterpret_cast<T *>(half + sw128(jj, (q & 63) >> 3))[q & 7] = v;
+                sts16(smem_u32(half + sw128(jj, (q & 63) >> 3)), v);
             }
         }
         fence_proxy_async_smem();
         __syncthreads();
         if (threadIdx.x == 0) {
-            ok = mbar_wait(&full[st], (c >> 1) & 1, &abort_flag, err);
+            ok = mbar_wait(&full[st], (lc >> 1) & 1, &abort_flag, err);
             if (ok) {
                 tc_fence_after();
                 const uint64_t da = kCols ? sdesc_sw128(smem_u32(at), kATile / 2, 1024) : sdesc_sw128(smem_u32(at), 16, 1024);
@@ -229,31 +268,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < kChunk / 16; ++k) {
                     // K step k = sequence positions 16k .. 16k + 15
                     const uint64_t ak = kCols ? da + (uint64_t)((2048 * k) >> 4) : da + 2 * k;
-                    mma_f16_ss(tmem, ak, db + (uint64_t)((2048 * k) >> 4), idesc, (c > 0 || k > 0) ? 1u : 0u);
+                    mma_f16_ss(tmem, ak, db + (uint64_t)((2048 * k) >> 4), idesc, (lc > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(&empty[st]);
-                if (c == nch - 1) mma_commit(&done);
+                if (c == c1 - 1) mma_commit(&done);
             }
         }
     }
     ok = __syncthreads_and(ok);
-    bool fin = ok && mbar_wait(&done, 0, &abort_flag, err);
+    const bool any = c1 > c0;
+    bool fin = ok && (!any || mbar_wait(&done, 0, &abort_flag, err));
     tc_fence_after();
+    // this CTA's partial sums (zero without chunks) into shared memory; the
+    // stages are idle once `done` has fired
     const int q = warp * 32 + lane;
-    if (__all_sync(0xffffffffu, fin)) {
-        for (int h = 0; h < 2; ++h) {
-            uint32_t v[32];
+    const bool have = __all_sync(0xffffffffu, fin) && any;
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        if (have) {
             tmem_ld32(tmem_addr(tmem, warp * 32, 32 * h), v);
             tmem_ld_wait();
-            if (q < qn) {
-                T *dst = reinterpret_cast<T *>(p.out) + ((size_t)bh * n + gl.idx[q0 + q]) * 64 + 32 * h;
-                for (int k = 0; k < 32; ++k) {
-                    const float x = p.alpha * __uint_as_float(v[k]);
-                    dst[k] = Elt<T>::from_f(kCols ? Elt<T>::to_f(dst[k]) + x : x);
-                }
-            }
         }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) part[q * kPartStride + 32 * h + k] = have ? __uint_as_float(v[k]) : 0.f;
     }
+    cluster_sync();
+    // rows [r0, r1) of the 128: the sum over the cluster's partials
+    const int per = (qn + kSplit - 1) / kSplit;
+    const int r0 = min(qn, rank * per), r1 = min(qn, r0 + per);
+    for (int e = threadIdx.x; e < (r1 - r0) * 64; e += kThreads) {
+        const int qq = r0 + (e >> 6), ch = e & 63;
+        const float *loc = part + qq * kPartStride + ch;
+        float acc = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < kSplit; ++rr) acc += ld_peer_f32(loc, rr);
+        T *dst = reinterpret_cast<T *>(p.out) + ((size_t)bh * n + gl.idx[q0 + qq]) * 64 + ch;
+        const float x = p.alpha * acc;
+        *dst = Elt<T>::from_f(kCols ? Elt<T>::to_f(*dst) + x : x);
+    }
+    // no CTA leaves while another still reads its partial
+    cluster_sync();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -287,7 +341,7 @@ cudaError_t launch_glob_reduce_tc(DType dt, const TmapSet &mapY, const GlobReduc
                                   cudaStream_t st) {
     if (a.gl.G < 1 || a.g.BH > 65535) return cudaErrorInvalidValue;
     const size_t smem = 2 * (size_t)kStageBytes + 1024 + (cols ? (size_t)((a.g.n + 31) / 32) * 4 : 0);
-    const dim3 grid(a.g.BH, (a.gl.G + kRows - 1) / kRows);
+    const dim3 grid(kSplit, a.g.BH, (a.gl.G + kRows - 1) / kRows);
     cudaError_t e;
 #define SWAB_LAUNCH_RED(TT, CC)                                                                              \
     e = ensure_smem(reinterpret_cast<const void *>(k_glob_reduce_tc<TT, CC>), (int)smem);                    \
