@@ -43,6 +43,12 @@ namespace {
 constexpr int kBM = 128;          // keys per chunk (MMA M)
 constexpr int kBN = 128;          // queries per tile (MMA N)
 constexpr int kStages = 2;        // key-chunk ring depth
+// A query tile's key chunks write disjoint band slots, so they can be split
+// over CTAs.  With the KEYS epilogue a CTA per chunk balances the SMs best
+// (49.8 -> 45.7 us at n = 4096, w = 256, dilation 3); the ROWS epilogue
+// keeps whole tiles (a split costs it a Q load and two partly shared pieces
+// a row a chunk: 35.5 -> 42 us).
+template <bool kRows> __host__ __device__ constexpr int chunks_per_cta() { return kRows ? (1 << 20) : 1; }
 constexpr int kThreads = 192;
 constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 halves
 constexpr int kSmemBytes = kStages * kTileBytes + kTileBytes + 1024 /*barriers*/ + 1024 /*align*/;
@@ -178,11 +184,19 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.y, bh = blockIdx.z;
     const int nr = residue_len(g.n, g.s, r);
-    const int a0 = blockIdx.x * kBN;
+    const int nsplit = p.nsplit > 0 ? p.nsplit : 1;
+    const int split = blockIdx.x % nsplit;
+    const int a0 = (blockIdx.x / nsplit) * kBN;
     if (a0 >= nr) return;  // whole CTA leaves before any barrier or allocation
-    const int kb_lo = max(a0 - g.w, 0);
+    const int kb_tile = max(a0 - g.w, 0);   // the tile's first key
     const int kb_hi = min(a0 + kBN - 1 + g.wu, nr - 1);
-    const int nck = (kb_hi - kb_lo + kBM) / kBM;
+    const int nck_tile = (kb_hi - kb_tile + kBM) / kBM;
+    constexpr int kCpc = chunks_per_cta<kRows>();
+    const int c_first = split * kCpc;
+    if (c_first >= nck_tile) return;
+    // this CTA's chunks: [c_first, c_first + nck) of the tile
+    const int kb_lo = kb_tile + c_first * kBM;
+    const int nck = min(kCpc, nck_tile - c_first);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -274,8 +288,10 @@ __global__ void __launch_bounds__(kThreads, 3)
             const int dl = (int)(e0 & 15);  // the same for every row of the CTA
             x.piece0 = (e0 - dl) / 16;
             if (qq < nr) {
-                x.ev_lo = erow + max(0, g.w - qq);
-                x.ev_hi = erow + min(g.D - 1, g.w + nr - 1 - qq);
+                // the row's valid slots among this CTA's chunks (the pieces at
+                // the ends of the range are shared with the neighbouring CTAs)
+                x.ev_lo = max(erow + max(0, g.w - qq), e0);
+                x.ev_hi = min(erow + min(g.D - 1, g.w + nr - 1 - qq), e0 + (long long)kBM * nck - 1);
             } else {
                 x.ev_lo = 1;
                 x.ev_hi = 0;
@@ -315,9 +331,9 @@ __global__ void __launch_bounds__(kThreads, 3)
             mbar_arrive(&tempty[b]);
         }
         }
-        // padding: slots whose key lies outside [0, nr)
+        // padding: slots whose key lies outside [0, nr) (the tile's first CTA)
         const T pad = Elt<T>::from_f(g.padding);
-        for (int q = warp - 2; q < kBN; q += 4) {
+        for (int q = warp - 2; split == 0 && q < kBN; q += 4) {
             const int qq = a0 + q;
             if (qq >= nr) break;
             const int t_lo = max(0, g.w - qq);
@@ -364,9 +380,15 @@ __global__ void __launch_bounds__(128) k_band_qk_f32(const DenseArgs p) {
 }
 
 template <typename T, bool kRows>
-cudaError_t launch_qk(const TmapSet &mapA, const TmapSet &mapB, const QKArgs &a, cudaStream_t st) {
-    const int tiles = (a.g.nsub + kBN - 1) / kBN;
-    dim3 grid(tiles, a.g.s, a.g.BH);
+cudaError_t launch_qk(const TmapSet &mapA, const TmapSet &mapB, const QKArgs &a0, cudaStream_t st) {
+    const int tiles = (a0.g.nsub + kBN - 1) / kBN;
+    // key chunks of a tile at most: its band spans kBN - 1 + w + w_upper keys
+    const long long max_nck = ((long long)kBN - 1 + a0.g.w + a0.g.wu + kBM) / kBM + 1;
+    QKArgs a = a0;
+    constexpr int kCpc = chunks_per_cta<kRows>();
+    a.nsplit = (int)((max_nck + kCpc - 1) / kCpc);
+    if ((long long)tiles * a.nsplit > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    dim3 grid((unsigned)(tiles * a.nsplit), a.g.s, a.g.BH);
     cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_qk_tc<T, kRows>), kSmemBytes);
     if (e != cudaSuccess) return e;
     k_band_qk_tc<T, kRows><<<grid, kThreads, kSmemBytes, st>>>(mapA, mapB, a);
