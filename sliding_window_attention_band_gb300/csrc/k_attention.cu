@@ -474,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint64_t xs2 = f2(xs_eff, xs_eff), nb2 = f2(-mb, -mb);
                 uint64_t lc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};   // partial row sums (two chains)
-                // p of each 32-key group, packed, into its 16 columns of P_b
+                // p of each 32-key group, packed, into its 16 columns of P_b;
+                // masked scores hold the value that never wins, so p is 0 there
 #pragma unroll
                 for (int gi = 0; gi < 2; ++gi) {
                     uint32_t pk[16];
@@ -489,10 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             f2split(fma2(f2(__uint_as_float(xg[2 * e]), __uint_as_float(xg[2 * e + 1])), xs2, nb2),
                                     y0, y1);
                             float p0 = ex2(y0), p1 = ex2(y1);
-                            if (!gfull[gi]) {
-                                if (!((vm[gi] >> (2 * e)) & 1u)) p0 = 0.f;
-                                if (!((vm[gi] >> (2 * e + 1)) & 1u)) p1 = 0.f;
-                            }
                             lc2[e & 1] = add2(lc2[e & 1], f2(p0, p1));   // the row sum is before dropout
                             if constexpr (kDrop) {   // dropped: 0 (kept: scaled in the epilogue)
                                 if (!((keep[gi] >> (2 * e)) & 1u)) p0 = 0.f;
