@@ -726,11 +726,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
     uint64_t *sempty = sfull + 1;      // 1, count fused::kWorkerWarps
     uint64_t *opfull = sempty + 1;     // 1, count fused::kWorkerWarps
     uint64_t *opempty = opfull + 1;    // 1 (also: dQ of that chunk is in TMEM)
-    uint64_t *dqempty = opempty + 1;   // 1, count fused::kWorkerWarps: dQ read out of TMEM
-    uint64_t *stfull = dqempty + 1;    // 1, count fused::kWorkerWarps
+    uint64_t *stfull = opempty + 1;    // 1, count fused::kWorkerWarps
     uint64_t *stempty = stfull + 1;    // 1
-    uint64_t *accempty = stempty + 1;  // 1, count fused::kWorkerWarps: dV, dK of a tile read out
-    uint64_t *mmadone = accempty + 1;  // 1
+    uint64_t *mmadone = stempty + 1;   // 1
     uint64_t *drain = mmadone + 1;     // a flag word that is never set
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -781,14 +779,12 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
         }
         mbar_init(vfull, 1);
         mbar_init(vempty, 1);
-        mbar_init(dqempty, fused::kWorkerWarps);
         mbar_init(sfull, 1);
         mbar_init(sempty, fused::kWorkerWarps);
         mbar_init(opfull, fused::kWorkerWarps);
         mbar_init(opempty, 1);
         mbar_init(stfull, fused::kWorkerWarps);
         mbar_init(stempty, 1);
-        mbar_init(accempty, fused::kWorkerWarps);
         mbar_init(mmadone, 1);
         *no_abort = 0;
         *abort_flag = 0;
@@ -900,12 +896,10 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 asm volatile("" ::"l"(dv_b[k]), "l"(dk_b[k]), "l"(dq_b[k]));
             }
             const uint32_t acc0 = first ? 0u : 1u;
-            // the softmax warps read dQ of chunk gg-1 out of TMEM in chunk gg
-            // (phase gg of dqempty), before they signal its operands
-            bool w = mbar_wait(opfull, gg & 1, abort_flag, p.err) &&
-                     mbar_wait(dqempty, gg & 1, abort_flag, p.err);
-            if (first) w = w && mbar_wait(accempty, (itt & 1) ^ 1, abort_flag, p.err);
-            if (!__all_sync(0xffffffffu, w)) return false;
+            // opfull (phase gg) also says that the softmax warps have read
+            // dQ of chunk gg-1 and, in a tile's first chunk, the previous
+            // tile's dV and dK out of TMEM: they do so before they arrive
+            if (!__all_sync(0xffffffffu, mbar_wait(opfull, gg & 1, abort_flag, p.err))) return false;
             tc_fence_after();
             if (lane == 0) {
 #pragma unroll
@@ -1102,8 +1096,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 }
             }
         };
-        // dV, dK of key row acc_row (channels [32 part, +32)) out of TMEM;
-        // the caller has waited for the tile's last products
+        // dV, dK of key row acc_row (channels [32 part, +32)) out of TMEM
+        // into dV, dK; the caller has waited for the tile's last products
         auto drain_acc = [&]() {
             uint32_t a0[16], b0[16], a1[16], b1[16];
             tmem_ld16(lane_base + kColDV + 32 * part, a0);
@@ -1111,8 +1105,6 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             tmem_ld16(lane_base + kColDV + 32 * part + 16, a1);
             tmem_ld16(lane_base + kColDK + 32 * part + 16, b1);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive_warp(accempty);
             drain16(a0, b0, 32 * part);
             drain16(a1, b1, 32 * part + 16);
         };
@@ -1319,6 +1311,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                     sts16(drow + off, make_uint4(dk[w][q], dk[w][q + 1], dk[w][q + 2], dk[w][q + 3]));
                 }
                 tmem_st_wait();
+                // the previous tile's dV, dK (in its first chunk) and dQ of
+                // chunk gc-1 out of TMEM before the operands are signalled:
+                // the next products overwrite them
                 if (acc_pend) {
                     drain_acc();
                     acc_pend = false;
@@ -1330,7 +1325,6 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
-                mbar_arrive_warp(dqempty);
                 mbar_arrive_warp(opfull);
                 if (dq_pend && !stage_dq(dqv)) {
                     ok = false;
