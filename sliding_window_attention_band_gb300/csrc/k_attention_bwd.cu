@@ -173,18 +173,30 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
     }
 }
 
-// dQ = scale * accumulator, rounded to the output type: 8 channels per thread
+// dQ = scale * accumulator, rounded to the output type: 8 channels per thread.
+// The accumulator is dead once read (the next call clears it again), so its
+// 128-byte lines are then dropped from L2 without being written back: the
+// clearing and the reduce-adds never cost DRAM writes.
 template <typename T>
 __global__ void __launch_bounds__(256) k_bwd_dq_out(const BwdArgs p) {
     pdl_wait();   // every dQ addition of the one-pass kernel has landed
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8-channel group
-    if (i >= (long long)p.g.BH * p.g.n * 8) return;
-    const float4 *acc = reinterpret_cast<const float4 *>(p.dqacc) + 2 * i;
-    const float4 a = acc[0], b = acc[1];
-    const float c = p.scale;
-    const long long off = dense_row(p.g, i >> 3, p.g.rs_p) / 8 + (i & 7);   // row i / 8, group i % 8
-    reinterpret_cast<uint4 *>(p.dQ)[off] = make_uint4(pack2<T>(c * a.x, c * a.y), pack2<T>(c * a.z, c * a.w),
-                                                    pack2<T>(c * b.x, c * b.y), pack2<T>(c * b.z, c * b.w));
+    const long long groups = (long long)p.g.BH * p.g.n * 8;
+    if (i < groups) {
+        const float4 *acc = reinterpret_cast<const float4 *>(p.dqacc) + 2 * i;
+        const float4 a = acc[0], b = acc[1];
+        const float c = p.scale;
+        const long long off = dense_row(p.g, i >> 3, p.g.rs_p) / 8 + (i & 7);   // row i / 8, group i % 8
+        reinterpret_cast<uint4 *>(p.dQ)[off] = make_uint4(pack2<T>(c * a.x, c * a.y), pack2<T>(c * a.z, c * a.w),
+                                                        pack2<T>(c * b.x, c * b.y), pack2<T>(c * b.z, c * b.w));
+    }
+    // four consecutive threads read one 128-byte line (rows are 256 bytes);
+    // their loads are complete (the values were used above) when the warp
+    // synchronises, and the first of the four drops the line
+    __syncwarp();
+    if ((reinterpret_cast<uintptr_t>(p.dqacc) & 127u) == 0 && (i & 3) == 0 && i < groups)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(reinterpret_cast<const float4 *>(p.dqacc) + 2 * i)
+                     : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -661,7 +673,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace fused {
 constexpr int kParts = 2;                       // 64 query columns per softmax warp
 constexpr int kWorkerWarps = 4 * kParts;        // 8
-constexpr int kWorkers = 32 * kWorkerWarps;     // 256
 constexpr int kReducerWarp = 2 + kWorkerWarps;  // 10
 constexpr int kThreads = 32 * (kReducerWarp + 1);
 constexpr int kQS = 2 * kTile;                  // Q and dO of a query chunk: 32 KB
