@@ -1188,7 +1188,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 // dropout: bit j of keepcol[w] = keep(query column 32 w + j of the
                 // part, this key).  Lane l draws the block of query column 32 w + l
                 // for the warp's 32 keys (one block: the warp's keys start on a
-                // multiple of 32) and 32 ballots transpose the bits to the key rows.
+                // multiple of 32) and a transpose of the warp's 32 x 32 bit
+                // matrix hands each key row its bits.
                 uint32_t keepcol[2] = {0xffffffffu, 0xffffffffu};
                 if constexpr (kDrop) {
                     if (!empty) {
@@ -1198,12 +1199,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                             philox4x64_10((unsigned long long)((tl.a0 + 32 * quarter) / 32),
                                           (unsigned long long)(tl.r + (long long)g.s * (cbase + 32 * w + lane)),
                                           (unsigned long long)tl.bh, 0, g.seed, 0, wv);
-                            const uint32_t row = keep_bits32(wv, g.drop_t);
-#pragma unroll
-                            for (int l = 0; l < 32; ++l) {
-                                const uint32_t col = __ballot_sync(0xffffffffu, (row >> l) & 1u);
-                                if (l == lane) keepcol[w] = col;
-                            }
+                            keepcol[w] = bit_transpose32(keep_bits32(wv, g.drop_t), lane);
                         }
                     }
                 }

@@ -491,6 +491,22 @@ __device__ __forceinline__ uint32_t keep_bits32(const unsigned long long (&w)[4]
     return bits;
 }
 
+// Transpose of a 32 x 32 bit matrix held by a warp, row `lane` in x (bit c =
+// column c): returns column `lane` (bit r = row r).  Five butterfly steps;
+// step j swaps, inside every 2j x 2j block, the upper right j x j block
+// with the lower left one between the lanes j apart.
+__device__ __forceinline__ uint32_t bit_transpose32(uint32_t x, int lane) {
+    constexpr uint32_t kLeft[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int j = 16 >> k;
+        const uint32_t m = kLeft[k];   // the columns c with (c & j) == 0
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+        x = (lane & j) ? ((x & ~m) | ((y & ~m) >> j)) : ((x & m) | ((y & m) << j));
+    }
+    return x;
+}
+
 // keep-and-scale factor of one element (the exact fp32 paths)
 __device__ __forceinline__ float drop_factor(const Geom &g, long long bh, long long i, long long j) {
     if (g.drop_t <= 0) return 1.f;
