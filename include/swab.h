@@ -132,6 +132,15 @@ typedef struct swab_desc {
      * take the contiguous layout only (SWAB_ERR_UNSUPPORTED). */
     int64_t qkv_row_stride;
     int64_t out_row_stride;
+    /* Optional keep-bit cache of the fused dropout (f16 / bf16 band_attention
+     * and band_attention_bwd with dropout_p > 0): DEVICE buffer of
+     * band_attention_dropout_mask_bytes(desc) bytes, 4-byte aligned; NULL for
+     * none.  band_attention writes into it the keep bits it draws (32 keys of
+     * a query row to a word); band_attention_bwd, given the buffer that
+     * band_attention filled for the same description (sizes, window, dilation,
+     * dropout_p, dropout_seed), reads them instead of drawing them again.  The
+     * decisions are the same either way.  The other calls ignore it. */
+    uint32_t *dropout_mask;
 } swab_desc;
 
 /* Companion of a band tensor when n_global > 0 (device pointers, dtype of the
@@ -299,6 +308,10 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
                                         const void *K, const void *V, const void *O,
                                         const void *dO, const float *lse, void *dQ, void *dK,
                                         void *dV, void *workspace, void *stream);
+
+/* Bytes of the keep-bit cache (swab_desc.dropout_mask) for `desc`: b*h*n rows
+ * of ceil((w + w_upper + 1) / 32) + 1 words (0 if desc is NULL). */
+SWAB_API size_t band_attention_dropout_mask_bytes(const swab_desc *desc);
 
 /* Bytes of workspace band_attention_bwd needs for `desc` (0 if desc is NULL):
  * fp16 / bf16: round_up(b*h*n*4, 256) + b*h*n*64*4, plus with global tokens

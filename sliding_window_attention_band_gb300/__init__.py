@@ -8,7 +8,7 @@ computes attention on the host.
 from ._binding import (API_FUNCTIONS, Desc, SwabError, add_bias_transpose,  # noqa: F401
                        band_attention,
                        band_attention_bwd, band_attention_bwd_noalloc,
-                       band_attention_bwd_workspace, band_pv,
+                       band_attention_bwd_workspace, band_attention_dropout_mask_bytes, band_pv,
                        band_pv_bwd_t, band_qk, band_qk_bwd_t, band_softmax, band_softmax_bwd,
                        band_softmax_dropout,
                        device_status, global_attention, global_attention_bwd,
@@ -21,6 +21,6 @@ __all__ = ["Desc", "SwabError", "add_bias_transpose", "band_qk", "band_softmax",
            "global_attention_bwd", "global_attention_workspace",
            "band_pv_bwd_t", "band_softmax_bwd", "band_attention", "band_attention_bwd",
            "band_attention_bwd_noalloc",
-           "band_attention_bwd_workspace", "device_status", "selftest_wait_timeout", "load",
+           "band_attention_bwd_workspace", "band_attention_dropout_mask_bytes", "device_status", "selftest_wait_timeout", "load",
            "library_path", "version", "status_string", "WORKLOADS", "Workload",
            "seeded_qkvo", "workload_inputs"]

@@ -28,6 +28,7 @@ API_FUNCTIONS = ("add_bias_transpose", "global_attention", "global_attention_bwd
                  "global_attention_workspace", "band_qk", "band_softmax", "band_softmax_dropout", "band_pv", "band_qk_bwd_t", "band_pv_bwd_t",
                  "band_softmax_bwd", "band_attention", "band_attention_bwd",
                  "band_attention_bwd_workspace", "band_attention_bwd_noalloc",
+                 "band_attention_dropout_mask_bytes",
                  "swab_status_string", "swab_device_status",
                  "swab_selftest_wait_timeout", "swab_version")
 
@@ -48,7 +49,7 @@ class _Desc(ctypes.Structure):
                 ("n_global", ctypes.c_int32), ("global_idx", ctypes.POINTER(ctypes.c_int32)),
                 ("key_bias", ctypes.c_void_p), ("dropout_p", ctypes.c_float),
                 ("dropout_seed", ctypes.c_uint64), ("qkv_row_stride", ctypes.c_int64),
-                ("out_row_stride", ctypes.c_int64)]
+                ("out_row_stride", ctypes.c_int64), ("dropout_mask", ctypes.c_void_p)]
 
 
 class _Glob(ctypes.Structure):
@@ -60,7 +61,7 @@ class Desc:
 
     def __init__(self, b, h, n, head_dim, w, w_upper, dilation=0, padding=0.0,
                  dtype=torch.float16, global_idx=None, key_bias=None, dropout_p=0.0,
-                 dropout_seed=0, qkv_row_stride=0, out_row_stride=0):
+                 dropout_seed=0, qkv_row_stride=0, out_row_stride=0, dropout_mask=None):
         if dtype not in _DTYPES:
             raise ValueError(f"unsupported dtype {dtype}")
         self.b, self.h, self.n, self.head_dim = int(b), int(h), int(n), int(head_dim)
@@ -80,11 +81,15 @@ class Desc:
         self.dropout_p, self.dropout_seed = float(dropout_p), int(dropout_seed)
         # strided dense layout of the fused calls: rows of [b, n, stride]
         self.qkv_row_stride, self.out_row_stride = int(qkv_row_stride), int(out_row_stride)
+        # keep-bit cache of the fused dropout: a CUDA tensor of at least
+        # band_attention_dropout_mask_bytes bytes (kept alive here), or None
+        self.dropout_mask = dropout_mask
         self.c = _Desc(self.b, self.h, self.n, self.head_dim, self.w, self.w_upper,
                        self.dilation, self.padding, _DTYPES[dtype], len(gi),
                        ctypes.cast(self._gi, ctypes.POINTER(ctypes.c_int32)) if gi else None,
                        key_bias.data_ptr() if key_bias is not None else None, self.dropout_p,
-                       self.dropout_seed, self.qkv_row_stride, self.out_row_stride)
+                       self.dropout_seed, self.qkv_row_stride, self.out_row_stride,
+                       dropout_mask.data_ptr() if dropout_mask is not None else None)
 
     @property
     def drop_t(self):
@@ -156,6 +161,8 @@ def load():
             lib.global_attention_workspace.restype = ctypes.c_size_t
             lib.band_attention_bwd_workspace.argtypes = [D]
             lib.band_attention_bwd_workspace.restype = ctypes.c_size_t
+            lib.band_attention_dropout_mask_bytes.argtypes = [D]
+            lib.band_attention_dropout_mask_bytes.restype = ctypes.c_size_t
             lib.swab_status_string.restype = ctypes.c_char_p
             lib.swab_status_string.argtypes = [ctypes.c_int]
             lib.swab_version.restype = ctypes.c_char_p
@@ -337,6 +344,11 @@ def band_attention(desc: Desc, scale, Q, K, V, O, lse=None, stream=None):
 def band_attention_bwd_workspace(desc: Desc) -> int:
     """Bytes of device workspace band_attention_bwd needs."""
     return int(load().band_attention_bwd_workspace(ctypes.byref(desc.c)))
+
+
+def band_attention_dropout_mask_bytes(desc: Desc) -> int:
+    """Bytes of the fused dropout's keep-bit cache (Desc(dropout_mask=...))."""
+    return int(load().band_attention_dropout_mask_bytes(ctypes.byref(desc.c)))
 
 
 def band_attention_bwd(desc: Desc, scale, Q, K, V, O, dO, lse, dQ, dK, dV, workspace,

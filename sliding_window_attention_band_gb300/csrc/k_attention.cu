@@ -395,6 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           (unsigned long long)(tl.r + (long long)g.s * qq),
                                           (unsigned long long)tl.bh, 0, g.seed, 0, wv);
                             keep[gi] = keep_bits32(wv, g.drop_t);
+                            if (g.dmask) {   // the keep-bit cache the backward reads
+                                const long long wi =
+                                    dmask_word(g, tl.bh, tl.r + (long long)g.s * qq, qq, (kbase + 32 * gi) / 32);
+                                if (wi >= 0) g.dmask[wi] = keep[gi];
+                            }
                         }
                     }
                 }

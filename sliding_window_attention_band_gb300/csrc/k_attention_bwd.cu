@@ -1120,19 +1120,29 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             drain16(a1, b1, 32 * part + 16);
         };
         // lse, delta of the queries cb + lane and cb + 32 + lane
-        auto load_rowstats = [&](const KTile &tl, int cb, float (&l)[2], float (&d)[2]) {
+        // (with the keep-bit cache, also the cached keep bits of those
+        // queries for the warp's 32 keys)
+        auto load_rowstats = [&](const KTile &tl, int cb, float (&l)[2], float (&d)[2], uint32_t (&km)[2]) {
 #pragma unroll
             for (int w = 0; w < 2; ++w) {
                 l[w] = 0.f;
                 d[w] = 0.f;
-                if (cb + 32 * w + lane < tl.nr) {
-                    const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * (cb + 32 * w + lane);
+                km[w] = 0u;
+                const int qs = cb + 32 * w + lane;
+                if (qs < tl.nr) {
+                    const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * qs;
                     l[w] = p.lse[row];
                     d[w] = p.delta[row];
+                    if (kDrop && g.dmask) {
+                        const long long wi =
+                            dmask_word(g, tl.bh, tl.r + (long long)g.s * qs, qs, (tl.a0 + 32 * quarter) / 32);
+                        if (wi >= 0) km[w] = __ldg(g.dmask + wi);
+                    }
                 }
             }
         };
         float lq_next[2] = {0.f, 0.f}, dq_next[2] = {0.f, 0.f};
+        uint32_t km_next[2] = {0u, 0u};
         // dQ of chunk dq_g (channels [32 part, +32) of query row m) into the
         // staging tile, once the reducer has read the previous one
         auto stage_dq = [&](const uint32_t (&dqv)[32]) -> bool {
@@ -1192,7 +1202,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 // matrix hands each key row its bits.
                 uint32_t keepcol[2] = {0xffffffffu, 0xffffffffu};
                 if constexpr (kDrop) {
-                    if (!empty) {
+                    if (!empty && !g.dmask) {
 #pragma unroll
                         for (int w = 0; w < 2; ++w) {
                             unsigned long long wv[4];
@@ -1207,15 +1217,26 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 // (the first chunk of a tile here), so that their latency is
                 // hidden behind the previous chunk
                 float lq[2], dq[2];
+                uint32_t km[2];
                 if (c == 0) {
-                    load_rowstats(tl, cbase, lq, dq);
+                    load_rowstats(tl, cbase, lq, dq, km);
                 } else {
                     lq[0] = lq_next[0];
                     lq[1] = lq_next[1];
                     dq[0] = dq_next[0];
                     dq[1] = dq_next[1];
+                    km[0] = km_next[0];
+                    km[1] = km_next[1];
                 }
-                if (c + 1 < tl.nck) load_rowstats(tl, cbase + kB, lq_next, dq_next);
+                if (c + 1 < tl.nck) load_rowstats(tl, cbase + kB, lq_next, dq_next, km_next);
+                if constexpr (kDrop) {
+                    // the cached keep bits (query column 32 w + lane's word for
+                    // the warp's keys), transposed to the key rows
+                    if (!empty && g.dmask) {
+#pragma unroll
+                        for (int w = 0; w < 2; ++w) keepcol[w] = bit_transpose32(km[w], lane);
+                    }
+                }
                 if (!__all_sync(0xffffffffu, mbar_wait(sfull, gc & 1, abort_flag, p.err))) {
                     ok = false;
                     break;

@@ -103,6 +103,10 @@ swab_status check_desc(const swab_desc *d, Geom *g, DType *dt) {
     }
     g->rs_p = d->qkv_row_stride;
     g->rs_o = d->out_row_stride;
+    // the keep-bit cache: used by the fused calls with dropout only
+    g->dmask = drop_t > 0 ? d->dropout_mask : nullptr;
+    g->dm_nb = (int)((D + 31) / 32 + 1);
+    if (g->dmask && reinterpret_cast<uintptr_t>(g->dmask) % 4 != 0) return SWAB_ERR_MISALIGNED;
     *dt = static_cast<DType>(d->dtype);
     return SWAB_OK;
 }
@@ -741,6 +745,12 @@ static BwdGlobLayout bwd_glob_layout(const swab_desc *desc, size_t start) {
     L.gp = take(global_proj_workspace_bytes((long long)BH, (int)G, (int)n));
     L.end = o;
     return L;
+}
+
+SWAB_API size_t band_attention_dropout_mask_bytes(const swab_desc *desc) {
+    if (!desc || desc->b < 1 || desc->h < 1 || desc->n < 1 || desc->w < 0 || desc->w_upper < 0) return 0;
+    const size_t D = (size_t)desc->w + desc->w_upper + 1;
+    return (size_t)desc->b * desc->h * desc->n * ((D + 31) / 32 + 1) * sizeof(uint32_t);
 }
 
 SWAB_API size_t band_attention_bwd_workspace(const swab_desc *desc) {

@@ -47,6 +47,9 @@ struct Geom {
     // 0 = contiguous [b, h, n, hd]; otherwise rows of [b, n, rs] with the heads
     // side by side (head hh at hh * hd).  rs_p: Q, K, V, dQ, dK, dV; rs_o: O, dO.
     long long rs_p, rs_o;
+    // keep-bit cache of the fused dropout, or null: dm_nb words a query row
+    uint32_t *dmask;
+    int dm_nb;
 };
 
 // Element offset of dense row R = bh * n + i under row stride rs (R < 2^31:
@@ -505,6 +508,15 @@ __device__ __forceinline__ uint32_t bit_transpose32(uint32_t x, int lane) {
         x = (lane & j) ? ((x & ~m) | ((y & ~m) >> j)) : ((x & m) | ((y & m) << j));
     }
     return x;
+}
+
+// Word of the keep-bit cache holding the keys [32 kb, 32 kb + 32) (sub-indices
+// of the row's residue) of query position i, sub-index a: the row's words
+// start at its first key block, floor(max(a - w, 0) / 32); -1 outside them.
+__host__ __device__ __forceinline__ long long dmask_word(const Geom &g, long long bh, long long i, int a, int kb) {
+    const int rel = kb - (a > g.w ? a - g.w : 0) / 32;
+    if (rel < 0 || rel >= g.dm_nb) return -1;
+    return (bh * g.n + i) * g.dm_nb + rel;
 }
 
 // keep-and-scale factor of one element (the exact fp32 paths)

@@ -367,3 +367,20 @@ def test_global_attention_validation(lib):
         UNSUPPORTED
     assert fb(ctypes.byref(d.c), 0.1, *(P(FAKE) for _ in range(5)), None,
               *(P(FAKE) for _ in range(4)), None) == INVALID   # lseg required
+
+
+def test_dropout_mask_size_and_validation(lib):
+    """The fused dropout's keep-bit cache: b*h*n rows of ceil(D / 32) + 1 words,
+    4-byte aligned when dropout is on, ignored without dropout."""
+    d = desc(dropout_p=0.1)
+    words = (d.D + 31) // 32 + 1
+    assert lib.band_attention_dropout_mask_bytes(ctypes.byref(d.c)) == d.BH * d.n * words * 4
+    assert lib.band_attention_dropout_mask_bytes(None) == 0
+    assert B.band_attention_dropout_mask_bytes(desc(w=100, w_upper=27)) == 2 * 256 * 5 * 4
+    d.c.dropout_mask = FAKE + 2
+    assert call(lib, "band_attention", d, FAKE, FAKE, FAKE, FAKE) == MISALIGNED
+    d.c.dropout_mask = FAKE
+    assert call(lib, "band_attention", d, FAKE, FAKE, FAKE, FAKE) in (OK, CUDA)
+    d0 = desc()
+    d0.c.dropout_mask = FAKE + 2   # no dropout: the cache is not used
+    assert call(lib, "band_attention", d0, FAKE, FAKE, FAKE, FAKE) in (OK, CUDA)

@@ -115,3 +115,26 @@ def test_dropout_workload():
     Q, K, V, dO = workload_inputs(wl)
     check_dropout(wl.b, wl.h, wl.n, wl.w, wl.w_upper, wl.dilation, wl.dtype, Q, K, V, dO, None,
                   0.1, 42, (0, 7))
+
+
+@pytest.mark.parametrize("case", [c for c in CASES if c[6] != torch.float32], ids=ids)
+def test_dropout_keep_bit_cache(case):
+    """With the keep-bit cache the forward stores the bits it draws and the
+    backward reads them instead of drawing them: O, lse, dK, dV are bitwise
+    those of the run without the cache (whose parity test_fused_dropout
+    checks), dQ within the rounding of its run-to-run accumulation order."""
+    b, h, n, w, wu, dil, dtype, with_bias = case
+    Q, K, V, dO = seeded_qkvo(b * h, n, 64, dtype, seed=n + 21)
+    bias = make_bias(b, n, seed=n + 22).cuda() if with_bias else None
+    kw = dict(key_bias=bias, dropout_p=0.15, dropout_seed=4242 + n)
+    plain = swab.Desc(b, h, n, 64, w, wu, dil, 0.0, dtype, **kw)
+    mask = torch.full((swab.band_attention_dropout_mask_bytes(plain) // 4,), -1, dtype=torch.int32,
+                      device="cuda")   # every bit set: the forward must write what is read
+    cached = swab.Desc(b, h, n, 64, w, wu, dil, 0.0, dtype, dropout_mask=mask, **kw)
+    r0 = run_pair(plain, Q, K, V, dO, 0.125)
+    r1 = run_pair(cached, Q, K, V, dO, 0.125)
+    for name, x0, x1 in zip(("O", "lse", "dQ", "dK", "dV"), r0, r1):
+        if name == "dQ":
+            torch.testing.assert_close(x1.float(), x0.float(), rtol=1e-2, atol=1e-3)
+        else:
+            assert torch.equal(x0, x1), name
