@@ -248,8 +248,9 @@ class FusedStep(Step):
 
 class FusedVariantStep(FusedStep):
     """The fused step with one of the optional features of the fused calls:
-    dropout of the probabilities (p = 0.1), a key-padding bias (a quarter of
-    the keys masked with -10000), or the strided layout (Q, K, V read from a
+    dropout of the probabilities (p = 0.1; also with the keep-bit cache, the
+    forward storing the keep bits for the backward), a key-padding bias (a
+    quarter of the keys masked with -10000), or the strided layout (Q, K, V read from a
     merged [b, n, 3, h, 64] projection buffer, dQ, dK, dV written into one)."""
 
     def __init__(self, wl, device, feature):
@@ -261,6 +262,13 @@ class FusedVariantStep(FusedStep):
         kw = {}
         if feature == "dropout p=0.1":
             kw = dict(dropout_p=0.1, dropout_seed=1234)
+        elif feature == "dropout p=0.1 keep-bit cache":
+            # the forward stores its keep bits, the backward reads them
+            d0 = swab.Desc(wl.b, wl.h, wl.n, wl.head_dim, wl.w, wl.w_upper, wl.dilation,
+                           wl.padding, wl.dtype, dropout_p=0.1, dropout_seed=1234)
+            self.mask = torch.empty(swab.band_attention_dropout_mask_bytes(d0) // 4,
+                                    dtype=torch.int32, device=device)
+            kw = dict(dropout_p=0.1, dropout_seed=1234, dropout_mask=self.mask)
         elif feature == "key bias":
             g = torch.Generator().manual_seed(77)
             keep = torch.rand(wl.b, wl.n, generator=g) > 0.25
@@ -836,7 +844,7 @@ def main():
         summ["forward_tflops"] = round(2 * 2.0 * wl5.head_dim * valid_pairs(wl5) / (fwd_ms * 1e-3) / 1e12, 2)
         also[f"materialised:{wl5.name}"] = summ
         del st
-        for feature in ("dropout p=0.1", "key bias", "strided qkv"):
+        for feature in ("dropout p=0.1", "dropout p=0.1 keep-bit cache", "key bias", "strided qkv"):
             st = FusedVariantStep(wl, device, feature)
             ps, pk = time_steps(st, n_also, 3, flush)
             also[f"fused+{feature.replace(' ', '_')}:{wl.name}"] = step_summary(wl, st, ps, pk, peaks)
