@@ -309,22 +309,23 @@ __global__ void __launch_bounds__(kThreads, 3)
             if (!__all_sync(0xffffffffu, ok)) break;  // keep the warp converged for tcgen05.ld
             tc_fence_after();
             const int kk = kb_lo + c * kBM + m;  // key sub-index of this lane
-            const bool key_ok = kk <= kb_hi;
-            // element offset of (query a0, this key); query q adds q*stepq
-            const long long off0 = row0 * g.D + (kk - a0 + g.w);
             const int tq0 = kk - a0 + g.w;  // slot of query a0; query q has tq0 - q
+            // the queries whose band holds this key: slot tq0 - q in [0, D),
+            // query inside its residue; none for a key past the band's end
+            const int qlo = max(tq0 - g.D + 1, 0);
+            const int qhi = kk <= kb_hi ? min(tq0, nr - 1 - a0) : -1;
+            // element (query a0, this key); query q is q*stepq further
+            T *const col = S + row0 * g.D + tq0;
 #pragma unroll 1
             for (int grp = 0; grp < 4; ++grp) {
                 uint32_t v[32];
                 tmem_ld32(tmem_addr(tmem, quarter * 32, b * kBN + grp * 32), v);
                 tmem_ld_wait();
+                T *dst = col + (long long)(grp * 32) * stepq;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < 32; ++j, dst += stepq) {
                     const int q = grp * 32 + j;
-                    const int t = tq0 - q;
-                    if (key_ok && (unsigned)t < (unsigned)g.D && a0 + q < nr) {
-                        S[off0 + (long long)q * stepq] = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
-                    }
+                    if (q >= qlo && q <= qhi) *dst = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
                 }
             }
             tc_fence_before();
