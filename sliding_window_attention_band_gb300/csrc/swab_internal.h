@@ -32,7 +32,7 @@ struct QKArgs {
     float alpha;
     void *S;          // band output [BH, n, D]
     unsigned *err;    // device status word
-    int nsplit;       // CTAs a query tile's key chunks are split over (set by the launcher)
+    int nsplit;       // CTAs a query tile's key chunks are split over, one each (set by the launcher)
 };
 
 struct GatherArgs {
