@@ -164,14 +164,25 @@ __global__ void __launch_bounds__(kThreads, 3)
             T *const col = S + row0 * g.D + tq0;
 #pragma unroll 1
             for (int grp = 0; grp < 4; ++grp) {
+                // the group's queries [32 grp, +32): none of them in any lane's
+                // range (an edge chunk) -- skip; all of them in every lane's
+                // range (the band's interior) -- store without a compare
+                const int g0 = grp * 32;
+                if (!__any_sync(0xffffffffu, qlo <= g0 + 31 && qhi >= g0)) continue;
+                const bool all_in = __all_sync(0xffffffffu, qlo <= g0 && qhi >= g0 + 31);
                 uint32_t v[32];
-                tmem_ld32(tmem_addr(tmem, quarter * 32, b * kBN + grp * 32), v);
+                tmem_ld32(tmem_addr(tmem, quarter * 32, b * kBN + g0), v);
                 tmem_ld_wait();
-                T *dst = col + (long long)(grp * 32) * stepq;
+                T *dst = col + (long long)g0 * stepq;
+                if (all_in) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j, dst += stepq) {
-                    const int q = grp * 32 + j;
-                    if (q >= qlo && q <= qhi) *dst = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
+                    for (int j = 0; j < 32; ++j, dst += stepq) *dst = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j, dst += stepq) {
+                        const int q = g0 + j;
+                        if (q >= qlo && q <= qhi) *dst = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
+                    }
                 }
             }
             tc_fence_before();
