@@ -71,8 +71,9 @@ __device__ __forceinline__ uint4 shift_extract(const uint4 &lo, const uint4 &hi)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The same with e known only at run time (uniform across the warp).
 __device__ __forceinline__ uint4 extract_elems(const uint4 &lo, const uint4 &hi, int e) {
-    switch (e) {  // e is uniform across the warp
+    switch (e) {
         case 0: return lo;
         case 1: return shift_extract<1>(lo, hi);
         case 2: return shift_extract<2>(lo, hi);
@@ -95,7 +96,9 @@ __device__ __forceinline__ uint4 mask_elems(uint4 v, int lo, int hi) {
     return make_uint4(v.x & m[0], v.y & m[1], v.z & m[2], v.w & m[3]);
 }
 
-template <typename T, bool kTrans, bool kGlob>
+// kUni: every gather warp's realignment shift is the same (s*D - 1 a
+// multiple of 8, e.g. every undilated band with D = 2^k + 1)
+template <typename T, bool kTrans, bool kGlob, bool kUni>
 __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
     k_band_gather_tc(const __grid_constant__ TmapSet mapB, const GatherArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
         long long e_line[kTasks];  // element offset of this lane's 8 elements, stage 0
         int vlo[kTasks];           // first valid element of the lane's piece, stage 0
         int vcap[kTasks];          // valid elements end at min(vlo + D, vcap - stage*64) (pv) / vcap (t)
-        int shift[kTasks];
+        int shift[kTasks];         // realignment (the same for every task: one class mod 8)
         int qline[kTasks];         // band_t: query sub-index of the lane's line at stage 0
         int kkey[kTasks];          // key sub-index of the lane's first element at stage 0
         uint32_t dst[kTasks];      // byte offset inside the A stage
@@ -266,6 +269,16 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
         }
         e_step = kTrans ? (long long)kKC * ((long long)g.s * g.D - 1) : kKC;
         bool ok = true;
+        // The realignment shift is the same for all of the warp's tasks and
+        // stages (their lines are of one class mod 8 and a stage moves a line
+        // by a multiple of 8 elements).  When it is the same for every warp
+        // too (kUni), the stage loop compiled for that shift runs; otherwise
+        // one loop realigns with the shift known at run time (E < 0), since
+        // eight loop copies in flight on one SM would crowd its instruction
+        // cache.
+        auto stage_loop = [&](auto shift_c) {
+        constexpr int E = decltype(shift_c)::value;
+
         for (int c = 0; c < nck; ++c) {
             const int st = c % kStages;
             const uint32_t ph = (c / kStages) & 1;
@@ -288,9 +301,12 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
                 lo[u] = make_uint4(0, 0, 0, 0);
                 hi[u] = make_uint4(0, 0, 0, 0);
                 if (plo[u] < phi[u]) {
-                    const uint16_t *ptr = band + (e_line[u] + e_step * c - shift[u]);
-                    if (shift[u] + plo[u] < 8) lo[u] = ldg16(ptr);
-                    if (shift[u] + phi[u] > 8) hi[u] = ldg16(ptr + 8);
+                    // (kept per task for the run-time shift: one shift test per
+                    // piece, not the whole loop copied per shift value)
+                    const int sh = E < 0 ? shift[u] : E;
+                    const uint16_t *ptr = band + (e_line[u] + e_step * c - sh);
+                    if (sh + plo[u] < 8) lo[u] = ldg16(ptr);
+                    if (sh + phi[u] > 8) hi[u] = ldg16(ptr + 8);
                 }
             }
             ok = mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err);
@@ -300,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
             for (int u = 0; u < kTasks; ++u) {
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (plo[u] < phi[u]) {
-                    v = extract_elems(lo[u], hi[u], shift[u]);
+                    if constexpr (E < 0) v = extract_elems(lo[u], hi[u], shift[u]);
+                    else v = shift_extract<E>(lo[u], hi[u]);
                     if (plo[u] > 0 || phi[u] < 8) v = mask_elems(v, plo[u], phi[u]);
                     if constexpr (kGlob) {
                         // keys of this piece that are global are not band keys
@@ -321,6 +338,19 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[st]);
+        }
+        };
+        if constexpr (!kUni) {
+            stage_loop(std::integral_constant<int, -1>{});
+        } else switch (shift[0]) {
+            case 0: stage_loop(std::integral_constant<int, 0>{}); break;
+            case 1: stage_loop(std::integral_constant<int, 1>{}); break;
+            case 2: stage_loop(std::integral_constant<int, 2>{}); break;
+            case 3: stage_loop(std::integral_constant<int, 3>{}); break;
+            case 4: stage_loop(std::integral_constant<int, 4>{}); break;
+            case 5: stage_loop(std::integral_constant<int, 5>{}); break;
+            case 6: stage_loop(std::integral_constant<int, 6>{}); break;
+            default: stage_loop(std::integral_constant<int, 7>{}); break;
         }
         if (kGlob && p.gl.G <= kGlobTc && ok) {
             // the global chunk, in the layouts of a band chunk (K = global
@@ -506,21 +536,24 @@ __global__ void __launch_bounds__(128) k_band_t_f32(const DenseArgs p) {
     reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
 }
 
-template <typename T, bool kTrans, bool kGlob>
+template <typename T, bool kTrans, bool kGlob, bool kUni>
 cudaError_t launch_gather(const TmapSet &mapB, const GatherArgs &a, cudaStream_t st) {
     const int tiles = (a.g.nsub + kBM - 1) / kBM;
     dim3 grid(tiles, a.g.s, a.g.BH);
     const size_t smem = kSmemBytes + (kGlob ? gather_glob_smem(a.g.n, a.gl.G) : 0);
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_band_gather_tc<T, kTrans, kGlob>), (int)smem);
+    cudaError_t e =
+        ensure_smem(reinterpret_cast<const void *>(k_band_gather_tc<T, kTrans, kGlob, kUni>), (int)smem);
     if (e != cudaSuccess) return e;
-    k_band_gather_tc<T, kTrans, kGlob><<<grid, kThreads, smem, st>>>(mapB, a);
+    k_band_gather_tc<T, kTrans, kGlob, kUni><<<grid, kThreads, smem, st>>>(mapB, a);
     return cudaGetLastError();
 }
 
 template <typename T, bool kTrans>
 cudaError_t launch_gather2(const TmapSet &mapB, const GatherArgs &a, cudaStream_t st) {
-    return a.gl.G > 0 ? launch_gather<T, kTrans, true>(mapB, a, st)
-                      : launch_gather<T, kTrans, false>(mapB, a, st);
+    const bool uni = ((long long)a.g.s * a.g.D - 1) % 8 == 0;
+    if (a.gl.G > 0)
+        return uni ? launch_gather<T, kTrans, true, true>(mapB, a, st) : launch_gather<T, kTrans, true, false>(mapB, a, st);
+    return uni ? launch_gather<T, kTrans, false, true>(mapB, a, st) : launch_gather<T, kTrans, false, false>(mapB, a, st);
 }
 
 }  // namespace
