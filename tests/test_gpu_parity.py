@@ -117,6 +117,7 @@ UNIT_CASES = [  # BH, n, w, w_upper, dilation, dtype
     (1, 129, 1, 2, 0, torch.bfloat16),
     (2, 200, 20, 20, 0, torch.float32),
     (1, 333, 7, 30, 2, torch.float32),
+    (2, 900, 9, 9, 2, torch.float16),     # dilated, s*D - 1 a multiple of 8: one gather shift
 ]
 
 
@@ -213,6 +214,7 @@ PROBE_CASES = [  # BH, n, w, w_upper, dilation, dtype
     (2, 1000, 64, 64, 0, torch.float16),
     (1, 4100, 256, 256, 3, torch.bfloat16),
     (1, 2049, 500, 0, 1, torch.float16),
+    (1, 1500, 5, 5, 2, torch.bfloat16),   # dilated, s*D - 1 a multiple of 8
 ]
 
 
