@@ -72,7 +72,9 @@ typedef enum swab_status {
     SWAB_ERR_UNSUPPORTED = 2, /* head_dim / dtype / size outside what is built */
     SWAB_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned */
     SWAB_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed */
-    SWAB_ERR_TIMEOUT = 5      /* a device wait gave up (see swab_device_status) */
+    SWAB_ERR_TIMEOUT = 5,     /* a device wait gave up (see swab_device_status) */
+    SWAB_ERR_BOUNDS = 6       /* bounds-checked build only: a kernel's global access
+                                 fell outside the call's buffers (swab_bounds_report) */
 } swab_status;
 
 typedef enum swab_dtype { SWAB_F32 = 0, SWAB_F16 = 1, SWAB_BF16 = 2 } swab_dtype;
@@ -368,6 +370,44 @@ SWAB_API swab_status swab_device_status(int32_t *flags, int32_t reset);
  * result with swab_device_status().  No counterpart on the pages: it tests
  * the library's own error reporting. */
 SWAB_API swab_status swab_selftest_wait_timeout(uint32_t limit_us, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Bounds-checked build.  The library also builds as libswab_bounds.so with
+ * SWAB_BOUNDS_CHECK=1: the same kernels, in which every plain global load,
+ * store and reduction first tests the bytes it touches against the extents of
+ * the call's buffers.  The host derives those extents from the descriptor and
+ * the documented shapes (dense [b, h, n, hd] or rows of [b, n, row_stride];
+ * band [b*h, n, D]; companions, lse, key bias, keep-bit cache and workspace by
+ * their sizes above), plus the library's own device arrays.  An access outside
+ * all of them is not made (a store is dropped, a load reads a scratch line):
+ * the kernel raises SWAB_ERR_BOUNDS in the device status word, records the
+ * first such access (swab_bounds_report) and runs on.  TMA copies are clipped
+ * by the hardware to their tensor map; the host checks each map's footprint
+ * against the same extents before launching and returns SWAB_ERR_BOUNDS (no
+ * launch) if one overhangs.  No counterpart on the pages: it stands in for a
+ * memory checker where none can run.  The checked build is slower; its
+ * results are the regular build's, bit for bit.
+ * ------------------------------------------------------------------------- */
+
+/* 1 in the bounds-checked build, 0 in the regular one. */
+SWAB_API int32_t swab_bounds_checked(void);
+
+/* First out-of-bounds access recorded on the current device since the last
+ * reset: out[0] = source site (file id << 16 | line) + 1, 0 if none;
+ * out[1] = its address; out[2] = its size in bytes.  Synchronises the device;
+ * reset != 0 clears the record.  Always zero in the regular build. */
+SWAB_API swab_status swab_bounds_report(uint64_t *out, int32_t reset);
+
+/* Self-test of the bounds checks (checked build only, SWAB_ERR_UNSUPPORTED
+ * otherwise): one warp stores through the check into a library-owned device
+ * array of 128 floats with an extent table that covers only its first 64.
+ * Lane l stores to element l (inside the extent) and to element 64 + l
+ * (valid memory outside it).  Synchronises `stream`; returns SWAB_OK when the
+ * stores inside landed and the ones outside did not (else SWAB_ERR_BOUNDS).
+ * The refused stores also raise SWAB_ERR_BOUNDS in the device status word and
+ * are recorded (swab_bounds_report).  Nothing outside the array is ever
+ * addressed. */
+SWAB_API swab_status swab_selftest_bounds(void *stream);
 
 /* Library version, e.g. "0.1.0". */
 SWAB_API const char *swab_version(void);

@@ -13,6 +13,7 @@ from ._binding import (API_FUNCTIONS, Desc, SwabError, add_bias_transpose,  # no
                        band_softmax_dropout,
                        device_status, global_attention, global_attention_bwd,
                        global_attention_workspace, library_path, load, selftest_wait_timeout,
+                       bounds_checked, bounds_report, selftest_bounds,
                        status_string, version)
 from .inputs import WORKLOADS, Workload, seeded_qkvo, workload_inputs  # noqa: F401
 
@@ -21,6 +22,7 @@ __all__ = ["Desc", "SwabError", "add_bias_transpose", "band_qk", "band_softmax",
            "global_attention_bwd", "global_attention_workspace",
            "band_pv_bwd_t", "band_softmax_bwd", "band_attention", "band_attention_bwd",
            "band_attention_bwd_noalloc",
-           "band_attention_bwd_workspace", "band_attention_dropout_mask_bytes", "device_status", "selftest_wait_timeout", "load",
+           "band_attention_bwd_workspace", "band_attention_dropout_mask_bytes", "device_status", "selftest_wait_timeout", "bounds_checked", "bounds_report",
+           "selftest_bounds", "load",
            "library_path", "version", "status_string", "WORKLOADS", "Workload",
            "seeded_qkvo", "workload_inputs"]

@@ -3,7 +3,8 @@
 Argument marshalling only: every computation runs in the library's CUDA
 kernels.  PyTorch supplies device memory and the current stream.  If the
 library has not been built, every call raises ``SwabError`` -- there is no
-fallback implementation.
+fallback implementation.  With SWAB_BOUNDS_CHECK=1 in the environment at the
+first call, the bounds-checked build (libswab_bounds.so) is loaded instead.
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ from . import build as _build
 
 SWAB_OK = 0
 STATUS_NAMES = ["SWAB_OK", "SWAB_ERR_INVALID_ARG", "SWAB_ERR_UNSUPPORTED",
-                "SWAB_ERR_MISALIGNED", "SWAB_ERR_CUDA", "SWAB_ERR_TIMEOUT"]
+                "SWAB_ERR_MISALIGNED", "SWAB_ERR_CUDA", "SWAB_ERR_TIMEOUT", "SWAB_ERR_BOUNDS"]
 MAX_GLOBAL = 256
 MAX_DILATION = 15
 
@@ -30,7 +31,8 @@ API_FUNCTIONS = ("add_bias_transpose", "global_attention", "global_attention_bwd
                  "band_attention_bwd_workspace", "band_attention_bwd_noalloc",
                  "band_attention_dropout_mask_bytes",
                  "swab_status_string", "swab_device_status",
-                 "swab_selftest_wait_timeout", "swab_version")
+                 "swab_selftest_wait_timeout", "swab_bounds_checked", "swab_bounds_report",
+                 "swab_selftest_bounds", "swab_version")
 
 
 class SwabError(RuntimeError):
@@ -119,7 +121,9 @@ _lock = threading.Lock()
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The library ``load()`` takes: the bounds-checked build when the
+    environment sets SWAB_BOUNDS_CHECK=1, else the regular one."""
+    return _build.LIB_BOUNDS if os.environ.get("SWAB_BOUNDS_CHECK") == "1" else _build.LIB
 
 
 def load():
@@ -127,7 +131,7 @@ def load():
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
+            path = library_path()
             if not os.path.exists(path):
                 raise SwabError("load (libswab.so not built; run "
                                 "sliding_window_attention_band_gb300.build.build())", 4)
@@ -152,6 +156,8 @@ def load():
                 "band_attention_bwd_noalloc": [D, f, P, P, P, P, P, P, P, P, P, P],
                 "swab_device_status": [ctypes.POINTER(i32), i32],
                 "swab_selftest_wait_timeout": [ctypes.c_uint32, P],
+                "swab_bounds_report": [ctypes.POINTER(ctypes.c_uint64), i32],
+                "swab_selftest_bounds": [P],
             }
             for name, args in sigs.items():
                 fn = getattr(lib, name)
@@ -166,6 +172,8 @@ def load():
             lib.swab_status_string.restype = ctypes.c_char_p
             lib.swab_status_string.argtypes = [ctypes.c_int]
             lib.swab_version.restype = ctypes.c_char_p
+            lib.swab_bounds_checked.argtypes = []
+            lib.swab_bounds_checked.restype = ctypes.c_int32
             _lib = lib
     return _lib
 
@@ -440,6 +448,29 @@ def band_attention_bwd_noalloc(desc: Desc, scale, Q, K, V, O, dO, lse, dQ, dK, d
     _call("band_attention_bwd_noalloc", ctypes.byref(desc.c), float(scale), _ptr(Q), _ptr(K),
           _ptr(V), _ptr(O), _ptr(dO), _ptr(lse), _ptr(dQ), _ptr(dK), _ptr(dV),
           _stream(stream, dQ))
+
+
+def bounds_checked() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(load().swab_bounds_checked())
+
+
+def bounds_report(reset: bool = True):
+    """The first out-of-bounds access the checked build recorded since the
+    last reset: (site, address, bytes), site = (file id << 16 | line) + 1, or
+    None when there was none."""
+    out = (ctypes.c_uint64 * 3)()
+    _call("swab_bounds_report", out, 1 if reset else 0)
+    return None if out[0] == 0 else (int(out[0]), int(out[1]), int(out[2]))
+
+
+def selftest_bounds(stream=None):
+    """Run the bounds checks' self-test (checked build); raises SwabError if
+    the checks misbehave or the build has none (SWAB_ERR_UNSUPPORTED)."""
+    s = _stream(stream, None)
+    if s is None and torch.cuda.is_available():
+        s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    _call("swab_selftest_bounds", s)
 
 
 def device_status(reset: bool = True) -> int:

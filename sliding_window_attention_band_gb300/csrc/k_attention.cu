@@ -46,6 +46,8 @@
 
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 1;   // site id of the bounds checks
+
 namespace swab {
 namespace {
 
@@ -339,12 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             w4[e] = pack2<T>(fmaf(__uint_as_float(o1[i]), g1, __uint_as_float(o0[i]) * g0),
                                              fmaf(__uint_as_float(o1[i + 1]), g1, __uint_as_float(o0[i + 1]) * g0));
                         }
-                        o4[2 * v + u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        *GP(g.bnd, &o4[2 * v + u]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
             }
             if (epi_ok) {
-                if (p.lse && half == 0) p.lse[epi_row] = M * 0.6931471805599453f + logf(L);
+                if (p.lse && half == 0) *GP(g.bnd, p.lse + epi_row) = M * 0.6931471805599453f + logf(L);
             }
             return true;
         };
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (g.dmask) {   // the keep-bit cache the backward reads
                                 const long long wi =
                                     dmask_word(g, tl.bh, tl.r + (long long)g.s * qq, qq, (kbase + 32 * gi) / 32);
-                                if (wi >= 0) g.dmask[wi] = keep[gi];
+                                if (wi >= 0) *GP(g.bnd, g.dmask + wi) = keep[gi];
                             }
                         }
                     }
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int sub = kbase + 32 * u + lane;
                         float kb = 0.f;
                         if (!gempty[u] && sub < tl.nr)
-                            kb = __ldg(g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * sub) * kLog2e;
+                            kb = __ldg(GP(g.bnd, g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * sub)) * kLog2e;
                         bslot[32 * u + lane] = kb;
                     }
                     __syncwarp();
@@ -588,13 +590,13 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
     const float *K = p.K + dense_row(g, bh * g.n, g.rs_p);   // row j of the slice: j * ks
     const float *V = p.V + dense_row(g, bh * g.n, g.rs_p);
     const long long ks = g.rs_p ? g.rs_p : g.hd;
-    const float qc = c < g.hd ? Q[c] : 0.f;
+    const float qc = c < g.hd ? *GP(g.bnd, Q + c) : 0.f;
     const int t_lo = max(0, g.w - i / g.s);
     const int t_hi = min(g.D - 1, g.w + (g.n - 1 - i) / g.s);
     float m = -INFINITY, l = 0.f, acc = 0.f;
     for (int t = t_lo; t <= t_hi; ++t) {
         const long long j = (long long)i + (long long)(t - g.w) * g.s;
-        float x = c < g.hd ? qc * K[j * ks + c] : 0.f;
+        float x = c < g.hd ? qc * *GP(g.bnd, K + j * ks + c) : 0.f;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
         if (lane == 0) part[wid] = x;
@@ -603,16 +605,16 @@ __global__ void __launch_bounds__(128) k_band_attention_f32(const AttnArgsF32 p)
         for (int k = 0; k < nw; ++k) sdot += part[k];
         __syncthreads();
         const float sc = sdot * p.scale +
-                         (g.kbias ? g.kbias[(size_t)(bh / g.h) * g.n + (size_t)j] : 0.f);
+                         (g.kbias ? *GP(g.bnd, g.kbias + (size_t)(bh / g.h) * g.n + (size_t)j) : 0.f);
         const float m_new = fmaxf(m, sc);
         const float corr = (m == -INFINITY) ? 0.f : expf(m - m_new);
         const float pv = expf(sc - m_new);
         l = l * corr + pv;   // the row sum is before dropout
-        if (c < g.hd) acc = acc * corr + pv * drop_factor(g, bh, i, j) * V[j * ks + c];
+        if (c < g.hd) acc = acc * corr + pv * drop_factor(g, bh, i, j) * *GP(g.bnd, V + j * ks + c);
         m = m_new;
     }
-    if (c < g.hd) p.O[dense_row(g, R, g.rs_o) + c] = acc / l;
-    if (c == 0 && p.lse) p.lse[R] = m + logf(l);
+    if (c < g.hd) *GP(g.bnd, p.O + dense_row(g, R, g.rs_o) + c) = acc / l;
+    if (c == 0 && p.lse) *GP(g.bnd, p.lse + R) = m + logf(l);
 }
 
 template <typename T, bool kBias, bool kDrop, bool kGlob = false>

@@ -27,6 +27,8 @@
 
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 2;   // site id of the bounds checks
+
 namespace swab {
 
 // Device scratch for band_attention_bwd_noalloc: the per-row delta that the
@@ -141,8 +143,8 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
         const long long R = warp_row0 + 4 * k + (lane >> 3);
         if (R < rows) {
             const long long off = dense_row(p.g, R, p.g.rs_o) / 8;   // 8 elements per 16 bytes
-            o[k] = ldg16(O + off + (lane & 7));
-            d[k] = ldg16(dO + off + (lane & 7));
+            o[k] = ldg16(GP(p.g.bnd, O + off + (lane & 7)));
+            d[k] = ldg16(GP(p.g.bnd, dO + off + (lane & 7)));
         } else {
             o[k] = d[k] = make_uint4(0, 0, 0, 0);
         }
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
 #pragma unroll
         for (int off = 4; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
         const long long R = warp_row0 + 4 * k + (lane >> 3);
-        if ((lane & 7) == 0 && R < rows) p.delta[R] = v;
+        if ((lane & 7) == 0 && R < rows) *GP(p.g.bnd, p.delta + R) = v;
     }
     if (p.dqacc) {
         // the one-pass backward adds dQ contributions into an fp32 accumulator:
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(256) k_bwd_delta(const BwdArgs p) {
         for (int k = 0; k < kDeltaRowsPerWarp * 16 / 32; ++k) {
             const int idx = k * 32 + lane;
             const long long R = warp_row0 + idx / 16;
-            if (R < rows) acc[R * 16 + (idx & 15)] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (R < rows) *GP(p.g.bnd, acc + R * 16 + (idx & 15)) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
 }
@@ -184,10 +186,10 @@ __global__ void __launch_bounds__(256) k_bwd_dq_out(const BwdArgs p) {
     const long long groups = (long long)p.g.BH * p.g.n * 8;
     if (i < groups) {
         const float4 *acc = reinterpret_cast<const float4 *>(p.dqacc) + 2 * i;
-        const float4 a = acc[0], b = acc[1];
+        const float4 a = *GP(p.g.bnd, acc), b = *GP(p.g.bnd, acc + 1);
         const float c = p.scale;
         const long long off = dense_row(p.g, i >> 3, p.g.rs_p) / 8 + (i & 7);   // row i / 8, group i % 8
-        reinterpret_cast<uint4 *>(p.dQ)[off] = make_uint4(pack2<T>(c * a.x, c * a.y), pack2<T>(c * a.z, c * a.w),
+        *GP(p.g.bnd, reinterpret_cast<uint4 *>(p.dQ) + off) = make_uint4(pack2<T>(c * a.x, c * a.y), pack2<T>(c * a.z, c * a.w),
                                                         pack2<T>(c * b.x, c * b.y), pack2<T>(c * b.z, c * b.w));
     }
     // four consecutive threads read one 128-byte line (rows are 256 bytes);
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(256) k_bwd_dq_out(const BwdArgs p) {
     // synchronises, and the first of the four drops the line
     __syncwarp();
     if ((reinterpret_cast<uintptr_t>(p.dqacc) & 127u) == 0 && (i & 3) == 0 && i < groups)
-        asm volatile("discard.global.L2 [%0], 128;" ::"l"(reinterpret_cast<const float4 *>(p.dqacc) + 2 * i)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(GPN(p.g.bnd, reinterpret_cast<const float4 *>(p.dqacc) + 2 * i, 128))
                      : "memory");
 }
 
@@ -338,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qi = tid & (kB - 1);
                 const int qq = qbase + qi;
                 const long long row = (long long)bh * g.n + r + (long long)g.s * qq;
-                if (tid < kB) ql[qi] = qq < nr ? p.lse[row] * kLog2e : INFINITY;
-                else ql[kB + qi] = qq < nr ? p.delta[row] : 0.f;
+                if (tid < kB) ql[qi] = qq < nr ? *GP(g.bnd, p.lse + row) * kLog2e : INFINITY;
+                else ql[kB + qi] = qq < nr ? *GP(g.bnd, p.delta + row) : 0.f;
             }
             // every worker's statistics are in (a bounded wait: a timeout
             // anywhere lets every warp leave)
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint4 *o4 = reinterpret_cast<uint4 *>(dst_row + h * 32);
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
-                            o4[u] = make_uint4(
+                            *GP(g.bnd, o4 + u) = make_uint4(
                                 pack2<T>(mul * __uint_as_float(v[8 * u]), mul * __uint_as_float(v[8 * u + 1])),
                                 pack2<T>(mul * __uint_as_float(v[8 * u + 2]), mul * __uint_as_float(v[8 * u + 3])),
                                 pack2<T>(mul * __uint_as_float(v[8 * u + 4]), mul * __uint_as_float(v[8 * u + 5])),
@@ -563,8 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l2 = INFINITY, dl = 0.f;
         const long long row = (long long)bh * g.n + r + (long long)g.s * qq;
         if (qq < nr) {
-            l2 = p.lse[row] * kLog2e;
-            dl = p.delta[row];
+            l2 = *GP(g.bnd, p.lse + row) * kLog2e;
+            dl = *GP(g.bnd, p.delta + row);
         }
         const uint32_t lane_base = tmem_addr(tmem, quarter * 32, 0);
         bool ok = true;
@@ -624,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint4 *o4 = reinterpret_cast<uint4 *>(dst_row + h * 32);
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        o4[u] = make_uint4(
+                        *GP(g.bnd, o4 + u) = make_uint4(
                             pack2<T>(mul * __uint_as_float(v[8 * u]), mul * __uint_as_float(v[8 * u + 1])),
                             pack2<T>(mul * __uint_as_float(v[8 * u + 2]), mul * __uint_as_float(v[8 * u + 3])),
                             pack2<T>(mul * __uint_as_float(v[8 * u + 4]), mul * __uint_as_float(v[8 * u + 5])),
@@ -1037,9 +1039,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int i = 4 * u;
-                        cv[u] = make_float4(__uint_as_float(a[i]), __uint_as_float(a[i + 1]),
+                        *GP(g.bnd, cv + u) = make_float4(__uint_as_float(a[i]), __uint_as_float(a[i + 1]),
                                             __uint_as_float(a[i + 2]), __uint_as_float(a[i + 3]));
-                        ck[u] = make_float4(sc * __uint_as_float(b[i]), sc * __uint_as_float(b[i + 1]),
+                        *GP(g.bnd, ck + u) = make_float4(sc * __uint_as_float(b[i]), sc * __uint_as_float(b[i + 1]),
                                             sc * __uint_as_float(b[i + 2]), sc * __uint_as_float(b[i + 3]));
                     }
                 }
@@ -1056,7 +1058,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                     float fv[16], fk[16];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const uint4 wv = gv[u], wk = gk[u];
+                        const uint4 wv = *GP(g.bnd, gv + u), wk = *GP(g.bnd, gk + u);
                         const uint32_t v32[4] = {wv.x, wv.y, wv.z, wv.w}, k32[4] = {wk.x, wk.y, wk.z, wk.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -1071,8 +1073,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                         const float *ck = p.cdK + ((size_t)acc_bh * gl.G + acc_gi) * 64 + ch0;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            fv[i] += cv[i];
-                            fk[i] += ck[i];
+                            fv[i] += *GP(g.bnd, cv + i);
+                            fk[i] += *GP(g.bnd, ck + i);
                         }
                     }
                     uint4 *v4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.dV) + goff);
@@ -1080,9 +1082,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int i = 8 * u;
-                        v4[u] = make_uint4(pack2<T>(fv[i], fv[i + 1]), pack2<T>(fv[i + 2], fv[i + 3]),
+                        *GP(g.bnd, v4 + u) = make_uint4(pack2<T>(fv[i], fv[i + 1]), pack2<T>(fv[i + 2], fv[i + 3]),
                                            pack2<T>(fv[i + 4], fv[i + 5]), pack2<T>(fv[i + 6], fv[i + 7]));
-                        k4[u] = make_uint4(pack2<T>(fk[i], fk[i + 1]), pack2<T>(fk[i + 2], fk[i + 3]),
+                        *GP(g.bnd, k4 + u) = make_uint4(pack2<T>(fk[i], fk[i + 1]), pack2<T>(fk[i + 2], fk[i + 3]),
                                            pack2<T>(fk[i + 4], fk[i + 5]), pack2<T>(fk[i + 6], fk[i + 7]));
                     }
                 }
@@ -1096,11 +1098,11 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int i = 8 * u;
-                    v4[u] = make_uint4(pack2<T>(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
+                    *GP(g.bnd, v4 + u) = make_uint4(pack2<T>(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
                                        pack2<T>(__uint_as_float(a[i + 2]), __uint_as_float(a[i + 3])),
                                        pack2<T>(__uint_as_float(a[i + 4]), __uint_as_float(a[i + 5])),
                                        pack2<T>(__uint_as_float(a[i + 6]), __uint_as_float(a[i + 7])));
-                    k4[u] = make_uint4(pack2<T>(sc * __uint_as_float(b[i]), sc * __uint_as_float(b[i + 1])),
+                    *GP(g.bnd, k4 + u) = make_uint4(pack2<T>(sc * __uint_as_float(b[i]), sc * __uint_as_float(b[i + 1])),
                                        pack2<T>(sc * __uint_as_float(b[i + 2]), sc * __uint_as_float(b[i + 3])),
                                        pack2<T>(sc * __uint_as_float(b[i + 4]), sc * __uint_as_float(b[i + 5])),
                                        pack2<T>(sc * __uint_as_float(b[i + 6]), sc * __uint_as_float(b[i + 7])));
@@ -1131,12 +1133,12 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
                 const int qs = cb + 32 * w + lane;
                 if (qs < tl.nr) {
                     const long long row = (long long)tl.bh * g.n + tl.r + (long long)g.s * qs;
-                    l[w] = p.lse[row];
-                    d[w] = p.delta[row];
+                    l[w] = *GP(g.bnd, p.lse + row);
+                    d[w] = *GP(g.bnd, p.delta + row);
                     if (kDrop && g.dmask) {
                         const long long wi =
                             dmask_word(g, tl.bh, tl.r + (long long)g.s * qs, qs, (tl.a0 + 32 * quarter) / 32);
-                        if (wi >= 0) km[w] = __ldg(g.dmask + wi);
+                        if (wi >= 0) km[w] = __ldg(GP(g.bnd, g.dmask + wi));
                     }
                 }
             }
@@ -1164,7 +1166,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             uint64_t kb2 = f2(0.f, 0.f);
             if constexpr (kBias) {
                 if (kk < tl.nr) {
-                    const float kb = __ldg(g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * kk) * kLog2e;
+                    const float kb = __ldg(GP(g.bnd, g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * kk)) * kLog2e;
                     kb2 = f2(kb, kb);
                 }
             }
@@ -1450,27 +1452,27 @@ __global__ void __launch_bounds__(128) k_bwd_f32(const BwdArgs p, int pass) {
                                       : (long long)x - (long long)(t - g.w) * g.s;
         if (y < 0 || y >= g.n) continue;
         const long long i = pass == 0 ? x : y, j = pass == 0 ? y : x;
-        const float sdot = block_dot(on ? Q[i * ps + c] * K[j * ps + c] : 0.f, part);
-        const float pdot = block_dot(on ? dO[i * os + c] * V[j * ps + c] : 0.f, part);
-        const float kb = g.kbias ? g.kbias[(size_t)(bh / g.h) * g.n + (size_t)j] : 0.f;
-        const float pr = expf(p.scale * sdot + kb - lse[i]);
+        const float sdot = block_dot(on ? *GP(g.bnd, Q + i * ps + c) * *GP(g.bnd, K + j * ps + c) : 0.f, part);
+        const float pdot = block_dot(on ? *GP(g.bnd, dO + i * os + c) * *GP(g.bnd, V + j * ps + c) : 0.f, part);
+        const float kb = g.kbias ? *GP(g.bnd, g.kbias + (size_t)(bh / g.h) * g.n + (size_t)j) : 0.f;
+        const float pr = expf(p.scale * sdot + kb - *GP(g.bnd, lse + i));
         const float f = drop_factor(g, bh, i, j);   // dropout keep-and-scale factor
-        const float ds = pr * (f * pdot - delta[i]);
+        const float ds = pr * (f * pdot - *GP(g.bnd, delta + i));
         if (!on) continue;
         if (pass == 0) {
-            acc_a = fmaf(ds, K[j * ps + c], acc_a);
+            acc_a = fmaf(ds, *GP(g.bnd, K + j * ps + c), acc_a);
         } else {
-            acc_a = fmaf(ds, Q[i * ps + c], acc_a);   // dK
-            acc_b = fmaf(pr * f, dO[i * os + c], acc_b);  // dV
+            acc_a = fmaf(ds, *GP(g.bnd, Q + i * ps + c), acc_a);   // dK
+            acc_b = fmaf(pr * f, *GP(g.bnd, dO + i * os + c), acc_b);  // dV
         }
     }
     if (!on) return;
     const long long out = dense_row(g, R, g.rs_p) + c;
     if (pass == 0) {
-        reinterpret_cast<float *>(p.dQ)[out] = p.scale * acc_a;
+        *GP(g.bnd, reinterpret_cast<float *>(p.dQ) + out) = p.scale * acc_a;
     } else {
-        reinterpret_cast<float *>(p.dK)[out] = p.scale * acc_a;
-        reinterpret_cast<float *>(p.dV)[out] = acc_b;
+        *GP(g.bnd, reinterpret_cast<float *>(p.dK) + out) = p.scale * acc_a;
+        *GP(g.bnd, reinterpret_cast<float *>(p.dV) + out) = acc_b;
     }
 }
 
@@ -1480,8 +1482,8 @@ __global__ void __launch_bounds__(128) k_bwd_delta_f32(const BwdArgs p) {
     __shared__ float part[4];
     const float *O = reinterpret_cast<const float *>(p.O) + dense_row(p.g, R, p.g.rs_o);
     const float *dO = reinterpret_cast<const float *>(p.dO) + dense_row(p.g, R, p.g.rs_o);
-    const float v = block_dot(c < p.g.hd ? O[c] * dO[c] : 0.f, part);
-    if (c == 0) p.delta[R] = v;
+    const float v = block_dot(c < p.g.hd ? *GP(p.g.bnd, O + c) * *GP(p.g.bnd, dO + c) : 0.f, part);
+    if (c == 0) *GP(p.g.bnd, p.delta + R) = v;
 }
 
 template <typename T>
@@ -1564,22 +1566,23 @@ __global__ void __launch_bounds__(256) k_glob_gather(const BwdArgs p, const __gr
         uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
         if (row < G) {
             const size_t src = ((size_t)bh * n + gl.idx[row]) * 8 + c;
-            kv = K4[src];
-            vv = V4[src];
+            kv = *GP(p.g.bnd, K4 + src);
+            vv = *GP(p.g.bnd, V4 + src);
         }
-        KG4[((size_t)bh * grows + row) * 8 + c] = kv;
-        VG4[((size_t)bh * grows + row) * 8 + c] = vv;
+        *GP(p.g.bnd, KG4 + ((size_t)bh * grows + row) * 8 + c) = kv;
+        *GP(p.g.bnd, VG4 + ((size_t)bh * grows + row) * 8 + c) = vv;
     }
     uint4 *Qg4 = reinterpret_cast<uint4 *>(gb.Qg), *Og4 = reinterpret_cast<uint4 *>(gb.Og);
     uint4 *dOg4 = reinterpret_cast<uint4 *>(gb.dOg);
     for (int i = threadIdx.x; i < G * 8; i += blockDim.x) {
         const int row = i >> 3, c = i & 7;
         const size_t src = ((size_t)bh * n + gl.idx[row]) * 8 + c, dst = ((size_t)bh * G + row) * 8 + c;
-        Qg4[dst] = Q4[src];
-        Og4[dst] = O4[src];
-        dOg4[dst] = dO4[src];
+        *GP(p.g.bnd, Qg4 + dst) = *GP(p.g.bnd, Q4 + src);
+        *GP(p.g.bnd, Og4 + dst) = *GP(p.g.bnd, O4 + src);
+        *GP(p.g.bnd, dOg4 + dst) = *GP(p.g.bnd, dO4 + src);
     }
-    for (int k = threadIdx.x; k < G; k += blockDim.x) gb.lseg[bh * G + k] = p.lse[bh * n + gl.idx[k]];
+    for (int k = threadIdx.x; k < G; k += blockDim.x)
+        *GP(p.g.bnd, gb.lseg + bh * G + k) = *GP(p.g.bnd, p.lse + bh * n + gl.idx[k]);
 }
 
 // the global rows' dQ (computed by the global-query backward) into dQ
@@ -1590,7 +1593,7 @@ __global__ void __launch_bounds__(256) k_glob_dq_rows(const BwdArgs p, const __g
     uint4 *dst = reinterpret_cast<uint4 *>(p.dQ);
     for (int i = threadIdx.x; i < gl.G * 8; i += blockDim.x) {
         const int row = i >> 3, c = i & 7;
-        dst[((size_t)bh * p.g.n + gl.idx[row]) * 8 + c] = src[((size_t)bh * gl.G + row) * 8 + c];
+        *GP(p.g.bnd, dst + ((size_t)bh * p.g.n + gl.idx[row]) * 8 + c) = *GP(p.g.bnd, src + ((size_t)bh * gl.G + row) * 8 + c);
     }
 }
 

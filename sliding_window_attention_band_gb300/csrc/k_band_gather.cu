@@ -32,6 +32,8 @@
 
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 4;   // site id of the bounds checks
+
 namespace swab {
 namespace {
 
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
         if (p.gl.G > kGlobTc) {   // the FFMA epilogue's global rows of Y
             const T *ysrc = reinterpret_cast<const T *>(p.gy) + (long long)bh * g.n * 64;
             for (int e = threadIdx.x; e < p.gl.G * 64; e += blockDim.x)
-                gyrows[e] = Elt<T>::to_f(ysrc[(long long)p.gl.idx[e >> 6] * 64 + (e & 63)]);
+                gyrows[e] = Elt<T>::to_f(*GP(g.bnd, ysrc + (long long)p.gl.idx[e >> 6] * 64 + (e & 63)));
         }
     }
     tc_fence_before();
@@ -305,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
                     // piece, not the whole loop copied per shift value)
                     const int sh = E < 0 ? shift[u] : E;
                     const uint16_t *ptr = band + (e_line[u] + e_step * c - sh);
-                    if (sh + plo[u] < 8) lo[u] = ldg16(ptr);
-                    if (sh + phi[u] > 8) hi[u] = ldg16(ptr + 8);
+                    if (sh + plo[u] < 8) lo[u] = ldg16(GPN(g.bnd, ptr, 16));
+                    if (sh + phi[u] > 8) hi[u] = ldg16(GPN(g.bnd, ptr + 8, 16));
                 }
             }
             ok = mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err);
@@ -379,11 +381,11 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
                             if (!is_global(ri)) {
                                 const T *wp = W + ((long long)bh * g.n + ri) * G + 8 * c;
                                 if ((G & 7) == 0 && (reinterpret_cast<uintptr_t>(wp) & 15) == 0) {
-                                    v = *reinterpret_cast<const uint4 *>(wp);
+                                    v = *GP(g.bnd, reinterpret_cast<const uint4 *>(wp));
                                 } else {
                                     float f[8];
 #pragma unroll
-                                    for (int u = 0; u < 8; ++u) f[u] = 8 * c + u < G ? Elt<T>::to_f(wp[u]) : 0.f;
+                                    for (int u = 0; u < 8; ++u) f[u] = 8 * c + u < G ? Elt<T>::to_f(*GP(g.bnd, wp + u)) : 0.f;
                                     v = make_uint4(pack2<T>(f[0], f[1]), pack2<T>(f[2], f[3]),
                                                    pack2<T>(f[4], f[5]), pack2<T>(f[6], f[7]));
                                 }
@@ -399,12 +401,12 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
                             const T *wp = W + ((long long)bh * G + q) * g.n + r + (long long)g.s * (a0 + m0);
                             if (g.s == 1 && a0 + m0 + 8 <= nr &&
                                 (reinterpret_cast<uintptr_t>(wp) & 15) == 0) {
-                                v = *reinterpret_cast<const uint4 *>(wp);
+                                v = *GP(g.bnd, reinterpret_cast<const uint4 *>(wp));
                             } else {
                                 float f[8];
 #pragma unroll
                                 for (int u = 0; u < 8; ++u)
-                                    f[u] = a0 + m0 + u < nr ? Elt<T>::to_f(wp[(long long)g.s * u]) : 0.f;
+                                    f[u] = a0 + m0 + u < nr ? Elt<T>::to_f(*GP(g.bnd, wp + (long long)g.s * u)) : 0.f;
                                 v = make_uint4(pack2<T>(f[0], f[1]), pack2<T>(f[2], f[3]),
                                                pack2<T>(f[4], f[5]), pack2<T>(f[6], f[7]));
                             }
@@ -454,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
                     for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]);
                     for (int q = 0; q < p.gl.G; ++q) {
                         const float wv = kTrans
-                            ? Elt<T>::to_f(gw[((long long)bh * p.gl.G + q) * g.n + ri])
-                            : Elt<T>::to_f(gw[((long long)bh * g.n + ri) * p.gl.G + q]);
+                            ? Elt<T>::to_f(*GP(g.bnd, gw + ((long long)bh * p.gl.G + q) * g.n + ri))
+                            : Elt<T>::to_f(*GP(g.bnd, gw + ((long long)bh * g.n + ri) * p.gl.G + q));
                         const float *yr = gyrows + q * 64 + half * 32;
 #pragma unroll
                         for (int i = 0; i < 32; ++i) acc[i] = fmaf(wv, yr[i], acc[i]);
@@ -479,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, kGlob ? 2 : 3)
                     w.y = pack2<T>(p.alpha * __uint_as_float(v[8 * q + 2]), p.alpha * __uint_as_float(v[8 * q + 3]));
                     w.z = pack2<T>(p.alpha * __uint_as_float(v[8 * q + 4]), p.alpha * __uint_as_float(v[8 * q + 5]));
                     w.w = pack2<T>(p.alpha * __uint_as_float(v[8 * q + 6]), p.alpha * __uint_as_float(v[8 * q + 7]));
-                    o4[q] = w;
+                    *GP(g.bnd, o4 + q) = w;
                 }
             }
         }
@@ -511,9 +513,9 @@ __global__ void __launch_bounds__(128) k_band_pv_f32(const DenseArgs p) {
     float acc = 0.f;
     for (int t = t_lo; t <= t_hi; ++t) {
         const long long j = (long long)i + (long long)(t - g.w) * g.s;
-        acc = fmaf(P[t], V[j * g.hd + c], acc);
+        acc = fmaf(*GP(g.bnd, P + t), *GP(g.bnd, V + j * g.hd + c), acc);
     }
-    reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
+    *GP(g.bnd, reinterpret_cast<float *>(p.out) + R * g.hd + c) = p.alpha * acc;
 }
 
 // band_t: one CTA per output row j (a key), one thread per channel; the
@@ -531,9 +533,9 @@ __global__ void __launch_bounds__(128) k_band_t_f32(const DenseArgs p) {
     for (int t = 0; t < g.D; ++t) {
         const long long i = (long long)j - (long long)(t - g.w) * g.s;
         if (i < 0 || i >= g.n) continue;
-        acc = fmaf(Bd[i * g.D + t], Y[i * g.hd + c], acc);
+        acc = fmaf(*GP(g.bnd, Bd + i * g.D + t), *GP(g.bnd, Y + i * g.hd + c), acc);
     }
-    reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
+    *GP(g.bnd, reinterpret_cast<float *>(p.out) + R * g.hd + c) = p.alpha * acc;
 }
 
 template <typename T, bool kTrans, bool kGlob, bool kUni>

@@ -27,6 +27,8 @@
 
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 3;   // site id of the bounds checks
+
 namespace swab {
 namespace {
 
@@ -176,12 +178,12 @@ __global__ void __launch_bounds__(kThreads, 3)
                 T *dst = col + (long long)g0 * stepq;
                 if (all_in) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j, dst += stepq) *dst = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
+                    for (int j = 0; j < 32; ++j, dst += stepq) *GP(g.bnd, dst) = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j, dst += stepq) {
                         const int q = g0 + j;
-                        if (q >= qlo && q <= qhi) *dst = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
+                        if (q >= qlo && q <= qhi) *GP(g.bnd, dst) = Elt<T>::from_f(alpha * __uint_as_float(v[j]));
                     }
                 }
             }
@@ -196,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 3)
             const int t_lo = max(0, g.w - qq);
             const int t_hi = min(g.D - 1, g.w + nr - 1 - qq);
             T *row = S + ((long long)bh * g.n + r + (long long)g.s * qq) * g.D;
-            for (int t = lane; t < t_lo; t += 32) row[t] = pad;
-            for (int t = t_hi + 1 + lane; t < g.D; t += 32) row[t] = pad;
+            for (int t = lane; t < t_lo; t += 32) *GP(g.bnd, row + t) = pad;
+            for (int t = t_hi + 1 + lane; t < g.D; t += 32) *GP(g.bnd, row + t) = pad;
         }
     }
     tc_fence_before();
@@ -220,18 +222,18 @@ __global__ void __launch_bounds__(128) k_band_qk_f32(const DenseArgs p) {
     __shared__ float arow[128];
     const float *A = reinterpret_cast<const float *>(p.A) + R * g.hd;
     const float *B = reinterpret_cast<const float *>(p.B) + bh * g.n * g.hd;
-    for (int c = threadIdx.x; c < g.hd; c += blockDim.x) arow[c] = A[c];
+    for (int c = threadIdx.x; c < g.hd; c += blockDim.x) arow[c] = *GP(g.bnd, A + c);
     __syncthreads();
     float *S = reinterpret_cast<float *>(p.out) + R * g.D;
     for (int t = threadIdx.x; t < g.D; t += blockDim.x) {
         const long long j = (long long)i + (long long)(t - g.w) * g.s;
         if (j < 0 || j >= g.n) {
-            S[t] = g.padding;
+            *GP(g.bnd, S + t) = g.padding;
         } else {
             const float *b = B + j * g.hd;
             float acc = 0.f;
-            for (int c = 0; c < g.hd; ++c) acc = fmaf(arow[c], b[c], acc);
-            S[t] = p.alpha * acc;
+            for (int c = 0; c < g.hd; ++c) acc = fmaf(arow[c], *GP(g.bnd, b + c), acc);
+            *GP(g.bnd, S + t) = p.alpha * acc;
         }
     }
 }

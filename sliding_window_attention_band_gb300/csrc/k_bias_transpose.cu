@@ -13,6 +13,8 @@
 // HBM-bound: 2 * b*n*M*h*hd * size bytes (plus the bias, L2-resident).
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 5;   // site id of the bounds checks
+
 namespace swab {
 namespace {
 
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(256) k_add_bias_transpose(const BiasTransposeA
     const unsigned cc = q % (unsigned)p.cpr, mh = q / (unsigned)p.cpr;
     const unsigned hh = mh % (unsigned)p.h, m = mh / (unsigned)p.h;
     uint4 bv = make_uint4(0, 0, 0, 0);
-    if (p.bias) bv = ldg16(reinterpret_cast<const uint4 *>(p.bias) + q);   // bias is [M, h, cpr]
+    if (p.bias) bv = ldg16(GP(p.bnd, reinterpret_cast<const uint4 *>(p.bias) + q));   // bias is [M, h, cpr]
     // Y chunk of (m, bb, hh, i, cc): ((m * b + bb) * h + hh) * n + i, times cpr, plus cc
     const long long ybase = (((long long)m * p.b * p.h + hh) * p.n) * p.cpr + cc;
     const uint4 *X = reinterpret_cast<const uint4 *>(p.X);
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(256) k_add_bias_transpose(const BiasTransposeA
 #pragma unroll
         for (int k = 0; k < kRowsPerThread; ++k) {
             const long long row = row0 + k;
-            v[k] = row < p.rows ? ldg16(X + row * chunks_per_row + q) : make_uint4(0, 0, 0, 0);
+            v[k] = row < p.rows ? ldg16(GP(p.bnd, X + row * chunks_per_row + q)) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int k = 0; k < kRowsPerThread; ++k) {
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(256) k_add_bias_transpose(const BiasTransposeA
             if (row >= p.rows) break;
             const unsigned bb = (unsigned)row / (unsigned)p.n, i = (unsigned)row - bb * (unsigned)p.n;
             const uint4 y = p.bias ? add_chunk<T>(v[k], bv) : v[k];
-            Y[ybase + ((long long)bb * p.h * p.n + i) * p.cpr] = y;
+            *GP(p.bnd, Y + ybase + ((long long)bb * p.h * p.n + i) * p.cpr) = y;
         }
     }
 }

@@ -14,6 +14,8 @@
 
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 7;   // site id of the bounds checks
+
 namespace swab {
 namespace {
 
@@ -32,20 +34,20 @@ template <typename T> __device__ __forceinline__ float ld(const T *p) { return E
 
 // rows [row0, row0 + 64) of a [n, 64] slice into smem as fp32 (zero past n)
 template <typename T>
-__device__ __forceinline__ void load_tile(float *dst, const T *slice, int row0, int n) {
+__device__ __forceinline__ void load_tile(const Geom &g, float *dst, const T *slice, int row0, int n) {
     for (int e = threadIdx.x; e < kTile * 64; e += blockDim.x) {
         const int rr = e >> 6, c = e & 63;
         const int row = row0 + rr;
-        dst[rr * kPad + c] = row < n ? ld(slice + (long long)row * 64 + c) : 0.f;
+        dst[rr * kPad + c] = row < n ? ld(GP(g.bnd, slice + (long long)row * 64 + c)) : 0.f;
     }
 }
 
 // the G global rows of a [n, 64] slice into smem as fp32
 template <typename T>
-__device__ __forceinline__ void load_global_rows(float *dst, const T *slice, const GlobArgs &gl) {
+__device__ __forceinline__ void load_global_rows(const Geom &g, float *dst, const T *slice, const GlobArgs &gl) {
     for (int e = threadIdx.x; e < gl.G * 64; e += blockDim.x) {
         const int gg = e >> 6, c = e & 63;
-        dst[gg * kPad + c] = ld(slice + (long long)gl.idx[gg] * 64 + c);
+        dst[gg * kPad + c] = ld(GP(g.bnd, slice + (long long)gl.idx[gg] * 64 + c));
     }
 }
 
@@ -66,10 +68,10 @@ __global__ void __launch_bounds__(kThreads) k_glob_scores(const GlobScoreArgs p)
     float *b_g = a_g + G * kPad;            // B[G]
     const T *A = reinterpret_cast<const T *>(p.A) + (long long)bh * n * 64;
     const T *B = reinterpret_cast<const T *>(p.B) + (long long)bh * n * 64;
-    load_tile(a_t, A, i0, n);
-    load_tile(b_t, B, i0, n);
-    load_global_rows(a_g, A, gl);
-    load_global_rows(b_g, B, gl);
+    load_tile(p.g, a_t, A, i0, n);
+    load_tile(p.g, b_t, B, i0, n);
+    load_global_rows(p.g, a_g, A, gl);
+    load_global_rows(p.g, b_g, B, gl);
     __syncthreads();
     T *cols = reinterpret_cast<T *>(p.cols) + (long long)bh * n * G;
     T *rows = reinterpret_cast<T *>(p.rows) + (long long)bh * G * n;
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(kThreads) k_glob_scores(const GlobScoreArgs p)
         float acc = 0.f;
 #pragma unroll 16
         for (int c = 0; c < 64; ++c) acc = fmaf(x[c], y[c], acc);
-        cols[(long long)(i0 + ii) * G + g] = Elt<T>::from_f(p.alpha * acc);
+        *GP(p.g.bnd, cols + (long long)(i0 + ii) * G + g) = Elt<T>::from_f(p.alpha * acc);
     }
     for (int o = threadIdx.x; o < kTile * G; o += blockDim.x) {
         const int jj = o % kTile, g = o / kTile;
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) k_glob_scores(const GlobScoreArgs p)
         float acc = 0.f;
 #pragma unroll 16
         for (int c = 0; c < 64; ++c) acc = fmaf(x[c], y[c], acc);
-        rows[(long long)g * n + i0 + jj] = Elt<T>::from_f(p.alpha * acc);
+        *GP(p.g.bnd, rows + (long long)g * n + i0 + jj) = Elt<T>::from_f(p.alpha * acc);
     }
 }
 
@@ -143,8 +145,8 @@ __global__ void __launch_bounds__(kThreads) k_softmax_glob(const SoftmaxGlobArgs
         const T *sc = reinterpret_cast<const T *>(p.Scols) + (long long)R * G;
         T *pc = reinterpret_cast<T *>(p.Pcols) + (long long)R * G;
         if (in_bitmap(bm, i)) {
-            for (int t = lane; t < g.D; t += 32) prow[t] = Elt<T>::from_f(0.f);
-            for (int q = lane; q < G; q += 32) pc[q] = Elt<T>::from_f(0.f);
+            for (int t = lane; t < g.D; t += 32) *GP(p.g.bnd, prow + t) = Elt<T>::from_f(0.f);
+            for (int q = lane; q < G; q += 32) *GP(p.g.bnd, pc + q) = Elt<T>::from_f(0.f);
             continue;
         }
         auto used = [&](int t) {
@@ -153,23 +155,23 @@ __global__ void __launch_bounds__(kThreads) k_softmax_glob(const SoftmaxGlobArgs
         };
         float m = -INFINITY;
         for (int t = lane; t < g.D; t += 32)
-            if (used(t)) m = fmaxf(m, ld(srow + t));
-        for (int q = lane; q < G; q += 32) m = fmaxf(m, ld(sc + q));
+            if (used(t)) m = fmaxf(m, ld(GP(p.g.bnd, srow + t)));
+        for (int q = lane; q < G; q += 32) m = fmaxf(m, ld(GP(p.g.bnd, sc + q)));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
         const float mb = m * kLog2e;
         float z = 0.f;
         for (int t = lane; t < g.D; t += 32)
-            if (used(t)) z += ex2(fmaf(ld(srow + t), kLog2e, -mb));
-        for (int q = lane; q < G; q += 32) z += ex2(fmaf(ld(sc + q), kLog2e, -mb));
+            if (used(t)) z += ex2(fmaf(ld(GP(p.g.bnd, srow + t)), kLog2e, -mb));
+        for (int q = lane; q < G; q += 32) z += ex2(fmaf(ld(GP(p.g.bnd, sc + q)), kLog2e, -mb));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         const float inv = 1.f / z;
         for (int t = lane; t < g.D; t += 32)
-            prow[t] = Elt<T>::from_f(used(t) ? ex2(fmaf(ld(srow + t), kLog2e, -mb)) * inv : 0.f);
+            *GP(p.g.bnd, prow + t) = Elt<T>::from_f(used(t) ? ex2(fmaf(ld(GP(p.g.bnd, srow + t)), kLog2e, -mb)) * inv : 0.f);
         for (int q = lane; q < G; q += 32)
-            pc[q] = Elt<T>::from_f(ex2(fmaf(ld(sc + q), kLog2e, -mb)) * inv);
-        if (p.lse && lane == 0) p.lse[R] = m + logf(z);
+            *GP(p.g.bnd, pc + q) = Elt<T>::from_f(ex2(fmaf(ld(GP(p.g.bnd, sc + q)), kLog2e, -mb)) * inv);
+        if (p.lse && lane == 0) *GP(p.g.bnd, p.lse + R) = m + logf(z);
     }
 }
 
@@ -185,17 +187,17 @@ __global__ void __launch_bounds__(kThreads) k_glob_rows_softmax(const SoftmaxGlo
     const T *x = reinterpret_cast<const T *>(p.Srows) + (long long)W * g.n;
     T *y = reinterpret_cast<T *>(p.Prows) + (long long)W * g.n;
     float m = -INFINITY;
-    for (int j = lane; j < g.n; j += 32) m = fmaxf(m, ld(x + j));
+    for (int j = lane; j < g.n; j += 32) m = fmaxf(m, ld(GP(p.g.bnd, x + j)));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     const float mb = m * kLog2e;
     float z = 0.f;
-    for (int j = lane; j < g.n; j += 32) z += ex2(fmaf(ld(x + j), kLog2e, -mb));
+    for (int j = lane; j < g.n; j += 32) z += ex2(fmaf(ld(GP(p.g.bnd, x + j)), kLog2e, -mb));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     const float inv = 1.f / z;
-    for (int j = lane; j < g.n; j += 32) y[j] = Elt<T>::from_f(ex2(fmaf(ld(x + j), kLog2e, -mb)) * inv);
-    if (p.lse && lane == 0) p.lse[(long long)bh * g.n + gl.idx[gg]] = m + logf(z);
+    for (int j = lane; j < g.n; j += 32) *GP(p.g.bnd, y + j) = Elt<T>::from_f(ex2(fmaf(ld(GP(p.g.bnd, x + j)), kLog2e, -mb)) * inv);
+    if (p.lse && lane == 0) *GP(p.g.bnd, p.lse + (long long)bh * g.n + gl.idx[gg]) = m + logf(z);
 }
 
 // ---------------------------------------------------------------------------
@@ -223,8 +225,8 @@ __global__ void __launch_bounds__(kThreads) k_softmax_bwd_glob(const SoftmaxGlob
         const T *dPc = reinterpret_cast<const T *>(p.S2cols) + (long long)R * G;
         T *dSc = reinterpret_cast<T *>(p.Pcols) + (long long)R * G;
         if (in_bitmap(bm, i)) {
-            for (int t = lane; t < g.D; t += 32) dS[t] = Elt<T>::from_f(0.f);
-            for (int q = lane; q < G; q += 32) dSc[q] = Elt<T>::from_f(0.f);
+            for (int t = lane; t < g.D; t += 32) *GP(p.g.bnd, dS + t) = Elt<T>::from_f(0.f);
+            for (int q = lane; q < G; q += 32) *GP(p.g.bnd, dSc + q) = Elt<T>::from_f(0.f);
             continue;
         }
         auto used = [&](int t) {
@@ -233,13 +235,13 @@ __global__ void __launch_bounds__(kThreads) k_softmax_bwd_glob(const SoftmaxGlob
         };
         float delta = 0.f;
         for (int t = lane; t < g.D; t += 32)
-            if (used(t)) delta = fmaf(ld(P + t), ld(dP + t), delta);
-        for (int q = lane; q < G; q += 32) delta = fmaf(ld(Pc + q), ld(dPc + q), delta);
+            if (used(t)) delta = fmaf(ld(GP(p.g.bnd, P + t)), ld(GP(p.g.bnd, dP + t)), delta);
+        for (int q = lane; q < G; q += 32) delta = fmaf(ld(GP(p.g.bnd, Pc + q)), ld(GP(p.g.bnd, dPc + q)), delta);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
         for (int t = lane; t < g.D; t += 32)
-            dS[t] = Elt<T>::from_f(used(t) ? ld(P + t) * (ld(dP + t) - delta) : 0.f);
-        for (int q = lane; q < G; q += 32) dSc[q] = Elt<T>::from_f(ld(Pc + q) * (ld(dPc + q) - delta));
+            *GP(p.g.bnd, dS + t) = Elt<T>::from_f(used(t) ? ld(GP(p.g.bnd, P + t)) * (ld(GP(p.g.bnd, dP + t)) - delta) : 0.f);
+        for (int q = lane; q < G; q += 32) *GP(p.g.bnd, dSc + q) = Elt<T>::from_f(ld(GP(p.g.bnd, Pc + q)) * (ld(GP(p.g.bnd, dPc + q)) - delta));
     }
 }
 
@@ -254,10 +256,10 @@ __global__ void __launch_bounds__(kThreads) k_glob_rows_softmax_bwd(const Softma
     const T *dP = reinterpret_cast<const T *>(p.S2rows) + (long long)W * g.n;
     T *dS = reinterpret_cast<T *>(p.Prows) + (long long)W * g.n;
     float delta = 0.f;
-    for (int j = lane; j < g.n; j += 32) delta = fmaf(ld(P + j), ld(dP + j), delta);
+    for (int j = lane; j < g.n; j += 32) delta = fmaf(ld(GP(p.g.bnd, P + j)), ld(GP(p.g.bnd, dP + j)), delta);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
-    for (int j = lane; j < g.n; j += 32) dS[j] = Elt<T>::from_f(ld(P + j) * (ld(dP + j) - delta));
+    for (int j = lane; j < g.n; j += 32) *GP(p.g.bnd, dS + j) = Elt<T>::from_f(ld(GP(p.g.bnd, P + j)) * (ld(GP(p.g.bnd, dP + j)) - delta));
 }
 
 // ---------------------------------------------------------------------------
@@ -289,16 +291,16 @@ __global__ void __launch_bounds__(kThreads) k_glob_reduce(const GlobReduceArgs p
         for (int k = 0; k < 16; ++k) acc[k] = 0.f;
         for (int j0 = 0; j0 < n; j0 += kTile) {
             __syncthreads();
-            load_tile(y_t, Y, j0, n);
+            load_tile(p.g, y_t, Y, j0, n);
             for (int e = threadIdx.x; e < gn * kTile; e += blockDim.x) {
                 const int gg = e / kTile, jj = e % kTile;
                 const int j = j0 + jj;
                 float wv = 0.f;
                 if (j < n) {
                     if (kCols) {
-                        if (!in_bitmap(bm, j)) wv = ld(Wt + ((long long)bh * n + j) * G + gb + gg);
+                        if (!in_bitmap(bm, j)) wv = ld(GP(p.g.bnd, Wt + ((long long)bh * n + j) * G + gb + gg));
                     } else {
-                        wv = ld(Wt + ((long long)bh * G + gb + gg) * n + j);
+                        wv = ld(GP(p.g.bnd, Wt + ((long long)bh * G + gb + gg) * n + j));
                     }
                 }
                 w_t[gg * kPad + jj] = wv;
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(kThreads) k_glob_reduce(const GlobReduceArgs p
             if (gg < gn) {
                 T *dst = out + (long long)gl.idx[gb + gg] * 64 + c;
                 const float v = p.alpha * acc[k];
-                *dst = Elt<T>::from_f(kCols ? ld(dst) + v : v);
+                *GP(p.g.bnd, dst) = Elt<T>::from_f(kCols ? ld(GP(p.g.bnd, dst)) + v : v);
             }
         }
     }
@@ -352,12 +354,13 @@ __global__ void __launch_bounds__(128) k_band_pv_f32_glob(const DenseGlobArgs p)
         for (int t = 0; t < g.D; ++t) {
             const long long j = (long long)i + (long long)(t - g.w) * g.s;
             if (j < 0 || j >= g.n || in_bitmap(bm, j)) continue;
-            acc = fmaf(P[t], V[j * g.hd + c], acc);
+            acc = fmaf(*GP(g.bnd, P + t), *GP(g.bnd, V + j * g.hd + c), acc);
         }
         const float *cols = reinterpret_cast<const float *>(p.cols) + R * p.gl.G;
-        for (int q = 0; q < p.gl.G; ++q) acc = fmaf(cols[q], V[(long long)p.gl.idx[q] * g.hd + c], acc);
+        for (int q = 0; q < p.gl.G; ++q)
+            acc = fmaf(*GP(g.bnd, cols + q), *GP(g.bnd, V + (long long)p.gl.idx[q] * g.hd + c), acc);
     }
-    reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
+    *GP(g.bnd, reinterpret_cast<float *>(p.out) + R * g.hd + c) = p.alpha * acc;
 }
 
 __global__ void __launch_bounds__(128) k_band_t_f32_glob(const DenseGlobArgs p) {
@@ -376,13 +379,13 @@ __global__ void __launch_bounds__(128) k_band_t_f32_glob(const DenseGlobArgs p) 
         for (int t = 0; t < g.D; ++t) {
             const long long i = (long long)j - (long long)(t - g.w) * g.s;
             if (i < 0 || i >= g.n || in_bitmap(bm, i)) continue;
-            acc = fmaf(Bd[i * g.D + t], Y[i * g.hd + c], acc);
+            acc = fmaf(*GP(g.bnd, Bd + i * g.D + t), *GP(g.bnd, Y + i * g.hd + c), acc);
         }
     }
     const float *rows = reinterpret_cast<const float *>(p.rows) + bh * p.gl.G * g.n;
     for (int q = 0; q < p.gl.G; ++q)
-        acc = fmaf(rows[(long long)q * g.n + j], Y[(long long)p.gl.idx[q] * g.hd + c], acc);
-    reinterpret_cast<float *>(p.out)[R * g.hd + c] = p.alpha * acc;
+        acc = fmaf(*GP(g.bnd, rows + (long long)q * g.n + j), *GP(g.bnd, Y + (long long)p.gl.idx[q] * g.hd + c), acc);
+    *GP(g.bnd, reinterpret_cast<float *>(p.out) + R * g.hd + c) = p.alpha * acc;
 }
 
 unsigned grid_rows(long long rows_total) {
@@ -485,8 +488,8 @@ __global__ void __launch_bounds__(kGlobColThreads) k_fused_glob_cols(const Fused
     const T *V = reinterpret_cast<const T *>(p.V) + (long long)bh * n * 64;
     for (int e = threadIdx.x; e < G * 64; e += kGlobColThreads) {
         const int gg = e >> 6, c = e & 63;
-        kg[e] = ld(K + (long long)gl.idx[gg] * 64 + c);
-        vg[e] = ld(V + (long long)gl.idx[gg] * 64 + c);
+        kg[e] = ld(GP(p.g.bnd, K + (long long)gl.idx[gg] * 64 + c));
+        vg[e] = ld(GP(p.g.bnd, V + (long long)gl.idx[gg] * 64 + c));
     }
     __syncthreads();
     const int i = blockIdx.x * kGlobColThreads + threadIdx.x;
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(kGlobColThreads) k_fused_glob_cols(const Fused
         const uint4 *qr = reinterpret_cast<const uint4 *>(Q + (long long)i * 64);
 #pragma unroll
         for (int k = 0; k < 64 * (int)sizeof(T) / 16; ++k) {
-            const uint4 v = ldg16(qr + k);
+            const uint4 v = ldg16(GP(p.g.bnd, qr + k));
             if constexpr (sizeof(T) == 2) {
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -545,7 +548,7 @@ __global__ void __launch_bounds__(kGlobColThreads) k_fused_glob_cols(const Fused
     }
     // merge with the band part (O, lse of the keys outside G)
     const long long row = (long long)bh * n + i;
-    const float lse_a = p.lse[row];
+    const float lse_a = *GP(p.g.bnd, p.lse + row);
     const float lse_b = m / kLog2e + logf(l);
     const float m2 = fmaxf(lse_a, lse_b);
     const float wa = expf(lse_a - m2), wb = expf(lse_b - m2);
@@ -554,7 +557,7 @@ __global__ void __launch_bounds__(kGlobColThreads) k_fused_glob_cols(const Fused
     uint4 *o4 = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.O) + row * 64);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint4 a = o4[k];
+        const uint4 a = *GP(p.g.bnd, o4 + k);
         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
         uint32_t r[4];
 #pragma unroll
@@ -562,9 +565,9 @@ __global__ void __launch_bounds__(kGlobColThreads) k_fused_glob_cols(const Fused
             const int c = 8 * k + 2 * u;
             r[u] = pack2<T>(fmaf(lo16<T>(w[u]), fa, acc[c] * fb), fmaf(hi16<T>(w[u]), fa, acc[c + 1] * fb));
         }
-        o4[k] = make_uint4(r[0], r[1], r[2], r[3]);
+        *GP(p.g.bnd, o4 + k) = make_uint4(r[0], r[1], r[2], r[3]);
     }
-    p.lse[row] = m2 + logf(den);
+    *GP(p.g.bnd, p.lse + row) = m2 + logf(den);
 }
 
 // CTA per (global query, slice): 16 key groups of 16 threads, 4 channels each
@@ -576,7 +579,7 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArg
     const int i = p.gl.idx[gg];
     const T *K = reinterpret_cast<const T *>(p.K) + (long long)bh * n * 64;
     const T *V = reinterpret_cast<const T *>(p.V) + (long long)bh * n * 64;
-    if (threadIdx.x < 64) qs[threadIdx.x] = ld(reinterpret_cast<const T *>(p.Q) + ((long long)bh * n + i) * 64 + threadIdx.x);
+    if (threadIdx.x < 64) qs[threadIdx.x] = ld(GP(p.g.bnd, reinterpret_cast<const T *>(p.Q) + ((long long)bh * n + i) * 64 + threadIdx.x));
     __syncthreads();
     const int kg = threadIdx.x >> 4, cq = threadIdx.x & 15;
     const float q0 = qs[4 * cq], q1 = qs[4 * cq + 1], q2 = qs[4 * cq + 2], q3 = qs[4 * cq + 3];
@@ -591,8 +594,8 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArg
         for (int u = 0; u < 4; ++u) {
             const int j = jb + 16 * u + kg;
             const long long off = (long long)(j < n ? j : 0) * 64 + 4 * cq;
-            kw[u] = *reinterpret_cast<const uint2 *>(K + off);
-            vw[u] = *reinterpret_cast<const uint2 *>(V + off);
+            kw[u] = *GP(p.g.bnd, reinterpret_cast<const uint2 *>(K + off));
+            vw[u] = *GP(p.g.bnd, reinterpret_cast<const uint2 *>(V + off));
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -635,8 +638,8 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArg
             o = fmaf(red[k][2 + c], f, o);
         }
         const long long row = (long long)bh * n + i;
-        reinterpret_cast<T *>(p.O)[row * 64 + c] = Elt<T>::from_f(o / L);
-        if (c == 0) p.lse[row] = M / kLog2e + logf(L);
+        *GP(p.g.bnd, reinterpret_cast<T *>(p.O) + row * 64 + c) = Elt<T>::from_f(o / L);
+        if (c == 0) *GP(p.g.bnd, p.lse + row) = M / kLog2e + logf(L);
     }
 }
 

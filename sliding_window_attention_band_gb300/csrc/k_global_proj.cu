@@ -20,6 +20,8 @@
 
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 9;   // site id of the bounds checks
+
 namespace swab {
 namespace {
 
@@ -53,14 +55,14 @@ __device__ __forceinline__ void axpy4(float4 &acc, float a, const float4 v) {
 // rows [row0, row0 + nrows) of a [*, 64] array into smem as fp32 rows of kPad,
 // 16 bytes per load (rows at or past `limit` are zero)
 template <typename T>
-__device__ __forceinline__ void load_rows(float *dst, const T *src, int row0, int nrows, int limit) {
+__device__ __forceinline__ void load_rows(const GlobalProjArgs &p, float *dst, const T *src, int row0, int nrows, int limit) {
     constexpr int V = 16 / sizeof(T);   // elements per 16-byte load
     for (int e = threadIdx.x; e < nrows * (64 / V); e += kThreads) {
         const int r = e / (64 / V), c0 = (e % (64 / V)) * V;
         const int row = row0 + r;
         float *d = dst + r * kPad + c0;
         if (row < limit) {
-            const uint4 v = ldg16(reinterpret_cast<const uint4 *>(src + (long long)row * 64 + c0));
+            const uint4 v = ldg16(GP(p.bnd, reinterpret_cast<const uint4 *>(src + (long long)row * 64 + c0)));
             if constexpr (sizeof(T) == 4) {
                 *reinterpret_cast<float4 *>(d) = make_float4(__uint_as_float(v.x), __uint_as_float(v.y),
                                                              __uint_as_float(v.z), __uint_as_float(v.w));
@@ -87,13 +89,13 @@ template <typename T> struct TileRegs {
 };
 
 template <typename T>
-__device__ __forceinline__ void fetch_tile(TileRegs<T> &r, const T *src, int row0, int limit) {
+__device__ __forceinline__ void fetch_tile(const GlobalProjArgs &p, TileRegs<T> &r, const T *src, int row0, int limit) {
     constexpr int V = 16 / sizeof(T), PR = 64 / V;   // elements per piece, pieces per row
 #pragma unroll
     for (int k = 0; k < TileRegs<T>::kPer; ++k) {
         const int e = threadIdx.x + kThreads * k;
         const int row = row0 + e / PR;
-        r.v[k] = row < limit ? ldg16(reinterpret_cast<const uint4 *>(src + (long long)row * 64 + (e % PR) * V))
+        r.v[k] = row < limit ? ldg16(GP(p.bnd, reinterpret_cast<const uint4 *>(src + (long long)row * 64 + (e % PR) * V)))
                              : make_uint4(0, 0, 0, 0);
     }
 }
@@ -129,21 +131,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_gproj_fwd(const GlobalProjArgs 
     const T *Qg = reinterpret_cast<const T *>(p.Qg) + (long long)bh * G * 64;
     const T *Kg = reinterpret_cast<const T *>(p.Kg) + (long long)bh * n * 64;
     const T *Vg = reinterpret_cast<const T *>(p.Vg) + (long long)bh * n * 64;
-    load_rows(qs, Qg, gc * kGC, kGC, G);
+    load_rows(p, qs, Qg, gc * kGC, kGC, G);
     const float xs = p.scale * kLog2e;
     float m = -INFINITY, l = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);   // channels 4 sub .. + 3
     const int k0 = kc * kChunkKeys, k1 = min(n, k0 + kChunkKeys);
     TileRegs<T> kr, vr;
-    fetch_tile(kr, Kg, k0, n);
-    fetch_tile(vr, Vg, k0, n);
+    fetch_tile(p, kr, Kg, k0, n);
+    fetch_tile(p, vr, Vg, k0, n);
     for (int j0 = k0; j0 < k1; j0 += kKT) {
         __syncthreads();   // the previous tile's readers are done
         store_tile(ks, kr);
         store_tile(vs, vr);
         if (j0 + kKT < k1) {   // the next tile's loads fly during this tile's products
-            fetch_tile(kr, Kg, j0 + kKT, n);
-            fetch_tile(vr, Vg, j0 + kKT, n);
+            fetch_tile(p, kr, Kg, j0 + kKT, n);
+            fetch_tile(p, vr, Vg, j0 + kKT, n);
         }
         __syncthreads();
         float s[4] = {0.f, 0.f, 0.f, 0.f}, tmax = -INFINITY;
@@ -193,13 +195,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gproj_fwd(const GlobalProjArgs 
     // partial of (slice, chunk, query): [m (log2 units), l, acc[64]]
     float *part = p.ws + (((long long)bh * p.nchunks + kc) * G + gg) * 66;
     if (sub == 0) {
-        part[0] = m;
-        part[1] = l;
+        *GP(p.bnd, part) = m;
+        *GP(p.bnd, part + 1) = l;
     }
-    part[2 + 4 * sub] = acc.x;
-    part[3 + 4 * sub] = acc.y;
-    part[4 + 4 * sub] = acc.z;
-    part[5 + 4 * sub] = acc.w;
+    *GP(p.bnd, part + 2 + 4 * sub) = acc.x;
+    *GP(p.bnd, part + 3 + 4 * sub) = acc.y;
+    *GP(p.bnd, part + 4 + 4 * sub) = acc.z;
+    *GP(p.bnd, part + 5 + 4 * sub) = acc.w;
 }
 
 // merge the chunks: a warp per (slice, query); lane k < nchunks reads chunk
@@ -214,11 +216,12 @@ __global__ void __launch_bounds__(kThreads) k_gproj_combine(const GlobalProjArgs
     const float *base = p.ws + ((long long)bh * p.nchunks * p.G + gg) * 66;
     const long long step = (long long)p.G * 66;     // next chunk of the same query
     float M = -INFINITY;
-    for (int k = lane; k < p.nchunks; k += 32) M = fmaxf(M, base[k * step]);
+    for (int k = lane; k < p.nchunks; k += 32) M = fmaxf(M, *GP(p.bnd, base + k * step));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
-    for (int k = lane; k < p.nchunks; k += 32) L = fmaf(base[k * step + 1], ex2(base[k * step] - M), L);
+    for (int k = lane; k < p.nchunks; k += 32)
+        L = fmaf(*GP(p.bnd, base + k * step + 1), ex2(*GP(p.bnd, base + k * step) - M), L);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     float o0 = 0.f, o1 = 0.f;
@@ -228,9 +231,9 @@ __global__ void __launch_bounds__(kThreads) k_gproj_combine(const GlobalProjArgs
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const float *c = base + (k + u) * step;
-            f[u] = c[0];
-            a[u] = c[2 + 2 * lane];
-            b[u] = c[3 + 2 * lane];
+            f[u] = *GP(p.bnd, c);
+            a[u] = *GP(p.bnd, c + 2 + 2 * lane);
+            b[u] = *GP(p.bnd, c + 3 + 2 * lane);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -241,15 +244,15 @@ __global__ void __launch_bounds__(kThreads) k_gproj_combine(const GlobalProjArgs
     }
     for (; k < p.nchunks; ++k) {
         const float *c = base + k * step;
-        const float w = ex2(c[0] - M);
-        o0 = fmaf(c[2 + 2 * lane], w, o0);
-        o1 = fmaf(c[3 + 2 * lane], w, o1);
+        const float w = ex2(*GP(p.bnd, c) - M);
+        o0 = fmaf(*GP(p.bnd, c + 2 + 2 * lane), w, o0);
+        o1 = fmaf(*GP(p.bnd, c + 3 + 2 * lane), w, o1);
     }
     const float inv = 1.f / L;
     T *o = reinterpret_cast<T *>(p.Og) + bg * 64 + 2 * lane;
-    o[0] = Elt<T>::from_f(o0 * inv);
-    o[1] = Elt<T>::from_f(o1 * inv);
-    if (lane == 0 && p.lseg) p.lseg[bg] = M / kLog2e + logf(L);
+    *GP(p.bnd, o) = Elt<T>::from_f(o0 * inv);
+    *GP(p.bnd, o + 1) = Elt<T>::from_f(o1 * inv);
+    if (lane == 0 && p.lseg) *GP(p.bnd, p.lseg + bg) = M / kLog2e + logf(L);
 }
 
 // ---------------------------------------------------------------------------
@@ -274,8 +277,8 @@ __global__ void __launch_bounds__(kThreads) k_gproj_bwd(const GlobalProjArgs p) 
     const T *dOg = reinterpret_cast<const T *>(p.dOg) + (long long)bh * G * 64;
     const T *Kg = reinterpret_cast<const T *>(p.Kg) + (long long)bh * n * 64;
     const T *Vg = reinterpret_cast<const T *>(p.Vg) + (long long)bh * n * 64;
-    load_rows(ks, Kg, j0, kKT, n);
-    load_rows(vs, Vg, j0, kKT, n);
+    load_rows(p, ks, Kg, j0, kKT, n);
+    load_rows(p, vs, Vg, j0, kKT, n);
     // dK, dV of key jr = t / 4, channels 16 (t % 4) .. + 16
     const int jr = t >> 2, cq = (t & 3) * 16;
     float dk[16], dv[16];
@@ -284,9 +287,9 @@ __global__ void __launch_bounds__(kThreads) k_gproj_bwd(const GlobalProjArgs p) 
     const float xs = p.scale * kLog2e;
     for (int g0 = 0; g0 < G; g0 += kGC) {
         __syncthreads();   // the previous chunk's readers are done
-        load_rows(qs, Qg, g0, kGC, G);
-        load_rows(dos, dOg, g0, kGC, G);
-        if (t < kGC) lse_s[t] = g0 + t < G ? p.lseg[(long long)bh * G + g0 + t] * kLog2e : 0.f;
+        load_rows(p, qs, Qg, g0, kGC, G);
+        load_rows(p, dos, dOg, g0, kGC, G);
+        if (t < kGC) lse_s[t] = g0 + t < G ? *GP(p.bnd, p.lseg + (long long)bh * G + g0 + t) * kLog2e : 0.f;
         // delta_g = dOg[g].Og[g]: 16 threads per query, 4 channels each
         {
             float d = 0.f;
@@ -294,8 +297,8 @@ __global__ void __launch_bounds__(kThreads) k_gproj_bwd(const GlobalProjArgs p) 
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int c = sub + 16 * u;
-                    d = fmaf(Elt<T>::to_f(dOg[(long long)(g0 + g) * 64 + c]),
-                             Elt<T>::to_f(Og[(long long)(g0 + g) * 64 + c]), d);
+                    d = fmaf(Elt<T>::to_f(*GP(p.bnd, dOg + (long long)(g0 + g) * 64 + c)),
+                             Elt<T>::to_f(*GP(p.bnd, Og + (long long)(g0 + g) * 64 + c)), d);
                 }
             }
 #pragma unroll
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kThreads) k_gproj_bwd(const GlobalProjArgs p) 
                 axpy4(dq, d4.w, lds4(kr + 3 * kPad));
             }
             float *part = p.ws + (((long long)bh * p.nchunks + kt) * G + g0 + g) * 64 + 4 * sub;
-            *reinterpret_cast<float4 *>(part) =
+            *GP(p.bnd, reinterpret_cast<float4 *>(part)) =
                 make_float4(p.scale * dq.x, p.scale * dq.y, p.scale * dq.z, p.scale * dq.w);
         }
         // dK[jr] += scale sum_g ds_g,jr Qg[g];  dV[jr] += sum_g p_g,jr dOg[g]
@@ -365,8 +368,8 @@ __global__ void __launch_bounds__(kThreads) k_gproj_bwd(const GlobalProjArgs p) 
     T *dV = reinterpret_cast<T *>(p.dVg) + ((long long)bh * n + j0 + jr) * 64 + cq;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        dK[k] = Elt<T>::from_f(p.scale * dk[k]);
-        dV[k] = Elt<T>::from_f(dv[k]);
+        *GP(p.bnd, dK + k) = Elt<T>::from_f(p.scale * dk[k]);
+        *GP(p.bnd, dV + k) = Elt<T>::from_f(dv[k]);
     }
 }
 
@@ -516,10 +519,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const T *Og = reinterpret_cast<const T *>(p.Og) + (long long)bh * G * 64;
         const T *dOg = reinterpret_cast<const T *>(p.dOg) + (long long)bh * G * 64;
         for (int gg = t; gg < G; gg += 128) {
-            lse2[gg] = p.lseg[(long long)bh * G + gg] * kLog2e;
+            lse2[gg] = *GP(p.bnd, p.lseg + (long long)bh * G + gg) * kLog2e;
             float d = 0.f;
             for (int c = 0; c < 64; ++c)
-                d = fmaf(Elt<T>::to_f(Og[(long long)gg * 64 + c]), Elt<T>::to_f(dOg[(long long)gg * 64 + c]), d);
+                d = fmaf(Elt<T>::to_f(*GP(p.bnd, Og + (long long)gg * 64 + c)),
+                         Elt<T>::to_f(*GP(p.bnd, dOg + (long long)gg * 64 + c)), d);
             del[gg] = d;
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");   // the workers' lse, delta
@@ -581,7 +585,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kGC; ++q) {
                     const int gg = c * kGC + q;
-                    if (gg < G) part[(long long)gg * 64] = p.scale * __uint_as_float(qv[q]);
+                    if (gg < G) *GP(p.bnd, part + (long long)gg * 64) = p.scale * __uint_as_float(qv[q]);
                 }
             }
             tc_fence_before();
@@ -604,7 +608,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         uint4 *o4 = reinterpret_cast<uint4 *>((which ? dK : dV) + 32 * h);
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
-                            o4[u] = make_uint4(
+                            *GP(p.bnd, o4 + u) = make_uint4(
                                 pack2<T>(mul * __uint_as_float(v[8 * u]), mul * __uint_as_float(v[8 * u + 1])),
                                 pack2<T>(mul * __uint_as_float(v[8 * u + 2]), mul * __uint_as_float(v[8 * u + 3])),
                                 pack2<T>(mul * __uint_as_float(v[8 * u + 4]), mul * __uint_as_float(v[8 * u + 5])),
@@ -808,8 +812,10 @@ __global__ void __launch_bounds__(kTcThreads, 4)
             float *part = p.ws + ((long long)bh * p.nchunks + kt) * G * 66;
             if (t < kGC && c * kGC + t < G) {
                 const int gg = c * kGC + t;
-                part[(long long)gg * 66] = max3(wmax[t], wmax[kGC + t], fmaxf(wmax[2 * kGC + t], wmax[3 * kGC + t]));
-                part[(long long)gg * 66 + 1] = (wsum[t] + wsum[kGC + t]) + (wsum[2 * kGC + t] + wsum[3 * kGC + t]);
+                *GP(p.bnd, part + (long long)gg * 66) =
+                    max3(wmax[t], wmax[kGC + t], fmaxf(wmax[2 * kGC + t], wmax[3 * kGC + t]));
+                *GP(p.bnd, part + (long long)gg * 66 + 1) =
+                    (wsum[t] + wsum[kGC + t]) + (wsum[2 * kGC + t] + wsum[3 * kGC + t]);
             }
             if (!__all_sync(0xffffffffu, mbar_wait(ofull, c & 1, abort_flag, p.err))) {
                 ok = false;
@@ -823,7 +829,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
 #pragma unroll
                 for (int q = 0; q < kGC; ++q) {
                     const int gg = c * kGC + q;
-                    if (gg < G) part[(long long)gg * 66 + 2 + m] = __uint_as_float(ov[q]);
+                    if (gg < G) *GP(p.bnd, part + (long long)gg * 66 + 2 + m) = __uint_as_float(ov[q]);
                 }
             }
             tc_fence_before();
@@ -912,8 +918,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int r = e >> 3, c = e & 7;
             uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
             if (r < G) {
-                kv = ldg16(Kb + (long long)p.gl.idx[r] * 64 + 8 * c);
-                vv = ldg16(Vb + (long long)p.gl.idx[r] * 64 + 8 * c);
+                kv = ldg16(GPN(p.bnd, Kb + (long long)p.gl.idx[r] * 64 + 8 * c, 16));
+                vv = ldg16(GPN(p.bnd, Vb + (long long)p.gl.idx[r] * 64 + 8 * c, 16));
             }
             const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
             sts16(smem_u32(kgb) + off, kv);
@@ -1015,7 +1021,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             uint32_t ov[32];
             const long long row = (long long)bh * n + (write ? i : 0);
-            const float lse_a = write ? p.lse[row] : 0.f;
+            const float lse_a = write ? *GP(p.bnd, p.lse + row) : 0.f;
             const float lse_b = mb / kLog2e + logf(lb);
             const float m2 = fmaxf(lse_a, lse_b);
             const float wa = expf(lse_a - m2), wb = expf(lse_b - m2);
@@ -1029,7 +1035,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (write) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint4 a = o4[4 * h + k];
+                        const uint4 a = *GP(p.bnd, o4 + 4 * h + k);
                         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
                         uint32_t r[4];
 #pragma unroll
@@ -1038,11 +1044,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             r[u] = pack2<T>(fmaf(lo16<T>(w[u]), fa, __uint_as_float(ov[c]) * fb),
                                             fmaf(hi16<T>(w[u]), fa, __uint_as_float(ov[c + 1]) * fb));
                         }
-                        o4[4 * h + k] = make_uint4(r[0], r[1], r[2], r[3]);
+                        *GP(p.bnd, o4 + 4 * h + k) = make_uint4(r[0], r[1], r[2], r[3]);
                     }
                 }
             }
-            if (write) p.lse[row] = m2 + logf(den);
+            if (write) *GP(p.bnd, p.lse + row) = m2 + logf(den);
         }
     }
     tc_fence_before();
@@ -1118,7 +1124,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the 16 queries' rows into the swizzled Q tile, zeros past G
         const int t = threadIdx.x - 64, j = t >> 3, c = t & 7, gg = gc * kGC + j;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (gg < G) v = ldg16(reinterpret_cast<const T *>(p.Q) + ((long long)bh * n + p.gl.idx[gg]) * 64 + 8 * c);
+        if (gg < G) v = ldg16(GPN(p.bnd, reinterpret_cast<const T *>(p.Q) + ((long long)bh * n + p.gl.idx[gg]) * 64 + 8 * c, 16));
         sts16(smem_u32(qbuf) + j * 128 + ((c ^ (j & 7)) << 4), v);
         fence_proxy_async_smem();
     }
@@ -1297,7 +1303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 inv[q] = 1.f / l;
                 const int gg = gc * kGC + q;
                 if (wi == 0 && lane == q && gg < G)
-                    p.lse[(long long)bh * n + p.gl.idx[gg]] = mx[q] / kLog2e + logf(l);
+                    *GP(p.bnd, p.lse + (long long)bh * n + p.gl.idx[gg]) = mx[q] / kLog2e + logf(l);
             }
             if (quarter < 2) {   // TMEM lanes 0-63: the 64 channels of O^T
                 uint32_t ov[16];
@@ -1308,7 +1314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int q = 0; q < kGC; ++q) {
                     const int gg = gc * kGC + q;
                     if (gg < G)
-                        O[((long long)bh * n + p.gl.idx[gg]) * 64 + m] = Elt<T>::from_f(__uint_as_float(ov[q]) * inv[q]);
+                        *GP(p.bnd, O + ((long long)bh * n + p.gl.idx[gg]) * 64 + m) = Elt<T>::from_f(__uint_as_float(ov[q]) * inv[q]);
                 }
             }
         }
@@ -1338,12 +1344,12 @@ __global__ void __launch_bounds__(kThreads) k_gproj_dq(const GlobalProjArgs p) {
     for (; k + 8 <= p.nchunks; k += 8) {
         float v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = base[(k + u) * step];
+        for (int u = 0; u < 8; ++u) v[u] = *GP(p.bnd, base + (k + u) * step);
 #pragma unroll
         for (int u = 0; u < 8; ++u) s += v[u];
     }
-    for (; k < p.nchunks; ++k) s += base[k * step];
-    reinterpret_cast<T *>(p.dQg)[e] = Elt<T>::from_f(s);
+    for (; k < p.nchunks; ++k) s += *GP(p.bnd, base + k * step);
+    *GP(p.bnd, reinterpret_cast<T *>(p.dQg) + e) = Elt<T>::from_f(s);
 }
 
 template <typename T>

@@ -23,6 +23,8 @@
 
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 8;   // site id of the bounds checks
+
 namespace swab {
 namespace {
 
@@ -74,7 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = threadIdx.x; e < Gp * 8; e += kThreads) {
         const int q = e >> 3, c = e & 7;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (q < G) v = *reinterpret_cast<const uint4 *>(ysrc + (size_t)p.gl.idx[q] * 64 + 8 * c);
+        if (q < G) v = *GP(p.g.bnd, reinterpret_cast<const uint4 *>(ysrc + (size_t)p.gl.idx[q] * 64 + 8 * c));
         *reinterpret_cast<uint4 *>(yg + sw128(q, c)) = v;
     }
     fence_proxy_async_smem();
@@ -113,11 +115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!rows) {
                     T *dst = reinterpret_cast<T *>(p.cols) + ((size_t)bh * n + row) * G;
                     for (int k = 0; k < 32 && g0 + k < G; ++k)
-                        dst[g0 + k] = Elt<T>::from_f(p.alpha * __uint_as_float(v[k]));
+                        *GP(p.g.bnd, dst + g0 + k) = Elt<T>::from_f(p.alpha * __uint_as_float(v[k]));
                 } else {
                     T *dst = reinterpret_cast<T *>(p.rows) + (size_t)bh * G * n + row;
                     for (int k = 0; k < 32 && g0 + k < G; ++k)
-                        dst[(size_t)(g0 + k) * n] = Elt<T>::from_f(p.alpha * __uint_as_float(v[k]));
+                        *GP(p.g.bnd, dst + (size_t)(g0 + k) * n) = Elt<T>::from_f(p.alpha * __uint_as_float(v[k]));
                 }
             }
         }
@@ -229,10 +231,10 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
         // they are in range and aligned, else element by element
         auto piece = [&](const T *src, int cnt) -> uint4 {
             if (cnt >= 8 && (reinterpret_cast<uintptr_t>(src) & 15) == 0)
-                return *reinterpret_cast<const uint4 *>(src);
+                return *GP(g.bnd, reinterpret_cast<const uint4 *>(src));
             float f[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) f[u] = u < cnt ? Elt<T>::to_f(src[u]) : 0.f;
+            for (int u = 0; u < 8; ++u) f[u] = u < cnt ? Elt<T>::to_f(*GP(g.bnd, src + u)) : 0.f;
             return make_uint4(pack2<T>(f[0], f[1]), pack2<T>(f[2], f[3]), pack2<T>(f[4], f[5]),
                               pack2<T>(f[6], f[7]));
         };
@@ -304,7 +306,7 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
         for (int rr = 0; rr < kSplit; ++rr) acc += ld_peer_f32(loc, rr);
         T *dst = reinterpret_cast<T *>(p.out) + ((size_t)bh * n + gl.idx[q0 + qq]) * 64 + ch;
         const float x = p.alpha * acc;
-        *dst = Elt<T>::from_f(kCols ? Elt<T>::to_f(*dst) + x : x);
+        *GP(g.bnd, dst) = Elt<T>::from_f(kCols ? Elt<T>::to_f(*GP(g.bnd, dst)) + x : x);
     }
     // no CTA leaves while another still reads its partial
     cluster_sync();

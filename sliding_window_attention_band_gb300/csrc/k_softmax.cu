@@ -29,6 +29,8 @@
 // instruction (relative error about 2^-22).
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 6;   // site id of the bounds checks
+
 namespace swab {
 namespace {
 
@@ -99,17 +101,17 @@ __device__ __forceinline__ Row make_row(const Geom &g, int R) {
 }
 
 template <typename T>
-__device__ __forceinline__ void store_piece(uint4 *out, int pc, const Row &rw,
+__device__ __forceinline__ void store_piece(const Geom &g, uint4 *out, int pc, const Row &rw,
                                             const float (&y)[Vec<T>::N]) {
     constexpr int N = Vec<T>::N;
     const int x0 = pc * N;
     if (x0 >= rw.lead && x0 + N <= rw.xend) {
-        out[pc] = pack<T>(y);
+        *GP(g.bnd, out + pc) = pack<T>(y);
     } else {
         T *e = reinterpret_cast<T *>(out + pc);
 #pragma unroll
         for (int u = 0; u < N; ++u)
-            if (x0 + u >= rw.lead && x0 + u < rw.xend) e[u] = Elt<T>::from_f(y[u]);
+            if (x0 + u >= rw.lead && x0 + u < rw.xend) *GP(g.bnd, e + u) = Elt<T>::from_f(y[u]);
     }
 }
 
@@ -130,7 +132,7 @@ __device__ __forceinline__ void add_key_bias(float (&x)[N], int x0, const Row &r
 #pragma unroll
     for (int u = 0; u < N; ++u) {
         const int xx = x0 + u;
-        if (xx >= rw.xlo && xx <= rw.xhi) x[u] += __ldg(brow + i + (xx - rw.lead - g.w) * g.s);
+        if (xx >= rw.xlo && xx <= rw.xhi) x[u] += __ldg(GP(g.bnd, brow + i + (xx - rw.lead - g.w) * g.s));
     }
 }
 
@@ -184,7 +186,7 @@ __device__ __forceinline__ void apply_keep(float (&y)[N], int x0, const Row &rw,
 
 // Stores f * y for a piece of probabilities (0 on invalid slots).
 template <typename T>
-__device__ __forceinline__ void store_dropped(uint4 *out, int pc, const Row &rw, const Keep &kp,
+__device__ __forceinline__ void store_dropped(const Geom &g, uint4 *out, int pc, const Row &rw, const Keep &kp,
                                               const float (&y)[Vec<T>::N]) {
     constexpr int N = Vec<T>::N;
     const int x0 = pc * N;
@@ -192,7 +194,7 @@ __device__ __forceinline__ void store_dropped(uint4 *out, int pc, const Row &rw,
 #pragma unroll
     for (int u = 0; u < N; ++u)
         yd[u] = (x0 + u >= rw.xlo && x0 + u <= rw.xhi) ? y[u] * keep_factor(kp, x0 + u) : 0.f;
-    store_piece<T>(out, pc, rw, yd);
+    store_piece<T>(g, out, pc, rw, yd);
 }
 
 // ---------------------------------------------------------------------------
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
         const int pc = lane + 32 * k;
-        raw[k] = pc < rw.npieces ? ldg16(src + pc) : make_uint4(0, 0, 0, 0);
+        raw[k] = pc < rw.npieces ? ldg16(GP(g.bnd, src + pc)) : make_uint4(0, 0, 0, 0);
     }
     // the keep bits are drawn while the row's loads are in flight
     extern __shared__ uint32_t keep_smem[];
@@ -327,13 +329,13 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_reg(const Softma
 #pragma unroll
         for (int u = 0; u < N; u += 2) f2split(mul2(f2(y[u], y[u + 1]), inv2), y[u], y[u + 1]);
         if constexpr (kDrop) {
-            if (p.P) store_piece<T>(dst, pc, rw, y);
-            store_dropped<T>(dstd, pc, rw, kp, y);
+            if (p.P) store_piece<T>(g, dst, pc, rw, y);
+            store_dropped<T>(g, dstd, pc, rw, kp, y);
         } else {
-            store_piece<T>(dst, pc, rw, y);
+            store_piece<T>(g, dst, pc, rw, y);
         }
     }
-    if (p.lse && lane == 0) p.lse[R] = m + logf(z);
+    if (p.lse && lane == 0) *GP(g.bnd, p.lse + R) = m + logf(z);
 }
 
 template <typename T, int NCH, bool kDrop>
@@ -352,8 +354,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const So
     for (int k = 0; k < NCH; ++k) {
         const int pc = lane + 32 * k;
         const bool in = pc < rw.npieces;
-        rp[k] = in ? ldg16(sp + pc) : make_uint4(0, 0, 0, 0);
-        rd[k] = in ? ldg16(sd + pc) : make_uint4(0, 0, 0, 0);
+        rp[k] = in ? ldg16(GP(g.bnd, sp + pc)) : make_uint4(0, 0, 0, 0);
+        rd[k] = in ? ldg16(GP(g.bnd, sd + pc)) : make_uint4(0, 0, 0, 0);
     }
     // the keep bits are drawn while the row's loads are in flight
     extern __shared__ uint32_t keep_smem[];
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_reg(const So
 #pragma unroll
         for (int u = 0; u < N; u += 2)
             f2split(mul2(f2(x[u], x[u + 1]), add2(f2(y[u], y[u + 1]), nd2)), x[u], x[u + 1]);
-        store_piece<T>(dst, pc, rw, x);
+        store_piece<T>(g, dst, pc, rw, x);
     }
 }
 
@@ -460,7 +462,7 @@ __global__ void __launch_bounds__(kWideThreads) k_softmax_wide(const SoftmaxArgs
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
         const int pc = tid + kWideThreads * k;
-        raw[k] = pc < rw.npieces ? ldg16(src + pc) : make_uint4(0, 0, 0, 0);
+        raw[k] = pc < rw.npieces ? ldg16(GP(g.bnd, src + pc)) : make_uint4(0, 0, 0, 0);
     }
     __shared__ float red[kWideWarps];
     extern __shared__ uint32_t keep_smem[];
@@ -508,13 +510,13 @@ __global__ void __launch_bounds__(kWideThreads) k_softmax_wide(const SoftmaxArgs
 #pragma unroll
         for (int u = 0; u < N; u += 2) f2split(mul2(f2(xs[k * N + u], xs[k * N + u + 1]), inv2), y[u], y[u + 1]);
         if constexpr (kDrop) {
-            if (p.P) store_piece<T>(dst, pc, rw, y);
-            store_dropped<T>(dstd, pc, rw, kp, y);
+            if (p.P) store_piece<T>(g, dst, pc, rw, y);
+            store_dropped<T>(g, dstd, pc, rw, kp, y);
         } else {
-            store_piece<T>(dst, pc, rw, y);
+            store_piece<T>(g, dst, pc, rw, y);
         }
     }
-    if (p.lse && tid == 0) p.lse[R] = m + logf(z);
+    if (p.lse && tid == 0) *GP(g.bnd, p.lse + R) = m + logf(z);
 }
 
 template <typename T, int NCH, bool kDrop>
@@ -533,8 +535,8 @@ __global__ void __launch_bounds__(kWideThreads) k_softmax_bwd_wide(const Softmax
     for (int k = 0; k < NCH; ++k) {
         const int pc = tid + kWideThreads * k;
         const bool in = pc < rw.npieces;
-        rp[k] = in ? ldg16(sp + pc) : make_uint4(0, 0, 0, 0);
-        rd[k] = in ? ldg16(sd + pc) : make_uint4(0, 0, 0, 0);
+        rp[k] = in ? ldg16(GP(g.bnd, sp + pc)) : make_uint4(0, 0, 0, 0);
+        rd[k] = in ? ldg16(GP(g.bnd, sd + pc)) : make_uint4(0, 0, 0, 0);
     }
     __shared__ float red[kWideWarps];
     extern __shared__ uint32_t keep_smem[];
@@ -574,7 +576,7 @@ __global__ void __launch_bounds__(kWideThreads) k_softmax_bwd_wide(const Softmax
         for (int u = 0; u < N; u += 2)
             f2split(mul2(f2(xp[k * N + u], xp[k * N + u + 1]), add2(f2(yd[k * N + u], yd[k * N + u + 1]), nd2)),
                     x[u], x[u + 1]);
-        store_piece<T>(dst, pc, rw, x);
+        store_piece<T>(g, dst, pc, rw, x);
     }
 }
 
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
     float m = -INFINITY, z = 0.f;
     for (int pc = lane; pc < rw.npieces; pc += 32) {
         float x[N];
-        unpack<T>(ldg16(src + pc), x);
+        unpack<T>(ldg16(GP(g.bnd, src + pc)), x);
         const int x0 = pc * N;
         if (brow) add_key_bias(x, x0, rw, brow, qi, g);
         float pm = -INFINITY;
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
     uint4 *dstd = reinterpret_cast<uint4 *>(p.Pd) + rw.piece0;
     for (int pc = lane; pc < rw.npieces; pc += 32) {
         float x[N];
-        unpack<T>(ldg16(src + pc), x);
+        unpack<T>(ldg16(GP(g.bnd, src + pc)), x);
         const int x0 = pc * N;
         if (brow) add_key_bias(x, x0, rw, brow, qi, g);
 #pragma unroll
@@ -638,10 +640,10 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_stream(const Sof
             const bool v = x0 + u >= rw.xlo && x0 + u <= rw.xhi;
             x[u] = v ? ex2(fmaf(x[u], kLog2e, -m)) * inv : 0.f;
         }
-        if (p.P) store_piece<T>(dst, pc, rw, x);
-        if (drop) store_dropped<T>(dstd, pc, rw, kp, x);
+        if (p.P) store_piece<T>(g, dst, pc, rw, x);
+        if (drop) store_dropped<T>(g, dstd, pc, rw, kp, x);
     }
-    if (p.lse && lane == 0) p.lse[R] = m / kLog2e + logf(z);
+    if (p.lse && lane == 0) *GP(g.bnd, p.lse + R) = m / kLog2e + logf(z);
 }
 
 template <typename T>
@@ -661,8 +663,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const
     float delta = 0.f;
     for (int pc = lane; pc < rw.npieces; pc += 32) {
         float x[N], y[N];
-        unpack<T>(ldg16(sp + pc), x);
-        unpack<T>(ldg16(sd + pc), y);
+        unpack<T>(ldg16(GP(g.bnd, sp + pc)), x);
+        unpack<T>(ldg16(GP(g.bnd, sd + pc)), y);
         const int x0 = pc * N;
         if (drop) apply_keep<N>(y, x0, rw, kp);
 #pragma unroll
@@ -674,8 +676,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const
     uint4 *dst = reinterpret_cast<uint4 *>(p.P) + rw.piece0;
     for (int pc = lane; pc < rw.npieces; pc += 32) {
         float x[N], y[N];
-        unpack<T>(ldg16(sp + pc), x);
-        unpack<T>(ldg16(sd + pc), y);
+        unpack<T>(ldg16(GP(g.bnd, sp + pc)), x);
+        unpack<T>(ldg16(GP(g.bnd, sd + pc)), y);
         const int x0 = pc * N;
         if (drop) apply_keep<N>(y, x0, rw, kp);
 #pragma unroll
@@ -683,7 +685,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_stream(const
             const bool v = x0 + u >= rw.xlo && x0 + u <= rw.xhi;
             x[u] = v ? x[u] * (y[u] - delta) : 0.f;
         }
-        store_piece<T>(dst, pc, rw, x);
+        store_piece<T>(g, dst, pc, rw, x);
     }
 }
 
@@ -741,8 +743,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_glob_reg(const S
         float zero[N];
 #pragma unroll
         for (int u = 0; u < N; ++u) zero[u] = 0.f;
-        for (int pc = lane; pc < rw.npieces; pc += 32) store_piece<T>(dst, pc, rw, zero);
-        for (int q = lane; q < G; q += 32) pcol[q] = Elt<T>::from_f(0.f);
+        for (int pc = lane; pc < rw.npieces; pc += 32) store_piece<T>(g, dst, pc, rw, zero);
+        for (int q = lane; q < G; q += 32) *GP(g.bnd, pcol + q) = Elt<T>::from_f(0.f);
         return;
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
@@ -750,14 +752,14 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_glob_reg(const S
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
         const int pc = lane + 32 * k;
-        raw[k] = pc < rw.npieces ? ldg16(src + pc) : make_uint4(0, 0, 0, 0);
+        raw[k] = pc < rw.npieces ? ldg16(GP(g.bnd, src + pc)) : make_uint4(0, 0, 0, 0);
     }
     const T *scol = reinterpret_cast<const T *>(p.Scols) + R * G;
     float cv[kColsPerLane];
 #pragma unroll
     for (int k = 0; k < kColsPerLane; ++k) {
         const int q = lane + 32 * k;
-        cv[k] = q < G ? ld(scol + q) : -INFINITY;
+        cv[k] = q < G ? ld(GP(g.bnd, scol + q)) : -INFINITY;
     }
     float xs[NCH * N];
     float m = -INFINITY;
@@ -807,14 +809,14 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_glob_reg(const S
         float y[N];
 #pragma unroll
         for (int u = 0; u < N; u += 2) f2split(mul2(f2(xs[k * N + u], xs[k * N + u + 1]), inv2), y[u], y[u + 1]);
-        store_piece<T>(dst, pc, rw, y);
+        store_piece<T>(g, dst, pc, rw, y);
     }
 #pragma unroll
     for (int k = 0; k < kColsPerLane; ++k) {
         const int q = lane + 32 * k;
-        if (q < G) pcol[q] = Elt<T>::from_f(cv[k] * inv);
+        if (q < G) *GP(g.bnd, pcol + q) = Elt<T>::from_f(cv[k] * inv);
     }
-    if (p.lse && lane == 0) p.lse[R] = m + logf(z);
+    if (p.lse && lane == 0) *GP(g.bnd, p.lse + R) = m + logf(z);
 }
 
 // dS = P (dP - delta) on the used slots and dSc = Pc (dPc - delta) on the
@@ -837,8 +839,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_glob_reg(con
         float zero[N];
 #pragma unroll
         for (int u = 0; u < N; ++u) zero[u] = 0.f;
-        for (int pc = lane; pc < rw.npieces; pc += 32) store_piece<T>(dst, pc, rw, zero);
-        for (int q = lane; q < G; q += 32) dscol[q] = Elt<T>::from_f(0.f);
+        for (int pc = lane; pc < rw.npieces; pc += 32) store_piece<T>(g, dst, pc, rw, zero);
+        for (int q = lane; q < G; q += 32) *GP(g.bnd, dscol + q) = Elt<T>::from_f(0.f);
         return;
     }
     const uint4 *sp = reinterpret_cast<const uint4 *>(p.S) + rw.piece0;
@@ -848,8 +850,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_glob_reg(con
     for (int k = 0; k < NCH; ++k) {
         const int pc = lane + 32 * k;
         const bool in = pc < rw.npieces;
-        rp[k] = in ? ldg16(sp + pc) : make_uint4(0, 0, 0, 0);
-        rd[k] = in ? ldg16(sd + pc) : make_uint4(0, 0, 0, 0);
+        rp[k] = in ? ldg16(GP(g.bnd, sp + pc)) : make_uint4(0, 0, 0, 0);
+        rd[k] = in ? ldg16(GP(g.bnd, sd + pc)) : make_uint4(0, 0, 0, 0);
     }
     const T *pcol = reinterpret_cast<const T *>(p.Scols) + R * G;
     const T *dpcol = reinterpret_cast<const T *>(p.S2cols) + R * G;
@@ -857,8 +859,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_glob_reg(con
 #pragma unroll
     for (int k = 0; k < kColsPerLane; ++k) {
         const int q = lane + 32 * k;
-        pv[k] = q < G ? ld(pcol + q) : 0.f;
-        dv[k] = q < G ? ld(dpcol + q) : 0.f;
+        pv[k] = q < G ? ld(GP(g.bnd, pcol + q)) : 0.f;
+        dv[k] = q < G ? ld(GP(g.bnd, dpcol + q)) : 0.f;
     }
     float xp[NCH * N], yd[NCH * N];
     uint64_t d2 = f2(0.f, 0.f);
@@ -897,12 +899,12 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_bwd_glob_reg(con
         for (int u = 0; u < N; u += 2)
             f2split(mul2(f2(xp[k * N + u], xp[k * N + u + 1]), add2(f2(yd[k * N + u], yd[k * N + u + 1]), nd2)),
                     x[u], x[u + 1]);
-        store_piece<T>(dst, pc, rw, x);
+        store_piece<T>(g, dst, pc, rw, x);
     }
 #pragma unroll
     for (int k = 0; k < kColsPerLane; ++k) {
         const int q = lane + 32 * k;
-        if (q < G) dscol[q] = Elt<T>::from_f(pv[k] * (dv[k] - delta));
+        if (q < G) *GP(g.bnd, dscol + q) = Elt<T>::from_f(pv[k] * (dv[k] - delta));
     }
 }
 
@@ -928,7 +930,7 @@ __global__ void __launch_bounds__(kWideThreads) k_glob_rows_wide(const SoftmaxGl
         for (int k = 0; k < NCH; ++k) {
             const int pc = tid + kWideThreads * k;
             float x[N];
-            unpack<T>(pc < np ? ldg16(x4 + pc) : make_uint4(0, 0, 0, 0), x);
+            unpack<T>(pc < np ? ldg16(GP(g.bnd, x4 + pc)) : make_uint4(0, 0, 0, 0), x);
 #pragma unroll
             for (int u = 0; u < N; ++u) {
                 xs[k * N + u] = pc < np ? x[u] : -INFINITY;
@@ -952,9 +954,9 @@ __global__ void __launch_bounds__(kWideThreads) k_glob_rows_wide(const SoftmaxGl
             float y[N];
 #pragma unroll
             for (int u = 0; u < N; ++u) y[u] = xs[k * N + u] * inv;
-            y4[pc] = pack<T>(y);
+            *GP(g.bnd, y4 + pc) = pack<T>(y);
         }
-        if (p.lse && tid == 0) p.lse[(W / gl.G) * g.n + gl.idx[W % gl.G]] = m + logf(z);
+        if (p.lse && tid == 0) *GP(g.bnd, p.lse + (W / gl.G) * g.n + gl.idx[W % gl.G]) = m + logf(z);
     } else {
         const uint4 *d4 = reinterpret_cast<const uint4 *>(p.S2rows) + W * np;
         float ys[NCH * N];
@@ -963,8 +965,8 @@ __global__ void __launch_bounds__(kWideThreads) k_glob_rows_wide(const SoftmaxGl
         for (int k = 0; k < NCH; ++k) {
             const int pc = tid + kWideThreads * k;
             float x[N], y[N];
-            unpack<T>(pc < np ? ldg16(x4 + pc) : make_uint4(0, 0, 0, 0), x);
-            unpack<T>(pc < np ? ldg16(d4 + pc) : make_uint4(0, 0, 0, 0), y);
+            unpack<T>(pc < np ? ldg16(GP(g.bnd, x4 + pc)) : make_uint4(0, 0, 0, 0), x);
+            unpack<T>(pc < np ? ldg16(GP(g.bnd, d4 + pc)) : make_uint4(0, 0, 0, 0), y);
 #pragma unroll
             for (int u = 0; u < N; ++u) {
                 xs[k * N + u] = x[u];
@@ -980,7 +982,7 @@ __global__ void __launch_bounds__(kWideThreads) k_glob_rows_wide(const SoftmaxGl
             float y[N];
 #pragma unroll
             for (int u = 0; u < N; ++u) y[u] = xs[k * N + u] * (ys[k * N + u] - delta);
-            y4[pc] = pack<T>(y);
+            *GP(g.bnd, y4 + pc) = pack<T>(y);
         }
     }
 }

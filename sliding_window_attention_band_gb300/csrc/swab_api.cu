@@ -13,10 +13,18 @@
 
 #include "swab_internal.h"
 
+static constexpr unsigned kSwabFile = 10;   // site id of the bounds checks
+
 namespace swab {
 
 // The device status word: bit k set = a kernel raised swab_status k.
 __device__ unsigned g_status_word;
+
+// Bounds-checked build: the first access a kernel found outside the call's
+// extents (site + 1, address, bytes) and the scratch line such accesses are
+// redirected to.  Present in both builds so the report reads zeros here.
+__device__ unsigned long long g_bounds_rec[3];
+__device__ __align__(256) unsigned char g_bounds_sink[256];
 
 namespace {
 
@@ -36,9 +44,22 @@ __global__ void k_selftest_wait(unsigned *err, unsigned long long limit_ns) {
     __syncthreads();
 }
 
+#if SWAB_BOUNDS_CHECK
+// Self-test of the bounds checks: the extent handed in covers buf[0, 64);
+// lane l stores to buf[l] (inside) and to buf[64 + l] (valid memory outside
+// the extent), both through the check.
+__device__ float g_selftest_buf[128];
+
+__global__ void k_selftest_bounds(const Bounds b, float *buf) {
+    const int l = threadIdx.x;
+    *GP(b, buf + l) = (float)(l + 1);
+    *GP(b, buf + 64 + l) = (float)(l + 1000);
+}
+#endif
+
 const char *const kStatusNames[] = {
     "SWAB_OK", "SWAB_ERR_INVALID_ARG", "SWAB_ERR_UNSUPPORTED",
-    "SWAB_ERR_MISALIGNED", "SWAB_ERR_CUDA", "SWAB_ERR_TIMEOUT",
+    "SWAB_ERR_MISALIGNED", "SWAB_ERR_CUDA", "SWAB_ERR_TIMEOUT", "SWAB_ERR_BOUNDS",
 };
 
 size_t elt_size(DType dt) { return dt == kF32 ? 4 : 2; }
@@ -136,6 +157,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
+#if SWAB_BOUNDS_CHECK
+bool map_fits(const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides, size_t es);
+#endif
+
 // One map per residue r: rows r, r+s, ... of every slice of a [BH, n, 64]
 // tensor; box = 64 elements x box_rows rows, 128-byte swizzle, zero fill
 // outside the residue's rows.
@@ -155,6 +180,9 @@ bool build_rows_maps(TmapSet *set, const void *base, const Geom &g, DType dt, in
         cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
         cuuint32_t estr[3] = {1, 1, 1};
         void *ptr = const_cast<char *>(static_cast<const char *>(base)) + (size_t)rr * 64 * es;
+#if SWAB_BOUNDS_CHECK
+        if (!map_fits(ptr, 3, dims, strides, es)) return false;
+#endif
         CUresult res = enc(&set->m[r], ty, 3, ptr, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -201,6 +229,9 @@ bool build_dense_maps(TmapSet *set, const void *base, const Geom &g, DType dt, i
         }
         cuuint32_t estr[4] = {1, 1, 1, 1};
         void *ptr = const_cast<char *>(static_cast<const char *>(base)) + first;
+#if SWAB_BOUNDS_CHECK
+        if (!map_fits(ptr, 4, dims, strides, es)) return false;
+#endif
         CUresult res = enc(&set->m[r], ty, 4, ptr, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -224,6 +255,9 @@ bool build_acc_maps(TmapSet *set, float *base, const Geom &g) {
         cuuint64_t strides[2] = {(cuuint64_t)g.s * 64 * 4, (cuuint64_t)g.n * 64 * 4};
         cuuint32_t box[3] = {32, 128, 1};
         cuuint32_t estr[3] = {1, 1, 1};
+#if SWAB_BOUNDS_CHECK
+        if (!map_fits(base + (size_t)rr * 64, 3, dims, strides, 4)) return false;
+#endif
         CUresult res = enc(&set->m[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base + (size_t)rr * 64, dims,
                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -247,7 +281,91 @@ unsigned *status_word() {
     return cache[dev];
 }
 
-swab_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SWAB_OK : SWAB_ERR_CUDA; }
+// ---------------------------------------------------------------------------
+// Extents of a call's buffers (bounds-checked build).  Each entry point lists
+// its buffers with the byte sizes the descriptor gives them; the list goes
+// into the kernels' arguments and, for the tensor maps' footprints, into a
+// thread-local copy.  In the regular build SWAB_BOUNDS is SWAB_OK.
+// ---------------------------------------------------------------------------
+struct Extent {
+    const void *p;
+    size_t bytes;
+};
+
+size_t round16(size_t bytes) { return (bytes + 15) / 16 * 16; }
+
+// Byte sizes of a call's buffers as the descriptor lays them out.
+size_t bh_n(const swab_desc *d) { return (size_t)d->b * d->h * d->n; }
+size_t esize(const swab_desc *d) { return d->dtype == SWAB_F32 ? 4 : 2; }
+// dense [b, h, n, hd], or rows of [b, n, rs] with this head block the last
+size_t dense_bytes(const swab_desc *d, long long rs) {
+    if (rs == 0) return bh_n(d) * d->head_dim * esize(d);
+    return ((size_t)d->b * d->n - 1) * (size_t)rs * esize(d) + (size_t)d->h * d->head_dim * esize(d);
+}
+// band [b, h, n, D], readable to the next 16-byte boundary
+size_t band_bytes(const swab_desc *d) {
+    return round16(bh_n(d) * ((size_t)d->w + d->w_upper + 1) * esize(d));
+}
+size_t glob_bytes(const swab_desc *d) { return bh_n(d) * (size_t)d->n_global * esize(d); }
+size_t rows_f32_bytes(const swab_desc *d) { return bh_n(d) * 4; }
+size_t kbias_bytes(const swab_desc *d) { return (size_t)d->b * d->n * 4; }
+// the companions of band tensors (null entries are skipped)
+Extent gcols(const swab_desc *d, const swab_glob *q) { return {d->n_global > 0 && q ? q->cols : nullptr, glob_bytes(d)}; }
+Extent grows(const swab_desc *d, const swab_glob *q) { return {d->n_global > 0 && q ? q->rows : nullptr, glob_bytes(d)}; }
+
+#if SWAB_BOUNDS_CHECK
+thread_local Bounds t_bounds;        // the current call's extents
+thread_local bool t_map_overhang;    // one of its tensor maps overhung them
+
+swab_status set_bounds(Bounds *b, std::initializer_list<Extent> ext) {
+    t_map_overhang = false;
+    Bounds nb{};
+    for (const Extent &e : ext) {
+        if (!e.p || e.bytes == 0) continue;
+        if (nb.n == kBoundsMax) return SWAB_ERR_UNSUPPORTED;
+        nb.lo[nb.n] = reinterpret_cast<unsigned long long>(e.p);
+        nb.hi[nb.n] = nb.lo[nb.n] + e.bytes;
+        ++nb.n;
+    }
+    void *rec = nullptr, *sink = nullptr;
+    if (cudaGetSymbolAddress(&rec, g_bounds_rec) != cudaSuccess ||
+        cudaGetSymbolAddress(&sink, g_bounds_sink) != cudaSuccess)
+        return SWAB_ERR_CUDA;
+    nb.err = status_word();
+    if (!nb.err) return SWAB_ERR_CUDA;
+    nb.rec = static_cast<unsigned long long *>(rec);
+    nb.sink = sink;
+    *b = nb;
+    t_bounds = nb;
+    return SWAB_OK;
+}
+
+// The bytes a tensor map can address, [base, base + (dims[0]-1) es +
+// sum_k (dims[k]-1) strides[k-1] + es), lie inside one extent of the call.
+bool map_fits(const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides, size_t es) {
+    unsigned long long last = (dims[0] - 1) * es;
+    for (int k = 1; k < rank; ++k) last += (dims[k] - 1) * strides[k - 1];
+    const unsigned long long lo = reinterpret_cast<unsigned long long>(base), hi = lo + last + es;
+    for (int k = 0; k < t_bounds.n; ++k)
+        if (lo >= t_bounds.lo[k] && hi <= t_bounds.hi[k]) return true;
+    t_map_overhang = true;
+    return false;
+}
+#define SWAB_BOUNDS(target, ...) ::swab::set_bounds((target), {__VA_ARGS__})
+#else
+#define SWAB_BOUNDS(target, ...) SWAB_OK
+#endif
+
+// The status of a failed CUDA step: SWAB_ERR_BOUNDS when a tensor map of the
+// call overhung its extents (checked build), else SWAB_ERR_CUDA.
+swab_status fail_cuda() {
+#if SWAB_BOUNDS_CHECK
+    if (t_map_overhang) return SWAB_ERR_BOUNDS;
+#endif
+    return SWAB_ERR_CUDA;
+}
+
+swab_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SWAB_OK : fail_cuda(); }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
@@ -296,6 +414,9 @@ swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, co
     GlobArgs gl;
     if ((s = check_globals(desc, {Bg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({Bd, Y, X})) != SWAB_OK) return s;
+    if ((s = SWAB_BOUNDS(&g.bnd, {Bd, band_bytes(desc)}, gcols(desc, Bg), grows(desc, Bg), {Y, dense_bytes(desc, 0)},
+                         {X, dense_bytes(desc, 0)})) != SWAB_OK)
+        return s;
     cudaStream_t st = as_stream(stream);
     cudaError_t e;
     if (dt == kF32) {
@@ -308,9 +429,9 @@ swab_status band_t_common(const swab_desc *desc, float alpha, const void *Bd, co
         }
     } else {
         TmapSet mapY;
-        if (!build_rows_maps(&mapY, Y, g, dt, kGatherBoxRows)) return SWAB_ERR_CUDA;
+        if (!build_rows_maps(&mapY, Y, g, dt, kGatherBoxRows)) return fail_cuda();
         unsigned *err = status_word();
-        if (!err) return SWAB_ERR_CUDA;
+        if (!err) return fail_cuda();
         GatherArgs a{g, alpha, Bd, X, err, gl, gl.G > 0 ? Bg->rows : nullptr, Y};
         e = launch_band_gather_tc(dt, true, mapY, a, st);
     }
@@ -373,21 +494,61 @@ SWAB_API const char *swab_status_string(swab_status status) {
 SWAB_API swab_status swab_selftest_wait_timeout(uint32_t limit_us, void *stream) {
     if (limit_us == 0 || limit_us > 1000000u) return SWAB_ERR_INVALID_ARG;
     unsigned *err = status_word();
-    if (!err) return SWAB_ERR_CUDA;
+    if (!err) return fail_cuda();
     k_selftest_wait<<<1, 32, 0, as_stream(stream)>>>(err, 1000ull * limit_us);
     return from_cuda(cudaGetLastError());
 }
 
+SWAB_API int32_t swab_bounds_checked(void) { return SWAB_BOUNDS_CHECK ? 1 : 0; }
+
+SWAB_API swab_status swab_bounds_report(uint64_t *out, int32_t reset) {
+    if (!out) return SWAB_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SWAB_ERR_CUDA;
+    unsigned long long rec[3] = {0, 0, 0};
+    if (cudaMemcpyFromSymbol(rec, g_bounds_rec, sizeof(rec)) != cudaSuccess) return SWAB_ERR_CUDA;
+    for (int k = 0; k < 3; ++k) out[k] = rec[k];
+    if (reset) {
+        const unsigned long long zero[3] = {0, 0, 0};
+        if (cudaMemcpyToSymbol(g_bounds_rec, zero, sizeof(zero)) != cudaSuccess) return SWAB_ERR_CUDA;
+    }
+    return SWAB_OK;
+}
+
+SWAB_API swab_status swab_selftest_bounds(void *stream) {
+#if SWAB_BOUNDS_CHECK
+    void *buf = nullptr;
+    if (cudaGetSymbolAddress(&buf, g_selftest_buf) != cudaSuccess) return SWAB_ERR_CUDA;
+    Bounds b;
+    const swab_status s = set_bounds(&b, {{buf, 64 * sizeof(float)}});
+    if (s != SWAB_OK) return s;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(buf, 0, 128 * sizeof(float), st) != cudaSuccess) return SWAB_ERR_CUDA;
+    k_selftest_bounds<<<1, 32, 0, st>>>(b, static_cast<float *>(buf));
+    if (cudaGetLastError() != cudaSuccess) return SWAB_ERR_CUDA;
+    float host[128];
+    if (cudaMemcpyAsync(host, buf, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return SWAB_ERR_CUDA;
+    // the stores inside the extent landed, the ones outside it did not
+    for (int l = 0; l < 32; ++l)
+        if (host[l] != (float)(l + 1) || host[64 + l] != 0.f) return SWAB_ERR_BOUNDS;
+    return SWAB_OK;
+#else
+    (void)stream;
+    return SWAB_ERR_UNSUPPORTED;
+#endif
+}
+
 SWAB_API swab_status swab_device_status(int32_t *flags, int32_t reset) {
     if (!flags) return SWAB_ERR_INVALID_ARG;
-    if (cudaDeviceSynchronize() != cudaSuccess) return SWAB_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail_cuda();
     unsigned v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return SWAB_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return fail_cuda();
     *flags = static_cast<int32_t>(v);
     if (reset) {
         const unsigned zero = 0;
         if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess)
-            return SWAB_ERR_CUDA;
+            return fail_cuda();
     }
     return SWAB_OK;
 }
@@ -402,6 +563,9 @@ SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, 
     GlobArgs gl;
     if ((s = check_globals(desc, {Sg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({A, B, S})) != SWAB_OK) return s;
+    if ((s = SWAB_BOUNDS(&g.bnd, {A, dense_bytes(desc, 0)}, {B, dense_bytes(desc, 0)}, {S, band_bytes(desc)},
+                         gcols(desc, Sg), grows(desc, Sg))) != SWAB_OK)
+        return s;
     cudaStream_t st = as_stream(stream);
     cudaError_t e;
     if (dt == kF32) {
@@ -411,9 +575,9 @@ SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, 
         TmapSet mapA, mapB;
         if (!build_rows_maps(&mapA, A, g, dt, kQKBoxRows) ||
             !build_rows_maps(&mapB, B, g, dt, kQKBoxRows))
-            return SWAB_ERR_CUDA;
+            return fail_cuda();
         unsigned *err = status_word();
-        if (!err) return SWAB_ERR_CUDA;
+        if (!err) return fail_cuda();
         QKArgs a{g, alpha, S, err};
         e = launch_band_qk_tc(dt, mapA, mapB, a, st);
     }
@@ -427,9 +591,9 @@ SWAB_API swab_status band_qk(const swab_desc *desc, float alpha, const void *A, 
             g1.s = 1;
             g1.nsub = g.n;
             TmapSet ma, mb;
-            if (!build_rows_maps(&ma, A, g1, dt, 128) || !build_rows_maps(&mb, B, g1, dt, 128)) return SWAB_ERR_CUDA;
+            if (!build_rows_maps(&ma, A, g1, dt, 128) || !build_rows_maps(&mb, B, g1, dt, 128)) return fail_cuda();
             a.err = status_word();
-            if (!a.err) return SWAB_ERR_CUDA;
+            if (!a.err) return fail_cuda();
             e = launch_glob_scores_tc(dt, ma, mb, a, st);
         }
     }
@@ -447,6 +611,10 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
     if ((s = check_globals(desc, {Sg, Pg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({S, P})) != SWAB_OK) return s;
     if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
+    if ((s = SWAB_BOUNDS(&g.bnd, {S, band_bytes(desc)}, {P, band_bytes(desc)}, gcols(desc, Sg), grows(desc, Sg),
+                         gcols(desc, Pg), grows(desc, Pg), {lse, rows_f32_bytes(desc)},
+                         {g.kbias, kbias_bytes(desc)})) != SWAB_OK)
+        return s;
     if (gl.G > 0) {
         SoftmaxGlobArgs a{g, gl, S, nullptr, Sg->cols, nullptr, Sg->rows, nullptr,
                           P, Pg->cols, Pg->rows, lse};
@@ -476,6 +644,9 @@ SWAB_API swab_status add_bias_transpose(const swab_desc *desc, int32_t M, const 
     // Y must not overlap X
     const char *x0 = static_cast<const char *>(X), *y0 = static_cast<const char *>(Y);
     if (x0 < y0 + total && y0 < x0 + total) return SWAB_ERR_INVALID_ARG;
+    if ((s = SWAB_BOUNDS(&a.bnd, {X, (size_t)total}, {bias, (size_t)(a.M * a.h * row_bytes)}, {Y, (size_t)total})) !=
+        SWAB_OK)
+        return s;
     return from_cuda(launch_add_bias_transpose(dt, a, as_stream(stream)));
 }
 
@@ -516,6 +687,12 @@ SWAB_API swab_status global_attention(const swab_desc *desc, float scale, const 
     a.Og = Og;
     a.lseg = lseg;
     a.ws = static_cast<float *>(workspace);
+    {
+        const size_t gq = (size_t)a.BH * a.G * 64 * elt_size(dt), kv = (size_t)a.BH * a.n * 64 * elt_size(dt);
+        if ((s = SWAB_BOUNDS(&a.bnd, {Qg, gq}, {Kg, kv}, {Vg, kv}, {Og, gq}, {lseg, (size_t)a.BH * a.G * 4},
+                             {workspace, global_attention_workspace(desc)})) != SWAB_OK)
+            return s;
+    }
     if (dt == kF32) return from_cuda(launch_global_proj(dt, a, false, as_stream(stream)));
     Geom gk{}, gq{};
     gk.BH = gq.BH = (int)a.BH;
@@ -525,9 +702,9 @@ SWAB_API swab_status global_attention(const swab_desc *desc, float scale, const 
     TmapSet mk, mv, mq;
     if (!build_rows_maps(&mk, Kg, gk, dt, 128) || !build_rows_maps(&mv, Vg, gk, dt, 128) ||
         !build_rows_maps(&mq, Qg, gq, dt, 16))
-        return SWAB_ERR_CUDA;
+        return fail_cuda();
     a.err = status_word();
-    if (!a.err) return SWAB_ERR_CUDA;
+    if (!a.err) return fail_cuda();
     return from_cuda(launch_global_proj_fwd_tc(dt, mk, mv, mq, a, as_stream(stream)));
 }
 
@@ -550,6 +727,12 @@ SWAB_API swab_status global_attention_bwd(const swab_desc *desc, float scale, co
     a.dKg = dKg;
     a.dVg = dVg;
     a.ws = static_cast<float *>(workspace);
+    {
+        const size_t gq = (size_t)a.BH * a.G * 64 * elt_size(dt), kv = (size_t)a.BH * a.n * 64 * elt_size(dt);
+        if ((s = SWAB_BOUNDS(&a.bnd, {Qg, gq}, {Kg, kv}, {Vg, kv}, {Og, gq}, {dOg, gq}, {lseg, (size_t)a.BH * a.G * 4},
+                             {dQg, gq}, {dKg, kv}, {dVg, kv}, {workspace, global_attention_workspace(desc)})) != SWAB_OK)
+            return s;
+    }
     if (dt == kF32) return from_cuda(launch_global_proj(dt, a, true, as_stream(stream)));
     // tensor-core path: [n, 64] slices of Kg, Vg and [G, 64] slices of Qg, dOg
     Geom gk{}, gq{};
@@ -560,9 +743,9 @@ SWAB_API swab_status global_attention_bwd(const swab_desc *desc, float scale, co
     TmapSet mk, mv, mq, mo;
     if (!build_rows_maps(&mk, Kg, gk, dt, 128) || !build_rows_maps(&mv, Vg, gk, dt, 128) ||
         !build_rows_maps(&mq, Qg, gq, dt, 16) || !build_rows_maps(&mo, dOg, gq, dt, 16))
-        return SWAB_ERR_CUDA;
+        return fail_cuda();
     a.err = status_word();
-    if (!a.err) return SWAB_ERR_CUDA;
+    if (!a.err) return fail_cuda();
     return from_cuda(launch_global_proj_bwd_tc(dt, mk, mv, mq, mo, a, as_stream(stream)));
 }
 
@@ -581,6 +764,9 @@ SWAB_API swab_status band_softmax_dropout(const swab_desc *desc, const void *S, 
     if (P && !aligned16(P)) return SWAB_ERR_MISALIGNED;
     if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
     if (g.D > kMaxDropBand) return SWAB_ERR_UNSUPPORTED;
+    if ((s = SWAB_BOUNDS(&g.bnd, {S, band_bytes(desc)}, {P, band_bytes(desc)}, {Pd, band_bytes(desc)},
+                         {lse, rows_f32_bytes(desc)}, {g.kbias, kbias_bytes(desc)})) != SWAB_OK)
+        return s;
     SoftmaxArgs a{g, S, nullptr, P, lse, nullptr, Pd};
     return from_cuda(launch_band_softmax(dt, a, as_stream(stream)));
 }
@@ -595,6 +781,9 @@ SWAB_API swab_status band_pv(const swab_desc *desc, float alpha, const void *P,
     GlobArgs gl;
     if ((s = check_globals(desc, {Pg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({P, V, O})) != SWAB_OK) return s;
+    if ((s = SWAB_BOUNDS(&g.bnd, {P, band_bytes(desc)}, gcols(desc, Pg), grows(desc, Pg), {V, dense_bytes(desc, 0)},
+                         {O, dense_bytes(desc, 0)})) != SWAB_OK)
+        return s;
     cudaStream_t st = as_stream(stream);
     cudaError_t e;
     if (dt == kF32) {
@@ -607,9 +796,9 @@ SWAB_API swab_status band_pv(const swab_desc *desc, float alpha, const void *P,
         }
     } else {
         TmapSet mapV;
-        if (!build_rows_maps(&mapV, V, g, dt, kGatherBoxRows)) return SWAB_ERR_CUDA;
+        if (!build_rows_maps(&mapV, V, g, dt, kGatherBoxRows)) return fail_cuda();
         unsigned *err = status_word();
-        if (!err) return SWAB_ERR_CUDA;
+        if (!err) return fail_cuda();
         GatherArgs a{g, alpha, P, O, err, gl, gl.G > 0 ? Pg->cols : nullptr, V};
         e = launch_band_gather_tc(dt, false, mapV, a, st);
     }
@@ -641,6 +830,10 @@ SWAB_API swab_status band_softmax_bwd(const swab_desc *desc, const void *P, cons
     if ((s = check_globals(desc, {Pg, dPg, dSg}, &gl)) != SWAB_OK) return s;
     if ((s = check_ptrs({P, dP, dS})) != SWAB_OK) return s;
     if (g.drop_t > 0 && g.D > kMaxDropBand) return SWAB_ERR_UNSUPPORTED;
+    if ((s = SWAB_BOUNDS(&g.bnd, {P, band_bytes(desc)}, {dP, band_bytes(desc)}, {dS, band_bytes(desc)}, gcols(desc, Pg),
+                         grows(desc, Pg), gcols(desc, dPg), grows(desc, dPg), gcols(desc, dSg),
+                         grows(desc, dSg))) != SWAB_OK)
+        return s;
     if (gl.G > 0) {
         SoftmaxGlobArgs a{g, gl, P, dP, Pg->cols, dPg->cols, Pg->rows, dPg->rows,
                           dS, dSg->cols, dSg->rows, nullptr};
@@ -659,6 +852,11 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
     if (s != SWAB_OK) return s;
     if ((s = check_ptrs({Q, K, V, O})) != SWAB_OK) return s;
     if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
+    if ((s = SWAB_BOUNDS(&g.bnd, {Q, dense_bytes(desc, g.rs_p)}, {K, dense_bytes(desc, g.rs_p)},
+                         {V, dense_bytes(desc, g.rs_p)}, {O, dense_bytes(desc, g.rs_o)}, {lse, rows_f32_bytes(desc)},
+                         {g.kbias, kbias_bytes(desc)},
+                         {g.dmask, g.dmask ? band_attention_dropout_mask_bytes(desc) : 0})) != SWAB_OK)
+        return s;
     if (desc->n_global > 0) {
         // band keys outside G by the fused kernel, then the global columns
         // merged into local rows (needs lse) and the global rows
@@ -671,9 +869,9 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
         TmapSet mq, mk, mv;
         if (!build_dense_maps(&mq, Q, g, dt, kQKBoxRows, 0) || !build_dense_maps(&mk, K, g, dt, kQKBoxRows, 0) ||
             !build_dense_maps(&mv, V, g, dt, kQKBoxRows, 0))
-            return SWAB_ERR_CUDA;
+            return fail_cuda();
         unsigned *err = status_word();
-        if (!err) return SWAB_ERR_CUDA;
+        if (!err) return fail_cuda();
         AttnArgs a{g, scale, O, lse, err};
         cudaStream_t st = as_stream(stream);
         cudaError_t e = launch_band_attention_glob(dt, mq, mk, mv, a, gl, st);
@@ -682,11 +880,14 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
         gr.n = g.n;
         gr.s = 1;
         GlobalRowsArgs r{g.BH, g.n, scale, Q, K, V, O, lse, gl, err};
+#if SWAB_BOUNDS_CHECK
+        r.bnd = g.bnd;
+#endif
         bool cols_done = false, rows_done = false;
         if (e == cudaSuccess && gl.G <= 64) {
             // the global columns on the tensor cores
             TmapSet mq1;
-            if (!build_rows_maps(&mq1, Q, gr, dt, 128)) return SWAB_ERR_CUDA;
+            if (!build_rows_maps(&mq1, Q, gr, dt, 128)) return fail_cuda();
             e = launch_fused_glob_cols_tc(dt, mq1, r, st);
             cols_done = true;
         }
@@ -696,7 +897,7 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
             // chunk, slice) CTAs fill the GPU
             TmapSet mk1, mv1;
             if (!build_rows_maps(&mk1, K, gr, dt, 128) || !build_rows_maps(&mv1, V, gr, dt, 128))
-                return SWAB_ERR_CUDA;
+                return fail_cuda();
             e = launch_fused_glob_rows_tc(dt, mk1, mv1, r, st);
             rows_done = true;
         }
@@ -712,9 +913,9 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
     if (!build_dense_maps(&mq, Q, g, dt, kQKBoxRows, g.rs_p) ||
         !build_dense_maps(&mk, K, g, dt, kQKBoxRows, g.rs_p) ||
         !build_dense_maps(&mv, V, g, dt, kQKBoxRows, g.rs_p))
-        return SWAB_ERR_CUDA;
+        return fail_cuda();
     unsigned *err = status_word();
-    if (!err) return SWAB_ERR_CUDA;
+    if (!err) return fail_cuda();
     AttnArgs a{g, scale, O, lse, err};
     return from_cuda(launch_band_attention_tc(dt, mq, mk, mv, a, as_stream(stream)));
 }
@@ -793,13 +994,13 @@ static swab_status bwd_with_globals(const swab_desc *desc, const Geom &g, DType 
     a.cdK = reinterpret_cast<float *>(ws + L.cdK);
     a.cdV = reinterpret_cast<float *>(ws + L.cdV);
     a.err = status_word();
-    if (!a.err) return SWAB_ERR_CUDA;
+    if (!a.err) return fail_cuda();
     // band pass: the per-residue maps
     TmapSet mq, mk, mv, mo, macc;
     if (!build_dense_maps(&mq, a.Q, g, dt, kQKBoxRows, 0) || !build_dense_maps(&mk, a.K, g, dt, kQKBoxRows, 0) ||
         !build_dense_maps(&mv, a.V, g, dt, kQKBoxRows, 0) || !build_dense_maps(&mo, a.dO, g, dt, kQKBoxRows, 0) ||
         !build_acc_maps(&macc, a.dqacc, g))
-        return SWAB_ERR_CUDA;
+        return fail_cuda();
     // global columns: Q, dO and the accumulator with stride 1; the gathered
     // global keys / values as [b, h, 128 x ceil(G / 128), 64]
     Geom g1 = g;
@@ -813,7 +1014,7 @@ static swab_status bwd_with_globals(const swab_desc *desc, const Geom &g, DType 
     if (!build_dense_maps(&mq1, a.Q, g1, dt, kQKBoxRows, 0) || !build_dense_maps(&mo1, a.dO, g1, dt, kQKBoxRows, 0) ||
         !build_dense_maps(&mkc, gb.KG, gk, dt, kQKBoxRows, 0) || !build_dense_maps(&mvc, gb.VG, gk, dt, kQKBoxRows, 0) ||
         !build_acc_maps(&macc1, a.dqacc, g1))
-        return SWAB_ERR_CUDA;
+        return fail_cuda();
     // global rows: the global-query backward with Kg = K, Vg = V
     GlobalProjArgs gp{};
     gp.BH = g.BH;
@@ -831,6 +1032,9 @@ static swab_status bwd_with_globals(const swab_desc *desc, const Geom &g, DType 
     gp.dVg = const_cast<void *>(a.gdV);
     gp.ws = reinterpret_cast<float *>(ws + L.gp);
     gp.err = a.err;
+#if SWAB_BOUNDS_CHECK
+    gp.bnd = g.bnd;
+#endif
     Geom gkr{}, gqr{};
     gkr.BH = gqr.BH = g.BH;
     gkr.s = gqr.s = 1;
@@ -839,7 +1043,7 @@ static swab_status bwd_with_globals(const swab_desc *desc, const Geom &g, DType 
     TmapSet gmk, gmv, gmq, gmo;
     if (!build_rows_maps(&gmk, a.K, gkr, dt, 128) || !build_rows_maps(&gmv, a.V, gkr, dt, 128) ||
         !build_rows_maps(&gmq, gb.Qg, gqr, dt, 16) || !build_rows_maps(&gmo, gb.dOg, gqr, dt, 16))
-        return SWAB_ERR_CUDA;
+        return fail_cuda();
     return from_cuda(launch_band_attention_bwd_glob(dt, mq, mk, mv, mo, macc, mq1, mo1, mkc, mvc, macc1, gl, gb, a,
                                                     gp, gmk, gmv, gmq, gmo, st));
 }
@@ -853,6 +1057,13 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
     swab_status s = check_desc(desc, &g, &dt);
     if (s != SWAB_OK) return s;
     if ((s = check_ptrs({Q, K, V, O, dO, lse, dQ, dK, dV, workspace})) != SWAB_OK) return s;
+    if ((s = SWAB_BOUNDS(&g.bnd, {Q, dense_bytes(desc, g.rs_p)}, {K, dense_bytes(desc, g.rs_p)},
+                         {V, dense_bytes(desc, g.rs_p)}, {O, dense_bytes(desc, g.rs_o)}, {dO, dense_bytes(desc, g.rs_o)},
+                         {lse, rows_f32_bytes(desc)}, {dQ, dense_bytes(desc, g.rs_p)}, {dK, dense_bytes(desc, g.rs_p)},
+                         {dV, dense_bytes(desc, g.rs_p)}, {workspace, band_attention_bwd_workspace(desc)},
+                         {g.kbias, kbias_bytes(desc)},
+                         {g.dmask, g.dmask ? band_attention_dropout_mask_bytes(desc) : 0})) != SWAB_OK)
+        return s;
     cudaStream_t st = as_stream(stream);
     BwdArgs a{g, scale, Q, K, V, O, dO, lse, static_cast<float *>(workspace), dQ, dK, dV, nullptr};
     if (desc->n_global > 0) return bwd_with_globals(desc, g, dt, a, st);
@@ -862,14 +1073,14 @@ SWAB_API swab_status band_attention_bwd(const swab_desc *desc, float scale, cons
         !build_dense_maps(&mk, K, g, dt, kQKBoxRows, g.rs_p) ||
         !build_dense_maps(&mv, V, g, dt, kQKBoxRows, g.rs_p) ||
         !build_dense_maps(&mo, dO, g, dt, kQKBoxRows, g.rs_o))
-        return SWAB_ERR_CUDA;
+        return fail_cuda();
     a.err = status_word();
-    if (!a.err) return SWAB_ERR_CUDA;
+    if (!a.err) return fail_cuda();
     const size_t rows = (size_t)g.BH * g.n;
     a.dqacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                         (rows * sizeof(float) + 255) / 256 * 256);
     TmapSet macc;
-    if (!build_acc_maps(&macc, a.dqacc, g)) return SWAB_ERR_CUDA;
+    if (!build_acc_maps(&macc, a.dqacc, g)) return fail_cuda();
     return from_cuda(launch_band_attention_bwd_fused(dt, mq, mk, mv, mo, macc, a, st));
 }
 
@@ -891,15 +1102,20 @@ SWAB_API swab_status band_attention_bwd_noalloc(const swab_desc *desc, float sca
     float *scratch = nullptr;
     const cudaError_t se = noalloc_delta_scratch(&scratch, st);
     if (se == cudaErrorStreamCaptureUnsupported) return SWAB_ERR_UNSUPPORTED;
-    if (se != cudaSuccess) return SWAB_ERR_CUDA;
+    if (se != cudaSuccess) return fail_cuda();
+    if ((s = SWAB_BOUNDS(&g.bnd, {Q, dense_bytes(desc, 0)}, {K, dense_bytes(desc, 0)}, {V, dense_bytes(desc, 0)},
+                         {O, dense_bytes(desc, 0)}, {dO, dense_bytes(desc, 0)}, {lse, rows_f32_bytes(desc)},
+                         {dQ, dense_bytes(desc, 0)}, {dK, dense_bytes(desc, 0)}, {dV, dense_bytes(desc, 0)},
+                         {scratch, (size_t)SWAB_NOALLOC_MAX_ROWS * sizeof(float)})) != SWAB_OK)
+        return s;
     BwdArgs a{g, scale, Q, K, V, O, dO, lse, scratch, dQ, dK, dV, nullptr};
     if (dt == kF32) return from_cuda(launch_band_attention_bwd_f32(a, st));
     TmapSet mq, mk, mv, mo;
     if (!build_rows_maps(&mq, Q, g, dt, kQKBoxRows) || !build_rows_maps(&mk, K, g, dt, kQKBoxRows) ||
         !build_rows_maps(&mv, V, g, dt, kQKBoxRows) || !build_rows_maps(&mo, dO, g, dt, kQKBoxRows))
-        return SWAB_ERR_CUDA;
+        return fail_cuda();
     a.err = status_word();
-    if (!a.err) return SWAB_ERR_CUDA;
+    if (!a.err) return fail_cuda();
     return from_cuda(launch_band_attention_bwd_tc(dt, mq, mk, mv, mo, a, st));
 }
 

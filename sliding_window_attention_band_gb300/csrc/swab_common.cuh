@@ -19,6 +19,55 @@ constexpr int kMaxGlobal = SWAB_MAX_GLOBAL;
 
 // Bits of the device status word (bit k <-> swab_status k).
 constexpr unsigned kErrTimeout = 1u << SWAB_ERR_TIMEOUT;
+constexpr unsigned kErrBounds = 1u << SWAB_ERR_BOUNDS;
+
+// ---------------------------------------------------------------------------
+// Bounds checks (SWAB_BOUNDS_CHECK=1 builds).  Every plain global access of a
+// kernel names its address through GP(bounds, pointer) (or GPN with an
+// explicit byte count for vector and bulk accesses).  In the regular build
+// the macro is the pointer itself.  In the checked build it tests the bytes
+// [p, p + size) against the call's buffer extents, which the host writes into
+// the kernel arguments; outside all of them the access is redirected to a
+// scratch line of the library (a store lands there, a load reads it), the
+// status word gets SWAB_ERR_BOUNDS and the first such site is recorded.
+// ---------------------------------------------------------------------------
+#ifndef SWAB_BOUNDS_CHECK
+#define SWAB_BOUNDS_CHECK 0
+#endif
+
+constexpr int kBoundsMax = 24;
+
+struct Bounds {
+    int n;                                  // extents in use
+    unsigned long long lo[kBoundsMax];      // byte ranges [lo, hi)
+    unsigned long long hi[kBoundsMax];
+    unsigned *err;                          // device status word
+    unsigned long long *rec;                // first miss: site + 1, address, bytes
+    void *sink;                             // 256-byte scratch line
+};
+
+#if SWAB_BOUNDS_CHECK
+static __device__ __noinline__ void *bounds_check(const Bounds *b, const void *p, unsigned bytes, unsigned site) {
+    const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+    for (int k = 0; k < b->n; ++k)
+        if (a >= b->lo[k] && a + bytes <= b->hi[k]) return const_cast<void *>(p);
+    atomicOr(b->err, kErrBounds);
+    if (atomicCAS(b->rec, 0ull, (unsigned long long)site + 1ull) == 0ull) {
+        b->rec[1] = a;
+        b->rec[2] = bytes;
+    }
+    return b->sink;
+}
+template <typename P>
+__device__ __forceinline__ P *gp_check(const Bounds &b, P *p, unsigned bytes, unsigned site) {
+    return (P *)bounds_check(&b, (const void *)p, bytes, site);
+}
+#define GPN(B, p, bytes) ::swab::gp_check((B), (p), (unsigned)(bytes), (kSwabFile << 16) | (unsigned)__LINE__)
+#define GP(B, p) GPN(B, p, sizeof(*(p)))
+#else
+#define GPN(B, p, bytes) (p)
+#define GP(B, p) (p)
+#endif
 
 // A wait gives up after this long (the kernels here run for micro- to
 // milliseconds; a wait this long means a lost arrival).
@@ -50,6 +99,9 @@ struct Geom {
     // keep-bit cache of the fused dropout, or null: dm_nb words a query row
     uint32_t *dmask;
     int dm_nb;
+#if SWAB_BOUNDS_CHECK
+    Bounds bnd;   // the call's buffer extents (checked build)
+#endif
 };
 
 // Element offset of dense row R = bh * n + i under row stride rs (R < 2^31:

@@ -154,6 +154,9 @@ struct GlobalRowsArgs {   // dense rows of the global queries (fused forward)
     float *lse;              // [BH, n]
     GlobArgs gl;
     unsigned *err;           // device status word (tensor-core kernel)
+#if SWAB_BOUNDS_CHECK
+    Bounds bnd;              // the call's buffer extents (checked build)
+#endif
 };
 // global columns on the tensor cores (G <= 64): map of Q (128-row boxes),
 // contiguous [BH, n, 64]
@@ -216,6 +219,9 @@ struct BiasTransposeArgs {   // AddBiasTranspose
     long long rows;    // b * n
     long long b, n, h, M;
     long long cpr;     // 16-byte chunks per head row (hd * size / 16)
+#if SWAB_BOUNDS_CHECK
+    Bounds bnd;        // the call's buffer extents (checked build)
+#endif
 };
 cudaError_t launch_add_bias_transpose(DType dt, const BiasTransposeArgs &a, cudaStream_t st);
 
@@ -232,6 +238,9 @@ struct GlobalProjArgs {   // global queries with their own projections
     float *ws;             // workspace (partials)
     int nchunks;           // set by the launcher
     unsigned *err;         // device status word (tensor-core backward)
+#if SWAB_BOUNDS_CHECK
+    Bounds bnd;            // the call's buffer extents (checked build)
+#endif
 };
 size_t global_proj_workspace_bytes(long long BH, int G, int n);
 cudaError_t launch_global_proj(DType dt, const GlobalProjArgs &a, bool bwd, cudaStream_t st);

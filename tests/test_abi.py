@@ -1,7 +1,8 @@
 """C-ABI boundary tests that need no GPU.
 
 * the library builds, loads on a machine without a driver, and exports every
-  function include/swab.h declares;
+  function include/swab.h declares -- the regular build and the
+  bounds-checked one (which says so; the regular one says it is not);
 * invalid arguments come back as the documented status before any CUDA call
   (the pointers below are fake, never dereferenced: validation rejects the
   call first).
@@ -45,6 +46,20 @@ def test_header_lists_every_binding():
 def test_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
+
+
+def test_bounds_checked_build_exports_and_identifies_itself(lib):
+    swab_build.build_all()
+    checked = ctypes.CDLL(swab_build.LIB_BOUNDS)   # loading needs no driver
+    for name in declared_functions():
+        assert hasattr(checked, name), name
+    checked.swab_bounds_checked.restype = ctypes.c_int32
+    lib.swab_bounds_checked.restype = ctypes.c_int32
+    assert checked.swab_bounds_checked() == 1
+    assert lib.swab_bounds_checked() == 0
+    # the report validates its argument before any CUDA call
+    assert checked.swab_bounds_report(None, 0) == INVALID
+    assert lib.swab_bounds_report(None, 0) == INVALID
 
 
 def test_version_and_status_strings(lib):
