@@ -20,6 +20,11 @@ loads the checked build, and requires
 
 No case addresses memory outside its buffers in either build: the checked
 build would record such an access instead of making it.
+
+The whole GPU suite can also run on the checked build (SWAB_BOUNDS_CHECK=1 in
+the environment of pytest): every module's status-word guard then fails on an
+out-of-bounds access.  The two tests here compare the two builds and are
+skipped in that mode.
 """
 import os
 import subprocess
@@ -31,7 +36,9 @@ import torch
 import sliding_window_attention_band_gb300 as swab
 from sliding_window_attention_band_gb300 import build as swab_build
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(os.environ.get("SWAB_BOUNDS_CHECK") == "1",
+                                 reason="compares the checked build with the regular one in this process")]
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 BOUNDS_BIT = 1 << 6          # SWAB_ERR_BOUNDS in the device status word

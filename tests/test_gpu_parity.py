@@ -118,6 +118,13 @@ UNIT_CASES = [  # BH, n, w, w_upper, dilation, dtype
     (2, 200, 20, 20, 0, torch.float32),
     (1, 333, 7, 30, 2, torch.float32),
     (2, 900, 9, 9, 2, torch.float16),     # dilated, s*D - 1 a multiple of 8: one gather shift
+    # degenerate and extreme geometries
+    (2, 1, 0, 0, 0, torch.float16),       # n = 1, D = 1: one key per row
+    (3, 257, 0, 0, 0, torch.bfloat16),    # D = 1: the diagonal alone
+    (1, 20, 2, 3, 15, torch.float16),     # the largest dilation (s = 16)
+    (2, 10, 4, 4, 15, torch.bfloat16),    # n < s: six residues empty, one row per residue
+    (1, 100, 256, 256, 0, torch.float16), # a window wider than the sequence
+    (2, 50, 0, 0, 1, torch.float32),      # fp32, D = 1, dilated
 ]
 
 
@@ -215,6 +222,8 @@ PROBE_CASES = [  # BH, n, w, w_upper, dilation, dtype
     (1, 4100, 256, 256, 3, torch.bfloat16),
     (1, 2049, 500, 0, 1, torch.float16),
     (1, 1500, 5, 5, 2, torch.bfloat16),   # dilated, s*D - 1 a multiple of 8
+    (1, 10, 4, 4, 15, torch.float16),     # n < s: empty residues, the largest dilation
+    (2, 1, 0, 0, 0, torch.bfloat16),      # n = 1
 ]
 
 
@@ -415,3 +424,47 @@ def test_band_attention_bwd_config(cfg, slices):
     Q, K, V, dO = workload_inputs(wl)
     check_fused_bwd(swab.Desc.from_workload(wl), Q, K, V, dO, wl.scale, slices,
                     wl.dtype == torch.float32)
+
+
+# ---------------------------------------------------------------------------
+# rows with a single key: the softmax weight is exactly 1, so the attention
+# returns V exactly and passes dO straight to dV (closed forms, bitwise)
+# ---------------------------------------------------------------------------
+SINGLE_KEY_CASES = [  # BH, n, w, w_upper, dilation: every row's band holds only its own key
+    (2, 1, 0, 0, 0),      # n = 1
+    (3, 300, 0, 0, 0),    # D = 1
+    (2, 12, 3, 5, 15),    # n <= s: one row per residue
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32],
+                         ids=lambda t: str(t).split(".")[-1])
+@pytest.mark.parametrize("case", SINGLE_KEY_CASES, ids=lambda c: "BH{}-n{}-w{}-wu{}-d{}".format(*c))
+def test_single_key_rows_return_v(case, dtype):
+    BH, n, w, wu, dil = case
+    d = mkdesc(BH, n, w, wu, dil, dtype)
+    Q, K, V, dO = dev(*seeded_qkvo(BH, n, 64, dtype, seed=29))
+    # fused forward and backward
+    O = empty_dense(d)
+    lse = torch.empty((BH, n), dtype=torch.float32, device="cuda")
+    swab.band_attention(d, 0.125, Q, K, V, O, lse)
+    dQ, dK, dV = (empty_dense(d) for _ in range(3))
+    ws = torch.empty(swab.band_attention_bwd_workspace(d) // 4, dtype=torch.float32, device="cuda")
+    swab.band_attention_bwd(d, 0.125, Q, K, V, O, dO, lse, dQ, dK, dV, ws)
+    # the materialised forward
+    S, P = empty_band(d), empty_band(d)
+    Om = empty_dense(d)
+    swab.band_qk(d, 0.125, Q, K, S)
+    swab.band_softmax(d, S, P)
+    swab.band_pv(d, 1.0, P, V, Om)
+    torch.cuda.synchronize()
+    assert torch.equal(O, V) and torch.equal(Om, V)
+    assert torch.equal(dV, dO)
+    m = torch.from_numpy(valid_mask(n, w, wu, dil))   # the diagonal slot alone
+    assert torch.all(P.cpu()[:, m] == 1) and torch.all(P.cpu()[:, ~m] == 0)
+    # lse is the row's own scaled score; dS = P (dP - delta) = 0 up to the
+    # rounding of two dot products of the same vectors
+    qk = (Q.double() * K.double()).sum(-1) * 0.125
+    assert torch.allclose(lse.double(), qk, rtol=1e-5, atol=2e-3 if dtype != torch.float32 else 1e-5)
+    for g in (dQ, dK):
+        assert float(g.double().abs().max()) <= 2e-3
