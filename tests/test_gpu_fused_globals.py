@@ -149,6 +149,18 @@ def test_fused_backward_globals_more_than_128():
     check_bwd(d, Q, K, V, dO, 0.125, range(BH))
 
 
+def test_fused_globals_largest_count():
+    """G = 256 global tokens (the largest count), dilated: the forward's
+    global columns and rows off the tensor-core paths' limits, the backward's
+    global columns as two tiles of gathered keys."""
+    BH, n, gidx = 2, 700, tuple(range(0, 512, 2))
+    assert len(gidx) == swab._binding.MAX_GLOBAL
+    d = swab.Desc(1, BH, n, 64, 24, 40, 1, 0.0, torch.bfloat16, gidx)
+    Q, K, V, dO = seeded_qkvo(BH, n, 64, torch.bfloat16, seed=19)
+    check(d, Q, K, V, 0.125, range(BH))
+    check_bwd(d, Q, K, V, dO, 0.125, range(BH))
+
+
 def test_fused_backward_globals_training_workload_sampled():
     """b = 12, h = 12, n = 4096, w = 256, 16 global tokens, bf16 (slices 0, 77, 143)."""
     wl = WORKLOADS[4]

@@ -39,6 +39,8 @@ CASES = [  # BH, n, w, w_upper, dilation, dtype, global idx
     (1, 129, 1, 2, 0, torch.bfloat16, (64,)),
     # more than 64 global tokens: the band products' global term on FFMA
     (1, 700, 30, 30, 0, torch.float16, tuple(range(0, 700, 9))),
+    # the largest number of global tokens (256), dilated
+    (1, 600, 16, 16, 1, torch.bfloat16, tuple(range(0, 512, 2))),
 ]
 
 
