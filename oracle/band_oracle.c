@@ -497,7 +497,6 @@ int orc_attention_fwd(int BH, int n, int hd, int w, int wu, int dil, double scal
                       double *lse, int G, const int *gidx, const double *kbias, uint64_t seed,
                       int drop_t) {
     if (check_geom(BH, n, hd, w, wu, dil)) return -1;
-    if (G > 0 && kbias) return -4;
     if (drop_t < 0 || drop_t > 255 || (G > 0 && drop_t > 0)) return -4;
     const int s_ = dil + 1;
     unsigned char *gm; int *gp;
@@ -549,7 +548,6 @@ int orc_attention_bwd(int BH, int n, int hd, int w, int wu, int dil, double scal
                       const double *dO, double *dQ, double *dK, double *dV, int G,
                       const int *gidx, const double *kbias, uint64_t seed, int drop_t) {
     if (check_geom(BH, n, hd, w, wu, dil)) return -1;
-    if (G > 0 && kbias) return -4;
     if (drop_t < 0 || drop_t > 255 || (G > 0 && drop_t > 0)) return -4;
     const int s_ = dil + 1;
     unsigned char *gm; int *gp;

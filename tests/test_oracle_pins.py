@@ -389,16 +389,26 @@ def torch_attention_bias(Q, K, V, mask, scale, kb):
     return torch.softmax(s, -1) @ V, torch.logsumexp(s, -1)
 
 
-def pin_bias(n, hd, w, wu, d):
+def pin_bias(n, hd, w, wu, d, gidx=()):
     Q, K, V, dO = (randn(3, n, hd, seed=s) for s in (61, 62, 63, 64))
     kb = key_bias(3, n, seed=65)
     scale = 1.0 / np.sqrt(hd)
-    mask = dense_mask(n, w, wu, d)
+    mask = dense_mask(n, w, wu, d, gidx)
     tQ, tK, tV, tb = (torch.from_numpy(x) for x in (Q, K, V, kb))
     O_t, lse_t = torch_attention_bias(tQ, tK, tV, mask, scale, tb)
-    O, lse = oracle.attention_fwd(Q, K, V, w, wu, d, scale, key_bias=kb)
+    gi = list(gidx) or None
+    O, lse = oracle.attention_fwd(Q, K, V, w, wu, d, scale, global_idx=gi, key_bias=kb)
     np.testing.assert_allclose(O, O_t.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(lse, lse_t.numpy(), rtol=1e-12, atol=1e-9)
+    if gidx:
+        # gradients against autograd of the dense reference
+        t = [x.clone().requires_grad_(True) for x in (tQ, tK, tV)]
+        O_a, _ = torch_attention_bias(*t, mask, scale, tb)
+        O_a.backward(torch.from_numpy(dO))
+        got = oracle.attention_bwd(Q, K, V, dO, w, wu, d, scale, global_idx=gi, key_bias=kb)
+        for g, r in zip(got, t):
+            np.testing.assert_allclose(g, r.grad.numpy(), rtol=1e-9, atol=1e-11)
+        return
     # the materialised chain with the bias in band_softmax
     S = oracle.band_qk(Q, K, w, wu, d, alpha=scale, padding=11.0)
     P, lse2 = oracle.band_softmax(S, w, wu, d, key_bias=kb)
@@ -417,6 +427,23 @@ def pin_bias(n, hd, w, wu, d):
 @pytest.mark.parametrize("n,hd,w,wu,d", BIAS_CASES)
 def test_key_bias_vs_torch(n, hd, w, wu, d):
     pin_bias(n, hd, w, wu, d)
+
+
+# The key-padding bias with global tokens: the bias is added to the scaled
+# score of every key a row attends to, whatever its key set -- the band keys
+# and the global columns of a local row, every key of a global row (the
+# additive mask of the nvFuser fusion applied to the attention of ONNX
+# Runtime's item (1)).
+BIAS_GLOBAL_CASES = [  # n, hd, w, w_upper, dilation, global idx
+    (41, 6, 4, 2, 0, (0, 7, 40)),
+    (45, 4, 2, 5, 3, (3, 4, 22)),
+    (24, 8, 30, 30, 0, (11,)),
+]
+
+
+@pytest.mark.parametrize("n,hd,w,wu,d,gidx", BIAS_GLOBAL_CASES)
+def test_key_bias_with_globals_vs_torch(n, hd, w, wu, d, gidx):
+    pin_bias(n, hd, w, wu, d, gidx)
 
 
 def test_key_bias_constant_is_a_shift():
