@@ -100,9 +100,12 @@ typedef struct swab_desc {
      * scaled scores): DEVICE array of b*n fp32, 4-byte aligned, row bb holding
      * the term added to the score of every query of batch bb with key j
      * before the softmax; NULL for none.  Read by band_softmax, band_attention
-     * and band_attention_bwd (the other calls do not depend on it); with
-     * n_global > 0, and by band_attention_bwd_noalloc, it is
-     * SWAB_ERR_UNSUPPORTED. */
+     * and band_attention_bwd (the other calls do not depend on it).  With
+     * n_global > 0 the fused pair adds it to every key a row attends to: the
+     * band keys and the global columns of a local row, every key of a global
+     * row.  band_softmax with n_global > 0, global_attention,
+     * global_attention_bwd and band_attention_bwd_noalloc return
+     * SWAB_ERR_UNSUPPORTED when it is set. */
     const float *key_bias;
     /* Optional dropout of the attention probabilities (the nvFuser fusion 1
      * dropout, p with 1/(1-p) scaling), in band_attention and

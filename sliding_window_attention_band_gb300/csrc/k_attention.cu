@@ -652,6 +652,10 @@ cudaError_t launch_band_attention_f32(const AttnArgsF32 &a, cudaStream_t st) {
 cudaError_t launch_band_attention_glob(DType dt, const TmapSet &mapQ, const TmapSet &mapK,
                                        const TmapSet &mapV, const AttnArgs &a, const GlobArgs &gl,
                                        cudaStream_t st) {
+    if (a.g.kbias) {   // the key bias of the band keys (global keys: their own kernels)
+        if (dt == kF16) return launch_t<__half, true, false, true>(mapQ, mapK, mapV, a, st, &gl);
+        return launch_t<__nv_bfloat16, true, false, true>(mapQ, mapK, mapV, a, st, &gl);
+    }
     if (dt == kF16) return launch_t<__half, false, false, true>(mapQ, mapK, mapV, a, st, &gl);
     return launch_t<__nv_bfloat16, false, false, true>(mapQ, mapK, mapV, a, st, &gl);
 }

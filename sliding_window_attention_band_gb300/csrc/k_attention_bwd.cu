@@ -1165,8 +1165,11 @@ __global__ void __launch_bounds__(fused::kThreads, 1)
             // key bias of this thread's key (log2 units), the same for every query
             uint64_t kb2 = f2(0.f, 0.f);
             if constexpr (kBias) {
-                if (kk < tl.nr) {
-                    const float kb = __ldg(GP(g.bnd, g.kbias + (size_t)(tl.bh / g.h) * g.n + tl.r + (size_t)g.s * kk)) * kLog2e;
+                // the key's position: kMode 2 gathers the global keys (index
+                // kk in G; the rows past G are padding)
+                const int pos = kMode == 2 ? (kk < gl.G ? gl.idx[kk] : -1) : (kk < tl.nr ? tl.r + g.s * kk : -1);
+                if (pos >= 0) {
+                    const float kb = __ldg(GP(g.bnd, g.kbias + (size_t)(tl.bh / g.h) * g.n + pos)) * kLog2e;
                     kb2 = f2(kb, kb);
                 }
             }
@@ -1597,7 +1600,7 @@ __global__ void __launch_bounds__(256) k_glob_dq_rows(const BwdArgs p, const __g
     }
 }
 
-template <typename T>
+template <typename T, bool kBias>
 cudaError_t launch_glob_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &mv, const TmapSet &mo,
                           const TmapSet &macc, const TmapSet &mq1, const TmapSet &mo1, const TmapSet &mkc,
                           const TmapSet &mvc, const TmapSet &macc1, const GlobArgs &gl, const GlobBwdBufs &gb,
@@ -1625,18 +1628,18 @@ cudaError_t launch_glob_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &m
         BwdArgs ac = a;
         ac.g.s = 1;
         ac.g.nsub = a.g.n;
-        e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, false, false, 2>), (int)smem);
+        e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, kBias, false, 2>), (int)smem);
         if (e != cudaSuccess) return e;
         const int ctiles = a.g.BH * ((gl.G + kB - 1) / kB);
         const int grid = ctiles < sms ? ctiles : sms;
-        k_bwd_fused<T, false, false, 2><<<grid, fused::kThreads, smem, st>>>(mq1, mkc, mvc, mo1, macc1, ac, gl);
+        k_bwd_fused<T, kBias, false, 2><<<grid, fused::kThreads, smem, st>>>(mq1, mkc, mvc, mo1, macc1, ac, gl);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 5. the band (global keys and queries left out), its dK, dV drain adding
     //    the global terms; 6. the dQ rounding -- both programmatic dependents
     const long long tiles = (long long)((a.g.nsub + kB - 1) / kB) * a.g.s * a.g.BH;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, false, false, 1>), (int)smem);
+    e = ensure_smem(reinterpret_cast<const void *>(k_bwd_fused<T, kBias, false, 1>), (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1648,7 +1651,7 @@ cudaError_t launch_glob_t(const TmapSet &mq, const TmapSet &mk, const TmapSet &m
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_bwd_fused<T, false, false, 1>, mq, mk, mv, mo, macc, a, gl);
+    e = cudaLaunchKernelEx(&cfg, k_bwd_fused<T, kBias, false, 1>, mq, mk, mv, mo, macc, a, gl);
     if (e != cudaSuccess) return e;
     const long long groups = rows * 8;
     cfg.gridDim = dim3((unsigned)((groups + 255) / 256));
@@ -1670,12 +1673,12 @@ cudaError_t launch_band_attention_bwd_glob(DType dt, const TmapSet &mq, const Tm
                                            const TmapSet &gmv, const TmapSet &gmq, const TmapSet &gmo,
                                            cudaStream_t st) {
     if (!a.dqacc || gl.G < 1 || a.g.BH > 65535) return cudaErrorInvalidValue;
-    if (dt == kF16)
-        return launch_glob_t<__half>(mq, mk, mv, mo, macc, mq1, mo1, mkc, mvc, macc1, gl, gb, a, gp, gmk, gmv, gmq,
-                                     gmo, st);
-    if (dt == kBF16)
-        return launch_glob_t<__nv_bfloat16>(mq, mk, mv, mo, macc, mq1, mo1, mkc, mvc, macc1, gl, gb, a, gp, gmk,
-                                            gmv, gmq, gmo, st);
+    // with the key bias: its band pass and its global-columns pass
+#define SWAB_GLOB_BWD(T, B)                                                                                  \
+    launch_glob_t<T, B>(mq, mk, mv, mo, macc, mq1, mo1, mkc, mvc, macc1, gl, gb, a, gp, gmk, gmv, gmq, gmo, st)
+    if (dt == kF16) return a.g.kbias ? SWAB_GLOB_BWD(__half, true) : SWAB_GLOB_BWD(__half, false);
+    if (dt == kBF16) return a.g.kbias ? SWAB_GLOB_BWD(__nv_bfloat16, true) : SWAB_GLOB_BWD(__nv_bfloat16, false);
+#undef SWAB_GLOB_BWD
     return cudaErrorInvalidValue;
 }
 

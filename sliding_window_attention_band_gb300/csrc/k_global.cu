@@ -530,7 +530,9 @@ __global__ void __launch_bounds__(kGlobColThreads) k_fused_glob_cols(const Fused
             const float4 k4 = kr[c4];
             d = fmaf(q[4 * c4 + 3], k4.w, fmaf(q[4 * c4 + 2], k4.z, fmaf(q[4 * c4 + 1], k4.y, fmaf(q[4 * c4], k4.x, d))));
         }
-        const float x = d * xs;
+        // plus the global key's bias (log2 units)
+        const float x = p.g.kbias ? fmaf(d, xs, *GP(p.g.bnd, p.g.kbias + (size_t)(bh / p.g.h) * n + gl.idx[gg]) * kLog2e)
+                                  : d * xs;
         const float mn = fmaxf(m, x);
         const float corr = ex2(m - mn);   // 0 for the first key (m = -inf)
         const float pg = ex2(x - mn);
@@ -605,7 +607,9 @@ __global__ void __launch_bounds__(kThreads) k_fused_glob_rows(const FusedGlobArg
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
             if (!live) continue;
-            const float x = d * xs;
+            const int j = jb + 16 * u + kg;   // plus key j's bias (log2 units)
+            const float x = p.g.kbias ? fmaf(d, xs, *GP(p.g.bnd, p.g.kbias + (size_t)(bh / p.g.h) * n + j) * kLog2e)
+                                      : d * xs;
             const float mn = fmaxf(m, x);
             const float corr = m == -INFINITY ? 0.f : ex2(m - mn);
             const float pj = ex2(x - mn);

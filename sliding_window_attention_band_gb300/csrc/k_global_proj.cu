@@ -529,6 +529,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         asm volatile("bar.sync 1, 128;" ::: "memory");   // the workers' lse, delta
         const bool kvalid = j0 + m < n;
         const float xs = p.scale * kLog2e;
+        // this key's bias (log2 units), the same for every global query
+        const float kb = (p.kbias && kvalid) ? *GP(p.bnd, p.kbias + (size_t)(bh / p.h) * n + j0 + m) * kLog2e : 0.f;
         const uint32_t pa_row = smem_u32(pa) + m * 128, dsa_row = smem_u32(dsa) + m * 128;
         for (int c = 0; c < nch && ok; ++c) {
             if (!__all_sync(0xffffffffu, mbar_wait(sfull, c & 1, abort_flag, p.err))) {
@@ -545,7 +547,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int q = 0; q < kGC; ++q) {
                 const int gg = c * kGC + q;
                 const bool live = kvalid && gg < G;
-                const float pr = live ? ex2(__uint_as_float(sv[q]) * xs - lse2[gg < G ? gg : 0]) : 0.f;
+                const float pr = live ? ex2(fmaf(__uint_as_float(sv[q]), xs, kb) - lse2[gg < G ? gg : 0]) : 0.f;
                 pv[q] = pr;
                 dsv[q] = pr * (__uint_as_float(dv[q]) - (gg < G ? del[gg] : 0.f));
             }
@@ -991,10 +993,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int u = 0; u < 16; ++u) x[c0 + u] = 0.f;
                 }
             }
+            // the key bias of global key c (log2 units), the same for every row
+            const float *kbrow = p.kbias ? p.kbias + (size_t)(bh / p.h) * n : nullptr;
             mb = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                x[c] = c < G ? x[c] * xs : -INFINITY;
+                const float kb = (kbrow && c < G) ? *GP(p.bnd, kbrow + p.gl.idx[c]) * kLog2e : 0.f;
+                x[c] = c < G ? fmaf(x[c], xs, kb) : -INFINITY;
                 mb = fmaxf(mb, x[c]);
             }
             lb = 0.f;
@@ -1234,10 +1239,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_before();
             mbar_arrive(&sempty[sb]);   // the scores are in registers
             const bool kvalid = c * kTcKeys + m < n;
+            // this key's bias (log2 units), the same for the chunk's 16 queries
+            const float kb = (p.kbias && kvalid)
+                                 ? *GP(p.bnd, p.kbias + (size_t)(bh / p.h) * n + c * kTcKeys + m) * kLog2e
+                                 : 0.f;
             if (st < nck) {
                 if (kvalid) {
 #pragma unroll
-                    for (int q = 0; q < kGC; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(sv[q]) * xs);
+                    for (int q = 0; q < kGC; ++q) mx[q] = fmaxf(mx[q], fmaf(__uint_as_float(sv[q]), xs, kb));
                 }
                 if (st == nck - 1) {
                     // every query's maximum: the warp's keys, then the four warps
@@ -1262,7 +1271,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float pr[kGC];
 #pragma unroll
                 for (int q = 0; q < kGC; ++q) {
-                    pr[q] = kvalid ? ex2(__uint_as_float(sv[q]) * xs - mx[q]) : 0.f;
+                    pr[q] = kvalid ? ex2(fmaf(__uint_as_float(sv[q]), xs, kb) - mx[q]) : 0.f;
                     ls[q] += pr[q];
                 }
                 if (!__all_sync(0xffffffffu, mbar_wait(&pempty[pi], ((c2 >> 1) & 1) ^ 1, abort_flag, p.err))) {

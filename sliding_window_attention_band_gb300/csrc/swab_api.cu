@@ -83,10 +83,7 @@ swab_status check_desc(const swab_desc *d, Geom *g, DType *dt) {
         }
     }
     if (d->dilation > SWAB_MAX_DILATION) return SWAB_ERR_UNSUPPORTED;
-    if (d->key_bias) {
-        if (reinterpret_cast<uintptr_t>(d->key_bias) % 4 != 0) return SWAB_ERR_MISALIGNED;
-        if (d->n_global > 0) return SWAB_ERR_UNSUPPORTED;  // key bias with global tokens
-    }
+    if (d->key_bias && reinterpret_cast<uintptr_t>(d->key_bias) % 4 != 0) return SWAB_ERR_MISALIGNED;
     if (!(d->dropout_p >= 0.f && d->dropout_p < 1.f)) return SWAB_ERR_INVALID_ARG;  // NaN too
     const int drop_t = (int)std::min(255.f, std::nearbyint(d->dropout_p * 256.f));
     if (drop_t > 0 && d->n_global > 0) return SWAB_ERR_UNSUPPORTED;  // dropout with globals
@@ -609,6 +606,7 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
     if (g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;  // the dropped output: band_softmax_dropout
     GlobArgs gl;
     if ((s = check_globals(desc, {Sg, Pg}, &gl)) != SWAB_OK) return s;
+    if (gl.G > 0 && g.kbias) return SWAB_ERR_UNSUPPORTED;   // the key bias with global tokens: fused calls only
     if ((s = check_ptrs({S, P})) != SWAB_OK) return s;
     if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
     if ((s = SWAB_BOUNDS(&g.bnd, {S, band_bytes(desc)}, {P, band_bytes(desc)}, gcols(desc, Sg), grows(desc, Sg),
@@ -659,6 +657,7 @@ static swab_status global_proj_setup(const swab_desc *desc, float scale, GlobalP
     if (desc->n_global < 1) return SWAB_ERR_INVALID_ARG;
     if (desc->head_dim != 64) return SWAB_ERR_UNSUPPORTED;
     if (g.rs_p || g.rs_o) return SWAB_ERR_UNSUPPORTED;
+    if (g.kbias) return SWAB_ERR_UNSUPPORTED;   // no key bias in the separate projections
     *a = GlobalProjArgs{};
     a->BH = g.BH;
     a->G = desc->n_global;
@@ -879,7 +878,7 @@ SWAB_API swab_status band_attention(const swab_desc *desc, float scale, const vo
         gr.BH = g.BH;
         gr.n = g.n;
         gr.s = 1;
-        GlobalRowsArgs r{g.BH, g.n, scale, Q, K, V, O, lse, gl, err};
+        GlobalRowsArgs r{g.BH, g.n, scale, Q, K, V, O, lse, gl, err, g.kbias, g.h};
 #if SWAB_BOUNDS_CHECK
         r.bnd = g.bnd;
 #endif
@@ -974,7 +973,7 @@ static swab_status bwd_with_globals(const swab_desc *desc, const Geom &g, DType 
     GlobArgs gl;
     swab_status s = check_globals(desc, {}, &gl);
     if (s != SWAB_OK) return s;
-    if (dt == kF32 || g.rs_p || g.rs_o || g.kbias || g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;
+    if (dt == kF32 || g.rs_p || g.rs_o || g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;
     if ((long long)(g.n + 31) / 32 * 4 > 12 * 1024) return SWAB_ERR_UNSUPPORTED;   // key bitmap in shared memory
     const size_t rows = (size_t)g.BH * g.n;
     char *ws = static_cast<char *>(static_cast<void *>(a.delta));
@@ -1032,6 +1031,8 @@ static swab_status bwd_with_globals(const swab_desc *desc, const Geom &g, DType 
     gp.dVg = const_cast<void *>(a.gdV);
     gp.ws = reinterpret_cast<float *>(ws + L.gp);
     gp.err = a.err;
+    gp.kbias = g.kbias;   // the global rows see the key bias of every key
+    gp.h = g.h;
 #if SWAB_BOUNDS_CHECK
     gp.bnd = g.bnd;
 #endif

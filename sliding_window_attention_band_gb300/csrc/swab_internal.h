@@ -154,6 +154,8 @@ struct GlobalRowsArgs {   // dense rows of the global queries (fused forward)
     float *lse;              // [BH, n]
     GlobArgs gl;
     unsigned *err;           // device status word (tensor-core kernel)
+    const float *kbias;      // [b, n] key-padding bias (natural-log units), or null
+    int h;                   // heads: slice bh belongs to batch bh / h
 #if SWAB_BOUNDS_CHECK
     Bounds bnd;              // the call's buffer extents (checked build)
 #endif
@@ -238,6 +240,8 @@ struct GlobalProjArgs {   // global queries with their own projections
     float *ws;             // workspace (partials)
     int nchunks;           // set by the launcher
     unsigned *err;         // device status word (tensor-core backward)
+    const float *kbias;    // [b, n] key-padding bias, or null (the fused backward's global rows)
+    int h;                 // heads: slice bh belongs to batch bh / h
 #if SWAB_BOUNDS_CHECK
     Bounds bnd;            // the call's buffer extents (checked build)
 #endif

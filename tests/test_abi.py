@@ -254,16 +254,16 @@ def test_binding_checks_companion_shapes():
 
 
 def test_key_bias_validation(lib):
-    """The key-padding bias must be 4-byte aligned, is not combined with global
-    tokens, and the allocation-free backward does not take it."""
+    """The key-padding bias must be 4-byte aligned; the separate global
+    projections and the allocation-free backward do not take it."""
     d = desc()
     d.c.key_bias = FAKE + 2
     assert call(lib, "band_softmax", d, FAKE, FAKE) == MISALIGNED
+    P = ctypes.c_void_p
     dg = desc(n=512, global_idx=[0, 5])
     dg.c.key_bias = FAKE
-    assert call(lib, "band_qk", dg, FAKE, FAKE, FAKE) == UNSUPPORTED
+    assert lib.global_attention(ctypes.byref(dg.c), 0.125, *(P(FAKE) for _ in range(6)), None) == UNSUPPORTED
     d.c.key_bias = FAKE
-    P = ctypes.c_void_p
     assert lib.band_attention_bwd_noalloc(ctypes.byref(d.c), 0.125, *(P(FAKE) for _ in range(9)),
                                           None) == UNSUPPORTED
 

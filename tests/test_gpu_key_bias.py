@@ -1,7 +1,9 @@
 """Key-padding bias on the GPU: (1 - mask) * -10000 per key added to the scaled
 scores before the softmax (nvFuser issue "HuggingFace BertForMaskedLM - Log
 Softmax Fusion with Autocast has bad perf", fusion 1), in band_softmax and the
-fused forward and backward, against the fp64 oracle."""
+fused forward and backward, against the fp64 oracle -- also together with
+global tokens (ONNX Runtime issue "[WIP] Improve LongformerAttention
+performance", item (1)), where it applies to every key a row attends to."""
 import numpy as np
 import pytest
 import torch
@@ -64,8 +66,9 @@ def test_band_softmax_key_bias(case):
     np.testing.assert_allclose(lse.cpu().double().numpy(), reflse, rtol=1e-4, atol=2e-3)
 
 
-def check_fused_bias(b, h, n, w, wu, dil, dtype, Q, K, V, dO, bias, slices):
-    d = swab.Desc(b, h, n, 64, w, wu, dil, 0.0, dtype, key_bias=bias.cuda())
+def check_fused_bias(b, h, n, w, wu, dil, dtype, Q, K, V, dO, bias, slices, gidx=None):
+    d = swab.Desc(b, h, n, 64, w, wu, dil, 0.0, dtype, global_idx=gidx, key_bias=bias.cuda())
+    gi = list(gidx) if gidx else None
     q, k, v, go = (x.cuda() for x in (Q, K, V, dO))
     scale = 0.125
     O = empty_dense(d)
@@ -80,9 +83,9 @@ def check_fused_bias(b, h, n, w, wu, dil, dtype, Q, K, V, dO, bias, slices):
     for sl_i in slices:
         sl = slice(sl_i, sl_i + 1)
         refO, reflse = oracle.attention_fwd(f64(Q[sl]), f64(K[sl]), f64(V[sl]), w, wu, dil, scale,
-                                            key_bias=kb[sl])
+                                            global_idx=gi, key_bias=kb[sl])
         refs = oracle.attention_bwd(f64(Q[sl]), f64(K[sl]), f64(V[sl]), f64(dO[sl]), w, wu, dil,
-                                    scale, key_bias=kb[sl])
+                                    scale, global_idx=gi, key_bias=kb[sl])
         np.testing.assert_allclose(lse[sl].cpu().double().numpy(), reflse, rtol=1e-4, atol=2e-3)
         for name, got, ref in (("O", O, refO), ("dQ", dQ, refs[0]), ("dK", dK, refs[1]),
                                ("dV", dV, refs[2])):
@@ -107,3 +110,34 @@ def test_fused_key_bias_workload():
     Q, K, V, dO = workload_inputs(wl)
     check_fused_bias(wl.b, wl.h, wl.n, wl.w, wl.w_upper, wl.dilation, wl.dtype, Q, K, V, dO,
                      make_bias(wl.b, wl.n, seed=4096), (0, 7))
+
+
+GLOBAL_CASES = [  # b, h, n, w, w_upper, dilation, dtype, global idx
+    # few global tokens: global columns on the tensor cores, rows on FFMA
+    (2, 2, 700, 64, 64, 0, torch.float16, (0, 1, 350, 699)),
+    # more than 64: global columns on FFMA; dilated
+    (1, 3, 777, 100, 37, 2, torch.bfloat16, tuple(range(0, 777, 9))),
+    # enough (16-query chunk, slice) pairs for the tensor-core global rows
+    (12, 2, 600, 32, 32, 0, torch.float16, tuple(range(0, 600, 9))[:64]),
+]
+
+
+def gids(c):
+    return ids(c[:7]) + f"-G{len(c[7])}"
+
+
+@pytest.mark.parametrize("case", GLOBAL_CASES, ids=gids)
+def test_fused_key_bias_with_globals(case):
+    b, h, n, w, wu, dil, dtype, gidx = case
+    Q, K, V, dO = seeded_qkvo(b * h, n, 64, dtype, seed=n + 9)
+    slices = range(b * h) if b * h <= 6 else (0, b * h // 2, b * h - 1)
+    check_fused_bias(b, h, n, w, wu, dil, dtype, Q, K, V, dO, make_bias(b, n, seed=n + 10), slices, gidx)
+
+
+def test_fused_key_bias_with_globals_training_workload_sampled():
+    """b = 12, h = 12, n = 4096, w = 256, 16 global tokens, bf16, with a quarter
+    of the keys masked (a padded batch): slices 0, 77, 143."""
+    wl = WORKLOADS[4]
+    Q, K, V, dO = workload_inputs(wl)
+    check_fused_bias(wl.b, wl.h, wl.n, wl.w, wl.w_upper, wl.dilation, wl.dtype, Q, K, V, dO,
+                     make_bias(wl.b, wl.n, seed=4097), (0, 77, 143), wl.global_idx)
