@@ -371,7 +371,21 @@ def prologue_and_globals(device, steps, flush, peaks):
         "bound": "tensor",
         "note": "band_attention then band_attention_bwd with 16 global tokens, bf16; flops = 6 contractions x "
                 "2 x head_dim over the attended (query, key) pairs"}
-    del Q4, K4, V4, O4, dO4, dQ4, dK4, dV4, ws4
+    # the same step on a padded batch: a key-padding bias (a quarter of the keys
+    # masked) together with the global tokens
+    kb4 = torch.where(torch.rand(w4.b, w4.n, generator=g) > 0.25, 0.0, -10000.0).to(device)
+    d4b = swab.Desc(w4.b, w4.h, w4.n, w4.head_dim, w4.w, w4.w_upper, w4.dilation, w4.padding, w4.dtype,
+                    w4.global_idx, key_bias=kb4)
+    msf = time_graph(lambda: swab.band_attention(d4b, w4.scale, Q4, K4, V4, O4, lse4), steps, 3, flush)
+    msbk = time_graph(lambda: swab.band_attention_bwd(d4b, w4.scale, Q4, K4, V4, O4, dO4, lse4, dQ4, dK4, dV4, ws4),
+                      steps, 3, flush)
+    out[f"fused+globals+key_bias:{w4.name}"] = {
+        "ms_per_step": round(msf + msbk, 4), "fwd_ms": round(msf, 4), "bwd_ms": round(msbk, 4),
+        "tflops": round((fl4 + fl4b) / ((msf + msbk) * 1e-3) / 1e12, 2),
+        "roofline_frac": round((fl4 + fl4b) / (peaks["bf16_tflops"] * 1e12) / ((msf + msbk) * 1e-3), 4),
+        "bound": "tensor",
+        "note": "the step above with a key-padding bias (a quarter of the keys masked); flops counted as above"}
+    del Q4, K4, V4, O4, dO4, dQ4, dK4, dV4, ws4, kb4
     dg = swab.Desc.from_workload(w4)
     G, BH, n = dg.G, w4.BH, w4.n
     mk = lambda *sh: torch.randn(*sh, generator=g).to(w4.dtype).to(device)  # noqa: E731

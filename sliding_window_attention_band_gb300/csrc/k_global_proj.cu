@@ -871,7 +871,7 @@ __host__ __device__ constexpr int tc_cols_smem() {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 3)   // three CTAs an SM (tensor memory allows four)
     k_fused_glob_cols_tc(const __grid_constant__ TmapSet mapQ, const GlobalRowsArgs p) {
     extern __shared__ uint8_t smraw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
@@ -888,6 +888,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = blockIdx.x, bh = blockIdx.y, a0 = qt * kTcKeys;
+    // the key bias of the global keys (log2 units; 0 past G), visible to the
+    // workers after the block barrier below
+    __shared__ __align__(16) float gbias[64];
+    if (p.kbias && threadIdx.x < 64)
+        gbias[threadIdx.x] =
+            threadIdx.x < G ? *GP(p.bnd, p.kbias + (size_t)(bh / p.h) * n + p.gl.idx[threadIdx.x]) * kLog2e : 0.f;
     if (threadIdx.x == 0) {
         mbar_init(ldfull, 1 + 32);   // the Q copy, and warp 0's lanes after K_G, V_G
         mbar_init(sfull, 1);
@@ -993,15 +999,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int u = 0; u < 16; ++u) x[c0 + u] = 0.f;
                 }
             }
-            // the key bias of global key c (log2 units), the same for every row
-            const float *kbrow = p.kbias ? p.kbias + (size_t)(bh / p.h) * n : nullptr;
             mb = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float kb = (kbrow && c < G) ? *GP(p.bnd, kbrow + p.gl.idx[c]) * kLog2e : 0.f;
-                x[c] = c < G ? fmaf(x[c], xs, kb) : -INFINITY;
-                mb = fmaxf(mb, x[c]);
+            for (int c = 0; c < 64; ++c) x[c] = c < G ? x[c] * xs : -INFINITY;
+            if (p.kbias) {   // the key bias of global key c (staged above), the same for every row
+#pragma unroll
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 kb = *reinterpret_cast<const float4 *>(&gbias[c]);
+                    x[c] += kb.x;
+                    x[c + 1] += kb.y;
+                    x[c + 2] += kb.z;
+                    x[c + 3] += kb.w;
+                }
             }
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mb = fmaxf(mb, x[c]);
             lb = 0.f;
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
