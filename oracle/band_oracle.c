@@ -160,6 +160,8 @@ int orc_band_qk(int BH, int n, int hd, int w, int wu, int dil, double alpha,
  *   global row i = G[g] : softmax of the dense row Sr[g,:] -> Pr[g,:];
  *                 P[i,:] = 0, Pg[i,:] = 0
  *   lse[i] = m + log Z.
+ * With a key bias, kbias[bh, j] is added to every score of key j first: the
+ * band slots, the global columns (j = G[g]) and the dense global rows.
  * --------------------------------------------------------------------- */
 static double drop_factor(uint64_t seed, int drop_t, int bh, int i, int j, int s);
 
@@ -168,7 +170,6 @@ int orc_band_softmax(int BH, int n, int w, int wu, int dil, const double *S,
                      const double *Sg, const double *Sr, double *Pg, double *Pr,
                      const double *kbias, uint64_t seed, int drop_t, double *Pd) {
     if (check_geom(BH, n, 1, w, wu, dil)) return -1;
-    if (G > 0 && kbias) return -4;  /* key bias with global tokens: not defined here */
     if (drop_t < 0 || drop_t > 255 || (drop_t > 0 && (G > 0 || !Pd))) return -4;
     const int D = w + wu + 1, s = dil + 1;
     unsigned char *gm; int *gp;
@@ -191,25 +192,30 @@ int orc_band_softmax(int BH, int n, int w, int wu, int dil, const double *S,
             const double *srow = xb;
             double *prow = P + ((size_t)bh * n + i) * D;
             if (gmask && gmask[i]) {
+                /* the dense row, plus the key bias of every key */
                 const int g = gp[i];
-                const double *x = Sr + ((size_t)bh * G + g) * n;
+                const double *x0 = Sr + ((size_t)bh * G + g) * n;
                 double *p = Pr + ((size_t)bh * G + g) * n;
+#define XR(j) (x0[j] + (kbias ? kbias[(size_t)bh * n + (j)] : 0.0))
                 double m = -INFINITY, z = 0.0;
-                for (int j = 0; j < n; ++j) m = fmax(m, x[j]);
-                for (int j = 0; j < n; ++j) z += exp(x[j] - m);
-                for (int j = 0; j < n; ++j) p[j] = exp(x[j] - m) / z;
+                for (int j = 0; j < n; ++j) m = fmax(m, XR(j));
+                for (int j = 0; j < n; ++j) z += exp(XR(j) - m);
+                for (int j = 0; j < n; ++j) p[j] = exp(XR(j) - m) / z;
+#undef XR
                 for (int t = 0; t < D; ++t) prow[t] = 0.0;
                 for (int q = 0; q < G; ++q) Pg[((size_t)bh * n + i) * G + q] = 0.0;
                 if (lse) lse[(size_t)bh * n + i] = m + log(z);
                 continue;
             }
+            /* the global columns, plus the key bias of each global key */
+#define XG(q) (Sg[((size_t)bh * n + i) * G + (q)] + (kbias ? kbias[(size_t)bh * n + gidx[q]] : 0.0))
             double m = -INFINITY, z = 0.0;
             for (int t = 0; t < D; ++t)
                 if (slot_used(i, t, w, s, n, gmask)) m = fmax(m, srow[t]);
-            for (int q = 0; q < G; ++q) m = fmax(m, Sg[((size_t)bh * n + i) * G + q]);
+            for (int q = 0; q < G; ++q) m = fmax(m, XG(q));
             for (int t = 0; t < D; ++t)
                 if (slot_used(i, t, w, s, n, gmask)) z += exp(srow[t] - m);
-            for (int q = 0; q < G; ++q) z += exp(Sg[((size_t)bh * n + i) * G + q] - m);
+            for (int q = 0; q < G; ++q) z += exp(XG(q) - m);
             for (int t = 0; t < D; ++t)
                 prow[t] = slot_used(i, t, w, s, n, gmask) ? exp(srow[t] - m) / z : 0.0;
             /* dropped probabilities: the keep-and-scale factor of the slot's key */
@@ -220,10 +226,8 @@ int orc_band_softmax(int BH, int n, int w, int wu, int dil, const double *S,
                                   ? drop_factor(seed, drop_t, bh, i, i + (t - w) * s, s) * prow[t]
                                   : 0.0;
             }
-            for (int q = 0; q < G; ++q) {
-                size_t k = ((size_t)bh * n + i) * G + q;
-                Pg[k] = exp(Sg[k] - m) / z;
-            }
+            for (int q = 0; q < G; ++q) Pg[((size_t)bh * n + i) * G + q] = exp(XG(q) - m) / z;
+#undef XG
             if (lse) lse[(size_t)bh * n + i] = m + log(z);
         }
     }

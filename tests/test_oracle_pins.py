@@ -408,6 +408,13 @@ def pin_bias(n, hd, w, wu, d, gidx=()):
         got = oracle.attention_bwd(Q, K, V, dO, w, wu, d, scale, global_idx=gi, key_bias=kb)
         for g, r in zip(got, t):
             np.testing.assert_allclose(g, r.grad.numpy(), rtol=1e-9, atol=1e-11)
+        # the materialised forward with global tokens: the bias in band_softmax
+        # reaches the band slots, the global columns and the global rows
+        S, Sg, Sr = oracle.band_qk(Q, K, w, wu, d, alpha=scale, padding=11.0, global_idx=gi)
+        P, lse2, Pg, Pr = oracle.band_softmax(S, w, wu, d, global_idx=gi, Sg=Sg, Sr=Sr, key_bias=kb)
+        O2 = oracle.band_pv(P, V, w, wu, d, 1.0, global_idx=gi, Pg=Pg, Pr=Pr)
+        np.testing.assert_allclose(O2, O_t.numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse2, lse_t.numpy(), rtol=1e-12, atol=1e-9)
         return
     # the materialised chain with the bias in band_softmax
     S = oracle.band_qk(Q, K, w, wu, d, alpha=scale, padding=11.0)
@@ -707,8 +714,10 @@ MUTANTS = {
     "bwd_dk_scale": ("+= scale * sbuf[(size_t)bh * nnz + u] * qi;",
                      "+= sbuf[(size_t)bh * nnz + u] * qi;"),
     "global_cols_dropped_from_sum": (
-        "for (int q = 0; q < G; ++q) z += exp(Sg[((size_t)bh * n + i) * G + q] - m);", ""),
+        "for (int q = 0; q < G; ++q) z += exp(XG(q) - m);", ""),
     "global_key_not_excluded": ("if (gmask && gmask[j]) return 0;", ""),
+    "global_cols_key_bias_ignored": ("(kbias ? kbias[(size_t)bh * n + gidx[q]] : 0.0)", "0.0"),
+    "global_rows_key_bias_ignored": ("(kbias ? kbias[(size_t)bh * n + (j)] : 0.0)", "0.0"),
     "key_bias_ignored": ("(kbias ? kbias[(size_t)bh * n + ks.key[b0 + u]] : 0.0)", "0.0"),
     "softmax_key_bias_ignored": ("((kbias && j >= 0 && j < n) ? kbias[(size_t)bh * n + j] : 0.0)",
                                  "0.0"),
@@ -740,6 +749,8 @@ def run_all_pins():
     for c in GRAD_CASES:
         pin_grads(*c)
     for c in BIAS_CASES:
+        pin_bias(*c)
+    for c in BIAS_GLOBAL_CASES:
         pin_bias(*c)
     pin_dropout()
     test_dropout_factor_definition()
