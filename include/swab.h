@@ -103,9 +103,10 @@ typedef struct swab_desc {
      * and band_attention_bwd (the other calls do not depend on it).  With
      * n_global > 0 the fused pair adds it to every key a row attends to: the
      * band keys and the global columns of a local row, every key of a global
-     * row.  band_softmax with n_global > 0, global_attention,
-     * global_attention_bwd and band_attention_bwd_noalloc return
-     * SWAB_ERR_UNSUPPORTED when it is set. */
+     * row; band_softmax likewise adds it to the band slots, the global
+     * columns (key global_idx[g]) and the dense global rows.
+     * global_attention, global_attention_bwd and band_attention_bwd_noalloc
+     * return SWAB_ERR_UNSUPPORTED when it is set. */
     const float *key_bias;
     /* Optional dropout of the attention probabilities (the nvFuser fusion 1
      * dropout, p with 1/(1-p) scaling), in band_attention and

@@ -153,24 +153,31 @@ __global__ void __launch_bounds__(kThreads) k_softmax_glob(const SoftmaxGlobArgs
             const long long j = (long long)i + (long long)(t - g.w) * g.s;
             return j >= 0 && j < g.n && !in_bitmap(bm, j);
         };
+        // scores plus the key bias: slot t (a used slot: its key is in range)
+        // and global column q (key G[q])
+        const float *brow = g.kbias ? g.kbias + (size_t)(R / g.n / g.h) * g.n : nullptr;
+        auto xb = [&](int t) {
+            return ld(GP(p.g.bnd, srow + t)) + (brow ? __ldg(GP(p.g.bnd, brow + i + (t - g.w) * g.s)) : 0.f);
+        };
+        auto xc = [&](int q) { return ld(GP(p.g.bnd, sc + q)) + (brow ? __ldg(GP(p.g.bnd, brow + gl.idx[q])) : 0.f); };
         float m = -INFINITY;
         for (int t = lane; t < g.D; t += 32)
-            if (used(t)) m = fmaxf(m, ld(GP(p.g.bnd, srow + t)));
-        for (int q = lane; q < G; q += 32) m = fmaxf(m, ld(GP(p.g.bnd, sc + q)));
+            if (used(t)) m = fmaxf(m, xb(t));
+        for (int q = lane; q < G; q += 32) m = fmaxf(m, xc(q));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
         const float mb = m * kLog2e;
         float z = 0.f;
         for (int t = lane; t < g.D; t += 32)
-            if (used(t)) z += ex2(fmaf(ld(GP(p.g.bnd, srow + t)), kLog2e, -mb));
-        for (int q = lane; q < G; q += 32) z += ex2(fmaf(ld(GP(p.g.bnd, sc + q)), kLog2e, -mb));
+            if (used(t)) z += ex2(fmaf(xb(t), kLog2e, -mb));
+        for (int q = lane; q < G; q += 32) z += ex2(fmaf(xc(q), kLog2e, -mb));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         const float inv = 1.f / z;
         for (int t = lane; t < g.D; t += 32)
-            *GP(p.g.bnd, prow + t) = Elt<T>::from_f(used(t) ? ex2(fmaf(ld(GP(p.g.bnd, srow + t)), kLog2e, -mb)) * inv : 0.f);
+            *GP(p.g.bnd, prow + t) = Elt<T>::from_f(used(t) ? ex2(fmaf(xb(t), kLog2e, -mb)) * inv : 0.f);
         for (int q = lane; q < G; q += 32)
-            *GP(p.g.bnd, pc + q) = Elt<T>::from_f(ex2(fmaf(ld(GP(p.g.bnd, sc + q)), kLog2e, -mb)) * inv);
+            *GP(p.g.bnd, pc + q) = Elt<T>::from_f(ex2(fmaf(xc(q), kLog2e, -mb)) * inv);
         if (p.lse && lane == 0) *GP(p.g.bnd, p.lse + R) = m + logf(z);
     }
 }
@@ -186,17 +193,20 @@ __global__ void __launch_bounds__(kThreads) k_glob_rows_softmax(const SoftmaxGlo
     const int bh = W / gl.G, gg = W % gl.G;
     const T *x = reinterpret_cast<const T *>(p.Srows) + (long long)W * g.n;
     T *y = reinterpret_cast<T *>(p.Prows) + (long long)W * g.n;
+    // the dense row's scores plus the key bias of every key
+    const float *brow = g.kbias ? g.kbias + (size_t)(bh / g.h) * g.n : nullptr;
+    auto xr = [&](int j) { return ld(GP(p.g.bnd, x + j)) + (brow ? __ldg(GP(p.g.bnd, brow + j)) : 0.f); };
     float m = -INFINITY;
-    for (int j = lane; j < g.n; j += 32) m = fmaxf(m, ld(GP(p.g.bnd, x + j)));
+    for (int j = lane; j < g.n; j += 32) m = fmaxf(m, xr(j));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     const float mb = m * kLog2e;
     float z = 0.f;
-    for (int j = lane; j < g.n; j += 32) z += ex2(fmaf(ld(GP(p.g.bnd, x + j)), kLog2e, -mb));
+    for (int j = lane; j < g.n; j += 32) z += ex2(fmaf(xr(j), kLog2e, -mb));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     const float inv = 1.f / z;
-    for (int j = lane; j < g.n; j += 32) *GP(p.g.bnd, y + j) = Elt<T>::from_f(ex2(fmaf(ld(GP(p.g.bnd, x + j)), kLog2e, -mb)) * inv);
+    for (int j = lane; j < g.n; j += 32) *GP(p.g.bnd, y + j) = Elt<T>::from_f(ex2(fmaf(xr(j), kLog2e, -mb)) * inv);
     if (p.lse && lane == 0) *GP(p.g.bnd, p.lse + (long long)bh * g.n + gl.idx[gg]) = m + logf(z);
 }
 

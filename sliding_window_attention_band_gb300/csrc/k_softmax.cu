@@ -757,9 +757,11 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_glob_reg(const S
     const T *scol = reinterpret_cast<const T *>(p.Scols) + R * G;
     float cv[kColsPerLane];
 #pragma unroll
+    // the key bias (band slots and the global columns' keys G[q])
+    const float *brow = g.kbias ? g.kbias + (size_t)(blockIdx.y / g.h) * g.n : nullptr;
     for (int k = 0; k < kColsPerLane; ++k) {
         const int q = lane + 32 * k;
-        cv[k] = q < G ? ld(GP(g.bnd, scol + q)) : -INFINITY;
+        cv[k] = q < G ? ld(GP(g.bnd, scol + q)) + (brow ? __ldg(GP(g.bnd, brow + gl.idx[q])) : 0.f) : -INFINITY;
     }
     float xs[NCH * N];
     float m = -INFINITY;
@@ -768,6 +770,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) k_softmax_glob_reg(const S
         float x[N];
         const int x0 = (lane + 32 * k) * N;
         unpack<T>(raw[k], x);
+        if (brow) add_key_bias(x, x0, rw, brow, qi, g);
         mask_piece<N>(x, x0, rw, -INFINITY);
         mask_global_keys<N>(x, x0, rw, qi, g, gl, -INFINITY);
 #pragma unroll
@@ -925,12 +928,18 @@ __global__ void __launch_bounds__(kWideThreads) k_glob_rows_wide(const SoftmaxGl
     uint4 *y4 = reinterpret_cast<uint4 *>(p.Prows) + W * np;
     float xs[NCH * N];
     if constexpr (!kBwd) {
+        // plus the key bias of every key (the row spans the sequence)
+        const float *brow = g.kbias ? g.kbias + (size_t)(W / gl.G / g.h) * g.n : nullptr;
         float m = -INFINITY;
 #pragma unroll
         for (int k = 0; k < NCH; ++k) {
             const int pc = tid + kWideThreads * k;
             float x[N];
             unpack<T>(pc < np ? ldg16(GP(g.bnd, x4 + pc)) : make_uint4(0, 0, 0, 0), x);
+            if (brow && pc < np) {
+#pragma unroll
+                for (int u = 0; u < N; ++u) x[u] += __ldg(GP(g.bnd, brow + (size_t)pc * N + u));
+            }
 #pragma unroll
             for (int u = 0; u < N; ++u) {
                 xs[k * N + u] = pc < np ? x[u] : -INFINITY;

@@ -606,7 +606,6 @@ SWAB_API swab_status band_softmax(const swab_desc *desc, const void *S, const sw
     if (g.drop_t > 0) return SWAB_ERR_UNSUPPORTED;  // the dropped output: band_softmax_dropout
     GlobArgs gl;
     if ((s = check_globals(desc, {Sg, Pg}, &gl)) != SWAB_OK) return s;
-    if (gl.G > 0 && g.kbias) return SWAB_ERR_UNSUPPORTED;   // the key bias with global tokens: fused calls only
     if ((s = check_ptrs({S, P})) != SWAB_OK) return s;
     if (lse && !aligned16(lse)) return SWAB_ERR_MISALIGNED;
     if ((s = SWAB_BOUNDS(&g.bnd, {S, band_bytes(desc)}, {P, band_bytes(desc)}, gcols(desc, Sg), grows(desc, Sg),

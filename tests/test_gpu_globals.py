@@ -121,6 +121,31 @@ def test_band_softmax_globals(case):
 
 
 @pytest.mark.parametrize("case", CASES, ids=ids)
+def test_band_softmax_globals_key_bias(case):
+    """With a key-padding bias (a quarter of the keys masked by -10000, plus a
+    small per-key term): added to the band slots, the global columns (key
+    G[g]) and the dense global rows."""
+    BH, n, w, wu, dil, dtype, gidx = case
+    gen = torch.Generator().manual_seed(n + 34)
+    kb = torch.where(torch.rand(1, n, generator=gen) > 0.25, 0.0, -10000.0) + 0.3 * torch.randn(1, n, generator=gen)
+    d = swab.Desc(1, BH, n, 64, w, wu, dil, 0.0, dtype, gidx, key_bias=kb.cuda())
+    S = (seeded_band(BH, n, d.D, torch.float32, seed=35) * 3).to(dtype)
+    Sc, Sr = glob_pair(BH, n, d.G, dtype, seed=36)
+    Sp, Scp = poison(S, Sc, n, w, wu, dil, gidx)
+    P = empty_band(d)
+    Pg = empty_glob(d)
+    lse = torch.empty(BH, n, dtype=torch.float32, device="cuda")
+    swab.band_softmax(d, Sp.cuda(), P, lse, Sg=(Scp.cuda(), Sr.cuda()), Pg=Pg)
+    refP, reflse, refPc, refPr = oracle.band_softmax(f64(S), w, wu, dil, gidx, f64(Sc), f64(Sr),
+                                                     key_bias=kb.repeat(BH, 1).double().numpy())
+    tol = 1e-6 if dtype == torch.float32 else ABS_TOL
+    assert np.max(np.abs(f64(P) - refP)) <= tol
+    assert np.max(np.abs(f64(Pg[0]) - refPc)) <= tol
+    assert np.max(np.abs(f64(Pg[1]) - refPr)) <= tol
+    assert np.max(np.abs(f64(lse) - reflse)) <= 1e-4 * max(1.0, np.max(np.abs(reflse)))
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
 def test_band_pv_globals(case):
     BH, n, w, wu, dil, dtype, gidx = case
     d = mk(*case)
